@@ -1,0 +1,120 @@
+"""Seeded synthetic workloads (shapes and input generators only).
+
+This module holds no arithmetic of the operators: it draws random inputs and
+quantises them to bf16 with PyTorch's own conversion.  The same bytes are
+handed to the CUDA path and to the CPU oracle.
+
+Shapes follow the workloads the Syncopate summary page evaluates ("Experiments",
+paper §6.1: AG-GEMM, GEMM-RS and GEMM-AR on Llama-3 and Qwen FFN shapes), at
+tensor-parallel degree 8 with the other ranks simulated in one GPU's memory.
+No dataset or trained weights are involved: activations are N(0,1), weights
+N(0, 0.02) (0.02 is a standard deviation), peer partials N(0,1) fp32.
+
+Recipe (fixed order, numpy PCG64 ``default_rng(seed)``):
+  AG : shards q = 0..R-1 (each [M_r, K]), then B [K, N]
+  RS : A [M, K], then B [K, N], then the peers q != r in ascending q ([M, N] fp32)
+  AR : same as RS
+Every normal draw is ``standard_normal(float32) * scale``; bf16 operands are
+then rounded to nearest-even by ``torch.Tensor.to(torch.bfloat16)``.
+``kind="int"`` draws integers in [-3, 3] instead (exactly representable, and
+small enough that every partial sum is exact in fp32 for K <= 512 * 8).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+OP_AG, OP_RS, OP_AR = "ag", "rs", "ar"
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    op: str              # "ag" | "rs" | "ar"
+    R: int               # simulated tensor-parallel ranks
+    M: int               # gathered / output rows (all ranks)
+    K: int
+    N: int
+    a_scale: float       # std of activations (A / shards)
+    b_scale: float       # std of the weight B
+    peer_scale: float = 1.0
+    splits: tuple = (1,)  # chunks per shard (AG) or per rank row block (RS/AR)
+    note: str = ""
+
+    @property
+    def M_r(self) -> int:
+        return self.M // self.R
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+
+# The five workloads.  Names say what they are; sizes are the full ones.
+TINY_AG = Workload("tiny-ag-R4-M256-K256-N256", OP_AG, 4, 256, 256, 256, 1.0 / 16, 1.0 / 16,
+                   splits=(1,), note="4 shards of 64 rows; each 128-row tile straddles 2 shards")
+LLAMA3_8B_UP_AG = Workload("llama3-8b-ffn-up-ag-tp8-M8192-K4096-N1792", OP_AG, 8, 8192, 4096, 1792,
+                           1.0, 0.02, splits=(1, 2, 4))
+LLAMA3_8B_DOWN_RS = Workload("llama3-8b-ffn-down-rs-tp8-M8192-K1792-N4096", OP_RS, 8, 8192, 1792, 4096,
+                             1.0, 0.02, 1.0, splits=(1, 2, 4))
+QWEN2_7B_DOWN_AR = Workload("qwen2-7b-ffn-down-ar-tp8-M4096-K2368-N3584", OP_AR, 8, 4096, 2368, 3584,
+                            1.0, 0.02, 1.0, splits=(1, 2, 3, 4))
+LLAMA3_70B_UP_AG = Workload("llama3-70b-ffn-up-ag-tp8-M16384-K8192-N3584", OP_AG, 8, 16384, 8192, 3584,
+                            1.0, 0.02, splits=(1, 2, 3, 4, 5, 6, 7, 8))
+
+ALL = (TINY_AG, LLAMA3_8B_UP_AG, LLAMA3_8B_DOWN_RS, QWEN2_7B_DOWN_AR, LLAMA3_70B_UP_AG)
+
+
+def scaled(w: Workload, M: int | None = None, K: int | None = None, N: int | None = None,
+           R: int | None = None) -> Workload:
+    """Same workload family at another size (for small parity cases)."""
+    return Workload(f"{w.name}-scaled", w.op, R or w.R, M or w.M, K or w.K, N or w.N,
+                    w.a_scale, w.b_scale, w.peer_scale, w.splits, w.note)
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16) via PyTorch's round-to-nearest-even."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _draw(rng: np.random.Generator, shape, scale: float, kind: str) -> np.ndarray:
+    if kind == "int":
+        return rng.integers(-3, 4, size=shape).astype(np.float32)
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if scale != 1.0:
+        x *= np.float32(scale)
+    return x
+
+
+@dataclass
+class Inputs:
+    w: Workload
+    r: int
+    shards: list = field(default_factory=list)   # AG: R x uint16 [M_r, K]
+    A: np.ndarray | None = None                  # RS/AR: uint16 [M, K]
+    B: np.ndarray | None = None                  # uint16 [K, N]
+    peers: list = field(default_factory=list)    # RS/AR: R entries, fp32 [M, N], None at r
+
+
+def make_inputs(w: Workload, r: int = 0, seed: int = 0, kind: str = "normal") -> Inputs:
+    """Draw the inputs of workload ``w`` for local rank ``r``."""
+    rng = np.random.default_rng(seed)
+    out = Inputs(w=w, r=r)
+    if w.op == OP_AG:
+        out.shards = [to_bf16_bits(_draw(rng, (w.M_r, w.K), w.a_scale, kind)) for _ in range(w.R)]
+        out.B = to_bf16_bits(_draw(rng, (w.K, w.N), w.b_scale, kind))
+    else:
+        out.A = to_bf16_bits(_draw(rng, (w.M, w.K), w.a_scale, kind))
+        out.B = to_bf16_bits(_draw(rng, (w.K, w.N), w.b_scale, kind))
+        out.peers = [None if q == r else _draw(rng, (w.M, w.N), w.peer_scale, kind)
+                     for q in range(w.R)]
+    return out
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float32 (via PyTorch)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float32).numpy()

@@ -1,0 +1,339 @@
+"""Pins for the CPU oracle, against facts that do not come from the oracle.
+
+Each test ties one oracle entry point to something fixed independently of it:
+hand-worked values (tests/golden), the IEEE rounding rule, an exact fp64
+brute force under a rigorous error bound, integer inputs where every order is
+exact, identity and one-hot matrices, a library matmul, and the invariants of
+the operators (row-block independence, concat-K, zero peers, R = 1).
+
+Operators: the Syncopate summary page, Experiments (paper §6.1) — AG-GEMM,
+GEMM-RS, GEMM-AR in their standard tensor-parallel meaning; chunking never
+changes the result (method, paper §5.1-§5.2; pith review: outputs of the fused
+and the original kernel must match).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from chunk_scheduled_communication_gb300 import workloads as wl
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+U = 2.0 ** -24      # fp32 unit roundoff
+U_BF16 = 2.0 ** -8  # bf16 unit roundoff (8-bit significand)
+
+
+def gamma(n):
+    return n * U / (1 - n * U)
+
+
+def bits_to_f64(bits):
+    return wl.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def torch_rne(x64):
+    """Library rounding of fp64 values to bf16 bits (independent of the oracle)."""
+    t = torch.from_numpy(np.asarray(x64, dtype=np.float64)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+# --------------------------------------------------------------------------- bf16 rounding
+def test_bf16_rne_golden_cases(oracle_lib):
+    rows = []
+    with open(os.path.join(GOLD, "bf16_rne_cases.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                a, b = line.split()[:2]
+                rows.append((int(a, 16), int(b, 16)))
+    f32 = np.array([r[0] for r in rows], dtype=np.uint32).view(np.float32)
+    want = np.array([r[1] for r in rows], dtype=np.uint16)
+    got = oracle_lib.bf16_rne(f32)
+    assert (got == want).all(), list(zip([hex(x) for x in got], [hex(x) for x in want]))
+
+
+def test_bf16_rne_matches_library_on_random_and_ties(oracle_lib):
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 2 ** 32, size=200_000, dtype=np.uint64).astype(np.uint32)
+    # force a quarter of them onto exact ties and exclude NaN payloads
+    bits[::4] = (bits[::4] & 0xFFFF0000) | 0x8000
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    lib = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert (oracle_lib.bf16_rne(x) == lib).all()
+
+
+# --------------------------------------------------------------------------- hand-worked values
+def _bits(a):
+    return wl.to_bf16_bits(np.array(a, dtype=np.float32))
+
+
+def test_hand_worked_ag(oracle_lib):
+    g = json.load(open(os.path.join(GOLD, "hand_worked_ops.json")))["ag_gemm"]
+    shards = [_bits(s) for s in g["shards"]]
+    gathered, C = oracle_lib.ag_gemm(shards, _bits(g["B"]))
+    assert (gathered == _bits(g["gathered"])).all()
+    assert (C == np.array(g["C_bits"], dtype=np.uint16)).all()
+
+
+def test_hand_worked_rs(oracle_lib):
+    for g in json.load(open(os.path.join(GOLD, "hand_worked_ops.json")))["gemm_rs"]:
+        peers = [None if p is None else np.array(p, dtype=np.float32) for p in g["peers"]]
+        out, send = oracle_lib.gemm_rs(_bits(g["A"]), _bits(g["B"]), peers, g["R"], g["r"],
+                                       send_rows=tuple(g["send_rows"]))
+        assert (out == np.array(g["out_bits"], dtype=np.uint16)).all()
+        assert (send == np.array(g["send"], dtype=np.float32)).all()
+
+
+def test_hand_worked_ar_and_peer_order(oracle_lib):
+    for g in json.load(open(os.path.join(GOLD, "hand_worked_ops.json")))["gemm_ar"]:
+        peers = [None if p is None else np.array(p, dtype=np.float32) for p in g["peers"]]
+        out, pub = oracle_lib.gemm_ar(_bits(g["A"]), _bits(g["B"]), peers, g["R"], g["r"],
+                                      want_publish=True)
+        assert (out == np.array(g["out_bits"], dtype=np.uint16)).all(), g["derivation"]
+        assert (pub == np.array(g["publish"], dtype=np.float32)).all()
+
+
+def test_hand_worked_sequential_k(oracle_lib):
+    g = json.load(open(os.path.join(GOLD, "hand_worked_ops.json")))["sequential_k"]
+    A = np.array(g["A_bits"], dtype=np.uint16)
+    B = np.array(g["B_bits"], dtype=np.uint16)
+    _, C = oracle_lib.ag_gemm([A], B)
+    assert (C == np.array(g["C_bits"], dtype=np.uint16)).all()
+    P = oracle_lib.gemm_f32(A, B)
+    assert P[0, 0] == 0.0  # the fp64 sum would be 1
+
+
+# --------------------------------------------------------------------------- brute force fp64
+def _rand_bits(rng, shape, scale=1.0):
+    return wl.to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(scale))
+
+
+def _check_bound(got_bits, exact, abs_terms, n_sum):
+    """|rne(fl(sum)) - exact| <= gamma_n * S + 2^-8 (|exact| + gamma_n * S)."""
+    got = bits_to_f64(got_bits)
+    e = gamma(n_sum) * abs_terms
+    bound = e + U_BF16 * (np.abs(exact) + e)
+    bad = np.abs(got - exact) > bound
+    assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], exact[bad][:5])
+
+
+@pytest.mark.parametrize("R,M_r,K,N", [(2, 16, 48, 24), (4, 8, 64, 40), (3, 5, 33, 7)])
+def test_ag_brute_force_fp64(oracle_lib, R, M_r, K, N):
+    rng = np.random.default_rng(R * 1000 + K)
+    shards = [_rand_bits(rng, (M_r, K)) for _ in range(R)]
+    B = _rand_bits(rng, (K, N), 0.5)
+    gathered, C = oracle_lib.ag_gemm(shards, B)
+    G = np.concatenate([bits_to_f64(s) for s in shards])
+    Bf = bits_to_f64(B)
+    exact = G @ Bf
+    S = np.abs(G) @ np.abs(Bf)
+    _check_bound(C, exact, S, K)
+    # the unrounded fp32 P, checked without the bf16 term
+    P = oracle_lib.gemm_f32(gathered, B).astype(np.float64)
+    assert (np.abs(P - exact) <= gamma(K) * S).all()
+
+
+@pytest.mark.parametrize("R,r", [(2, 0), (2, 1), (4, 2), (8, 7)])
+def test_rs_brute_force_fp64(oracle_lib, R, r):
+    rng = np.random.default_rng(7 + R + r)
+    M_r, K, N = 4, 40, 12
+    M = R * M_r
+    A = _rand_bits(rng, (M, K))
+    B = _rand_bits(rng, (K, N), 0.3)
+    peers = [None if q == r else rng.standard_normal((M, N), dtype=np.float32) for q in range(R)]
+    out, send = oracle_lib.gemm_rs(A, B, peers, R, r, send_rows=(0, M))
+    Af, Bf = bits_to_f64(A), bits_to_f64(B)
+    P = Af @ Bf
+    S = np.abs(Af) @ np.abs(Bf)
+    rows = slice(r * M_r, (r + 1) * M_r)
+    exact = P[rows] + sum(peers[q][rows].astype(np.float64) for q in range(R) if q != r)
+    abs_terms = S[rows] + sum(np.abs(peers[q][rows]).astype(np.float64) for q in range(R) if q != r)
+    _check_bound(out, exact, abs_terms, K + R)
+    for q in range(R):
+        rq = slice(q * M_r, (q + 1) * M_r)
+        if q == r:
+            assert np.isnan(send[rq]).all()  # rows of rank r are not written
+        else:
+            assert (np.abs(send[rq].astype(np.float64) - P[rq]) <= gamma(K) * S[rq]).all()
+
+
+@pytest.mark.parametrize("R,r", [(1, 0), (2, 1), (8, 3)])
+def test_ar_brute_force_fp64(oracle_lib, R, r):
+    rng = np.random.default_rng(70 + R + r)
+    M, K, N = 10, 56, 9
+    A = _rand_bits(rng, (M, K))
+    B = _rand_bits(rng, (K, N), 0.3)
+    peers = [None if q == r else rng.standard_normal((M, N), dtype=np.float32) for q in range(R)]
+    out, pub = oracle_lib.gemm_ar(A, B, peers, R, r, want_publish=True)
+    Af, Bf = bits_to_f64(A), bits_to_f64(B)
+    P = Af @ Bf
+    S = np.abs(Af) @ np.abs(Bf)
+    exact = P + sum((peers[q].astype(np.float64) for q in range(R) if q != r), np.zeros_like(P))
+    abs_terms = S + sum((np.abs(peers[q]).astype(np.float64) for q in range(R) if q != r), np.zeros_like(P))
+    _check_bound(out, exact, abs_terms, K + R)
+    assert (np.abs(pub.astype(np.float64) - P) <= gamma(K) * S).all()
+
+
+# --------------------------------------------------------------------------- exact integer cases
+@pytest.mark.parametrize("r", [0, 3])
+def test_integer_inputs_exact_all_ops(oracle_lib, r):
+    rng = np.random.default_rng(11)
+    R, M_r, K, N = 4, 6, 96, 20
+    M = R * M_r
+    ints = lambda shape: rng.integers(-3, 4, size=shape).astype(np.float32)
+    shards = [wl.to_bf16_bits(ints((M_r, K))) for _ in range(R)]
+    B = wl.to_bf16_bits(ints((K, N)))
+    A = wl.to_bf16_bits(ints((M, K)))
+    peers = [None if q == r else ints((M, N)) for q in range(R)]
+    Bf = bits_to_f64(B)
+    # AG
+    _, C = oracle_lib.ag_gemm(shards, B)
+    exact = np.concatenate([bits_to_f64(s) for s in shards]) @ Bf
+    assert (C == torch_rne(exact)).all()
+    # RS and AR
+    P = bits_to_f64(A) @ Bf
+    red = P + sum(peers[q].astype(np.float64) for q in range(R) if q != r)
+    out_r, send = oracle_lib.gemm_rs(A, B, peers, R, r, send_rows=(0, M))
+    assert (out_r == torch_rne(red[r * M_r:(r + 1) * M_r])).all()
+    keep = np.ones(M, bool)
+    keep[r * M_r:(r + 1) * M_r] = False
+    assert (send[keep] == P[keep]).all()
+    out, pub = oracle_lib.gemm_ar(A, B, peers, R, r, want_publish=True)
+    assert (out == torch_rne(red)).all()
+    assert (pub == P).all()
+
+
+# --------------------------------------------------------------------------- special matrices
+def test_identity_B_returns_gathered(oracle_lib):
+    rng = np.random.default_rng(3)
+    R, M_r, K = 3, 7, 32
+    shards = [_rand_bits(rng, (M_r, K)) for _ in range(R)]
+    eye = wl.to_bf16_bits(np.eye(K, dtype=np.float32))
+    gathered, C = oracle_lib.ag_gemm(shards, eye)
+    assert (C == gathered).all()
+    assert (gathered == np.concatenate(shards)).all()
+
+
+def test_one_hot_selects_single_element(oracle_lib):
+    rng = np.random.default_rng(4)
+    R, M_r, K, N = 2, 5, 24, 10
+    shards = [_rand_bits(rng, (M_r, K)) for _ in range(R)]
+    for k0, j0 in [(0, 0), (23, 9), (11, 4)]:
+        Bf = np.zeros((K, N), np.float32)
+        Bf[k0, j0] = 1.0
+        gathered, C = oracle_lib.ag_gemm(shards, wl.to_bf16_bits(Bf))
+        assert (C[:, j0] == gathered[:, k0]).all()
+        other = np.ones(N, bool)
+        other[j0] = False
+        assert (bits_to_f64(C[:, other]) == 0).all()
+    # one-hot rows of A pick rows of B (transpose check)
+    A = np.zeros((4, K), np.float32)
+    for i, k in enumerate([0, 5, 17, 23]):
+        A[i, k] = 1.0
+    B = _rand_bits(rng, (K, N))
+    _, C = oracle_lib.ag_gemm([wl.to_bf16_bits(A)], B)
+    assert (C == B[[0, 5, 17, 23]]).all()
+
+
+def test_row_block_independence(oracle_lib):
+    rng = np.random.default_rng(5)
+    R, M_r, K, N = 4, 6, 40, 16
+    shards = [_rand_bits(rng, (M_r, K)) for _ in range(R)]
+    B = _rand_bits(rng, (K, N))
+    _, C0 = oracle_lib.ag_gemm(shards, B)
+    shards2 = list(shards)
+    shards2[2] = _rand_bits(rng, (M_r, K))
+    _, C1 = oracle_lib.ag_gemm(shards2, B)
+    changed = (C0 != C1).any(axis=1)
+    assert not changed[:2 * M_r].any() and not changed[3 * M_r:].any()
+    assert changed[2 * M_r:3 * M_r].any()
+
+
+def test_row_ranges_compose(oracle_lib):
+    rng = np.random.default_rng(6)
+    R, M_r, K, N = 4, 8, 64, 24
+    M = R * M_r
+    shards = [_rand_bits(rng, (M_r, K)) for _ in range(R)]
+    B = _rand_bits(rng, (K, N))
+    _, C = oracle_lib.ag_gemm(shards, B)
+    parts = [oracle_lib.ag_gemm(shards, B, a, b, want_gathered=False)[1]
+             for a, b in [(0, 5), (5, 19), (19, M)]]
+    assert (np.concatenate(parts) == C).all()
+    A = np.concatenate(shards)
+    peers = [None] + [rng.standard_normal((M, N), dtype=np.float32) for _ in range(R - 1)]
+    out, _ = oracle_lib.gemm_ar(A, B, peers, R, 0)
+    out2 = np.concatenate([oracle_lib.gemm_ar(A, B, peers, R, 0, a, b)[0] for a, b in [(0, 13), (13, M)]])
+    assert (out == out2).all()
+    rs, _ = oracle_lib.gemm_rs(A, B, peers, R, 0)
+    rs2 = np.concatenate([oracle_lib.gemm_rs(A, B, peers, R, 0, a, b)[0] for a, b in [(0, 3), (3, M_r)]])
+    assert (rs == rs2).all()
+
+
+def test_library_matmul_cross_check(oracle_lib):
+    rng = np.random.default_rng(8)
+    A = _rand_bits(rng, (64, 512))
+    B = _rand_bits(rng, (512, 96), 0.02)
+    P = oracle_lib.gemm_f32(A, B).astype(np.float64)
+    lib = (torch.from_numpy(wl.bf16_bits_to_f32(A)) @ torch.from_numpy(wl.bf16_bits_to_f32(B))).double().numpy()
+    S = np.abs(bits_to_f64(A)) @ np.abs(bits_to_f64(B))
+    # both are within gamma_K * S of the exact value
+    assert (np.abs(P - lib) <= 2 * gamma(512) * S).all()
+
+
+# --------------------------------------------------------------------------- operator invariants
+def test_concat_k_invariant_rs_ar_exact(oracle_lib):
+    """sum_q A_q . B_q == [A_0|...|A_{R-1}] . [B_0;...;B_{R-1}] (integer inputs: exact)."""
+    rng = np.random.default_rng(9)
+    R, M_r, Kq, N = 4, 3, 32, 8
+    M = R * M_r
+    ints = lambda shape: wl.to_bf16_bits(rng.integers(-3, 4, size=shape).astype(np.float32))
+    As = [ints((M, Kq)) for _ in range(R)]
+    Bs = [ints((Kq, N)) for _ in range(R)]
+    Acat, Bcat = np.concatenate(As, axis=1), np.concatenate(Bs, axis=0)
+    _, full = oracle_lib.ag_gemm([Acat], Bcat)
+    for r in range(R):
+        peers = [None if q == r else oracle_lib.gemm_f32(As[q], Bs[q]) for q in range(R)]
+        out_r, _ = oracle_lib.gemm_rs(As[r], Bs[r], peers, R, r)
+        assert (out_r == full[r * M_r:(r + 1) * M_r]).all()
+        out, _ = oracle_lib.gemm_ar(As[r], Bs[r], peers, R, r)
+        assert (out == full).all()
+
+
+def test_concat_k_invariant_random_within_bound(oracle_lib):
+    rng = np.random.default_rng(10)
+    R, M_r, Kq, N = 4, 4, 48, 12
+    M = R * M_r
+    As = [_rand_bits(rng, (M, Kq)) for _ in range(R)]
+    Bs = [_rand_bits(rng, (Kq, N), 0.2) for _ in range(R)]
+    Acat = np.concatenate([bits_to_f64(a) for a in As], axis=1)
+    Bcat = np.concatenate([bits_to_f64(b) for b in Bs], axis=0)
+    exact, S = Acat @ Bcat, np.abs(Acat) @ np.abs(Bcat)
+    r = 1
+    peers = [None if q == r else oracle_lib.gemm_f32(As[q], Bs[q]) for q in range(R)]
+    out, _ = oracle_lib.gemm_ar(As[r], Bs[r], peers, R, r)
+    _check_bound(out, exact, S, Kq + R)
+
+
+def test_zero_peers_reduce_rs_to_plain_gemm_rows(oracle_lib):
+    rng = np.random.default_rng(12)
+    R, M_r, K, N = 4, 5, 64, 16
+    M = R * M_r
+    A = _rand_bits(rng, (M, K))
+    B = _rand_bits(rng, (K, N))
+    _, C = oracle_lib.ag_gemm([A], B)
+    for r in range(R):
+        peers = [None if q == r else np.zeros((M, N), np.float32) for q in range(R)]
+        out_r, _ = oracle_lib.gemm_rs(A, B, peers, R, r)
+        assert (out_r == C[r * M_r:(r + 1) * M_r]).all()
+
+
+def test_single_rank_ar_is_plain_gemm(oracle_lib):
+    rng = np.random.default_rng(13)
+    A = _rand_bits(rng, (9, 40))
+    B = _rand_bits(rng, (40, 11))
+    _, C = oracle_lib.ag_gemm([A], B)
+    out, _ = oracle_lib.gemm_ar(A, B, [None], 1, 0)
+    assert (out == C).all()
