@@ -1,0 +1,607 @@
+// fused.cuh -- the fused, persistent, chunk-scheduled GEMM kernel for sm_103a.
+//
+// One launch computes a whole AG-GEMM, GEMM-RS or GEMM-AR (Syncopate summary
+// page, Experiments, paper §6.1) while the chunks it consumes are still being
+// staged: each output tile waits only on the chunks its rows touch (method ¶2:
+// chunk-tile dependencies and inserted waits), and the persistent CTAs walk the
+// host-built tile list, which is sorted by chunk arrival (method ¶4, paper
+// §5.2, Fig. 6).  The chunks are staged by the copy engine, by dedicated
+// staging CTAs of this same grid, or by a staging warp inside every GEMM CTA
+// (method ¶3, paper §5.2, Fig. 7); all three publish per-chunk ready flags in
+// global memory.
+//
+// CTA layout (256 threads, one CTA per SM, cooperative launch so that every
+// CTA is resident and flag waits between CTAs cannot deadlock):
+//   warp 0      TMA producer: waits on chunk flags (AG), then streams A/B
+//               tiles into an S-stage shared-memory ring (mbarrier tx counts)
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (128 x BN x 16
+//               bf16 UMMAs into a double-buffered fp32 TMEM accumulator)
+//   warps 2-5   epilogue: tcgen05.ld rows out of TMEM; AG: bf16 store;
+//               RS/AR: add the peer partial tiles (ascending rank), bf16 store,
+//               fp32 send/publish stores and producer counters
+//   warp 6      RS/AR peer loader: waits on the peer chunks' flags, then TMA-
+//               loads 128 x 32 fp32 peer sub-tiles into a P-slot ring
+//   warp 7      co-located stager: copies this CTA's share of chunk slices with
+//               TMA bulk copies and publishes the chunk flags
+// CTAs with blockIdx.x >= G are dedicated staging CTAs (one thread copies).
+//
+// Every wait is bounded (global timer) and ends in SYN_ERR_TIMEOUT written to
+// the plan's error word; the CTA then drains its own outstanding asynchronous
+// copies and MMAs, frees TMEM and returns.  Nothing traps.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "fused.h"
+#include "ptx.cuh"
+
+namespace syn {
+
+template <int OP, int BN>
+struct KCfg {
+    static constexpr int BM = 128, BK = 64, UK = 16;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BK * BN * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int S = OP == OP_AG ? (BN == 256 ? 4 : 6) : (BN == 256 ? 3 : 4);
+    static constexpr int P = OP == OP_AG ? 0 : (BN == 256 ? 3 : 4);
+    static constexpr int PEER_COLS = 32;
+    static constexpr int PEER_BYTES = BM * PEER_COLS * 4;
+    static constexpr int NSTG = 2;
+    static constexpr int STG_BYTES = 16384;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + S * A_BYTES;
+    static constexpr int OFF_PEER = OFF_B + S * B_BYTES;
+    static constexpr int OFF_STG = OFF_PEER + P * PEER_BYTES;
+    static constexpr int OFF_BAR = OFF_STG + NSTG * STG_BYTES;
+    // barrier slots
+    static constexpr int BAR_FULL = 0;
+    static constexpr int BAR_EMPTY = BAR_FULL + S;
+    static constexpr int BAR_TFULL = BAR_EMPTY + S;
+    static constexpr int BAR_TEMPTY = BAR_TFULL + 2;
+    static constexpr int BAR_PFULL = BAR_TEMPTY + 2;
+    static constexpr int BAR_PEMPTY = BAR_PFULL + P;
+    static constexpr int BAR_STG = BAR_PEMPTY + P;
+    static constexpr int BAR_DRAIN = BAR_STG + NSTG;
+    static constexpr int NBAR = BAR_DRAIN + 1;
+    static constexpr int COMM_BUF_BYTES = 32768;
+    static constexpr int COMM_NBUF = OFF_BAR / COMM_BUF_BYTES;
+    static constexpr int NBAR_ALL = NBAR > COMM_NBUF ? NBAR : COMM_NBUF;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR_ALL * 8;
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(OFF_B % 1024 == 0 && OFF_PEER % 1024 == 0 && OFF_STG % 1024 == 0, "1 KiB atoms");
+    static_assert(BN == 128 || BN == 256, "tile_n");
+    static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, true);
+};
+
+// ------------------------------------------------------------------ errors and bounded waits
+__device__ __forceinline__ void raise_error(const KernelParams &p, int code, int where, int info) {
+    if (atomicCAS(p.err, 0, code) == 0) {
+        p.err[1] = where;
+        p.err[2] = (int)blockIdx.x;
+        p.err[3] = info;
+    }
+}
+
+__device__ __forceinline__ bool grid_failed(const KernelParams &p) {
+    return *reinterpret_cast<volatile int32_t *>(p.err) != 0;
+}
+
+// Wait for the phase of parity `parity` of mbarrier `bar`.  False once the CTA
+// aborts, the grid reports an error, or the bound runs out (then raises).
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                      const KernelParams &p) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    const uint64_t limit = p.timeout_ns * 4ull + 200000000ull;
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if ((n & 31u) == 0u) {
+            if (grid_failed(p)) {
+                *abort = 1;
+                return false;
+            }
+            if (ptx::globaltimer() - t0 > limit) {
+                raise_error(p, SYN_ERR_TIMEOUT, WHERE_PIPE, (int)bar);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Wait used only while draining on the way out: ignores the abort flag.
+__device__ __forceinline__ void bwait_drain(uint32_t bar, uint32_t parity, const KernelParams &p) {
+    const uint64_t t0 = ptx::globaltimer();
+    const uint64_t limit = p.timeout_ns * 4ull + 200000000ull;
+    for (uint32_t n = 0;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return;
+        if ((n & 31u) == 31u && ptx::globaltimer() - t0 > limit) {
+            raise_error(p, SYN_ERR_TIMEOUT, WHERE_PIPE, (int)bar);
+            return;
+        }
+    }
+}
+
+// Acquire-wait until the ready flag of a chunk carries this call's epoch.
+__device__ __forceinline__ bool wait_flag(const uint32_t *flag, const KernelParams &p,
+                                          volatile int *abort, int where, int info,
+                                          unsigned long long &waited_ns) {
+    if ((int32_t)(ptx::ld_acquire_gpu(flag) - p.epoch) >= 0) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        __nanosleep(40);
+        if ((int32_t)(ptx::ld_acquire_gpu(flag) - p.epoch) >= 0) {
+            waited_ns += ptx::globaltimer() - t0;
+            return true;
+        }
+        if (*abort) return false;
+        if ((n & 15u) == 0u) {
+            if (grid_failed(p)) {
+                *abort = 1;
+                return false;
+            }
+            if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                raise_error(p, SYN_ERR_TIMEOUT, where, info);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Rows of tile row tm clipped to M, as a row-chunk range [lo, hi].
+__device__ __forceinline__ void chunk_range(const KernelParams &p, int tm, int &lo, int &hi) {
+    const int r0 = tm * 128;
+    const int r1 = min(r0 + 128, p.M);
+    lo = r0 / p.cr;
+    hi = (r1 - 1) / p.cr;
+}
+
+// Does tile row tm reduce peers?  AR: always; RS: tiles of the local row block.
+template <int OP>
+__device__ __forceinline__ bool reduces(const KernelParams &p, int tm) {
+    if (OP == OP_AR) return true;
+    if (OP == OP_RS) return (tm * 128) / p.M_r == p.rank;
+    return false;
+}
+
+// ------------------------------------------------------------------ staging (device backends)
+// Copy `len` bytes src -> dst through an nbuf-slot shared-memory ring with TMA
+// bulk copies (global -> smem with mbarrier completion, smem -> global bulk
+// group).  `phase_bits` carries each slot's barrier parity across calls.
+__device__ __forceinline__ bool bulk_copy(const uint8_t *src, uint8_t *dst, int64_t len,
+                                          uint32_t buf0, int nbuf, uint32_t buf_bytes,
+                                          uint32_t bar0, uint32_t &phase_bits,
+                                          volatile int *abort, const KernelParams &p) {
+    const int n = (int)((len + buf_bytes - 1) / buf_bytes);
+    auto piece = [&](int i) -> uint32_t {
+        const int64_t rem = len - (int64_t)i * buf_bytes;
+        return (uint32_t)(rem < (int64_t)buf_bytes ? rem : (int64_t)buf_bytes);
+    };
+    auto issue = [&](int i) {
+        const int b = i % nbuf;
+        const uint32_t bytes = piece(i);
+        ptx::mbar_arrive_expect_tx(bar0 + 8 * b, bytes);
+        ptx::bulk_g2s(buf0 + b * buf_bytes, src + (int64_t)i * buf_bytes, bytes, bar0 + 8 * b);
+    };
+    const int pre = n < nbuf ? n : nbuf;
+    for (int i = 0; i < pre; ++i) issue(i);
+    for (int i = 0; i < n; ++i) {
+        const int b = i % nbuf;
+        const uint32_t par = (phase_bits >> b) & 1u;
+        if (!bwait(bar0 + 8 * b, par, abort, p)) {
+            // drain every load still in flight, then the stores
+            for (int j = i; j < n && j < i + nbuf; ++j) {
+                const int bj = j % nbuf;
+                bwait_drain(bar0 + 8 * bj, (phase_bits >> bj) & 1u, p);
+                phase_bits ^= 1u << bj;
+            }
+            ptx::bulk_wait_all();
+            return false;
+        }
+        phase_bits ^= 1u << b;
+        ptx::fence_proxy_async_smem();
+        ptx::bulk_s2g(dst + (int64_t)i * buf_bytes, buf0 + b * buf_bytes, piece(i));
+        ptx::bulk_commit();
+        if (i + nbuf < n) {
+            ptx::bulk_wait_read_all();  // slot b has been read by its store
+            issue(i + nbuf);
+        }
+    }
+    ptx::bulk_wait_all();  // every store of this range has completed
+    return true;
+}
+
+// Stage this worker's share of chunk slices (worker w of W takes global slices
+// w, w+W, ... in arrival order) and publish a chunk's flag once its last slice
+// has landed (last arriver on the epoch-parity slice counter).
+__device__ __forceinline__ void stage_slices(const KernelParams &p, int worker, int W,
+                                             uint32_t buf0, int nbuf, uint32_t buf_bytes,
+                                             uint32_t bar0, volatile int *abort) {
+    const int spt = p.slices_per_transfer;
+    const int total = p.n_transfers * spt;
+    const int n_flags = p.n_rc * p.R;
+    uint32_t *cnt = p.in_cnt + (size_t)(p.epoch & 1u) * n_flags;
+    uint32_t phase_bits = 0;
+    for (int g = worker; g < total; g += W) {
+        const int a = g / spt, sl = g % spt;
+        const int code = p.transfers[a];
+        if (p.op == OP_AG && p.local_inplace && code % p.R == p.rank) continue;
+        const uint8_t *src;
+        uint8_t *dst;
+        int64_t bytes;
+        transfer_span(p, code, src, dst, bytes);
+        const int64_t off = (int64_t)sl * p.slice_bytes;
+        const int64_t rem = bytes - off;
+        const int64_t len = rem < p.slice_bytes ? rem : p.slice_bytes;
+        if (!bulk_copy(src + off, dst + off, len, buf0, nbuf, buf_bytes, bar0, phase_bits, abort, p))
+            return;
+        ptx::fence_proxy_async();
+        const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + code, 1u);
+        if (old + 1u == (uint32_t)spt && a != p.drop_transfer)
+            ptx::st_release_gpu(p.in_flags + code, p.epoch);
+    }
+}
+
+// ------------------------------------------------------------------ epilogue helpers
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void store_bf16_row32(uint16_t *dst, const float (&f)[32]) {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 v;
+        v.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
+        v.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
+        v.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
+        v.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
+        d[j] = v;
+    }
+}
+
+__device__ __forceinline__ void store_f32_row32(float *dst, const float (&f)[32]) {
+    float4 *d = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+}
+
+// Producer side of a tile that writes send/publish rows: once this warp's rows
+// are stored, count the warp on every row chunk the tile covers; the last of
+// the 4 * tiles_n * (tile rows) arrivals publishes the chunk's out flag.
+__device__ __forceinline__ void count_produced(const KernelParams &p, int tm, int lane) {
+    __syncwarp();
+    if (lane == 0) {
+        ptx::fence_acq_rel_gpu();
+        int lo, hi;
+        chunk_range(p, tm, lo, hi);
+        uint32_t *cnt = p.out_cnt + (size_t)(p.epoch & 1u) * p.n_rc;
+        for (int rc = lo; rc <= hi; ++rc) {
+            const int t_lo = (rc * p.cr) / 128;
+            const int t_hi = (rc * p.cr + p.cr - 1) / 128;
+            const uint32_t need = 4u * (uint32_t)((t_hi - t_lo + 1) * p.tiles_n);
+            const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + rc, 1u);
+            if (old + 1u == need) ptx::st_release_gpu(p.out_flags + rc, p.epoch);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int OP, int BN>
+__global__ void __launch_bounds__(256, 1)
+    syn_fused_kernel(const __grid_constant__ KernelParams p, const __grid_constant__ TensorMaps tm) {
+    using C = KCfg<OP, BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_u32(sm);
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t t_start = ptx::globaltimer();
+
+    // ---- dedicated staging CTA -------------------------------------------
+    if ((int)blockIdx.x >= p.G) {
+        if (threadIdx.x == 0) {
+            *abort = 0;
+            for (int b = 0; b < C::COMM_NBUF; ++b) ptx::mbar_init(bar0 + 8 * b, 1);
+            ptx::fence_mbar_init();
+            ptx::fence_proxy_async_smem();
+            stage_slices(p, (int)blockIdx.x - p.G, p.n_comm, sbase, C::COMM_NBUF, C::COMM_BUF_BYTES,
+                         bar0, abort);
+        }
+        return;
+    }
+
+    // ---- GEMM CTA set-up ---------------------------------------------------
+    if (threadIdx.x == 0) {
+        *abort = 0;
+        for (int s = 0; s < C::S; ++s) {
+            ptx::mbar_init(bar0 + 8 * (C::BAR_FULL + s), 1);
+            ptx::mbar_init(bar0 + 8 * (C::BAR_EMPTY + s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(bar0 + 8 * (C::BAR_TFULL + a), 1);
+            ptx::mbar_init(bar0 + 8 * (C::BAR_TEMPTY + a), 128);
+        }
+        for (int s = 0; s < C::P; ++s) {
+            ptx::mbar_init(bar0 + 8 * (C::BAR_PFULL + s), 1);
+            ptx::mbar_init(bar0 + 8 * (C::BAR_PEMPTY + s), 4);
+        }
+        for (int s = 0; s < C::NSTG; ++s) ptx::mbar_init(bar0 + 8 * (C::BAR_STG + s), 1);
+        ptx::mbar_init(bar0 + 8 * C::BAR_DRAIN, 1);
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    // CTA 0 clears the counters of the other epoch parity for the next call.
+    if (blockIdx.x == 0) {
+        const int nf = p.n_rc * p.R;
+        uint32_t *nin = p.in_cnt + (size_t)((p.epoch + 1u) & 1u) * nf;
+        uint32_t *nout = p.out_cnt + (size_t)((p.epoch + 1u) & 1u) * p.n_rc;
+        for (int i = threadIdx.x; i < nf; i += blockDim.x) nin[i] = 0u;
+        for (int i = threadIdx.x; i < p.n_rc; i += blockDim.x) nout[i] = 0u;
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    unsigned long long wait_ns = 0;
+    const int KB = p.K / C::BK;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            const uint32_t sA = sbase + C::OFF_A, sB = sbase + C::OFF_B;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = p.t_begin + (int)blockIdx.x; ok && t < p.t_end; t += p.G) {
+                const int tile = p.tile_list[t];
+                const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
+                if (OP == OP_AG && p.waits) {
+                    int lo, hi;
+                    chunk_range(p, tmi, lo, hi);
+                    for (int rc = lo; ok && rc <= hi; ++rc) {
+                        const int q = rc / p.split;
+                        if (p.local_inplace && q == p.rank) continue;
+                        ok = wait_flag(p.in_flags + rc * p.R + q, p, abort, WHERE_AG_FLAG,
+                                       rc * p.R + q, wait_ns);
+                    }
+                    if (!ok) break;
+                    ptx::fence_proxy_async();  // generic acquire -> async-proxy (TMA) reads
+                }
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = (int)(it % C::S);
+                    const uint32_t ph = (it / C::S) & 1u;
+                    if (!bwait(bar0 + 8 * (C::BAR_EMPTY + s), ph ^ 1u, abort, p)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = bar0 + 8 * (C::BAR_FULL + s);
+                    ptx::mbar_arrive_expect_tx(full, C::STAGE_BYTES);
+                    ptx::tma_load_2d(sA + s * C::A_BYTES, &tm.a, full, kb * C::BK, tmi * C::BM);
+#pragma unroll
+                    for (int i = 0; i < BN / 64; ++i)
+                        ptx::tma_load_2d(sB + s * C::B_BYTES + i * 8192, &tm.b, full,
+                                         tni * BN + i * 64, kb * C::BK);
+                }
+            }
+            // drain: every armed stage's last phase must have landed
+            for (uint32_t s = 0; s < (uint32_t)C::S; ++s) {
+                if (it > s) {
+                    const uint32_t last = s + ((it - 1u - s) / C::S) * C::S;
+                    bwait_drain(bar0 + 8 * (C::BAR_FULL + s), (last / C::S) & 1u, p);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            const uint32_t sA = sbase + C::OFF_A, sB = sbase + C::OFF_B;
+            uint32_t it = 0, tc = 0;
+            bool ok = true;
+            for (int t = p.t_begin + (int)blockIdx.x; ok && t < p.t_end; t += p.G) {
+                const int acc = (int)(tc & 1u);
+                const uint32_t aph = (tc >> 1) & 1u;
+                if (!bwait(bar0 + 8 * (C::BAR_TEMPTY + acc), aph ^ 1u, abort, p)) break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = (int)(it % C::S);
+                    const uint32_t ph = (it / C::S) & 1u;
+                    if (!bwait(bar0 + 8 * (C::BAR_FULL + s), ph, abort, p)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a0 = sA + s * C::A_BYTES, b0 = sB + s * C::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < C::BK / C::UK; ++k) {
+                        // A: K-major, 128-byte swizzle; a 16-wide K slice is +32 bytes
+                        const uint64_t ad = ptx::sdesc_sw128(a0 + k * 32, 16, 1024);
+                        // B: N-major, 128-byte swizzle; LBO = next 64-column block,
+                        // SBO = next 8 K-rows; a 16-deep K slice is +16 rows of 128 B
+                        const uint64_t bd = ptx::sdesc_sw128(b0 + k * 2048, p.b_lbo, p.b_sbo);
+                        ptx::umma_bf16(d, ad, bd, C::IDESC ^ p.idesc_xor, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    ptx::umma_commit(bar0 + 8 * (C::BAR_EMPTY + s));
+                }
+                if (!ok) break;
+                ptx::umma_commit(bar0 + 8 * (C::BAR_TFULL + acc));
+                ++tc;
+            }
+            // every MMA this thread issued must finish before TMEM is released
+            ptx::umma_commit(bar0 + 8 * C::BAR_DRAIN);
+            bwait_drain(bar0 + 8 * C::BAR_DRAIN, 0, p);
+        }
+    } else if (warp >= 2 && warp < 6) {
+        // ================= epilogue =================
+        const int qd = warp & 3;  // TMEM lane quadrant this warp may access
+        const int lrow = qd * 32 + lane;
+        uint32_t tc = 0, pit = 0;
+        const uint32_t sPeer = sbase + C::OFF_PEER;
+        for (int t = p.t_begin + (int)blockIdx.x; t < p.t_end; t += p.G) {
+            const int tile = p.tile_list[t];
+            const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
+            const int acc = (int)(tc & 1u);
+            const uint32_t aph = (tc >> 1) & 1u;
+            bool ok = bwait(bar0 + 8 * (C::BAR_TFULL + acc), aph, abort, p);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            ptx::tc_fence_after();
+            const int row = tmi * C::BM + lrow;
+            const bool in_range = row < p.M;
+            const bool red = reduces<OP>(p, tmi);
+            const uint32_t tbase = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * BN);
+            bool dead = false;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
+                ptx::tmem_ld_wait();
+                float f[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+                const int col = tni * BN + cc * 32;
+                if constexpr (OP == OP_AG) {
+                    if (in_range) store_bf16_row32(p.out + (int64_t)row * p.N + col, f);
+                    continue;
+                } else {
+                if (p.f32_out != nullptr && in_range && (OP == OP_AR || !red))
+                    store_f32_row32(p.f32_out + (int64_t)row * p.N + col, f);
+                if (!red) continue;
+                for (int q = 0; q < p.R; ++q) {
+                    if (q == p.rank) continue;
+                    const int slot = (int)(pit % C::P);
+                    const uint32_t ph = (pit / C::P) & 1u;
+                    bool okp = bwait(bar0 + 8 * (C::BAR_PFULL + slot), ph, abort, p);
+                    if (!__all_sync(0xffffffffu, okp)) {
+                        dead = true;
+                        break;
+                    }
+                    // 128 rows x 128 B, 128-byte swizzle: 16-byte chunk c of row r sits
+                    // at chunk position c ^ (r & 7)
+                    const uint32_t rowaddr = sPeer + slot * C::PEER_BYTES + lrow * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        float4 x;
+                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                                     : "r"(rowaddr + ((uint32_t)(c ^ (lrow & 7)) << 4)));
+                        f[4 * c + 0] = f[4 * c + 0] + x.x;
+                        f[4 * c + 1] = f[4 * c + 1] + x.y;
+                        f[4 * c + 2] = f[4 * c + 2] + x.z;
+                        f[4 * c + 3] = f[4 * c + 3] + x.w;
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar0 + 8 * (C::BAR_PEMPTY + slot));
+                    ++pit;
+                }
+                if (dead) break;
+                if (in_range) {
+                    const int orow = OP == OP_RS ? row - p.rank * p.M_r : row;
+                    store_bf16_row32(p.out + (int64_t)orow * p.N + col, f);
+                }
+                }  // OP != OP_AG
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar0 + 8 * (C::BAR_TEMPTY + acc));
+            if (dead) break;
+            if (OP != OP_AG && p.f32_out != nullptr && (OP == OP_AR || !red))
+                count_produced(p, tmi, lane);
+            ++tc;
+        }
+    } else if (warp == 6) {
+        // ================= peer loader (GEMM-RS / GEMM-AR) =================
+        if constexpr (OP != OP_AG) if (lane == 0) {
+            const uint32_t sPeer = sbase + C::OFF_PEER;
+            uint32_t pit = 0;
+            bool ok = true;
+            for (int t = p.t_begin + (int)blockIdx.x; ok && t < p.t_end; t += p.G) {
+                const int tile = p.tile_list[t];
+                const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
+                if (!reduces<OP>(p, tmi)) continue;
+                if (p.waits) {
+                    int lo, hi;
+                    chunk_range(p, tmi, lo, hi);
+                    for (int rc = lo; ok && rc <= hi; ++rc)
+                        for (int q = 0; ok && q < p.R; ++q) {
+                            if (q == p.rank) continue;
+                            ok = wait_flag(p.in_flags + rc * p.R + q, p, abort, WHERE_PEER_FLAG,
+                                           rc * p.R + q, wait_ns);
+                        }
+                    if (!ok) break;
+                    ptx::fence_proxy_async();
+                }
+                const int prow = tmi * C::BM - p.peer_row_off;
+                for (int cc = 0; ok && cc < BN / 32; ++cc)
+                    for (int q = 0; q < p.R; ++q) {
+                        if (q == p.rank) continue;
+                        const int slot = (int)(pit % C::P);
+                        const uint32_t ph = (pit / C::P) & 1u;
+                        if (!bwait(bar0 + 8 * (C::BAR_PEMPTY + slot), ph ^ 1u, abort, p)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t full = bar0 + 8 * (C::BAR_PFULL + slot);
+                        ptx::mbar_arrive_expect_tx(full, C::PEER_BYTES);
+                        ptx::tma_load_2d(sPeer + slot * C::PEER_BYTES, &tm.peer[q], full,
+                                         tni * BN + cc * 32, prow);
+                        ++pit;
+                    }
+            }
+            for (uint32_t s = 0; s < (uint32_t)C::P; ++s) {
+                if (pit > s) {
+                    const uint32_t last = s + ((pit - 1u - s) / C::P) * C::P;
+                    bwait_drain(bar0 + 8 * (C::BAR_PFULL + s), (last / C::P) & 1u, p);
+                }
+            }
+        }
+    } else {
+        // ================= co-located stager =================
+        if (p.colocated && lane == 0)
+            stage_slices(p, (int)blockIdx.x, p.G, sbase + C::OFF_STG, C::NSTG, C::STG_BYTES,
+                         bar0 + 8 * C::BAR_STG, abort);
+    }
+
+    // ---- teardown -----------------------------------------------------------
+    if (p.stats != nullptr && wait_ns != 0ull) atomicAdd(p.stats + 0, wait_ns);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (threadIdx.x == 0 && p.stats != nullptr)
+        atomicAdd(p.stats + 1, (unsigned long long)(ptx::globaltimer() - t_start));
+}
+
+template <int OP, int BN>
+cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid, cudaStream_t st) {
+    using C = KCfg<OP, BN>;
+    cudaError_t e = cudaFuncSetAttribute(syn_fused_kernel<OP, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, syn_fused_kernel<OP, BN>, p, tm);
+}
+
+}  // namespace syn

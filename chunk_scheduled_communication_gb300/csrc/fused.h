@@ -1,0 +1,103 @@
+// fused.h -- parameter block of the fused persistent kernels, shared by the
+// host launcher and the device code, plus the address rule of a staging
+// transfer (used identically by the copy-engine, dedicated-SM and co-located
+// stagers).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "schedule.h"
+
+#if defined(__CUDACC__)
+#define SYN_HD __host__ __device__ __forceinline__
+#else
+#define SYN_HD inline
+#endif
+
+namespace syn {
+
+enum : int { OP_AG = 0, OP_RS = 1, OP_AR = 2 };
+
+// Device-side failure sites recorded in err[1] (for diagnostics).
+enum : int {
+    WHERE_AG_FLAG = 1,      // producer waiting for a gathered chunk
+    WHERE_PEER_FLAG = 2,    // peer loader waiting for a staged peer chunk
+    WHERE_PIPE = 3,         // a shared-memory pipeline barrier
+    WHERE_STAGER = 4,       // a stager's own copy barrier
+    WHERE_BOUNDS = 5        // an index check
+};
+
+struct TensorMaps {  // CUtensorMap carries its own alignment
+    CUtensorMap a;                 // AG: gathered [M,K]; RS/AR: A [M,K]   (bf16, box 64x128)
+    CUtensorMap b;                 // B [K,N]                               (bf16, box 64x64)
+    CUtensorMap peer[kMaxRanks];   // RS/AR: peer q partial rows            (fp32, box 32x128)
+};
+
+struct KernelParams {
+    int32_t op, R, rank;
+    int32_t M, N, K, M_r, cr, split, n_rc;
+    int32_t tiles_m, tiles_n;
+    int32_t t_begin, t_end;        // range of tile_list this launch runs
+    int32_t G;                     // GEMM CTAs: blockIdx.x < G
+    int32_t n_comm;                // dedicated staging CTAs: blockIdx.x >= G
+    int32_t colocated;             // GEMM CTAs run the staging warp
+    int32_t waits;                 // consumers wait on in_flags
+    int32_t local_inplace;         // AG: local shard aliases its gathered slot
+    int32_t drop_transfer;         // fault injection: arrival index never published
+    int32_t peer_row_off;          // row coordinate offset of the peer tensor maps
+    uint32_t epoch;
+    uint64_t timeout_ns;
+    const int32_t *tile_list;
+    const int32_t *transfers;      // rc * R + q, arrival order
+    int32_t n_transfers;
+    int32_t slice_bytes;           // device stagers: bytes per slice
+    int32_t slices_per_transfer;
+    uint32_t *in_flags;            // [n_rc * R]
+    uint32_t *in_cnt;              // [2][n_rc * R] slice counters (epoch parity)
+    uint32_t *out_flags;           // [n_rc]
+    uint32_t *out_cnt;             // [2][n_rc] producer counters (epoch parity)
+    int32_t *err;                  // [4] code, site, cta, info
+    unsigned long long *stats;     // [2] flag-wait ns, CTA-busy ns (nullable)
+    const uint8_t *stage_src[kMaxRanks];  // AG: shard q; RS/AR: peer q partial
+    uint8_t *stage_dst;            // AG: gathered; RS/AR: receive buffer
+    int64_t row_bytes;             // bytes of one row of a transfer
+    int64_t recv_slot_rows;        // RS/AR: rows per peer slot of the receive buffer
+    uint16_t *out;                 // AG: C; RS: out_r; AR: out   (bf16)
+    float *f32_out;                // RS: send; AR: publish  (nullable)
+    uint32_t b_lbo, b_sbo;         // B operand descriptor byte offsets (8192, 1024)
+    uint32_t idesc_xor;            // diagnostic only: bits flipped in the instruction descriptor
+};
+
+// Receive-buffer slot of source rank q (the local rank has none).
+SYN_HD int recv_slot(int q, int rank) { return q - (q > rank ? 1 : 0); }
+
+// Source, destination and size of staging transfer `code` = rc * R + q.
+//   AG : shard q rows [(rc - q*split)*cr, +cr)  ->  gathered rows [rc*cr, +cr)
+//   RS : peer q rows [rc*cr, +cr)               ->  recv[slot q] rows [rc*cr - rank*M_r, +cr)
+//   AR : peer q rows [rc*cr, +cr)               ->  recv[slot q] rows [rc*cr, +cr)
+SYN_HD void transfer_span(const KernelParams &p, int code, const uint8_t *&src, uint8_t *&dst,
+                          int64_t &bytes) {
+    const int rc = code / p.R, q = code % p.R;
+    bytes = (int64_t)p.cr * p.row_bytes;
+    if (p.op == OP_AG) {
+        src = p.stage_src[q] + (int64_t)(rc - q * p.split) * p.cr * p.row_bytes;
+        dst = p.stage_dst + (int64_t)rc * p.cr * p.row_bytes;
+    } else {
+        const int64_t row = (int64_t)rc * p.cr - (p.op == OP_RS ? (int64_t)p.rank * p.M_r : 0);
+        src = p.stage_src[q] + (int64_t)rc * p.cr * p.row_bytes;
+        dst = p.stage_dst + ((int64_t)recv_slot(q, p.rank) * p.recv_slot_rows + row) * p.row_bytes;
+    }
+}
+
+// Host launchers (one translation unit per operator).
+cudaError_t launch_fused_ag(const KernelParams &p, const TensorMaps &tm, int tile_n, int grid,
+                            cudaStream_t st);
+cudaError_t launch_fused_rs(const KernelParams &p, const TensorMaps &tm, int tile_n, int grid,
+                            cudaStream_t st);
+cudaError_t launch_fused_ar(const KernelParams &p, const TensorMaps &tm, int tile_n, int grid,
+                            cudaStream_t st);
+int fused_smem_bytes(int op, int tile_n);
+
+}  // namespace syn

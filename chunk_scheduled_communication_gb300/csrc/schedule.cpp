@@ -1,0 +1,210 @@
+// schedule.cpp -- host-side chunk plan builder (no CUDA calls).
+//
+// Chunks (Syncopate summary page, method ¶1, paper §5.1): a chunk is a block
+// of rows of a logical tensor holding one or more compute tiles.  Here every
+// operator's row space [0, M) is cut into row chunks of `cr` rows; rank q owns
+// row chunks [q*split, (q+1)*split).  A staging transfer is (row chunk rc,
+// source rank q): the rows of rc held by rank q that the local rank needs.
+//
+//   AG-GEMM : transfer (rc, q = rc / split) copies shard q's rows into the
+//             gathered buffer; tiles wait on every row chunk their rows touch.
+//   GEMM-RS : transfers (rc, q) for rc in the local block and q != r copy peer
+//             q's partial rows_r; only reduce tiles (local block) wait; send
+//             tiles of other blocks produce chunks.
+//   GEMM-AR : transfers (rc, q) for every rc and q != r; every tile waits on
+//             its row chunks from all peers.
+//
+// Arrival order (method ¶1: ring plans): the local rank's data first, then a
+// ring pull q = r+1, r+2, ..., r-1; chunk index ascending within a rank.  For
+// GEMM-RS/AR, row chunks are the outer loop (local block first, then the ring
+// of blocks) and peers the inner ring, so each row chunk completes early.
+//
+// Tile order (method ¶4, paper §5.2, Fig. 6): tiles are sorted by the latest
+// arrival index among the chunks they consume, so the persistent grid walks
+// chunks in arrival order; ties keep the chosen intra-chunk traversal.  GEMM-RS
+// send tiles come first, ordered by destination ring position (Entwine
+// abstract: produce data for communication at a regular pace).
+#include "schedule.h"
+
+#include <algorithm>
+#include <numeric>
+#include <tuple>
+
+namespace syn {
+
+static int ring_pos(int q, int r, int R) { return ((q - r) % R + R) % R; }
+
+int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
+                   int64_t chunk_rows, int split, syn_order_t order,
+                   const syn_knobs_t &kn, Schedule &s, std::string &err) {
+    if (op != SYN_OP_AG_GEMM && op != SYN_OP_GEMM_RS && op != SYN_OP_GEMM_AR) {
+        err = "unknown op";
+        return SYN_ERR_INVALID;
+    }
+    if (R < 1 || rank < 0 || rank >= R) {
+        err = "need 1 <= R and 0 <= rank < R";
+        return SYN_ERR_INVALID;
+    }
+    if (R > kMaxRanks) {
+        err = "R > 8 is not supported";
+        return SYN_ERR_UNSUPPORTED;
+    }
+    if (L.M <= 0 || L.N <= 0 || L.K <= 0) {
+        err = "M, N, K must be positive";
+        return SYN_ERR_INVALID;
+    }
+    if (L.M % R != 0) {
+        err = "M must be divisible by R";
+        return SYN_ERR_INVALID;
+    }
+    if ((L.lda != 0 && L.lda != L.K) || (L.ldb != 0 && L.ldb != L.N) ||
+        (L.ldc != 0 && L.ldc != L.N)) {
+        err = "only dense row-major layouts are supported";
+        return SYN_ERR_UNSUPPORTED;
+    }
+    if (order < SYN_ORDER_ROW_MAJOR || order > SYN_ORDER_GROUPED) {
+        err = "unknown tile order";
+        return SYN_ERR_INVALID;
+    }
+    const int64_t M_r = L.M / R;
+    if (chunk_rows < 0 || split < 0) {
+        err = "chunk_rows and split must be >= 0";
+        return SYN_ERR_INVALID;
+    }
+    if (chunk_rows == 0 && split == 0) split = 1;
+    if (chunk_rows > 0 && split > 0 && chunk_rows * split != M_r) {
+        err = "chunk_rows * split must equal M/R";
+        return SYN_ERR_INVALID;
+    }
+    if (chunk_rows > 0 && split == 0) {
+        if (M_r % chunk_rows != 0) {
+            err = "chunk_rows must divide M/R";
+            return SYN_ERR_INVALID;
+        }
+        split = (int)(M_r / chunk_rows);
+    }
+    if (M_r % split != 0) {
+        err = "split must divide M/R";
+        return SYN_ERR_INVALID;
+    }
+    const int tile_m = kn.tile_m == 0 ? kTileM : kn.tile_m;
+    const int tile_n = kn.tile_n == 0 ? 256 : kn.tile_n;
+    if (tile_m != kTileM) {
+        err = "tile_m must be 128";
+        return SYN_ERR_UNSUPPORTED;
+    }
+    if (tile_n != 128 && tile_n != 256) {
+        err = "tile_n must be 128 or 256";
+        return SYN_ERR_UNSUPPORTED;
+    }
+    if (L.K % kTileK != 0) {
+        err = "K must be a multiple of 64";
+        return SYN_ERR_UNSUPPORTED;
+    }
+    if (L.N % tile_n != 0) {
+        err = "N must be a multiple of tile_n";
+        return SYN_ERR_UNSUPPORTED;
+    }
+    if (op == SYN_OP_GEMM_RS && M_r % tile_m != 0) {
+        err = "GEMM-RS needs (M/R) % 128 == 0";
+        return SYN_ERR_UNSUPPORTED;
+    }
+    if (L.M > (int64_t)1 << 30 || L.N > (int64_t)1 << 30 || L.K > (int64_t)1 << 30) {
+        err = "dimension too large";
+        return SYN_ERR_UNSUPPORTED;
+    }
+
+    s = Schedule();
+    s.op = op;
+    s.R = R;
+    s.rank = rank;
+    s.M = L.M;
+    s.N = L.N;
+    s.K = L.K;
+    s.M_r = M_r;
+    s.split = split;
+    s.cr = M_r / split;
+    s.order = order;
+    s.group_m = kn.group_m > 0 ? kn.group_m : 8;
+    s.tile_m = tile_m;
+    s.tile_n = tile_n;
+    s.tiles_m = (int)((L.M + tile_m - 1) / tile_m);
+    s.tiles_n = (int)(L.N / tile_n);
+    s.n_tiles = s.tiles_m * s.tiles_n;
+    s.n_rc = (int)(L.M / s.cr);
+
+    // ---- staging transfers in arrival order -----------------------------
+    s.arrival.assign((size_t)s.n_rc * R, -1);
+    auto add = [&](int rc, int q) {
+        s.arrival[(size_t)rc * R + q] = (int)s.transfers.size();
+        s.transfers.push_back(rc * R + q);
+    };
+    if (op == SYN_OP_AG_GEMM) {
+        for (int d = 0; d < R; ++d) {
+            const int q = (rank + d) % R;
+            for (int j = 0; j < split; ++j) add(q * split + j, q);
+        }
+    } else {
+        const int nblocks = (op == SYN_OP_GEMM_RS) ? 1 : R;  // RS: only the local block
+        for (int db = 0; db < nblocks; ++db) {
+            const int b = (rank + db) % R;
+            for (int j = 0; j < split; ++j)
+                for (int dq = 1; dq < R; ++dq) add(b * split + j, (rank + dq) % R);
+        }
+    }
+
+    // ---- tile keys from the chunk -> tile dependency ranges ---------------
+    struct Item {
+        int32_t key;
+        int64_t t0, t1, t2;
+        int32_t tile;
+    };
+    std::vector<Item> items;
+    items.reserve(s.n_tiles);
+    for (int tm = 0; tm < s.tiles_m; ++tm) {
+        int lo, hi;
+        tile_row_chunks(s, tm, lo, hi);
+        int32_t key = -1;
+        const int block = (int)(((int64_t)tm * tile_m) / M_r);
+        if (op == SYN_OP_GEMM_RS && block != rank) {
+            // send tile: produces chunk(s) for rank `block`; ring order
+            const int j = (int)((((int64_t)tm * tile_m) % M_r) / s.cr);
+            key = (ring_pos(block, rank, R) - 1) * split + j - (R - 1) * split;
+        } else {
+            for (int rc = lo; rc <= hi; ++rc)
+                for (int q = 0; q < R; ++q) {
+                    const int a = s.arrival[(size_t)rc * R + q];
+                    if (a > key) key = a;
+                }
+        }
+        for (int tn = 0; tn < s.tiles_n; ++tn) {
+            Item it;
+            it.key = key;
+            it.tile = tm * s.tiles_n + tn;
+            switch (order) {
+                case SYN_ORDER_ROW_MAJOR:
+                    it.t0 = tm, it.t1 = tn, it.t2 = 0;
+                    break;
+                case SYN_ORDER_COL_MAJOR:
+                    it.t0 = tn, it.t1 = tm, it.t2 = 0;
+                    break;
+                default:
+                    it.t0 = tm / s.group_m, it.t1 = tn, it.t2 = tm % s.group_m;
+                    break;
+            }
+            items.push_back(it);
+        }
+    }
+    std::stable_sort(items.begin(), items.end(), [](const Item &a, const Item &b) {
+        return std::tie(a.key, a.t0, a.t1, a.t2) < std::tie(b.key, b.t0, b.t1, b.t2);
+    });
+    s.tile_list.resize(items.size());
+    s.tile_key.resize(items.size());
+    for (size_t i = 0; i < items.size(); ++i) {
+        s.tile_list[i] = items[i].tile;
+        s.tile_key[i] = items[i].key;
+    }
+    return SYN_OK;
+}
+
+}  // namespace syn

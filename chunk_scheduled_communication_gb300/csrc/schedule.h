@@ -1,0 +1,53 @@
+// schedule.h -- host-side chunk plan: chunk partition, chunk->tile dependency
+// ranges, arrival order of staging transfers and the rewritten tile order.
+//
+// Syncopate summary page, method ¶2 (the chunk-tile dependency graph: which
+// chunks each tile consumes or produces, and where waits go) and ¶4 (paper
+// §5.2, Fig. 6: order chunks by communication order, then keep or adjust the
+// tile traversal inside a chunk).  The producer-side order of GEMM-RS (send
+// tiles first) follows Entwine's abstract: produce data for communication at a
+// regular pace.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "syn.h"
+
+namespace syn {
+
+constexpr int kTileM = 128;
+constexpr int kTileK = 64;
+constexpr int kMaxRanks = 8;
+
+struct Schedule {
+    int op = 0, R = 1, rank = 0;
+    int64_t M = 0, N = 0, K = 0, M_r = 0;
+    int64_t cr = 0;      // chunk rows
+    int split = 1;       // chunks per rank row block
+    int order = 0, group_m = 8;
+    int tile_m = kTileM, tile_n = 256;
+    int tiles_m = 0, tiles_n = 0, n_tiles = 0;
+    int n_rc = 0;        // row chunks over [0, M)
+    std::vector<int32_t> tile_list;   // execution order (tile ids)
+    std::vector<int32_t> tile_key;    // sort key of each entry of tile_list
+    std::vector<int32_t> transfers;   // rc * R + q, arrival order
+    std::vector<int32_t> arrival;     // arrival index of (rc * R + q), -1 if none
+};
+
+// Fills `s` or returns a SYN_ERR_* code with a message in `err`.
+int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &layout,
+                   int64_t chunk_rows, int split, syn_order_t order,
+                   const syn_knobs_t &knobs, Schedule &s, std::string &err);
+
+// Row-chunk range [lo, hi] covered by tile row tm (rows clipped to M).
+inline void tile_row_chunks(const Schedule &s, int tm, int &lo, int &hi) {
+    int64_t r0 = (int64_t)tm * s.tile_m;
+    int64_t r1 = r0 + s.tile_m;
+    if (r1 > s.M) r1 = s.M;
+    lo = (int)(r0 / s.cr);
+    hi = (int)((r1 - 1) / s.cr);
+}
+
+}  // namespace syn

@@ -1,0 +1,209 @@
+// tune.cu -- enumerate-and-measure autotuner.
+//
+// The Syncopate summary page (method ¶4; paper §6.3, Fig. 11) searches chunk
+// size / split factor, tile shape, tile order, communication backend and the
+// number of communication SMs by compiling and timing candidates, and reports
+// that a wrong backend, SM allocation or tile order can cost more than 2x.
+// Entwine's abstract adds that the SMs given to communication must be balanced
+// against the slowdown of compute.  Here every candidate is a runtime
+// configuration of the same precompiled kernels, so the search is: create a
+// plan, warm up, time a few calls with CUDA events (L2 flushed in between),
+// keep the median, pick the fastest.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <fstream>
+#include <sstream>
+#include <string>
+#include <vector>
+
+#include "syn.h"
+
+namespace {
+
+struct Cand {
+    syn_knobs_t kn;
+    int split;
+    syn_order_t order;
+};
+
+std::string cache_key(int op, int R, int rank, const syn_layout_t &L) {
+    std::ostringstream o;
+    o << "\"op\":" << op << ",\"R\":" << R << ",\"rank\":" << rank << ",\"M\":" << L.M
+      << ",\"N\":" << L.N << ",\"K\":" << L.K;
+    return o.str();
+}
+
+long field(const std::string &line, const char *name) {
+    const std::string k = std::string("\"") + name + "\":";
+    const size_t pos = line.find(k);
+    if (pos == std::string::npos) return -1;
+    return std::strtol(line.c_str() + pos + k.size(), nullptr, 10);
+}
+
+double field_d(const std::string &line, const char *name) {
+    const std::string k = std::string("\"") + name + "\":";
+    const size_t pos = line.find(k);
+    if (pos == std::string::npos) return -1;
+    return std::strtod(line.c_str() + pos + k.size(), nullptr);
+}
+
+struct DevBuf {
+    void *p = nullptr;
+    ~DevBuf() { cudaFree(p); }
+};
+
+}  // namespace
+
+extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *layout, double budget_s,
+                            syn_knobs_t *best, int *best_split, syn_order_t *best_order,
+                            double *best_us) {
+    if (layout == nullptr || best == nullptr || best_split == nullptr || best_order == nullptr)
+        return SYN_ERR_INVALID;
+    const syn_layout_t L = *layout;
+    if (L.M <= 0 || L.N <= 0 || L.K <= 0 || R < 1 || L.M % R != 0) return SYN_ERR_INVALID;
+    if (budget_s <= 0) budget_s = 60.0;
+    const std::string key = cache_key(op, R, rank, L);
+    const char *cache_path = std::getenv("SYN_TUNE_CACHE");
+
+    // ---- cache hit ----------------------------------------------------------
+    if (cache_path != nullptr && *cache_path) {
+        std::ifstream in(cache_path);
+        std::string line, hit;
+        while (std::getline(in, line))
+            if (line.find(key) != std::string::npos) hit = line;  // latest entry wins
+        if (!hit.empty()) {
+            syn_knobs_default(best);
+            best->backend = (syn_backend_t)field(hit, "backend");
+            best->comm_sms = (int)field(hit, "comm_sms");
+            best->tile_n = (int)field(hit, "tile_n");
+            best->group_m = (int)field(hit, "group_m");
+            *best_split = (int)field(hit, "split");
+            *best_order = (syn_order_t)field(hit, "order");
+            if (best_us) *best_us = field_d(hit, "us");
+            return SYN_OK;
+        }
+    }
+
+    // ---- scratch operands ------------------------------------------------------
+    const int64_t M_r = L.M / R;
+    DevBuf a, b, c, peerbuf, f32, flush;
+    const size_t flush_bytes = 512ull << 20;
+    if (cudaMalloc(&b.p, (size_t)L.K * L.N * 2) != cudaSuccess) return SYN_ERR_CUDA;
+    if (cudaMalloc(&a.p, (size_t)L.M * L.K * 2) != cudaSuccess) return SYN_ERR_CUDA;
+    if (cudaMalloc(&flush.p, flush_bytes) != cudaSuccess) return SYN_ERR_CUDA;
+    cudaMemset(a.p, 0x3C, (size_t)L.M * L.K * 2);
+    cudaMemset(b.p, 0x3C, (size_t)L.K * L.N * 2);
+    std::vector<const void *> shards(R);
+    std::vector<const float *> peers(R, nullptr);
+    if (op == SYN_OP_AG_GEMM) {
+        if (cudaMalloc(&peerbuf.p, (size_t)L.M * L.K * 2) != cudaSuccess) return SYN_ERR_CUDA;
+        if (cudaMalloc(&c.p, (size_t)L.M * L.N * 2) != cudaSuccess) return SYN_ERR_CUDA;
+        cudaMemset(peerbuf.p, 0x3C, (size_t)L.M * L.K * 2);
+        for (int q = 0; q < R; ++q)
+            shards[q] = (q == rank ? (uint8_t *)a.p : (uint8_t *)peerbuf.p) + (size_t)q * M_r * L.K * 2;
+    } else {
+        const size_t pbytes = (size_t)L.M * L.N * 4;
+        if (R > 1 && cudaMalloc(&peerbuf.p, (size_t)(R - 1) * pbytes) != cudaSuccess) return SYN_ERR_CUDA;
+        if (R > 1) cudaMemset(peerbuf.p, 0x3C, (size_t)(R - 1) * pbytes);
+        if (cudaMalloc(&c.p, (size_t)L.M * L.N * 2) != cudaSuccess) return SYN_ERR_CUDA;
+        if (op == SYN_OP_GEMM_RS && cudaMalloc(&f32.p, pbytes) != cudaSuccess) return SYN_ERR_CUDA;
+        int slot = 0;
+        for (int q = 0; q < R; ++q)
+            if (q != rank) peers[q] = (const float *)((uint8_t *)peerbuf.p + (size_t)(slot++) * pbytes);
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) return SYN_ERR_CUDA;
+
+    // ---- candidate space ---------------------------------------------------------
+    std::vector<syn_backend_t> backends = {SYN_BACKEND_CE, SYN_BACKEND_TMA_DEDICATED,
+                                           SYN_BACKEND_TMA_COLOCATED};
+    if (op != SYN_OP_AG_GEMM) backends.push_back(SYN_BACKEND_TMA_COLOCATED_SMEM);
+    const int comm_opts[] = {4, 8, 16};
+    const int split_opts[] = {1, 2, 3, 4, 6, 8};
+    const syn_order_t order_opts[] = {SYN_ORDER_ROW_MAJOR, SYN_ORDER_COL_MAJOR, SYN_ORDER_GROUPED};
+    const int tile_opts[] = {256, 128};
+    std::vector<Cand> cands;
+    for (int tn : tile_opts) {
+        if (L.N % tn) continue;
+        for (syn_backend_t be : backends)
+            for (int ci = 0; ci < (be == SYN_BACKEND_TMA_DEDICATED ? 3 : 1); ++ci)
+                for (int sp : split_opts) {
+                    if (M_r % sp) continue;
+                    for (syn_order_t od : order_opts) {
+                        Cand cd;
+                        syn_knobs_default(&cd.kn);
+                        cd.kn.backend = be;
+                        cd.kn.comm_sms = comm_opts[ci];
+                        cd.kn.tile_n = tn;
+                        cd.split = sp;
+                        cd.order = od;
+                        cands.push_back(cd);
+                    }
+                }
+    }
+
+    cudaStream_t st;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return SYN_ERR_CUDA;
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    const auto t_start = std::chrono::steady_clock::now();
+    double best_t = 1e30;
+    int best_i = -1;
+    for (size_t i = 0; i < cands.size(); ++i) {
+        const double el =
+            std::chrono::duration<double>(std::chrono::steady_clock::now() - t_start).count();
+        if (el > budget_s) break;
+        const Cand &cd = cands[i];
+        syn_plan_t plan = nullptr;
+        if (syn_plan_create(&plan, op, R, rank, &L, 0, cd.split, cd.order, &cd.kn) != SYN_OK) continue;
+        auto call = [&]() -> int {
+            if (op == SYN_OP_AG_GEMM) return syn_ag_gemm(plan, shards.data(), a.p, b.p, c.p, st);
+            if (op == SYN_OP_GEMM_RS)
+                return syn_gemm_rs(plan, a.p, b.p, peers.data(), (float *)f32.p, c.p, st);
+            return syn_gemm_ar(plan, a.p, b.p, peers.data(), nullptr, c.p, st);
+        };
+        bool ok = true;
+        for (int w = 0; w < 2 && ok; ++w) ok = call() == SYN_OK;
+        ok = ok && syn_sync_status(plan, st) == SYN_OK;
+        std::vector<float> ts;
+        for (int rep = 0; rep < 5 && ok; ++rep) {
+            cudaMemsetAsync(flush.p, rep, flush_bytes, st);
+            cudaEventRecord(e0, st);
+            ok = call() == SYN_OK;
+            cudaEventRecord(e1, st);
+            if (ok) ok = syn_sync_status(plan, st) == SYN_OK;
+            float ms = 0;
+            if (ok) cudaEventElapsedTime(&ms, e0, e1);
+            ts.push_back(ms);
+        }
+        syn_plan_destroy(plan);
+        if (!ok) continue;
+        std::sort(ts.begin(), ts.end());
+        const double med = ts[ts.size() / 2] * 1000.0;
+        if (med < best_t) {
+            best_t = med;
+            best_i = (int)i;
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaStreamDestroy(st);
+    if (best_i < 0) return SYN_ERR_CUDA;
+    *best = cands[best_i].kn;
+    *best_split = cands[best_i].split;
+    *best_order = cands[best_i].order;
+    if (best_us) *best_us = best_t;
+    if (cache_path != nullptr && *cache_path) {
+        std::ofstream out(cache_path, std::ios::app);
+        out << "{" << key << ",\"backend\":" << (int)best->backend << ",\"comm_sms\":" << best->comm_sms
+            << ",\"tile_n\":" << best->tile_n << ",\"group_m\":" << best->group_m
+            << ",\"split\":" << *best_split << ",\"order\":" << (int)*best_order << ",\"us\":" << best_t
+            << "}\n";
+    }
+    return SYN_OK;
+}

@@ -60,7 +60,7 @@ LLAMA3_8B_UP_AG = Workload("llama3-8b-ffn-up-ag-tp8-M8192-K4096-N1792", OP_AG, 8
 LLAMA3_8B_DOWN_RS = Workload("llama3-8b-ffn-down-rs-tp8-M8192-K1792-N4096", OP_RS, 8, 8192, 1792, 4096,
                              1.0, 0.02, 1.0, splits=(1, 2, 4))
 QWEN2_7B_DOWN_AR = Workload("qwen2-7b-ffn-down-ar-tp8-M4096-K2368-N3584", OP_AR, 8, 4096, 2368, 3584,
-                            1.0, 0.02, 1.0, splits=(1, 2, 3, 4))
+                            1.0, 0.02, 1.0, splits=(1, 2, 4))
 LLAMA3_70B_UP_AG = Workload("llama3-70b-ffn-up-ag-tp8-M16384-K8192-N3584", OP_AG, 8, 16384, 8192, 3584,
                             1.0, 0.02, splits=(1, 2, 3, 4, 5, 6, 7, 8))
 

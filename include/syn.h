@@ -1,0 +1,261 @@
+/*
+ * syn.h -- C ABI of libsyn: chunk-scheduled compute/communication overlap for
+ * tensor-parallel GEMMs on one GB300 (sm_103a).
+ *
+ * Source of the method: "Syncopate: Efficient Multi-GPU AI Kernels via
+ * Automatic Chunk-Centric Compute-Communication Overlap" (OSDI 2026 summary
+ * page and arXiv abstract), with Entwine (arXiv 2609.11562 abstract) as
+ * related work.  Communication is expressed as transfers of *chunks* -- a block
+ * of a logical tensor holding one or more compute tiles (summary page, method
+ * ¶1, paper §5.1).  A chunk->tile dependency graph says which chunks each tile
+ * consumes or produces and where waits go (method ¶2).  The tile scheduler is
+ * rewritten to walk chunks in communication order while keeping locality
+ * inside a chunk (method ¶4, paper §5.2, Fig. 6).  One plan lowers to several
+ * staging backends: copy engine, TMA on dedicated SMs, TMA co-located with
+ * compute (method ¶3, paper §5.2, Fig. 7).  The three operators are the
+ * summary page's GEMM workloads (Experiments, paper §6.1): AG-GEMM, GEMM-RS,
+ * GEMM-AR.
+ *
+ * Ranks.  All R tensor-parallel ranks live in one GPU: the R-1 peers are
+ * simulated by buffers in the same HBM, and "communication" is the staging of
+ * those buffers into the local rank's buffers.
+ *
+ * Conventions for every call:
+ *  - Every function returns an int status: SYN_OK (0) or a negative SYN_ERR_*.
+ *    No C++ exception crosses this boundary.  syn_last_error() gives a message
+ *    for the most recent failure on the calling thread.
+ *  - Device pointers are plain CUDA device addresses, 16-byte aligned, owned by
+ *    the caller.  Arrays of device pointers (shards, peer partials) are HOST
+ *    arrays of length R.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Operator calls are asynchronous on it; check completion and device-side
+ *    errors with syn_sync_status().  One plan must not run on two streams at
+ *    once.
+ *  - Matrices are row-major.  bf16 operands are IEEE bfloat16; partials fp32.
+ *  - The plan owns its flags, counters, error word, tables, staging receive
+ *    buffers and helper streams; syn_plan_destroy() frees them.
+ *  - Limits of this version: 1 <= R <= 8; K % 64 == 0; N % tile_n == 0; dense
+ *    layouts (ld* == 0 or equal to the row length); GEMM-RS needs
+ *    (M/R) % 128 == 0.  M may have a tail (M % 128 != 0) for AG-GEMM and
+ *    GEMM-AR.
+ */
+#ifndef SYN_H
+#define SYN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define SYN_OK 0
+#define SYN_ERR_INVALID (-1)     /* bad argument, shape, alignment or split     */
+#define SYN_ERR_UNSUPPORTED (-2) /* valid but outside this version's limits     */
+#define SYN_ERR_CUDA (-3)        /* a CUDA runtime/driver call failed          */
+#define SYN_ERR_TIMEOUT (-4)     /* a device wait on a chunk flag or pipeline
+                                    barrier ran past the plan's timeout         */
+#define SYN_ERR_BOUNDS (-5)      /* a device-side index check failed           */
+
+typedef struct syn_plan_s *syn_plan_t; /* opaque, owned by the library */
+
+/* The three operators (summary page, Experiments, paper §6.1). */
+typedef enum {
+    SYN_OP_AG_GEMM = 0, /* C = concat_q(shard_q) . B                          */
+    SYN_OP_GEMM_RS = 1, /* out_r = rows_r(A.B) + sum_{q!=r} rows_r(peer_q)    */
+    SYN_OP_GEMM_AR = 2  /* out = A.B + sum_{q!=r} peer_q                      */
+} syn_op_t;
+
+/* Tile traversal inside a chunk (method ¶4, paper §5.2, Fig. 6: keep or
+ * adjust the traversal to trade arrival time against locality). */
+typedef enum {
+    SYN_ORDER_ROW_MAJOR = 0, /* tile rows in order, columns fastest             */
+    SYN_ORDER_COL_MAJOR = 1, /* tile columns in order, rows fastest             */
+    SYN_ORDER_GROUPED = 2    /* group_m tile rows at a time, column by column   */
+} syn_order_t;
+
+/* Staging backends for one plan (method ¶3, paper §5.2, Fig. 7), plus the two
+ * comparison paths of paper Fig. 2(b). */
+typedef enum {
+    SYN_BACKEND_CE = 0,             /* copy engine: cudaMemcpyAsync on a side
+                                       stream + a stream-ordered flag write per
+                                       chunk                                      */
+    SYN_BACKEND_TMA_DEDICATED = 1,  /* comm_sms extra CTAs of the same persistent
+                                       grid copy chunks with TMA bulk copies     */
+    SYN_BACKEND_TMA_COLOCATED = 2,  /* one staging warp in every GEMM CTA copies
+                                       chunk slices with TMA bulk copies (mbarrier
+                                       pipelined), slice ownership by CTA index  */
+    SYN_BACKEND_TMA_COLOCATED_SMEM = 3, /* GEMM-RS/AR only: each GEMM CTA fetches
+                                       the peer tiles it needs straight into
+                                       shared memory with TMA (no global staging) */
+    SYN_BACKEND_UNFUSED = 4,        /* baseline: whole staging copy first, then
+                                       the same GEMM kernel without waits         */
+    SYN_BACKEND_DECOMPOSED = 5      /* baseline: one GEMM launch per chunk group,
+                                       each after its chunks' copies (Fig. 2(b)) */
+} syn_backend_t;
+
+/* Shapes.  M = rows of the gathered / full output space (all ranks),
+ * K = contraction, N = output columns.  Rank q owns rows [q*M/R, (q+1)*M/R).
+ * ld* are leading dimensions in elements; 0 means dense row-major. */
+typedef struct {
+    int64_t M, N, K;
+    int64_t lda, ldb, ldc;
+} syn_layout_t;
+
+/* Tuning knobs (the search space of paper §6.3, Fig. 11, and Entwine's
+ * communication-SM allocation). */
+typedef struct {
+    syn_backend_t backend;
+    int comm_sms;          /* TMA_DEDICATED: CTAs (SMs) given to staging, 1..32  */
+    int tile_m;            /* 128 (0 = default)                                  */
+    int tile_n;            /* 128 or 256 (0 = 256)                               */
+    int group_m;           /* SYN_ORDER_GROUPED group height in tiles (0 = 8)   */
+    int slice_kb;          /* device stagers: KiB per slice of a chunk (0 = 128) */
+    uint64_t timeout_ns;   /* bound on every device wait (0 = 2 s, or the
+                              SYN_TIMEOUT_NS environment variable)              */
+    int debug_drop_chunk;  /* fault injection: arrival index of a staging
+                              transfer whose ready flag is never published
+                              (-1 = off); the call then ends in SYN_ERR_TIMEOUT */
+    int trace;             /* 1 = accumulate flag-wait and CTA-busy nanoseconds
+                              (read with syn_plan_stats)                        */
+} syn_knobs_t;
+
+/* Everything a caller or a test may want to know about a plan. */
+typedef struct {
+    int op, R, rank, backend, order;
+    int64_t M, N, K, M_r;
+    int64_t chunk_rows;    /* rows per chunk                                    */
+    int split;             /* chunks per rank row block                         */
+    int n_row_chunks;      /* chunks over the whole row space = M / chunk_rows  */
+    int n_transfers;       /* staging transfers (row chunk, source rank)        */
+    int tile_m, tile_n, tiles_m, tiles_n, n_tiles;
+    int grid_compute;      /* GEMM CTAs (0 before a device plan exists)          */
+    int grid_comm;         /* dedicated staging CTAs                             */
+    int smem_bytes;        /* dynamic shared memory per CTA                      */
+    int num_sms;
+    uint32_t epoch;        /* calls issued so far                               */
+    uint64_t recv_bytes;   /* plan-owned staging receive buffer                 */
+} syn_plan_info_t;
+
+/* Host-only schedule builder: no CUDA call, usable without a GPU.
+ * Builds the chunk partition, the arrival order of the staging transfers and
+ * the rewritten tile order exactly as syn_plan_create does (method ¶2 and ¶4,
+ * paper §5.2, Fig. 6).  Any output array may be NULL; call once with NULLs to
+ * learn the sizes from *info.
+ *   tile_list[i]  = tile id (tile_row * tiles_n + tile_col) of the i-th tile
+ *                   in execution order; persistent CTA c runs entries
+ *                   c, c + G, c + 2G, ...
+ *   tile_key[i]   = the chunk-arrival key the order is sorted by (the latest
+ *                   arrival index among the chunks the tile consumes; negative
+ *                   for GEMM-RS tiles that only produce send chunks)
+ *   transfers[a]  = row_chunk * R + source_rank of the a-th staging transfer
+ *                   in arrival order
+ * Returns SYN_ERR_INVALID / SYN_ERR_UNSUPPORTED for shapes outside the limits. */
+int syn_schedule_build(syn_op_t op, int R, int rank, const syn_layout_t *layout,
+                       int64_t chunk_rows, int split, syn_order_t order,
+                       const syn_knobs_t *knobs, syn_plan_info_t *info,
+                       int32_t *tile_list, int32_t *tile_key, int32_t *transfers);
+
+/* Fill *knobs with the defaults (CE backend, 128x256 tiles, 2 s timeout). */
+int syn_knobs_default(syn_knobs_t *knobs);
+
+/* Build a plan on the current CUDA device: validates, builds the schedule,
+ * allocates and uploads flags, counters, tables and (for backends that stage
+ * through global memory in GEMM-RS/AR) the receive buffer.
+ * chunk_rows and split: chunks per rank row block; give either (the other 0)
+ * or both with chunk_rows * split == M/R; both 0 means split = 1.
+ * knobs may be NULL (defaults).  On success *out owns device memory. */
+int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank,
+                    const syn_layout_t *layout, int64_t chunk_rows, int split,
+                    syn_order_t order, const syn_knobs_t *knobs);
+
+/* Free a plan (synchronises its helper stream first).  NULL is a no-op. */
+int syn_plan_destroy(syn_plan_t plan);
+
+/* AllGather-GEMM (summary page, Experiments, paper §6.1).
+ *   shards   : host array of R device pointers, bf16 [M/R, K] each; shards[r]
+ *              may alias gathered + r*(M/R)*K (in-place local slot, not copied)
+ *   gathered : bf16 [M, K] output; gathered[q*M/R + i] = shards[q][i] bit for bit
+ *   B        : bf16 [K, N]
+ *   C        : bf16 [M, N] output, C = gathered . B, fp32 accumulation, one
+ *              round-to-nearest-even
+ * Tiles of C start as soon as the chunks of gathered they read have arrived. */
+int syn_ag_gemm(syn_plan_t plan, const void *const *shards, void *gathered,
+                const void *B, void *C, void *stream);
+
+/* GEMM-ReduceScatter for the plan's rank r (summary page, Experiments, paper
+ * §6.1).
+ *   A             : bf16 [M, K], B : bf16 [K, N]
+ *   peer_partials : host array of R device pointers, fp32 [M, N] each: peer q's
+ *                   partial product; entry r is ignored (may be NULL)
+ *   send          : nullable fp32 [M, N]; rows of every rank q != r receive
+ *                   the local partial P = A.B (the chunks peers would pull);
+ *                   rows of rank r are not written
+ *   out_r         : bf16 [M/R, N] = rne(P[rows_r] + sum_{q != r, ascending}
+ *                   peer_q[rows_r])
+ * Send tiles run first (in ring order of their destination), reduce tiles last. */
+int syn_gemm_rs(syn_plan_t plan, const void *A, const void *B,
+                const float *const *peer_partials, float *send, void *out_r,
+                void *stream);
+
+/* GEMM-AllReduce for the plan's rank r (summary page, Experiments, paper §6.1).
+ *   out     : bf16 [M, N] = rne(A.B + sum_{q != r, ascending} peer_q)
+ *   publish : nullable fp32 [M, N] = A.B (the local partial peers would pull)
+ * Other arguments as for syn_gemm_rs. */
+int syn_gemm_ar(syn_plan_t plan, const void *A, const void *B,
+                const float *const *peer_partials, float *publish, void *out,
+                void *stream);
+
+/* Synchronise `stream`, then read and clear the plan's device error word.
+ * Returns SYN_OK, SYN_ERR_TIMEOUT or SYN_ERR_BOUNDS (device side) or
+ * SYN_ERR_CUDA.  After a device error the plan's flag/counter state is reset,
+ * so the next call starts clean. */
+int syn_sync_status(syn_plan_t plan, void *stream);
+
+/* Plan facts (sizes, grid, epoch). */
+int syn_plan_query(syn_plan_t plan, syn_plan_info_t *info);
+
+/* Copy the plan's host schedule tables out (same meaning as in
+ * syn_schedule_build; each pointer may be NULL). */
+int syn_plan_tables(syn_plan_t plan, int32_t *tile_list, int32_t *tile_key,
+                    int32_t *transfers);
+
+/* Copy the device ready flags out (synchronous).  in_flags has
+ * n_row_chunks * R entries (row_chunk * R + source_rank) and holds the epoch
+ * of the call that last published that transfer; out_flags has n_row_chunks
+ * entries and holds the epoch of the call whose tiles last finished producing
+ * that row chunk of `send` (GEMM-RS) or `publish` (GEMM-AR). */
+int syn_plan_flags(syn_plan_t plan, uint32_t *in_flags, uint32_t *out_flags);
+
+/* Trace counters (knobs.trace = 1): total nanoseconds the GEMM CTAs spent in
+ * chunk-flag waits, and total nanoseconds they were resident, summed over CTAs
+ * since the plan was created.  Synchronous. */
+int syn_plan_stats(syn_plan_t plan, uint64_t *flag_wait_ns, uint64_t *cta_busy_ns);
+
+/* Enumerate-and-measure autotuner (summary page, method ¶4 and paper §6.3,
+ * Fig. 11; Entwine's communication-SM balance).  Allocates its own scratch
+ * operands of the given shape, times every candidate (backend, comm_sms,
+ * split, tile order, tile_n) with CUDA events, and returns the fastest.
+ * budget_s bounds the wall time (0 = 60 s).  If the SYN_TUNE_CACHE
+ * environment variable names a file, results are cached there as JSON lines
+ * keyed by (op, R, rank, M, N, K) and a cache hit returns without measuring.
+ * best_us may be NULL. */
+int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *layout,
+                 double budget_s, syn_knobs_t *best, int *best_split,
+                 syn_order_t *best_order, double *best_us);
+
+/* Number of SMs of the current device (0 and SYN_ERR_CUDA without a GPU). */
+int syn_device_sms(int *num_sms);
+
+/* Static description of a status code. */
+const char *syn_status_string(int status);
+
+/* Message for the most recent failing call on this thread ("" if none). */
+const char *syn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SYN_H */

@@ -1,0 +1,55 @@
+"""The C ABI: libsyn.so loads and exports every function include/syn.h
+declares; status strings and defaults; device calls fail loudly without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from chunk_scheduled_communication_gb300 import syn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "syn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(syn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("syn_plan_create", "syn_plan_destroy", "syn_ag_gemm", "syn_gemm_rs", "syn_gemm_ar",
+                 "syn_sync_status", "syn_plan_query", "syn_autotune", "syn_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(syn.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(declared_functions()) == set(syn._SIGS)
+
+
+def test_status_strings_and_defaults():
+    L = syn.lib()
+    assert L.syn_status_string(0) == b"SYN_OK"
+    assert L.syn_status_string(-4) == b"SYN_ERR_TIMEOUT"
+    k = syn.make_knobs()
+    assert k.backend == syn.BACKEND_CE and k.tile_n == 256 and k.debug_drop_chunk == -1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
+def test_plan_create_fails_loudly_without_gpu():
+    with pytest.raises(syn.SynError) as e:
+        syn.Plan("ag", 4, 0, 256, 256, 256)
+    assert e.value.status == syn.ERR_CUDA
+
+
+def test_null_arguments_are_rejected():
+    L = syn.lib()
+    assert L.syn_plan_destroy(None) == 0
+    assert L.syn_sync_status(None, None) == syn.ERR_INVALID
+    assert L.syn_ag_gemm(None, None, None, None, None, None) == syn.ERR_INVALID
+    assert L.syn_plan_query(None, None) == syn.ERR_INVALID

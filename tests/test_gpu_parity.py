@@ -1,0 +1,258 @@
+"""GPU parity: the fused chunk-scheduled kernels against the CPU oracle.
+
+Everything is called through the C ABI (libsyn.so) on cuda:0.  The bar:
+gathered buffers bit-exact; bf16 outputs within |gpu-ref| <= 1e-2 + 1e-2*|ref|
+per element and relative Frobenius error <= 2e-3; fp32 send/publish within the
+same per-element bound; integer-valued inputs bit-exact everywhere; and every
+backend, split and tile order gives bit-identical GPU outputs (chunking changes
+when data moves, never what is computed: Syncopate summary page, method
+§5.1-§5.2; pith review, "outputs match").
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunk_scheduled_communication_gb300 import runner, syn
+from chunk_scheduled_communication_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV_BACKENDS = ["ce", "tma_dedicated", "tma_colocated", "unfused", "decomposed"]
+RSAR_BACKENDS = DEV_BACKENDS + ["tma_colocated_smem"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    torch.cuda.set_device(0)
+    syn.lib()
+    oracle.build()
+
+
+@functools.lru_cache(maxsize=8)
+def inputs(w, r, seed=0, kind="normal"):
+    return wl.make_inputs(w, r=r, seed=seed, kind=kind)
+
+
+@functools.lru_cache(maxsize=8)
+def reference(w, r, seed=0, kind="normal", rows=None):
+    """Oracle outputs (all rows, or the sampled row list `rows`)."""
+    inp = inputs(w, r, seed, kind)
+    if w.op == "ag":
+        g, C = oracle.ag_gemm(inp.shards, inp.B)
+        return {"gathered": g, "out": C}
+    if w.op == "rs":
+        out, send = oracle.gemm_rs(inp.A, inp.B, inp.peers, w.R, r, send_rows=(0, w.M))
+        return {"out": out, "f32": send}
+    out, pub = oracle.gemm_ar(inp.A, inp.B, inp.peers, w.R, r, want_publish=True)
+    return {"out": out, "f32": pub}
+
+
+def run(w, r, backend="ce", split=1, order="grouped", tile_n=None, comm_sms=8, kind="normal",
+        inplace_local=True, with_f32=True, calls=1):
+    if tile_n is None:
+        tile_n = 256 if w.N % 256 == 0 else 128
+    inp = inputs(w, r, 0, kind)
+    d = runner.upload(inp, inplace_local=inplace_local, with_f32_out=with_f32)
+    with runner.make_plan(d, split=split, order=order, backend=backend, tile_n=tile_n,
+                          comm_sms=comm_sms) as plan:
+        for _ in range(calls):
+            runner.call(plan, d)
+        st = plan.sync()
+        assert st == syn.OK, syn.lib().syn_last_error()
+        fin, fout = plan.flags()
+        epoch = plan.info()["epoch"]
+    out = {"out": runner.dev_to_u16(d.out), "flags": (fin, fout, epoch)}
+    if w.op == "ag":
+        out["gathered"] = runner.dev_to_u16(d.gathered)
+    elif d.f32_out is not None:
+        out["f32"] = d.f32_out.cpu().numpy()
+    return out
+
+
+def check_against_oracle(w, r, got, kind="normal"):
+    ref = reference(w, r, 0, kind)
+    if w.op == "ag":
+        assert (got["gathered"] == ref["gathered"]).all(), "gathered buffer not bit-exact"
+    if kind == "int":
+        assert (got["out"] == ref["out"]).all(), "integer inputs must match bit for bit"
+    else:
+        ok, exc, frob = runner.bf16_close(got["out"], ref["out"])
+        assert ok, f"out: excess={exc:.3g} frob={frob:.3g}"
+    if "f32" in got and w.op != "ag":
+        g, rf = got["f32"], ref["f32"]
+        if w.op == "rs":
+            keep = np.ones(w.M, bool)
+            keep[r * w.M_r:(r + 1) * w.M_r] = False
+            g, rf = g[keep], rf[keep]
+        if kind == "int":
+            assert (g == rf).all()
+        else:
+            ok, exc, frob = runner.f_close(g, rf)
+            assert ok, f"f32 out: excess={exc:.3g} frob={frob:.3g}"
+
+
+# ----------------------------------------------------------------------------- tiny AG, every rank
+@pytest.mark.parametrize("backend", DEV_BACKENDS)
+@pytest.mark.parametrize("r", [0, 1, 2, 3])
+def test_tiny_ag_every_rank_and_backend(r, backend):
+    got = run(wl.TINY_AG, r, backend=backend, order="row", comm_sms=2)
+    check_against_oracle(wl.TINY_AG, r, got)
+
+
+def test_tiny_ag_not_inplace_copies_local_slot():
+    got = run(wl.TINY_AG, 2, inplace_local=False)
+    check_against_oracle(wl.TINY_AG, 2, got)
+
+
+# ----------------------------------------------------------------------------- exact integer cases
+INT_AG = wl.scaled(wl.TINY_AG, M=3 * 200, K=192, N=512, R=3)        # M tail, chunks straddle tiles
+INT_RS = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=4 * 256, K=320, N=256, R=4)
+INT_AR = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=2 * 333, K=128, N=384, R=2)  # M tail
+
+
+@pytest.mark.parametrize("w", [INT_AG, INT_RS, INT_AR], ids=["ag", "rs", "ar"])
+@pytest.mark.parametrize("backend", ["ce", "tma_dedicated", "tma_colocated"])
+def test_integer_inputs_bit_exact(w, backend):
+    for r in (0, w.R - 1):
+        got = run(w, r, backend=backend, kind="int", comm_sms=3)
+        check_against_oracle(w, r, got, kind="int")
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_integer_ar_colocated_smem_and_tile128(tile_n):
+    got = run(INT_AR, 1, backend="tma_colocated_smem", kind="int", tile_n=tile_n)
+    check_against_oracle(INT_AR, 1, got, kind="int")
+
+
+# ----------------------------------------------------------------------------- edge shapes
+@pytest.mark.parametrize("shape", [
+    dict(R=1, M=128, K=64, N=256),     # one rank, one k-block, one tile
+    dict(R=2, M=2 * 40, K=64, N=128),  # M smaller than a tile
+    dict(R=5, M=5 * 96, K=640, N=384),  # odd R, ragged tail, N/128 tiles
+    dict(R=8, M=8 * 16, K=128, N=256),  # 8 chunks inside one tile
+])
+def test_ag_edge_shapes(shape):
+    w = wl.scaled(wl.TINY_AG, **shape)
+    for backend in ("ce", "tma_colocated", "tma_dedicated"):
+        got = run(w, shape["R"] - 1, backend=backend, comm_sms=2)
+        check_against_oracle(w, shape["R"] - 1, got)
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+def test_llama3_8b_ag_full_all_splits_bit_identical():
+    w = wl.LLAMA3_8B_UP_AG
+    base = None
+    for split in w.splits:
+        got = run(w, 0, backend="ce", split=split)
+        if base is None:
+            check_against_oracle(w, 0, got)
+            base = got
+        else:
+            assert (got["out"] == base["out"]).all() and (got["gathered"] == base["gathered"]).all()
+    for backend in ("tma_dedicated", "tma_colocated", "unfused", "decomposed"):
+        got = run(w, 0, backend=backend, split=2, order="row")
+        assert (got["out"] == base["out"]).all(), backend
+        assert (got["gathered"] == base["gathered"]).all(), backend
+
+
+def test_llama3_8b_rs_full():
+    w = wl.LLAMA3_8B_DOWN_RS
+    base = run(w, 0, backend="ce", split=1)
+    check_against_oracle(w, 0, base)
+    fin, fout, epoch = base["flags"]
+    # with split 1, row chunk rc is rank rc's block: every send chunk (rc != 0)
+    # published this call's epoch, and every staged peer chunk arrived
+    assert all(fout[rc] == epoch for rc in range(1, w.R))
+    assert all(fin[0 * w.R + q] == epoch for q in range(1, w.R))
+    for backend, split in (("tma_dedicated", 2), ("tma_colocated", 4), ("tma_colocated_smem", 1),
+                           ("unfused", 2), ("decomposed", 2)):
+        got = run(w, 0, backend=backend, split=split)
+        assert (got["out"] == base["out"]).all(), backend
+        keep = np.ones(w.M, bool)
+        keep[:w.M_r] = False
+        assert (got["f32"][keep] == base["f32"][keep]).all(), backend
+
+
+def test_qwen2_7b_ar_full():
+    w = wl.QWEN2_7B_DOWN_AR
+    base = run(w, 0, backend="tma_colocated_smem", split=1)
+    check_against_oracle(w, 0, base)
+    for backend, split in (("ce", 2), ("tma_dedicated", 4), ("tma_colocated", 1), ("unfused", 1)):
+        got = run(w, 0, backend=backend, split=split)
+        assert (got["out"] == base["out"]).all(), backend
+        assert (got["f32"] == base["f32"]).all(), backend
+
+
+def test_llama3_70b_ag_full_sampled_rows():
+    """Full-size 70B up-projection: sampled rows against the oracle (row by row),
+    and every split 1..8 bit-identical on the GPU."""
+    w = wl.LLAMA3_70B_UP_AG
+    inp = inputs(w, 0)
+    base = run(w, 0, backend="ce", split=1)
+    g_ref = np.concatenate(inp.shards)
+    assert (base["gathered"] == g_ref).all()
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(w.M, size=192, replace=False))
+    for lo in range(0, len(rows), 64):
+        for i in rows[lo:lo + 64]:
+            _, ref = oracle.ag_gemm(inp.shards, inp.B, int(i), int(i) + 1, want_gathered=False)
+            ok, exc, frob = runner.bf16_close(base["out"][i:i + 1], ref)
+            assert ok, (i, exc, frob)
+    for split in (2, 3, 4, 5, 6, 7, 8):
+        got = run(w, 0, backend="ce", split=split, order="row")
+        assert (got["out"] == base["out"]).all(), split
+    for backend in ("tma_dedicated", "tma_colocated"):
+        got = run(w, 0, backend=backend, split=4, comm_sms=16)
+        assert (got["out"] == base["out"]).all(), backend
+
+
+# ----------------------------------------------------------------------------- protocol
+def test_repeated_calls_and_epochs():
+    w = wl.TINY_AG
+    got = run(w, 1, backend="tma_colocated", calls=5)
+    check_against_oracle(w, 1, got)
+    fin, fout, epoch = got["flags"]
+    assert epoch == 5
+    # every non-local transfer published epoch 5
+    info, tl, tk, tr = syn.schedule_build("ag", 4, 1, 256, 256, 256)
+    for code in tr:
+        if code % 4 != 1:
+            assert fin[code] == 5
+
+
+@pytest.mark.parametrize("backend", ["ce", "tma_dedicated", "tma_colocated"])
+def test_dropped_chunk_times_out_then_recovers(backend):
+    w = wl.TINY_AG
+    inp = inputs(w, 0)
+    d = runner.upload(inp)
+    with runner.make_plan(d, backend=backend, comm_sms=2, drop_chunk=2, timeout_ns=20_000_000) as bad:
+        runner.call(bad, d)
+        assert bad.sync() == syn.ERR_TIMEOUT
+    with runner.make_plan(d, backend=backend, comm_sms=2) as good:
+        runner.call(good, d)
+        assert good.sync() == syn.OK
+    check_against_oracle(w, 0, {"out": runner.dev_to_u16(d.out), "gathered": runner.dev_to_u16(d.gathered)})
+
+
+def test_trace_counters():
+    w = wl.scaled(wl.LLAMA3_8B_UP_AG, M=8 * 256, K=1024, N=512)
+    inp = inputs(w, 0)
+    d = runner.upload(inp)
+    with runner.make_plan(d, backend="ce", trace=1, split=2) as plan:
+        runner.call(plan, d)
+        assert plan.sync() == syn.OK
+        wait_ns, busy_ns = plan.stats()
+    assert busy_ns > 0 and 0 <= wait_ns <= busy_ns * 2
+
+
+def test_autotune_small_budget(tmp_path, monkeypatch):
+    monkeypatch.setenv("SYN_TUNE_CACHE", str(tmp_path / "tune.jsonl"))
+    best = syn.autotune("ag", 4, 0, 4 * 256, 512, 512, budget_s=5.0)
+    assert best["backend"] in syn.BACKENDS and best["us"] > 0
+    again = syn.autotune("ag", 4, 0, 4 * 256, 512, 512, budget_s=5.0)  # cache hit
+    assert again["backend"] == best["backend"] and again["split"] == best["split"]

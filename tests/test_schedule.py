@@ -1,0 +1,146 @@
+"""Host-side chunk plan (no GPU): partition, arrival order, dependency keys
+and the rewritten tile order (Syncopate summary page, method ¶2 and ¶4, paper
+§5.2, Fig. 6; Entwine abstract for the producer-side send order).
+
+Every property is recomputed here from its definition, independently of the
+library's code, and compared with what syn_schedule_build returns.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+from chunk_scheduled_communication_gb300 import syn
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    syn.lib()
+
+
+def expected_transfers(op, R, r, split):
+    """Arrival order by definition: local data first, then the ring q = r+1..r-1."""
+    out = []
+    if op == "ag":
+        for d in range(R):
+            q = (r + d) % R
+            out += [(q * split + j) * R + q for j in range(split)]
+    else:
+        blocks = [r] if op == "rs" else [(r + d) % R for d in range(R)]
+        for b in blocks:
+            for j in range(split):
+                out += [(b * split + j) * R + (r + d) % R for d in range(1, R)]
+    return out
+
+
+def deps(op, R, r, M, M_r, cr, tm, tile_m=128):
+    rows = range(tm * tile_m, min((tm + 1) * tile_m, M))
+    rcs = sorted({i // cr for i in rows})
+    if op == "ag":
+        return [rc * R + rc // (M_r // cr) for rc in rcs]
+    if op == "rs" and (tm * tile_m) // M_r != r:
+        return []
+    return [rc * R + q for rc in rcs for q in range(R) if q != r]
+
+
+CASES = [
+    ("ag", 4, 1, 256, 256, 256, 1),     # tiny: each tile straddles 2 shards
+    ("ag", 8, 0, 8192, 1792, 4096, 2),
+    ("ag", 8, 5, 8192, 1792, 4096, 4),
+    ("ag", 3, 2, 600, 512, 192, 1),     # ragged M tail, chunk rows 200
+    ("ag", 8, 3, 16384, 3584, 8192, 8),
+    ("ag", 8, 7, 128, 256, 128, 1),     # 8 chunks inside one tile
+    ("rs", 8, 0, 8192, 4096, 1792, 1),
+    ("rs", 8, 6, 8192, 4096, 1792, 4),
+    ("rs", 4, 1, 1024, 256, 320, 2),
+    ("ar", 8, 0, 4096, 3584, 2368, 1),
+    ("ar", 8, 4, 4096, 3584, 2368, 4),
+    ("ar", 2, 1, 666, 384, 128, 1),
+]
+
+
+@pytest.mark.parametrize("op,R,r,M,N,K,split", CASES)
+@pytest.mark.parametrize("order", ["row", "col", "grouped"])
+def test_schedule_properties(op, R, r, M, N, K, split, order):
+    tile_n = 256 if N % 256 == 0 else 128
+    info, tl, tk, tr = syn.schedule_build(op, R, r, M, N, K, split=split, order=order, tile_n=tile_n)
+    M_r = M // R
+    cr = M_r // split
+    tiles_m, tiles_n = -(-M // 128), N // tile_n
+    assert info["chunk_rows"] == cr and info["n_row_chunks"] == M // cr
+    assert info["n_tiles"] == tiles_m * tiles_n
+    # the tile list is a permutation of all tiles
+    assert sorted(tl.tolist()) == list(range(tiles_m * tiles_n))
+    # arrival order
+    assert tr.tolist() == expected_transfers(op, R, r, split)
+    arrival = {code: a for a, code in enumerate(tr.tolist())}
+    # each tile's key is the latest arrival among the chunks it consumes;
+    # RS send tiles (consume nothing) are negative and come in ring order
+    for t, key in zip(tl.tolist(), tk.tolist()):
+        tm = t // tiles_n
+        d = deps(op, R, r, M, M_r, cr, tm)
+        if d:
+            assert key == max(arrival[c] for c in d), (t, key, d)
+        else:
+            assert op == "rs" and key < 0
+            block = (tm * 128) // M_r
+            j = ((tm * 128) % M_r) // cr
+            assert key == (((block - r) % R) - 1) * split + j - (R - 1) * split
+    # the list is sorted by key (chunks walked in arrival order)
+    assert (np.diff(tk) >= 0).all()
+    # within a key group, the chosen traversal
+    for key, grp in itertools.groupby(zip(tk.tolist(), tl.tolist()), key=lambda x: x[0]):
+        ids = [t for _, t in grp]
+        coords = [(t // tiles_n, t % tiles_n) for t in ids]
+        if order == "row":
+            want = sorted(coords)
+        elif order == "col":
+            want = sorted(coords, key=lambda c: (c[1], c[0]))
+        else:
+            want = sorted(coords, key=lambda c: (c[0] // 8, c[1], c[0] % 8))
+        assert coords == want
+
+
+def test_tiny_each_tile_depends_on_two_chunks():
+    info, tl, tk, tr = syn.schedule_build("ag", 4, 0, 256, 256, 256, split=1)
+    assert info["n_tiles"] == 2 and info["chunk_rows"] == 64
+    for tm in range(2):
+        assert len(deps("ag", 4, 0, 256, 64, 64, tm)) == 2
+
+
+def test_rs_send_tiles_first_reduce_tiles_last():
+    info, tl, tk, tr = syn.schedule_build("rs", 8, 2, 8192, 4096, 1792, split=2)
+    tiles_n = 4096 // 256
+    blocks = [(t // tiles_n) * 128 // 1024 for t in tl]
+    n_local = (1024 // 128) * tiles_n
+    assert all(b == 2 for b in blocks[-n_local:])
+    assert all(b != 2 for b in blocks[:-n_local])
+    first = [b for b in blocks[:-n_local]]
+    # destinations in ring order 3, 4, ..., 1
+    seen = [b for i, b in enumerate(first) if i == 0 or first[i - 1] != b]
+    assert seen == [3, 4, 5, 6, 7, 0, 1]
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(op="ag", R=4, rank=4, M=256, N=256, K=256), syn.ERR_INVALID),
+    (dict(op="ag", R=3, rank=0, M=256, N=256, K=256), syn.ERR_INVALID),      # M % R
+    (dict(op="ag", R=4, rank=0, M=256, N=256, K=100), syn.ERR_UNSUPPORTED),  # K % 64
+    (dict(op="ag", R=4, rank=0, M=256, N=200, K=256), syn.ERR_UNSUPPORTED),  # N % tile_n
+    (dict(op="ag", R=16, rank=0, M=256, N=256, K=256), syn.ERR_UNSUPPORTED),  # R > 8
+    (dict(op="rs", R=4, rank=0, M=4 * 96, N=256, K=256), syn.ERR_UNSUPPORTED),  # M_r % 128
+    (dict(op="ag", R=4, rank=0, M=256, N=256, K=256, split=3), syn.ERR_INVALID),  # split ∤ M_r
+    (dict(op="ag", R=4, rank=0, M=256, N=256, K=256, chunk_rows=32, split=4), syn.ERR_INVALID),
+])
+def test_invalid_shapes_rejected(kw, status):
+    kw = dict(kw)
+    args = [kw.pop(k) for k in ("op", "R", "rank", "M", "N", "K")]
+    with pytest.raises(syn.SynError) as e:
+        syn.schedule_build(*args, **kw)
+    assert e.value.status == status
+
+
+def test_chunk_rows_and_split_agree():
+    a = syn.schedule_build("ag", 8, 0, 8192, 1792, 4096, chunk_rows=256, split=0)
+    b = syn.schedule_build("ag", 8, 0, 8192, 1792, 4096, chunk_rows=0, split=4)
+    assert a[0]["split"] == b[0]["split"] == 4
+    assert (a[1] == b[1]).all() and (a[3] == b[3]).all()
