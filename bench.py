@@ -1,0 +1,481 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused chunk-scheduled AG-GEMM / GEMM-RS / GEMM-AR on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  AG-GEMM  Llama-3-8B FFN up-projection, TP=8   (M=8192, K=4096, N=1792)
+  GEMM-RS  Llama-3-8B FFN down-projection, TP=8 (M=8192, K=1792, N=4096, send on)
+  GEMM-AR  Qwen2-7B FFN down-projection, TP=8   (M=4096, K=2368, N=3584)
+each as one fused chunk-scheduled call through the C ABI, the 7 other ranks
+simulated in the same HBM (Syncopate summary page, Experiments, paper §6.1).
+
+Metric: TFLOP/s over the step (2*M*N*K summed over the three operators), with
+each operator's fraction of its roofline beside it.  Inputs are resident in
+HBM before the timed region; the step streams ~2 GB, far more than the 135 MB
+L2, so no explicit flush is needed between steps.  `e2e` repeats the
+measurement with the inputs copied from pinned host memory and the bf16
+outputs copied back inside the timed region.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch with torch.distributed.run: every rank runs an independent
+replica (the tensor-parallel ranks are already simulated inside one GPU).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from chunk_scheduled_communication_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "fused AG-GEMM/GEMM-RS/GEMM-AR TFLOPS and % of roofline on 1 GB300"
+UNIT = "TFLOP/s"
+WORKLOAD_NAME = ("llama3-8b-ffn-tp8 step: AG-GEMM up (8192x4096x1792) + GEMM-RS down "
+                 "(8192x1792x4096, send) + qwen2-7b GEMM-AR down (4096x2368x3584)")
+STEP = [wl.LLAMA3_8B_UP_AG, wl.LLAMA3_8B_DOWN_RS, wl.QWEN2_7B_DOWN_AR]
+
+# Knobs per operator (backend, split, order, tile_n, comm_sms).
+DEFAULT_KNOBS = {
+    "ag": dict(backend="ce", split=1, order="grouped", tile_n=256, comm_sms=8),
+    "rs": dict(backend="tma_colocated_smem", split=1, order="grouped", tile_n=256, comm_sms=8),
+    "ar": dict(backend="tma_colocated_smem", split=1, order="grouped", tile_n=256, comm_sms=8),
+}
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def algorithmic_bytes(w: wl.Workload, with_send=True) -> float:
+    """Bytes the method must move through this HBM (each operand read once,
+    each output written once; AG: staged peer shards read + written; RS/AR:
+    each peer byte read once; RS: the fp32 send rows)."""
+    M, N, K, R = w.M, w.N, w.K, w.R
+    if w.op == "ag":
+        staged = (R - 1) * w.M_r * K * 2
+        return M * K * 2 + K * N * 2 + M * N * 2 + 2 * staged
+    if w.op == "rs":
+        peers = (R - 1) * w.M_r * N * 4
+        send = (R - 1) * w.M_r * N * 4 if with_send else 0
+        return M * K * 2 + K * N * 2 + peers + send + w.M_r * N * 2
+    return M * K * 2 + K * N * 2 + (R - 1) * M * N * 4 + M * N * 2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunk_scheduled_communication_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cuh", ".cu", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(op: str):
+    """DRAM traffic per launch recorded from an ncu capture of the current
+    kernel sources (profiles/dram_traffic.txt lines: `op src_hash bytes`);
+    None when absent or when the kernels changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    cur = kernel_source_hash()
+    for line in open(p):
+        parts = line.split("#")[0].split()
+        if len(parts) >= 3 and parts[0] == op and parts[1] == cur:
+            return float(parts[2])
+    return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1].split()[0]))
+                smax.append(float(f[2].split()[0]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup(n_gpus: int):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+def barrier(dist, dev=None):
+    if dist is not None:
+        if dev is not None:
+            dist.barrier(device_ids=[dev])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, x: float, dev=None) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=f"cuda:{dev}" if dev is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+def oracle_sample(inputs, frac: float):
+    """Run the CPU oracle on `frac` of each operator's output rows (at least
+    one row each).  Returns (seconds, flops, description)."""
+    import oracle
+    flops = 0.0
+    desc = []
+    t0 = time.perf_counter()
+    for w, inp in zip(STEP, inputs):
+        if w.op == "ag":
+            rows = max(1, int(w.M * frac))
+            oracle.ag_gemm(inp.shards, inp.B, 0, rows, want_gathered=False)
+        elif w.op == "rs":
+            rows = max(1, int(w.M_r * frac))
+            oracle.gemm_rs(inp.A, inp.B, inp.peers, w.R, 0, 0, rows)
+            srows = max(1, int((w.M - w.M_r) * frac))
+            oracle.gemm_rs(inp.A, inp.B, inp.peers, w.R, 0, 0, 1, send_rows=(w.M_r, w.M_r + srows))
+            rows = rows + srows + 1
+        else:
+            rows = max(1, int(w.M * frac))
+            oracle.gemm_ar(inp.A, inp.B, inp.peers, w.R, 0, 0, rows)
+        flops += 2.0 * rows * w.N * w.K
+        desc.append(f"{w.op}:{rows} rows")
+    return time.perf_counter() - t0, flops, ", ".join(desc)
+
+
+def run_reference(args, dist, rank):
+    """`--impl reference`: the CPU oracle timed on the host cores."""
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    inputs = [wl.make_inputs(w, r=0, seed=0) for w in STEP]
+    # size each step so the whole run ends within a few minutes
+    t_cal, f_cal, _ = oracle_sample(inputs, 1.0 / 1024)
+    rate = f_cal / max(t_cal, 1e-6)
+    full = sum(w.flops for w in STEP)
+    budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    frac = min(1.0, max(1.0 / 8192, budget * rate / full))
+    for _ in range(args.warmup):
+        oracle_sample(inputs, frac)
+    tot_t, tot_f, desc = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        t, f, desc = oracle_sample(inputs, frac)
+        tot_t += t
+        tot_f += f
+    value = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded normal, Llama-3/Qwen FFN shapes)",
+            "config": {"workload": WORKLOAD_NAME, "parallelism": f"tp8 simulated in one device x{args.gpus}"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                             "sample": f"per step {desc} ({frac:.5f} of each operator's rows)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="syn", choices=["syn", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-frac", type=float, default=1.0,
+                    help="fraction of each operator's rows the CPU oracle baseline computes")
+    ap.add_argument("--no-baselines", action="store_true")
+    ap.add_argument("--knobs", default="", help="JSON overriding the per-operator knobs")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    dist, rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        return run_reference(args, dist, rank)
+
+    import torch
+
+    from chunk_scheduled_communication_gb300 import runner, syn
+
+    torch.cuda.set_device(local)
+    syn.lib()  # raises if the CUDA library is missing: there is no fallback
+    knobs = {k: dict(v) for k, v in DEFAULT_KNOBS.items()}
+    if args.knobs:
+        for k, v in json.loads(args.knobs).items():
+            knobs[k].update(v)
+    peaks, peak_src = load_peaks()
+
+    host_inputs = [wl.make_inputs(w, r=0, seed=0) for w in STEP]
+    devs, plans = [], []
+    for w, inp in zip(STEP, host_inputs):
+        d = runner.upload(inp, with_f32_out=(w.op == "rs"))
+        kn = dict(knobs[w.op])
+        split, order = kn.pop("split"), kn.pop("order")
+        plans.append(runner.make_plan(d, split=split, order=order, **kn))
+        devs.append(d)
+    stream = torch.cuda.current_stream()
+    n_ops = len(STEP)
+
+    def step():
+        for p, d in zip(plans, devs):
+            runner.call(p, d, stream)
+
+    for _ in range(args.warmup):
+        step()
+    for p in plans:
+        p.check(stream)
+
+    # ---------------- timed region (device-resident inputs) ----------------
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ops)]
+          for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist, local)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for k in range(args.steps):
+        for i, (p, d) in enumerate(zip(plans, devs)):
+            ev[k][i][0].record(stream)
+            runner.call(p, d, stream)
+            ev[k][i][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    clk = clocks.stop()
+    for p in plans:
+        p.check(stream)
+    total_ms = e0.elapsed_time(e1)
+    total_ms = max_over_ranks(dist, total_ms, local)
+    ms_per_step = total_ms / args.steps
+    op_ms = [statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
+             for i in range(n_ops)]
+    step_flops = sum(w.flops for w in STEP)
+    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+
+    per_op = {}
+    for w, ms in zip(STEP, op_ms):
+        byts = algorithmic_bytes(w)
+        t_roof = max(w.flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+        per_op[w.op] = {"workload": w.name, "us": ms * 1e3, "tflops": w.flops / (ms * 1e-3) / 1e12,
+                        "gbs": byts / (ms * 1e-3) / 1e9, "algorithmic_bytes": byts,
+                        "roofline_frac": t_roof / (ms * 1e-3),
+                        "bound": "tensor" if w.flops / (peaks["bf16_tflops"] * 1e12) >= byts / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                        "knobs": knobs[w.op]}
+    dom = max(per_op, key=lambda k: per_op[k]["us"])
+    dw = STEP[[w.op for w in STEP].index(dom)]
+    if per_op[dom]["bound"] == "tensor":
+        achieved, peak, unit = per_op[dom]["tflops"], peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = per_op[dom]["gbs"], peaks["hbm_gbs"], "GB/s"
+    roofline = {"bound": per_op[dom]["bound"], "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": recorded_traffic(dom), "kernel": f"syn_fused_kernel<{dom}>",
+                "workload": dw.name, "peak_source": f"{peak_src} (burst)",
+                "algorithmic_per_launch": dw.flops if unit == "TFLOP/s" else algorithmic_bytes(dw)}
+
+    # ---------------- end to end: pinned host inputs in, bf16 outputs out ----------------
+    import torch as _t
+    pinned = []
+    h2d = d2h = 0
+    for w, inp, d in zip(STEP, host_inputs, devs):
+        pairs = []
+        if w.op == "ag":
+            for q in range(w.R):
+                h = _t.from_numpy(inp.shards[q].view(np.int16)).view(_t.bfloat16).pin_memory()
+                pairs.append((h, d.shards[q]))
+        else:
+            pairs.append((_t.from_numpy(inp.A.view(np.int16)).view(_t.bfloat16).pin_memory(), d.A))
+            for q in range(w.R):
+                if d.peers[q] is not None:
+                    pairs.append((_t.from_numpy(inp.peers[q]).pin_memory(), d.peers[q]))
+        pairs.append((_t.from_numpy(inp.B.view(np.int16)).view(_t.bfloat16).pin_memory(), d.B))
+        out_h = _t.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
+        pinned.append((pairs, out_h, d.out))
+        h2d += sum(h.numel() * h.element_size() for h, _ in pairs)
+        d2h += out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for (pairs, out_h, out_d), p, d in zip(pinned, plans, devs):
+            for h, dd in pairs:
+                dd.copy_(h, non_blocking=True)
+            runner.call(p, d, stream)
+            out_h.copy_(out_d, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist, local)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, a0.elapsed_time(a1), local) / args.e2e_steps
+    for p in plans:
+        p.check(stream)
+    e2e = {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ---------------- comparisons (rank 0): unfused / decomposed baselines, cuBLAS+copy ----------------
+    baselines = {}
+    if rank == 0 and not args.no_baselines:
+        for w, inp, d in zip(STEP, host_inputs, devs):
+            res = {}
+            for be in ("unfused", "decomposed"):
+                kn = dict(knobs[w.op])
+                split, order = kn.pop("split"), kn.pop("order")
+                kn["backend"] = be
+                with runner.make_plan(d, split=split, order=order, **kn) as bp:
+                    for _ in range(5):
+                        runner.call(bp, d, stream)
+                    bp.check(stream)
+                    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    reps = 200
+                    b0.record(stream)
+                    for _ in range(reps):
+                        runner.call(bp, d, stream)
+                    b1.record(stream)
+                    torch.cuda.synchronize()
+                    bp.check(stream)
+                    res[f"{be}_us"] = b0.elapsed_time(b1) / reps * 1e3
+            res["fused_us"] = per_op[w.op]["us"]
+            res["fused_speedup_vs_unfused"] = res["unfused_us"] / res["fused_us"]
+            res["cublas_plus_copy_us"] = cublas_plus_copy_us(w, d, stream)
+            baselines[w.op] = res
+
+    # ---------------- CPU oracle baseline (rank 0, N = 1) ----------------
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_frac > 0:
+        import oracle
+        oracle.build()
+        t, f, desc = oracle_sample(host_inputs, args.cpu_frac)
+        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+               "seconds": t, "sample": f"{desc} of the same workload (seed 0, rank 0)"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded normal; no dataset or weights)",
+                "config": {"workload": WORKLOAD_NAME, "global_batch": None, "seq_len": None,
+                           "parallelism": f"tp8 simulated in one device, {world} replica(s)",
+                           "l2": "inputs > L2 (each step streams ~2 GB through the 135 MB L2); no flush"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": sum(launches_per_call(p) for p in plans) * args.steps,
+                "clocks": clk, "per_op": per_op, "baselines": baselines,
+                "peaks": {**peaks, "source": peak_src}}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def launches_per_call(plan) -> int:
+    i = plan.info()
+    return 1 if i["backend"] != 5 else len(set(plan.tables()[1].tolist()))
+
+
+def cublas_plus_copy_us(w, d, stream) -> float:
+    """Context only: the staging copy plus torch.matmul (cuBLAS) on the same
+    operands, and for RS/AR the peer sum in PyTorch (not a fused path)."""
+    import torch
+    reps = 50
+
+    def once():
+        if w.op == "ag":
+            for q in range(w.R):
+                if q != 0:
+                    d.gathered[q * w.M_r:(q + 1) * w.M_r].copy_(d.shards[q])
+            torch.matmul(d.gathered, d.B, out=d.out)
+        else:
+            P = torch.matmul(d.A, d.B).float()
+            rows = slice(0, w.M_r) if w.op == "rs" else slice(0, w.M)
+            acc = P[rows]
+            for q in range(w.R):
+                if d.peers[q] is not None:
+                    acc = acc + d.peers[q][rows]
+            d.out.copy_(acc)
+    for _ in range(3):
+        once()
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(reps):
+        once()
+    b1.record(stream)
+    torch.cuda.synchronize()
+    return b0.elapsed_time(b1) / reps * 1e3
+
+
+if __name__ == "__main__":
+    sys.exit(main())

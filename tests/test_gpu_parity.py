@@ -123,10 +123,13 @@ def test_integer_inputs_bit_exact(w, backend):
         check_against_oracle(w, r, got, kind="int")
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
-def test_integer_ar_colocated_smem_and_tile128(tile_n):
-    got = run(INT_AR, 1, backend="tma_colocated_smem", kind="int", tile_n=tile_n)
-    check_against_oracle(INT_AR, 1, got, kind="int")
+INT_AR_N512 = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=2 * 333, K=128, N=512, R=2)
+
+
+@pytest.mark.parametrize("w,tile_n", [(INT_AR, 128), (INT_AR_N512, 128), (INT_AR_N512, 256)])
+def test_integer_ar_colocated_smem_both_tiles(w, tile_n):
+    got = run(w, 1, backend="tma_colocated_smem", kind="int", tile_n=tile_n)
+    check_against_oracle(w, 1, got, kind="int")
 
 
 # ----------------------------------------------------------------------------- edge shapes
