@@ -46,9 +46,9 @@ STEP = [wl.LLAMA3_8B_UP_AG, wl.LLAMA3_8B_DOWN_RS, wl.QWEN2_7B_DOWN_AR]
 
 # Knobs per operator (backend, split, order, tile_n, comm_sms).
 DEFAULT_KNOBS = {
-    "ag": dict(backend="ce", split=1, order="grouped", tile_n=256, comm_sms=8),
-    "rs": dict(backend="tma_colocated_smem", split=1, order="grouped", tile_n=256, comm_sms=8),
-    "ar": dict(backend="tma_colocated_smem", split=1, order="grouped", tile_n=256, comm_sms=8),
+    "ag": dict(backend="tma_colocated", split=4, order="row", tile_n=256, comm_sms=8, stages=0),
+    "rs": dict(backend="tma_colocated_smem", split=1, order="row", tile_n=256, comm_sms=8, stages=3),
+    "ar": dict(backend="tma_colocated_smem", split=1, order="row", tile_n=256, comm_sms=8, stages=2),
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}

@@ -107,6 +107,7 @@ struct syn_plan_s {
     syn_knobs_t kn;
     int device = 0, num_sms = 0;
     int grid_compute = 0, grid_comm = 0, smem = 0;
+    LaunchCfg lc = {256, 4, false, 0};  // compiled kernel instance
     uint32_t epoch = 0;
     // device state
     int32_t *d_tiles = nullptr, *d_transfers = nullptr, *d_err = nullptr;
@@ -243,10 +244,12 @@ int finish_params_for_staging(syn_plan_s *pl, KernelParams &p) {
 }
 
 cudaError_t launch(syn_plan_s *pl, const KernelParams &p, int grid, cudaStream_t st) {
+    LaunchCfg lc = pl->lc;
+    lc.grid = grid;
     switch (pl->s.op) {
-        case SYN_OP_AG_GEMM: return launch_fused_ag(p, pl->maps, pl->s.tile_n, grid, st);
-        case SYN_OP_GEMM_RS: return launch_fused_rs(p, pl->maps, pl->s.tile_n, grid, st);
-        default: return launch_fused_ar(p, pl->maps, pl->s.tile_n, grid, st);
+        case SYN_OP_AG_GEMM: return launch_fused_ag(p, pl->maps, lc, st);
+        case SYN_OP_GEMM_RS: return launch_fused_rs(p, pl->maps, lc, st);
+        default: return launch_fused_ar(p, pl->maps, lc, st);
     }
 }
 
@@ -355,6 +358,7 @@ int syn_knobs_default(syn_knobs_t *k) {
     k->timeout_ns = 0;
     k->debug_drop_chunk = -1;
     k->trace = 0;
+    k->stages = 0;
     return SYN_OK;
 }
 
@@ -420,7 +424,13 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
     int coop = 0;
     PL_CK(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, pl->device));
     if (!coop) return bail(SYN_ERR_UNSUPPORTED, "device has no cooperative launch");
-    pl->smem = fused_smem_bytes(s.op, s.tile_n);
+    pl->lc.tile_n = s.tile_n;
+    pl->lc.smem_peers = (kn.backend == SYN_BACKEND_TMA_COLOCATED_SMEM);
+    pl->lc.stages = kn.stages > 0 ? kn.stages : default_stages(s.op, s.tile_n);
+    pl->smem = fused_smem_bytes(s.op, pl->lc);
+    if (pl->smem < 0)
+        return bail(SYN_ERR_UNSUPPORTED, "stages = " + std::to_string(pl->lc.stages) +
+                                             " is not compiled for this operator, tile_n and backend");
     if (kn.backend == SYN_BACKEND_TMA_DEDICATED) {
         pl->grid_comm = kn.comm_sms;
         if (pl->grid_comm >= pl->num_sms) return bail(SYN_ERR_INVALID, "comm_sms >= SM count");

@@ -37,18 +37,31 @@
 
 namespace syn {
 
-template <int OP, int BN>
+// Shared memory given to the operand ring, the peer ring and the staging
+// buffers (barriers and bookkeeping come on top).
+constexpr int kSmemRings = 224 * 1024;
+
+// Compile-time shape of one kernel instance: operator, tile width BN, GEMM
+// pipeline stages S, and whether RS/AR peers are fetched per tile straight
+// into shared memory (SMEMP: no co-located staging buffers, so the peer ring
+// takes the rest of the budget).
+template <int OP, int BN, int S_, bool SMEMP>
 struct KCfg {
     static constexpr int BM = 128, BK = 64, UK = 16;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BK * BN * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int S = OP == OP_AG ? (BN == 256 ? 4 : 6) : (BN == 256 ? 3 : 4);
-    static constexpr int P = OP == OP_AG ? 0 : (BN == 256 ? 3 : 4);
+    static constexpr int S = S_;
+    static constexpr int BN_ = BN;
+    static constexpr bool SMEMP_ = SMEMP;
     static constexpr int PEER_COLS = 32;
     static constexpr int PEER_BYTES = BM * PEER_COLS * 4;
-    static constexpr int NSTG = 2;
+    static constexpr int NSTG = SMEMP ? 0 : 2;
     static constexpr int STG_BYTES = 16384;
+    static constexpr int P =
+        OP == OP_AG ? 0 : (kSmemRings - NSTG * STG_BYTES - S * STAGE_BYTES) / PEER_BYTES;
+    static_assert(OP == OP_AG || P >= 2, "peer ring needs at least two slots");
+    static_assert(S * STAGE_BYTES + P * PEER_BYTES + NSTG * STG_BYTES <= kSmemRings, "rings");
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + S * A_BYTES;
@@ -158,8 +171,8 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *flag, const KernelPara
 __device__ __forceinline__ void chunk_range(const KernelParams &p, int tm, int &lo, int &hi) {
     const int r0 = tm * 128;
     const int r1 = min(r0 + 128, p.M);
-    lo = r0 / p.cr;
-    hi = (r1 - 1) / p.cr;
+    lo = chunk_of_row(p.M_r, p.split, r0);
+    hi = chunk_of_row(p.M_r, p.split, r1 - 1);
 }
 
 // Does tile row tm reduce peers?  AR: always; RS: tiles of the local row block.
@@ -236,10 +249,12 @@ __device__ __forceinline__ void stage_slices(const KernelParams &p, int worker, 
         uint8_t *dst;
         int64_t bytes;
         transfer_span(p, code, src, dst, bytes);
+        // slices past the end of a shorter chunk copy nothing but still count
         const int64_t off = (int64_t)sl * p.slice_bytes;
         const int64_t rem = bytes - off;
         const int64_t len = rem < p.slice_bytes ? rem : p.slice_bytes;
-        if (!bulk_copy(src + off, dst + off, len, buf0, nbuf, buf_bytes, bar0, phase_bits, abort, p))
+        if (len > 0 &&
+            !bulk_copy(src + off, dst + off, len, buf0, nbuf, buf_bytes, bar0, phase_bits, abort, p))
             return;
         ptx::fence_proxy_async();
         const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + code, 1u);
@@ -284,8 +299,10 @@ __device__ __forceinline__ void count_produced(const KernelParams &p, int tm, in
         chunk_range(p, tm, lo, hi);
         uint32_t *cnt = p.out_cnt + (size_t)(p.epoch & 1u) * p.n_rc;
         for (int rc = lo; rc <= hi; ++rc) {
-            const int t_lo = (rc * p.cr) / 128;
-            const int t_hi = (rc * p.cr + p.cr - 1) / 128;
+            const int64_t row0 = chunk_row0(p.M_r, p.split, rc);
+            const int64_t row1 = chunk_row0(p.M_r, p.split, rc + 1);
+            const int t_lo = (int)(row0 / 128);
+            const int t_hi = (int)((row1 - 1) / 128);
             const uint32_t need = 4u * (uint32_t)((t_hi - t_lo + 1) * p.tiles_n);
             const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + rc, 1u);
             if (old + 1u == need) ptx::st_release_gpu(p.out_flags + rc, p.epoch);
@@ -294,10 +311,10 @@ __device__ __forceinline__ void count_produced(const KernelParams &p, int tm, in
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int OP, int BN>
+template <int OP, int BN, int S, bool SMEMP>
 __global__ void __launch_bounds__(256, 1)
     syn_fused_kernel(const __grid_constant__ KernelParams p, const __grid_constant__ TensorMaps tm) {
-    using C = KCfg<OP, BN>;
+    using C = KCfg<OP, BN, S, SMEMP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -570,9 +587,10 @@ __global__ void __launch_bounds__(256, 1)
         }
     } else {
         // ================= co-located stager =================
-        if (p.colocated && lane == 0)
-            stage_slices(p, (int)blockIdx.x, p.G, sbase + C::OFF_STG, C::NSTG, C::STG_BYTES,
-                         bar0 + 8 * C::BAR_STG, abort);
+        if constexpr (C::NSTG > 0)
+            if (p.colocated && lane == 0)
+                stage_slices(p, (int)blockIdx.x, p.G, sbase + C::OFF_STG, C::NSTG, C::STG_BYTES,
+                             bar0 + 8 * C::BAR_STG, abort);
     }
 
     // ---- teardown -----------------------------------------------------------
@@ -585,10 +603,10 @@ __global__ void __launch_bounds__(256, 1)
         atomicAdd(p.stats + 1, (unsigned long long)(ptx::globaltimer() - t_start));
 }
 
-template <int OP, int BN>
+template <int OP, int BN, int S, bool SMEMP>
 cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid, cudaStream_t st) {
-    using C = KCfg<OP, BN>;
-    cudaError_t e = cudaFuncSetAttribute(syn_fused_kernel<OP, BN>,
+    using C = KCfg<OP, BN, S, SMEMP>;
+    cudaError_t e = cudaFuncSetAttribute(syn_fused_kernel<OP, BN, S, SMEMP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -601,7 +619,52 @@ cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, syn_fused_kernel<OP, BN>, p, tm);
+    return cudaLaunchKernelEx(&cfg, syn_fused_kernel<OP, BN, S, SMEMP>, p, tm);
+}
+
+// Dispatch over the instantiated (tile_n, stages, smem-peer) combinations of
+// one operator.  `Fn` receives the KCfg type; returns false when the
+// combination is not instantiated.
+template <int OP, typename Fn>
+bool dispatch_cfg(int tile_n, int stages, bool smem_peers, Fn &&fn) {
+    if constexpr (OP == OP_AG) {
+        if (tile_n == 256 && stages == 4) return fn(KCfg<OP, 256, 4, false>{}), true;
+        if (tile_n == 128 && stages == 6) return fn(KCfg<OP, 128, 6, false>{}), true;
+        return false;
+    } else {
+    if (!smem_peers) {
+        if (tile_n == 256 && stages == 3) return fn(KCfg<OP, 256, 3, false>{}), true;
+        if (tile_n == 128 && stages == 4) return fn(KCfg<OP, 128, 4, false>{}), true;
+        return false;
+    }
+    if (tile_n == 256 && stages == 2) return fn(KCfg<OP, 256, 2, true>{}), true;
+    if (tile_n == 256 && stages == 3) return fn(KCfg<OP, 256, 3, true>{}), true;
+    if (tile_n == 256 && stages == 4) return fn(KCfg<OP, 256, 4, true>{}), true;
+    if (tile_n == 128 && stages == 3) return fn(KCfg<OP, 128, 3, true>{}), true;
+    if (tile_n == 128 && stages == 4) return fn(KCfg<OP, 128, 4, true>{}), true;
+    if (tile_n == 128 && stages == 6) return fn(KCfg<OP, 128, 6, true>{}), true;
+    return false;
+    }
+}
+
+template <int OP>
+cudaError_t launch_op(const KernelParams &p, const TensorMaps &tm, const LaunchCfg &lc,
+                      cudaStream_t st) {
+    cudaError_t err = cudaErrorInvalidValue;
+    dispatch_cfg<OP>(lc.tile_n, lc.stages, lc.smem_peers, [&](auto c) {
+        using C = decltype(c);
+        err = launch_fused_t<OP, C::BN_, C::S, C::SMEMP_>(p, tm, lc.grid, st);
+    });
+    return err;
+}
+
+template <int OP>
+int smem_bytes_op(const LaunchCfg &lc) {
+    int bytes = -1;
+    dispatch_cfg<OP>(lc.tile_n, lc.stages, lc.smem_peers, [&](auto c) {
+        bytes = decltype(c)::SMEM_ALLOC;
+    });
+    return bytes;
 }
 
 }  // namespace syn

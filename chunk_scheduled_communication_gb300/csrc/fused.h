@@ -37,7 +37,7 @@ struct TensorMaps {  // CUtensorMap carries its own alignment
 
 struct KernelParams {
     int32_t op, R, rank;
-    int32_t M, N, K, M_r, cr, split, n_rc;
+    int32_t M, N, K, M_r, cr, split, n_rc;  // cr: rows of the largest chunk
     int32_t tiles_m, tiles_n;
     int32_t t_begin, t_end;        // range of tile_list this launch runs
     int32_t G;                     // GEMM CTAs: blockIdx.x < G
@@ -73,31 +73,49 @@ struct KernelParams {
 // Receive-buffer slot of source rank q (the local rank has none).
 SYN_HD int recv_slot(int q, int rank) { return q - (q > rank ? 1 : 0); }
 
-// Source, destination and size of staging transfer `code` = rc * R + q.
-//   AG : shard q rows [(rc - q*split)*cr, +cr)  ->  gathered rows [rc*cr, +cr)
-//   RS : peer q rows [rc*cr, +cr)               ->  recv[slot q] rows [rc*cr - rank*M_r, +cr)
-//   AR : peer q rows [rc*cr, +cr)               ->  recv[slot q] rows [rc*cr, +cr)
+// Source, destination and size of staging transfer `code` = rc * R + q, where
+// row chunk rc covers rows [row0, row1) (chunk_row0 in schedule.h):
+//   AG : shard q rows [row0 - q*M_r, ...)  ->  gathered rows [row0, row1)
+//   RS : peer q rows [row0, row1)           ->  recv[slot q] rows [row0 - rank*M_r, ...)
+//   AR : peer q rows [row0, row1)           ->  recv[slot q] rows [row0, row1)
 SYN_HD void transfer_span(const KernelParams &p, int code, const uint8_t *&src, uint8_t *&dst,
                           int64_t &bytes) {
     const int rc = code / p.R, q = code % p.R;
-    bytes = (int64_t)p.cr * p.row_bytes;
+    const int64_t row0 = chunk_row0(p.M_r, p.split, rc);
+    const int64_t row1 = chunk_row0(p.M_r, p.split, rc + 1);
+    bytes = (row1 - row0) * p.row_bytes;
     if (p.op == OP_AG) {
-        src = p.stage_src[q] + (int64_t)(rc - q * p.split) * p.cr * p.row_bytes;
-        dst = p.stage_dst + (int64_t)rc * p.cr * p.row_bytes;
+        src = p.stage_src[q] + (row0 - (int64_t)q * p.M_r) * p.row_bytes;
+        dst = p.stage_dst + row0 * p.row_bytes;
     } else {
-        const int64_t row = (int64_t)rc * p.cr - (p.op == OP_RS ? (int64_t)p.rank * p.M_r : 0);
-        src = p.stage_src[q] + (int64_t)rc * p.cr * p.row_bytes;
+        const int64_t row = row0 - (p.op == OP_RS ? (int64_t)p.rank * p.M_r : 0);
+        src = p.stage_src[q] + row0 * p.row_bytes;
         dst = p.stage_dst + ((int64_t)recv_slot(q, p.rank) * p.recv_slot_rows + row) * p.row_bytes;
     }
 }
 
-// Host launchers (one translation unit per operator).
-cudaError_t launch_fused_ag(const KernelParams &p, const TensorMaps &tm, int tile_n, int grid,
+// Which compiled kernel instance a launch uses, and its grid.
+struct LaunchCfg {
+    int tile_n;       // 128 or 256
+    int stages;       // GEMM pipeline stages
+    bool smem_peers;  // RS/AR: peers fetched per tile into shared memory
+    int grid;         // CTAs
+};
+
+// Host launchers (one translation unit per operator).  cudaErrorInvalidValue
+// if (tile_n, stages, smem_peers) is not a compiled combination.
+cudaError_t launch_fused_ag(const KernelParams &p, const TensorMaps &tm, const LaunchCfg &lc,
                             cudaStream_t st);
-cudaError_t launch_fused_rs(const KernelParams &p, const TensorMaps &tm, int tile_n, int grid,
+cudaError_t launch_fused_rs(const KernelParams &p, const TensorMaps &tm, const LaunchCfg &lc,
                             cudaStream_t st);
-cudaError_t launch_fused_ar(const KernelParams &p, const TensorMaps &tm, int tile_n, int grid,
+cudaError_t launch_fused_ar(const KernelParams &p, const TensorMaps &tm, const LaunchCfg &lc,
                             cudaStream_t st);
-int fused_smem_bytes(int op, int tile_n);
+// Dynamic shared memory of a combination (-1 if not compiled).
+int fused_smem_bytes(int op, const LaunchCfg &lc);
+// Default pipeline depth: AG 4 (tile_n 256) / 6 (128); RS/AR 3 / 4.
+inline int default_stages(int op, int tile_n) {
+    if (op == OP_AG) return tile_n == 256 ? 4 : 6;
+    return tile_n == 256 ? 3 : 4;
+}
 
 }  // namespace syn

@@ -1,24 +1,28 @@
-// kernel_ag.cu -- instantiations of the fused chunk-scheduled kernel for
-// the AG-GEMM operator (128x256 and 128x128 tiles).
+// kernel_ag.cu -- compiled instances of the fused chunk-scheduled kernel
+// for the AG-GEMM operator (every tile width / pipeline depth / peer-path
+// combination that dispatch_cfg lists).
 #include "fused.cuh"
 
 namespace syn {
 
-cudaError_t launch_fused_ag(const KernelParams &p, const TensorMaps &tm, int tile_n, int grid,
+cudaError_t launch_fused_ag(const KernelParams &p, const TensorMaps &tm, const LaunchCfg &lc,
                             cudaStream_t st) {
-    if (tile_n == 256) return launch_fused_t<OP_AG, 256>(p, tm, grid, st);
-    if (tile_n == 128) return launch_fused_t<OP_AG, 128>(p, tm, grid, st);
-    return cudaErrorInvalidValue;
+    return launch_op<OP_AG>(p, tm, lc, st);
 }
+
+int smem_bytes_ag(const LaunchCfg &lc) { return smem_bytes_op<OP_AG>(lc); }
 
 }  // namespace syn
 
 namespace syn {
 
-int fused_smem_bytes(int op, int tile_n) {
-    if (op == OP_AG) return tile_n == 256 ? KCfg<OP_AG, 256>::SMEM_ALLOC : KCfg<OP_AG, 128>::SMEM_ALLOC;
-    if (op == OP_RS) return tile_n == 256 ? KCfg<OP_RS, 256>::SMEM_ALLOC : KCfg<OP_RS, 128>::SMEM_ALLOC;
-    return tile_n == 256 ? KCfg<OP_AR, 256>::SMEM_ALLOC : KCfg<OP_AR, 128>::SMEM_ALLOC;
+int smem_bytes_rs(const LaunchCfg &lc);
+int smem_bytes_ar(const LaunchCfg &lc);
+
+int fused_smem_bytes(int op, const LaunchCfg &lc) {
+    if (op == OP_AG) return smem_bytes_ag(lc);
+    if (op == OP_RS) return smem_bytes_rs(lc);
+    return smem_bytes_ar(lc);
 }
 
 }  // namespace syn

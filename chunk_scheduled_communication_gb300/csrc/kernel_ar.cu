@@ -1,14 +1,15 @@
-// kernel_ar.cu -- instantiations of the fused chunk-scheduled kernel for
-// the GEMM-AR operator (128x256 and 128x128 tiles).
+// kernel_ar.cu -- compiled instances of the fused chunk-scheduled kernel
+// for the GEMM-AR operator (every tile width / pipeline depth / peer-path
+// combination that dispatch_cfg lists).
 #include "fused.cuh"
 
 namespace syn {
 
-cudaError_t launch_fused_ar(const KernelParams &p, const TensorMaps &tm, int tile_n, int grid,
+cudaError_t launch_fused_ar(const KernelParams &p, const TensorMaps &tm, const LaunchCfg &lc,
                             cudaStream_t st) {
-    if (tile_n == 256) return launch_fused_t<OP_AR, 256>(p, tm, grid, st);
-    if (tile_n == 128) return launch_fused_t<OP_AR, 128>(p, tm, grid, st);
-    return cudaErrorInvalidValue;
+    return launch_op<OP_AR>(p, tm, lc, st);
 }
+
+int smem_bytes_ar(const LaunchCfg &lc) { return smem_bytes_op<OP_AR>(lc); }
 
 }  // namespace syn

@@ -2,8 +2,9 @@
 //
 // Chunks (Syncopate summary page, method ¶1, paper §5.1): a chunk is a block
 // of rows of a logical tensor holding one or more compute tiles.  Here every
-// operator's row space [0, M) is cut into row chunks of `cr` rows; rank q owns
-// row chunks [q*split, (q+1)*split).  A staging transfer is (row chunk rc,
+// operator's row space [0, M) is cut into row chunks: each rank's block of
+// M_r rows into `split` chunks of ceil or floor(M_r/split) rows (chunk_row0 in
+// schedule.h); rank q owns row chunks [q*split, (q+1)*split).  A staging transfer is (row chunk rc,
 // source rank q): the rows of rc held by rank q that the local rank needs.
 //
 //   AG-GEMM : transfer (rc, q = rc / split) copies shard q's rows into the
@@ -83,8 +84,8 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         }
         split = (int)(M_r / chunk_rows);
     }
-    if (M_r % split != 0) {
-        err = "split must divide M/R";
+    if (split > M_r) {
+        err = "split must not exceed M/R";
         return SYN_ERR_INVALID;
     }
     const int tile_m = kn.tile_m == 0 ? kTileM : kn.tile_m;
@@ -123,7 +124,7 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
     s.K = L.K;
     s.M_r = M_r;
     s.split = split;
-    s.cr = M_r / split;
+    s.cr = (M_r + split - 1) / split;
     s.order = order;
     s.group_m = kn.group_m > 0 ? kn.group_m : 8;
     s.tile_m = tile_m;
@@ -131,7 +132,7 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
     s.tiles_m = (int)((L.M + tile_m - 1) / tile_m);
     s.tiles_n = (int)(L.N / tile_n);
     s.n_tiles = s.tiles_m * s.tiles_n;
-    s.n_rc = (int)(L.M / s.cr);
+    s.n_rc = R * split;
 
     // ---- staging transfers in arrival order -----------------------------
     s.arrival.assign((size_t)s.n_rc * R, -1);
@@ -144,7 +145,8 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
             const int q = (rank + d) % R;
             for (int j = 0; j < split; ++j) add(q * split + j, q);
         }
-    } else {
+    } else if (kn.backend != SYN_BACKEND_TMA_COLOCATED_SMEM) {
+        // (TMA_COLOCATED_SMEM fetches resident peer partials per tile: no transfers)
         const int nblocks = (op == SYN_OP_GEMM_RS) ? 1 : R;  // RS: only the local block
         for (int db = 0; db < nblocks; ++db) {
             const int b = (rank + db) % R;
@@ -168,8 +170,11 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         const int block = (int)(((int64_t)tm * tile_m) / M_r);
         if (op == SYN_OP_GEMM_RS && block != rank) {
             // send tile: produces chunk(s) for rank `block`; ring order
-            const int j = (int)((((int64_t)tm * tile_m) % M_r) / s.cr);
+            const int j = chunk_of_row(M_r, split, (int64_t)tm * tile_m) - block * split;
             key = (ring_pos(block, rank, R) - 1) * split + j - (R - 1) * split;
+        } else if (op == SYN_OP_GEMM_RS && kn.backend == SYN_BACKEND_TMA_COLOCATED_SMEM) {
+            // the peers' rows_r are resident from the start: reduce tiles first
+            key = -(R - 1) * split - 1;
         } else {
             for (int rc = lo; rc <= hi; ++rc)
                 for (int q = 0; q < R; ++q) {

@@ -15,6 +15,12 @@
 
 #include "syn.h"
 
+#if defined(__CUDACC__)
+#define SYN_SCHED_HD __host__ __device__ __forceinline__
+#else
+#define SYN_SCHED_HD inline
+#endif
+
 namespace syn {
 
 constexpr int kTileM = 128;
@@ -24,7 +30,7 @@ constexpr int kMaxRanks = 8;
 struct Schedule {
     int op = 0, R = 1, rank = 0;
     int64_t M = 0, N = 0, K = 0, M_r = 0;
-    int64_t cr = 0;      // chunk rows
+    int64_t cr = 0;      // rows of the largest chunk, ceil(M_r / split)
     int split = 1;       // chunks per rank row block
     int order = 0, group_m = 8;
     int tile_m = kTileM, tile_n = 256;
@@ -41,13 +47,26 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &layout,
                    int64_t chunk_rows, int split, syn_order_t order,
                    const syn_knobs_t &knobs, Schedule &s, std::string &err);
 
+// Chunk geometry.  Rank q's block of M_r rows is cut into `split` chunks;
+// chunk j of the block covers local rows [ceil(j*M_r/split), ceil((j+1)*M_r/split)),
+// so chunk sizes differ by at most one row when split does not divide M_r.
+// Row chunk rc = q*split + j.
+SYN_SCHED_HD int64_t chunk_row0(int64_t M_r, int split, int rc) {
+    const int q = rc / split, j = rc - q * split;
+    return (int64_t)q * M_r + ((int64_t)j * M_r + split - 1) / split;
+}
+SYN_SCHED_HD int chunk_of_row(int64_t M_r, int split, int64_t row) {
+    const int64_t q = row / M_r, rr = row - q * M_r;
+    return (int)(q * split + (rr * split) / M_r);
+}
+
 // Row-chunk range [lo, hi] covered by tile row tm (rows clipped to M).
 inline void tile_row_chunks(const Schedule &s, int tm, int &lo, int &hi) {
     int64_t r0 = (int64_t)tm * s.tile_m;
     int64_t r1 = r0 + s.tile_m;
     if (r1 > s.M) r1 = s.M;
-    lo = (int)(r0 / s.cr);
-    hi = (int)((r1 - 1) / s.cr);
+    lo = chunk_of_row(s.M_r, s.split, r0);
+    hi = chunk_of_row(s.M_r, s.split, r1 - 1);
 }
 
 }  // namespace syn

@@ -119,15 +119,20 @@ typedef struct {
                               (-1 = off); the call then ends in SYN_ERR_TIMEOUT */
     int trace;             /* 1 = accumulate flag-wait and CTA-busy nanoseconds
                               (read with syn_plan_stats)                        */
+    int stages;            /* GEMM shared-memory pipeline depth (0 = default:
+                              AG 4 / RS, AR 3 at tile_n 256; 6 / 4 at 128).
+                              With TMA_COLOCATED_SMEM the peer-tile ring gets
+                              the shared memory the stages leave: tile_n 256
+                              takes 2, 3 or 4; tile_n 128 takes 3, 4 or 6.   */
 } syn_knobs_t;
 
 /* Everything a caller or a test may want to know about a plan. */
 typedef struct {
     int op, R, rank, backend, order;
     int64_t M, N, K, M_r;
-    int64_t chunk_rows;    /* rows per chunk                                    */
+    int64_t chunk_rows;    /* rows of the largest chunk, ceil((M/R) / split)    */
     int split;             /* chunks per rank row block                         */
-    int n_row_chunks;      /* chunks over the whole row space = M / chunk_rows  */
+    int n_row_chunks;      /* chunks over the whole row space = R * split       */
     int n_transfers;       /* staging transfers (row chunk, source rank)        */
     int tile_m, tile_n, tiles_m, tiles_n, n_tiles;
     int grid_compute;      /* GEMM CTAs (0 before a device plan exists)          */
@@ -164,7 +169,10 @@ int syn_knobs_default(syn_knobs_t *knobs);
  * allocates and uploads flags, counters, tables and (for backends that stage
  * through global memory in GEMM-RS/AR) the receive buffer.
  * chunk_rows and split: chunks per rank row block; give either (the other 0)
- * or both with chunk_rows * split == M/R; both 0 means split = 1.
+ * or both with chunk_rows * split == M/R; both 0 means split = 1.  A split
+ * that does not divide M/R (1 <= split <= M/R) cuts each rank block into
+ * chunks of floor or ceil((M/R)/split) rows: chunk j holds local rows
+ * [ceil(j*(M/R)/split), ceil((j+1)*(M/R)/split)).
  * knobs may be NULL (defaults).  On success *out owns device memory. */
 int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank,
                     const syn_layout_t *layout, int64_t chunk_rows, int split,

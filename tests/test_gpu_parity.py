@@ -259,3 +259,31 @@ def test_autotune_small_budget(tmp_path, monkeypatch):
     assert best["backend"] in syn.BACKENDS and best["us"] > 0
     again = syn.autotune("ag", 4, 0, 4 * 256, 512, 512, budget_s=5.0)  # cache hit
     assert again["backend"] == best["backend"] and again["split"] == best["split"]
+
+
+# ----------------------------------------------------------------------------- pipeline depths
+INT_RS_SMALL = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=4 * 128, K=192, N=512, R=4)
+
+
+@pytest.mark.parametrize("w", [INT_RS_SMALL, INT_AR_N512], ids=["rs", "ar"])
+@pytest.mark.parametrize("tile_n,stages", [(256, 2), (256, 3), (256, 4), (128, 3), (128, 4), (128, 6)])
+def test_smem_peer_ring_depths_bit_exact(w, tile_n, stages):
+    """Every compiled (tile_n, stages) instance of the per-tile shared-memory
+    peer path gives the oracle's bits on integer inputs."""
+    inp = inputs(w, 1, 0, "int")
+    d = runner.upload(inp)
+    with runner.make_plan(d, split=2, order="row", backend="tma_colocated_smem", tile_n=tile_n,
+                          stages=stages) as plan:
+        runner.call(plan, d)
+        runner.call(plan, d)
+        assert plan.sync() == syn.OK
+    got = {"out": runner.dev_to_u16(d.out), "f32": d.f32_out.cpu().numpy()}
+    check_against_oracle(w, 1, got, kind="int")
+
+
+def test_uncompiled_stage_count_is_rejected():
+    inp = inputs(INT_AR_N512, 0, 0, "int")
+    d = runner.upload(inp)
+    with pytest.raises(syn.SynError) as e:
+        runner.make_plan(d, backend="tma_colocated_smem", tile_n=256, stages=5)
+    assert e.value.status == syn.ERR_UNSUPPORTED

@@ -33,11 +33,24 @@ def expected_transfers(op, R, r, split):
     return out
 
 
-def deps(op, R, r, M, M_r, cr, tm, tile_m=128):
+def chunk_bounds(M_r, split):
+    """Local row boundaries of the split chunks of one rank block: chunk j is
+    [ceil(j*M_r/split), ceil((j+1)*M_r/split)) -- written with integer ceil."""
+    return [-(-j * M_r // split) for j in range(split + 1)]
+
+
+def chunk_of(row, M_r, split):
+    q, rr = divmod(row, M_r)
+    b = chunk_bounds(M_r, split)
+    j = max(k for k in range(split) if b[k] <= rr)
+    return q * split + j
+
+
+def deps(op, R, r, M, M_r, split, tm, tile_m=128):
     rows = range(tm * tile_m, min((tm + 1) * tile_m, M))
-    rcs = sorted({i // cr for i in rows})
+    rcs = sorted({chunk_of(i, M_r, split) for i in rows})
     if op == "ag":
-        return [rc * R + rc // (M_r // cr) for rc in rcs]
+        return [rc * R + rc // split for rc in rcs]
     if op == "rs" and (tm * tile_m) // M_r != r:
         return []
     return [rc * R + q for rc in rcs for q in range(R) if q != r]
@@ -49,10 +62,15 @@ CASES = [
     ("ag", 8, 5, 8192, 1792, 4096, 4),
     ("ag", 3, 2, 600, 512, 192, 1),     # ragged M tail, chunk rows 200
     ("ag", 8, 3, 16384, 3584, 8192, 8),
+    ("ag", 8, 0, 16384, 3584, 8192, 3),   # split does not divide M/R: uneven chunks
+    ("ag", 8, 6, 16384, 3584, 8192, 7),
+    ("ag", 4, 2, 4 * 100, 256, 128, 3),   # 34/33/33-row chunks straddling tiles
+    ("ar", 8, 5, 4096, 3584, 2368, 3),
     ("ag", 8, 7, 128, 256, 128, 1),     # 8 chunks inside one tile
     ("rs", 8, 0, 8192, 4096, 1792, 1),
     ("rs", 8, 6, 8192, 4096, 1792, 4),
     ("rs", 4, 1, 1024, 256, 320, 2),
+    ("rs", 8, 2, 8192, 4096, 1792, 3),
     ("ar", 8, 0, 4096, 3584, 2368, 1),
     ("ar", 8, 4, 4096, 3584, 2368, 4),
     ("ar", 2, 1, 666, 384, 128, 1),
@@ -65,9 +83,8 @@ def test_schedule_properties(op, R, r, M, N, K, split, order):
     tile_n = 256 if N % 256 == 0 else 128
     info, tl, tk, tr = syn.schedule_build(op, R, r, M, N, K, split=split, order=order, tile_n=tile_n)
     M_r = M // R
-    cr = M_r // split
     tiles_m, tiles_n = -(-M // 128), N // tile_n
-    assert info["chunk_rows"] == cr and info["n_row_chunks"] == M // cr
+    assert info["chunk_rows"] == -(-M_r // split) and info["n_row_chunks"] == R * split
     assert info["n_tiles"] == tiles_m * tiles_n
     # the tile list is a permutation of all tiles
     assert sorted(tl.tolist()) == list(range(tiles_m * tiles_n))
@@ -78,13 +95,13 @@ def test_schedule_properties(op, R, r, M, N, K, split, order):
     # RS send tiles (consume nothing) are negative and come in ring order
     for t, key in zip(tl.tolist(), tk.tolist()):
         tm = t // tiles_n
-        d = deps(op, R, r, M, M_r, cr, tm)
+        d = deps(op, R, r, M, M_r, split, tm)
         if d:
             assert key == max(arrival[c] for c in d), (t, key, d)
         else:
             assert op == "rs" and key < 0
             block = (tm * 128) // M_r
-            j = ((tm * 128) % M_r) // cr
+            j = chunk_of(tm * 128, M_r, split) - block * split
             assert key == (((block - r) % R) - 1) * split + j - (R - 1) * split
     # the list is sorted by key (chunks walked in arrival order)
     assert (np.diff(tk) >= 0).all()
@@ -105,7 +122,7 @@ def test_tiny_each_tile_depends_on_two_chunks():
     info, tl, tk, tr = syn.schedule_build("ag", 4, 0, 256, 256, 256, split=1)
     assert info["n_tiles"] == 2 and info["chunk_rows"] == 64
     for tm in range(2):
-        assert len(deps("ag", 4, 0, 256, 64, 64, tm)) == 2
+        assert len(deps("ag", 4, 0, 256, 64, 1, tm)) == 2
 
 
 def test_rs_send_tiles_first_reduce_tiles_last():
@@ -128,7 +145,7 @@ def test_rs_send_tiles_first_reduce_tiles_last():
     (dict(op="ag", R=4, rank=0, M=256, N=200, K=256), syn.ERR_UNSUPPORTED),  # N % tile_n
     (dict(op="ag", R=16, rank=0, M=256, N=256, K=256), syn.ERR_UNSUPPORTED),  # R > 8
     (dict(op="rs", R=4, rank=0, M=4 * 96, N=256, K=256), syn.ERR_UNSUPPORTED),  # M_r % 128
-    (dict(op="ag", R=4, rank=0, M=256, N=256, K=256, split=3), syn.ERR_INVALID),  # split ∤ M_r
+    (dict(op="ag", R=4, rank=0, M=256, N=256, K=256, split=65), syn.ERR_INVALID),  # split > M_r
     (dict(op="ag", R=4, rank=0, M=256, N=256, K=256, chunk_rows=32, split=4), syn.ERR_INVALID),
 ])
 def test_invalid_shapes_rejected(kw, status):
@@ -144,3 +161,20 @@ def test_chunk_rows_and_split_agree():
     b = syn.schedule_build("ag", 8, 0, 8192, 1792, 4096, chunk_rows=0, split=4)
     assert a[0]["split"] == b[0]["split"] == 4
     assert (a[1] == b[1]).all() and (a[3] == b[3]).all()
+
+
+def test_smem_peer_backend_has_no_transfers_and_reduce_tiles_first():
+    """TMA_COLOCATED_SMEM fetches the resident peer partials tile by tile: there
+    is nothing to stage, every peer chunk is available at t = 0, so GEMM-RS
+    reduce tiles (which read peers) come first and GEMM-AR keeps pure traversal
+    order."""
+    info, tl, tk, tr = syn.schedule_build("rs", 8, 3, 8192, 4096, 1792, split=2, order="row",
+                                          backend="tma_colocated_smem")
+    assert info["n_transfers"] == 0 and len(tr) == 0
+    tiles_n = 4096 // 256
+    blocks = [(t // tiles_n) * 128 // 1024 for t in tl]
+    n_local = (1024 // 128) * tiles_n
+    assert all(b == 3 for b in blocks[:n_local]) and all(b != 3 for b in blocks[n_local:])
+    info, tl, tk, tr = syn.schedule_build("ar", 8, 3, 4096, 3584, 2368, split=1, order="row",
+                                          backend="tma_colocated_smem")
+    assert info["n_transfers"] == 0 and tl.tolist() == list(range(info["n_tiles"]))
