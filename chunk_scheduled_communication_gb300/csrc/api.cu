@@ -102,6 +102,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+void syn::set_last_error(const std::string &msg) { g_err = msg; }
+
 struct syn_plan_s {
     Schedule s;
     syn_knobs_t kn;

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cstdint>
+#include <string>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -117,5 +118,8 @@ inline int default_stages(int op, int tile_n) {
     if (op == OP_AG) return tile_n == 256 ? 4 : 6;
     return tile_n == 256 ? 3 : 4;
 }
+
+// Record the message syn_last_error() returns on this thread.
+void set_last_error(const std::string &msg);
 
 }  // namespace syn

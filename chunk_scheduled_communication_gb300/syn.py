@@ -81,6 +81,8 @@ _SIGS = {
                                     ctypes.c_double, ctypes.POINTER(Knobs), ctypes.POINTER(ctypes.c_int),
                                     ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]),
     "syn_device_sms": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
+    "syn_ag_gemm_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.POINTER(Layout), ctypes.c_int,
+                                           ctypes.c_int, _P, _P, _P, _P, _P, _P]),
     "syn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "syn_last_error": (ctypes.c_char_p, []),
 }
@@ -260,6 +262,15 @@ def autotune(op, R, rank, M, N, K, budget_s=60.0):
                           ctypes.byref(order), ctypes.byref(us)), "syn_autotune")
     return {"backend": BACKEND_NAMES.get(kn.backend, kn.backend), "comm_sms": kn.comm_sms, "tile_n": kn.tile_n,
             "group_m": kn.group_m, "split": split.value, "order": order.value, "us": us.value}
+
+
+def ag_gemm_noalloc(R, rank, M, N, K, shards, gathered, B, C, split=1, order="row", status=None,
+                    stream=None):
+    """AG-GEMM through syn_ag_gemm_noalloc (no device allocation; see include/syn.h)."""
+    lay = Layout(M, N, K, 0, 0, 0)
+    arr = (_P * R)(*[_ptr(s) for s in shards])
+    _check(lib().syn_ag_gemm_noalloc(R, rank, ctypes.byref(lay), split, _order(order), arr, _ptr(gathered),
+                                     _ptr(B), _ptr(C), _ptr(status), _stream(stream)), "syn_ag_gemm_noalloc")
 
 
 def device_sms() -> int:

@@ -253,6 +253,38 @@ int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *layout,
                  double budget_s, syn_knobs_t *best, int *best_split,
                  syn_order_t *best_order, double *best_us);
 
+/* ---- AG-GEMM without any device allocation ------------------------------
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory: plug-in hosts (inference-server
+ * backends, framework custom ops under a caching allocator) that give an
+ * operator only its input and output tensors, and serving loops that forbid
+ * cudaMalloc/cudaFree after start-up because those calls can synchronise the
+ * device and can fail mid-step.  syn_plan_create allocates; this does not.
+ *
+ * Same operation and arguments as syn_ag_gemm (co-located TMA staging, tile
+ * order `order`, `split` chunks per shard), without a plan.  Its scratch (tile
+ * and transfer lists, ready flags, counters, error word) lives in one static
+ * device array of SYN_NOALLOC_SCRATCH_BYTES that every GPU loading libsyn
+ * keeps until the process exits.  The first call on a device looks up that
+ * array's address (cudaGetSymbolAddress) with the device current; make that
+ * first call before any stream capture.  Shapes beyond SYN_NOALLOC_MAX_TILES
+ * output tiles (128 x tile_n, tile_n = 256 if N % 256 == 0 else 128) or
+ * SYN_NOALLOC_MAX_ROW_CHUNKS chunks return SYN_ERR_UNSUPPORTED with a
+ * message in syn_last_error().  No cudaMalloc, cudaFree or allocating library
+ * routine is called.  Every call clears the flags, counters and error word it
+ * needs, but all calls on a device share the one array: calls that overlap on
+ * the GPU (other streams, other host threads) race and give undefined results.
+ *   status_dev : nullable device int32[4]; receives {code, site, CTA, info} of
+ *                this call's device error word (code 0 = no error) once the
+ *                call completes on `stream`
+ * Returns after enqueuing on `stream` (SYN_OK) or a SYN_ERR_* host error. */
+#define SYN_NOALLOC_MAX_TILES 4096
+#define SYN_NOALLOC_MAX_ROW_CHUNKS 64
+#define SYN_NOALLOC_SCRATCH_BYTES 32768
+int syn_ag_gemm_noalloc(int R, int rank, const syn_layout_t *layout, int split,
+                        syn_order_t order, const void *const *shards, void *gathered,
+                        const void *B, void *C, int32_t *status_dev, void *stream);
+
 /* Number of SMs of the current device (0 and SYN_ERR_CUDA without a GPU). */
 int syn_device_sms(int *num_sms);
 
