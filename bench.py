@@ -48,7 +48,7 @@ STEP = [wl.LLAMA3_8B_UP_AG, wl.LLAMA3_8B_DOWN_RS, wl.QWEN2_7B_DOWN_AR]
 DEFAULT_KNOBS = {
     "ag": dict(backend="tma_colocated", split=4, order="row", tile_n=256, comm_sms=8, stages=0),
     "rs": dict(backend="tma_colocated_smem", split=1, order="row", tile_n=256, comm_sms=8, stages=3),
-    "ar": dict(backend="tma_colocated_smem", split=1, order="row", tile_n=256, comm_sms=8, stages=2),
+    "ar": dict(backend="tma_colocated_smem", split=1, order="row", tile_n=256, comm_sms=8, stages=3),
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -255,6 +255,9 @@ def main():
                     help="fraction of each operator's rows the CPU oracle baseline computes")
     ap.add_argument("--no-baselines", action="store_true")
     ap.add_argument("--knobs", default="", help="JSON overriding the per-operator knobs")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the step: the Llama-3-70B AG-GEMM sweep (splits 1-8, tile order, "
+                         "backend, comm SMs), one JSON line per point")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -262,6 +265,8 @@ def main():
     dist, rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         return run_reference(args, dist, rank)
+    if args.sweep:
+        return run_sweep(args)
 
     import torch
 
@@ -396,6 +401,7 @@ def main():
                 kn = dict(knobs[w.op])
                 split, order = kn.pop("split"), kn.pop("order")
                 kn["backend"] = be
+                kn["stages"] = 0  # the default depth of the baseline kernel instance
                 with runner.make_plan(d, split=split, order=order, **kn) as bp:
                     for _ in range(5):
                         runner.call(bp, d, stream)
@@ -438,6 +444,52 @@ def main():
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+    return 0
+
+
+def run_sweep(args):
+    """The pages' tuning-space study on the Llama-3-70B FFN up-projection AG-GEMM
+    (Syncopate summary, §6.3, Fig. 11): chunk splits 1-8 x tile order x staging
+    backend x communication SMs, each point timed with CUDA events (median of
+    --steps calls after --warmup), next to the unfused baseline."""
+    import torch
+
+    from chunk_scheduled_communication_gb300 import runner, syn
+
+    torch.cuda.set_device(0)
+    syn.lib()
+    peaks, peak_src = load_peaks()
+    w = wl.LLAMA3_70B_UP_AG
+    d = runner.upload(wl.make_inputs(w, r=0, seed=0))
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 20))
+    points = [dict(backend="unfused", split=1, order="row")]
+    for split in range(1, 9):
+        for order in ("row", "grouped", "col"):
+            points.append(dict(backend="ce", split=split, order=order))
+            points.append(dict(backend="tma_colocated", split=split, order=order))
+        for cs in (4, 8, 16):
+            points.append(dict(backend="tma_dedicated", split=split, order="row", comm_sms=cs))
+    for pt in points:
+        kn = dict(pt)
+        split, order = kn.pop("split"), kn.pop("order")
+        with runner.make_plan(d, split=split, order=order, **kn) as plan:
+            for _ in range(args.warmup):
+                runner.call(plan, d, stream)
+            plan.check(stream)
+            times = []
+            for _ in range(steps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                runner.call(plan, d, stream)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            plan.check(stream)
+        us = statistics.median(times) * 1e3
+        t_roof = max(w.flops / (peaks["bf16_tflops"] * 1e12), algorithmic_bytes(w) / (peaks["hbm_gbs"] * 1e9))
+        print(json.dumps({"sweep": w.name, **pt, "us": us, "tflops": w.flops / us / 1e6,
+                          "roofline_frac": t_roof / (us * 1e-6), "peak_source": peak_src}), flush=True)
     return 0
 
 

@@ -84,16 +84,17 @@ uint64_t env_timeout_ns() {
     return 2000000000ull;
 }
 
-// 2-D tiled tensor map over a row-major matrix [rows, cols] with 128-byte swizzle.
+// 2-D tiled tensor map over a row-major matrix [rows, cols].
 int encode_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, uint64_t cols,
-              uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+              uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * (uint64_t)esize};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = p_encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(SYN_ERR_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)r));
     return SYN_OK;
 }
@@ -109,12 +110,13 @@ struct syn_plan_s {
     syn_knobs_t kn;
     int device = 0, num_sms = 0;
     int grid_compute = 0, grid_comm = 0, smem = 0;
-    LaunchCfg lc = {256, 4, false, 0};  // compiled kernel instance
+    LaunchCfg lc = {256, 64, 4, false, 0};  // compiled kernel instance
     uint32_t epoch = 0;
     // device state
     int32_t *d_tiles = nullptr, *d_transfers = nullptr, *d_err = nullptr;
     uint32_t *d_in_flags = nullptr, *d_in_cnt = nullptr, *d_out_flags = nullptr, *d_out_cnt = nullptr;
     unsigned long long *d_stats = nullptr;
+    unsigned long long *d_trace = nullptr;  // trace = 2: [n_tiles][4] stamps
     uint8_t *d_recv = nullptr;
     uint64_t recv_bytes = 0;
     int64_t recv_slot_rows = 0;
@@ -145,6 +147,7 @@ void free_plan(syn_plan_s *pl) {
     cudaFree(pl->d_out_flags);
     cudaFree(pl->d_out_cnt);
     cudaFree(pl->d_stats);
+    cudaFree(pl->d_trace);
     cudaFree(pl->d_recv);
     for (cudaEvent_t e : pl->ev_transfer) cudaEventDestroy(e);
     if (pl->ev_fork) cudaEventDestroy(pl->ev_fork);
@@ -222,17 +225,21 @@ KernelParams base_params(syn_plan_s *pl) {
     p.out_cnt = pl->d_out_cnt;
     p.err = pl->d_err;
     p.stats = pl->kn.trace ? pl->d_stats : nullptr;
-    p.b_lbo = 8192;
-    p.b_sbo = 1024;
-    p.idesc_xor = 0;
-    // Diagnostic variants of the B-operand layout (all address the same 32 KiB
-    // stage): 1 swaps the two byte offsets, 2 flips the B-major bit.
-    if (const char *dv = std::getenv("SYN_DEBUG_DESC")) {
-        const int v = std::atoi(dv);
-        if (v & 1) std::swap(p.b_lbo, p.b_sbo);
-        if (v & 2) p.idesc_xor = 1u << 16;
-    }
+    p.trace = pl->d_trace;
     return p;
+}
+
+// Operand tensor maps for the plan's kernel instance: A / gathered [M, K] in
+// boxes of tile_k x 128 rows (128-byte swizzle at tile_k 64, 64-byte at 32),
+// B [K, N] in boxes of 64 columns x tile_k rows (128-byte swizzle).
+int encode_operands(syn_plan_s *pl, const void *A, const void *B) {
+    const Schedule &s = pl->s;
+    const int tk = pl->lc.tile_k;
+    const CUtensorMapSwizzle a_swz = tk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    int rc = encode_2d(&pl->maps.a, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.K, s.M, tk, 128, a_swz);
+    if (rc != SYN_OK) return rc;
+    return encode_2d(&pl->maps.b, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.N, s.K, 64, tk,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int finish_params_for_staging(syn_plan_s *pl, KernelParams &p) {
@@ -361,6 +368,7 @@ int syn_knobs_default(syn_knobs_t *k) {
     k->debug_drop_chunk = -1;
     k->trace = 0;
     k->stages = 0;
+    k->tile_k = 0;
     return SYN_OK;
 }
 
@@ -427,12 +435,16 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
     PL_CK(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, pl->device));
     if (!coop) return bail(SYN_ERR_UNSUPPORTED, "device has no cooperative launch");
     pl->lc.tile_n = s.tile_n;
-    pl->lc.smem_peers = (kn.backend == SYN_BACKEND_TMA_COLOCATED_SMEM);
-    pl->lc.stages = kn.stages > 0 ? kn.stages : default_stages(s.op, s.tile_n);
+    pl->lc.tile_k = kn.tile_k == 0 ? 64 : kn.tile_k;
+    pl->lc.stg = (kn.backend == SYN_BACKEND_TMA_COLOCATED);
+    pl->lc.stages =
+        kn.stages > 0 ? kn.stages : default_stages(s.op, s.tile_n, pl->lc.tile_k, pl->lc.stg);
     pl->smem = fused_smem_bytes(s.op, pl->lc);
     if (pl->smem < 0)
-        return bail(SYN_ERR_UNSUPPORTED, "stages = " + std::to_string(pl->lc.stages) +
-                                             " is not compiled for this operator, tile_n and backend");
+        return bail(SYN_ERR_UNSUPPORTED,
+                    "no compiled kernel for tile_n " + std::to_string(pl->lc.tile_n) + ", tile_k " +
+                        std::to_string(pl->lc.tile_k) + ", stages " + std::to_string(pl->lc.stages) +
+                        " with this operator and backend");
     if (kn.backend == SYN_BACKEND_TMA_DEDICATED) {
         pl->grid_comm = kn.comm_sms;
         if (pl->grid_comm >= pl->num_sms) return bail(SYN_ERR_INVALID, "comm_sms >= SM count");
@@ -461,6 +473,10 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
     PL_CK(cudaMemset(pl->d_out_flags, 0, (size_t)s.n_rc * sizeof(uint32_t)));
     PL_CK(cudaMemset(pl->d_out_cnt, 0, 2 * (size_t)s.n_rc * sizeof(uint32_t)));
     PL_CK(cudaMemset(pl->d_stats, 0, 2 * sizeof(unsigned long long)));
+    if (kn.trace >= 2) {
+        PL_CK(cudaMalloc(&pl->d_trace, 4 * (size_t)s.n_tiles * sizeof(unsigned long long)));
+        PL_CK(cudaMemset(pl->d_trace, 0, 4 * (size_t)s.n_tiles * sizeof(unsigned long long)));
+    }
     if (staged_peers(pl)) {
         pl->recv_slot_rows = (s.op == SYN_OP_GEMM_RS) ? s.M_r : s.M;
         pl->recv_bytes = (uint64_t)(s.R - 1) * pl->recv_slot_rows * s.N * sizeof(float);
@@ -509,12 +525,7 @@ int syn_ag_gemm(syn_plan_t plan, const void *const *shards, void *gathered, cons
     // tensor maps (cached on the operand pointers)
     std::vector<const void *> key = {gathered, B};
     if (key != plan->map_key) {
-        if ((rc = encode_2d(&plan->maps.a, gathered, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.K, s.M, 64,
-                            128)) != SYN_OK)
-            return rc;
-        if ((rc = encode_2d(&plan->maps.b, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.N, s.K, 64, 64)) !=
-            SYN_OK)
-            return rc;
+        if ((rc = encode_operands(plan, gathered, B)) != SYN_OK) return rc;
         plan->map_key = key;
     }
     plan->epoch += 1;
@@ -549,12 +560,7 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
     if (!staged)
         for (int q = 0; q < s.R; ++q) key.push_back(q == s.rank ? nullptr : peers[q]);
     if (key != plan->map_key) {
-        if ((rc = encode_2d(&plan->maps.a, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.K, s.M, 64, 128)) !=
-            SYN_OK)
-            return rc;
-        if ((rc = encode_2d(&plan->maps.b, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.N, s.K, 64, 64)) !=
-            SYN_OK)
-            return rc;
+        if ((rc = encode_operands(plan, A, B)) != SYN_OK) return rc;
         for (int q = 0; q < s.R; ++q) {
             if (q == s.rank) continue;
             const void *base;
@@ -642,6 +648,15 @@ int syn_plan_flags(syn_plan_t plan, uint32_t *in_flags, uint32_t *out_flags) {
     if (out_flags)
         SYN_CK(cudaMemcpy(out_flags, plan->d_out_flags, (size_t)plan->s.n_rc * sizeof(uint32_t),
                           cudaMemcpyDeviceToHost));
+    return SYN_OK;
+}
+
+int syn_plan_trace(syn_plan_t plan, uint64_t *out) {
+    if (plan == nullptr || out == nullptr) return fail(SYN_ERR_INVALID, "null argument");
+    if (plan->d_trace == nullptr) return fail(SYN_ERR_INVALID, "plan was created without trace = 2");
+    SYN_CK(cudaDeviceSynchronize());
+    SYN_CK(cudaMemcpy(out, plan->d_trace, 4 * (size_t)plan->s.n_tiles * sizeof(uint64_t),
+                      cudaMemcpyDeviceToHost));
     return SYN_OK;
 }
 

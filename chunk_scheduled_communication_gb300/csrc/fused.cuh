@@ -22,8 +22,8 @@
 //   warp 6      RS/AR peer loader: waits on the peer chunks' flags, then TMA-
 //               loads 128 x 32 fp32 peer sub-tiles into a P-slot ring
 //   warp 7      co-located stager: copies this CTA's share of chunk slices with
-//               TMA bulk copies and publishes the chunk flags
-// CTAs with blockIdx.x >= G are dedicated staging CTAs (one thread copies).
+//               TMA bulk copies (double-buffered) and publishes the chunk flags
+// CTAs with blockIdx.x >= G are dedicated staging CTAs (7 single-buffer copier threads).
 //
 // Every wait is bounded (global timer) and ends in SYN_ERR_TIMEOUT written to
 // the plan's error word; the CTA then drains its own outstanding asynchronous
@@ -42,21 +42,27 @@ namespace syn {
 constexpr int kSmemRings = 224 * 1024;
 
 // Compile-time shape of one kernel instance: operator, tile width BN, GEMM
-// pipeline stages S, and whether RS/AR peers are fetched per tile straight
-// into shared memory (SMEMP: no co-located staging buffers, so the peer ring
-// takes the rest of the budget).
-template <int OP, int BN, int S_, bool SMEMP>
+// pipeline stages S, k-block depth BK (64: 128-byte A rows, 128-byte swizzle;
+// 32: 64-byte A rows, 64-byte swizzle, half-size stages so twice as many fit),
+// and whether the CTA carries the co-located staging buffers (STG).  For
+// RS/AR the peer-tile ring takes whatever shared memory is left.
+template <int OP, int BN, int S_, int BK_, bool STG>
 struct KCfg {
-    static constexpr int BM = 128, BK = 64, UK = 16;
+    static constexpr int BM = 128, BK = BK_, UK = 16;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BK * BN * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int S = S_;
     static constexpr int BN_ = BN;
-    static constexpr bool SMEMP_ = SMEMP;
+    static constexpr bool STG_ = STG;
+    // A (K-major): 8-row swizzle atoms of 8 * BK * 2 bytes
+    static constexpr uint32_t A_SBO = 8 * BK * 2;
+    static constexpr uint32_t A_SWZ = BK == 64 ? ptx::kSwizzle128B : ptx::kSwizzle64B;
+    // B (N-major): one TMA box of 64 columns x BK rows per 64 output columns
+    static constexpr uint32_t B_BOX_BYTES = BK * 128;
     static constexpr int PEER_COLS = 32;
     static constexpr int PEER_BYTES = BM * PEER_COLS * 4;
-    static constexpr int NSTG = SMEMP ? 0 : 2;
+    static constexpr int NSTG = STG ? 2 : 0;
     static constexpr int STG_BYTES = 16384;
     static constexpr int P =
         OP == OP_AG ? 0 : (kSmemRings - NSTG * STG_BYTES - S * STAGE_BYTES) / PEER_BYTES;
@@ -87,6 +93,7 @@ struct KCfg {
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(OFF_B % 1024 == 0 && OFF_PEER % 1024 == 0 && OFF_STG % 1024 == 0, "1 KiB atoms");
     static_assert(BN == 128 || BN == 256, "tile_n");
+    static_assert(BK == 64 || BK == 32, "tile_k");
     static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, true);
 };
 
@@ -311,10 +318,10 @@ __device__ __forceinline__ void count_produced(const KernelParams &p, int tm, in
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int OP, int BN, int S, bool SMEMP>
+template <int OP, int BN, int S, int BK, bool STG>
 __global__ void __launch_bounds__(256, 1)
     syn_fused_kernel(const __grid_constant__ KernelParams p, const __grid_constant__ TensorMaps tm) {
-    using C = KCfg<OP, BN, S, SMEMP>;
+    using C = KCfg<OP, BN, S, BK, STG>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -327,13 +334,19 @@ __global__ void __launch_bounds__(256, 1)
 
     // ---- dedicated staging CTA -------------------------------------------
     if ((int)blockIdx.x >= p.G) {
+        // COMM_NBUF independent copiers (threads 0..COMM_NBUF-1), each with its
+        // own 32 KiB buffer and barrier, so several bulk copies are in flight.
         if (threadIdx.x == 0) {
             *abort = 0;
             for (int b = 0; b < C::COMM_NBUF; ++b) ptx::mbar_init(bar0 + 8 * b, 1);
             ptx::fence_mbar_init();
             ptx::fence_proxy_async_smem();
-            stage_slices(p, (int)blockIdx.x - p.G, p.n_comm, sbase, C::COMM_NBUF, C::COMM_BUF_BYTES,
-                         bar0, abort);
+        }
+        __syncthreads();
+        if ((int)threadIdx.x < C::COMM_NBUF) {
+            const int c = (int)threadIdx.x;
+            stage_slices(p, ((int)blockIdx.x - p.G) * C::COMM_NBUF + c, p.n_comm * C::COMM_NBUF,
+                         sbase + c * C::COMM_BUF_BYTES, 1, C::COMM_BUF_BYTES, bar0 + 8 * c, abort);
         }
         return;
     }
@@ -411,7 +424,7 @@ __global__ void __launch_bounds__(256, 1)
                     ptx::tma_load_2d(sA + s * C::A_BYTES, &tm.a, full, kb * C::BK, tmi * C::BM);
 #pragma unroll
                     for (int i = 0; i < BN / 64; ++i)
-                        ptx::tma_load_2d(sB + s * C::B_BYTES + i * 8192, &tm.b, full,
+                        ptx::tma_load_2d(sB + s * C::B_BYTES + i * C::B_BOX_BYTES, &tm.b, full,
                                          tni * BN + i * 64, kb * C::BK);
                 }
             }
@@ -434,6 +447,7 @@ __global__ void __launch_bounds__(256, 1)
                 const uint32_t aph = (tc >> 1) & 1u;
                 if (!bwait(bar0 + 8 * (C::BAR_TEMPTY + acc), aph ^ 1u, abort, p)) break;
                 ptx::tc_fence_after();
+                if (p.trace != nullptr) p.trace[4 * t + 0] = ptx::globaltimer();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = (int)(it % C::S);
@@ -446,17 +460,20 @@ __global__ void __launch_bounds__(256, 1)
                     const uint32_t a0 = sA + s * C::A_BYTES, b0 = sB + s * C::B_BYTES;
 #pragma unroll
                     for (int k = 0; k < C::BK / C::UK; ++k) {
-                        // A: K-major, 128-byte swizzle; a 16-wide K slice is +32 bytes
-                        const uint64_t ad = ptx::sdesc_sw128(a0 + k * 32, 16, 1024);
-                        // B: N-major, 128-byte swizzle; LBO = next 64-column block,
+                        // A: K-major, 128- or 64-byte swizzle (BK 64 / 32); SBO = next
+                        // 8-row atom; a 16-wide K slice is +32 bytes inside the row
+                        const uint64_t ad = ptx::sdesc(a0 + k * 32, 16, C::A_SBO, C::A_SWZ);
+                        // B: N-major, 128-byte swizzle; LBO = next 64-column box,
                         // SBO = next 8 K-rows; a 16-deep K slice is +16 rows of 128 B
-                        const uint64_t bd = ptx::sdesc_sw128(b0 + k * 2048, p.b_lbo, p.b_sbo);
-                        ptx::umma_bf16(d, ad, bd, C::IDESC ^ p.idesc_xor, (kb | k) != 0 ? 1u : 0u);
+                        const uint64_t bd =
+                            ptx::sdesc(b0 + k * 2048, C::B_BOX_BYTES, 1024, ptx::kSwizzle128B);
+                        ptx::umma_bf16(d, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
                     }
                     ptx::umma_commit(bar0 + 8 * (C::BAR_EMPTY + s));
                 }
                 if (!ok) break;
                 ptx::umma_commit(bar0 + 8 * (C::BAR_TFULL + acc));
+                if (p.trace != nullptr) p.trace[4 * t + 1] = ptx::globaltimer();
                 ++tc;
             }
             // every MMA this thread issued must finish before TMEM is released
@@ -477,6 +494,7 @@ __global__ void __launch_bounds__(256, 1)
             bool ok = bwait(bar0 + 8 * (C::BAR_TFULL + acc), aph, abort, p);
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
+            if (p.trace != nullptr && warp == 2 && lane == 0) p.trace[4 * t + 2] = ptx::globaltimer();
             const int row = tmi * C::BM + lrow;
             const bool in_range = row < p.M;
             const bool red = reduces<OP>(p, tmi);
@@ -534,6 +552,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar0 + 8 * (C::BAR_TEMPTY + acc));
+            if (p.trace != nullptr && warp == 2 && lane == 0) p.trace[4 * t + 3] = ptx::globaltimer();
             if (dead) break;
             if (OP != OP_AG && p.f32_out != nullptr && (OP == OP_AR || !red))
                 count_produced(p, tmi, lane);
@@ -588,6 +607,8 @@ __global__ void __launch_bounds__(256, 1)
     } else {
         // ================= co-located stager =================
         if constexpr (C::NSTG > 0)
+            // one copier per CTA, double-buffered: with one worker per GEMM CTA the
+            // first round of slices covers only the earliest chunks in arrival order
             if (p.colocated && lane == 0)
                 stage_slices(p, (int)blockIdx.x, p.G, sbase + C::OFF_STG, C::NSTG, C::STG_BYTES,
                              bar0 + 8 * C::BAR_STG, abort);
@@ -603,10 +624,10 @@ __global__ void __launch_bounds__(256, 1)
         atomicAdd(p.stats + 1, (unsigned long long)(ptx::globaltimer() - t_start));
 }
 
-template <int OP, int BN, int S, bool SMEMP>
+template <int OP, int BN, int S, int BK, bool STG>
 cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid, cudaStream_t st) {
-    using C = KCfg<OP, BN, S, SMEMP>;
-    cudaError_t e = cudaFuncSetAttribute(syn_fused_kernel<OP, BN, S, SMEMP>,
+    using C = KCfg<OP, BN, S, BK, STG>;
+    cudaError_t e = cudaFuncSetAttribute(syn_fused_kernel<OP, BN, S, BK, STG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -619,41 +640,40 @@ cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, syn_fused_kernel<OP, BN, S, SMEMP>, p, tm);
+    return cudaLaunchKernelEx(&cfg, syn_fused_kernel<OP, BN, S, BK, STG>, p, tm);
 }
 
-// Dispatch over the instantiated (tile_n, stages, smem-peer) combinations of
-// one operator.  `Fn` receives the KCfg type; returns false when the
-// combination is not instantiated.
+// Every compiled kernel instance, per operator: (tile_n, stages, tile_k, stg).
+// `Fn` receives the KCfg type; returns false when the combination is not
+// compiled.
 template <int OP, typename Fn>
-bool dispatch_cfg(int tile_n, int stages, bool smem_peers, Fn &&fn) {
+bool dispatch_cfg(const LaunchCfg &lc, Fn &&fn) {
+    const int tn = lc.tile_n, st = lc.stages, tk = lc.tile_k;
+    const bool g = lc.stg;
+#define SYN_CFG(TN, ST, TK, G) \
+    if (tn == TN && st == ST && tk == TK && g == G) return fn(KCfg<OP, TN, ST, TK, G>{}), true;
     if constexpr (OP == OP_AG) {
-        if (tile_n == 256 && stages == 4) return fn(KCfg<OP, 256, 4, false>{}), true;
-        if (tile_n == 128 && stages == 6) return fn(KCfg<OP, 128, 6, false>{}), true;
+        SYN_CFG(256, 4, 64, true) SYN_CFG(256, 4, 64, false)
+        SYN_CFG(128, 6, 64, true) SYN_CFG(128, 6, 64, false)
+        SYN_CFG(256, 8, 32, true) SYN_CFG(256, 9, 32, false)
         return false;
     } else {
-    if (!smem_peers) {
-        if (tile_n == 256 && stages == 3) return fn(KCfg<OP, 256, 3, false>{}), true;
-        if (tile_n == 128 && stages == 4) return fn(KCfg<OP, 128, 4, false>{}), true;
+        SYN_CFG(256, 3, 64, true) SYN_CFG(128, 4, 64, true) SYN_CFG(256, 6, 32, true)
+        SYN_CFG(256, 2, 64, false) SYN_CFG(256, 3, 64, false) SYN_CFG(256, 4, 64, false)
+        SYN_CFG(128, 3, 64, false) SYN_CFG(128, 4, 64, false) SYN_CFG(128, 6, 64, false)
+        SYN_CFG(256, 4, 32, false) SYN_CFG(256, 5, 32, false) SYN_CFG(256, 6, 32, false)
         return false;
     }
-    if (tile_n == 256 && stages == 2) return fn(KCfg<OP, 256, 2, true>{}), true;
-    if (tile_n == 256 && stages == 3) return fn(KCfg<OP, 256, 3, true>{}), true;
-    if (tile_n == 256 && stages == 4) return fn(KCfg<OP, 256, 4, true>{}), true;
-    if (tile_n == 128 && stages == 3) return fn(KCfg<OP, 128, 3, true>{}), true;
-    if (tile_n == 128 && stages == 4) return fn(KCfg<OP, 128, 4, true>{}), true;
-    if (tile_n == 128 && stages == 6) return fn(KCfg<OP, 128, 6, true>{}), true;
-    return false;
-    }
+#undef SYN_CFG
 }
 
 template <int OP>
 cudaError_t launch_op(const KernelParams &p, const TensorMaps &tm, const LaunchCfg &lc,
                       cudaStream_t st) {
     cudaError_t err = cudaErrorInvalidValue;
-    dispatch_cfg<OP>(lc.tile_n, lc.stages, lc.smem_peers, [&](auto c) {
+    dispatch_cfg<OP>(lc, [&](auto c) {
         using C = decltype(c);
-        err = launch_fused_t<OP, C::BN_, C::S, C::SMEMP_>(p, tm, lc.grid, st);
+        err = launch_fused_t<OP, C::BN_, C::S, C::BK, C::STG_>(p, tm, lc.grid, st);
     });
     return err;
 }
@@ -661,9 +681,7 @@ cudaError_t launch_op(const KernelParams &p, const TensorMaps &tm, const LaunchC
 template <int OP>
 int smem_bytes_op(const LaunchCfg &lc) {
     int bytes = -1;
-    dispatch_cfg<OP>(lc.tile_n, lc.stages, lc.smem_peers, [&](auto c) {
-        bytes = decltype(c)::SMEM_ALLOC;
-    });
+    dispatch_cfg<OP>(lc, [&](auto c) { bytes = decltype(c)::SMEM_ALLOC; });
     return bytes;
 }
 

@@ -61,14 +61,14 @@ struct KernelParams {
     uint32_t *out_cnt;             // [2][n_rc] producer counters (epoch parity)
     int32_t *err;                  // [4] code, site, cta, info
     unsigned long long *stats;     // [2] flag-wait ns, CTA-busy ns (nullable)
+    unsigned long long *trace;     // [n_tiles][4] per tile-list entry: MMA start, MMA end
+                                   // (last commit issued), epilogue start, end (nullable)
     const uint8_t *stage_src[kMaxRanks];  // AG: shard q; RS/AR: peer q partial
     uint8_t *stage_dst;            // AG: gathered; RS/AR: receive buffer
     int64_t row_bytes;             // bytes of one row of a transfer
     int64_t recv_slot_rows;        // RS/AR: rows per peer slot of the receive buffer
     uint16_t *out;                 // AG: C; RS: out_r; AR: out   (bf16)
     float *f32_out;                // RS: send; AR: publish  (nullable)
-    uint32_t b_lbo, b_sbo;         // B operand descriptor byte offsets (8192, 1024)
-    uint32_t idesc_xor;            // diagnostic only: bits flipped in the instruction descriptor
 };
 
 // Receive-buffer slot of source rank q (the local rank has none).
@@ -97,14 +97,15 @@ SYN_HD void transfer_span(const KernelParams &p, int code, const uint8_t *&src, 
 
 // Which compiled kernel instance a launch uses, and its grid.
 struct LaunchCfg {
-    int tile_n;       // 128 or 256
-    int stages;       // GEMM pipeline stages
-    bool smem_peers;  // RS/AR: peers fetched per tile into shared memory
-    int grid;         // CTAs
+    int tile_n;   // 128 or 256
+    int tile_k;   // k-block depth: 64 or 32
+    int stages;   // GEMM pipeline stages
+    bool stg;     // CTA carries the co-located staging buffers
+    int grid;     // CTAs
 };
 
 // Host launchers (one translation unit per operator).  cudaErrorInvalidValue
-// if (tile_n, stages, smem_peers) is not a compiled combination.
+// if (tile_n, tile_k, stages, stg) is not a compiled combination.
 cudaError_t launch_fused_ag(const KernelParams &p, const TensorMaps &tm, const LaunchCfg &lc,
                             cudaStream_t st);
 cudaError_t launch_fused_rs(const KernelParams &p, const TensorMaps &tm, const LaunchCfg &lc,
@@ -113,8 +114,9 @@ cudaError_t launch_fused_ar(const KernelParams &p, const TensorMaps &tm, const L
                             cudaStream_t st);
 // Dynamic shared memory of a combination (-1 if not compiled).
 int fused_smem_bytes(int op, const LaunchCfg &lc);
-// Default pipeline depth: AG 4 (tile_n 256) / 6 (128); RS/AR 3 / 4.
-inline int default_stages(int op, int tile_n) {
+// Default pipeline depth of a (tile_n, tile_k, stg) choice.
+inline int default_stages(int op, int tile_n, int tile_k, bool stg) {
+    if (tile_k == 32) return op == OP_AG ? (stg ? 8 : 9) : 6;
     if (op == OP_AG) return tile_n == 256 ? 4 : 6;
     return tile_n == 256 ? 3 : 4;
 }

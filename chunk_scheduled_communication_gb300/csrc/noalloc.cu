@@ -198,14 +198,12 @@ extern "C" int syn_ag_gemm_noalloc(int R, int rank, const syn_layout_t *layout, 
     p.slices_per_transfer = (int32_t)((tbytes + slice - 1) / slice);
     p.out = static_cast<uint16_t *>(C);
     p.f32_out = nullptr;
-    p.b_lbo = 8192;
-    p.b_sbo = 1024;
-    p.idesc_xor = 0;
 
     LaunchCfg lc;
     lc.tile_n = s.tile_n;
-    lc.stages = default_stages(OP_AG, s.tile_n);
-    lc.smem_peers = false;
+    lc.tile_k = 64;
+    lc.stg = true;
+    lc.stages = default_stages(OP_AG, s.tile_n, lc.tile_k, lc.stg);
     lc.grid = p.G;
     const cudaError_t le = launch_fused_ag(p, maps, lc, st);
     if (le != cudaSuccess) return fail(SYN_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(le));

@@ -166,17 +166,19 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor (tcgen05), 128-byte swizzle.
+// Shared-memory matrix descriptor (tcgen05).
 //   bits  0-13 start address >> 4
 //   bits 16-29 leading-dimension byte offset >> 4
 //   bits 32-45 stride-dimension byte offset >> 4
 //   bits 46-47 descriptor version (1 on this architecture)
-//   bits 49-51 base offset (0: atoms are 1024-byte aligned)
-//   bits 61-63 swizzle mode (2 = 128-byte swizzle)
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                uint32_t sbo_bytes) {
+//   bits 49-51 base offset (0: swizzle atoms are aligned)
+//   bits 61-63 swizzle mode (2 = 128-byte, 4 = 64-byte swizzle)
+constexpr uint32_t kSwizzle128B = 2, kSwizzle64B = 4;
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                          uint32_t swizzle_mode) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+           ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+           ((uint64_t)swizzle_mode << 61);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, dense:

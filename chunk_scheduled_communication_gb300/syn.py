@@ -40,7 +40,7 @@ class Knobs(ctypes.Structure):
     _fields_ = [("backend", ctypes.c_int), ("comm_sms", ctypes.c_int), ("tile_m", ctypes.c_int),
                 ("tile_n", ctypes.c_int), ("group_m", ctypes.c_int), ("slice_kb", ctypes.c_int),
                 ("timeout_ns", ctypes.c_uint64), ("debug_drop_chunk", ctypes.c_int),
-                ("trace", ctypes.c_int), ("stages", ctypes.c_int)]
+                ("trace", ctypes.c_int), ("stages", ctypes.c_int), ("tile_k", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -77,6 +77,7 @@ _SIGS = {
     "syn_plan_tables": (ctypes.c_int, [_P, _P, _P, _P]),
     "syn_plan_flags": (ctypes.c_int, [_P, _P, _P]),
     "syn_plan_stats": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
+    "syn_plan_trace": (ctypes.c_int, [_P, _P]),
     "syn_autotune": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Layout),
                                     ctypes.c_double, ctypes.POINTER(Knobs), ctypes.POINTER(ctypes.c_int),
                                     ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]),
@@ -121,12 +122,12 @@ def _check(status: int, where: str):
 
 
 def make_knobs(backend="ce", comm_sms=8, tile_n=256, group_m=8, slice_kb=128, timeout_ns=0,
-               drop_chunk=-1, trace=0, stages=0) -> Knobs:
+               drop_chunk=-1, trace=0, stages=0, tile_k=0) -> Knobs:
     k = Knobs()
     _check(lib().syn_knobs_default(ctypes.byref(k)), "syn_knobs_default")
     k.backend = BACKENDS[backend] if isinstance(backend, str) else int(backend)
     k.comm_sms, k.tile_n, k.group_m, k.slice_kb = comm_sms, tile_n, group_m, slice_kb
-    k.timeout_ns, k.debug_drop_chunk, k.trace, k.stages = timeout_ns, drop_chunk, trace, stages
+    k.timeout_ns, k.debug_drop_chunk, k.trace, k.stages, k.tile_k = timeout_ns, drop_chunk, trace, stages, tile_k
     return k
 
 
@@ -226,6 +227,15 @@ class Plan:
         a, b = ctypes.c_uint64(), ctypes.c_uint64()
         _check(self._L.syn_plan_stats(self._h, ctypes.byref(a), ctypes.byref(b)), "syn_plan_stats")
         return a.value, b.value
+
+    def trace(self):
+        """Per-tile timeline of the last call (trace=2): int64 [n_tiles, 4] of
+        (MMA start, MMA end, epilogue start, epilogue end) global-timer ns, rows
+        in tile-list order."""
+        n = self.info()["n_tiles"]
+        out = np.zeros((n, 4), np.uint64)
+        _check(self._L.syn_plan_trace(self._h, out.ctypes.data), "syn_plan_trace")
+        return out.astype(np.int64)
 
     # -- operators (asynchronous on `stream`)
     def ag_gemm(self, shards, gathered, B, C, stream=None):

@@ -118,12 +118,19 @@ typedef struct {
                               transfer whose ready flag is never published
                               (-1 = off); the call then ends in SYN_ERR_TIMEOUT */
     int trace;             /* 1 = accumulate flag-wait and CTA-busy nanoseconds
-                              (read with syn_plan_stats)                        */
+                              (read with syn_plan_stats); 2 = also record four
+                              global-timer stamps per tile of the last call
+                              (read with syn_plan_trace)                       */
     int stages;            /* GEMM shared-memory pipeline depth (0 = default:
                               AG 4 / RS, AR 3 at tile_n 256; 6 / 4 at 128).
                               With TMA_COLOCATED_SMEM the peer-tile ring gets
                               the shared memory the stages leave: tile_n 256
-                              takes 2, 3 or 4; tile_n 128 takes 3, 4 or 6.   */
+                              takes 2, 3 or 4; tile_n 128 takes 3, 4 or 6.
+                              At tile_k 32: AG 8 (co-located) / 9, RS and AR
+                              6 (co-located) or 4, 5, 6.                     */
+    int tile_k;            /* k-block depth per pipeline stage: 64 or 32
+                              (0 = 64).  32 halves each stage, so twice as
+                              many fit and more loads are in flight.         */
 } syn_knobs_t;
 
 /* Everything a caller or a test may want to know about a plan. */
@@ -240,6 +247,14 @@ int syn_plan_flags(syn_plan_t plan, uint32_t *in_flags, uint32_t *out_flags);
  * chunk-flag waits, and total nanoseconds they were resident, summed over CTAs
  * since the plan was created.  Synchronous. */
 int syn_plan_stats(syn_plan_t plan, uint64_t *flag_wait_ns, uint64_t *cta_busy_ns);
+
+/* Per-tile timeline of the plan's most recent call (knobs.trace = 2), as
+ * global-timer nanoseconds: for tile-list entry i, out[4i+0] = the MMA issuer
+ * starts the tile, out[4i+1] = its last MMA commit is issued, out[4i+2] = the
+ * epilogue sees the accumulator ready, out[4i+3] = the epilogue has released
+ * it.  out has 4 * n_tiles entries (host memory).  Synchronous.
+ * SYN_ERR_INVALID if the plan was created without trace = 2. */
+int syn_plan_trace(syn_plan_t plan, uint64_t *out);
 
 /* Enumerate-and-measure autotuner (summary page, method ¶4 and paper §6.3,
  * Fig. 11; Entwine's communication-SM balance).  Allocates its own scratch

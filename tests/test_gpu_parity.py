@@ -253,6 +253,25 @@ def test_trace_counters():
     assert busy_ns > 0 and 0 <= wait_ns <= busy_ns * 2
 
 
+def test_per_tile_trace_is_consistent():
+    """trace=2 stamps every tile: MMA start <= MMA end <= epilogue start <=
+    epilogue end, and each CTA's tiles run in list order."""
+    w = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=8 * 256, K=512, N=1024)
+    inp = inputs(w, 0)
+    d = runner.upload(inp)
+    with runner.make_plan(d, backend="tma_colocated_smem", trace=2, split=2) as plan:
+        runner.call(plan, d)
+        assert plan.sync() == syn.OK
+        tr = plan.trace()
+        G = plan.info()["grid_compute"]
+    assert (tr > 0).all()
+    assert (tr[:, 0] <= tr[:, 1]).all() and (tr[:, 2] <= tr[:, 3]).all()
+    assert (tr[:, 1] <= tr[:, 3]).all()
+    for c in range(G):
+        mine = tr[c::G, 0]
+        assert (np.diff(mine) >= 0).all()
+
+
 def test_autotune_small_budget(tmp_path, monkeypatch):
     monkeypatch.setenv("SYN_TUNE_CACHE", str(tmp_path / "tune.jsonl"))
     best = syn.autotune("ag", 4, 0, 4 * 256, 512, 512, budget_s=5.0)
@@ -279,6 +298,33 @@ def test_smem_peer_ring_depths_bit_exact(w, tile_n, stages):
         assert plan.sync() == syn.OK
     got = {"out": runner.dev_to_u16(d.out), "f32": d.f32_out.cpu().numpy()}
     check_against_oracle(w, 1, got, kind="int")
+
+
+@pytest.mark.parametrize("w,backend,stages", [
+    (INT_AG, "tma_colocated", 8), (INT_AG, "ce", 9), (INT_AG, "tma_dedicated", 9),
+    (INT_RS_SMALL, "tma_colocated_smem", 4), (INT_RS_SMALL, "tma_colocated_smem", 5),
+    (INT_RS_SMALL, "tma_colocated_smem", 6), (INT_RS_SMALL, "tma_colocated", 6), (INT_RS_SMALL, "ce", 6),
+    (INT_AR_N512, "tma_colocated_smem", 6), (INT_AR_N512, "tma_colocated", 6), (INT_AR_N512, "ce", 4),
+], ids=lambda v: str(getattr(v, "op", v)))
+def test_tile_k32_instances_bit_exact(w, backend, stages):
+    """k-blocks of 32 (64-byte swizzled A, half-size stages) give the oracle's
+    bits on integer inputs, for every compiled tile_k 32 instance."""
+    r = w.R - 1
+    got = run(w, r, backend=backend, kind="int", comm_sms=3, split=2)
+    inp = inputs(w, r, 0, "int")
+    d = runner.upload(inp)
+    with runner.make_plan(d, split=2, order="row", backend=backend, tile_n=256, tile_k=32,
+                          stages=stages, comm_sms=3) as plan:
+        runner.call(plan, d)
+        runner.call(plan, d)
+        assert plan.sync() == syn.OK
+    k32 = {"out": runner.dev_to_u16(d.out)}
+    if w.op == "ag":
+        k32["gathered"] = runner.dev_to_u16(d.gathered)
+    else:
+        k32["f32"] = d.f32_out.cpu().numpy()
+    check_against_oracle(w, r, k32, kind="int")
+    assert (k32["out"] == got["out"]).all()
 
 
 def test_uncompiled_stage_count_is_rejected():
