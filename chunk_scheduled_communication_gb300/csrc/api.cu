@@ -110,7 +110,8 @@ struct syn_plan_s {
     syn_knobs_t kn;
     int device = 0, num_sms = 0;
     int grid_compute = 0, grid_comm = 0, smem = 0;
-    LaunchCfg lc = {256, 64, 4, false, 0};  // compiled kernel instance
+    int resident = 0;                              // CTAs that fit on the device at once
+    LaunchCfg lc = {256, 64, 4, false, false, 0};  // compiled kernel instance
     uint32_t epoch = 0;
     // device state
     int32_t *d_tiles = nullptr, *d_transfers = nullptr, *d_err = nullptr;
@@ -330,7 +331,8 @@ int run(syn_plan_s *pl, KernelParams &p, cudaStream_t st) {
                 KernelParams q = p;
                 q.t_begin = pl->groups[g].first;
                 q.t_end = pl->groups[g].second;
-                const int grid = std::min(q.t_end - q.t_begin, pl->num_sms);
+                const int per = pl->lc.pair ? 2 : 1;
+                const int grid = std::min(q.t_end - q.t_begin, pl->resident / per) * per;
                 q.G = grid;
                 SYN_CK(launch(pl, q, grid, st));
             }
@@ -437,21 +439,31 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
     pl->lc.tile_n = s.tile_n;
     pl->lc.tile_k = kn.tile_k == 0 ? 64 : kn.tile_k;
     pl->lc.stg = (kn.backend == SYN_BACKEND_TMA_COLOCATED);
-    pl->lc.stages =
-        kn.stages > 0 ? kn.stages : default_stages(s.op, s.tile_n, pl->lc.tile_k, pl->lc.stg);
+    pl->lc.pair = (s.tile_m == 256);
+    pl->lc.stages = kn.stages > 0 ? kn.stages
+                                  : default_stages(s.op, s.tile_n, pl->lc.tile_k, pl->lc.stg, pl->lc.pair);
     pl->smem = fused_smem_bytes(s.op, pl->lc);
     if (pl->smem < 0)
         return bail(SYN_ERR_UNSUPPORTED,
-                    "no compiled kernel for tile_n " + std::to_string(pl->lc.tile_n) + ", tile_k " +
-                        std::to_string(pl->lc.tile_k) + ", stages " + std::to_string(pl->lc.stages) +
-                        " with this operator and backend");
+                    "no compiled kernel for tile_m " + std::to_string(s.tile_m) + ", tile_n " +
+                        std::to_string(pl->lc.tile_n) + ", tile_k " + std::to_string(pl->lc.tile_k) +
+                        ", stages " + std::to_string(pl->lc.stages) + " with this operator and backend");
+    // CTAs that can be resident at once: one per SM, or (CTA pairs) twice the
+    // co-resident 2-CTA clusters, which may be fewer than SMs / 2
+    pl->resident = pl->num_sms;
+    if (pl->lc.pair) {
+        const int nc = fused_max_clusters(s.op, pl->lc);
+        if (nc <= 0) return bail(SYN_ERR_UNSUPPORTED, "2-CTA clusters of this kernel cannot be resident");
+        pl->resident = std::min(pl->num_sms, 2 * nc);
+    }
+    const int cta_per_tile = pl->lc.pair ? 2 : 1;
     if (kn.backend == SYN_BACKEND_TMA_DEDICATED) {
-        pl->grid_comm = kn.comm_sms;
-        if (pl->grid_comm >= pl->num_sms) return bail(SYN_ERR_INVALID, "comm_sms >= SM count");
-        pl->grid_compute = std::min(s.n_tiles, pl->num_sms - pl->grid_comm);
+        pl->grid_comm = pl->lc.pair ? (kn.comm_sms + 1) / 2 * 2 : kn.comm_sms;
+        if (pl->grid_comm >= pl->resident) return bail(SYN_ERR_INVALID, "comm_sms >= resident CTAs");
+        pl->grid_compute = std::min(s.n_tiles, (pl->resident - pl->grid_comm) / cta_per_tile) * cta_per_tile;
     } else {
         pl->grid_comm = 0;
-        pl->grid_compute = std::min(s.n_tiles, pl->num_sms);
+        pl->grid_compute = std::min(s.n_tiles, pl->resident / cta_per_tile) * cta_per_tile;
     }
     const size_t n_flags = (size_t)s.n_rc * s.R;
     PL_CK(cudaMalloc(&pl->d_tiles, s.tile_list.size() * sizeof(int32_t)));

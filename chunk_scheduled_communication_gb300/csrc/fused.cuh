@@ -14,8 +14,8 @@
 // CTA is resident and flag waits between CTAs cannot deadlock):
 //   warp 0      TMA producer: waits on chunk flags (AG), then streams A/B
 //               tiles into an S-stage shared-memory ring (mbarrier tx counts)
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (128 x BN x 16
-//               bf16 UMMAs into a double-buffered fp32 TMEM accumulator)
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer into a
+//               double-buffered fp32 TMEM accumulator
 //   warps 2-5   epilogue: tcgen05.ld rows out of TMEM; AG: bf16 store;
 //               RS/AR: add the peer partial tiles (ascending rank), bf16 store,
 //               fp32 send/publish stores and producer counters
@@ -24,6 +24,18 @@
 //   warp 7      co-located stager: copies this CTA's share of chunk slices with
 //               TMA bulk copies (double-buffered) and publishes the chunk flags
 // CTAs with blockIdx.x >= G are dedicated staging CTAs (7 single-buffer copier threads).
+//
+// Two MMA shapes.  Single CTA: 128 x BN x 16 UMMAs (tcgen05 cta_group::1), each
+// CTA stages its A rows and all BN columns of B.  CTA pair (PAIR, 2-CTA
+// clusters): the even CTA issues 256 x BN x 16 UMMAs (cta_group::2) that read A
+// rows 0-127 and B columns 0..BN/2 from its own shared memory and A rows 128-255
+// and the other B columns from its peer's, and write each CTA's accumulator
+// rows into that CTA's TMEM.  Per SM this halves the B bytes staged and read
+// for the same MMA work, which is what lets the tensor pipe run near its peak
+// on this architecture.  The peer's TMA loads complete on the even CTA's ring
+// barrier; stage releases and accumulator-ready signals are forwarded to the
+// peer with remote mbarrier arrives, and the peer's epilogue releases the
+// accumulator the same way.  No multicast form is used.
 //
 // Every wait is bounded (global timer) and ends in SYN_ERR_TIMEOUT written to
 // the plan's error word; the CTA then drains its own outstanding asynchronous
@@ -44,21 +56,27 @@ constexpr int kSmemRings = 224 * 1024;
 // Compile-time shape of one kernel instance: operator, tile width BN, GEMM
 // pipeline stages S, k-block depth BK (64: 128-byte A rows, 128-byte swizzle;
 // 32: 64-byte A rows, 64-byte swizzle, half-size stages so twice as many fit),
-// and whether the CTA carries the co-located staging buffers (STG).  For
-// RS/AR the peer-tile ring takes whatever shared memory is left.
-template <int OP, int BN, int S_, int BK_, bool STG>
+// whether the CTA carries the co-located staging buffers (STG), and whether
+// CTA pairs share 256-row tiles (PAIR).  For RS/AR the peer-tile ring takes
+// whatever shared memory is left.
+template <int OP, int BN, int S_, int BK_, bool STG, bool PAIR>
 struct KCfg {
+    static constexpr int CTAS = PAIR ? 2 : 1;
     static constexpr int BM = 128, BK = BK_, UK = 16;
+    static constexpr int TILE_M = BM * CTAS;          // output rows of one tile
+    static constexpr int BN_CTA = BN / CTAS;          // B columns staged per CTA
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BK * BN * 2;
+    static constexpr int B_BYTES = BK * BN_CTA * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t TX_BYTES = CTAS * STAGE_BYTES;  // one ring phase, all CTAs
     static constexpr int S = S_;
     static constexpr int BN_ = BN;
     static constexpr bool STG_ = STG;
+    static constexpr bool PAIR_ = PAIR;
     // A (K-major): 8-row swizzle atoms of 8 * BK * 2 bytes
     static constexpr uint32_t A_SBO = 8 * BK * 2;
     static constexpr uint32_t A_SWZ = BK == 64 ? ptx::kSwizzle128B : ptx::kSwizzle64B;
-    // B (N-major): one TMA box of 64 columns x BK rows per 64 output columns
+    // B (N-major): one TMA box of 64 columns x BK rows per 64 staged columns
     static constexpr uint32_t B_BOX_BYTES = BK * 128;
     static constexpr int PEER_COLS = 32;
     static constexpr int PEER_BYTES = BM * PEER_COLS * 4;
@@ -94,7 +112,8 @@ struct KCfg {
     static_assert(OFF_B % 1024 == 0 && OFF_PEER % 1024 == 0 && OFF_STG % 1024 == 0, "1 KiB atoms");
     static_assert(BN == 128 || BN == 256, "tile_n");
     static_assert(BK == 64 || BK == 32, "tile_k");
-    static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, true);
+    static_assert(BN_CTA % 64 == 0, "B is staged in 64-column boxes");
+    static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(TILE_M, BN, true);
 };
 
 // ------------------------------------------------------------------ errors and bounded waits
@@ -110,15 +129,25 @@ __device__ __forceinline__ bool grid_failed(const KernelParams &p) {
     return *reinterpret_cast<volatile int32_t *>(p.err) != 0;
 }
 
-// Wait for the phase of parity `parity` of mbarrier `bar`.  False once the CTA
-// aborts, the grid reports an error, or the bound runs out (then raises).
+template <bool CL>
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
+    if constexpr (CL)
+        return ptx::mbar_try_wait_cluster(bar, parity);
+    else
+        return ptx::mbar_try_wait(bar, parity);
+}
+
+// Wait for the phase of parity `parity` of mbarrier `bar` (acquire at cluster
+// scope when CL).  False once the CTA aborts, the grid reports an error, or the
+// bound runs out (then raises).
+template <bool CL = false>
 __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int *abort,
                                       const KernelParams &p) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (try_wait<CL>(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
     const uint64_t limit = p.timeout_ns * 4ull + 200000000ull;
     for (uint32_t n = 1;; ++n) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (try_wait<CL>(bar, parity)) return true;
         if (*abort) return false;
         if ((n & 31u) == 0u) {
             if (grid_failed(p)) {
@@ -174,19 +203,26 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *flag, const KernelPara
     }
 }
 
-// Rows of tile row tm clipped to M, as a row-chunk range [lo, hi].
-__device__ __forceinline__ void chunk_range(const KernelParams &p, int tm, int &lo, int &hi) {
-    const int r0 = tm * 128;
-    const int r1 = min(r0 + 128, p.M);
+// Row chunks [lo, hi] that rows [r0, r0 + nrows) clipped to M touch; lo > hi
+// when every row lies past M (the odd CTA of a ragged last pair tile).
+__device__ __forceinline__ void chunk_range(const KernelParams &p, int r0, int nrows, int &lo,
+                                            int &hi) {
+    const int r1 = min(r0 + nrows, p.M);
+    if (r0 >= r1) {
+        lo = 0;
+        hi = -1;
+        return;
+    }
     lo = chunk_of_row(p.M_r, p.split, r0);
     hi = chunk_of_row(p.M_r, p.split, r1 - 1);
 }
 
-// Does tile row tm reduce peers?  AR: always; RS: tiles of the local row block.
+// Does the tile starting at row r0 reduce peers?  AR: always; RS: tiles of the
+// local row block (tiles never straddle rank blocks for RS).
 template <int OP>
-__device__ __forceinline__ bool reduces(const KernelParams &p, int tm) {
+__device__ __forceinline__ bool reduces(const KernelParams &p, int r0) {
     if (OP == OP_AR) return true;
-    if (OP == OP_RS) return (tm * 128) / p.M_r == p.rank;
+    if (OP == OP_RS) return r0 / p.M_r == p.rank;
     return false;
 }
 
@@ -296,21 +332,23 @@ __device__ __forceinline__ void store_f32_row32(float *dst, const float (&f)[32]
 }
 
 // Producer side of a tile that writes send/publish rows: once this warp's rows
-// are stored, count the warp on every row chunk the tile covers; the last of
-// the 4 * tiles_n * (tile rows) arrivals publishes the chunk's out flag.
-__device__ __forceinline__ void count_produced(const KernelParams &p, int tm, int lane) {
+// are stored, count the warp on every row chunk the tile (rows [r0, r0 +
+// tile_m)) covers; the last of the 4 * ctas * tiles_n * (tile rows over the
+// chunk) arrivals publishes the chunk's out flag.
+__device__ __forceinline__ void count_produced(const KernelParams &p, int r0, int tile_m, int ctas,
+                                               int lane) {
     __syncwarp();
     if (lane == 0) {
         ptx::fence_acq_rel_gpu();
         int lo, hi;
-        chunk_range(p, tm, lo, hi);
+        chunk_range(p, r0, tile_m, lo, hi);
         uint32_t *cnt = p.out_cnt + (size_t)(p.epoch & 1u) * p.n_rc;
         for (int rc = lo; rc <= hi; ++rc) {
             const int64_t row0 = chunk_row0(p.M_r, p.split, rc);
             const int64_t row1 = chunk_row0(p.M_r, p.split, rc + 1);
-            const int t_lo = (int)(row0 / 128);
-            const int t_hi = (int)((row1 - 1) / 128);
-            const uint32_t need = 4u * (uint32_t)((t_hi - t_lo + 1) * p.tiles_n);
+            const int t_lo = (int)(row0 / tile_m);
+            const int t_hi = (int)((row1 - 1) / tile_m);
+            const uint32_t need = 4u * (uint32_t)ctas * (uint32_t)((t_hi - t_lo + 1) * p.tiles_n);
             const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + rc, 1u);
             if (old + 1u == need) ptx::st_release_gpu(p.out_flags + rc, p.epoch);
         }
@@ -318,10 +356,10 @@ __device__ __forceinline__ void count_produced(const KernelParams &p, int tm, in
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int OP, int BN, int S, int BK, bool STG>
+template <int OP, int BN, int S, int BK, bool STG, bool PAIR>
 __global__ void __launch_bounds__(256, 1)
     syn_fused_kernel(const __grid_constant__ KernelParams p, const __grid_constant__ TensorMaps tm) {
-    using C = KCfg<OP, BN, S, BK, STG>;
+    using C = KCfg<OP, BN, S, BK, STG, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -348,8 +386,16 @@ __global__ void __launch_bounds__(256, 1)
             stage_slices(p, ((int)blockIdx.x - p.G) * C::COMM_NBUF + c, p.n_comm * C::COMM_NBUF,
                          sbase + c * C::COMM_BUF_BYTES, 1, C::COMM_BUF_BYTES, bar0 + 8 * c, abort);
         }
+        __syncthreads();
+        if constexpr (PAIR) ptx::cluster_sync();  // the pair's CTAs leave together
         return;
     }
+
+    // rank in the CTA pair (0 = the CTA that issues the MMAs) and tile walk
+    const uint32_t crank = PAIR ? ptx::cluster_ctarank() : 0u;
+    const int unit = (int)blockIdx.x / C::CTAS;  // pair (or CTA) index
+    const int n_units = p.G / C::CTAS;
+    const bool leader = crank == 0;
 
     // ---- GEMM CTA set-up ---------------------------------------------------
     if (threadIdx.x == 0) {
@@ -360,7 +406,7 @@ __global__ void __launch_bounds__(256, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bar0 + 8 * (C::BAR_TFULL + a), 1);
-            ptx::mbar_init(bar0 + 8 * (C::BAR_TEMPTY + a), 128);
+            ptx::mbar_init(bar0 + 8 * (C::BAR_TEMPTY + a), 128 * C::CTAS);
         }
         for (int s = 0; s < C::P; ++s) {
             ptx::mbar_init(bar0 + 8 * (C::BAR_PFULL + s), 1);
@@ -380,11 +426,17 @@ __global__ void __launch_bounds__(256, 1)
         for (int i = threadIdx.x; i < p.n_rc; i += blockDim.x) nout[i] = 0u;
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) ptx::cluster_sync();  // both CTAs' barriers exist before any remote arrive
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -397,12 +449,13 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t sA = sbase + C::OFF_A, sB = sbase + C::OFF_B;
             uint32_t it = 0;
             bool ok = true;
-            for (int t = p.t_begin + (int)blockIdx.x; ok && t < p.t_end; t += p.G) {
+            for (int t = p.t_begin + unit; ok && t < p.t_end; t += n_units) {
                 const int tile = p.tile_list[t];
                 const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
+                const int r0 = tmi * C::TILE_M + (int)crank * C::BM;  // this CTA's rows
                 if (OP == OP_AG && p.waits) {
                     int lo, hi;
-                    chunk_range(p, tmi, lo, hi);
+                    chunk_range(p, r0, C::BM, lo, hi);
                     for (int rc = lo; ok && rc <= hi; ++rc) {
                         const int q = rc / p.split;
                         if (p.local_inplace && q == p.rank) continue;
@@ -415,44 +468,66 @@ __global__ void __launch_bounds__(256, 1)
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = (int)(it % C::S);
                     const uint32_t ph = (it / C::S) & 1u;
-                    if (!bwait(bar0 + 8 * (C::BAR_EMPTY + s), ph ^ 1u, abort, p)) {
+                    const uint32_t empty = bar0 + 8 * (C::BAR_EMPTY + s);
+                    // even CTA: wait until the MMAs released the stage (its first use
+                    // is free); odd CTA: wait for the even CTA's go for this very
+                    // use, which it sends right before arming the phase, so every
+                    // load of the odd CTA lands on an armed phase the drain covers
+                    if (!bwait<PAIR>(empty, leader ? (ph ^ 1u) : ph, abort, p)) {
                         ok = false;
                         break;
                     }
                     const uint32_t full = bar0 + 8 * (C::BAR_FULL + s);
-                    ptx::mbar_arrive_expect_tx(full, C::STAGE_BYTES);
-                    ptx::tma_load_2d(sA + s * C::A_BYTES, &tm.a, full, kb * C::BK, tmi * C::BM);
+                    const uint32_t a_dst = sA + s * C::A_BYTES, b_dst = sB + s * C::B_BYTES;
+                    const int bcol = tni * BN + (int)crank * C::BN_CTA;
+                    if (leader) {
+                        // the stage is free in both CTAs once the pair's MMAs read it:
+                        // tell the odd CTA, then arm the phase both CTAs' bytes complete
+                        if constexpr (PAIR) ptx::mbar_arrive_remote(ptx::mapa(empty, 1));
+                        ptx::mbar_arrive_expect_tx(full, C::TX_BYTES);
+                        ptx::tma_load_2d(a_dst, &tm.a, full, kb * C::BK, r0);
 #pragma unroll
-                    for (int i = 0; i < BN / 64; ++i)
-                        ptx::tma_load_2d(sB + s * C::B_BYTES + i * C::B_BOX_BYTES, &tm.b, full,
-                                         tni * BN + i * 64, kb * C::BK);
+                        for (int i = 0; i < C::BN_CTA / 64; ++i)
+                            ptx::tma_load_2d(b_dst + i * C::B_BOX_BYTES, &tm.b, full, bcol + i * 64,
+                                             kb * C::BK);
+                    } else {
+                        // the odd CTA's bytes complete on the even CTA's ring barrier
+                        const uint32_t rfull = ptx::mapa(full, 0);
+                        ptx::tma_load_2d_pair(a_dst, &tm.a, rfull, kb * C::BK, r0);
+#pragma unroll
+                        for (int i = 0; i < C::BN_CTA / 64; ++i)
+                            ptx::tma_load_2d_pair(b_dst + i * C::B_BOX_BYTES, &tm.b, rfull,
+                                                  bcol + i * 64, kb * C::BK);
+                    }
                 }
             }
-            // drain: every armed stage's last phase must have landed
-            for (uint32_t s = 0; s < (uint32_t)C::S; ++s) {
-                if (it > s) {
-                    const uint32_t last = s + ((it - 1u - s) / C::S) * C::S;
-                    bwait_drain(bar0 + 8 * (C::BAR_FULL + s), (last / C::S) & 1u, p);
+            // drain: every armed stage's last phase must have landed (the even
+            // CTA's phases include the odd CTA's bytes)
+            if (leader)
+                for (uint32_t s = 0; s < (uint32_t)C::S; ++s) {
+                    if (it > s) {
+                        const uint32_t last = s + ((it - 1u - s) / C::S) * C::S;
+                        bwait_drain(bar0 + 8 * (C::BAR_FULL + s), (last / C::S) & 1u, p);
+                    }
                 }
-            }
         }
     } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (lane == 0) {
+        // ================= MMA issuer (the pair's even CTA) =================
+        if (lane == 0 && leader) {
             const uint32_t sA = sbase + C::OFF_A, sB = sbase + C::OFF_B;
             uint32_t it = 0, tc = 0;
             bool ok = true;
-            for (int t = p.t_begin + (int)blockIdx.x; ok && t < p.t_end; t += p.G) {
+            for (int t = p.t_begin + unit; ok && t < p.t_end; t += n_units) {
                 const int acc = (int)(tc & 1u);
                 const uint32_t aph = (tc >> 1) & 1u;
-                if (!bwait(bar0 + 8 * (C::BAR_TEMPTY + acc), aph ^ 1u, abort, p)) break;
+                if (!bwait<PAIR>(bar0 + 8 * (C::BAR_TEMPTY + acc), aph ^ 1u, abort, p)) break;
                 ptx::tc_fence_after();
                 if (p.trace != nullptr) p.trace[4 * t + 0] = ptx::globaltimer();
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = (int)(it % C::S);
                     const uint32_t ph = (it / C::S) & 1u;
-                    if (!bwait(bar0 + 8 * (C::BAR_FULL + s), ph, abort, p)) {
+                    if (!bwait<PAIR>(bar0 + 8 * (C::BAR_FULL + s), ph, abort, p)) {
                         ok = false;
                         break;
                     }
@@ -467,17 +542,29 @@ __global__ void __launch_bounds__(256, 1)
                         // SBO = next 8 K-rows; a 16-deep K slice is +16 rows of 128 B
                         const uint64_t bd =
                             ptx::sdesc(b0 + k * 2048, C::B_BOX_BYTES, 1024, ptx::kSwizzle128B);
-                        ptx::umma_bf16(d, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+                        if constexpr (PAIR)
+                            ptx::umma_bf16_pair(d, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+                        else
+                            ptx::umma_bf16(d, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
                     }
-                    ptx::umma_commit(bar0 + 8 * (C::BAR_EMPTY + s));
+                    if constexpr (PAIR)
+                        ptx::umma_commit_pair(bar0 + 8 * (C::BAR_EMPTY + s));
+                    else
+                        ptx::umma_commit(bar0 + 8 * (C::BAR_EMPTY + s));
                 }
                 if (!ok) break;
-                ptx::umma_commit(bar0 + 8 * (C::BAR_TFULL + acc));
+                if constexpr (PAIR)
+                    ptx::umma_commit_pair(bar0 + 8 * (C::BAR_TFULL + acc));
+                else
+                    ptx::umma_commit(bar0 + 8 * (C::BAR_TFULL + acc));
                 if (p.trace != nullptr) p.trace[4 * t + 1] = ptx::globaltimer();
                 ++tc;
             }
             // every MMA this thread issued must finish before TMEM is released
-            ptx::umma_commit(bar0 + 8 * C::BAR_DRAIN);
+            if constexpr (PAIR)
+                ptx::umma_commit_pair(bar0 + 8 * C::BAR_DRAIN);
+            else
+                ptx::umma_commit(bar0 + 8 * C::BAR_DRAIN);
             bwait_drain(bar0 + 8 * C::BAR_DRAIN, 0, p);
         }
     } else if (warp >= 2 && warp < 6) {
@@ -486,18 +573,24 @@ __global__ void __launch_bounds__(256, 1)
         const int lrow = qd * 32 + lane;
         uint32_t tc = 0, pit = 0;
         const uint32_t sPeer = sbase + C::OFF_PEER;
-        for (int t = p.t_begin + (int)blockIdx.x; t < p.t_end; t += p.G) {
+        for (int t = p.t_begin + unit; t < p.t_end; t += n_units) {
             const int tile = p.tile_list[t];
             const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
             const int acc = (int)(tc & 1u);
             const uint32_t aph = (tc >> 1) & 1u;
-            bool ok = bwait(bar0 + 8 * (C::BAR_TFULL + acc), aph, abort, p);
+            const uint32_t tfull = bar0 + 8 * (C::BAR_TFULL + acc);
+            bool ok = bwait<PAIR>(tfull, aph, abort, p);
             if (!__all_sync(0xffffffffu, ok)) break;
+            // the even CTA's MMA commit arrives only on its own barrier: forward
+            if constexpr (PAIR)
+                if (leader && warp == 2 && lane == 0) ptx::mbar_arrive_remote(ptx::mapa(tfull, 1));
             ptx::tc_fence_after();
-            if (p.trace != nullptr && warp == 2 && lane == 0) p.trace[4 * t + 2] = ptx::globaltimer();
-            const int row = tmi * C::BM + lrow;
+            if (p.trace != nullptr && leader && warp == 2 && lane == 0)
+                p.trace[4 * t + 2] = ptx::globaltimer();
+            const int tr0 = tmi * C::TILE_M;                       // tile's first row
+            const int row = tr0 + (int)crank * C::BM + lrow;       // this thread's row
             const bool in_range = row < p.M;
-            const bool red = reduces<OP>(p, tmi);
+            const bool red = reduces<OP>(p, tr0);
             const uint32_t tbase = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * BN);
             bool dead = false;
 #pragma unroll 1
@@ -551,11 +644,16 @@ __global__ void __launch_bounds__(256, 1)
                 }  // OP != OP_AG
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar0 + 8 * (C::BAR_TEMPTY + acc));
-            if (p.trace != nullptr && warp == 2 && lane == 0) p.trace[4 * t + 3] = ptx::globaltimer();
+            const uint32_t tempty = bar0 + 8 * (C::BAR_TEMPTY + acc);
+            if (leader)
+                ptx::mbar_arrive(tempty);
+            else
+                ptx::mbar_arrive_remote(ptx::mapa(tempty, 0));
+            if (p.trace != nullptr && leader && warp == 2 && lane == 0)
+                p.trace[4 * t + 3] = ptx::globaltimer();
             if (dead) break;
             if (OP != OP_AG && p.f32_out != nullptr && (OP == OP_AR || !red))
-                count_produced(p, tmi, lane);
+                count_produced(p, tr0, C::TILE_M, C::CTAS, lane);
             ++tc;
         }
     } else if (warp == 6) {
@@ -564,13 +662,15 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t sPeer = sbase + C::OFF_PEER;
             uint32_t pit = 0;
             bool ok = true;
-            for (int t = p.t_begin + (int)blockIdx.x; ok && t < p.t_end; t += p.G) {
+            for (int t = p.t_begin + unit; ok && t < p.t_end; t += n_units) {
                 const int tile = p.tile_list[t];
                 const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
-                if (!reduces<OP>(p, tmi)) continue;
+                const int tr0 = tmi * C::TILE_M;
+                if (!reduces<OP>(p, tr0)) continue;
+                const int r0 = tr0 + (int)crank * C::BM;  // this CTA's rows
                 if (p.waits) {
                     int lo, hi;
-                    chunk_range(p, tmi, lo, hi);
+                    chunk_range(p, r0, C::BM, lo, hi);
                     for (int rc = lo; ok && rc <= hi; ++rc)
                         for (int q = 0; ok && q < p.R; ++q) {
                             if (q == p.rank) continue;
@@ -580,7 +680,7 @@ __global__ void __launch_bounds__(256, 1)
                     if (!ok) break;
                     ptx::fence_proxy_async();
                 }
-                const int prow = tmi * C::BM - p.peer_row_off;
+                const int prow = r0 - p.peer_row_off;
                 for (int cc = 0; ok && cc < BN / 32; ++cc)
                     for (int q = 0; q < p.R; ++q) {
                         if (q == p.rank) continue;
@@ -618,50 +718,108 @@ __global__ void __launch_bounds__(256, 1)
     if (p.stats != nullptr && wait_ns != 0ull) atomicAdd(p.stats + 0, wait_ns);
     ptx::tc_fence_before();
     __syncthreads();
+    // the pair leaves together: no remote arrive may target a CTA that has exited,
+    // and the even CTA's drain above covered the odd CTA's in-flight loads
+    if constexpr (PAIR) ptx::cluster_sync();
     ptx::tc_fence_after();
-    if (warp == 1) ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (warp == 1) {
+        if constexpr (PAIR)
+            ptx::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else
+            ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
     if (threadIdx.x == 0 && p.stats != nullptr)
         atomicAdd(p.stats + 1, (unsigned long long)(ptx::globaltimer() - t_start));
 }
 
-template <int OP, int BN, int S, int BK, bool STG>
+template <int OP, int BN, int S, int BK, bool STG, bool PAIR>
 cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid, cudaStream_t st) {
-    using C = KCfg<OP, BN, S, BK, STG>;
-    cudaError_t e = cudaFuncSetAttribute(syn_fused_kernel<OP, BN, S, BK, STG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    using C = KCfg<OP, BN, S, BK, STG, PAIR>;
+    auto kern = syn_fused_kernel<OP, BN, S, BK, STG, PAIR>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    int n = 1;
+    if (PAIR) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, syn_fused_kernel<OP, BN, S, BK, STG>, p, tm);
+    cfg.numAttrs = n;
+    e = cudaLaunchKernelEx(&cfg, kern, p, tm);
+    if (e != cudaSuccess && PAIR) {
+        // clusters without the cooperative attribute: the grid is sized to the
+        // co-resident cluster count, so every CTA is still resident
+        (void)cudaGetLastError();
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, p, tm);
+    }
+    return e;
 }
 
-// Every compiled kernel instance, per operator: (tile_n, stages, tile_k, stg).
-// `Fn` receives the KCfg type; returns false when the combination is not
-// compiled.
+// Co-resident 2-CTA clusters of one instance (0 when the query fails).
+template <int OP, int BN, int S, int BK, bool STG, bool PAIR>
+int max_clusters_t() {
+    using C = KCfg<OP, BN, S, BK, STG, PAIR>;
+    auto kern = syn_fused_kernel<OP, BN, S, BK, STG, PAIR>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// Every compiled kernel instance, per operator: (tile_m, tile_n, stages,
+// tile_k, stg).  tile_m 256 is the CTA-pair kernel.  `Fn` receives the KCfg
+// type; returns false when the combination is not compiled.
 template <int OP, typename Fn>
 bool dispatch_cfg(const LaunchCfg &lc, Fn &&fn) {
     const int tn = lc.tile_n, st = lc.stages, tk = lc.tile_k;
-    const bool g = lc.stg;
-#define SYN_CFG(TN, ST, TK, G) \
-    if (tn == TN && st == ST && tk == TK && g == G) return fn(KCfg<OP, TN, ST, TK, G>{}), true;
+    const bool g = lc.stg, pr = lc.pair;
+#define SYN_CFG(PR, TN, ST, TK, G)                                                 \
+    if (pr == PR && tn == TN && st == ST && tk == TK && g == G)                    \
+        return fn(KCfg<OP, TN, ST, TK, G, PR>{}), true;
     if constexpr (OP == OP_AG) {
-        SYN_CFG(256, 4, 64, true) SYN_CFG(256, 4, 64, false)
-        SYN_CFG(128, 6, 64, true) SYN_CFG(128, 6, 64, false)
-        SYN_CFG(256, 8, 32, true) SYN_CFG(256, 9, 32, false)
+        SYN_CFG(false, 256, 4, 64, true) SYN_CFG(false, 256, 4, 64, false)
+        SYN_CFG(false, 128, 6, 64, true) SYN_CFG(false, 128, 6, 64, false)
+        SYN_CFG(false, 256, 8, 32, true) SYN_CFG(false, 256, 9, 32, false)
+        SYN_CFG(true, 256, 6, 64, true) SYN_CFG(true, 256, 7, 64, false)
+        SYN_CFG(true, 256, 5, 64, true) SYN_CFG(true, 256, 5, 64, false)
         return false;
     } else {
-        SYN_CFG(256, 3, 64, true) SYN_CFG(128, 4, 64, true) SYN_CFG(256, 6, 32, true)
-        SYN_CFG(256, 2, 64, false) SYN_CFG(256, 3, 64, false) SYN_CFG(256, 4, 64, false)
-        SYN_CFG(128, 3, 64, false) SYN_CFG(128, 4, 64, false) SYN_CFG(128, 6, 64, false)
-        SYN_CFG(256, 4, 32, false) SYN_CFG(256, 5, 32, false) SYN_CFG(256, 6, 32, false)
+        SYN_CFG(false, 256, 3, 64, true) SYN_CFG(false, 128, 4, 64, true) SYN_CFG(false, 256, 6, 32, true)
+        SYN_CFG(false, 256, 2, 64, false) SYN_CFG(false, 256, 3, 64, false) SYN_CFG(false, 256, 4, 64, false)
+        SYN_CFG(false, 128, 3, 64, false) SYN_CFG(false, 128, 4, 64, false) SYN_CFG(false, 128, 6, 64, false)
+        SYN_CFG(false, 256, 4, 32, false) SYN_CFG(false, 256, 5, 32, false) SYN_CFG(false, 256, 6, 32, false)
+        SYN_CFG(true, 256, 4, 64, true)
+        SYN_CFG(true, 256, 3, 64, false) SYN_CFG(true, 256, 4, 64, false) SYN_CFG(true, 256, 5, 64, false)
         return false;
     }
 #undef SYN_CFG
@@ -673,7 +831,7 @@ cudaError_t launch_op(const KernelParams &p, const TensorMaps &tm, const LaunchC
     cudaError_t err = cudaErrorInvalidValue;
     dispatch_cfg<OP>(lc, [&](auto c) {
         using C = decltype(c);
-        err = launch_fused_t<OP, C::BN_, C::S, C::BK, C::STG_>(p, tm, lc.grid, st);
+        err = launch_fused_t<OP, C::BN_, C::S, C::BK, C::STG_, C::PAIR_>(p, tm, lc.grid, st);
     });
     return err;
 }
@@ -683,6 +841,16 @@ int smem_bytes_op(const LaunchCfg &lc) {
     int bytes = -1;
     dispatch_cfg<OP>(lc, [&](auto c) { bytes = decltype(c)::SMEM_ALLOC; });
     return bytes;
+}
+
+template <int OP>
+int max_clusters_op(const LaunchCfg &lc) {
+    int n = 0;
+    dispatch_cfg<OP>(lc, [&](auto c) {
+        using C = decltype(c);
+        if constexpr (C::PAIR_) n = max_clusters_t<OP, C::BN_, C::S, C::BK, C::STG_, C::PAIR_>();
+    });
+    return n;
 }
 
 }  // namespace syn

@@ -101,6 +101,7 @@ struct LaunchCfg {
     int tile_k;   // k-block depth: 64 or 32
     int stages;   // GEMM pipeline stages
     bool stg;     // CTA carries the co-located staging buffers
+    bool pair;    // 2-CTA clusters share 256-row tiles (tile_m 256)
     int grid;     // CTAs
 };
 
@@ -115,11 +116,14 @@ cudaError_t launch_fused_ar(const KernelParams &p, const TensorMaps &tm, const L
 // Dynamic shared memory of a combination (-1 if not compiled).
 int fused_smem_bytes(int op, const LaunchCfg &lc);
 // Default pipeline depth of a (tile_n, tile_k, stg) choice.
-inline int default_stages(int op, int tile_n, int tile_k, bool stg) {
+inline int default_stages(int op, int tile_n, int tile_k, bool stg, bool pair) {
+    if (pair) return op == OP_AG ? (stg ? 6 : 7) : 4;
     if (tile_k == 32) return op == OP_AG ? (stg ? 8 : 9) : 6;
     if (op == OP_AG) return tile_n == 256 ? 4 : 6;
     return tile_n == 256 ? 3 : 4;
 }
+// Co-resident 2-CTA clusters for a pair instance (0 if unknown / not a pair).
+int fused_max_clusters(int op, const LaunchCfg &lc);
 
 // Record the message syn_last_error() returns on this thread.
 void set_last_error(const std::string &msg);

@@ -1,6 +1,6 @@
 // kernel_ar.cu -- compiled instances of the fused chunk-scheduled kernel
-// for the GEMM-AR operator (every tile width / pipeline depth / peer-path
-// combination that dispatch_cfg lists).
+// for the GEMM-AR operator (every tile shape / pipeline depth / staging-buffer
+// combination that dispatch_cfg lists, single CTA and CTA pair).
 #include "fused.cuh"
 
 namespace syn {
@@ -11,5 +11,7 @@ cudaError_t launch_fused_ar(const KernelParams &p, const TensorMaps &tm, const L
 }
 
 int smem_bytes_ar(const LaunchCfg &lc) { return smem_bytes_op<OP_AR>(lc); }
+
+int max_clusters_ar(const LaunchCfg &lc) { return max_clusters_op<OP_AR>(lc); }
 
 }  // namespace syn

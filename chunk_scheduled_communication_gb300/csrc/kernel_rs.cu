@@ -1,6 +1,6 @@
 // kernel_rs.cu -- compiled instances of the fused chunk-scheduled kernel
-// for the GEMM-RS operator (every tile width / pipeline depth / peer-path
-// combination that dispatch_cfg lists).
+// for the GEMM-RS operator (every tile shape / pipeline depth / staging-buffer
+// combination that dispatch_cfg lists, single CTA and CTA pair).
 #include "fused.cuh"
 
 namespace syn {
@@ -11,5 +11,7 @@ cudaError_t launch_fused_rs(const KernelParams &p, const TensorMaps &tm, const L
 }
 
 int smem_bytes_rs(const LaunchCfg &lc) { return smem_bytes_op<OP_RS>(lc); }
+
+int max_clusters_rs(const LaunchCfg &lc) { return max_clusters_op<OP_RS>(lc); }
 
 }  // namespace syn

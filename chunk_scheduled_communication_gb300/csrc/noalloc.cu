@@ -203,7 +203,8 @@ extern "C" int syn_ag_gemm_noalloc(int R, int rank, const syn_layout_t *layout, 
     lc.tile_n = s.tile_n;
     lc.tile_k = 64;
     lc.stg = true;
-    lc.stages = default_stages(OP_AG, s.tile_n, lc.tile_k, lc.stg);
+    lc.pair = false;
+    lc.stages = default_stages(OP_AG, s.tile_n, lc.tile_k, lc.stg, lc.pair);
     lc.grid = p.G;
     const cudaError_t le = launch_fused_ag(p, maps, lc, st);
     if (le != cudaSuccess) return fail(SYN_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(le));

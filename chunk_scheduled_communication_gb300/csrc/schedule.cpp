@@ -90,8 +90,8 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
     }
     const int tile_m = kn.tile_m == 0 ? kTileM : kn.tile_m;
     const int tile_n = kn.tile_n == 0 ? 256 : kn.tile_n;
-    if (tile_m != kTileM) {
-        err = "tile_m must be 128";
+    if (tile_m != kTileM && tile_m != 2 * kTileM) {
+        err = "tile_m must be 128 (one CTA per tile) or 256 (a CTA pair per tile)";
         return SYN_ERR_UNSUPPORTED;
     }
     if (tile_n != 128 && tile_n != 256) {
@@ -107,7 +107,7 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         return SYN_ERR_UNSUPPORTED;
     }
     if (op == SYN_OP_GEMM_RS && M_r % tile_m != 0) {
-        err = "GEMM-RS needs (M/R) % 128 == 0";
+        err = "GEMM-RS needs (M/R) % tile_m == 0";
         return SYN_ERR_UNSUPPORTED;
     }
     if (L.M > (int64_t)1 << 30 || L.N > (int64_t)1 << 30 || L.K > (int64_t)1 << 30) {

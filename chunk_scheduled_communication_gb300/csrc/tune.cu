@@ -81,6 +81,8 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
             best->backend = (syn_backend_t)field(hit, "backend");
             best->comm_sms = (int)field(hit, "comm_sms");
             best->tile_n = (int)field(hit, "tile_n");
+            const long tm = field(hit, "tile_m");
+            best->tile_m = tm > 0 ? (int)tm : 128;
             best->group_m = (int)field(hit, "group_m");
             *best_split = (int)field(hit, "split");
             *best_order = (syn_order_t)field(hit, "order");
@@ -124,20 +126,25 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
     if (op != SYN_OP_AG_GEMM) backends.push_back(SYN_BACKEND_TMA_COLOCATED_SMEM);
     const int comm_opts[] = {4, 8, 16};
     const int split_opts[] = {1, 2, 3, 4, 6, 8};
-    const syn_order_t order_opts[] = {SYN_ORDER_ROW_MAJOR, SYN_ORDER_COL_MAJOR, SYN_ORDER_GROUPED};
-    const int tile_opts[] = {256, 128};
+    const syn_order_t order_opts[] = {SYN_ORDER_ROW_MAJOR, SYN_ORDER_GROUPED, SYN_ORDER_COL_MAJOR};
+    // tile shapes: 256 x 256 on a CTA pair first (the fastest instances), then
+    // 128 x 256 and 128 x 128 on one CTA
+    const int shape_opts[][2] = {{256, 256}, {128, 256}, {128, 128}};
     std::vector<Cand> cands;
-    for (int tn : tile_opts) {
+    for (const auto &shape : shape_opts) {
+        const int tm = shape[0], tn = shape[1];
         if (L.N % tn) continue;
+        if (op == SYN_OP_GEMM_RS && M_r % tm) continue;
         for (syn_backend_t be : backends)
             for (int ci = 0; ci < (be == SYN_BACKEND_TMA_DEDICATED ? 3 : 1); ++ci)
                 for (int sp : split_opts) {
-                    if (M_r % sp) continue;
+                    if (sp > M_r) continue;
                     for (syn_order_t od : order_opts) {
                         Cand cd;
                         syn_knobs_default(&cd.kn);
                         cd.kn.backend = be;
                         cd.kn.comm_sms = comm_opts[ci];
+                        cd.kn.tile_m = tm;
                         cd.kn.tile_n = tn;
                         cd.split = sp;
                         cd.order = od;
@@ -201,7 +208,8 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
     if (cache_path != nullptr && *cache_path) {
         std::ofstream out(cache_path, std::ios::app);
         out << "{" << key << ",\"backend\":" << (int)best->backend << ",\"comm_sms\":" << best->comm_sms
-            << ",\"tile_n\":" << best->tile_n << ",\"group_m\":" << best->group_m
+            << ",\"tile_m\":" << best->tile_m << ",\"tile_n\":" << best->tile_n
+            << ",\"group_m\":" << best->group_m
             << ",\"split\":" << *best_split << ",\"order\":" << (int)*best_order << ",\"us\":" << best_t
             << "}\n";
     }

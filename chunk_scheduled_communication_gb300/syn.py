@@ -122,12 +122,13 @@ def _check(status: int, where: str):
 
 
 def make_knobs(backend="ce", comm_sms=8, tile_n=256, group_m=8, slice_kb=128, timeout_ns=0,
-               drop_chunk=-1, trace=0, stages=0, tile_k=0) -> Knobs:
+               drop_chunk=-1, trace=0, stages=0, tile_k=0, tile_m=0) -> Knobs:
     k = Knobs()
     _check(lib().syn_knobs_default(ctypes.byref(k)), "syn_knobs_default")
     k.backend = BACKENDS[backend] if isinstance(backend, str) else int(backend)
     k.comm_sms, k.tile_n, k.group_m, k.slice_kb = comm_sms, tile_n, group_m, slice_kb
     k.timeout_ns, k.debug_drop_chunk, k.trace, k.stages, k.tile_k = timeout_ns, drop_chunk, trace, stages, tile_k
+    k.tile_m = tile_m
     return k
 
 
@@ -270,7 +271,8 @@ def autotune(op, R, rank, M, N, K, budget_s=60.0):
     us = ctypes.c_double()
     _check(L.syn_autotune(_op(op), R, rank, ctypes.byref(lay), budget_s, ctypes.byref(kn), ctypes.byref(split),
                           ctypes.byref(order), ctypes.byref(us)), "syn_autotune")
-    return {"backend": BACKEND_NAMES.get(kn.backend, kn.backend), "comm_sms": kn.comm_sms, "tile_n": kn.tile_n,
+    return {"backend": BACKEND_NAMES.get(kn.backend, kn.backend), "comm_sms": kn.comm_sms,
+            "tile_m": kn.tile_m, "tile_n": kn.tile_n,
             "group_m": kn.group_m, "split": split.value, "order": order.value, "us": us.value}
 
 

@@ -327,6 +327,61 @@ def test_tile_k32_instances_bit_exact(w, backend, stages):
     assert (k32["out"] == got["out"]).all()
 
 
+# ----------------------------------------------------------------------------- CTA pairs (tile_m 256)
+INT_AG_PAIR = wl.scaled(wl.TINY_AG, M=3 * 200, K=192, N=512, R=3)       # ragged: last pair half past M
+INT_RS_PAIR = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=4 * 256, K=320, N=512, R=4)
+INT_AR_PAIR = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=2 * 333, K=128, N=512, R=2)
+
+
+@pytest.mark.parametrize("w,backend,stages", [
+    (INT_AG_PAIR, "tma_colocated", 6), (INT_AG_PAIR, "tma_colocated", 5), (INT_AG_PAIR, "ce", 7),
+    (INT_AG_PAIR, "ce", 5), (INT_AG_PAIR, "tma_dedicated", 7), (INT_AG_PAIR, "unfused", 7),
+    (INT_AG_PAIR, "decomposed", 7),
+    (INT_RS_PAIR, "tma_colocated_smem", 3), (INT_RS_PAIR, "tma_colocated_smem", 4),
+    (INT_RS_PAIR, "tma_colocated_smem", 5), (INT_RS_PAIR, "tma_colocated", 4), (INT_RS_PAIR, "ce", 4),
+    (INT_AR_PAIR, "tma_colocated_smem", 4), (INT_AR_PAIR, "tma_colocated", 4), (INT_AR_PAIR, "ce", 3),
+], ids=lambda v: str(getattr(v, "op", v)))
+def test_cta_pair_instances_bit_exact(w, backend, stages):
+    """256-row tiles shared by a CTA pair (2-CTA UMMA) give the oracle's bits
+    on integer inputs, for every compiled pair instance and both ranks' ends."""
+    for r in (0, w.R - 1):
+        inp = inputs(w, r, 0, "int")
+        d = runner.upload(inp)
+        with runner.make_plan(d, split=2, order="row", backend=backend, tile_m=256, tile_n=256,
+                              stages=stages, comm_sms=4) as plan:
+            runner.call(plan, d)
+            runner.call(plan, d)
+            assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+            assert plan.info()["grid_compute"] % 2 == 0
+        got = {"out": runner.dev_to_u16(d.out)}
+        if w.op == "ag":
+            got["gathered"] = runner.dev_to_u16(d.gathered)
+        else:
+            got["f32"] = d.f32_out.cpu().numpy()
+        check_against_oracle(w, r, got, kind="int")
+
+
+@pytest.mark.parametrize("w,backend", [(wl.LLAMA3_8B_UP_AG, "tma_colocated"),
+                                       (wl.LLAMA3_8B_DOWN_RS, "tma_colocated_smem"),
+                                       (wl.QWEN2_7B_DOWN_AR, "tma_colocated_smem")],
+                         ids=["ag", "rs", "ar"])
+def test_cta_pair_full_size_against_oracle(w, backend):
+    got = run(w, 0, backend=backend, split=2, order="row")  # single-CTA reference run
+    inp = inputs(w, 0)
+    d = runner.upload(inp, with_f32_out=(w.op != "ag"))
+    with runner.make_plan(d, split=2, order="row", backend=backend, tile_m=256) as plan:
+        runner.call(plan, d)
+        assert plan.sync() == syn.OK
+    pair = {"out": runner.dev_to_u16(d.out)}
+    if w.op == "ag":
+        pair["gathered"] = runner.dev_to_u16(d.gathered)
+    else:
+        pair["f32"] = d.f32_out.cpu().numpy()
+    check_against_oracle(w, 0, pair)
+    ok, exc, frob = runner.bf16_close(pair["out"], got["out"])
+    assert ok, (exc, frob)
+
+
 def test_uncompiled_stage_count_is_rejected():
     inp = inputs(INT_AR_N512, 0, 0, "int")
     d = runner.upload(inp)

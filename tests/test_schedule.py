@@ -178,3 +178,30 @@ def test_smem_peer_backend_has_no_transfers_and_reduce_tiles_first():
     info, tl, tk, tr = syn.schedule_build("ar", 8, 3, 4096, 3584, 2368, split=1, order="row",
                                           backend="tma_colocated_smem")
     assert info["n_transfers"] == 0 and tl.tolist() == list(range(info["n_tiles"]))
+
+
+@pytest.mark.parametrize("op,R,r,M,N,K,split", [
+    ("ag", 8, 0, 8192, 1792, 4096, 2), ("ag", 3, 1, 600, 512, 192, 1), ("rs", 8, 2, 8192, 4096, 1792, 4),
+    ("ar", 8, 5, 4096, 3584, 2368, 3), ("ar", 2, 1, 666, 512, 128, 1)])
+def test_pair_tiles_of_256_rows(op, R, r, M, N, K, split):
+    """tile_m = 256 (a CTA pair per tile): same rules over 256-row tiles."""
+    info, tl, tk, tr = syn.schedule_build(op, R, r, M, N, K, split=split, order="row", tile_m=256)
+    M_r = M // R
+    tiles_m, tiles_n = -(-M // 256), N // 256
+    assert info["tile_m"] == 256 and info["n_tiles"] == tiles_m * tiles_n
+    assert sorted(tl.tolist()) == list(range(tiles_m * tiles_n))
+    arrival = {code: a for a, code in enumerate(tr.tolist())}
+    for t, key in zip(tl.tolist(), tk.tolist()):
+        tm = t // tiles_n
+        d = deps(op, R, r, M, M_r, split, tm, tile_m=256)
+        if d:
+            assert key == max(arrival[c] for c in d)
+        else:
+            assert op == "rs" and key < 0
+    assert (np.diff(tk) >= 0).all()
+
+
+def test_pair_tiles_rs_needs_256_row_blocks():
+    with pytest.raises(syn.SynError) as e:
+        syn.schedule_build("rs", 4, 0, 4 * 384, 256, 256, tile_m=256)
+    assert e.value.status == syn.ERR_UNSUPPORTED
