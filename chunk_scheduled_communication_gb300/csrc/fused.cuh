@@ -33,9 +33,12 @@
 // rows into that CTA's TMEM.  Per SM this halves the B bytes staged and read
 // for the same MMA work, which is what lets the tensor pipe run near its peak
 // on this architecture.  The peer's TMA loads complete on the even CTA's ring
-// barrier; stage releases and accumulator-ready signals are forwarded to the
-// peer with remote mbarrier arrives, and the peer's epilogue releases the
-// accumulator the same way.  No multicast form is used.
+// barrier; the MMA issuer commits each stage release and each accumulator-ready
+// signal to the barrier of both CTAs (two single-target commits, the second to
+// the peer's barrier through its shared::cluster address), and the peer's
+// epilogue releases the accumulator with a remote mbarrier arrive.  (Forwarding
+// those signals through a thread of the even CTA instead measured 2.5x slower.)
+// No multicast form is used.
 //
 // Every wait is bounded (global timer) and ends in SYN_ERR_TIMEOUT written to
 // the plan's error word; the CTA then drains its own outstanding asynchronous
@@ -101,7 +104,8 @@ struct KCfg {
     static constexpr int BAR_PEMPTY = BAR_PFULL + P;
     static constexpr int BAR_STG = BAR_PEMPTY + P;
     static constexpr int BAR_DRAIN = BAR_STG + NSTG;
-    static constexpr int NBAR = BAR_DRAIN + 1;
+    static constexpr int BAR_PEERDONE = BAR_DRAIN + 1;  // PAIR: odd producer finished issuing
+    static constexpr int NBAR = BAR_PEERDONE + 1;
     static constexpr int COMM_BUF_BYTES = 32768;
     static constexpr int COMM_NBUF = OFF_BAR / COMM_BUF_BYTES;
     static constexpr int NBAR_ALL = NBAR > COMM_NBUF ? NBAR : COMM_NBUF;
@@ -164,11 +168,12 @@ __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile in
 }
 
 // Wait used only while draining on the way out: ignores the abort flag.
+template <bool CL = false>
 __device__ __forceinline__ void bwait_drain(uint32_t bar, uint32_t parity, const KernelParams &p) {
     const uint64_t t0 = ptx::globaltimer();
     const uint64_t limit = p.timeout_ns * 4ull + 200000000ull;
     for (uint32_t n = 0;; ++n) {
-        if (ptx::mbar_try_wait(bar, parity)) return;
+        if (try_wait<CL>(bar, parity)) return;
         if ((n & 31u) == 31u && ptx::globaltimer() - t0 > limit) {
             raise_error(p, SYN_ERR_TIMEOUT, WHERE_PIPE, (int)bar);
             return;
@@ -406,8 +411,9 @@ __global__ void __launch_bounds__(256, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(bar0 + 8 * (C::BAR_TFULL + a), 1);
-            ptx::mbar_init(bar0 + 8 * (C::BAR_TEMPTY + a), 128 * C::CTAS);
+            ptx::mbar_init(bar0 + 8 * (C::BAR_TEMPTY + a), 4 * C::CTAS);  // one per epilogue warp
         }
+        ptx::mbar_init(bar0 + 8 * C::BAR_PEERDONE, 1);
         for (int s = 0; s < C::P; ++s) {
             ptx::mbar_init(bar0 + 8 * (C::BAR_PFULL + s), 1);
             ptx::mbar_init(bar0 + 8 * (C::BAR_PEMPTY + s), 4);
@@ -469,11 +475,9 @@ __global__ void __launch_bounds__(256, 1)
                     const int s = (int)(it % C::S);
                     const uint32_t ph = (it / C::S) & 1u;
                     const uint32_t empty = bar0 + 8 * (C::BAR_EMPTY + s);
-                    // even CTA: wait until the MMAs released the stage (its first use
-                    // is free); odd CTA: wait for the even CTA's go for this very
-                    // use, which it sends right before arming the phase, so every
-                    // load of the odd CTA lands on an armed phase the drain covers
-                    if (!bwait<PAIR>(empty, leader ? (ph ^ 1u) : ph, abort, p)) {
+                    // wait until the pair's MMAs released the stage (its first use is
+                    // free); the MMA commit arrives on this barrier in both CTAs
+                    if (!bwait<PAIR>(empty, ph ^ 1u, abort, p)) {
                         ok = false;
                         break;
                     }
@@ -481,9 +485,7 @@ __global__ void __launch_bounds__(256, 1)
                     const uint32_t a_dst = sA + s * C::A_BYTES, b_dst = sB + s * C::B_BYTES;
                     const int bcol = tni * BN + (int)crank * C::BN_CTA;
                     if (leader) {
-                        // the stage is free in both CTAs once the pair's MMAs read it:
-                        // tell the odd CTA, then arm the phase both CTAs' bytes complete
-                        if constexpr (PAIR) ptx::mbar_arrive_remote(ptx::mapa(empty, 1));
+                        // arm the phase that both CTAs' bytes complete
                         ptx::mbar_arrive_expect_tx(full, C::TX_BYTES);
                         ptx::tma_load_2d(a_dst, &tm.a, full, kb * C::BK, r0);
 #pragma unroll
@@ -501,13 +503,38 @@ __global__ void __launch_bounds__(256, 1)
                     }
                 }
             }
-            // drain: every armed stage's last phase must have landed (the even
-            // CTA's phases include the odd CTA's bytes)
+            // drain: every phase this CTA (or, PAIR, the odd CTA) loaded into must
+            // have landed before the CTA may exit.  In a pair both producers wake
+            // on the same MMA commit, so the odd CTA can be one use of a stage
+            // ahead of the even CTA's arming; it reports how many k-blocks it
+            // issued, and the even CTA arms any phase only the odd CTA loaded
+            // into (with the odd CTA's bytes alone) before waiting for the last
+            // phase of every stage.  The pair's closing cluster barrier keeps the
+            // odd CTA alive until then.
+            uint32_t it_all = it;
+            if constexpr (PAIR) {
+                uint32_t *peer_it = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC + 8);
+                const uint32_t done = bar0 + 8 * C::BAR_PEERDONE;
+                if (!leader) {
+                    ptx::st_shared_cluster_u32(ptx::mapa(ptx::smem_u32(peer_it), 0), it);
+                    ptx::mbar_arrive_remote(ptx::mapa(done, 0));
+                } else {
+                    bwait_drain<true>(done, 0, p);
+                    const uint32_t it_p = *reinterpret_cast<volatile uint32_t *>(peer_it);
+                    for (uint32_t s = 0; s < (uint32_t)C::S; ++s) {
+                        const uint32_t uses_l = it > s ? (it - 1u - s) / C::S + 1u : 0u;
+                        const uint32_t uses_p = it_p > s ? (it_p - 1u - s) / C::S + 1u : 0u;
+                        if (uses_p > uses_l)
+                            ptx::mbar_arrive_expect_tx(bar0 + 8 * (C::BAR_FULL + s), C::STAGE_BYTES);
+                    }
+                    it_all = it_p > it ? it_p : it;
+                }
+            }
             if (leader)
                 for (uint32_t s = 0; s < (uint32_t)C::S; ++s) {
-                    if (it > s) {
-                        const uint32_t last = s + ((it - 1u - s) / C::S) * C::S;
-                        bwait_drain(bar0 + 8 * (C::BAR_FULL + s), (last / C::S) & 1u, p);
+                    if (it_all > s) {
+                        const uint32_t last = s + ((it_all - 1u - s) / C::S) * C::S;
+                        bwait_drain<PAIR>(bar0 + 8 * (C::BAR_FULL + s), (last / C::S) & 1u, p);
                     }
                 }
         }
@@ -547,16 +574,22 @@ __global__ void __launch_bounds__(256, 1)
                         else
                             ptx::umma_bf16(d, ad, bd, C::IDESC, (kb | k) != 0 ? 1u : 0u);
                     }
-                    if constexpr (PAIR)
+                    if constexpr (PAIR) {
+                        // the stage is free in both CTAs once these MMAs completed:
+                        // commit to each CTA's ring barrier directly
                         ptx::umma_commit_pair(bar0 + 8 * (C::BAR_EMPTY + s));
-                    else
+                        ptx::umma_commit_pair(ptx::mapa(bar0 + 8 * (C::BAR_EMPTY + s), 1));
+                    } else {
                         ptx::umma_commit(bar0 + 8 * (C::BAR_EMPTY + s));
+                    }
                 }
                 if (!ok) break;
-                if constexpr (PAIR)
+                if constexpr (PAIR) {
                     ptx::umma_commit_pair(bar0 + 8 * (C::BAR_TFULL + acc));
-                else
+                    ptx::umma_commit_pair(ptx::mapa(bar0 + 8 * (C::BAR_TFULL + acc), 1));
+                } else {
                     ptx::umma_commit(bar0 + 8 * (C::BAR_TFULL + acc));
+                }
                 if (p.trace != nullptr) p.trace[4 * t + 1] = ptx::globaltimer();
                 ++tc;
             }
@@ -581,9 +614,6 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t tfull = bar0 + 8 * (C::BAR_TFULL + acc);
             bool ok = bwait<PAIR>(tfull, aph, abort, p);
             if (!__all_sync(0xffffffffu, ok)) break;
-            // the even CTA's MMA commit arrives only on its own barrier: forward
-            if constexpr (PAIR)
-                if (leader && warp == 2 && lane == 0) ptx::mbar_arrive_remote(ptx::mapa(tfull, 1));
             ptx::tc_fence_after();
             if (p.trace != nullptr && leader && warp == 2 && lane == 0)
                 p.trace[4 * t + 2] = ptx::globaltimer();
@@ -643,12 +673,17 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 }  // OP != OP_AG
             }
+            // release the accumulator: one arrive per warp once all its lanes'
+            // TMEM loads completed (the even CTA's MMA waits for both CTAs)
             ptx::tc_fence_before();
+            __syncwarp();
             const uint32_t tempty = bar0 + 8 * (C::BAR_TEMPTY + acc);
-            if (leader)
-                ptx::mbar_arrive(tempty);
-            else
-                ptx::mbar_arrive_remote(ptx::mapa(tempty, 0));
+            if (lane == 0) {
+                if (leader)
+                    ptx::mbar_arrive(tempty);
+                else
+                    ptx::mbar_arrive_remote(ptx::mapa(tempty, 0));
+            }
             if (p.trace != nullptr && leader && warp == 2 && lane == 0)
                 p.trace[4 * t + 3] = ptx::globaltimer();
             if (dead) break;

@@ -228,15 +228,20 @@ def test_repeated_calls_and_epochs():
             assert fin[code] == 5
 
 
+@pytest.mark.parametrize("tile_m", [128, 256])
 @pytest.mark.parametrize("backend", ["ce", "tma_dedicated", "tma_colocated"])
-def test_dropped_chunk_times_out_then_recovers(backend):
+def test_dropped_chunk_times_out_then_recovers(backend, tile_m):
+    """A staging transfer whose ready flag is never published ends the call in
+    SYN_ERR_TIMEOUT (no hang, no trap); the next plan on the same device works.
+    With tile_m 256 this also exercises the CTA pair's abort and drain path."""
     w = wl.TINY_AG
     inp = inputs(w, 0)
     d = runner.upload(inp)
-    with runner.make_plan(d, backend=backend, comm_sms=2, drop_chunk=2, timeout_ns=20_000_000) as bad:
+    with runner.make_plan(d, backend=backend, comm_sms=2, drop_chunk=2, timeout_ns=20_000_000,
+                          tile_m=tile_m) as bad:
         runner.call(bad, d)
         assert bad.sync() == syn.ERR_TIMEOUT
-    with runner.make_plan(d, backend=backend, comm_sms=2) as good:
+    with runner.make_plan(d, backend=backend, comm_sms=2, tile_m=tile_m) as good:
         runner.call(good, d)
         assert good.sync() == syn.OK
     check_against_oracle(w, 0, {"out": runner.dev_to_u16(d.out), "gathered": runner.dev_to_u16(d.gathered)})
