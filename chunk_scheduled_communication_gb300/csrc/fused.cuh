@@ -83,8 +83,12 @@ struct KCfg {
     static constexpr uint32_t B_BOX_BYTES = BK * 128;
     static constexpr int PEER_COLS = 32;
     static constexpr int PEER_BYTES = BM * PEER_COLS * 4;
-    static constexpr int NSTG = STG ? 2 : 0;
+    // co-located staging buffers: two for RS/AR (the peer ring takes the rest);
+    // for AG every 16 KiB the pipeline stages leave (up to 8), so shallower
+    // pipelines trade MMA lookahead for more staging copies in flight
     static constexpr int STG_BYTES = 16384;
+    static constexpr int NSTG_AG = (kSmemRings - S * STAGE_BYTES) / STG_BYTES;
+    static constexpr int NSTG = !STG ? 0 : OP != OP_AG ? 2 : (NSTG_AG > 8 ? 8 : NSTG_AG);
     static constexpr int P =
         OP == OP_AG ? 0 : (kSmemRings - NSTG * STG_BYTES - S * STAGE_BYTES) / PEER_BYTES;
     static_assert(OP == OP_AG || P >= 2, "peer ring needs at least two slots");
@@ -779,29 +783,24 @@ cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    int n = 1;
+    // Single CTAs: a cooperative launch, which fails rather than run a grid
+    // whose CTAs cannot all be resident.  CTA pairs: a 2-CTA cluster launch
+    // whose grid the host sized to the co-resident cluster count
+    // (cudaOccupancyMaxActiveClusters), so every CTA is resident as well; were
+    // one not, the bounded waits would end the call in SYN_ERR_TIMEOUT.
+    cudaLaunchAttribute attr[1];
     if (PAIR) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 2;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        n = 2;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+    } else {
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
     }
     cfg.attrs = attr;
-    cfg.numAttrs = n;
-    e = cudaLaunchKernelEx(&cfg, kern, p, tm);
-    if (e != cudaSuccess && PAIR) {
-        // clusters without the cooperative attribute: the grid is sized to the
-        // co-resident cluster count, so every CTA is still resident
-        (void)cudaGetLastError();
-        cfg.attrs = attr + 1;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kern, p, tm);
-    }
-    return e;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, tm);
 }
 
 // Co-resident 2-CTA clusters of one instance (0 when the query fails).
@@ -847,6 +846,7 @@ bool dispatch_cfg(const LaunchCfg &lc, Fn &&fn) {
         SYN_CFG(false, 256, 8, 32, true) SYN_CFG(false, 256, 9, 32, false)
         SYN_CFG(true, 256, 6, 64, true) SYN_CFG(true, 256, 7, 64, false)
         SYN_CFG(true, 256, 5, 64, true) SYN_CFG(true, 256, 5, 64, false)
+        SYN_CFG(true, 256, 4, 64, true)
         return false;
     } else {
         SYN_CFG(false, 256, 3, 64, true) SYN_CFG(false, 128, 4, 64, true) SYN_CFG(false, 256, 6, 32, true)

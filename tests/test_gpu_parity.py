@@ -339,7 +339,8 @@ INT_AR_PAIR = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=2 * 333, K=128, N=512, R=2)
 
 
 @pytest.mark.parametrize("w,backend,stages", [
-    (INT_AG_PAIR, "tma_colocated", 6), (INT_AG_PAIR, "tma_colocated", 5), (INT_AG_PAIR, "ce", 7),
+    (INT_AG_PAIR, "tma_colocated", 6), (INT_AG_PAIR, "tma_colocated", 5), (INT_AG_PAIR, "tma_colocated", 4),
+    (INT_AG_PAIR, "ce", 7),
     (INT_AG_PAIR, "ce", 5), (INT_AG_PAIR, "tma_dedicated", 7), (INT_AG_PAIR, "unfused", 7),
     (INT_AG_PAIR, "decomposed", 7),
     (INT_RS_PAIR, "tma_colocated_smem", 3), (INT_RS_PAIR, "tma_colocated_smem", 4),
