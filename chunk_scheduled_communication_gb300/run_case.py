@@ -1,0 +1,65 @@
+"""Run one operator on one named workload with the given knobs.
+
+    python -m chunk_scheduled_communication_gb300.run_case --op rs \
+        --backend tma_colocated_smem --tile-m 256 --stages 4 --calls 4
+
+Issues ``--calls`` back-to-back calls of the fused operator on seeded
+synthetic inputs (rank 0 of the tensor-parallel group), checks the plan's
+error word, and prints the mean call time measured with CUDA events on the
+launching stream.  It is the single-kernel case that a kernel profiler
+attaches to; the time it prints is not a benchmark figure (no L2 flush, few
+calls).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+from . import runner, workloads as wl
+
+WORKLOADS = {
+    "ag": wl.LLAMA3_8B_UP_AG,
+    "rs": wl.LLAMA3_8B_DOWN_RS,
+    "ar": wl.QWEN2_7B_DOWN_AR,
+    "ag70": wl.LLAMA3_70B_UP_AG,
+}
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--op", choices=sorted(WORKLOADS), default="ag")
+    ap.add_argument("--backend", default="tma_colocated")
+    ap.add_argument("--split", type=int, default=1)
+    ap.add_argument("--order", default="row", choices=["row", "col", "grouped"])
+    ap.add_argument("--tile-m", type=int, default=0)
+    ap.add_argument("--tile-n", type=int, default=256)
+    ap.add_argument("--tile-k", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--comm-sms", type=int, default=8)
+    ap.add_argument("--calls", type=int, default=4)
+    a = ap.parse_args(argv)
+
+    w = WORKLOADS[a.op]
+    torch.cuda.set_device(0)
+    d = runner.upload(wl.make_inputs(w, r=0), with_f32_out=(w.op == "rs"))
+    stream = torch.cuda.current_stream()
+    with runner.make_plan(d, split=a.split, order=a.order, backend=a.backend, tile_m=a.tile_m,
+                          tile_n=a.tile_n, tile_k=a.tile_k, stages=a.stages, comm_sms=a.comm_sms) as p:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(a.calls):
+            runner.call(p, d, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        p.check(stream)
+        info = p.info()
+    print(json.dumps({"workload": w.name, "backend": a.backend, "split": a.split, "order": a.order,
+                      "tile_m": info.get("tile_m", a.tile_m), "calls": a.calls,
+                      "us_per_call": e0.elapsed_time(e1) / a.calls * 1e3}), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
