@@ -465,6 +465,8 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
         pl->grid_comm = 0;
         pl->grid_compute = std::min(s.n_tiles, pl->resident / cta_per_tile) * cta_per_tile;
     }
+    if (s.op == SYN_OP_GEMM_RS && kn.backend == SYN_BACKEND_TMA_COLOCATED_SMEM && kn.reduce_spread == 0)
+        spread_reduce_tiles(pl->s, pl->grid_compute / cta_per_tile);
     const size_t n_flags = (size_t)s.n_rc * s.R;
     PL_CK(cudaMalloc(&pl->d_tiles, s.tile_list.size() * sizeof(int32_t)));
     PL_CK(cudaMalloc(&pl->d_transfers, std::max<size_t>(1, s.transfers.size()) * sizeof(int32_t)));

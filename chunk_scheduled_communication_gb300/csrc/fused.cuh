@@ -720,7 +720,7 @@ __global__ void __launch_bounds__(256, 1)
                     ptx::fence_proxy_async();
                 }
                 const int prow = r0 - p.peer_row_off;
-                for (int cc = 0; ok && cc < BN / 32; ++cc)
+                for (int cc = 0; ok && cc < BN / 32; ++cc) {
                     for (int q = 0; q < p.R; ++q) {
                         if (q == p.rank) continue;
                         const int slot = (int)(pit % C::P);
@@ -735,6 +735,7 @@ __global__ void __launch_bounds__(256, 1)
                                          tni * BN + cc * 32, prow);
                         ++pit;
                     }
+                }
             }
             for (uint32_t s = 0; s < (uint32_t)C::P; ++s) {
                 if (pit > s) {
@@ -855,6 +856,7 @@ bool dispatch_cfg(const LaunchCfg &lc, Fn &&fn) {
         SYN_CFG(false, 256, 4, 32, false) SYN_CFG(false, 256, 5, 32, false) SYN_CFG(false, 256, 6, 32, false)
         SYN_CFG(true, 256, 4, 64, true)
         SYN_CFG(true, 256, 3, 64, false) SYN_CFG(true, 256, 4, 64, false) SYN_CFG(true, 256, 5, 64, false)
+        SYN_CFG(true, 256, 6, 64, false)
         return false;
     }
 #undef SYN_CFG

@@ -24,7 +24,10 @@
 // arrival index among the chunks they consume, so the persistent grid walks
 // chunks in arrival order; ties keep the chosen intra-chunk traversal.  GEMM-RS
 // send tiles come first, ordered by destination ring position (Entwine
-// abstract: produce data for communication at a regular pace).
+// abstract: produce data for communication at a regular pace).  With resident
+// peer partials (TMA_COLOCATED_SMEM) nothing is awaited, and the GEMM-RS
+// reduce tiles are spread over the walk instead (spread_reduce_tiles), so
+// their peer reads overlap MMA work rather than arriving as one burst.
 #include "schedule.h"
 
 #include <algorithm>
@@ -209,7 +212,59 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         s.tile_list[i] = items[i].tile;
         s.tile_key[i] = items[i].key;
     }
+    if (op == SYN_OP_GEMM_RS && kn.backend == SYN_BACKEND_TMA_COLOCATED_SMEM && kn.reduce_spread > 0)
+        spread_reduce_tiles(s, kn.reduce_spread);
     return SYN_OK;
+}
+
+void spread_reduce_tiles(Schedule &s, int units) {
+    const int T = (int)s.tile_list.size();
+    if (units <= 0 || T == 0) return;
+    const int rounds = T / units;  // full rounds of the walk
+    if (rounds < 3) return;
+    std::vector<int32_t> red, red_key, snd, snd_key;
+    for (int i = 0; i < T; ++i) {
+        const int tm = s.tile_list[i] / s.tiles_n;
+        const bool is_red = ((int64_t)tm * s.tile_m) / s.M_r == s.rank;
+        (is_red ? red : snd).push_back(s.tile_list[i]);
+        (is_red ? red_key : snd_key).push_back(s.tile_key[i]);
+    }
+    const int n_red = (int)red.size();
+    if (n_red == 0) return;
+    // Walkers [T mod units, units) run one tile fewer (no entry in the partial
+    // last round): they take the first reduce tiles.  A walker's last tile is
+    // in round rounds - 1 or rounds, so reduce tiles use rounds [0, rounds - 2].
+    const int first_unit = T % units;
+    const int use_rounds = rounds - 1;
+    std::vector<int32_t> pos_tile(T, -1), pos_key(T, 0);
+    std::vector<char> taken(T, 0);
+    for (int j = 0; j < n_red; ++j) {
+        const int u = (first_unit + j) % units;
+        const int rho = (int)(((int64_t)j * use_rounds) / n_red);
+        int pos = rho * units + u;
+        // with more reduce tiles than walkers a walker's later reduce tile may
+        // land on a taken entry: take the walker's next free round, else any
+        // free entry before the last round
+        while (pos < use_rounds * units && taken[pos]) pos += units;
+        if (pos >= use_rounds * units) {
+            pos = 0;
+            while (taken[pos]) ++pos;
+        }
+        taken[pos] = 1;
+        pos_tile[pos] = red[j];
+        pos_key[pos] = red_key[j];
+    }
+    size_t k = 0;
+    for (int i = 0; i < T; ++i) {
+        if (taken[i]) {
+            s.tile_list[i] = pos_tile[i];
+            s.tile_key[i] = pos_key[i];
+        } else {
+            s.tile_list[i] = snd[k];
+            s.tile_key[i] = snd_key[k];
+            ++k;
+        }
+    }
 }
 
 }  // namespace syn

@@ -47,6 +47,16 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &layout,
                    int64_t chunk_rows, int split, syn_order_t order,
                    const syn_knobs_t &knobs, Schedule &s, std::string &err);
 
+// GEMM-RS whose peer partials are resident (TMA_COLOCATED_SMEM): every chunk
+// is available at t = 0, so the order is free to place the reduce tiles (each
+// streams R-1 peer tiles through its epilogue) where their reads overlap the
+// most MMA work.  This moves them from the head of the order into evenly
+// spaced rounds of the walk by `units` persistent tile walkers (walker u runs
+// entries u, u + units, ...), one walker each where there are enough walkers,
+// never in the last round a walker runs; the send tiles keep their order in
+// the remaining entries.  No-op when the walk has fewer than three rounds.
+void spread_reduce_tiles(Schedule &s, int units);
+
 // Chunk geometry.  Rank q's block of M_r rows is cut into `split` chunks;
 // chunk j of the block covers local rows [ceil(j*M_r/split), ceil((j+1)*M_r/split)),
 // so chunk sizes differ by at most one row when split does not divide M_r.

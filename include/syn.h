@@ -131,6 +131,15 @@ typedef struct {
     int tile_k;            /* k-block depth per pipeline stage: 64 or 32
                               (0 = 64).  32 halves each stage, so twice as
                               many fit and more loads are in flight.         */
+    int reduce_spread;     /* GEMM-RS with TMA_COLOCATED_SMEM only: where the
+                              reduce tiles (the ones that stream the resident
+                              peer partials) go in the tile order.
+                              -1 = all first; n > 0 = one per persistent tile
+                              walker of a grid of n walkers (CTAs, or CTA
+                              pairs at tile_m 256), in evenly spaced rounds;
+                              0 = default: syn_plan_create spreads them over
+                              its own grid, syn_schedule_build (which knows no
+                              grid) keeps them first.                         */
 } syn_knobs_t;
 
 /* Everything a caller or a test may want to know about a plan. */

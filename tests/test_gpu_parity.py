@@ -344,8 +344,10 @@ INT_AR_PAIR = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=2 * 333, K=128, N=512, R=2)
     (INT_AG_PAIR, "ce", 5), (INT_AG_PAIR, "tma_dedicated", 7), (INT_AG_PAIR, "unfused", 7),
     (INT_AG_PAIR, "decomposed", 7),
     (INT_RS_PAIR, "tma_colocated_smem", 3), (INT_RS_PAIR, "tma_colocated_smem", 4),
-    (INT_RS_PAIR, "tma_colocated_smem", 5), (INT_RS_PAIR, "tma_colocated", 4), (INT_RS_PAIR, "ce", 4),
-    (INT_AR_PAIR, "tma_colocated_smem", 4), (INT_AR_PAIR, "tma_colocated", 4), (INT_AR_PAIR, "ce", 3),
+    (INT_RS_PAIR, "tma_colocated_smem", 5), (INT_RS_PAIR, "tma_colocated_smem", 6),
+    (INT_RS_PAIR, "tma_colocated", 4), (INT_RS_PAIR, "ce", 4),
+    (INT_AR_PAIR, "tma_colocated_smem", 4), (INT_AR_PAIR, "tma_colocated_smem", 6),
+    (INT_AR_PAIR, "tma_colocated", 4), (INT_AR_PAIR, "ce", 3),
 ], ids=lambda v: str(getattr(v, "op", v)))
 def test_cta_pair_instances_bit_exact(w, backend, stages):
     """256-row tiles shared by a CTA pair (2-CTA UMMA) give the oracle's bits
@@ -386,6 +388,28 @@ def test_cta_pair_full_size_against_oracle(w, backend):
     check_against_oracle(w, 0, pair)
     ok, exc, frob = runner.bf16_close(pair["out"], got["out"])
     assert ok, (exc, frob)
+
+
+INT_RS_SPREAD = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=4 * 512, K=256, N=1024, R=4)   # 32 pair tiles
+
+
+@pytest.mark.parametrize("spread,stages", [(-1, 4), (4, 4), (4, 5), (3, 6), (0, 4), (2, 3)])
+def test_smem_reduce_spread_bit_exact(spread, stages):
+    """Where the GEMM-RS reduce tiles sit in the walk changes when bytes move,
+    not what is computed: integer inputs give the oracle's bits for every
+    placement and pipeline depth."""
+    w, r = INT_RS_SPREAD, 1
+    inp = inputs(w, r, 0, "int")
+    d = runner.upload(inp)
+    with runner.make_plan(d, split=1, order="row", backend="tma_colocated_smem", tile_m=256,
+                          tile_n=256, stages=stages, reduce_spread=spread) as plan:
+        for _ in range(2):
+            runner.call(plan, d)
+        assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+        tl, _, _ = plan.tables()
+    assert sorted(tl.tolist()) == list(range(len(tl)))
+    got = {"out": runner.dev_to_u16(d.out), "f32": d.f32_out.cpu().numpy()}
+    check_against_oracle(w, r, got, kind="int")
 
 
 def test_uncompiled_stage_count_is_rejected():

@@ -205,3 +205,52 @@ def test_pair_tiles_rs_needs_256_row_blocks():
     with pytest.raises(syn.SynError) as e:
         syn.schedule_build("rs", 4, 0, 4 * 384, 256, 256, tile_m=256)
     assert e.value.status == syn.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("R,r,M,N,K,tile_m,tile_n,units", [
+    (8, 3, 8192, 4096, 1792, 256, 256, 76),   # Llama-3-8B FFN down, CTA pairs
+    (8, 0, 8192, 4096, 1792, 128, 256, 152),  # same, one CTA per tile
+    (8, 5, 8192, 4096, 1792, 128, 128, 76),   # more reduce tiles than walkers
+    (4, 1, 4096, 1024, 512, 128, 256, 16),
+])
+def test_smem_rs_reduce_tiles_spread_over_walkers(R, r, M, N, K, tile_m, tile_n, units):
+    """With resident peer partials the GEMM-RS reduce tiles can go anywhere;
+    reduce_spread = units lays them out one per walker where possible, in
+    evenly filled rounds before each walker's last round, and keeps the send
+    tiles' order in the other entries."""
+    kw = dict(split=1, order="row", backend="tma_colocated_smem", tile_m=tile_m, tile_n=tile_n)
+    _, tl0, tk0, _ = syn.schedule_build("rs", R, r, M, N, K, **kw)
+    info, tl, tk, _ = syn.schedule_build("rs", R, r, M, N, K, reduce_spread=units, **kw)
+    T = info["n_tiles"]
+    assert sorted(tl.tolist()) == list(range(T))
+    tiles_n = N // tile_n
+    M_r = M // R
+    is_red = np.array([(t // tiles_n) * tile_m // M_r == r for t in tl])
+    is_red0 = np.array([(t // tiles_n) * tile_m // M_r == r for t in tl0])
+    n_red = int(is_red.sum())
+    assert is_red0[:n_red].all()                      # default: all first
+    # send tiles: same relative order as before; keys travel with their tiles
+    assert tl[~is_red].tolist() == tl0[n_red:].tolist()
+    key_of = dict(zip(tl0.tolist(), tk0.tolist()))
+    assert all(key_of[t] == k for t, k in zip(tl.tolist(), tk.tolist()))
+    pos = np.nonzero(is_red)[0]
+    rounds = T // units
+    walker, rnd = pos % units, pos // units
+    # never in a walker's last round
+    last_round = np.array([(T - 1 - w) // units for w in range(units)])
+    assert (rnd < last_round[walker]).all()
+    if n_red <= units:
+        assert len(set(walker.tolist())) == n_red      # one per walker
+    counts = np.bincount(rnd, minlength=rounds - 1)[:rounds - 1]
+    assert counts.max() - counts.min() <= 1 + n_red // units
+    # the walkers with one tile fewer take the first reduce tiles
+    short = list(range(T % units, units))
+    if n_red >= len(short) and short:
+        assert set(short) <= set(walker.tolist())
+
+
+def test_smem_rs_spread_noop_for_short_walks():
+    kw = dict(split=1, order="row", backend="tma_colocated_smem", tile_m=128, tile_n=256)
+    _, tl0, _, _ = syn.schedule_build("rs", 4, 1, 1024, 512, 256, **kw)
+    _, tl1, _, _ = syn.schedule_build("rs", 4, 1, 1024, 512, 256, reduce_spread=8, **kw)
+    assert tl0.tolist() == tl1.tolist()  # 16 tiles over 8 walkers: 2 rounds only
