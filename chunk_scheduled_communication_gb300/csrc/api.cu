@@ -117,7 +117,7 @@ struct syn_plan_s {
     int32_t *d_tiles = nullptr, *d_transfers = nullptr, *d_err = nullptr;
     uint32_t *d_in_flags = nullptr, *d_in_cnt = nullptr, *d_out_flags = nullptr, *d_out_cnt = nullptr;
     unsigned long long *d_stats = nullptr;
-    unsigned long long *d_trace = nullptr;  // trace = 2: [n_tiles][4] stamps
+    unsigned long long *d_trace = nullptr;  // trace = 2: [n_tiles][5] stamps + walker
     uint8_t *d_recv = nullptr;
     uint64_t recv_bytes = 0;
     int64_t recv_slot_rows = 0;
@@ -488,8 +488,8 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
     PL_CK(cudaMemset(pl->d_out_cnt, 0, 2 * (size_t)s.n_rc * sizeof(uint32_t)));
     PL_CK(cudaMemset(pl->d_stats, 0, 2 * sizeof(unsigned long long)));
     if (kn.trace >= 2) {
-        PL_CK(cudaMalloc(&pl->d_trace, 4 * (size_t)s.n_tiles * sizeof(unsigned long long)));
-        PL_CK(cudaMemset(pl->d_trace, 0, 4 * (size_t)s.n_tiles * sizeof(unsigned long long)));
+        PL_CK(cudaMalloc(&pl->d_trace, 5 * (size_t)s.n_tiles * sizeof(unsigned long long)));
+        PL_CK(cudaMemset(pl->d_trace, 0, 5 * (size_t)s.n_tiles * sizeof(unsigned long long)));
     }
     if (staged_peers(pl)) {
         pl->recv_slot_rows = (s.op == SYN_OP_GEMM_RS) ? s.M_r : s.M;
@@ -669,7 +669,7 @@ int syn_plan_trace(syn_plan_t plan, uint64_t *out) {
     if (plan == nullptr || out == nullptr) return fail(SYN_ERR_INVALID, "null argument");
     if (plan->d_trace == nullptr) return fail(SYN_ERR_INVALID, "plan was created without trace = 2");
     SYN_CK(cudaDeviceSynchronize());
-    SYN_CK(cudaMemcpy(out, plan->d_trace, 4 * (size_t)plan->s.n_tiles * sizeof(uint64_t),
+    SYN_CK(cudaMemcpy(out, plan->d_trace, 5 * (size_t)plan->s.n_tiles * sizeof(uint64_t),
                       cudaMemcpyDeviceToHost));
     return SYN_OK;
 }

@@ -114,6 +114,7 @@ struct KCfg {
     static constexpr int COMM_NBUF = OFF_BAR / COMM_BUF_BYTES;
     static constexpr int NBAR_ALL = NBAR > COMM_NBUF ? NBAR : COMM_NBUF;
     static constexpr int OFF_MISC = OFF_BAR + NBAR_ALL * 8;
+    // misc words: +0 TMEM base, +4 abort flag, +8 odd CTA's k-block count
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -233,6 +234,14 @@ __device__ __forceinline__ bool reduces(const KernelParams &p, int r0) {
     if (OP == OP_AR) return true;
     if (OP == OP_RS) return r0 / p.M_r == p.rank;
     return false;
+}
+
+// ------------------------------------------------------------------ tile walk
+// A walker (a CTA, or a CTA pair) runs tile-list entries one after another:
+// walker u of n runs entries u, u + n, u + 2n, ...; -1 ends the walk.
+__device__ __forceinline__ int walk_entry(const KernelParams &p, int unit, int n_units, int i) {
+    const int t = p.t_begin + unit + i * n_units;
+    return t < p.t_end ? t : -1;
 }
 
 // ------------------------------------------------------------------ staging (device backends)
@@ -459,7 +468,9 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t sA = sbase + C::OFF_A, sB = sbase + C::OFF_B;
             uint32_t it = 0;
             bool ok = true;
-            for (int t = p.t_begin + unit; ok && t < p.t_end; t += n_units) {
+            for (int i = 0; ok; ++i) {
+                const int t = walk_entry(p, unit, n_units, i);
+                if (t < 0) break;
                 const int tile = p.tile_list[t];
                 const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
                 const int r0 = tmi * C::TILE_M + (int)crank * C::BM;  // this CTA's rows
@@ -548,12 +559,17 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t sA = sbase + C::OFF_A, sB = sbase + C::OFF_B;
             uint32_t it = 0, tc = 0;
             bool ok = true;
-            for (int t = p.t_begin + unit; ok && t < p.t_end; t += n_units) {
+            for (int i = 0; ok; ++i) {
+                const int t = walk_entry(p, unit, n_units, i);
+                if (t < 0) break;
                 const int acc = (int)(tc & 1u);
                 const uint32_t aph = (tc >> 1) & 1u;
                 if (!bwait<PAIR>(bar0 + 8 * (C::BAR_TEMPTY + acc), aph ^ 1u, abort, p)) break;
                 ptx::tc_fence_after();
-                if (p.trace != nullptr) p.trace[4 * t + 0] = ptx::globaltimer();
+                if (p.trace != nullptr) {
+                    p.trace[5 * t + 0] = ptx::globaltimer();
+                    p.trace[5 * t + 4] = (unsigned long long)unit;
+                }
                 const uint32_t d = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = (int)(it % C::S);
@@ -594,7 +610,7 @@ __global__ void __launch_bounds__(256, 1)
                 } else {
                     ptx::umma_commit(bar0 + 8 * (C::BAR_TFULL + acc));
                 }
-                if (p.trace != nullptr) p.trace[4 * t + 1] = ptx::globaltimer();
+                if (p.trace != nullptr) p.trace[5 * t + 1] = ptx::globaltimer();
                 ++tc;
             }
             // every MMA this thread issued must finish before TMEM is released
@@ -610,7 +626,9 @@ __global__ void __launch_bounds__(256, 1)
         const int lrow = qd * 32 + lane;
         uint32_t tc = 0, pit = 0;
         const uint32_t sPeer = sbase + C::OFF_PEER;
-        for (int t = p.t_begin + unit; t < p.t_end; t += n_units) {
+        for (int i = 0;; ++i) {
+            const int t = walk_entry(p, unit, n_units, i);
+            if (t < 0) break;
             const int tile = p.tile_list[t];
             const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
             const int acc = (int)(tc & 1u);
@@ -620,7 +638,7 @@ __global__ void __launch_bounds__(256, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             ptx::tc_fence_after();
             if (p.trace != nullptr && leader && warp == 2 && lane == 0)
-                p.trace[4 * t + 2] = ptx::globaltimer();
+                p.trace[5 * t + 2] = ptx::globaltimer();
             const int tr0 = tmi * C::TILE_M;                       // tile's first row
             const int row = tr0 + (int)crank * C::BM + lrow;       // this thread's row
             const bool in_range = row < p.M;
@@ -689,7 +707,7 @@ __global__ void __launch_bounds__(256, 1)
                     ptx::mbar_arrive_remote(ptx::mapa(tempty, 0));
             }
             if (p.trace != nullptr && leader && warp == 2 && lane == 0)
-                p.trace[4 * t + 3] = ptx::globaltimer();
+                p.trace[5 * t + 3] = ptx::globaltimer();
             if (dead) break;
             if (OP != OP_AG && p.f32_out != nullptr && (OP == OP_AR || !red))
                 count_produced(p, tr0, C::TILE_M, C::CTAS, lane);
@@ -701,7 +719,9 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t sPeer = sbase + C::OFF_PEER;
             uint32_t pit = 0;
             bool ok = true;
-            for (int t = p.t_begin + unit; ok && t < p.t_end; t += n_units) {
+            for (int i = 0; ok; ++i) {
+                const int t = walk_entry(p, unit, n_units, i);
+                if (t < 0) break;
                 const int tile = p.tile_list[t];
                 const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
                 const int tr0 = tmi * C::TILE_M;

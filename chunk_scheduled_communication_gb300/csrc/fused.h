@@ -61,8 +61,8 @@ struct KernelParams {
     uint32_t *out_cnt;             // [2][n_rc] producer counters (epoch parity)
     int32_t *err;                  // [4] code, site, cta, info
     unsigned long long *stats;     // [2] flag-wait ns, CTA-busy ns (nullable)
-    unsigned long long *trace;     // [n_tiles][4] per tile-list entry: MMA start, MMA end
-                                   // (last commit issued), epilogue start, end (nullable)
+    unsigned long long *trace;     // [n_tiles][5] per tile-list entry: MMA start, MMA end
+                                   // (last commit issued), epilogue start, end, walker (nullable)
     const uint8_t *stage_src[kMaxRanks];  // AG: shard q; RS/AR: peer q partial
     uint8_t *stage_dst;            // AG: gathered; RS/AR: receive buffer
     int64_t row_bytes;             // bytes of one row of a transfer

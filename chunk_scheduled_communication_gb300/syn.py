@@ -232,11 +232,11 @@ class Plan:
         return a.value, b.value
 
     def trace(self):
-        """Per-tile timeline of the last call (trace=2): int64 [n_tiles, 4] of
-        (MMA start, MMA end, epilogue start, epilogue end) global-timer ns, rows
-        in tile-list order."""
+        """Per-tile timeline of the last call (trace=2): int64 [n_tiles, 5] of
+        (MMA start, MMA end, epilogue start, epilogue end) global-timer ns and
+        the walker that ran the tile, rows in tile-list order."""
         n = self.info()["n_tiles"]
-        out = np.zeros((n, 4), np.uint64)
+        out = np.zeros((n, 5), np.uint64)
         _check(self._L.syn_plan_trace(self._h, out.ctypes.data), "syn_plan_trace")
         return out.astype(np.int64)
 

@@ -119,7 +119,8 @@ typedef struct {
                               (-1 = off); the call then ends in SYN_ERR_TIMEOUT */
     int trace;             /* 1 = accumulate flag-wait and CTA-busy nanoseconds
                               (read with syn_plan_stats); 2 = also record four
-                              global-timer stamps per tile of the last call
+                              global-timer stamps and the walker per tile of
+                              the last call
                               (read with syn_plan_trace)                       */
     int stages;            /* GEMM shared-memory pipeline depth (0 = default:
                               AG 4 / RS, AR 3 at tile_n 256; 6 / 4 at 128).
@@ -258,10 +259,11 @@ int syn_plan_flags(syn_plan_t plan, uint32_t *in_flags, uint32_t *out_flags);
 int syn_plan_stats(syn_plan_t plan, uint64_t *flag_wait_ns, uint64_t *cta_busy_ns);
 
 /* Per-tile timeline of the plan's most recent call (knobs.trace = 2), as
- * global-timer nanoseconds: for tile-list entry i, out[4i+0] = the MMA issuer
- * starts the tile, out[4i+1] = its last MMA commit is issued, out[4i+2] = the
- * epilogue sees the accumulator ready, out[4i+3] = the epilogue has released
- * it.  out has 4 * n_tiles entries (host memory).  Synchronous.
+ * global-timer nanoseconds: for tile-list entry i, out[5i+0] = the MMA issuer
+ * starts the tile, out[5i+1] = its last MMA commit is issued, out[5i+2] = the
+ * epilogue sees the accumulator ready, out[5i+3] = the epilogue has released
+ * it; out[5i+4] = the index of the tile walker (CTA, or CTA pair) that ran it.
+ * out has 5 * n_tiles entries (host memory).  Synchronous.
  * SYN_ERR_INVALID if the plan was created without trace = 2. */
 int syn_plan_trace(syn_plan_t plan, uint64_t *out);
 

@@ -258,23 +258,27 @@ def test_trace_counters():
     assert busy_ns > 0 and 0 <= wait_ns <= busy_ns * 2
 
 
-def test_per_tile_trace_is_consistent():
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_per_tile_trace_is_consistent(tile_m):
     """trace=2 stamps every tile: MMA start <= MMA end <= epilogue start <=
-    epilogue end, and each CTA's tiles run in list order."""
-    w = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=8 * 256, K=512, N=1024)
+    epilogue end, and walker u runs the entries u, u + n, ... in list order."""
+    w = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=8 * 512, K=512, N=1024)
     inp = inputs(w, 0)
     d = runner.upload(inp)
-    with runner.make_plan(d, backend="tma_colocated_smem", trace=2, split=2) as plan:
+    with runner.make_plan(d, backend="tma_colocated_smem", trace=2, split=2, tile_m=tile_m) as plan:
+        runner.call(plan, d)
         runner.call(plan, d)
         assert plan.sync() == syn.OK
         tr = plan.trace()
-        G = plan.info()["grid_compute"]
-    assert (tr > 0).all()
+        units = plan.info()["grid_compute"] // (tile_m // 128)
+    assert (tr[:, :4] > 0).all()
     assert (tr[:, 0] <= tr[:, 1]).all() and (tr[:, 2] <= tr[:, 3]).all()
     assert (tr[:, 1] <= tr[:, 3]).all()
-    for c in range(G):
-        mine = tr[c::G, 0]
-        assert (np.diff(mine) >= 0).all()
+    walker = tr[:, 4]
+    for c in range(units):
+        mine = np.nonzero(walker == c)[0]
+        assert mine.tolist() == list(range(c, len(tr), units))
+        assert (np.diff(tr[mine, 0]) >= 0).all()
 
 
 def test_autotune_small_budget(tmp_path, monkeypatch):
