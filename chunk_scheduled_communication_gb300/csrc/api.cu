@@ -120,6 +120,8 @@ struct syn_plan_s {
     unsigned long long *d_trace = nullptr;  // trace = 2: [n_tiles][5] stamps + walker
     uint8_t *d_recv = nullptr;
     uint64_t recv_bytes = 0;
+    float *d_red = nullptr;                 // RED: fp32 partials of the reducing tiles
+    size_t red_bytes = 0;
     int64_t recv_slot_rows = 0;
     cudaStream_t side = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -150,6 +152,7 @@ void free_plan(syn_plan_s *pl) {
     cudaFree(pl->d_stats);
     cudaFree(pl->d_trace);
     cudaFree(pl->d_recv);
+    cudaFree(pl->d_red);
     for (cudaEvent_t e : pl->ev_transfer) cudaEventDestroy(e);
     if (pl->ev_fork) cudaEventDestroy(pl->ev_fork);
     if (pl->ev_join) cudaEventDestroy(pl->ev_join);
@@ -440,8 +443,12 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
     pl->lc.tile_k = kn.tile_k == 0 ? 64 : kn.tile_k;
     pl->lc.stg = (kn.backend == SYN_BACKEND_TMA_COLOCATED);
     pl->lc.pair = (s.tile_m == 256);
+    // resident peers: reducer warps stream the peer sum (default), or the
+    // epilogue reduces through a shared-memory peer ring
+    pl->lc.red = uses_reducer_warps(s.op, kn, s.tile_n);
     pl->lc.stages = kn.stages > 0 ? kn.stages
-                                  : default_stages(s.op, s.tile_n, pl->lc.tile_k, pl->lc.stg, pl->lc.pair);
+                                  : default_stages(s.op, s.tile_n, pl->lc.tile_k, pl->lc.stg, pl->lc.pair,
+                                                   pl->lc.red);
     pl->smem = fused_smem_bytes(s.op, pl->lc);
     if (pl->smem < 0)
         return bail(SYN_ERR_UNSUPPORTED,
@@ -466,7 +473,7 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
         pl->grid_compute = std::min(s.n_tiles, pl->resident / cta_per_tile) * cta_per_tile;
     }
     if (s.op == SYN_OP_GEMM_RS && kn.backend == SYN_BACKEND_TMA_COLOCATED_SMEM && kn.reduce_spread == 0)
-        spread_reduce_tiles(pl->s, pl->grid_compute / cta_per_tile);
+        spread_reduce_tiles(pl->s, pl->grid_compute / cta_per_tile, pl->lc.red);
     const size_t n_flags = (size_t)s.n_rc * s.R;
     PL_CK(cudaMalloc(&pl->d_tiles, s.tile_list.size() * sizeof(int32_t)));
     PL_CK(cudaMalloc(&pl->d_transfers, std::max<size_t>(1, s.transfers.size()) * sizeof(int32_t)));
@@ -490,6 +497,12 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
     if (kn.trace >= 2) {
         PL_CK(cudaMalloc(&pl->d_trace, 5 * (size_t)s.n_tiles * sizeof(unsigned long long)));
         PL_CK(cudaMemset(pl->d_trace, 0, 5 * (size_t)s.n_tiles * sizeof(unsigned long long)));
+    }
+    if (pl->lc.red && s.op == SYN_OP_GEMM_RS) {
+        // the local block's partial rows (GEMM-AR keeps them in the publish
+        // buffer, or in a buffer made on the first call without one)
+        pl->red_bytes = (size_t)s.M_r * s.N * sizeof(float);
+        PL_CK(cudaMalloc(&pl->d_red, pl->red_bytes));
     }
     if (staged_peers(pl)) {
         pl->recv_slot_rows = (s.op == SYN_OP_GEMM_RS) ? s.M_r : s.M;
@@ -598,6 +611,20 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
         p.stage_src[q] = q == s.rank ? nullptr : reinterpret_cast<const uint8_t *>(peers[q]);
     p.stage_dst = plan->d_recv;
     p.row_bytes = s.N * 4;
+    if (plan->lc.red) {
+        if (op == SYN_OP_GEMM_RS) {
+            p.red_buf = plan->d_red;
+            p.red_row_off = (int32_t)(s.rank * s.M_r);
+        } else if (f32_out != nullptr) {
+            p.red_buf = f32_out;
+        } else {
+            if (plan->d_red == nullptr) {
+                plan->red_bytes = (size_t)s.M * s.N * sizeof(float);
+                SYN_CK(cudaMalloc(&plan->d_red, plan->red_bytes));
+            }
+            p.red_buf = plan->d_red;
+        }
+    }
     p.recv_slot_rows = plan->recv_slot_rows;
     p.peer_row_off = (staged && op == SYN_OP_GEMM_RS) ? (int32_t)(s.rank * s.M_r) : 0;
     p.out = static_cast<uint16_t *>(out);

@@ -24,6 +24,11 @@
 //   warp 7      co-located stager: copies this CTA's share of chunk slices with
 //               TMA bulk copies (double-buffered) and publishes the chunk flags
 // CTAs with blockIdx.x >= G are dedicated staging CTAs (7 single-buffer copier threads).
+// RED instances (GEMM-RS/AR with resident peers) run 384 threads: the epilogue
+// stores a reducing tile's fp32 partial and frees the accumulator at once, and
+// warps 8-11 (GEMM-AR: also 6-7), joined by every other warp once its own role
+// is done, add the peer partials to it with plain coalesced loads (same
+// additions, same order, as the epilogue's own peer path).
 //
 // Two MMA shapes.  Single CTA: 128 x BN x 16 UMMAs (tcgen05 cta_group::1), each
 // CTA stages its A rows and all BN columns of B.  CTA pair (PAIR, 2-CTA
@@ -62,7 +67,7 @@ constexpr int kSmemRings = 224 * 1024;
 // whether the CTA carries the co-located staging buffers (STG), and whether
 // CTA pairs share 256-row tiles (PAIR).  For RS/AR the peer-tile ring takes
 // whatever shared memory is left.
-template <int OP, int BN, int S_, int BK_, bool STG, bool PAIR>
+template <int OP, int BN, int S_, int BK_, bool STG, bool PAIR, bool RED>
 struct KCfg {
     static constexpr int CTAS = PAIR ? 2 : 1;
     static constexpr int BM = 128, BK = BK_, UK = 16;
@@ -76,6 +81,12 @@ struct KCfg {
     static constexpr int BN_ = BN;
     static constexpr bool STG_ = STG;
     static constexpr bool PAIR_ = PAIR;
+    // RED (GEMM-RS/AR with resident peers): the epilogue only stores the fp32
+    // partial of a reducing tile and frees the accumulator; four more warps
+    // (warps 8-11) then stream the peer sum with plain loads, so no peer ring
+    // is needed and every byte of the rings goes to pipeline stages
+    static constexpr bool RED_ = RED;
+    static constexpr int NTHREADS = RED ? 384 : 256;
     // A (K-major): 8-row swizzle atoms of 8 * BK * 2 bytes
     static constexpr uint32_t A_SBO = 8 * BK * 2;
     static constexpr uint32_t A_SWZ = BK == 64 ? ptx::kSwizzle128B : ptx::kSwizzle64B;
@@ -90,8 +101,9 @@ struct KCfg {
     static constexpr int NSTG_AG = (kSmemRings - S * STAGE_BYTES) / STG_BYTES;
     static constexpr int NSTG = !STG ? 0 : OP != OP_AG ? 2 : (NSTG_AG > 8 ? 8 : NSTG_AG);
     static constexpr int P =
-        OP == OP_AG ? 0 : (kSmemRings - NSTG * STG_BYTES - S * STAGE_BYTES) / PEER_BYTES;
-    static_assert(OP == OP_AG || P >= 2, "peer ring needs at least two slots");
+        OP == OP_AG || RED ? 0 : (kSmemRings - NSTG * STG_BYTES - S * STAGE_BYTES) / PEER_BYTES;
+    static_assert(OP == OP_AG || RED || P >= 2, "peer ring needs at least two slots");
+    static_assert(!RED || (OP != OP_AG && !STG), "deferred reduction: GEMM-RS/AR, resident peers");
     static_assert(S * STAGE_BYTES + P * PEER_BYTES + NSTG * STG_BYTES <= kSmemRings, "rings");
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int OFF_A = 0;
@@ -114,8 +126,14 @@ struct KCfg {
     static constexpr int COMM_NBUF = OFF_BAR / COMM_BUF_BYTES;
     static constexpr int NBAR_ALL = NBAR > COMM_NBUF ? NBAR : COMM_NBUF;
     static constexpr int OFF_MISC = OFF_BAR + NBAR_ALL * 8;
-    // misc words: +0 TMEM base, +4 abort flag, +8 odd CTA's k-block count
-    static constexpr int SMEM_USED = OFF_MISC + 16;
+    // misc words: +0 TMEM base, +4 abort flag, +8 odd CTA's k-block count,
+    // +16 (RED) per TMEM lane quadrant: reducing tiles whose partial is stored,
+    // +32 (RED) next reduction work item, +36 (RED) 1 + the walker's reducing
+    // tiles once the epilogue has seen them all (0 before)
+    static constexpr int OFF_RED_READY = OFF_MISC + 16;
+    static constexpr int OFF_RED_NEXT = OFF_MISC + 32;
+    static constexpr int OFF_RED_TOTAL = OFF_MISC + 36;
+    static constexpr int SMEM_USED = OFF_MISC + 48;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(OFF_B % 1024 == 0 && OFF_PEER % 1024 == 0 && OFF_STG % 1024 == 0, "1 KiB atoms");
@@ -208,6 +226,43 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *flag, const KernelPara
                 raise_error(p, SYN_ERR_TIMEOUT, where, info);
                 *abort = 1;
                 return false;
+            }
+        }
+    }
+}
+
+// Acquire-wait until the shared-memory counter at `addr` reaches `want`
+// (written by another warp of this CTA with a release store): 1.  2 once the
+// word at `total` (1 + the final count, 0 while unknown) shows the counter
+// will never get there; 0 on abort or timeout.
+__device__ __forceinline__ int wait_smem_count(uint32_t addr, uint32_t total, uint32_t want,
+                                               const KernelParams &p, volatile int *abort) {
+    auto state = [&]() -> int {
+        if ((int32_t)(ptx::ld_acquire_cta_shared(addr) - want) >= 0) return 1;
+        const uint32_t tot = ptx::ld_acquire_cta_shared(total);
+        return (tot != 0u && want > tot - 1u) ? 2 : -1;
+    };
+    int st = state();
+    if (st >= 0) return st;
+    const uint64_t t0 = ptx::globaltimer();
+    const uint64_t limit = p.timeout_ns * 4ull + 200000000ull;
+    // back off up to ~1 us: a waiting warp must not take issue slots from the
+    // MMA issuer and the epilogue of its SM for the whole walk
+    uint32_t sleep_ns = 32;
+    for (uint32_t n = 1;; ++n) {
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 1024u) sleep_ns *= 2u;
+        if ((st = state()) >= 0) return st;
+        if (*abort) return 0;
+        if ((n & 31u) == 0u) {
+            if (grid_failed(p)) {
+                *abort = 1;
+                return 0;
+            }
+            if (ptx::globaltimer() - t0 > limit) {
+                raise_error(p, SYN_ERR_TIMEOUT, WHERE_PIPE, (int)want);
+                *abort = 1;
+                return 0;
             }
         }
     }
@@ -373,11 +428,109 @@ __device__ __forceinline__ void count_produced(const KernelParams &p, int r0, in
     }
 }
 
+// Deferred reduction of ROWS rows x BN columns starting at (row0, col0): out =
+// bf16(((P + peer_q0) + peer_q1) + ...) over q != rank ascending, P the fp32
+// partial the epilogue stored in red_buf -- the same additions in the same
+// order as the epilogue's own peer path.  One warp; lane l takes columns
+// 4l..4l+3 of every 128-column half, so every load and store of the warp is
+// one contiguous row segment, and U rows x all sources are in flight at once.
+template <int OP, int BN, int ROWS>
+__device__ __forceinline__ void reduce_rows(const KernelParams &p, int row0, int col0, int lane) {
+    constexpr int H = BN / 128;
+    constexpr int U = 2;
+    static_assert(ROWS % U == 0, "rows per pass");
+    const int64_t N = p.N;
+#pragma unroll 1
+    for (int rr = 0; rr < ROWS; rr += U) {
+        float4 acc[U][H];
+        float4 pv[kMaxRanks][U][H];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int row = row0 + rr + u;
+            const bool live = row < p.M;
+            const float *src = p.red_buf + (int64_t)(row - p.red_row_off) * N + col0 + 4 * lane;
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                acc[u][h] = live ? ptx::ld_f4(src + 128 * h) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < kMaxRanks; ++q)
+                    if (live && q < p.R && q != p.rank)
+                        pv[q][u][h] = ptx::ld_nc_f4(reinterpret_cast<const float *>(p.stage_src[q]) +
+                                                    (int64_t)row * N + col0 + 4 * lane + 128 * h);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int row = row0 + rr + u;
+            if (row >= p.M) continue;
+            const int orow = OP == OP_RS ? row - p.rank * p.M_r : row;
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+                float4 a = acc[u][h];
+#pragma unroll
+                for (int q = 0; q < kMaxRanks; ++q)
+                    if (q < p.R && q != p.rank) {
+                        a.x = a.x + pv[q][u][h].x;
+                        a.y = a.y + pv[q][u][h].y;
+                        a.z = a.z + pv[q][u][h].z;
+                        a.w = a.w + pv[q][u][h].w;
+                    }
+                ptx::st_u32x2(p.out + (int64_t)orow * N + col0 + 4 * lane + 128 * h,
+                              pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+            }
+        }
+    }
+}
+
+// The CTA's reduction work (RED), shared by every warp that has nothing else
+// to do: item k is row group k % 4 (8 rows) of TMEM lane quadrant (k / 4) % 4
+// of the walker's (k / 16)-th reducing tile, in this CTA's rows.  Warps claim
+// items in order from a shared-memory counter; an item starts once the
+// epilogue warp of its quadrant has stored that tile's partial.  Warps 6-11
+// work from the start, the epilogue, producer and MMA warps join when their
+// own work is done, so the reduction that outlasts the MMAs runs on all twelve.
+template <class C, int OP, int BN>
+__device__ __forceinline__ void reduce_worker(const KernelParams &p, uint8_t *sm, uint32_t sbase, int unit,
+                                              int n_units, uint32_t crank, int lane, volatile int *abort) {
+    // two rows per item (one pass of reduce_rows): the finest split measured
+    // fastest (items of 32 / 8 / 4 / 2 rows: GEMM-RS 135 / 106 / 105 / 104 us,
+    // GEMM-AR 117 / 117 / 116.5 / 113.5 us on the FFN shapes)
+    constexpr int RG = 2;
+    constexpr int PER_Q = 32 / RG;
+    constexpr int PER_TILE = 4 * PER_Q;
+    uint32_t *next = reinterpret_cast<uint32_t *>(sm + C::OFF_RED_NEXT);
+    int scan_i = 0, scan_j = -1, cur_t = -1;  // cursor over this walker's reducing tiles
+    for (;;) {
+        uint32_t k = 0;
+        if (lane == 0) k = atomicAdd(next, 1u);
+        k = __shfl_sync(0xffffffffu, k, 0);
+        const int j = (int)(k / PER_TILE), q = (int)(k / PER_Q) % 4, g = (int)(k % PER_Q);
+        int st = 1;
+        if (lane == 0)
+            st = wait_smem_count(sbase + C::OFF_RED_READY + 4 * q, sbase + C::OFF_RED_TOTAL, (uint32_t)(j + 1),
+                                 p, abort);
+        __syncwarp();  // orders lane 0's acquire before every lane's loads
+        st = __shfl_sync(0xffffffffu, st, 0);
+        if (st != 1) return;  // aborted, or the walk has no j-th reducing tile
+        while (scan_j < j) {
+            const int t = walk_entry(p, unit, n_units, scan_i++);
+            if (t < 0) return;  // (cannot happen: the epilogue stored tile j)
+            if (reduces<OP>(p, (p.tile_list[t] / p.tiles_n) * C::TILE_M)) {
+                ++scan_j;
+                cur_t = t;
+            }
+        }
+        const int tile = p.tile_list[cur_t];
+        const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
+        reduce_rows<OP, BN, RG>(p, tmi * C::TILE_M + (int)crank * C::BM + q * 32 + g * RG, tni * BN, lane);
+    }
+}
+
 // ------------------------------------------------------------------ the kernel
-template <int OP, int BN, int S, int BK, bool STG, bool PAIR>
-__global__ void __launch_bounds__(256, 1)
+template <int OP, int BN, int S, int BK, bool STG, bool PAIR, bool RED>
+__global__ void __launch_bounds__(RED ? 384 : 256, 1)
     syn_fused_kernel(const __grid_constant__ KernelParams p, const __grid_constant__ TensorMaps tm) {
-    using C = KCfg<OP, BN, S, BK, STG, PAIR>;
+    using C = KCfg<OP, BN, S, BK, STG, PAIR, RED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -418,6 +571,12 @@ __global__ void __launch_bounds__(256, 1)
     // ---- GEMM CTA set-up ---------------------------------------------------
     if (threadIdx.x == 0) {
         *abort = 0;
+        if constexpr (RED) {
+            for (int q = 0; q < 4; ++q)
+                reinterpret_cast<volatile uint32_t *>(sm + C::OFF_RED_READY)[q] = 0u;
+            *reinterpret_cast<volatile uint32_t *>(sm + C::OFF_RED_NEXT) = 0u;
+            *reinterpret_cast<volatile uint32_t *>(sm + C::OFF_RED_TOTAL) = 0u;
+        }
         for (int s = 0; s < C::S; ++s) {
             ptx::mbar_init(bar0 + 8 * (C::BAR_FULL + s), 1);
             ptx::mbar_init(bar0 + 8 * (C::BAR_EMPTY + s), 1);
@@ -624,7 +783,7 @@ __global__ void __launch_bounds__(256, 1)
         // ================= epilogue =================
         const int qd = warp & 3;  // TMEM lane quadrant this warp may access
         const int lrow = qd * 32 + lane;
-        uint32_t tc = 0, pit = 0;
+        uint32_t tc = 0, pit = 0, red_done = 0;
         const uint32_t sPeer = sbase + C::OFF_PEER;
         for (int i = 0;; ++i) {
             const int t = walk_entry(p, unit, n_units, i);
@@ -660,6 +819,12 @@ __global__ void __launch_bounds__(256, 1)
                 } else {
                 if (p.f32_out != nullptr && in_range && (OP == OP_AR || !red))
                     store_f32_row32(p.f32_out + (int64_t)row * p.N + col, f);
+                if constexpr (RED) {
+                    // the reducer warps add the peers to the stored partial
+                    if (red && in_range && p.red_buf != p.f32_out)
+                        store_f32_row32(p.red_buf + (int64_t)(row - p.red_row_off) * p.N + col, f);
+                    continue;
+                } else {
                 if (!red) continue;
                 for (int q = 0; q < p.R; ++q) {
                     if (q == p.rank) continue;
@@ -693,6 +858,7 @@ __global__ void __launch_bounds__(256, 1)
                     const int orow = OP == OP_RS ? row - p.rank * p.M_r : row;
                     store_bf16_row32(p.out + (int64_t)orow * p.N + col, f);
                 }
+                }  // !RED
                 }  // OP != OP_AG
             }
             // release the accumulator: one arrive per warp once all its lanes'
@@ -709,13 +875,30 @@ __global__ void __launch_bounds__(256, 1)
             if (p.trace != nullptr && leader && warp == 2 && lane == 0)
                 p.trace[5 * t + 3] = ptx::globaltimer();
             if (dead) break;
+            if constexpr (RED) {
+                if (red) {
+                    // this quadrant's rows of the partial are stored: hand them to
+                    // the reducer warp of the same quadrant
+                    __threadfence_block();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ++red_done;
+                        ptx::st_release_cta_shared(sbase + C::OFF_RED_READY + 4 * qd, red_done);
+                    }
+                }
+            }
             if (OP != OP_AG && p.f32_out != nullptr && (OP == OP_AR || !red))
                 count_produced(p, tr0, C::TILE_M, C::CTAS, lane);
             ++tc;
         }
+        if constexpr (RED) {
+            // every reducing tile of the walk has been seen (or the CTA aborted)
+            __syncwarp();
+            if (lane == 0) ptx::st_release_cta_shared(sbase + C::OFF_RED_TOTAL, red_done + 1u);
+        }
     } else if (warp == 6) {
         // ================= peer loader (GEMM-RS / GEMM-AR) =================
-        if constexpr (OP != OP_AG) if (lane == 0) {
+        if constexpr (OP != OP_AG && !RED) if (lane == 0) {
             const uint32_t sPeer = sbase + C::OFF_PEER;
             uint32_t pit = 0;
             bool ok = true;
@@ -764,7 +947,7 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
         }
-    } else {
+    } else if (warp == 7) {
         // ================= co-located stager =================
         if constexpr (C::NSTG > 0)
             // one copier per CTA, double-buffered: with one worker per GEMM CTA the
@@ -772,6 +955,17 @@ __global__ void __launch_bounds__(256, 1)
             if (p.colocated && lane == 0)
                 stage_slices(p, (int)blockIdx.x, p.G, sbase + C::OFF_STG, C::NSTG, C::STG_BYTES,
                              bar0 + 8 * C::BAR_STG, abort);
+    }
+    // ================= reducers (RED) =================
+    // warps 8-11 from the start, the others once their own role is done.
+    // Warps 6-7 have no role here: GEMM-AR, whose reduction outlasts the MMAs,
+    // puts them to work at once; GEMM-RS, whose few reducing tiles run early
+    // beside MMAs that need the memory system, keeps them out.
+    if constexpr (RED) {
+        if (OP == OP_AR || (warp != 6 && warp != 7)) {
+            __syncwarp();
+            reduce_worker<C, OP, BN>(p, sm, sbase, unit, n_units, crank, lane, abort);
+        }
     }
 
     // ---- teardown -----------------------------------------------------------
@@ -792,16 +986,16 @@ __global__ void __launch_bounds__(256, 1)
         atomicAdd(p.stats + 1, (unsigned long long)(ptx::globaltimer() - t_start));
 }
 
-template <int OP, int BN, int S, int BK, bool STG, bool PAIR>
+template <int OP, int BN, int S, int BK, bool STG, bool PAIR, bool RED>
 cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid, cudaStream_t st) {
-    using C = KCfg<OP, BN, S, BK, STG, PAIR>;
-    auto kern = syn_fused_kernel<OP, BN, S, BK, STG, PAIR>;
+    using C = KCfg<OP, BN, S, BK, STG, PAIR, RED>;
+    auto kern = syn_fused_kernel<OP, BN, S, BK, STG, PAIR, RED>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(C::NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cfg.stream = st;
     // Single CTAs: a cooperative launch, which fails rather than run a grid
@@ -825,16 +1019,16 @@ cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid
 }
 
 // Co-resident 2-CTA clusters of one instance (0 when the query fails).
-template <int OP, int BN, int S, int BK, bool STG, bool PAIR>
+template <int OP, int BN, int S, int BK, bool STG, bool PAIR, bool RED>
 int max_clusters_t() {
-    using C = KCfg<OP, BN, S, BK, STG, PAIR>;
-    auto kern = syn_fused_kernel<OP, BN, S, BK, STG, PAIR>;
+    using C = KCfg<OP, BN, S, BK, STG, PAIR, RED>;
+    auto kern = syn_fused_kernel<OP, BN, S, BK, STG, PAIR, RED>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(C::NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -852,15 +1046,16 @@ int max_clusters_t() {
 }
 
 // Every compiled kernel instance, per operator: (tile_m, tile_n, stages,
-// tile_k, stg).  tile_m 256 is the CTA-pair kernel.  `Fn` receives the KCfg
-// type; returns false when the combination is not compiled.
+// tile_k, stg, red).  tile_m 256 is the CTA-pair kernel.  `Fn` receives the
+// KCfg type; returns false when the combination is not compiled.
 template <int OP, typename Fn>
 bool dispatch_cfg(const LaunchCfg &lc, Fn &&fn) {
     const int tn = lc.tile_n, st = lc.stages, tk = lc.tile_k;
-    const bool g = lc.stg, pr = lc.pair;
-#define SYN_CFG(PR, TN, ST, TK, G)                                                 \
-    if (pr == PR && tn == TN && st == ST && tk == TK && g == G)                    \
-        return fn(KCfg<OP, TN, ST, TK, G, PR>{}), true;
+    const bool g = lc.stg, pr = lc.pair, rd = lc.red;
+#define SYN_CFG_R(PR, TN, ST, TK, G, RD)                                           \
+    if (pr == PR && tn == TN && st == ST && tk == TK && g == G && rd == RD)        \
+        return fn(KCfg<OP, TN, ST, TK, G, PR, RD>{}), true;
+#define SYN_CFG(PR, TN, ST, TK, G) SYN_CFG_R(PR, TN, ST, TK, G, false)
     if constexpr (OP == OP_AG) {
         SYN_CFG(false, 256, 4, 64, true) SYN_CFG(false, 256, 4, 64, false)
         SYN_CFG(false, 128, 6, 64, true) SYN_CFG(false, 128, 6, 64, false)
@@ -877,9 +1072,14 @@ bool dispatch_cfg(const LaunchCfg &lc, Fn &&fn) {
         SYN_CFG(true, 256, 4, 64, true)
         SYN_CFG(true, 256, 3, 64, false) SYN_CFG(true, 256, 4, 64, false) SYN_CFG(true, 256, 5, 64, false)
         SYN_CFG(true, 256, 6, 64, false)
+        SYN_CFG_R(false, 256, 4, 64, false, true)
+        SYN_CFG_R(true, 256, 4, 64, false, true)
+        SYN_CFG_R(true, 256, 5, 64, false, true) SYN_CFG_R(true, 256, 6, 64, false, true)
+        SYN_CFG_R(true, 256, 7, 64, false, true)
         return false;
     }
 #undef SYN_CFG
+#undef SYN_CFG_R
 }
 
 template <int OP>
@@ -888,7 +1088,7 @@ cudaError_t launch_op(const KernelParams &p, const TensorMaps &tm, const LaunchC
     cudaError_t err = cudaErrorInvalidValue;
     dispatch_cfg<OP>(lc, [&](auto c) {
         using C = decltype(c);
-        err = launch_fused_t<OP, C::BN_, C::S, C::BK, C::STG_, C::PAIR_>(p, tm, lc.grid, st);
+        err = launch_fused_t<OP, C::BN_, C::S, C::BK, C::STG_, C::PAIR_, C::RED_>(p, tm, lc.grid, st);
     });
     return err;
 }
@@ -905,7 +1105,7 @@ int max_clusters_op(const LaunchCfg &lc) {
     int n = 0;
     dispatch_cfg<OP>(lc, [&](auto c) {
         using C = decltype(c);
-        if constexpr (C::PAIR_) n = max_clusters_t<OP, C::BN_, C::S, C::BK, C::STG_, C::PAIR_>();
+        if constexpr (C::PAIR_) n = max_clusters_t<OP, C::BN_, C::S, C::BK, C::STG_, C::PAIR_, C::RED_>();
     });
     return n;
 }

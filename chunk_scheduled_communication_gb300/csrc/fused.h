@@ -69,6 +69,8 @@ struct KernelParams {
     int64_t recv_slot_rows;        // RS/AR: rows per peer slot of the receive buffer
     uint16_t *out;                 // AG: C; RS: out_r; AR: out   (bf16)
     float *f32_out;                // RS: send; AR: publish  (nullable)
+    float *red_buf;                // RED instances: fp32 partials of the reducing tiles,
+    int32_t red_row_off;           // row r stored at row r - red_row_off
 };
 
 // Receive-buffer slot of source rank q (the local rank has none).
@@ -103,6 +105,7 @@ struct LaunchCfg {
     bool stg;     // CTA carries the co-located staging buffers
     bool pair;    // 2-CTA clusters share 256-row tiles (tile_m 256)
     int grid;     // CTAs
+    bool red = false;  // RS/AR, resident peers: reducer warps stream the peer sum
 };
 
 // Host launchers (one translation unit per operator).  cudaErrorInvalidValue
@@ -115,8 +118,9 @@ cudaError_t launch_fused_ar(const KernelParams &p, const TensorMaps &tm, const L
                             cudaStream_t st);
 // Dynamic shared memory of a combination (-1 if not compiled).
 int fused_smem_bytes(int op, const LaunchCfg &lc);
-// Default pipeline depth of a (tile_n, tile_k, stg) choice.
-inline int default_stages(int op, int tile_n, int tile_k, bool stg, bool pair) {
+// Default pipeline depth of a (tile_n, tile_k, stg, pair, red) choice.
+inline int default_stages(int op, int tile_n, int tile_k, bool stg, bool pair, bool red = false) {
+    if (red) return pair ? (op == OP_AR ? 5 : 6) : 4;
     if (pair) return op == OP_AG ? (stg ? 6 : 7) : 4;
     if (tile_k == 32) return op == OP_AG ? (stg ? 8 : 9) : 6;
     if (op == OP_AG) return tile_n == 256 ? 4 : 6;

@@ -213,11 +213,11 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         s.tile_key[i] = items[i].key;
     }
     if (op == SYN_OP_GEMM_RS && kn.backend == SYN_BACKEND_TMA_COLOCATED_SMEM && kn.reduce_spread > 0)
-        spread_reduce_tiles(s, kn.reduce_spread);
+        spread_reduce_tiles(s, kn.reduce_spread, uses_reducer_warps(op, kn, tile_n));
     return SYN_OK;
 }
 
-void spread_reduce_tiles(Schedule &s, int units) {
+void spread_reduce_tiles(Schedule &s, int units, bool early) {
     const int T = (int)s.tile_list.size();
     if (units <= 0 || T == 0) return;
     const int rounds = T / units;  // full rounds of the walk
@@ -233,9 +233,10 @@ void spread_reduce_tiles(Schedule &s, int units) {
     if (n_red == 0) return;
     // Walkers [T mod units, units) run one tile fewer (no entry in the partial
     // last round): they take the first reduce tiles.  A walker's last tile is
-    // in round rounds - 1 or rounds, so reduce tiles use rounds [0, rounds - 2].
+    // in round rounds - 1 or rounds, so reduce tiles use rounds [0, rounds - 2]
+    // (early: the first half of those).
     const int first_unit = T % units;
-    const int use_rounds = rounds - 1;
+    const int use_rounds = early ? std::max(1, (rounds - 1) / 2) : rounds - 1;
     std::vector<int32_t> pos_tile(T, -1), pos_key(T, 0);
     std::vector<char> taken(T, 0);
     for (int j = 0; j < n_red; ++j) {

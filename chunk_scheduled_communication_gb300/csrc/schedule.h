@@ -55,7 +55,17 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &layout,
 // entries u, u + units, ...), one walker each where there are enough walkers,
 // never in the last round a walker runs; the send tiles keep their order in
 // the remaining entries.  No-op when the walk has fewer than three rounds.
-void spread_reduce_tiles(Schedule &s, int units);
+// `early`: with reducer warps the walker's epilogue is short and the reducer
+// streams the peers afterwards, so the reduce tiles go into the first half of
+// the rounds, leaving the reducers the rest of the walk to finish.
+void spread_reduce_tiles(Schedule &s, int units, bool early);
+
+// Whether a GEMM-RS/AR plan reduces resident peers with reducer warps (the
+// default for TMA_COLOCATED_SMEM at tile_n 256, tile_k 64).
+inline bool uses_reducer_warps(int op, const syn_knobs_t &kn, int tile_n) {
+    return op != SYN_OP_AG_GEMM && kn.backend == SYN_BACKEND_TMA_COLOCATED_SMEM &&
+           kn.reduce_warps >= 0 && tile_n == 256 && (kn.tile_k == 0 || kn.tile_k == 64);
+}
 
 // Chunk geometry.  Rank q's block of M_r rows is cut into `split` chunks;
 // chunk j of the block covers local rows [ceil(j*M_r/split), ceil((j+1)*M_r/split)),

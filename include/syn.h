@@ -141,6 +141,18 @@ typedef struct {
                               0 = default: syn_plan_create spreads them over
                               its own grid, syn_schedule_build (which knows no
                               grid) keeps them first.                         */
+    int reduce_warps;      /* GEMM-RS/AR with TMA_COLOCATED_SMEM, tile_n 256,
+                              tile_k 64: 0 = default: the epilogue stores each
+                              reducing tile's fp32 partial and frees the
+                              accumulator at once, and four extra warps per CTA
+                              add the peer partials with plain loads (GEMM-RS:
+                              the plan holds a (M/R) x N fp32 buffer for the
+                              local block; GEMM-AR: the partial goes to
+                              `publish`, or to a M x N fp32 buffer the plan
+                              makes on the first call without one).  Same
+                              additions in the same order as -1, bit for bit.
+                              -1 = the epilogue adds the peers itself through a
+                              shared-memory ring of peer tiles.              */
 } syn_knobs_t;
 
 /* Everything a caller or a test may want to know about a plan. */

@@ -301,7 +301,7 @@ def test_smem_peer_ring_depths_bit_exact(w, tile_n, stages):
     inp = inputs(w, 1, 0, "int")
     d = runner.upload(inp)
     with runner.make_plan(d, split=2, order="row", backend="tma_colocated_smem", tile_n=tile_n,
-                          stages=stages) as plan:
+                          stages=stages, reduce_warps=-1) as plan:
         runner.call(plan, d)
         runner.call(plan, d)
         assert plan.sync() == syn.OK
@@ -347,20 +347,29 @@ INT_AR_PAIR = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=2 * 333, K=128, N=512, R=2)
     (INT_AG_PAIR, "ce", 7),
     (INT_AG_PAIR, "ce", 5), (INT_AG_PAIR, "tma_dedicated", 7), (INT_AG_PAIR, "unfused", 7),
     (INT_AG_PAIR, "decomposed", 7),
-    (INT_RS_PAIR, "tma_colocated_smem", 3), (INT_RS_PAIR, "tma_colocated_smem", 4),
-    (INT_RS_PAIR, "tma_colocated_smem", 5), (INT_RS_PAIR, "tma_colocated_smem", 6),
+    (INT_RS_PAIR, "smem_ring", 3), (INT_RS_PAIR, "smem_ring", 4),
+    (INT_RS_PAIR, "smem_ring", 5), (INT_RS_PAIR, "smem_ring", 6),
+    (INT_RS_PAIR, "tma_colocated_smem", 4), (INT_RS_PAIR, "tma_colocated_smem", 5),
+    (INT_RS_PAIR, "tma_colocated_smem", 6), (INT_RS_PAIR, "tma_colocated_smem", 7),
     (INT_RS_PAIR, "tma_colocated", 4), (INT_RS_PAIR, "ce", 4),
-    (INT_AR_PAIR, "tma_colocated_smem", 4), (INT_AR_PAIR, "tma_colocated_smem", 6),
+    (INT_AR_PAIR, "smem_ring", 4), (INT_AR_PAIR, "smem_ring", 6),
+    (INT_AR_PAIR, "tma_colocated_smem", 4), (INT_AR_PAIR, "tma_colocated_smem", 5),
+    (INT_AR_PAIR, "tma_colocated_smem", 6), (INT_AR_PAIR, "tma_colocated_smem", 7),
     (INT_AR_PAIR, "tma_colocated", 4), (INT_AR_PAIR, "ce", 3),
 ], ids=lambda v: str(getattr(v, "op", v)))
 def test_cta_pair_instances_bit_exact(w, backend, stages):
     """256-row tiles shared by a CTA pair (2-CTA UMMA) give the oracle's bits
-    on integer inputs, for every compiled pair instance and both ranks' ends."""
+    on integer inputs, for every compiled pair instance and both ranks' ends
+    ("smem_ring": resident peers reduced by the epilogue through the
+    shared-memory peer ring instead of the reducer warps)."""
+    extra = {}
+    if backend == "smem_ring":
+        backend, extra = "tma_colocated_smem", {"reduce_warps": -1}
     for r in (0, w.R - 1):
         inp = inputs(w, r, 0, "int")
         d = runner.upload(inp)
         with runner.make_plan(d, split=2, order="row", backend=backend, tile_m=256, tile_n=256,
-                              stages=stages, comm_sms=4) as plan:
+                              stages=stages, comm_sms=4, **extra) as plan:
             runner.call(plan, d)
             runner.call(plan, d)
             assert plan.sync() == syn.OK, syn.lib().syn_last_error()
@@ -397,16 +406,18 @@ def test_cta_pair_full_size_against_oracle(w, backend):
 INT_RS_SPREAD = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=4 * 512, K=256, N=1024, R=4)   # 32 pair tiles
 
 
-@pytest.mark.parametrize("spread,stages", [(-1, 4), (4, 4), (4, 5), (3, 6), (0, 4), (2, 3)])
-def test_smem_reduce_spread_bit_exact(spread, stages):
+@pytest.mark.parametrize("spread,stages,reduce_warps", [
+    (-1, 6, 0), (4, 5, 0), (3, 7, 0), (0, 6, 0), (0, 4, 0), (-1, 4, -1), (4, 4, -1), (2, 3, -1)])
+def test_smem_reduce_spread_bit_exact(spread, stages, reduce_warps):
     """Where the GEMM-RS reduce tiles sit in the walk changes when bytes move,
     not what is computed: integer inputs give the oracle's bits for every
-    placement and pipeline depth."""
+    placement, pipeline depth and reduction path."""
     w, r = INT_RS_SPREAD, 1
     inp = inputs(w, r, 0, "int")
     d = runner.upload(inp)
     with runner.make_plan(d, split=1, order="row", backend="tma_colocated_smem", tile_m=256,
-                          tile_n=256, stages=stages, reduce_spread=spread) as plan:
+                          tile_n=256, stages=stages, reduce_spread=spread,
+                          reduce_warps=reduce_warps) as plan:
         for _ in range(2):
             runner.call(plan, d)
         assert plan.sync() == syn.OK, syn.lib().syn_last_error()
@@ -414,6 +425,44 @@ def test_smem_reduce_spread_bit_exact(spread, stages):
     assert sorted(tl.tolist()) == list(range(len(tl)))
     got = {"out": runner.dev_to_u16(d.out), "f32": d.f32_out.cpu().numpy()}
     check_against_oracle(w, r, got, kind="int")
+
+
+@pytest.mark.parametrize("w", [wl.LLAMA3_8B_DOWN_RS, wl.QWEN2_7B_DOWN_AR], ids=["rs", "ar"])
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_reducer_warps_bit_identical_to_epilogue_ring(w, tile_m):
+    """Full size, normal inputs: the reducer warps make the same additions in
+    the same order as the epilogue's peer ring, so every output bit matches;
+    and both stay within tolerance of the oracle."""
+    outs = []
+    for rw in (0, -1):
+        inp = inputs(w, 0)
+        d = runner.upload(inp)
+        with runner.make_plan(d, split=1, order="row", backend="tma_colocated_smem", tile_m=tile_m,
+                              reduce_warps=rw) as plan:
+            runner.call(plan, d)
+            runner.call(plan, d)
+            assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+        outs.append({"out": runner.dev_to_u16(d.out), "f32": d.f32_out.cpu().numpy()})
+    assert (outs[0]["out"] == outs[1]["out"]).all()
+    keep = np.ones(w.M, bool)
+    if w.op == "rs":
+        keep[:w.M_r] = False
+    assert (outs[0]["f32"][keep] == outs[1]["f32"][keep]).all()
+    check_against_oracle(w, 0, outs[0])
+
+
+def test_reducer_warps_ar_without_publish():
+    """GEMM-AR with no publish buffer: the plan keeps the partials in a buffer
+    of its own, made on the first such call, and the output is unchanged."""
+    w, r = INT_AR_PAIR, 1
+    inp = inputs(w, r, 0, "int")
+    d = runner.upload(inp, with_f32_out=False)
+    with runner.make_plan(d, split=1, order="row", backend="tma_colocated_smem", tile_m=256,
+                          tile_n=256) as plan:
+        for _ in range(3):
+            runner.call(plan, d)
+        assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+    check_against_oracle(w, r, {"out": runner.dev_to_u16(d.out)}, kind="int")
 
 
 def test_uncompiled_stage_count_is_rejected():

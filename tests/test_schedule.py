@@ -213,12 +213,15 @@ def test_pair_tiles_rs_needs_256_row_blocks():
     (8, 5, 8192, 4096, 1792, 128, 128, 76),   # more reduce tiles than walkers
     (4, 1, 4096, 1024, 512, 128, 256, 16),
 ])
-def test_smem_rs_reduce_tiles_spread_over_walkers(R, r, M, N, K, tile_m, tile_n, units):
+@pytest.mark.parametrize("reduce_warps", [0, -1])
+def test_smem_rs_reduce_tiles_spread_over_walkers(R, r, M, N, K, tile_m, tile_n, units, reduce_warps):
     """With resident peer partials the GEMM-RS reduce tiles can go anywhere;
     reduce_spread = units lays them out one per walker where possible, in
-    evenly filled rounds before each walker's last round, and keeps the send
-    tiles' order in the other entries."""
-    kw = dict(split=1, order="row", backend="tma_colocated_smem", tile_m=tile_m, tile_n=tile_n)
+    evenly filled rounds before each walker's last round (with reducer warps:
+    the first half of those rounds), and keeps the send tiles' order in the
+    other entries."""
+    kw = dict(split=1, order="row", backend="tma_colocated_smem", tile_m=tile_m, tile_n=tile_n,
+              reduce_warps=reduce_warps)
     _, tl0, tk0, _ = syn.schedule_build("rs", R, r, M, N, K, **kw)
     info, tl, tk, _ = syn.schedule_build("rs", R, r, M, N, K, reduce_spread=units, **kw)
     T = info["n_tiles"]
@@ -241,7 +244,11 @@ def test_smem_rs_reduce_tiles_spread_over_walkers(R, r, M, N, K, tile_m, tile_n,
     assert (rnd < last_round[walker]).all()
     if n_red <= units:
         assert len(set(walker.tolist())) == n_red      # one per walker
-    counts = np.bincount(rnd, minlength=rounds - 1)[:rounds - 1]
+    early = reduce_warps == 0 and tile_n == 256
+    use_rounds = max(1, (rounds - 1) // 2) if early else rounds - 1
+    if n_red <= units * use_rounds:
+        assert (rnd < use_rounds).all()
+    counts = np.bincount(rnd, minlength=use_rounds)[:use_rounds]
     assert counts.max() - counts.min() <= 1 + n_red // units
     # the walkers with one tile fewer take the first reduce tiles
     short = list(range(T % units, units))
