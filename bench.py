@@ -48,8 +48,8 @@ STEP = [wl.LLAMA3_8B_UP_AG, wl.LLAMA3_8B_DOWN_RS, wl.QWEN2_7B_DOWN_AR]
 # AG staged by the co-located TMA warps, RS/AR peers fetched per tile).
 DEFAULT_KNOBS = {
     "ag": dict(backend="tma_colocated", split=4, order="grouped", tile_m=256, tile_n=256, comm_sms=8, stages=0),
-    "rs": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=4),
-    "ar": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=4),
+    "rs": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=6),
+    "ar": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=5),
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -58,7 +58,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def algorithmic_bytes(w: wl.Workload, with_send=True) -> float:
     """Bytes the method must move through this HBM (each operand read once,
     each output written once; AG: staged peer shards read + written; RS/AR:
-    each peer byte read once; RS: the fp32 send rows)."""
+    each peer byte read once; RS: the fp32 send rows; AR: the fp32 publish of
+    the local partial, which the peers pull)."""
     M, N, K, R = w.M, w.N, w.K, w.R
     if w.op == "ag":
         staged = (R - 1) * w.M_r * K * 2
@@ -67,7 +68,8 @@ def algorithmic_bytes(w: wl.Workload, with_send=True) -> float:
         peers = (R - 1) * w.M_r * N * 4
         send = (R - 1) * w.M_r * N * 4 if with_send else 0
         return M * K * 2 + K * N * 2 + peers + send + w.M_r * N * 2
-    return M * K * 2 + K * N * 2 + (R - 1) * M * N * 4 + M * N * 2
+    publish = M * N * 4 if with_send else 0
+    return M * K * 2 + K * N * 2 + (R - 1) * M * N * 4 + publish + M * N * 2
 
 
 def load_peaks():
@@ -284,7 +286,7 @@ def main():
     host_inputs = [wl.make_inputs(w, r=0, seed=0) for w in STEP]
     devs, plans = [], []
     for w, inp in zip(STEP, host_inputs):
-        d = runner.upload(inp, with_f32_out=(w.op == "rs"))
+        d = runner.upload(inp, with_f32_out=(w.op != "ag"))  # RS: send rows; AR: publish
         kn = dict(knobs[w.op])
         split, order = kn.pop("split"), kn.pop("order")
         plans.append(runner.make_plan(d, split=split, order=order, **kn))
@@ -330,24 +332,30 @@ def main():
     step_flops = sum(w.flops for w in STEP)
     value = step_flops * world / (ms_per_step * 1e-3) / 1e12
 
+    # The operators run back to back for the whole timed loop (seconds under
+    # the power cap), so the tensor denominator is the sustained bf16 figure.
+    tensor_peak = peaks["bf16_tflops_sustained"]
     per_op = {}
     for w, ms in zip(STEP, op_ms):
         byts = algorithmic_bytes(w)
-        t_roof = max(w.flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+        t_roof = max(w.flops / (tensor_peak * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
         per_op[w.op] = {"workload": w.name, "us": ms * 1e3, "tflops": w.flops / (ms * 1e-3) / 1e12,
                         "gbs": byts / (ms * 1e-3) / 1e9, "algorithmic_bytes": byts,
                         "roofline_frac": t_roof / (ms * 1e-3),
-                        "bound": "tensor" if w.flops / (peaks["bf16_tflops"] * 1e12) >= byts / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                        "roofline_frac_burst_peak": max(w.flops / (peaks["bf16_tflops"] * 1e12),
+                                                        byts / (peaks["hbm_gbs"] * 1e9)) / (ms * 1e-3),
+                        "bound": "tensor" if w.flops / (tensor_peak * 1e12) >= byts / (peaks["hbm_gbs"] * 1e9) else "hbm",
                         "knobs": knobs[w.op]}
     dom = max(per_op, key=lambda k: per_op[k]["us"])
     dw = STEP[[w.op for w in STEP].index(dom)]
     if per_op[dom]["bound"] == "tensor":
-        achieved, peak, unit = per_op[dom]["tflops"], peaks["bf16_tflops"], "TFLOP/s"
+        achieved, peak, unit = per_op[dom]["tflops"], tensor_peak, "TFLOP/s"
     else:
         achieved, peak, unit = per_op[dom]["gbs"], peaks["hbm_gbs"], "GB/s"
     roofline = {"bound": per_op[dom]["bound"], "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": recorded_traffic(dom), "kernel": f"syn_fused_kernel<{dom}>",
-                "workload": dw.name, "peak_source": f"{peak_src} (burst)",
+                "workload": dw.name,
+                "peak_source": f"{peak_src} ({'sustained bf16' if unit == 'TFLOP/s' else 'copy'})",
                 "algorithmic_per_launch": dw.flops if unit == "TFLOP/s" else algorithmic_bytes(dw)}
 
     # ---------------- end to end: pinned host inputs in, bf16 outputs out ----------------
