@@ -583,7 +583,28 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
     if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (f32_out && !aligned16(f32_out)))
         return fail(SYN_ERR_INVALID, "operand not 16-byte aligned");
     const bool staged = staged_peers(plan);
-    std::vector<const void *> key = {A, B};
+    // reducer warps: where the epilogue leaves the reducing tiles' fp32 partials
+    float *red_buf = nullptr;
+    int64_t red_rows = 0;
+    int32_t red_row_off = 0;
+    if (plan->lc.red) {
+        if (op == SYN_OP_GEMM_RS) {
+            red_buf = plan->d_red;
+            red_rows = s.M_r;
+            red_row_off = (int32_t)(s.rank * s.M_r);
+        } else if (f32_out != nullptr) {
+            red_buf = f32_out;
+            red_rows = s.M;
+        } else {
+            if (plan->d_red == nullptr) {
+                plan->red_bytes = (size_t)s.M * s.N * sizeof(float);
+                SYN_CK(cudaMalloc(&plan->d_red, plan->red_bytes));
+            }
+            red_buf = plan->d_red;
+            red_rows = s.M;
+        }
+    }
+    std::vector<const void *> key = {A, B, f32_out, red_buf};
     if (!staged)
         for (int q = 0; q < s.R; ++q) key.push_back(q == s.rank ? nullptr : peers[q]);
     if (key != plan->map_key) {
@@ -603,6 +624,16 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
                                 32, 128)) != SYN_OK)
                 return rc;
         }
+        // fp32 tile stores of the epilogue (used by instances with staging room):
+        // 32 columns x 32 rows, 128-byte swizzle
+        if (f32_out != nullptr &&
+            (rc = encode_2d(&plan->maps.f32out, f32_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.N, s.M, 32,
+                            32)) != SYN_OK)
+            return rc;
+        if (red_buf != nullptr &&
+            (rc = encode_2d(&plan->maps.red, red_buf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.N,
+                            (uint64_t)red_rows, 32, 32)) != SYN_OK)
+            return rc;
         plan->map_key = key;
     }
     plan->epoch += 1;
@@ -611,20 +642,8 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
         p.stage_src[q] = q == s.rank ? nullptr : reinterpret_cast<const uint8_t *>(peers[q]);
     p.stage_dst = plan->d_recv;
     p.row_bytes = s.N * 4;
-    if (plan->lc.red) {
-        if (op == SYN_OP_GEMM_RS) {
-            p.red_buf = plan->d_red;
-            p.red_row_off = (int32_t)(s.rank * s.M_r);
-        } else if (f32_out != nullptr) {
-            p.red_buf = f32_out;
-        } else {
-            if (plan->d_red == nullptr) {
-                plan->red_bytes = (size_t)s.M * s.N * sizeof(float);
-                SYN_CK(cudaMalloc(&plan->d_red, plan->red_bytes));
-            }
-            p.red_buf = plan->d_red;
-        }
-    }
+    p.red_buf = red_buf;
+    p.red_row_off = red_row_off;
     p.recv_slot_rows = plan->recv_slot_rows;
     p.peer_row_off = (staged && op == SYN_OP_GEMM_RS) ? (int32_t)(s.rank * s.M_r) : 0;
     p.out = static_cast<uint16_t *>(out);

@@ -105,12 +105,21 @@ struct KCfg {
     static_assert(OP == OP_AG || RED || P >= 2, "peer ring needs at least two slots");
     static_assert(!RED || (OP != OP_AG && !STG), "deferred reduction: GEMM-RS/AR, resident peers");
     static_assert(S * STAGE_BYTES + P * PEER_BYTES + NSTG * STG_BYTES <= kSmemRings, "rings");
+    // GEMM-RS/AR: when the rings leave room, each epilogue warp stages its fp32
+    // stores (32 rows x 32 columns, 128-byte swizzle) in two shared-memory
+    // buffers and writes them with TMA tile stores (whole 128-byte lines)
+    // instead of one 16-byte store per thread and row
+    static constexpr int EPI_SLOT = 32 * 32 * 4;
+    static constexpr int EPI_LEFT = kSmemRings - S * STAGE_BYTES - P * PEER_BYTES - NSTG * STG_BYTES;
+    static constexpr bool EPI_TMA = OP != OP_AG && EPI_LEFT >= 8 * EPI_SLOT;
+    static constexpr int EPI_BYTES = EPI_TMA ? 8 * EPI_SLOT : 0;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + S * A_BYTES;
     static constexpr int OFF_PEER = OFF_B + S * B_BYTES;
     static constexpr int OFF_STG = OFF_PEER + P * PEER_BYTES;
-    static constexpr int OFF_BAR = OFF_STG + NSTG * STG_BYTES;
+    static constexpr int OFF_EPI = OFF_STG + NSTG * STG_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
     // barrier slots
     static constexpr int BAR_FULL = 0;
     static constexpr int BAR_EMPTY = BAR_FULL + S;
@@ -136,7 +145,9 @@ struct KCfg {
     static constexpr int SMEM_USED = OFF_MISC + 48;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-    static_assert(OFF_B % 1024 == 0 && OFF_PEER % 1024 == 0 && OFF_STG % 1024 == 0, "1 KiB atoms");
+    static_assert(OFF_B % 1024 == 0 && OFF_PEER % 1024 == 0 && OFF_STG % 1024 == 0 && OFF_EPI % 1024 == 0,
+                  "1 KiB atoms");
+    static_assert(S * STAGE_BYTES + P * PEER_BYTES + NSTG * STG_BYTES + EPI_BYTES <= kSmemRings, "epilogue");
     static_assert(BN == 128 || BN == 256, "tile_n");
     static_assert(BK == 64 || BK == 32, "tile_k");
     static_assert(BN_CTA % 64 == 0, "B is staged in 64-column boxes");
@@ -804,6 +815,24 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
             const bool red = reduces<OP>(p, tr0);
             const uint32_t tbase = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * BN);
             bool dead = false;
+            // fp32 store of this tile (at most one): send / publish, or (RED) the
+            // reducing tile's partial; with EPI_TMA through this warp's staging
+            // buffers and TMA tile stores of its 32 rows
+            const int wrow0 = tr0 + (int)crank * C::BM + qd * 32;  // this warp's first row
+            const CUtensorMap *fmap = nullptr;
+            int fy = 0;
+            if constexpr (C::EPI_TMA) {
+                if (wrow0 < p.M) {
+                    if (p.f32_out != nullptr && (OP == OP_AR || !red)) {
+                        fmap = &tm.f32out;
+                        fy = wrow0;
+                    } else if (RED && red && p.red_buf != p.f32_out) {
+                        fmap = &tm.red;
+                        fy = wrow0 - p.red_row_off;
+                    }
+                }
+            }
+            const uint32_t ebuf = sbase + C::OFF_EPI + (uint32_t)((warp - 2) * 2 * C::EPI_SLOT);
 #pragma unroll 1
             for (int cc = 0; cc < BN / 32; ++cc) {
                 uint32_t v[32];
@@ -817,11 +846,30 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
                     if (in_range) store_bf16_row32(p.out + (int64_t)row * p.N + col, f);
                     continue;
                 } else {
-                if (p.f32_out != nullptr && in_range && (OP == OP_AR || !red))
-                    store_f32_row32(p.f32_out + (int64_t)row * p.N + col, f);
+                if constexpr (C::EPI_TMA) {
+                    if (fmap != nullptr) {
+                        const uint32_t buf = ebuf + (uint32_t)((cc & 1) * C::EPI_SLOT);
+                        if (lane == 0) ptx::bulk_wait_read<1>();  // the store of chunk cc - 2 read it
+                        __syncwarp();
+                        // row `lane`, 16-byte chunk c at position c ^ (lane & 7) (128-byte swizzle)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            ptx::st_shared_f4(buf + (uint32_t)(lane * 128) + ((uint32_t)(c ^ (lane & 7)) << 4),
+                                              f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(fmap, buf, col, fy);
+                            ptx::bulk_commit();
+                        }
+                    }
+                } else {
+                    if (p.f32_out != nullptr && in_range && (OP == OP_AR || !red))
+                        store_f32_row32(p.f32_out + (int64_t)row * p.N + col, f);
+                }
                 if constexpr (RED) {
                     // the reducer warps add the peers to the stored partial
-                    if (red && in_range && p.red_buf != p.f32_out)
+                    if (!C::EPI_TMA && red && in_range && p.red_buf != p.f32_out)
                         store_f32_row32(p.red_buf + (int64_t)(row - p.red_row_off) * p.N + col, f);
                     continue;
                 } else {
@@ -874,6 +922,15 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
             }
             if (p.trace != nullptr && leader && warp == 2 && lane == 0)
                 p.trace[5 * t + 3] = ptx::globaltimer();
+            if constexpr (C::EPI_TMA) {
+                // the tile's TMA stores must have landed before its chunk flags or
+                // the reducer hand-off publish them (the accumulator is already free)
+                if (fmap != nullptr && lane == 0) {
+                    ptx::bulk_wait_all();
+                    ptx::fence_proxy_async();
+                }
+                __syncwarp();
+            }
             if (dead) break;
             if constexpr (RED) {
                 if (red) {

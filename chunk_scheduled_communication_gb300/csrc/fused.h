@@ -34,6 +34,8 @@ struct TensorMaps {  // CUtensorMap carries its own alignment
     CUtensorMap a;                 // AG: gathered [M,K]; RS/AR: A [M,K]   (bf16, box 64x128)
     CUtensorMap b;                 // B [K,N]                               (bf16, box 64x64)
     CUtensorMap peer[kMaxRanks];   // RS/AR: peer q partial rows            (fp32, box 32x128)
+    CUtensorMap f32out;            // RS/AR: send / publish [M,N]           (fp32, box 32x32)
+    CUtensorMap red;               // RED: partials of reducing tiles       (fp32, box 32x32)
 };
 
 struct KernelParams {

@@ -90,10 +90,10 @@ __device__ __forceinline__ void st_release_cta_shared(uint32_t addr, uint32_t v)
 }
 
 // ---------------------------------------------------------------- vector global loads / stores
-// 16-byte load through L1 (data this CTA wrote earlier in the kernel)
+// 16-byte load from L2 (data this kernel wrote earlier, possibly through TMA)
 __device__ __forceinline__ float4 ld_f4(const float *p) {
     float4 v;
-    asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "l"(p)
                  : "memory");
@@ -119,6 +119,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// shared -> global tile store (bulk group of the issuing thread); the box is
+// laid out in shared memory as the tensor map's swizzle says
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+// wait until at most N of this thread's bulk groups still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void st_shared_f4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
 }
 
 // ---------------------------------------------------------------- bulk (non-tensor) copies
