@@ -550,9 +550,13 @@ int syn_ag_gemm(syn_plan_t plan, const void *const *shards, void *gathered, cons
         return fail(SYN_ERR_INVALID, "operand not 16-byte aligned");
     const int64_t row_bytes = s.K * 2;
     // tensor maps (cached on the operand pointers)
-    std::vector<const void *> key = {gathered, B};
+    std::vector<const void *> key = {gathered, B, C};
     if (key != plan->map_key) {
         if ((rc = encode_operands(plan, gathered, B)) != SYN_OK) return rc;
+        // bf16 tile stores of the epilogue: 32 columns x 32 rows, 64-byte swizzle
+        if ((rc = encode_2d(&plan->maps.c, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.N, s.M, 32, 32,
+                            CU_TENSOR_MAP_SWIZZLE_64B)) != SYN_OK)
+            return rc;
         plan->map_key = key;
     }
     plan->epoch += 1;
@@ -567,6 +571,7 @@ int syn_ag_gemm(syn_plan_t plan, const void *const *shards, void *gathered, cons
             : 0;
     p.out = static_cast<uint16_t *>(C);
     p.f32_out = nullptr;
+    p.epi_tma = 1;
     return run(plan, p, static_cast<cudaStream_t>(stream));
 }
 
@@ -644,6 +649,7 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
     p.row_bytes = s.N * 4;
     p.red_buf = red_buf;
     p.red_row_off = red_row_off;
+    p.epi_tma = 1;
     p.recv_slot_rows = plan->recv_slot_rows;
     p.peer_row_off = (staged && op == SYN_OP_GEMM_RS) ? (int32_t)(s.rank * s.M_r) : 0;
     p.out = static_cast<uint16_t *>(out);

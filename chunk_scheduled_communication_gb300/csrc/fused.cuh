@@ -94,25 +94,29 @@ struct KCfg {
     static constexpr uint32_t B_BOX_BYTES = BK * 128;
     static constexpr int PEER_COLS = 32;
     static constexpr int PEER_BYTES = BM * PEER_COLS * 4;
-    // co-located staging buffers: two for RS/AR (the peer ring takes the rest);
-    // for AG every 16 KiB the pipeline stages leave (up to 8), so shallower
-    // pipelines trade MMA lookahead for more staging copies in flight
+    // Epilogue store staging: when the rings leave room, each epilogue warp
+    // writes its 32 rows x 32 columns (GEMM-RS/AR fp32 with 128-byte swizzle,
+    // AG bf16 with 64-byte swizzle) into one of two shared-memory buffers and
+    // issues a TMA tile store (whole lines) instead of one 16-byte store per
+    // thread and row.  AG takes its buffers before the stager's.
+    static constexpr int EPI_SLOT = 32 * 32 * (OP == OP_AG ? 2 : 4);
+    static constexpr int EPI_WANT = 8 * EPI_SLOT;
     static constexpr int STG_BYTES = 16384;
-    static constexpr int NSTG_AG = (kSmemRings - S * STAGE_BYTES) / STG_BYTES;
+    static constexpr bool EPI_AG =
+        OP == OP_AG && PAIR && kSmemRings - S * STAGE_BYTES >= EPI_WANT + (STG ? STG_BYTES : 0);
+    // co-located staging buffers: two for RS/AR (the peer ring takes the rest);
+    // for AG every 16 KiB the stages and the epilogue buffers leave (up to 8),
+    // so shallower pipelines trade MMA lookahead for more staging copies
+    static constexpr int NSTG_AG = (kSmemRings - S * STAGE_BYTES - (EPI_AG ? EPI_WANT : 0)) / STG_BYTES;
     static constexpr int NSTG = !STG ? 0 : OP != OP_AG ? 2 : (NSTG_AG > 8 ? 8 : NSTG_AG);
     static constexpr int P =
         OP == OP_AG || RED ? 0 : (kSmemRings - NSTG * STG_BYTES - S * STAGE_BYTES) / PEER_BYTES;
     static_assert(OP == OP_AG || RED || P >= 2, "peer ring needs at least two slots");
     static_assert(!RED || (OP != OP_AG && !STG), "deferred reduction: GEMM-RS/AR, resident peers");
     static_assert(S * STAGE_BYTES + P * PEER_BYTES + NSTG * STG_BYTES <= kSmemRings, "rings");
-    // GEMM-RS/AR: when the rings leave room, each epilogue warp stages its fp32
-    // stores (32 rows x 32 columns, 128-byte swizzle) in two shared-memory
-    // buffers and writes them with TMA tile stores (whole 128-byte lines)
-    // instead of one 16-byte store per thread and row
-    static constexpr int EPI_SLOT = 32 * 32 * 4;
     static constexpr int EPI_LEFT = kSmemRings - S * STAGE_BYTES - P * PEER_BYTES - NSTG * STG_BYTES;
-    static constexpr bool EPI_TMA = OP != OP_AG && EPI_LEFT >= 8 * EPI_SLOT;
-    static constexpr int EPI_BYTES = EPI_TMA ? 8 * EPI_SLOT : 0;
+    static constexpr bool EPI_TMA = OP == OP_AG ? EPI_AG : EPI_LEFT >= EPI_WANT;
+    static constexpr int EPI_BYTES = EPI_TMA ? EPI_WANT : 0;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + S * A_BYTES;
@@ -821,8 +825,10 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
             const int wrow0 = tr0 + (int)crank * C::BM + qd * 32;  // this warp's first row
             const CUtensorMap *fmap = nullptr;
             int fy = 0;
-            if constexpr (C::EPI_TMA) {
-                if (wrow0 < p.M) {
+            if constexpr (C::EPI_TMA && OP == OP_AG) {
+                if (p.epi_tma && wrow0 < p.M) fmap = &tm.c;
+            } else if constexpr (C::EPI_TMA) {
+                if (p.epi_tma && wrow0 < p.M) {
                     if (p.f32_out != nullptr && (OP == OP_AR || !red)) {
                         fmap = &tm.f32out;
                         fy = wrow0;
@@ -843,11 +849,35 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
                 for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
                 const int col = tni * BN + cc * 32;
                 if constexpr (OP == OP_AG) {
-                    if (in_range) store_bf16_row32(p.out + (int64_t)row * p.N + col, f);
+                    if (C::EPI_TMA && fmap != nullptr) {
+                        {
+                            const uint32_t buf = ebuf + (uint32_t)((cc & 1) * C::EPI_SLOT);
+                            if (lane == 0) ptx::bulk_wait_read<1>();  // the store of chunk cc - 2 read it
+                            __syncwarp();
+                            // row `lane` (64 bytes), 16-byte chunk c at position c ^ ((lane >> 1) & 3)
+                            // (64-byte swizzle)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                ptx::st_shared_u4(buf + (uint32_t)(lane * 64) +
+                                                      ((uint32_t)(c ^ ((lane >> 1) & 3)) << 4),
+                                                  pack_bf16x2(f[8 * c], f[8 * c + 1]),
+                                                  pack_bf16x2(f[8 * c + 2], f[8 * c + 3]),
+                                                  pack_bf16x2(f[8 * c + 4], f[8 * c + 5]),
+                                                  pack_bf16x2(f[8 * c + 6], f[8 * c + 7]));
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                ptx::tma_store_2d(&tm.c, buf, col, wrow0);
+                                ptx::bulk_commit();
+                            }
+                        }
+                    } else if (in_range) {
+                        store_bf16_row32(p.out + (int64_t)row * p.N + col, f);
+                    }
                     continue;
                 } else {
-                if constexpr (C::EPI_TMA) {
-                    if (fmap != nullptr) {
+                if (C::EPI_TMA && fmap != nullptr) {
+                    {
                         const uint32_t buf = ebuf + (uint32_t)((cc & 1) * C::EPI_SLOT);
                         if (lane == 0) ptx::bulk_wait_read<1>();  // the store of chunk cc - 2 read it
                         __syncwarp();
@@ -866,12 +896,11 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
                 } else {
                     if (p.f32_out != nullptr && in_range && (OP == OP_AR || !red))
                         store_f32_row32(p.f32_out + (int64_t)row * p.N + col, f);
+                    if (RED && red && in_range && p.red_buf != p.f32_out)
+                        store_f32_row32(p.red_buf + (int64_t)(row - p.red_row_off) * p.N + col, f);
                 }
                 if constexpr (RED) {
-                    // the reducer warps add the peers to the stored partial
-                    if (!C::EPI_TMA && red && in_range && p.red_buf != p.f32_out)
-                        store_f32_row32(p.red_buf + (int64_t)(row - p.red_row_off) * p.N + col, f);
-                    continue;
+                    continue;  // the reducer warps add the peers to the stored partial
                 } else {
                 if (!red) continue;
                 for (int q = 0; q < p.R; ++q) {

@@ -35,6 +35,7 @@ struct TensorMaps {  // CUtensorMap carries its own alignment
     CUtensorMap b;                 // B [K,N]                               (bf16, box 64x64)
     CUtensorMap peer[kMaxRanks];   // RS/AR: peer q partial rows            (fp32, box 32x128)
     CUtensorMap f32out;            // RS/AR: send / publish [M,N]           (fp32, box 32x32)
+    CUtensorMap c;                 // AG: C [M,N]                           (bf16, box 32x32)
     CUtensorMap red;               // RED: partials of reducing tiles       (fp32, box 32x32)
 };
 
@@ -71,6 +72,8 @@ struct KernelParams {
     int64_t recv_slot_rows;        // RS/AR: rows per peer slot of the receive buffer
     uint16_t *out;                 // AG: C; RS: out_r; AR: out   (bf16)
     float *f32_out;                // RS: send; AR: publish  (nullable)
+    int32_t epi_tma;               // the f32out / red / c tensor maps are encoded: instances
+                                   // with staging room store the epilogue through TMA
     float *red_buf;                // RED instances: fp32 partials of the reducing tiles,
     int32_t red_row_off;           // row r stored at row r - red_row_off
 };
@@ -123,7 +126,7 @@ int fused_smem_bytes(int op, const LaunchCfg &lc);
 // Default pipeline depth of a (tile_n, tile_k, stg, pair, red) choice.
 inline int default_stages(int op, int tile_n, int tile_k, bool stg, bool pair, bool red = false) {
     if (red) return pair ? (op == OP_AR ? 5 : 6) : 4;
-    if (pair) return op == OP_AG ? (stg ? 6 : 7) : 4;
+    if (pair) return op == OP_AG ? (stg ? 5 : 7) : 4;
     if (tile_k == 32) return op == OP_AG ? (stg ? 8 : 9) : 6;
     if (op == OP_AG) return tile_n == 256 ? 4 : 6;
     return tile_n == 256 ? 3 : 4;
