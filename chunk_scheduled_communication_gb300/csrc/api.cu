@@ -259,6 +259,12 @@ int finish_params_for_staging(syn_plan_s *pl, KernelParams &p) {
 cudaError_t launch(syn_plan_s *pl, const KernelParams &p, int grid, cudaStream_t st) {
     LaunchCfg lc = pl->lc;
     lc.grid = grid;
+    // one kernel per call, nothing else queued before it by this call: its
+    // launch and set-up may overlap the previous kernel on the stream (the
+    // kernel waits for that grid before it touches global memory)
+    const int be = pl->kn.backend;
+    lc.overlap_prev = lc.pair && (be == SYN_BACKEND_TMA_DEDICATED || be == SYN_BACKEND_TMA_COLOCATED ||
+                                  be == SYN_BACKEND_TMA_COLOCATED_SMEM);
     switch (pl->s.op) {
         case SYN_OP_AG_GEMM: return launch_fused_ag(p, pl->maps, lc, st);
         case SYN_OP_GEMM_RS: return launch_fused_rs(p, pl->maps, lc, st);

@@ -45,6 +45,11 @@
 // those signals through a thread of the even CTA instead measured 2.5x slower.)
 // No multicast form is used.
 //
+// Single-launch CTA-pair calls are launched with programmatic stream
+// serialization: a CTA sets up its shared memory and TMEM, then waits
+// (griddepcontrol.wait) for the previous kernel on the stream before it reads
+// or writes global memory, so launch and set-up overlap that kernel's tail.
+//
 // Every wait is bounded (global timer) and ends in SYN_ERR_TIMEOUT written to
 // the plan's error word; the CTA then drains its own outstanding asynchronous
 // copies and MMAs, frees TMEM and returns.  Nothing traps.
@@ -558,6 +563,8 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
 
     // ---- dedicated staging CTA -------------------------------------------
     if ((int)blockIdx.x >= p.G) {
+        ptx::grid_dep_wait();  // (programmatic launch) the previous grid's writes are visible
+        ptx::grid_dep_launch_dependents();
         // COMM_NBUF independent copiers (threads 0..COMM_NBUF-1), each with its
         // own 32 KiB buffer and barrier, so several bulk copies are in flight.
         if (threadIdx.x == 0) {
@@ -610,14 +617,6 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
     }
-    // CTA 0 clears the counters of the other epoch parity for the next call.
-    if (blockIdx.x == 0) {
-        const int nf = p.n_rc * p.R;
-        uint32_t *nin = p.in_cnt + (size_t)((p.epoch + 1u) & 1u) * nf;
-        uint32_t *nout = p.out_cnt + (size_t)((p.epoch + 1u) & 1u) * p.n_rc;
-        for (int i = threadIdx.x; i < nf; i += blockDim.x) nin[i] = 0u;
-        for (int i = threadIdx.x; i < p.n_rc; i += blockDim.x) nout[i] = 0u;
-    }
     if (warp == 1) {
         if constexpr (PAIR) {
             ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
@@ -632,6 +631,21 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
     if constexpr (PAIR) ptx::cluster_sync();  // both CTAs' barriers exist before any remote arrive
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Launched with programmatic stream serialization, this grid may start while
+    // the previous kernel on the stream still runs (on SMs it has left): the
+    // set-up above touches only this CTA's shared memory and TMEM; everything
+    // from here on may read what the previous grid wrote, so wait for it.  Then
+    // let the next grid launch early too.
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch_dependents();
+    // CTA 0 clears the counters of the other epoch parity for the next call.
+    if (blockIdx.x == 0) {
+        const int nf = p.n_rc * p.R;
+        uint32_t *nin = p.in_cnt + (size_t)((p.epoch + 1u) & 1u) * nf;
+        uint32_t *nout = p.out_cnt + (size_t)((p.epoch + 1u) & 1u) * p.n_rc;
+        for (int i = threadIdx.x; i < nf; i += blockDim.x) nin[i] = 0u;
+        for (int i = threadIdx.x; i < p.n_rc; i += blockDim.x) nout[i] = 0u;
+    }
 
     unsigned long long wait_ns = 0;
     const int KB = p.K / C::BK;
@@ -1073,7 +1087,8 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
 }
 
 template <int OP, int BN, int S, int BK, bool STG, bool PAIR, bool RED>
-cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid, cudaStream_t st) {
+cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid, cudaStream_t st,
+                           bool overlap_prev) {
     using C = KCfg<OP, BN, S, BK, STG, PAIR, RED>;
     auto kern = syn_fused_kernel<OP, BN, S, BK, STG, PAIR, RED>;
     cudaError_t e =
@@ -1089,18 +1104,26 @@ cudaError_t launch_fused_t(const KernelParams &p, const TensorMaps &tm, int grid
     // whose grid the host sized to the co-resident cluster count
     // (cudaOccupancyMaxActiveClusters), so every CTA is resident as well; were
     // one not, the bounded waits would end the call in SYN_ERR_TIMEOUT.
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned n_attr = 1;
     if (PAIR) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        if (overlap_prev) {
+            // the kernel waits for the previous grid (griddepcontrol.wait) before
+            // touching global memory, so its launch and set-up may overlap it
+            attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[1].val.programmaticStreamSerializationAllowed = 1;
+            n_attr = 2;
+        }
     } else {
         attr[0].id = cudaLaunchAttributeCooperative;
         attr[0].val.cooperative = 1;
     }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n_attr;
     return cudaLaunchKernelEx(&cfg, kern, p, tm);
 }
 
@@ -1174,7 +1197,8 @@ cudaError_t launch_op(const KernelParams &p, const TensorMaps &tm, const LaunchC
     cudaError_t err = cudaErrorInvalidValue;
     dispatch_cfg<OP>(lc, [&](auto c) {
         using C = decltype(c);
-        err = launch_fused_t<OP, C::BN_, C::S, C::BK, C::STG_, C::PAIR_, C::RED_>(p, tm, lc.grid, st);
+        err = launch_fused_t<OP, C::BN_, C::S, C::BK, C::STG_, C::PAIR_, C::RED_>(p, tm, lc.grid, st,
+                                                                                lc.overlap_prev);
     });
     return err;
 }

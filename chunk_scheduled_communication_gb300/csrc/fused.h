@@ -111,6 +111,7 @@ struct LaunchCfg {
     bool pair;    // 2-CTA clusters share 256-row tiles (tile_m 256)
     int grid;     // CTAs
     bool red = false;  // RS/AR, resident peers: reducer warps stream the peer sum
+    bool overlap_prev = false;  // CTA pairs: programmatic launch after the previous kernel
 };
 
 // Host launchers (one translation unit per operator).  cudaErrorInvalidValue

@@ -23,6 +23,18 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// wait until the grids this one depends on (the previous kernel on the stream,
+// when launched with programmatic stream serialization) have completed and
+// their memory is visible; a no-op otherwise
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// allow the next grid on the stream to be launched before this one ends
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
