@@ -4,9 +4,11 @@
 // device tables, flags, counters, receive buffers), tensor-map encoding, and
 // the per-call orchestration of the staging backends of the Syncopate summary
 // page (method ¶3, paper §5.2, Fig. 7):
-//   CE            side stream: per chunk, cudaMemcpyAsync then a stream-ordered
-//                 flag write (cuStreamWriteValue32, which fences prior writes),
-//                 concurrent with the fused kernel on the caller's stream
+//   CE            side streams (chunks round-robin in arrival order, so several
+//                 copy engines run at once): per chunk, cudaMemcpyAsync then a
+//                 stream-ordered flag write (cuStreamWriteValue32, which fences
+//                 prior writes), concurrent with the fused kernel on the caller's
+//                 stream
 //   TMA_DEDICATED comm_sms extra CTAs of the same cooperative grid copy chunks
 //   TMA_COLOCATED a staging warp in every GEMM CTA copies chunk slices
 //   TMA_COLOCATED_SMEM  GEMM-RS/AR: peers fetched per tile into shared memory
@@ -123,7 +125,9 @@ struct syn_plan_s {
     float *d_red = nullptr;                 // RED: fp32 partials of the reducing tiles
     size_t red_bytes = 0;
     int64_t recv_slot_rows = 0;
-    cudaStream_t side = nullptr;
+    cudaStream_t side = nullptr;            // side stream 0 (DECOMPOSED copies; CE stream 0)
+    std::vector<cudaStream_t> ce_side;      // CE: transfers go round-robin over these
+    std::vector<cudaEvent_t> ce_join;       // CE: one join event per side stream
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     std::vector<cudaEvent_t> ev_transfer;  // DECOMPOSED: one per transfer
     std::vector<std::pair<int, int>> groups;  // DECOMPOSED: tile-list ranges of equal key
@@ -142,6 +146,8 @@ bool staged_peers(const syn_plan_s *pl) {
 void free_plan(syn_plan_s *pl) {
     if (pl == nullptr) return;
     if (pl->side) cudaStreamSynchronize(pl->side);
+    for (cudaStream_t x : pl->ce_side)
+        if (x != pl->side) cudaStreamSynchronize(x);
     cudaFree(pl->d_tiles);
     cudaFree(pl->d_transfers);
     cudaFree(pl->d_err);
@@ -156,6 +162,9 @@ void free_plan(syn_plan_s *pl) {
     for (cudaEvent_t e : pl->ev_transfer) cudaEventDestroy(e);
     if (pl->ev_fork) cudaEventDestroy(pl->ev_fork);
     if (pl->ev_join) cudaEventDestroy(pl->ev_join);
+    for (cudaEvent_t e : pl->ce_join) cudaEventDestroy(e);
+    for (cudaStream_t x : pl->ce_side)
+        if (x != pl->side) cudaStreamDestroy(x);
     if (pl->side) cudaStreamDestroy(pl->side);
     delete pl;
 }
@@ -274,9 +283,13 @@ cudaError_t launch(syn_plan_s *pl, const KernelParams &p, int grid, cudaStream_t
 
 // Issue the staging copies of all transfers on `st` (CE); optionally a flag
 // write after each and/or an event record after each.
-int ce_copies(syn_plan_s *pl, const KernelParams &p, cudaStream_t st, bool flags, bool events) {
+int ce_copies(syn_plan_s *pl, const KernelParams &p, const cudaStream_t *streams, int n_streams, bool flags,
+              bool events) {
     const Schedule &s = pl->s;
     for (size_t a = 0; a < s.transfers.size(); ++a) {
+        // transfer a on stream a mod n: copies in arrival order spread over the
+        // copy engines; each flag write follows its own copy in its stream
+        cudaStream_t st = streams[a % (size_t)n_streams];
         const int code = s.transfers[a];
         const bool skip = (s.op == SYN_OP_AG_GEMM && p.local_inplace && code % s.R == s.rank);
         if (!skip) {
@@ -306,10 +319,13 @@ int run(syn_plan_s *pl, KernelParams &p, cudaStream_t st) {
         case SYN_BACKEND_CE: {
             SYN_CK(cudaEventRecord(pl->ev_fork, st));
             SYN_CK(launch(pl, p, pl->grid_compute, st));
-            SYN_CK(cudaStreamWaitEvent(pl->side, pl->ev_fork, 0));
-            if ((rc = ce_copies(pl, p, pl->side, true, false)) != SYN_OK) return rc;
-            SYN_CK(cudaEventRecord(pl->ev_join, pl->side));
-            SYN_CK(cudaStreamWaitEvent(st, pl->ev_join, 0));
+            const int n = (int)pl->ce_side.size();
+            for (int i = 0; i < n; ++i) SYN_CK(cudaStreamWaitEvent(pl->ce_side[i], pl->ev_fork, 0));
+            if ((rc = ce_copies(pl, p, pl->ce_side.data(), n, true, false)) != SYN_OK) return rc;
+            for (int i = 0; i < n; ++i) {
+                SYN_CK(cudaEventRecord(pl->ce_join[i], pl->ce_side[i]));
+                SYN_CK(cudaStreamWaitEvent(st, pl->ce_join[i], 0));
+            }
             return SYN_OK;
         }
         case SYN_BACKEND_TMA_DEDICATED:
@@ -325,14 +341,14 @@ int run(syn_plan_s *pl, KernelParams &p, cudaStream_t st) {
             SYN_CK(launch(pl, p, pl->grid_compute, st));
             return SYN_OK;
         case SYN_BACKEND_UNFUSED:
-            if ((rc = ce_copies(pl, p, st, false, false)) != SYN_OK) return rc;
+            if ((rc = ce_copies(pl, p, &st, 1, false, false)) != SYN_OK) return rc;
             p.waits = 0;
             SYN_CK(launch(pl, p, pl->grid_compute, st));
             return SYN_OK;
         case SYN_BACKEND_DECOMPOSED: {
             SYN_CK(cudaEventRecord(pl->ev_fork, st));
             SYN_CK(cudaStreamWaitEvent(pl->side, pl->ev_fork, 0));
-            if ((rc = ce_copies(pl, p, pl->side, false, true)) != SYN_OK) return rc;
+            if ((rc = ce_copies(pl, p, &pl->side, 1, false, true)) != SYN_OK) return rc;
             p.waits = 0;
             for (size_t g = 0; g < pl->groups.size(); ++g) {
                 const int key = pl->group_key[g];
@@ -516,6 +532,20 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
         if (pl->recv_bytes > 0) PL_CK(cudaMalloc(&pl->d_recv, pl->recv_bytes));
     }
     PL_CK(cudaStreamCreateWithFlags(&pl->side, cudaStreamNonBlocking));
+    if (kn.backend == SYN_BACKEND_CE) {
+        const int n = kn.ce_streams > 0 ? std::min(kn.ce_streams, 16) : 4;
+        pl->ce_side.push_back(pl->side);
+        for (int i = 1; i < n; ++i) {
+            cudaStream_t x = nullptr;
+            PL_CK(cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking));
+            pl->ce_side.push_back(x);
+        }
+        for (int i = 0; i < n; ++i) {
+            cudaEvent_t e = nullptr;
+            PL_CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+            pl->ce_join.push_back(e);
+        }
+    }
     PL_CK(cudaEventCreateWithFlags(&pl->ev_fork, cudaEventDisableTiming));
     PL_CK(cudaEventCreateWithFlags(&pl->ev_join, cudaEventDisableTiming));
     if (kn.backend == SYN_BACKEND_DECOMPOSED) {
@@ -677,6 +707,7 @@ int syn_sync_status(syn_plan_t plan, void *stream) {
     if (plan == nullptr) return fail(SYN_ERR_INVALID, "null plan");
     SYN_CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
     SYN_CK(cudaStreamSynchronize(plan->side));
+    for (cudaStream_t x : plan->ce_side) SYN_CK(cudaStreamSynchronize(x));
     int32_t e[4] = {0, 0, 0, 0};
     SYN_CK(cudaMemcpy(e, plan->d_err, sizeof(e), cudaMemcpyDeviceToHost));
     if (e[0] == 0) return SYN_OK;

@@ -153,6 +153,9 @@ typedef struct {
                               additions in the same order as -1, bit for bit.
                               -1 = the epilogue adds the peers itself through a
                               shared-memory ring of peer tiles.              */
+    int ce_streams;        /* CE: side streams the chunk copies are spread over
+                              round-robin in arrival order, so several copy
+                              engines run at once (0 = 4; at most 16)        */
 } syn_knobs_t;
 
 /* Everything a caller or a test may want to know about a plan. */

@@ -465,6 +465,23 @@ def test_reducer_warps_ar_without_publish():
     check_against_oracle(w, r, {"out": runner.dev_to_u16(d.out)}, kind="int")
 
 
+@pytest.mark.parametrize("ce_streams", [1, 3, 16])
+def test_copy_engine_streams_bit_exact(ce_streams):
+    """Copy-engine staging spread over several side streams: every chunk's
+    flag still follows its own copy, so outputs and the gathered buffer stay
+    bit-exact (integer inputs) for any stream count."""
+    w, r = INT_AG_PAIR, 1
+    inp = inputs(w, r, 0, "int")
+    d = runner.upload(inp)
+    with runner.make_plan(d, split=2, order="row", backend="ce", tile_m=256, tile_n=256,
+                          ce_streams=ce_streams) as plan:
+        for _ in range(2):
+            runner.call(plan, d)
+        assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+    check_against_oracle(w, r, {"out": runner.dev_to_u16(d.out), "gathered": runner.dev_to_u16(d.gathered)},
+                         kind="int")
+
+
 def test_uncompiled_stage_count_is_rejected():
     inp = inputs(INT_AR_N512, 0, 0, "int")
     d = runner.upload(inp)
