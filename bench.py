@@ -55,11 +55,12 @@ DEFAULT_KNOBS = {
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def algorithmic_bytes(w: wl.Workload, with_send=True) -> float:
+def algorithmic_bytes(w: wl.Workload, with_send=True, with_publish=False) -> float:
     """Bytes the method must move through this HBM (each operand read once,
     each output written once; AG: staged peer shards read + written; RS/AR:
     each peer byte read once; RS: the fp32 send rows; AR: the fp32 publish of
-    the local partial, which the peers pull)."""
+    the local partial only when it is written -- the measured step leaves it
+    NULL, since every AR flop already feeds `out`)."""
     M, N, K, R = w.M, w.N, w.K, w.R
     if w.op == "ag":
         staged = (R - 1) * w.M_r * K * 2
@@ -68,7 +69,7 @@ def algorithmic_bytes(w: wl.Workload, with_send=True) -> float:
         peers = (R - 1) * w.M_r * N * 4
         send = (R - 1) * w.M_r * N * 4 if with_send else 0
         return M * K * 2 + K * N * 2 + peers + send + w.M_r * N * 2
-    publish = M * N * 4 if with_send else 0
+    publish = M * N * 4 if with_publish else 0
     return M * K * 2 + K * N * 2 + (R - 1) * M * N * 4 + publish + M * N * 2
 
 
@@ -286,7 +287,7 @@ def main():
     host_inputs = [wl.make_inputs(w, r=0, seed=0) for w in STEP]
     devs, plans = [], []
     for w, inp in zip(STEP, host_inputs):
-        d = runner.upload(inp, with_f32_out=(w.op != "ag"))  # RS: send rows; AR: publish
+        d = runner.upload(inp, with_f32_out=(w.op == "rs"))  # RS: send rows; AR: publish NULL
         kn = dict(knobs[w.op])
         split, order = kn.pop("split"), kn.pop("order")
         plans.append(runner.make_plan(d, split=split, order=order, **kn))
@@ -401,6 +402,43 @@ def main():
     e2e = {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    # ---------------- per-call distribution (rank 0): warm and L2-cold ----------------
+    # 5 warm-up calls, then 50 calls each between CUDA events: back to back
+    # ("warm"), and with a 512 MB buffer rewritten before each call ("cold",
+    # the flush outside the events).  Plus the share of CTA time spent waiting
+    # on chunk flags, from a traced plan (trace = 1).
+    per_call = {}
+    if rank == 0 and not args.no_baselines:
+        flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=stream.device)
+        for w, p, d in zip(STEP, plans, devs):
+            res = {}
+            for mode in ("warm", "cold"):
+                for _ in range(5):
+                    runner.call(p, d, stream)
+                ts = []
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(50)]
+                for a, b in evs:
+                    if mode == "cold":
+                        flush.fill_(1.0)
+                    a.record(stream)
+                    runner.call(p, d, stream)
+                    b.record(stream)
+                torch.cuda.synchronize()
+                ts = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+                res[mode] = {"p10_us": ts[4], "median_us": ts[24], "p90_us": ts[44]}
+            p.check(stream)
+            kn = dict(knobs[w.op])
+            split, order = kn.pop("split"), kn.pop("order")
+            with runner.make_plan(d, split=split, order=order, trace=1, **kn) as tp:
+                for _ in range(20):
+                    runner.call(tp, d, stream)
+                tp.check(stream)
+                wait_ns, busy_ns = tp.stats()
+            res["flag_wait_share"] = wait_ns / busy_ns if busy_ns else None
+            per_call[w.op] = res
+        del flush
+
     # ---------------- comparisons (rank 0): unfused / decomposed baselines, cuBLAS+copy ----------------
     baselines = {}
     if rank == 0 and not args.no_baselines:
@@ -448,6 +486,7 @@ def main():
                            "l2": "inputs > L2 (each step streams ~2 GB through the 135 MB L2); no flush"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": sum(launches_per_call(p) for p in plans) * args.steps,
+                "per_call": per_call,
                 "clocks": clk, "per_op": per_op, "baselines": baselines,
                 "peaks": {**peaks, "source": peak_src}}
         print(json.dumps(line), flush=True)

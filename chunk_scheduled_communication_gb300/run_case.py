@@ -43,7 +43,7 @@ def main(argv=None) -> int:
 
     w = WORKLOADS[a.op]
     torch.cuda.set_device(0)
-    d = runner.upload(wl.make_inputs(w, r=0), with_f32_out=(w.op != "ag"))  # RS: send; AR: publish
+    d = runner.upload(wl.make_inputs(w, r=0), with_f32_out=(w.op == "rs"))  # RS: send rows; AR: no publish
     stream = torch.cuda.current_stream()
     with runner.make_plan(d, split=a.split, order=a.order, backend=a.backend, tile_m=a.tile_m,
                           tile_n=a.tile_n, tile_k=a.tile_k, stages=a.stages, comm_sms=a.comm_sms) as p:
