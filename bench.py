@@ -165,7 +165,7 @@ def dist_setup(n_gpus: int):
     if ws > 1:
         import torch
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        backend = os.environ.get("SYN_DIST_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
         dist.init_process_group(backend)
         return dist, dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
     return None, 0, 1, 0

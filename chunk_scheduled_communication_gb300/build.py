@@ -18,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsyn.so")
+PROTO_LIB = os.path.join(PKG, "libsynproto.so")
+# the CPU emulation of the flag protocol is a separate host-only library
+PROTO_SRCS = ["proto_emu.cpp", "schedule.cpp"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -32,7 +35,8 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
+    srcs = glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp"))
+    return sorted(s for s in srcs if os.path.basename(s) != "proto_emu.cpp")
 
 
 def _headers_mtime() -> float:
@@ -75,5 +79,25 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
     return LIB
 
 
+def build_proto(verbose: bool = False) -> str:
+    """Compile libsynproto.so (host C++ only: the flag-protocol emulation over
+    the real plan builder); returns its path."""
+    srcs = [os.path.join(CSRC, f) for f in PROTO_SRCS]
+    newest = max([os.path.getmtime(x) for x in srcs] + [_headers_mtime()])
+    if os.path.exists(PROTO_LIB) and os.path.getmtime(PROTO_LIB) >= newest:
+        return PROTO_LIB
+    tmp = PROTO_LIB + f".tmp{os.getpid()}"
+    cmd = [os.environ.get("CXX", "g++"), "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
+           f"-I{INCLUDE}", f"-I{CSRC}", *srcs, "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"build failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, PROTO_LIB)
+    if verbose:
+        print("built", PROTO_LIB)
+    return PROTO_LIB
+
+
 if __name__ == "__main__":
     build(verbose=True, extra=sys.argv[1:])
+    build_proto(verbose=True)

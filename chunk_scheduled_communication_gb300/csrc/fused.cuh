@@ -58,6 +58,7 @@
 #include <cuda_bf16.h>
 
 #include "fused.h"
+#include "protocol.h"
 #include "ptx.cuh"
 
 namespace syn {
@@ -228,11 +229,11 @@ __device__ __forceinline__ void bwait_drain(uint32_t bar, uint32_t parity, const
 __device__ __forceinline__ bool wait_flag(const uint32_t *flag, const KernelParams &p,
                                           volatile int *abort, int where, int info,
                                           unsigned long long &waited_ns) {
-    if ((int32_t)(ptx::ld_acquire_gpu(flag) - p.epoch) >= 0) return true;
+    if (flag_ready(ptx::ld_acquire_gpu(flag), p.epoch)) return true;
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t n = 1;; ++n) {
         __nanosleep(40);
-        if ((int32_t)(ptx::ld_acquire_gpu(flag) - p.epoch) >= 0) {
+        if (flag_ready(ptx::ld_acquire_gpu(flag), p.epoch)) {
             waited_ns += ptx::globaltimer() - t0;
             return true;
         }
@@ -292,14 +293,7 @@ __device__ __forceinline__ int wait_smem_count(uint32_t addr, uint32_t total, ui
 // when every row lies past M (the odd CTA of a ragged last pair tile).
 __device__ __forceinline__ void chunk_range(const KernelParams &p, int r0, int nrows, int &lo,
                                             int &hi) {
-    const int r1 = min(r0 + nrows, p.M);
-    if (r0 >= r1) {
-        lo = 0;
-        hi = -1;
-        return;
-    }
-    lo = chunk_of_row(p.M_r, p.split, r0);
-    hi = chunk_of_row(p.M_r, p.split, r1 - 1);
+    chunk_range_of(p.M, p.M_r, p.split, r0, nrows, lo, hi);
 }
 
 // Does the tile starting at row r0 reduce peers?  AR: always; RS: tiles of the
@@ -315,8 +309,7 @@ __device__ __forceinline__ bool reduces(const KernelParams &p, int r0) {
 // A walker (a CTA, or a CTA pair) runs tile-list entries one after another:
 // walker u of n runs entries u, u + n, u + 2n, ...; -1 ends the walk.
 __device__ __forceinline__ int walk_entry(const KernelParams &p, int unit, int n_units, int i) {
-    const int t = p.t_begin + unit + i * n_units;
-    return t < p.t_end ? t : -1;
+    return walk_entry_of(p.t_begin, p.t_end, unit, n_units, i);
 }
 
 // ------------------------------------------------------------------ staging (device backends)
@@ -375,7 +368,7 @@ __device__ __forceinline__ void stage_slices(const KernelParams &p, int worker, 
     const int spt = p.slices_per_transfer;
     const int total = p.n_transfers * spt;
     const int n_flags = p.n_rc * p.R;
-    uint32_t *cnt = p.in_cnt + (size_t)(p.epoch & 1u) * n_flags;
+    uint32_t *cnt = p.in_cnt + (size_t)counter_half(p.epoch) * n_flags;
     uint32_t phase_bits = 0;
     for (int g = worker; g < total; g += W) {
         const int a = g / spt, sl = g % spt;
@@ -394,7 +387,7 @@ __device__ __forceinline__ void stage_slices(const KernelParams &p, int worker, 
             return;
         ptx::fence_proxy_async();
         const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + code, 1u);
-        if (old + 1u == (uint32_t)spt && a != p.drop_transfer)
+        if (completes_transfer(old, (uint32_t)spt) && a != p.drop_transfer)
             ptx::st_release_gpu(p.in_flags + code, p.epoch);
     }
 }
@@ -435,7 +428,7 @@ __device__ __forceinline__ void count_produced(const KernelParams &p, int r0, in
         ptx::fence_acq_rel_gpu();
         int lo, hi;
         chunk_range(p, r0, tile_m, lo, hi);
-        uint32_t *cnt = p.out_cnt + (size_t)(p.epoch & 1u) * p.n_rc;
+        uint32_t *cnt = p.out_cnt + (size_t)counter_half(p.epoch) * p.n_rc;
         for (int rc = lo; rc <= hi; ++rc) {
             const int64_t row0 = chunk_row0(p.M_r, p.split, rc);
             const int64_t row1 = chunk_row0(p.M_r, p.split, rc + 1);
@@ -641,8 +634,8 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
     // CTA 0 clears the counters of the other epoch parity for the next call.
     if (blockIdx.x == 0) {
         const int nf = p.n_rc * p.R;
-        uint32_t *nin = p.in_cnt + (size_t)((p.epoch + 1u) & 1u) * nf;
-        uint32_t *nout = p.out_cnt + (size_t)((p.epoch + 1u) & 1u) * p.n_rc;
+        uint32_t *nin = p.in_cnt + (size_t)spare_half(p.epoch) * nf;
+        uint32_t *nout = p.out_cnt + (size_t)spare_half(p.epoch) * p.n_rc;
         for (int i = threadIdx.x; i < nf; i += blockDim.x) nin[i] = 0u;
         for (int i = threadIdx.x; i < p.n_rc; i += blockDim.x) nout[i] = 0u;
     }

@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "protocol.h"
 #include "schedule.h"
 
 #if defined(__CUDACC__)
@@ -79,27 +80,16 @@ struct KernelParams {
 };
 
 // Receive-buffer slot of source rank q (the local rank has none).
-SYN_HD int recv_slot(int q, int rank) { return q - (q > rank ? 1 : 0); }
+SYN_HD int recv_slot(int q, int rank) { return recv_slot_of(q, rank); }
 
-// Source, destination and size of staging transfer `code` = rc * R + q, where
-// row chunk rc covers rows [row0, row1) (chunk_row0 in schedule.h):
-//   AG : shard q rows [row0 - q*M_r, ...)  ->  gathered rows [row0, row1)
-//   RS : peer q rows [row0, row1)           ->  recv[slot q] rows [row0 - rank*M_r, ...)
-//   AR : peer q rows [row0, row1)           ->  recv[slot q] rows [row0, row1)
+// Source, destination and size of staging transfer `code` (transfer_rows in
+// protocol.h gives the rows).
 SYN_HD void transfer_span(const KernelParams &p, int code, const uint8_t *&src, uint8_t *&dst,
                           int64_t &bytes) {
-    const int rc = code / p.R, q = code % p.R;
-    const int64_t row0 = chunk_row0(p.M_r, p.split, rc);
-    const int64_t row1 = chunk_row0(p.M_r, p.split, rc + 1);
-    bytes = (row1 - row0) * p.row_bytes;
-    if (p.op == OP_AG) {
-        src = p.stage_src[q] + (row0 - (int64_t)q * p.M_r) * p.row_bytes;
-        dst = p.stage_dst + row0 * p.row_bytes;
-    } else {
-        const int64_t row = row0 - (p.op == OP_RS ? (int64_t)p.rank * p.M_r : 0);
-        src = p.stage_src[q] + row0 * p.row_bytes;
-        dst = p.stage_dst + ((int64_t)recv_slot(q, p.rank) * p.recv_slot_rows + row) * p.row_bytes;
-    }
+    const TransferRows t = transfer_rows(p.op, p.R, p.rank, p.M_r, p.split, p.recv_slot_rows, code);
+    bytes = t.rows * p.row_bytes;
+    src = p.stage_src[t.q] + t.src_row * p.row_bytes;
+    dst = p.stage_dst + t.dst_row * p.row_bytes;
 }
 
 // Which compiled kernel instance a launch uses, and its grid.

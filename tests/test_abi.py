@@ -53,3 +53,13 @@ def test_null_arguments_are_rejected():
     assert L.syn_sync_status(None, None) == syn.ERR_INVALID
     assert L.syn_ag_gemm(None, None, None, None, None, None) == syn.ERR_INVALID
     assert L.syn_plan_query(None, None) == syn.ERR_INVALID
+
+
+def test_protocol_emulation_library_exports_its_header():
+    from chunk_scheduled_communication_gb300 import proto
+    src = open(os.path.join(ROOT, "include", "syn_proto.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = sorted(set(re.findall(r"\b(syn_[a-z0-9_]+)\s*\(", src)))
+    assert names == ["syn_proto_emulate", "syn_proto_last_error"]
+    lib = proto.lib()
+    assert all(hasattr(lib, n) for n in names)

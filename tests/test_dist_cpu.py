@@ -23,7 +23,7 @@ def _free_port():
 
 def _worker(rank, world, port, q):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
-                      RANK=str(rank), LOCAL_RANK=str(rank))
+                      RANK=str(rank), LOCAL_RANK=str(rank), SYN_DIST_BACKEND="gloo")
     import bench
     dist, r, ws, local = bench.dist_setup(world)
     assert (r, ws) == (rank, world)
