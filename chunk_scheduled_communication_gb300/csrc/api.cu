@@ -227,6 +227,8 @@ KernelParams base_params(syn_plan_s *pl) {
     p.colocated = 0;
     p.waits = 1;
     p.drop_transfer = pl->kn.debug_drop_chunk;
+    p.delay_transfer = pl->kn.debug_delay_us > 0 ? pl->kn.debug_delay_chunk : -1;
+    p.delay_ns = (uint32_t)std::min<int64_t>((int64_t)pl->kn.debug_delay_us * 1000, 4000000000ll);
     p.epoch = pl->epoch;
     p.timeout_ns = pl->kn.timeout_ns;
     p.tile_list = pl->d_tiles;
@@ -393,6 +395,7 @@ int syn_knobs_default(syn_knobs_t *k) {
     k->slice_kb = 128;
     k->timeout_ns = 0;
     k->debug_drop_chunk = -1;
+    k->debug_delay_chunk = -1;
     k->trace = 0;
     k->stages = 0;
     k->tile_k = 0;
@@ -507,9 +510,19 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
     PL_CK(cudaMalloc(&pl->d_stats, 2 * sizeof(unsigned long long)));
     PL_CK(cudaMemcpy(pl->d_tiles, s.tile_list.data(), s.tile_list.size() * sizeof(int32_t),
                      cudaMemcpyHostToDevice));
+    if (kn.debug_corrupt_entry > 0) {  // fault injection for the kernel's bounds checks
+        const int32_t bad_tile = s.n_tiles + 7;
+        const size_t i = (size_t)(kn.debug_corrupt_entry - 1) % s.tile_list.size();
+        PL_CK(cudaMemcpy(pl->d_tiles + i, &bad_tile, sizeof(int32_t), cudaMemcpyHostToDevice));
+    }
     if (!s.transfers.empty())
         PL_CK(cudaMemcpy(pl->d_transfers, s.transfers.data(), s.transfers.size() * sizeof(int32_t),
                          cudaMemcpyHostToDevice));
+    if (kn.debug_corrupt_entry > 0 && !s.transfers.empty()) {  // (the host keeps its own valid copy)
+        const int32_t bad_code = (int32_t)n_flags + 3;
+        const size_t i = (size_t)(kn.debug_corrupt_entry - 1) % s.transfers.size();
+        PL_CK(cudaMemcpy(pl->d_transfers + i, &bad_code, sizeof(int32_t), cudaMemcpyHostToDevice));
+    }
     PL_CK(cudaMemset(pl->d_err, 0, 4 * sizeof(int32_t)));
     PL_CK(cudaMemset(pl->d_in_flags, 0, n_flags * sizeof(uint32_t)));
     PL_CK(cudaMemset(pl->d_in_cnt, 0, 2 * n_flags * sizeof(uint32_t)));

@@ -312,6 +312,19 @@ __device__ __forceinline__ int walk_entry(const KernelParams &p, int unit, int n
     return walk_entry_of(p.t_begin, p.t_end, unit, n_units, i);
 }
 
+// Tile id at tile-list entry t, or -1 (with SYN_ERR_BOUNDS raised and the CTA
+// aborting) when the table holds an id outside the tile grid: no role ever
+// addresses memory from an unchecked entry.
+__device__ __forceinline__ int tile_at(const KernelParams &p, int t, volatile int *abort) {
+    const int tile = p.tile_list[t];
+    if (tile < 0 || tile >= p.tiles_m * p.tiles_n) {
+        raise_error(p, SYN_ERR_BOUNDS, WHERE_BOUNDS, t);
+        *abort = 1;
+        return -1;
+    }
+    return tile;
+}
+
 // ------------------------------------------------------------------ staging (device backends)
 // Copy `len` bytes src -> dst through an nbuf-slot shared-memory ring with TMA
 // bulk copies (global -> smem with mbarrier completion, smem -> global bulk
@@ -373,6 +386,11 @@ __device__ __forceinline__ void stage_slices(const KernelParams &p, int worker, 
     for (int g = worker; g < total; g += W) {
         const int a = g / spt, sl = g % spt;
         const int code = p.transfers[a];
+        if (code < 0 || code >= n_flags) {  // the transfer table holds a code outside the flags
+            raise_error(p, SYN_ERR_BOUNDS, WHERE_BOUNDS, a);
+            *abort = 1;
+            return;
+        }
         if (p.op == OP_AG && p.local_inplace && code % p.R == p.rank) continue;
         const uint8_t *src;
         uint8_t *dst;
@@ -387,8 +405,13 @@ __device__ __forceinline__ void stage_slices(const KernelParams &p, int worker, 
             return;
         ptx::fence_proxy_async();
         const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + code, 1u);
-        if (completes_transfer(old, (uint32_t)spt) && a != p.drop_transfer)
+        if (completes_transfer(old, (uint32_t)spt) && a != p.drop_transfer) {
+            if (a == p.delay_transfer) {  // fault injection: publish late (bounded by the delay)
+                const uint64_t t0 = ptx::globaltimer();
+                while (ptx::globaltimer() - t0 < p.delay_ns && !*abort) __nanosleep(1000);
+            }
             ptx::st_release_gpu(p.in_flags + code, p.epoch);
+        }
     }
 }
 
@@ -528,7 +551,9 @@ __device__ __forceinline__ void reduce_worker(const KernelParams &p, uint8_t *sm
         while (scan_j < j) {
             const int t = walk_entry(p, unit, n_units, scan_i++);
             if (t < 0) return;  // (cannot happen: the epilogue stored tile j)
-            if (reduces<OP>(p, (p.tile_list[t] / p.tiles_n) * C::TILE_M)) {
+            const int tl = tile_at(p, t, abort);
+            if (tl < 0) return;
+            if (reduces<OP>(p, (tl / p.tiles_n) * C::TILE_M)) {
                 ++scan_j;
                 cur_t = t;
             }
@@ -652,7 +677,8 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
             for (int i = 0; ok; ++i) {
                 const int t = walk_entry(p, unit, n_units, i);
                 if (t < 0) break;
-                const int tile = p.tile_list[t];
+                const int tile = tile_at(p, t, abort);
+                if (tile < 0) break;
                 const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
                 const int r0 = tmi * C::TILE_M + (int)crank * C::BM;  // this CTA's rows
                 if (OP == OP_AG && p.waits) {
@@ -810,7 +836,8 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
         for (int i = 0;; ++i) {
             const int t = walk_entry(p, unit, n_units, i);
             if (t < 0) break;
-            const int tile = p.tile_list[t];
+            const int tile = tile_at(p, t, abort);
+            if (tile < 0) break;
             const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
             const int acc = (int)(tc & 1u);
             const uint32_t aph = (tc >> 1) & 1u;
@@ -998,7 +1025,8 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
             for (int i = 0; ok; ++i) {
                 const int t = walk_entry(p, unit, n_units, i);
                 if (t < 0) break;
-                const int tile = p.tile_list[t];
+                const int tile = tile_at(p, t, abort);
+                if (tile < 0) break;
                 const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
                 const int tr0 = tmi * C::TILE_M;
                 if (!reduces<OP>(p, tr0)) continue;

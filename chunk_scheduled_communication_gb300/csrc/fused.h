@@ -51,6 +51,8 @@ struct KernelParams {
     int32_t waits;                 // consumers wait on in_flags
     int32_t local_inplace;         // AG: local shard aliases its gathered slot
     int32_t drop_transfer;         // fault injection: arrival index never published
+    int32_t delay_transfer;        // fault injection: arrival index published late (device stagers)
+    uint32_t delay_ns;             //   by this long
     int32_t peer_row_off;          // row coordinate offset of the peer tensor maps
     uint32_t epoch;
     uint64_t timeout_ns;

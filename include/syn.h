@@ -156,6 +156,18 @@ typedef struct {
     int ce_streams;        /* CE: side streams the chunk copies are spread over
                               round-robin in arrival order, so several copy
                               engines run at once (0 = 4; at most 16)        */
+    int debug_delay_chunk; /* fault injection (device stagers: TMA_DEDICATED,
+                              TMA_COLOCATED): arrival index of a staging
+                              transfer whose ready flag is published
+                              debug_delay_us late; the call only waits longer
+                              unless that exceeds timeout_ns                  */
+    int debug_delay_us;    /* (0 = off)                                        */
+    int debug_corrupt_entry; /* fault injection for the kernel's bounds checks
+                              (0 = off): n > 0 gives the device copy of
+                              tile-list entry n - 1 (and of transfer-list
+                              entry (n - 1) mod n_transfers) an out-of-range
+                              value at plan creation; every call then ends in
+                              SYN_ERR_BOUNDS, with no out-of-range access     */
 } syn_knobs_t;
 
 /* Everything a caller or a test may want to know about a plan. */

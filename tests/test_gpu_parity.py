@@ -247,6 +247,51 @@ def test_dropped_chunk_times_out_then_recovers(backend, tile_m):
     check_against_oracle(w, 0, {"out": runner.dev_to_u16(d.out), "gathered": runner.dev_to_u16(d.gathered)})
 
 
+@pytest.mark.parametrize("backend,tile_m,op", [
+    ("tma_colocated", 256, "ag"), ("tma_dedicated", 128, "ag"), ("ce", 128, "ag"), ("decomposed", 256, "ag"),
+    ("tma_colocated_smem", 256, "rs"), ("tma_colocated_smem", 256, "ar"), ("tma_colocated_smem", 128, "ar")])
+def test_corrupt_table_entry_is_caught(backend, tile_m, op):
+    """A tile-list entry (and a transfer-list entry) outside its range in the
+    device tables is caught by the kernel's bounds checks: SYN_ERR_BOUNDS on
+    every call, no out-of-range access, and a clean plan works afterwards."""
+    w = {"ag": INT_AG_PAIR, "rs": INT_RS_PAIR, "ar": INT_AR_PAIR}[op]
+    inp = inputs(w, 1, 0, "int")
+    d = runner.upload(inp)
+    with runner.make_plan(d, split=2, order="row", backend=backend, tile_m=tile_m, comm_sms=2,
+                          corrupt_entry=4, timeout_ns=200_000_000) as bad:
+        for _ in range(2):
+            runner.call(bad, d)
+            assert bad.sync() == syn.ERR_BOUNDS
+    with runner.make_plan(d, split=2, order="row", backend=backend, tile_m=tile_m, comm_sms=2) as good:
+        runner.call(good, d)
+        assert good.sync() == syn.OK
+    got = {"out": runner.dev_to_u16(d.out)}
+    if op == "ag":
+        got["gathered"] = runner.dev_to_u16(d.gathered)
+    else:
+        got["f32"] = d.f32_out.cpu().numpy()
+    check_against_oracle(w, 1, got, kind="int")
+
+
+@pytest.mark.parametrize("backend", ["tma_colocated", "tma_dedicated"])
+def test_late_flag_from_a_device_stager_only_delays(backend):
+    """A chunk flag published 3 ms late (fault injection in the device
+    stager) only lengthens the flag waits; the call succeeds and matches."""
+    w, r = INT_AG_PAIR, 0
+    inp = inputs(w, r, 0, "int")
+    d = runner.upload(inp)
+    waits = []
+    for delay in (0, 3000):
+        with runner.make_plan(d, split=2, order="row", backend=backend, tile_m=256, comm_sms=2, trace=1,
+                              delay_chunk=2, delay_us=delay) as plan:
+            runner.call(plan, d)
+            assert plan.sync() == syn.OK
+            waits.append(plan.stats()[0])
+        check_against_oracle(w, r, {"out": runner.dev_to_u16(d.out), "gathered": runner.dev_to_u16(d.gathered)},
+                             kind="int")
+    assert waits[1] > waits[0] + 1_000_000  # at least one CTA waited over a millisecond longer
+
+
 def test_trace_counters():
     w = wl.scaled(wl.LLAMA3_8B_UP_AG, M=8 * 256, K=1024, N=512)
     inp = inputs(w, 0)
