@@ -329,10 +329,11 @@ __device__ __forceinline__ int tile_at(const KernelParams &p, int t, volatile in
 // Copy `len` bytes src -> dst through an nbuf-slot shared-memory ring with TMA
 // bulk copies (global -> smem with mbarrier completion, smem -> global bulk
 // group).  `phase_bits` carries each slot's barrier parity across calls.
+template <typename Landed>
 __device__ __forceinline__ bool bulk_copy(const uint8_t *src, uint8_t *dst, int64_t len,
                                           uint32_t buf0, int nbuf, uint32_t buf_bytes,
                                           uint32_t bar0, uint32_t &phase_bits,
-                                          volatile int *abort, const KernelParams &p) {
+                                          volatile int *abort, const KernelParams &p, Landed &&prev_landed) {
     const int n = (int)((len + buf_bytes - 1) / buf_bytes);
     auto piece = [&](int i) -> uint32_t {
         const int64_t rem = len - (int64_t)i * buf_bytes;
@@ -344,8 +345,14 @@ __device__ __forceinline__ bool bulk_copy(const uint8_t *src, uint8_t *dst, int6
         ptx::mbar_arrive_expect_tx(bar0 + 8 * b, bytes);
         ptx::bulk_g2s(buf0 + b * buf_bytes, src + (int64_t)i * buf_bytes, bytes, bar0 + 8 * b);
     };
+    // the previous range's stores must have read the buffers before they are
+    // refilled; their completion in global memory is awaited only after this
+    // range's first loads are in flight (prev_landed), so that wait and the
+    // previous range's flag publication overlap the new loads
+    ptx::bulk_wait_read_all();
     const int pre = n < nbuf ? n : nbuf;
     for (int i = 0; i < pre; ++i) issue(i);
+    prev_landed();
     for (int i = 0; i < n; ++i) {
         const int b = i % nbuf;
         const uint32_t par = (phase_bits >> b) & 1u;
@@ -368,8 +375,7 @@ __device__ __forceinline__ bool bulk_copy(const uint8_t *src, uint8_t *dst, int6
             issue(i + nbuf);
         }
     }
-    ptx::bulk_wait_all();  // every store of this range has completed
-    return true;
+    return true;  // this range's stores may still be in flight
 }
 
 // Stage this worker's share of chunk slices (worker w of W takes global slices
@@ -383,10 +389,31 @@ __device__ __forceinline__ void stage_slices(const KernelParams &p, int worker, 
     const int n_flags = p.n_rc * p.R;
     uint32_t *cnt = p.in_cnt + (size_t)counter_half(p.epoch) * n_flags;
     uint32_t phase_bits = 0;
+    // the slice whose stores were issued last and are not yet counted (-1: none)
+    int pend_a = -1, pend_code = 0;
+    auto count_slice = [&](int a, int code) {  // its bytes have landed
+        ptx::fence_proxy_async();
+        const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + code, 1u);
+        if (completes_transfer(old, (uint32_t)spt) && a != p.drop_transfer) {
+            if (a == p.delay_transfer) {  // fault injection: publish late (bounded by the delay)
+                const uint64_t t0 = ptx::globaltimer();
+                while (ptx::globaltimer() - t0 < p.delay_ns && !*abort) __nanosleep(1000);
+            }
+            ptx::st_release_gpu(p.in_flags + code, p.epoch);
+        }
+    };
+    auto land_pending = [&]() {
+        if (pend_a >= 0) {
+            ptx::bulk_wait_all();
+            count_slice(pend_a, pend_code);
+            pend_a = -1;
+        }
+    };
     for (int g = worker; g < total; g += W) {
         const int a = g / spt, sl = g % spt;
         const int code = p.transfers[a];
         if (code < 0 || code >= n_flags) {  // the transfer table holds a code outside the flags
+            land_pending();
             raise_error(p, SYN_ERR_BOUNDS, WHERE_BOUNDS, a);
             *abort = 1;
             return;
@@ -400,19 +427,18 @@ __device__ __forceinline__ void stage_slices(const KernelParams &p, int worker, 
         const int64_t off = (int64_t)sl * p.slice_bytes;
         const int64_t rem = bytes - off;
         const int64_t len = rem < p.slice_bytes ? rem : p.slice_bytes;
-        if (len > 0 &&
-            !bulk_copy(src + off, dst + off, len, buf0, nbuf, buf_bytes, bar0, phase_bits, abort, p))
-            return;
-        ptx::fence_proxy_async();
-        const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + code, 1u);
-        if (completes_transfer(old, (uint32_t)spt) && a != p.drop_transfer) {
-            if (a == p.delay_transfer) {  // fault injection: publish late (bounded by the delay)
-                const uint64_t t0 = ptx::globaltimer();
-                while (ptx::globaltimer() - t0 < p.delay_ns && !*abort) __nanosleep(1000);
-            }
-            ptx::st_release_gpu(p.in_flags + code, p.epoch);
+        if (len > 0) {
+            if (!bulk_copy(src + off, dst + off, len, buf0, nbuf, buf_bytes, bar0, phase_bits, abort, p,
+                           land_pending))
+                return;
+            pend_a = a;
+            pend_code = code;
+        } else {
+            land_pending();
+            count_slice(a, code);
         }
     }
+    land_pending();
 }
 
 // ------------------------------------------------------------------ epilogue helpers
