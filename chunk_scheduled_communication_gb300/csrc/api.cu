@@ -480,6 +480,10 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
                     "no compiled kernel for tile_m " + std::to_string(s.tile_m) + ", tile_n " +
                         std::to_string(pl->lc.tile_n) + ", tile_k " + std::to_string(pl->lc.tile_k) +
                         ", stages " + std::to_string(pl->lc.stages) + " with this operator and backend");
+    if (kn.rs_push && (s.op != SYN_OP_GEMM_RS || epi_tma_rs(pl->lc) != 1))
+        return bail(SYN_ERR_UNSUPPORTED,
+                    "rs_push needs GEMM-RS with TMA_COLOCATED_SMEM reducer warps and a pipeline depth "
+                    "that leaves room for the epilogue's store staging (tile_n 256)");
     // CTAs that can be resident at once: one per SM, or (CTA pairs) twice the
     // co-resident 2-CTA clusters, which may be fewer than SMs / 2
     pl->resident = pl->num_sms;
@@ -699,6 +703,7 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
     p.red_buf = red_buf;
     p.red_row_off = red_row_off;
     p.epi_tma = 1;
+    p.send_push = (op == SYN_OP_GEMM_RS && plan->kn.rs_push) ? 1 : 0;
     p.recv_slot_rows = plan->recv_slot_rows;
     p.peer_row_off = (staged && op == SYN_OP_GEMM_RS) ? (int32_t)(s.rank * s.M_r) : 0;
     p.out = static_cast<uint16_t *>(out);

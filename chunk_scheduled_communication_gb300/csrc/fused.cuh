@@ -949,7 +949,12 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            ptx::tma_store_2d(fmap, buf, col, fy);
+                            // GEMM-RS push mode: send rows are added into the
+                            // destination's receive accumulator
+                            if (OP == OP_RS && !red && p.send_push)
+                                ptx::tma_reduce_add_2d(fmap, buf, col, fy);
+                            else
+                                ptx::tma_store_2d(fmap, buf, col, fy);
                             ptx::bulk_commit();
                         }
                     }
@@ -1255,6 +1260,15 @@ int smem_bytes_op(const LaunchCfg &lc) {
     int bytes = -1;
     dispatch_cfg<OP>(lc, [&](auto c) { bytes = decltype(c)::SMEM_ALLOC; });
     return bytes;
+}
+
+// 1 when the instance stages its epilogue stores through TMA, 0 when not,
+// -1 when it is not compiled.
+template <int OP>
+int epi_tma_op(const LaunchCfg &lc) {
+    int e = -1;
+    dispatch_cfg<OP>(lc, [&](auto c) { e = decltype(c)::EPI_TMA ? 1 : 0; });
+    return e;
 }
 
 template <int OP>

@@ -75,6 +75,7 @@ struct KernelParams {
     int64_t recv_slot_rows;        // RS/AR: rows per peer slot of the receive buffer
     uint16_t *out;                 // AG: C; RS: out_r; AR: out   (bf16)
     float *f32_out;                // RS: send; AR: publish  (nullable)
+    int32_t send_push;             // GEMM-RS push mode: send rows are added into `send`
     int32_t epi_tma;               // the f32out / red / c tensor maps are encoded: instances
                                    // with staging room store the epilogue through TMA
     float *red_buf;                // RED instances: fp32 partials of the reducing tiles,
@@ -126,6 +127,9 @@ inline int default_stages(int op, int tile_n, int tile_k, bool stg, bool pair, b
 }
 // Co-resident 2-CTA clusters for a pair instance (0 if unknown / not a pair).
 int fused_max_clusters(int op, const LaunchCfg &lc);
+// GEMM-RS: 1 if the instance stores its epilogue through TMA (needed by the
+// push mode), 0 if not, -1 if not compiled.
+int epi_tma_rs(const LaunchCfg &lc);
 
 // Record the message syn_last_error() returns on this thread.
 void set_last_error(const std::string &msg);

@@ -14,4 +14,6 @@ int smem_bytes_rs(const LaunchCfg &lc) { return smem_bytes_op<OP_RS>(lc); }
 
 int max_clusters_rs(const LaunchCfg &lc) { return max_clusters_op<OP_RS>(lc); }
 
+int epi_tma_rs(const LaunchCfg &lc) { return epi_tma_op<OP_RS>(lc); }
+
 }  // namespace syn

@@ -141,6 +141,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                  "r"(x), "r"(y), "r"(src)
                  : "memory");
 }
+// shared -> global tile reduce-add (fp32 add into the destination, performed
+// at the memory side; bulk group of the issuing thread)
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
 // wait until at most N of this thread's bulk groups still read shared memory
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {

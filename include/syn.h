@@ -156,6 +156,13 @@ typedef struct {
     int ce_streams;        /* CE: side streams the chunk copies are spread over
                               round-robin in arrival order, so several copy
                               engines run at once (0 = 4; at most 16)        */
+    int rs_push;           /* GEMM-RS, TMA_COLOCATED_SMEM with reducer warps:
+                              0 = pull mode (send rows stored for the peers to
+                              pull); 1 = push mode: each send row is added
+                              (fp32, TMA reduce-add at the destination) into
+                              `send`, which then holds the destination ranks'
+                              receive accumulators that all ranks add into;
+                              SYN_ERR_UNSUPPORTED elsewhere                   */
     int debug_delay_chunk; /* fault injection (device stagers: TMA_DEDICATED,
                               TMA_COLOCATED): arrival index of a staging
                               transfer whose ready flag is published

@@ -527,6 +527,54 @@ def test_copy_engine_streams_bit_exact(ce_streams):
                          kind="int")
 
 
+@pytest.mark.parametrize("w,stages,kind", [(INT_RS_SPREAD, 5, "int"), (INT_RS_PAIR, 6, "int"),
+                                           (wl.LLAMA3_8B_DOWN_RS, 6, "normal")], ids=["spread", "pair", "full"])
+def test_rs_push_mode_adds_send_rows(w, stages, kind):
+    """GEMM-RS push mode: every send row is added (fp32, TMA reduce-add) into
+    `send`, the destination ranks' receive accumulators; rows of the local
+    block are untouched and out_r is unchanged.  The added value is the same
+    P the pull mode stores, so the result is bit-exact against init + P, and
+    a second call adds P again."""
+    r = 1
+    inp = inputs(w, r, 0, kind)
+    rng = np.random.default_rng(7)
+    init = rng.integers(-4, 5, size=(w.M, w.N)).astype(np.float32) if kind == "int" else \
+        rng.standard_normal((w.M, w.N)).astype(np.float32)
+    common = dict(split=1, order="row", backend="tma_colocated_smem", tile_m=256, tile_n=256, stages=stages)
+    d = runner.upload(inp)
+    with runner.make_plan(d, **common) as pull:  # P rows as the pull mode stores them
+        runner.call(pull, d)
+        assert pull.sync() == syn.OK
+    P = d.f32_out.cpu().numpy()
+    d.f32_out.copy_(torch.from_numpy(init))
+    with runner.make_plan(d, rs_push=1, **common) as push:
+        runner.call(push, d)
+        assert push.sync() == syn.OK, syn.lib().syn_last_error()
+        once = d.f32_out.cpu().numpy()
+        runner.call(push, d)
+        assert push.sync() == syn.OK
+        twice = d.f32_out.cpu().numpy()
+    keep = np.ones(w.M, bool)
+    keep[r * w.M_r:(r + 1) * w.M_r] = False
+    assert (once[keep] == (init[keep] + P[keep])).all()
+    assert (twice[keep] == ((init[keep] + P[keep]) + P[keep])).all()
+    assert (once[~keep] == init[~keep]).all() and (twice[~keep] == init[~keep]).all()
+    check_against_oracle(w, r, {"out": runner.dev_to_u16(d.out)}, kind=kind)
+
+
+def test_rs_push_mode_rejected_where_unsupported():
+    inp = inputs(INT_AR_PAIR, 0, 0, "int")
+    d = runner.upload(inp)
+    with pytest.raises(syn.SynError) as e:
+        runner.make_plan(d, backend="tma_colocated_smem", tile_m=256, rs_push=1)
+    assert e.value.status == syn.ERR_UNSUPPORTED
+    inp = inputs(INT_RS_PAIR, 0, 0, "int")
+    d = runner.upload(inp)
+    with pytest.raises(syn.SynError) as e:
+        runner.make_plan(d, backend="ce", tile_m=256, rs_push=1)
+    assert e.value.status == syn.ERR_UNSUPPORTED
+
+
 def test_uncompiled_stage_count_is_rejected():
     inp = inputs(INT_AR_N512, 0, 0, "int")
     d = runner.upload(inp)
