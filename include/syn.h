@@ -86,9 +86,12 @@ typedef enum {
     SYN_BACKEND_TMA_COLOCATED = 2,  /* one staging warp in every GEMM CTA copies
                                        chunk slices with TMA bulk copies (mbarrier
                                        pipelined), slice ownership by CTA index  */
-    SYN_BACKEND_TMA_COLOCATED_SMEM = 3, /* GEMM-RS/AR only: each GEMM CTA fetches
-                                       the peer tiles it needs straight into
-                                       shared memory with TMA (no global staging) */
+    SYN_BACKEND_TMA_COLOCATED_SMEM = 3, /* GEMM-RS/AR only: the peers' partials are
+                                       resident and read in place, no global
+                                       staging: by reducer warps with plain
+                                       loads (default at tile_n 256, see
+                                       knobs.reduce_warps) or through a TMA ring
+                                       of peer tiles in the epilogue            */
     SYN_BACKEND_UNFUSED = 4,        /* baseline: whole staging copy first, then
                                        the same GEMM kernel without waits         */
     SYN_BACKEND_DECOMPOSED = 5      /* baseline: one GEMM launch per chunk group,
@@ -108,7 +111,10 @@ typedef struct {
 typedef struct {
     syn_backend_t backend;
     int comm_sms;          /* TMA_DEDICATED: CTAs (SMs) given to staging, 1..32  */
-    int tile_m;            /* 128 (0 = default)                                  */
+    int tile_m;            /* rows per output tile: 128 (one CTA per tile) or
+                              256 (a 2-CTA cluster shares the tile with
+                              cta_group::2 UMMAs; GEMM-RS then needs M/R to be
+                              a multiple of 256); 0 = 128                     */
     int tile_n;            /* 128 or 256 (0 = 256)                               */
     int group_m;           /* SYN_ORDER_GROUPED group height in tiles (0 = 8)   */
     int slice_kb;          /* device stagers: KiB per slice of a chunk (0 = 128) */
@@ -120,15 +126,19 @@ typedef struct {
     int trace;             /* 1 = accumulate flag-wait and CTA-busy nanoseconds
                               (read with syn_plan_stats); 2 = also record four
                               global-timer stamps and the walker per tile of
-                              the last call
-                              (read with syn_plan_trace)                       */
-    int stages;            /* GEMM shared-memory pipeline depth (0 = default:
-                              AG 4 / RS, AR 3 at tile_n 256; 6 / 4 at 128).
-                              With TMA_COLOCATED_SMEM the peer-tile ring gets
-                              the shared memory the stages leave: tile_n 256
-                              takes 2, 3 or 4; tile_n 128 takes 3, 4 or 6.
-                              At tile_k 32: AG 8 (co-located) / 9, RS and AR
-                              6 (co-located) or 4, 5, 6.                     */
+                              the last call (read with syn_plan_trace)        */
+    int stages;            /* GEMM shared-memory pipeline depth; 0 = the
+                              default of the chosen instance:
+                                tile_m 256: AG 5 (co-located stagers) / 7;
+                                  RS / AR with reducer warps 6 / 5, with the
+                                  epilogue peer ring 4;
+                                tile_m 128: reducer warps 4; AG 4 / 6
+                                  (tile_n 256 / 128); RS, AR 3 / 4;
+                                tile_k 32: AG 8 (co-located) / 9, RS, AR 6.
+                              Other compiled depths: tile_m 256 AG 4-7, RS /
+                              AR 3-7; tile_m 128 RS / AR 2-6 (the peer ring
+                              takes the memory the stages leave).  A depth
+                              that is not compiled is SYN_ERR_UNSUPPORTED.   */
     int tile_k;            /* k-block depth per pipeline stage: 64 or 32
                               (0 = 64).  32 halves each stage, so twice as
                               many fit and more loads are in flight.         */
@@ -253,7 +263,9 @@ int syn_ag_gemm(syn_plan_t plan, const void *const *shards, void *gathered,
  *                   rows of rank r are not written
  *   out_r         : bf16 [M/R, N] = rne(P[rows_r] + sum_{q != r, ascending}
  *                   peer_q[rows_r])
- * Send tiles run first (in ring order of their destination), reduce tiles last. */
+ * Send tiles run first (in ring order of their destination), reduce tiles last
+ * when peers are staged; with resident peers (TMA_COLOCATED_SMEM) the reduce
+ * tiles are spread over the walk (knobs.reduce_spread). */
 int syn_gemm_rs(syn_plan_t plan, const void *A, const void *B,
                 const float *const *peer_partials, float *send, void *out_r,
                 void *stream);
