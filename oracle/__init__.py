@@ -1,4 +1,4 @@
-"""Plain CPU oracle for AG-GEMM, GEMM-RS and GEMM-AR (test infrastructure).
+"""Plain CPU oracle for AG-GEMM, GEMM-RS, GEMM-AR and A2A-GEMM (test infrastructure).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` leg of ``bench.py`` may import this package; the product path
@@ -11,8 +11,9 @@ marshals numpy arrays through ctypes.
 
 Every function follows the plain definition of the operator as the Syncopate
 summary page names them ("Experiments", paper §6.1: AG-GEMM, GEMM-RS,
-GEMM-AR); chunking and tile order never change these values (method section,
-paper §5.1-§5.2).
+GEMM-AR; A2A-GEMM, the all-to-all + expert GEMM of the sensitivity study,
+paper §6.3 / Fig. 11); chunking and tile order never change these values
+(method section, paper §5.1-§5.2).
 
 Parity pins for every entry point are in ``tests/test_oracle_pins.py``.
 """
@@ -66,8 +67,9 @@ def _load():
         lib.oracle_gemm_rs_out.argtypes = [i32, i32, i64, i64, i64, p, p, p, i64, i64, p]
         lib.oracle_gemm_rs_send.argtypes = [i32, i32, i64, i64, i64, p, p, i64, i64, p]
         lib.oracle_gemm_ar.argtypes = [i32, i32, i64, i64, i64, p, p, p, i64, i64, p, p]
+        lib.oracle_a2a_gemm.argtypes = [i32, p, i64, i64, p, p, i64, i64, p, p]
         for f in ("oracle_gather", "oracle_gemm_f32", "oracle_ag_gemm", "oracle_gemm_rs_out",
-                  "oracle_gemm_rs_send", "oracle_gemm_ar"):
+                  "oracle_gemm_rs_send", "oracle_gemm_ar", "oracle_a2a_gemm"):
             getattr(lib, f).restype = None
         _lib = lib
         return lib
@@ -147,6 +149,26 @@ def ag_gemm(shards, B, row0: int = 0, row1: int | None = None, want_gathered: bo
     g = np.empty((M, K), dtype=np.uint16) if want_gathered else None
     lib.oracle_ag_gemm(R, M_r, K, N, _ptr_array(shards), _ptr(B), row0, row1,
                        _ptr(g) if g is not None else None, _ptr(C))
+    return g, C
+
+
+def a2a_gemm(parts, B, row0: int = 0, row1: int | None = None, want_gathered: bool = True):
+    """A2A-GEMM: parts[q] is the [rows_from[q], K] block source q sends (may
+    have 0 rows).  Returns (stacked input or None, C rows [row0,row1) as bf16
+    bits)."""
+    lib = _load()
+    B = _u16(B)
+    K, N = B.shape
+    parts = [_u16(np.asarray(x).reshape(-1, K)) for x in parts]
+    R = len(parts)
+    rows = np.array([x.shape[0] for x in parts], dtype=np.int64)
+    M = int(rows.sum())
+    row1 = M if row1 is None else row1
+    assert 0 <= row0 <= row1 <= M
+    C = np.empty((row1 - row0, N), dtype=np.uint16)
+    g = np.empty((M, K), dtype=np.uint16) if want_gathered else None
+    lib.oracle_a2a_gemm(R, _ptr(rows), K, N, _ptr_array(parts), _ptr(B), row0, row1,
+                        _ptr(g) if g is not None else None, _ptr(C))
     return g, C
 
 

@@ -1,5 +1,5 @@
 /*
- * syn_oracle.c -- plain CPU oracle for the three chunk-overlapped operators.
+ * syn_oracle.c -- plain CPU oracle for the chunk-overlapped operators.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
  * call this file: only the tests, the smoke check and the CPU-baseline leg of
@@ -20,6 +20,10 @@
  *              send[rows_q] = P[rows_q], q != r
  *              out_r = bf16_rne(P[rows_r] + sum_{q != r, ascending q} peer_q[rows_r])
  *   GEMM-AR  : out = bf16_rne(P + sum_{q != r, ascending q} peer_q);  publish = P
+ *   A2A-GEMM : G = concat_q(part_q), parts of rows_from[q] rows (bit copy),
+ *              C = bf16_rne(G . B)   -- the MoE-style all-to-all + expert
+ *              GEMM that the paper's sensitivity study (§6.3, Fig. 11)
+ *              tunes beside the other three
  *
  * Arithmetic.  bf16 inputs are widened exactly (bits << 16).  Every dot
  * product accumulates in fp32, sequentially in k, starting from +0.0.  The
@@ -133,6 +137,48 @@ void oracle_ag_gemm(int R, int64_t M_r, int64_t K, int64_t N,
         for (int64_t i = row0; i < row1; ++i) {
             const uint16_t *a = shards[i / M_r] + (i % M_r) * K;
             dot_row(a, B, N, K, N, acc);
+            uint16_t *c = C + (i - row0) * N;
+            for (int64_t j = 0; j < N; ++j)
+                c[j] = oracle_bf16_rne(acc[j]);
+        }
+        free(acc);
+    }
+}
+
+/* A2A-GEMM over rows [row0, row1) of the received row space.
+ * The all-to-all hands rank r one part per source rank q (rows_from[q] rows,
+ * possibly none); the expert's input is those parts stacked in ascending q:
+ *   G[off_q + i] = part_q[i],  off_q = rows_from[0] + ... + rows_from[q-1]
+ *   C = bf16_rne(G . B)
+ * The part holding row i is found by walking the parts in order.  If
+ * `gathered` is not NULL the whole stacked matrix [sum rows_from, K] is
+ * written too (independently of the row range). */
+void oracle_a2a_gemm(int R, const int64_t *rows_from, int64_t K, int64_t N,
+                     const uint16_t *const *parts, const uint16_t *B,
+                     int64_t row0, int64_t row1,
+                     uint16_t *gathered, uint16_t *C)
+{
+    if (gathered) {
+        int64_t off = 0;
+        for (int q = 0; q < R; ++q) {
+            if (rows_from[q] > 0)
+                memcpy(gathered + off * K, parts[q],
+                       (size_t)(rows_from[q] * K) * sizeof(uint16_t));
+            off += rows_from[q];
+        }
+    }
+#pragma omp parallel
+    {
+        float *acc = (float *)malloc((size_t)N * sizeof(float));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = row0; i < row1; ++i) {
+            int q = 0;
+            int64_t off = 0;
+            while (i >= off + rows_from[q]) {
+                off += rows_from[q];
+                ++q;
+            }
+            dot_row(parts[q] + (i - off) * K, B, N, K, N, acc);
             uint16_t *c = C + (i - row0) * N;
             for (int64_t j = 0; j < N; ++j)
                 c[j] = oracle_bf16_rne(acc[j]);

@@ -337,3 +337,82 @@ def test_single_rank_ar_is_plain_gemm(oracle_lib):
     _, C = oracle_lib.ag_gemm([A], B)
     out, _ = oracle_lib.gemm_ar(A, B, [None], 1, 0)
     assert (out == C).all()
+
+
+# --------------------------------------------------------------------------- A2A-GEMM
+# The all-to-all + expert GEMM of the paper's sensitivity study (§6.3, Fig. 11):
+# rank r's expert multiplies the rows every source q sends it (rows_from[q],
+# possibly 0), stacked in ascending q.
+def _parts(rng, rows_from, K, make=None):
+    make = make or (lambda shape: _rand_bits(rng, shape))
+    return [make((m, K)) for m in rows_from]
+
+
+def test_hand_worked_a2a(oracle_lib):
+    g = json.load(open(os.path.join(GOLD, "hand_worked_ops.json")))["a2a_gemm"]
+    parts = [_bits(np.array(x, dtype=np.float32).reshape(-1, 2)) for x in g["parts"]]
+    gathered, C = oracle_lib.a2a_gemm(parts, _bits(g["B"]))
+    assert (gathered == _bits(g["gathered"])).all()
+    assert (C == np.array(g["C_bits"], dtype=np.uint16)).all(), g["derivation"]
+
+
+@pytest.mark.parametrize("rows_from", [[5, 0, 9, 1], [0, 0, 7], [3], [1, 1, 1, 1, 1, 1, 1, 1], [0, 12]])
+def test_a2a_brute_force_fp64(oracle_lib, rows_from):
+    rng = np.random.default_rng(sum(rows_from) + len(rows_from))
+    K, N = 48, 20
+    parts = _parts(rng, rows_from, K)
+    B = _rand_bits(rng, (K, N), 0.5)
+    gathered, C = oracle_lib.a2a_gemm(parts, B)
+    G = np.concatenate([bits_to_f64(p) for p in parts])
+    assert (bits_to_f64(gathered) == G).all()
+    Bf = bits_to_f64(B)
+    _check_bound(C, G @ Bf, np.abs(G) @ np.abs(Bf), K)
+
+
+def test_a2a_integer_inputs_exact(oracle_lib):
+    rng = np.random.default_rng(21)
+    rows_from, K, N = [4, 0, 11, 2, 0, 6], 96, 18
+    ints = lambda shape: wl.to_bf16_bits(rng.integers(-3, 4, size=shape).astype(np.float32))
+    parts = _parts(rng, rows_from, K, ints)
+    B = ints((K, N))
+    _, C = oracle_lib.a2a_gemm(parts, B)
+    exact = np.concatenate([bits_to_f64(p) for p in parts]) @ bits_to_f64(B)
+    assert (C == torch_rne(exact)).all()
+
+
+def test_a2a_rows_come_from_their_own_part(oracle_lib):
+    """Each part filled with its own constant: row i of C must carry the
+    constant of the part that holds row i (catches a wrong offset or an index
+    into the wrong part)."""
+    rows_from, K, N = [3, 0, 5, 1, 0, 2], 64, 8
+    parts = [wl.to_bf16_bits(np.full((m, K), q + 1, np.float32)) for q, m in enumerate(rows_from)]
+    B = wl.to_bf16_bits(np.full((K, N), 1.0, np.float32))
+    _, C = oracle_lib.a2a_gemm(parts, B)
+    want = np.concatenate([np.full(m, (q + 1) * K, np.float64) for q, m in enumerate(rows_from)])
+    assert (bits_to_f64(C) == want[:, None]).all()
+
+
+def test_a2a_equal_parts_is_ag_gemm(oracle_lib):
+    rng = np.random.default_rng(22)
+    R, M_r, K, N = 4, 6, 64, 24
+    shards = [_rand_bits(rng, (M_r, K)) for _ in range(R)]
+    B = _rand_bits(rng, (K, N))
+    g0, C0 = oracle_lib.ag_gemm(shards, B)
+    g1, C1 = oracle_lib.a2a_gemm(shards, B)
+    assert (g0 == g1).all() and (C0 == C1).all()
+
+
+def test_a2a_part_independence_and_row_ranges(oracle_lib):
+    rng = np.random.default_rng(23)
+    rows_from, K, N = [7, 2, 0, 13], 40, 16
+    parts = _parts(rng, rows_from, K)
+    B = _rand_bits(rng, (K, N))
+    _, C = oracle_lib.a2a_gemm(parts, B)
+    off = np.concatenate([[0], np.cumsum(rows_from)])
+    for q, m in enumerate(rows_from):
+        if m:
+            _, Cq = oracle_lib.ag_gemm([parts[q]], B)   # the part alone
+            assert (C[off[q]:off[q + 1]] == Cq).all()
+    M = int(off[-1])
+    pieces = [oracle_lib.a2a_gemm(parts, B, a, b, want_gathered=False)[1] for a, b in [(0, 8), (8, 9), (9, M)]]
+    assert (np.concatenate(pieces) == C).all()
