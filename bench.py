@@ -50,18 +50,26 @@ DEFAULT_KNOBS = {
     "ag": dict(backend="tma_colocated", split=4, order="grouped", tile_m=256, tile_n=256, comm_sms=8, stages=0),
     "rs": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=6),
     "ar": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=5),
+    "a2a": dict(backend="tma_colocated", split=2, order="grouped", tile_m=256, tile_n=256, comm_sms=8, stages=0),
 }
+# A2A-GEMM (the MoE all-to-all + expert GEMM) is measured beside the step, on
+# its own line of the JSON ("a2a"), not inside the headline value.
+A2A = wl.MIXTRAL_8X7B_EXPERT_UP_A2A
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def algorithmic_bytes(w: wl.Workload, with_send=True, with_publish=False) -> float:
+def algorithmic_bytes(w: wl.Workload, with_send=True, with_publish=False, rows_from=None, r=0) -> float:
     """Bytes the method must move through this HBM (each operand read once,
     each output written once; AG: staged peer shards read + written; RS/AR:
     each peer byte read once; RS: the fp32 send rows; AR: the fp32 publish of
     the local partial only when it is written -- the measured step leaves it
     NULL, since every AR flop already feeds `out`)."""
     M, N, K, R = w.M, w.N, w.K, w.R
+    if w.op == "a2a":  # AG-GEMM over unequal blocks: every non-local row staged
+        M = sum(rows_from)
+        staged = (M - rows_from[r]) * K * 2
+        return M * K * 2 + K * N * 2 + M * N * 2 + 2 * staged
     if w.op == "ag":
         staged = (R - 1) * w.M_r * K * 2
         return M * K * 2 + K * N * 2 + M * N * 2 + 2 * staged
@@ -467,6 +475,8 @@ def main():
             res["cublas_plus_copy_us"] = cublas_plus_copy_us(w, d, stream)
             baselines[w.op] = res
 
+    a2a = measure_a2a(knobs["a2a"], peaks, stream) if rank == 0 and not args.no_baselines else None
+
     # ---------------- CPU oracle baseline (rank 0, N = 1) ----------------
     cpu = None
     if rank == 0 and world == 1 and args.cpu_frac > 0:
@@ -487,7 +497,7 @@ def main():
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": sum(launches_per_call(p) for p in plans) * args.steps,
                 "per_call": per_call,
-                "clocks": clk, "per_op": per_op, "baselines": baselines,
+                "clocks": clk, "per_op": per_op, "baselines": baselines, "a2a": a2a,
                 "peaks": {**peaks, "source": peak_src}}
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -543,6 +553,57 @@ def run_sweep(args):
     return 0
 
 
+def measure_a2a(knobs, peaks, stream, reps=200):
+    """A2A-GEMM on the expert-parallel MoE workload (rank 0's expert), timed
+    alone: CUDA events around `reps` back-to-back calls after warm-up, the
+    unfused baseline (all copies, then the GEMM) the same way, cuBLAS + copy
+    for context, and the flag-wait share from a traced plan."""
+    import torch
+
+    from chunk_scheduled_communication_gb300 import runner
+    w, r = A2A, 0
+    inp = wl.make_inputs(w, r=r, seed=0)
+    d = runner.upload(inp)
+    M = sum(inp.rows_from)
+    flops = 2.0 * M * w.N * w.K
+    byts = algorithmic_bytes(w, rows_from=inp.rows_from, r=r)
+
+    def timed(kn):
+        kn = dict(kn)
+        split, order = kn.pop("split"), kn.pop("order")
+        with runner.make_plan(d, split=split, order=order, **kn) as p:
+            for _ in range(10):
+                runner.call(p, d, stream)
+            p.check(stream)
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for _ in range(reps):
+                runner.call(p, d, stream)
+            b1.record(stream)
+            torch.cuda.synchronize()
+            p.check(stream)
+            return b0.elapsed_time(b1) / reps * 1e3, launches_per_call(p)
+
+    us, launches = timed(knobs)
+    unfused_us, _ = timed({**knobs, "backend": "unfused", "stages": 0})
+    kn = dict(knobs)
+    split, order = kn.pop("split"), kn.pop("order")
+    with runner.make_plan(d, split=split, order=order, trace=1, **kn) as tp:
+        for _ in range(20):
+            runner.call(tp, d, stream)
+        tp.check(stream)
+        wait_ns, busy_ns = tp.stats()
+    t_burst = max(flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+    return {"workload": w.name, "rank": r, "rows_from": inp.rows_from, "M": M, "N": w.N, "K": w.K,
+            "us": us, "tflops": flops / (us * 1e-6) / 1e12, "algorithmic_bytes": byts,
+            "bound": "tensor" if flops / (peaks["bf16_tflops"] * 1e12) >= byts / (peaks["hbm_gbs"] * 1e9) else "hbm",
+            "roofline_frac_burst_peak": t_burst / (us * 1e-6),
+            "unfused_us": unfused_us, "fused_speedup_vs_unfused": unfused_us / us,
+            "cublas_plus_copy_us": cublas_plus_copy_us(w, d, stream),
+            "flag_wait_share": wait_ns / busy_ns if busy_ns else None,
+            "gpu_launches_per_call": launches, "knobs": knobs}
+
+
 def launches_per_call(plan) -> int:
     i = plan.info()
     return 1 if i["backend"] != 5 else len(set(plan.tables()[1].tolist()))
@@ -559,6 +620,14 @@ def cublas_plus_copy_us(w, d, stream) -> float:
             for q in range(w.R):
                 if q != 0:
                     d.gathered[q * w.M_r:(q + 1) * w.M_r].copy_(d.shards[q])
+            torch.matmul(d.gathered, d.B, out=d.out)
+        elif w.op == "a2a":
+            o = 0
+            for q in range(w.R):
+                m = d.rows_from[q]
+                if q != d.r and m:
+                    d.gathered[o:o + m].copy_(d.shards[q])
+                o += m
             torch.matmul(d.gathered, d.B, out=d.out)
         else:
             P = torch.matmul(d.A, d.B).float()

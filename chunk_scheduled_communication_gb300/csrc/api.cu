@@ -169,6 +169,10 @@ void free_plan(syn_plan_s *pl) {
     delete pl;
 }
 
+// A2A-GEMM plans are AG-GEMM plans over per-source row blocks of their own
+// size (no uniform M/R).
+bool is_a2a(const Schedule &s) { return s.op == SYN_OP_AG_GEMM && s.M_r == 0; }
+
 void fill_info(const Schedule &s, const syn_knobs_t &kn, syn_plan_info_t *info) {
     std::memset(info, 0, sizeof(*info));
     info->op = s.op;
@@ -189,6 +193,7 @@ void fill_info(const Schedule &s, const syn_knobs_t &kn, syn_plan_info_t *info) 
     info->tiles_m = s.tiles_m;
     info->tiles_n = s.tiles_n;
     info->n_tiles = s.n_tiles;
+    info->a2a = is_a2a(s) ? 1 : 0;
 }
 
 syn_knobs_t resolve_knobs(const syn_knobs_t *k) {
@@ -217,6 +222,7 @@ KernelParams base_params(syn_plan_s *pl) {
     p.M_r = (int32_t)s.M_r;
     p.cr = (int32_t)s.cr;
     p.split = s.split;
+    p.rb = s.rb;
     p.n_rc = s.n_rc;
     p.tiles_m = s.tiles_m;
     p.tiles_n = s.tiles_n;
@@ -299,7 +305,8 @@ int ce_copies(syn_plan_s *pl, const KernelParams &p, const cudaStream_t *streams
             uint8_t *dst;
             int64_t bytes;
             transfer_span(p, code, src, dst, bytes);
-            SYN_CK(cudaMemcpyAsync(dst, src, (size_t)bytes, cudaMemcpyDeviceToDevice, st));
+            if (bytes > 0)  // (empty A2A-GEMM chunks still publish their flag)
+                SYN_CK(cudaMemcpyAsync(dst, src, (size_t)bytes, cudaMemcpyDeviceToDevice, st));
             if (flags && (int)a != p.drop_transfer) {
                 CUresult r = p_write32(reinterpret_cast<CUstream>(st),
                                        reinterpret_cast<CUdeviceptr>(pl->d_in_flags + code), p.epoch,
@@ -372,9 +379,10 @@ int run(syn_plan_s *pl, KernelParams &p, cudaStream_t st) {
     }
 }
 
-int check_plan(syn_plan_t plan, int op) {
+int check_plan(syn_plan_t plan, int op, bool a2a = false) {
     if (plan == nullptr) return fail(SYN_ERR_INVALID, "null plan");
-    if (plan->s.op != op) return fail(SYN_ERR_INVALID, "plan was created for another operator");
+    if (plan->s.op != op || is_a2a(plan->s) != a2a)
+        return fail(SYN_ERR_INVALID, "plan was created for another operator");
     return SYN_OK;
 }
 
@@ -427,8 +435,14 @@ int syn_device_sms(int *num_sms) {
     return SYN_OK;
 }
 
-int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_layout_t *layout,
-                    int64_t chunk_rows, int split, syn_order_t order, const syn_knobs_t *knobs) {
+}  // extern "C"
+
+namespace {
+
+// Plan creation shared by syn_plan_create and syn_plan_create_a2a
+// (block_rows: the A2A-GEMM per-source row counts, else NULL).
+int plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_layout_t *layout, int64_t chunk_rows,
+                int split, syn_order_t order, const syn_knobs_t *knobs, const int64_t *block_rows) {
     if (out == nullptr || layout == nullptr) return fail(SYN_ERR_INVALID, "null argument");
     *out = nullptr;
     int rc = load_driver();
@@ -444,7 +458,7 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
     syn_plan_s *pl = new syn_plan_s();
     pl->kn = kn;
     std::string err;
-    rc = build_schedule(op, R, rank, *layout, chunk_rows, split, order, kn, pl->s, err);
+    rc = build_schedule(op, R, rank, *layout, chunk_rows, split, order, kn, pl->s, err, block_rows);
     if (rc != SYN_OK) {
         delete pl;
         return fail(rc, err);
@@ -584,20 +598,79 @@ int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_lay
     return SYN_OK;
 }
 
+// A2A-GEMM row blocks: validated counts and their sum.
+int a2a_rows(int R, const int64_t *rows_from, int64_t &M) {
+    if (rows_from == nullptr) return fail(SYN_ERR_INVALID, "null rows_from");
+    if (R < 1) return fail(SYN_ERR_INVALID, "R must be >= 1");
+    if (R > kMaxRanks) return fail(SYN_ERR_UNSUPPORTED, "R > 8");
+    M = 0;
+    for (int q = 0; q < R; ++q) {
+        if (rows_from[q] < 0) return fail(SYN_ERR_INVALID, "rows_from entries must be >= 0");
+        M += rows_from[q];
+    }
+    if (M == 0) return fail(SYN_ERR_INVALID, "no rows to multiply (every rows_from entry is 0)");
+    return SYN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int syn_plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_layout_t *layout,
+                    int64_t chunk_rows, int split, syn_order_t order, const syn_knobs_t *knobs) {
+    return plan_create(out, op, R, rank, layout, chunk_rows, split, order, knobs, nullptr);
+}
+
+int syn_plan_create_a2a(syn_plan_t *out, int R, int rank, const int64_t *rows_from, int64_t N, int64_t K,
+                        int split, syn_order_t order, const syn_knobs_t *knobs) {
+    if (out == nullptr) return fail(SYN_ERR_INVALID, "null argument");
+    *out = nullptr;
+    int64_t M = 0;
+    int rc = a2a_rows(R, rows_from, M);
+    if (rc != SYN_OK) return rc;
+    const syn_layout_t L = {M, N, K, 0, 0, 0};
+    return plan_create(out, SYN_OP_AG_GEMM, R, rank, &L, 0, split, order, knobs, rows_from);
+}
+
+int syn_schedule_build_a2a(int R, int rank, const int64_t *rows_from, int64_t N, int64_t K, int split,
+                           syn_order_t order, const syn_knobs_t *knobs, syn_plan_info_t *info,
+                           int32_t *tile_list, int32_t *tile_key, int32_t *transfers) {
+    int64_t M = 0;
+    int rc = a2a_rows(R, rows_from, M);
+    if (rc != SYN_OK) return rc;
+    const syn_knobs_t kn = resolve_knobs(knobs);
+    const syn_layout_t L = {M, N, K, 0, 0, 0};
+    Schedule s;
+    std::string err;
+    rc = build_schedule(SYN_OP_AG_GEMM, R, rank, L, 0, split, order, kn, s, err, rows_from);
+    if (rc != SYN_OK) return fail(rc, err);
+    if (info) fill_info(s, kn, info);
+    if (tile_list) std::memcpy(tile_list, s.tile_list.data(), s.tile_list.size() * sizeof(int32_t));
+    if (tile_key) std::memcpy(tile_key, s.tile_key.data(), s.tile_key.size() * sizeof(int32_t));
+    if (transfers) std::memcpy(transfers, s.transfers.data(), s.transfers.size() * sizeof(int32_t));
+    return SYN_OK;
+}
+
 int syn_plan_destroy(syn_plan_t plan) {
     free_plan(plan);
     return SYN_OK;
 }
 
-int syn_ag_gemm(syn_plan_t plan, const void *const *shards, void *gathered, const void *B, void *C,
+}  // extern "C"
+
+namespace {
+
+// AG-GEMM and A2A-GEMM: source q's rows go to rows [off[q], off[q+1]) of
+// `gathered`, then C = gathered . B.
+int gather_gemm(syn_plan_t plan, bool a2a, const void *const *shards, void *gathered, const void *B, void *C,
                 void *stream) {
-    int rc = check_plan(plan, SYN_OP_AG_GEMM);
+    int rc = check_plan(plan, SYN_OP_AG_GEMM, a2a);
     if (rc != SYN_OK) return rc;
     if (shards == nullptr || gathered == nullptr || B == nullptr || C == nullptr)
         return fail(SYN_ERR_INVALID, "null operand");
     const Schedule &s = plan->s;
     for (int q = 0; q < s.R; ++q)
-        if (shards[q] == nullptr || !aligned16(shards[q]))
+        if ((shards[q] == nullptr && block_rows(s.rb, q) > 0) || !aligned16(shards[q]))
             return fail(SYN_ERR_INVALID, "shard pointer null or not 16-byte aligned");
     if (!aligned16(gathered) || !aligned16(B) || !aligned16(C))
         return fail(SYN_ERR_INVALID, "operand not 16-byte aligned");
@@ -619,13 +692,27 @@ int syn_ag_gemm(syn_plan_t plan, const void *const *shards, void *gathered, cons
     p.row_bytes = row_bytes;
     p.local_inplace =
         (static_cast<const uint8_t *>(shards[s.rank]) ==
-         static_cast<uint8_t *>(gathered) + (int64_t)s.rank * s.M_r * row_bytes)
+         static_cast<uint8_t *>(gathered) + s.rb.off[s.rank] * row_bytes)
             ? 1
             : 0;
     p.out = static_cast<uint16_t *>(C);
     p.f32_out = nullptr;
     p.epi_tma = 1;
     return run(plan, p, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int syn_ag_gemm(syn_plan_t plan, const void *const *shards, void *gathered, const void *B, void *C,
+                void *stream) {
+    return gather_gemm(plan, false, shards, gathered, B, C, stream);
+}
+
+int syn_a2a_gemm(syn_plan_t plan, const void *const *parts, void *gathered, const void *B, void *C,
+                 void *stream) {
+    return gather_gemm(plan, true, parts, gathered, B, C, stream);
 }
 
 static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,

@@ -293,7 +293,7 @@ __device__ __forceinline__ int wait_smem_count(uint32_t addr, uint32_t total, ui
 // when every row lies past M (the odd CTA of a ragged last pair tile).
 __device__ __forceinline__ void chunk_range(const KernelParams &p, int r0, int nrows, int &lo,
                                             int &hi) {
-    chunk_range_of(p.M, p.M_r, p.split, r0, nrows, lo, hi);
+    chunk_range_of(p.M, p.rb, r0, nrows, lo, hi);
 }
 
 // Does the tile starting at row r0 reduce peers?  AR: always; RS: tiles of the
@@ -479,8 +479,8 @@ __device__ __forceinline__ void count_produced(const KernelParams &p, int r0, in
         chunk_range(p, r0, tile_m, lo, hi);
         uint32_t *cnt = p.out_cnt + (size_t)counter_half(p.epoch) * p.n_rc;
         for (int rc = lo; rc <= hi; ++rc) {
-            const int64_t row0 = chunk_row0(p.M_r, p.split, rc);
-            const int64_t row1 = chunk_row0(p.M_r, p.split, rc + 1);
+            const int64_t row0 = chunk_row0(p.rb, rc);
+            const int64_t row1 = chunk_row0(p.rb, rc + 1);
             const int t_lo = (int)(row0 / tile_m);
             const int t_hi = (int)((row1 - 1) / tile_m);
             const uint32_t need = 4u * (uint32_t)ctas * (uint32_t)((t_hi - t_lo + 1) * p.tiles_n);
@@ -712,7 +712,7 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
                     chunk_range(p, r0, C::BM, lo, hi);
                     for (int rc = lo; ok && rc <= hi; ++rc) {
                         const int q = rc / p.split;
-                        if (p.local_inplace && q == p.rank) continue;
+                        if ((p.local_inplace && q == p.rank) || chunk_empty(p.rb, rc)) continue;
                         ok = wait_flag(p.in_flags + rc * p.R + q, p, abort, WHERE_AG_FLAG,
                                        rc * p.R + q, wait_ns);
                     }

@@ -43,6 +43,7 @@ struct TensorMaps {  // CUtensorMap carries its own alignment
 struct KernelParams {
     int32_t op, R, rank;
     int32_t M, N, K, M_r, cr, split, n_rc;  // cr: rows of the largest chunk
+    RowBlocks rb;                  // row blocks and chunk geometry
     int32_t tiles_m, tiles_n;
     int32_t t_begin, t_end;        // range of tile_list this launch runs
     int32_t G;                     // GEMM CTAs: blockIdx.x < G
@@ -89,7 +90,7 @@ SYN_HD int recv_slot(int q, int rank) { return recv_slot_of(q, rank); }
 // protocol.h gives the rows).
 SYN_HD void transfer_span(const KernelParams &p, int code, const uint8_t *&src, uint8_t *&dst,
                           int64_t &bytes) {
-    const TransferRows t = transfer_rows(p.op, p.R, p.rank, p.M_r, p.split, p.recv_slot_rows, code);
+    const TransferRows t = transfer_rows(p.op, p.rank, p.rb, p.recv_slot_rows, code);
     bytes = t.rows * p.row_bytes;
     src = p.stage_src[t.q] + t.src_row * p.row_bytes;
     dst = p.stage_dst + t.dst_row * p.row_bytes;

@@ -164,6 +164,7 @@ extern "C" int syn_ag_gemm_noalloc(int R, int rank, const syn_layout_t *layout, 
     p.M_r = (int32_t)s.M_r;
     p.cr = (int32_t)s.cr;
     p.split = s.split;
+    p.rb = s.rb;
     p.n_rc = s.n_rc;
     p.tiles_m = s.tiles_m;
     p.tiles_n = s.tiles_n;

@@ -41,7 +41,7 @@ struct State {
     Schedule s;
     int64_t row_bytes = 0, slot_rows = 0;
     bool local_inplace = true;
-    std::vector<std::vector<uint8_t>> src;   // R sources (AG shards [M_r] rows; RS/AR peers [M] rows)
+    std::vector<std::vector<uint8_t>> src;   // R sources (AG shards [M_r] rows, A2A parts; RS/AR peers [M] rows)
     std::vector<uint8_t> dst;                // AG gathered [M] rows; RS/AR receive buffer
     std::vector<std::atomic<uint32_t>> flags;
     std::vector<std::atomic<uint32_t>> cnt;  // [2][n_flags]
@@ -77,7 +77,7 @@ void stager(State &st, int worker, uint32_t epoch, int call) {
         const int code = st.s.transfers[a];
         if (c.op == 0 && st.local_inplace && code % st.s.R == st.s.rank) continue;
         if (c.jitter_us > 0) std::this_thread::sleep_for(std::chrono::microseconds(rng() % (c.jitter_us + 1)));
-        const TransferRows t = transfer_rows(c.op, st.s.R, st.s.rank, st.s.M_r, st.s.split, st.slot_rows, code);
+        const TransferRows t = transfer_rows(c.op, st.s.rank, st.s.rb, st.slot_rows, code);
         const int64_t bytes = t.rows * st.row_bytes;
         const int64_t off = (int64_t)sl * c.slice_bytes;
         const int64_t len = std::min<int64_t>(c.slice_bytes, bytes - off);
@@ -109,11 +109,11 @@ void tile_waits(const State &st, int tile, std::vector<int> &codes) {
     const int64_t r0 = (int64_t)(tile / s.tiles_n) * s.tile_m;
     if (op == 1 && r0 / s.M_r != s.rank) return;  // GEMM-RS send tile: consumes nothing
     int lo, hi;
-    chunk_range_of(s.M, s.M_r, s.split, r0, s.tile_m, lo, hi);
+    chunk_range_of(s.M, s.rb, r0, s.tile_m, lo, hi);
     for (int rc = lo; rc <= hi; ++rc) {
         if (op == 0) {
             const int q = rc / s.split;
-            if (!(st.local_inplace && q == s.rank)) codes.push_back(rc * s.R + q);
+            if (!(st.local_inplace && q == s.rank) && !chunk_empty(s.rb, rc)) codes.push_back(rc * s.R + q);
         } else {
             for (int q = 0; q < s.R; ++q)
                 if (q != s.rank) codes.push_back(rc * s.R + q);
@@ -123,7 +123,7 @@ void tile_waits(const State &st, int tile, std::vector<int> &codes) {
 
 // Every destination row of the tile's transfers must hold this call's bytes.
 bool rows_match(const State &st, int code, uint32_t epoch) {
-    const TransferRows t = transfer_rows(st.cfg->op, st.s.R, st.s.rank, st.s.M_r, st.s.split, st.slot_rows, code);
+    const TransferRows t = transfer_rows(st.cfg->op, st.s.rank, st.s.rb, st.slot_rows, code);
     for (int64_t r = 0; r < t.rows; ++r) {
         const uint8_t *d = st.dst.data() + (t.dst_row + r) * st.row_bytes;
         for (int64_t b = 0; b < st.row_bytes; ++b)
@@ -172,7 +172,16 @@ extern "C" int syn_proto_emulate(const syn_proto_cfg_t *cfg, int *status, int64_
     }
     State st;
     st.cfg = cfg;
-    syn_layout_t L = {c.M, c.N, c.K, 0, 0, 0};
+    if (c.rows_from != nullptr && (c.op != 0 || c.R < 1 || c.R > kMaxRanks)) {
+        g_err = "rows_from is for op 0 with 1 <= R <= 8";
+        return SYN_ERR_INVALID;
+    }
+    int64_t M = c.M;
+    if (c.rows_from != nullptr) {
+        M = 0;
+        for (int q = 0; q < c.R; ++q) M += c.rows_from[q];
+    }
+    syn_layout_t L = {M, c.N, c.K, 0, 0, 0};
     syn_knobs_t kn;
     std::memset(&kn, 0, sizeof(kn));
     kn.backend = SYN_BACKEND_TMA_COLOCATED;
@@ -181,7 +190,8 @@ extern "C" int syn_proto_emulate(const syn_proto_cfg_t *cfg, int *status, int64_
     kn.group_m = 8;
     kn.slice_kb = 128;
     std::string err;
-    const int rc = build_schedule((syn_op_t)c.op, c.R, c.rank, L, 0, c.split, (syn_order_t)c.order, kn, st.s, err);
+    const int rc = build_schedule((syn_op_t)c.op, c.R, c.rank, L, 0, c.split, (syn_order_t)c.order, kn, st.s, err,
+                                  c.rows_from);
     if (rc != SYN_OK) {
         g_err = err;
         return rc;
@@ -189,8 +199,9 @@ extern "C" int syn_proto_emulate(const syn_proto_cfg_t *cfg, int *status, int64_
     const Schedule &s = st.s;
     st.row_bytes = c.op == 0 ? c.K * 2 : c.N * 4;
     st.slot_rows = c.op == 1 ? s.M_r : s.M;
-    const int64_t src_rows = c.op == 0 ? s.M_r : s.M;
-    st.src.assign((size_t)s.R, std::vector<uint8_t>((size_t)(src_rows * st.row_bytes)));
+    auto src_rows = [&](int q) { return c.op == 0 ? block_rows(s.rb, q) : s.M; };
+    st.src.resize((size_t)s.R);
+    for (int q = 0; q < s.R; ++q) st.src[q].assign((size_t)(src_rows(q) * st.row_bytes), 0);
     st.dst.assign((size_t)((c.op == 0 ? s.M : (int64_t)(s.R - 1) * st.slot_rows) * st.row_bytes), 0);
     const int n_flags = s.n_rc * s.R;
     st.flags = std::vector<std::atomic<uint32_t>>((size_t)n_flags);
@@ -201,13 +212,13 @@ extern "C" int syn_proto_emulate(const syn_proto_cfg_t *cfg, int *status, int64_
         const uint32_t epoch = (uint32_t)call;
         // this call's sources; the destination poisoned so stale reads show
         for (int q = 0; q < s.R; ++q)
-            for (int64_t r = 0; r < src_rows; ++r)
+            for (int64_t r = 0; r < src_rows(q); ++r)
                 for (int64_t b = 0; b < st.row_bytes; ++b)
                     st.src[q][(size_t)(r * st.row_bytes + b)] = src_byte(epoch, q, r, b, c.seed);
         std::fill(st.dst.begin(), st.dst.end(), (uint8_t)0xEE);
         if (c.op == 0)  // the local shard is in place in its slot of the gathered buffer
-            std::memcpy(st.dst.data() + (int64_t)s.rank * s.M_r * st.row_bytes, st.src[s.rank].data(),
-                        (size_t)(s.M_r * st.row_bytes));
+            std::memcpy(st.dst.data() + s.rb.off[s.rank] * st.row_bytes, st.src[s.rank].data(),
+                        (size_t)(block_rows(s.rb, s.rank) * st.row_bytes));
         st.err.store(0);
         st.checked.store(0);
         std::vector<std::thread> th;

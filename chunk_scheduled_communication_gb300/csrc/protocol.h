@@ -43,16 +43,15 @@ SYN_SCHED_HD int walk_entry_of(int t_begin, int t_end, int unit, int n_units, in
 
 // Row chunks [lo, hi] that rows [r0, r0 + nrows) clipped to M touch; lo > hi
 // when every row lies past M.
-SYN_SCHED_HD void chunk_range_of(int64_t M, int64_t M_r, int split, int64_t r0, int64_t nrows, int &lo,
-                                 int &hi) {
+SYN_SCHED_HD void chunk_range_of(int64_t M, const RowBlocks &b, int64_t r0, int64_t nrows, int &lo, int &hi) {
     const int64_t r1 = r0 + nrows < M ? r0 + nrows : M;
     if (r0 >= r1) {
         lo = 0;
         hi = -1;
         return;
     }
-    lo = chunk_of_row(M_r, split, r0);
-    hi = chunk_of_row(M_r, split, r1 - 1);
+    lo = chunk_of_row(b, r0);
+    hi = chunk_of_row(b, r1 - 1);
 }
 
 // Receive-buffer slot of source rank q (the local rank has none).
@@ -60,29 +59,28 @@ SYN_SCHED_HD int recv_slot_of(int q, int rank) { return q - (q > rank ? 1 : 0); 
 
 // Rows of staging transfer `code` = rc * R + q (row chunk rc, from source
 // rank q): `rows` rows from row `src_row` of source q's buffer to row
-// `dst_row` of the destination (op 0 AG: the gathered buffer; op 1 RS / 2 AR:
-// the receive buffer, source q's slot at rows [slot * slot_rows, ...)).
-//   AG : shard q rows [row0 - q*M_r, ...)  ->  gathered rows [row0, row1)
-//   RS : peer q rows [row0, row1)           ->  slot q rows [row0 - rank*M_r, ...)
-//   AR : peer q rows [row0, row1)           ->  slot q rows [row0, row1)
+// `dst_row` of the destination (op 0 AG / A2A: the gathered buffer; op 1 RS /
+// 2 AR: the receive buffer, source q's slot at rows [slot * slot_rows, ...)).
+//   AG : shard q rows [row0 - off[q], ...)  ->  gathered rows [row0, row1)
+//   RS : peer q rows [row0, row1)            ->  slot q rows [row0 - off[rank], ...)
+//   AR : peer q rows [row0, row1)            ->  slot q rows [row0, row1)
 struct TransferRows {
     int q;
     int64_t src_row, dst_row, rows;
 };
-SYN_SCHED_HD TransferRows transfer_rows(int op, int R, int rank, int64_t M_r, int split, int64_t slot_rows,
-                                        int code) {
-    const int rc = code / R, q = code % R;
-    const int64_t row0 = chunk_row0(M_r, split, rc);
-    const int64_t row1 = chunk_row0(M_r, split, rc + 1);
+SYN_SCHED_HD TransferRows transfer_rows(int op, int rank, const RowBlocks &b, int64_t slot_rows, int code) {
+    const int rc = code / b.R, q = code % b.R;
+    const int64_t row0 = chunk_row0(b, rc);
+    const int64_t row1 = chunk_row0(b, rc + 1);
     TransferRows t;
     t.q = q;
     t.rows = row1 - row0;
     if (op == 0) {
-        t.src_row = row0 - (int64_t)q * M_r;
+        t.src_row = row0 - b.off[q];
         t.dst_row = row0;
     } else {
         t.src_row = row0;
-        t.dst_row = (int64_t)recv_slot_of(q, rank) * slot_rows + row0 - (op == 1 ? (int64_t)rank * M_r : 0);
+        t.dst_row = (int64_t)recv_slot_of(q, rank) * slot_rows + row0 - (op == 1 ? b.off[rank] : 0);
     }
     return t;
 }

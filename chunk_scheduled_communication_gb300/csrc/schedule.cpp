@@ -3,8 +3,9 @@
 // Chunks (Syncopate summary page, method ¶1, paper §5.1): a chunk is a block
 // of rows of a logical tensor holding one or more compute tiles.  Here every
 // operator's row space [0, M) is cut into row chunks: each rank's block of
-// M_r rows into `split` chunks of ceil or floor(M_r/split) rows (chunk_row0 in
-// schedule.h); rank q owns row chunks [q*split, (q+1)*split).  A staging transfer is (row chunk rc,
+// rows (M/R rows, or for A2A-GEMM the rows that rank sends) into `split`
+// chunks of near-equal size (RowBlocks in schedule.h); rank q owns row chunks
+// [q*split, (q+1)*split).  A staging transfer is (row chunk rc,
 // source rank q): the rows of rc held by rank q that the local rank needs.
 //
 //   AG-GEMM : transfer (rc, q = rc / split) copies shard q's rows into the
@@ -40,7 +41,7 @@ static int ring_pos(int q, int r, int R) { return ((q - r) % R + R) % R; }
 
 int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
                    int64_t chunk_rows, int split, syn_order_t order,
-                   const syn_knobs_t &kn, Schedule &s, std::string &err) {
+                   const syn_knobs_t &kn, Schedule &s, std::string &err, const int64_t *block_rows) {
     if (op != SYN_OP_AG_GEMM && op != SYN_OP_GEMM_RS && op != SYN_OP_GEMM_AR) {
         err = "unknown op";
         return SYN_ERR_INVALID;
@@ -57,7 +58,25 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         err = "M, N, K must be positive";
         return SYN_ERR_INVALID;
     }
-    if (L.M % R != 0) {
+    const bool var_blocks = block_rows != nullptr;
+    if (var_blocks) {
+        if (op != SYN_OP_AG_GEMM) {
+            err = "per-rank block sizes are for the A2A-GEMM (AG-GEMM) plan only";
+            return SYN_ERR_INVALID;
+        }
+        int64_t sum = 0;
+        for (int q = 0; q < R; ++q) {
+            if (block_rows[q] < 0) {
+                err = "block sizes must be >= 0";
+                return SYN_ERR_INVALID;
+            }
+            sum += block_rows[q];
+        }
+        if (sum != L.M) {
+            err = "M must equal the sum of the block sizes";
+            return SYN_ERR_INVALID;
+        }
+    } else if (L.M % R != 0) {
         err = "M must be divisible by R";
         return SYN_ERR_INVALID;
     }
@@ -70,9 +89,13 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         err = "unknown tile order";
         return SYN_ERR_INVALID;
     }
-    const int64_t M_r = L.M / R;
+    const int64_t M_r = var_blocks ? 0 : L.M / R;
     if (chunk_rows < 0 || split < 0) {
         err = "chunk_rows and split must be >= 0";
+        return SYN_ERR_INVALID;
+    }
+    if (var_blocks && chunk_rows != 0) {
+        err = "per-rank block sizes take a split, not chunk_rows";
         return SYN_ERR_INVALID;
     }
     if (chunk_rows == 0 && split == 0) split = 1;
@@ -87,8 +110,12 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         }
         split = (int)(M_r / chunk_rows);
     }
-    if (split > M_r) {
+    if (!var_blocks && split > M_r) {
         err = "split must not exceed M/R";
+        return SYN_ERR_INVALID;
+    }
+    if (var_blocks && split > 64) {
+        err = "split must not exceed 64";
         return SYN_ERR_INVALID;
     }
     const int tile_m = kn.tile_m == 0 ? kTileM : kn.tile_m;
@@ -127,7 +154,20 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
     s.K = L.K;
     s.M_r = M_r;
     s.split = split;
-    s.cr = (M_r + split - 1) / split;
+    if (var_blocks) {
+        s.rb.R = R;
+        s.rb.split = split;
+        s.rb.off[0] = 0;
+        for (int q = 0; q < kMaxRanks; ++q) s.rb.off[q + 1] = s.rb.off[q] + (q < R ? block_rows[q] : 0);
+        s.cr = 0;
+        for (int q = 0; q < R; ++q) {
+            const int64_t c = (block_rows[q] + split - 1) / split;
+            if (c > s.cr) s.cr = c;
+        }
+    } else {
+        s.rb = uniform_blocks(R, M_r, split);
+        s.cr = (M_r + split - 1) / split;
+    }
     s.order = order;
     s.group_m = kn.group_m > 0 ? kn.group_m : 8;
     s.tile_m = tile_m;
@@ -170,17 +210,17 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         int lo, hi;
         tile_row_chunks(s, tm, lo, hi);
         int32_t key = -1;
-        const int block = (int)(((int64_t)tm * tile_m) / M_r);
+        const int block = block_of_row(s.rb, (int64_t)tm * tile_m);
         if (op == SYN_OP_GEMM_RS && block != rank) {
             // send tile: produces chunk(s) for rank `block`; ring order
-            const int j = chunk_of_row(M_r, split, (int64_t)tm * tile_m) - block * split;
+            const int j = chunk_of_row(s.rb, (int64_t)tm * tile_m) - block * split;
             key = (ring_pos(block, rank, R) - 1) * split + j - (R - 1) * split;
         } else if (op == SYN_OP_GEMM_RS && kn.backend == SYN_BACKEND_TMA_COLOCATED_SMEM) {
             // the peers' rows_r are resident from the start: reduce tiles first
             key = -(R - 1) * split - 1;
         } else {
             for (int rc = lo; rc <= hi; ++rc)
-                for (int q = 0; q < R; ++q) {
+                for (int q = 0; q < R && !chunk_empty(s.rb, rc); ++q) {
                     const int a = s.arrival[(size_t)rc * R + q];
                     if (a > key) key = a;
                 }

@@ -27,11 +27,56 @@ constexpr int kTileM = 128;
 constexpr int kTileK = 64;
 constexpr int kMaxRanks = 8;
 
+// Row blocks of the R ranks: rank q owns rows [off[q], off[q+1]) of the row
+// space.  AG-GEMM, GEMM-RS and GEMM-AR use uniform blocks, off[q] = q * M / R;
+// A2A-GEMM has one block per source rank with its own size (the rows that
+// rank sends).  Block q (of m_q = off[q+1] - off[q] rows) is cut into `split`
+// chunks: chunk j covers rows off[q] + [ceil(j*m_q/split), ceil((j+1)*m_q/split)),
+// so chunk sizes within a block differ by at most one row.  Row chunk
+// rc = q*split + j.
+struct RowBlocks {
+    int R = 1, split = 1;
+    int64_t off[kMaxRanks + 1] = {0};
+};
+
+SYN_SCHED_HD RowBlocks uniform_blocks(int R, int64_t M_r, int split) {
+    RowBlocks b;
+    b.R = R;
+    b.split = split;
+    for (int q = 0; q <= kMaxRanks; ++q) b.off[q] = (int64_t)(q <= R ? q : R) * M_r;
+    return b;
+}
+SYN_SCHED_HD int64_t block_rows(const RowBlocks &b, int q) { return b.off[q + 1] - b.off[q]; }
+
+// First row of row chunk rc (rc == R*split gives the end of the row space).
+SYN_SCHED_HD int64_t chunk_row0(const RowBlocks &b, int rc) {
+    const int q = rc / b.split, j = rc - q * b.split;
+    if (q >= b.R) return b.off[b.R];
+    const int64_t m = block_rows(b, q);
+    return b.off[q] + ((int64_t)j * m + b.split - 1) / b.split;
+}
+// Row chunk rc holds no rows (A2A-GEMM: an empty block, or a block of fewer
+// rows than split).  Its transfer still publishes a flag, but no tile waits
+// for it.
+SYN_SCHED_HD bool chunk_empty(const RowBlocks &b, int rc) { return chunk_row0(b, rc + 1) == chunk_row0(b, rc); }
+// The rank whose block holds `row` (0 <= row < off[R]); empty blocks hold none.
+SYN_SCHED_HD int block_of_row(const RowBlocks &b, int64_t row) {
+    int q = 0;
+    while (q + 1 < b.R && b.off[q + 1] <= row) ++q;
+    return q;
+}
+SYN_SCHED_HD int chunk_of_row(const RowBlocks &b, int64_t row) {
+    const int q = block_of_row(b, row);
+    const int64_t m = block_rows(b, q);
+    return q * b.split + (int)(((row - b.off[q]) * b.split) / m);
+}
+
 struct Schedule {
     int op = 0, R = 1, rank = 0;
-    int64_t M = 0, N = 0, K = 0, M_r = 0;
-    int64_t cr = 0;      // rows of the largest chunk, ceil(M_r / split)
+    int64_t M = 0, N = 0, K = 0, M_r = 0;  // M_r: rows per rank (uniform blocks; 0 for A2A)
+    int64_t cr = 0;      // rows of the largest chunk
     int split = 1;       // chunks per rank row block
+    RowBlocks rb;        // row blocks and chunk geometry
     int order = 0, group_m = 8;
     int tile_m = kTileM, tile_n = 256;
     int tiles_m = 0, tiles_n = 0, n_tiles = 0;
@@ -42,10 +87,13 @@ struct Schedule {
     std::vector<int32_t> arrival;     // arrival index of (rc * R + q), -1 if none
 };
 
-// Fills `s` or returns a SYN_ERR_* code with a message in `err`.
+// Fills `s` or returns a SYN_ERR_* code with a message in `err`.  With
+// `block_rows` (AG-GEMM only: A2A-GEMM) rank q's block has block_rows[q] rows
+// and layout.M must be their sum; otherwise blocks are uniform, M / R rows.
 int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &layout,
                    int64_t chunk_rows, int split, syn_order_t order,
-                   const syn_knobs_t &knobs, Schedule &s, std::string &err);
+                   const syn_knobs_t &knobs, Schedule &s, std::string &err,
+                   const int64_t *block_rows = nullptr);
 
 // GEMM-RS whose peer partials are resident (TMA_COLOCATED_SMEM): every chunk
 // is available at t = 0, so the order is free to place the reduce tiles (each
@@ -67,26 +115,13 @@ inline bool uses_reducer_warps(int op, const syn_knobs_t &kn, int tile_n) {
            kn.reduce_warps >= 0 && tile_n == 256 && (kn.tile_k == 0 || kn.tile_k == 64);
 }
 
-// Chunk geometry.  Rank q's block of M_r rows is cut into `split` chunks;
-// chunk j of the block covers local rows [ceil(j*M_r/split), ceil((j+1)*M_r/split)),
-// so chunk sizes differ by at most one row when split does not divide M_r.
-// Row chunk rc = q*split + j.
-SYN_SCHED_HD int64_t chunk_row0(int64_t M_r, int split, int rc) {
-    const int q = rc / split, j = rc - q * split;
-    return (int64_t)q * M_r + ((int64_t)j * M_r + split - 1) / split;
-}
-SYN_SCHED_HD int chunk_of_row(int64_t M_r, int split, int64_t row) {
-    const int64_t q = row / M_r, rr = row - q * M_r;
-    return (int)(q * split + (rr * split) / M_r);
-}
-
 // Row-chunk range [lo, hi] covered by tile row tm (rows clipped to M).
 inline void tile_row_chunks(const Schedule &s, int tm, int &lo, int &hi) {
     int64_t r0 = (int64_t)tm * s.tile_m;
     int64_t r1 = r0 + s.tile_m;
     if (r1 > s.M) r1 = s.M;
-    lo = chunk_of_row(s.M_r, s.split, r0);
-    hi = chunk_of_row(s.M_r, s.split, r1 - 1);
+    lo = chunk_of_row(s.rb, r0);
+    hi = chunk_of_row(s.rb, r1 - 1);
 }
 
 }  // namespace syn

@@ -20,7 +20,7 @@ class Cfg(ctypes.Structure):
                 ("slice_bytes", ctypes.c_int64), ("calls", ctypes.c_int), ("drop_transfer", ctypes.c_int),
                 ("drop_call", ctypes.c_int), ("delay_transfer", ctypes.c_int), ("delay_us", ctypes.c_int),
                 ("timeout_us", ctypes.c_int), ("jitter_us", ctypes.c_int), ("seed", ctypes.c_uint64),
-                ("mutation", ctypes.c_int)]
+                ("mutation", ctypes.c_int), ("rows_from", ctypes.c_void_p)]
 
 
 def lib():
@@ -40,10 +40,13 @@ ORDERS = {"row": 0, "col": 1, "grouped": 2}
 
 def emulate(op="ag", R=4, rank=0, M=1024, N=256, K=64, split=1, order="row", tile_m=128, tile_n=256,
             walkers=8, stagers=4, slice_bytes=4096, calls=3, drop_transfer=-1, drop_call=1,
-            delay_transfer=-1, delay_us=0, timeout_us=200_000, jitter_us=20, seed=1, mutation=0):
-    """Run `calls` emulated calls; returns (statuses, tiles_checked) lists."""
+            delay_transfer=-1, delay_us=0, timeout_us=200_000, jitter_us=20, seed=1, mutation=0, rows_from=None):
+    """Run `calls` emulated calls; returns (statuses, tiles_checked) lists.
+    rows_from (op "ag" only): A2A-GEMM row counts per source; M is ignored."""
+    rows = None if rows_from is None else (ctypes.c_int64 * R)(*[int(x) for x in rows_from])
     c = Cfg(OPS[op], R, rank, M, N, K, split, ORDERS[order], tile_m, tile_n, walkers, stagers, slice_bytes,
-            calls, drop_transfer, drop_call, delay_transfer, delay_us, timeout_us, jitter_us, seed, mutation)
+            calls, drop_transfer, drop_call, delay_transfer, delay_us, timeout_us, jitter_us, seed, mutation,
+            ctypes.cast(rows, ctypes.c_void_p) if rows is not None else None)
     st = (ctypes.c_int * calls)()
     tc = (ctypes.c_int64 * calls)()
     rc = lib().syn_proto_emulate(ctypes.byref(c), st, tc)

@@ -36,7 +36,8 @@ class DeviceInputs:
     M: int
     N: int
     K: int
-    shards: list = field(default_factory=list)   # AG: shard tensors (shards[r] aliases gathered)
+    shards: list = field(default_factory=list)   # AG / A2A: shard (part) tensors (shards[r] aliases gathered)
+    rows_from: list | None = None                # A2A: rows each source sends
     gathered: torch.Tensor | None = None
     A: torch.Tensor | None = None
     B: torch.Tensor | None = None
@@ -51,7 +52,22 @@ def upload(inp: Inputs, device="cuda", inplace_local=True, with_f32_out=True) ->
     w = inp.w
     d = DeviceInputs(op=w.op, R=w.R, r=inp.r, M=w.M, N=w.N, K=w.K)
     d.B = _u16_to_dev(inp.B, device)
-    if w.op == "ag":
+    if w.op == "a2a":
+        d.rows_from = list(inp.rows_from)
+        d.M = M = sum(d.rows_from)
+        off = np.concatenate([[0], np.cumsum(d.rows_from)]).astype(int)
+        d.gathered = torch.zeros((M, w.K), dtype=torch.bfloat16, device=device)
+        for q in range(w.R):
+            if d.rows_from[q] == 0:
+                d.shards.append(None)  # nothing sent: a NULL part
+            elif q == inp.r and inplace_local:
+                slot = d.gathered[off[q]:off[q + 1]]
+                slot.copy_(_u16_to_dev(inp.shards[q], device))
+                d.shards.append(slot)
+            else:
+                d.shards.append(_u16_to_dev(inp.shards[q], device))
+        d.out = torch.empty((M, w.N), dtype=torch.bfloat16, device=device)
+    elif w.op == "ag":
         d.gathered = torch.zeros((w.M, w.K), dtype=torch.bfloat16, device=device)
         for q in range(w.R):
             if q == inp.r and inplace_local:
@@ -75,6 +91,8 @@ def call(plan: syn.Plan, d: DeviceInputs, stream=None):
     """Issue one asynchronous call of the plan's operator."""
     if d.op == "ag":
         plan.ag_gemm(d.shards, d.gathered, d.B, d.out, stream)
+    elif d.op == "a2a":
+        plan.a2a_gemm(d.shards, d.gathered, d.B, d.out, stream)
     elif d.op == "rs":
         plan.gemm_rs(d.A, d.B, d.peers, d.f32_out, d.out, stream)
     else:
@@ -82,6 +100,8 @@ def call(plan: syn.Plan, d: DeviceInputs, stream=None):
 
 
 def make_plan(d: DeviceInputs, split=1, order="row", **knobs) -> syn.Plan:
+    if d.op == "a2a":
+        return syn.Plan.a2a(d.R, d.r, d.rows_from, d.N, d.K, split=split, order=order, **knobs)
     return syn.Plan(d.op, d.R, d.r, d.M, d.N, d.K, split=split, order=order, **knobs)
 
 

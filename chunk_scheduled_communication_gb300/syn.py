@@ -55,7 +55,7 @@ class PlanInfo(ctypes.Structure):
                 ("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int), ("tiles_m", ctypes.c_int),
                 ("tiles_n", ctypes.c_int), ("n_tiles", ctypes.c_int), ("grid_compute", ctypes.c_int),
                 ("grid_comm", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("num_sms", ctypes.c_int),
-                ("epoch", ctypes.c_uint32), ("recv_bytes", ctypes.c_uint64)]
+                ("epoch", ctypes.c_uint32), ("recv_bytes", ctypes.c_uint64), ("a2a", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -71,6 +71,12 @@ _SIGS = {
     "syn_plan_create": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.POINTER(Layout), ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                        ctypes.POINTER(Knobs)]),
+    "syn_plan_create_a2a": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int, ctypes.c_int, _P, ctypes.c_int64,
+                                           ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(Knobs)]),
+    "syn_schedule_build_a2a": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _P, ctypes.c_int64, ctypes.c_int64,
+                                              ctypes.c_int, ctypes.c_int, ctypes.POINTER(Knobs),
+                                              ctypes.POINTER(PlanInfo), _P, _P, _P]),
+    "syn_a2a_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "syn_plan_destroy": (ctypes.c_int, [_P]),
     "syn_ag_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
     "syn_gemm_rs": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
@@ -167,6 +173,25 @@ def schedule_build(op, R, rank, M, N, K, chunk_rows=0, split=1, order="row", **k
     return info.as_dict(), tl, tk, tr[:info.n_transfers]
 
 
+def schedule_build_a2a(R, rank, rows_from, N, K, split=1, order="row", **knobs):
+    """Host-only A2A-GEMM schedule: info dict + tile_list, tile_key, transfers."""
+    L = lib()
+    rows = np.ascontiguousarray(rows_from, dtype=np.int64)
+    if rows.shape != (R,):
+        raise ValueError("rows_from needs R entries")
+    kn = make_knobs(**knobs)
+    info = PlanInfo()
+    _check(L.syn_schedule_build_a2a(R, rank, rows.ctypes.data, N, K, split, _order(order), ctypes.byref(kn),
+                                    ctypes.byref(info), None, None, None), "syn_schedule_build_a2a")
+    tl = np.empty(info.n_tiles, np.int32)
+    tk = np.empty(info.n_tiles, np.int32)
+    tr = np.empty(max(info.n_transfers, 1), np.int32)
+    _check(L.syn_schedule_build_a2a(R, rank, rows.ctypes.data, N, K, split, _order(order), ctypes.byref(kn),
+                                    ctypes.byref(info), tl.ctypes.data, tk.ctypes.data, tr.ctypes.data),
+           "syn_schedule_build_a2a")
+    return info.as_dict(), tl, tk, tr[:info.n_transfers]
+
+
 def _ptr(t) -> int:
     if t is None:
         return 0
@@ -194,6 +219,22 @@ class Plan:
                                        chunk_rows, split, _order(order), ctypes.byref(self.knobs)),
                "syn_plan_create")
         self.op, self.R, self.rank, self.M, self.N, self.K = _op(op), R, rank, M, N, K
+
+    @classmethod
+    def a2a(cls, R, rank, rows_from, N, K, split=1, order="row", **knobs):
+        """An A2A-GEMM plan: rank `rank`'s expert receives rows_from[q] rows from rank q."""
+        self = cls.__new__(cls)
+        self._L = lib()
+        self._h = _P()
+        rows = np.ascontiguousarray(rows_from, dtype=np.int64)
+        if rows.shape != (R,):
+            raise ValueError("rows_from needs R entries")
+        self.knobs = make_knobs(**knobs)
+        _check(self._L.syn_plan_create_a2a(ctypes.byref(self._h), R, rank, rows.ctypes.data, N, K, split,
+                                           _order(order), ctypes.byref(self.knobs)), "syn_plan_create_a2a")
+        self.op, self.R, self.rank, self.M, self.N, self.K = OPS["ag"], R, rank, int(rows.sum()), N, K
+        self.rows_from = rows
+        return self
 
     # -- lifetime
     def close(self):
@@ -253,6 +294,11 @@ class Plan:
         arr = (_P * self.R)(*[_ptr(s) for s in shards])
         _check(self._L.syn_ag_gemm(self._h, arr, _ptr(gathered), _ptr(B), _ptr(C), _stream(stream)),
                "syn_ag_gemm")
+
+    def a2a_gemm(self, parts, gathered, B, C, stream=None):
+        arr = (_P * self.R)(*[_ptr(s) for s in parts])
+        _check(self._L.syn_a2a_gemm(self._h, arr, _ptr(gathered), _ptr(B), _ptr(C), _stream(stream)),
+               "syn_a2a_gemm")
 
     def gemm_rs(self, A, B, peers, send, out_r, stream=None):
         arr = (_P * self.R)(*[_ptr(p) for p in peers])

@@ -14,6 +14,17 @@ Recipe (fixed order, numpy PCG64 ``default_rng(seed)``):
   AG : shards q = 0..R-1 (each [M_r, K]), then B [K, N]
   RS : A [M, K], then B [K, N], then the peers q != r in ascending q ([M, N] fp32)
   AR : same as RS
+  A2A: parts q = 0..R-1 (each [rows_from[q], K]), then B [K, N]; the routing
+       counts come from a generator of their own, ``default_rng(seed)`` in
+       ``Workload.rows_from`` (the same matrix of counts for every rank)
+A2A-GEMM (the MoE all-to-all + expert GEMM that the paper's sensitivity study,
+§6.3 / Fig. 11, tunes) has no shapes on the pages; the workload here is an
+expert-parallel mixture-of-experts FFN: R ranks, one expert each, every rank
+holding ``tokens`` tokens routed to ``top_k`` experts.  Routing counts: expert
+popularity p = softmax(skew * z), z ~ N(0, I_R); each source rank q sends
+expert r the count r of Multinomial(tokens * top_k, p), drawn for q = 0..R-1
+in order.  So blocks differ in size, the expert's row count M = sum_q rows_from[q]
+varies with r and the seed, and small configurations can have empty blocks.
 Every normal draw is ``standard_normal(float32) * scale``; bf16 operands are
 then rounded to nearest-even by ``torch.Tensor.to(torch.bfloat16)``.
 ``kind="int"`` draws integers in [-3, 3] instead (exactly representable, and
@@ -26,7 +37,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-OP_AG, OP_RS, OP_AR = "ag", "rs", "ar"
+OP_AG, OP_RS, OP_AR, OP_A2A = "ag", "rs", "ar", "a2a"
 
 
 @dataclass(frozen=True)
@@ -42,6 +53,9 @@ class Workload:
     peer_scale: float = 1.0
     splits: tuple = (1,)  # chunks per shard (AG) or per rank row block (RS/AR)
     note: str = ""
+    tokens: int = 0      # A2A: tokens per source rank
+    top_k: int = 0       # A2A: experts per token
+    skew: float = 0.0    # A2A: spread of the expert popularity logits
 
     @property
     def M_r(self) -> int:
@@ -50,6 +64,18 @@ class Workload:
     @property
     def flops(self) -> float:
         return 2.0 * self.M * self.N * self.K
+
+    def rows_from(self, r: int, seed: int = 0) -> list:
+        """A2A: the rows each source rank sends rank r's expert (recipe above)."""
+        assert self.op == OP_A2A
+        rng = np.random.default_rng(seed)
+        z = rng.standard_normal(self.R)
+        p = np.exp(self.skew * (z - z.max()))
+        p /= p.sum()
+        return [int(rng.multinomial(self.tokens * self.top_k, p)[r]) for _ in range(self.R)]
+
+    def a2a_flops(self, r: int, seed: int = 0) -> float:
+        return 2.0 * sum(self.rows_from(r, seed)) * self.N * self.K
 
 
 # The five workloads.  Names say what they are; sizes are the full ones.
@@ -64,14 +90,24 @@ QWEN2_7B_DOWN_AR = Workload("qwen2-7b-ffn-down-ar-tp8-M4096-K2368-N3584", OP_AR,
 LLAMA3_70B_UP_AG = Workload("llama3-70b-ffn-up-ag-tp8-M16384-K8192-N3584", OP_AG, 8, 16384, 8192, 3584,
                             1.0, 0.02, splits=(1, 2, 3, 4, 5, 6, 7, 8))
 
+# Expert-parallel MoE FFN up-projection in the shape of Mixtral-8x7B (hidden
+# 4096, expert FFN 14336, 8 experts, top-2): 8 ranks, one expert each, 4096
+# tokens per rank.  M is the nominal rows per expert (tokens * top_k); the
+# drawn counts vary around it.
+MIXTRAL_8X7B_EXPERT_UP_A2A = Workload("mixtral-8x7b-expert-up-a2a-ep8-T4096-top2-K4096-N14336", OP_A2A, 8,
+                                      4096 * 2, 4096, 14336, 1.0, 0.02, splits=(1, 2, 4),
+                                      tokens=4096, top_k=2, skew=0.5)
+TINY_A2A = Workload("tiny-a2a-R4-T96-top2-K256-N256", OP_A2A, 4, 96 * 2, 256, 256, 1.0 / 16, 1.0 / 16,
+                    tokens=96, top_k=2, skew=1.5, note="skewed routing: blocks of very different sizes")
+
 ALL = (TINY_AG, LLAMA3_8B_UP_AG, LLAMA3_8B_DOWN_RS, QWEN2_7B_DOWN_AR, LLAMA3_70B_UP_AG)
 
 
 def scaled(w: Workload, M: int | None = None, K: int | None = None, N: int | None = None,
-           R: int | None = None) -> Workload:
+           R: int | None = None, tokens: int | None = None) -> Workload:
     """Same workload family at another size (for small parity cases)."""
     return Workload(f"{w.name}-scaled", w.op, R or w.R, M or w.M, K or w.K, N or w.N,
-                    w.a_scale, w.b_scale, w.peer_scale, w.splits, w.note)
+                    w.a_scale, w.b_scale, w.peer_scale, w.splits, w.note, tokens or w.tokens, w.top_k, w.skew)
 
 
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -93,18 +129,25 @@ def _draw(rng: np.random.Generator, shape, scale: float, kind: str) -> np.ndarra
 class Inputs:
     w: Workload
     r: int
-    shards: list = field(default_factory=list)   # AG: R x uint16 [M_r, K]
+    shards: list = field(default_factory=list)   # AG: R x uint16 [M_r, K]; A2A: parts [rows_from[q], K]
+    rows_from: list | None = None                # A2A: rows each source sends
     A: np.ndarray | None = None                  # RS/AR: uint16 [M, K]
     B: np.ndarray | None = None                  # uint16 [K, N]
     peers: list = field(default_factory=list)    # RS/AR: R entries, fp32 [M, N], None at r
 
 
-def make_inputs(w: Workload, r: int = 0, seed: int = 0, kind: str = "normal") -> Inputs:
-    """Draw the inputs of workload ``w`` for local rank ``r``."""
+def make_inputs(w: Workload, r: int = 0, seed: int = 0, kind: str = "normal",
+                rows_from: tuple | None = None) -> Inputs:
+    """Draw the inputs of workload ``w`` for local rank ``r`` (A2A: ``rows_from``
+    overrides the drawn routing counts)."""
     rng = np.random.default_rng(seed)
     out = Inputs(w=w, r=r)
     if w.op == OP_AG:
         out.shards = [to_bf16_bits(_draw(rng, (w.M_r, w.K), w.a_scale, kind)) for _ in range(w.R)]
+        out.B = to_bf16_bits(_draw(rng, (w.K, w.N), w.b_scale, kind))
+    elif w.op == OP_A2A:
+        out.rows_from = list(rows_from) if rows_from is not None else w.rows_from(r, seed)
+        out.shards = [to_bf16_bits(_draw(rng, (m, w.K), w.a_scale, kind)) for m in out.rows_from]
         out.B = to_bf16_bits(_draw(rng, (w.K, w.N), w.b_scale, kind))
     else:
         out.A = to_bf16_bits(_draw(rng, (w.M, w.K), w.a_scale, kind))

@@ -202,6 +202,8 @@ typedef struct {
     int num_sms;
     uint32_t epoch;        /* calls issued so far                               */
     uint64_t recv_bytes;   /* plan-owned staging receive buffer                 */
+    int a2a;               /* 1: an A2A-GEMM plan (op is SYN_OP_AG_GEMM over
+                              per-source row blocks; M_r is 0)                 */
 } syn_plan_info_t;
 
 /* Host-only schedule builder: no CUDA call, usable without a GPU.
@@ -277,6 +279,46 @@ int syn_gemm_rs(syn_plan_t plan, const void *A, const void *B,
 int syn_gemm_ar(syn_plan_t plan, const void *A, const void *B,
                 const float *const *peer_partials, float *publish, void *out,
                 void *stream);
+
+/* A2A-GEMM: the MoE-style all-to-all followed by the expert GEMM (the
+ * operator pair the Syncopate paper's sensitivity study, §6.3 / Fig. 11,
+ * tunes beside AG-GEMM, GEMM-RS and GEMM-AR).  Rank r hosts one expert; every
+ * rank q (r included) sends it rows_from[q] token rows of K bf16 values.  The
+ * rows are gathered in source-rank order and multiplied by the expert weight:
+ *   gathered rows [off[q], off[q] + rows_from[q]) = part q, off[q] = sum_{p<q} rows_from[p]
+ *   C = gathered . B
+ * This is the AG-GEMM plan with row blocks of unequal size: block q is cut
+ * into `split` chunks of near-equal size (chunk j holds block rows
+ * [ceil(j*m/split), ceil((j+1)*m/split)), m = rows_from[q]; a block smaller
+ * than split has empty chunks, which still publish their flags); tiles wait
+ * only on the chunks they read, and the arrival order starts at the local
+ * block, then r+1, r+2, ... as in AG-GEMM.
+ *   rows_from : host int64 [R], each >= 0, sum M >= 1 (an expert that gets no
+ *               rows has nothing to compute: SYN_ERR_INVALID)
+ *   split     : 1 <= split <= 64 (0 means 1)
+ *   knobs     : as syn_plan_create (TMA_COLOCATED_SMEM is GEMM-RS/AR only)
+ * Every staging backend works as for AG-GEMM.  The plan reports a2a = 1. */
+int syn_plan_create_a2a(syn_plan_t *out, int R, int rank, const int64_t *rows_from,
+                        int64_t N, int64_t K, int split, syn_order_t order,
+                        const syn_knobs_t *knobs);
+
+/* Host-only A2A-GEMM schedule (no CUDA call), as syn_schedule_build. */
+int syn_schedule_build_a2a(int R, int rank, const int64_t *rows_from, int64_t N, int64_t K,
+                           int split, syn_order_t order, const syn_knobs_t *knobs,
+                           syn_plan_info_t *info, int32_t *tile_list, int32_t *tile_key,
+                           int32_t *transfers);
+
+/* Run an A2A-GEMM plan (asynchronous on `stream`).
+ *   parts    : host array of R device pointers, bf16 [rows_from[q], K] each
+ *              (NULL allowed where rows_from[q] == 0); parts[r] may alias
+ *              gathered + off[r]*K (in place, not copied)
+ *   gathered : bf16 [M, K] output, gathered[off[q] + i] = parts[q][i] bit for bit
+ *   B        : bf16 [K, N];  C : bf16 [M, N] = gathered . B (fp32 accumulation,
+ *              one round-to-nearest-even)
+ * Returns SYN_ERR_INVALID for a plan made by syn_plan_create (and syn_ag_gemm
+ * does for an A2A-GEMM plan). */
+int syn_a2a_gemm(syn_plan_t plan, const void *const *parts, void *gathered,
+                 const void *B, void *C, void *stream);
 
 /* Synchronise `stream`, then read and clear the plan's device error word.
  * Returns SYN_OK, SYN_ERR_TIMEOUT or SYN_ERR_BOUNDS (device side) or

@@ -49,6 +49,9 @@ typedef struct {
                              publishes its flag before its own copy and only
                              then copies (after a 2 ms pause), so consumers
                              must report SYN_PROTO_STALE_DATA                 */
+    const int64_t *rows_from; /* NULL, or (op 0 only) the A2A-GEMM row count
+                             each source sends, R entries; M is then ignored
+                             and taken as their sum                           */
 } syn_proto_cfg_t;
 
 /* Run cfg->calls calls.  status[c] receives the status of call c + 1; after a

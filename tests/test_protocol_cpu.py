@@ -83,3 +83,32 @@ def test_a_broken_protocol_is_caught():
 def test_rejected_plan_reports_invalid():
     with pytest.raises(ValueError):
         proto.emulate(op="rs", R=4, rank=0, M=4 * 100, N=256, K=64)  # M/R not a multiple of 128
+
+
+# --------------------------------------------------------------------------- A2A-GEMM row blocks
+@pytest.mark.parametrize("rows_from,rank,split,tile_m", [
+    ([300, 0, 41, 1000], 2, 1, 128),      # an empty block inside a tile's rows
+    ([300, 0, 41, 1000], 0, 3, 256),
+    ([5, 7, 0, 1, 900, 64, 0, 33], 6, 4, 128),
+    ([2, 3], 1, 8, 128),                  # blocks smaller than split: empty chunks
+    ([0, 0, 0, 700], 3, 2, 128),          # only the local rank sends
+])
+def test_a2a_every_tile_sees_its_chunks(rows_from, rank, split, tile_m):
+    M = sum(rows_from)
+    st, tc = proto.emulate(op="ag", R=len(rows_from), rank=rank, M=0, N=256, K=64, split=split, tile_m=tile_m,
+                           walkers=6, stagers=5, slice_bytes=2048, calls=3, rows_from=rows_from)
+    assert st == [0, 0, 0]
+    assert tc == [n_tiles(M, 256, tile_m, 256)] * 3
+
+
+def test_a2a_dropped_flag_times_out_then_recovers():
+    # rank 0 of [400, 100, 0, 250]: arrival 0 is the local chunk (in place);
+    # arrival 1 is source 1's chunk, which tiles 3 and 4 read
+    st, tc = proto.emulate(op="ag", R=4, rank=0, M=0, N=256, K=64, split=1, calls=3, drop_transfer=1,
+                           drop_call=2, timeout_us=50_000, rows_from=[400, 100, 0, 250])
+    assert st == [0, TIMEOUT, 0]
+
+
+def test_a2a_rows_from_rejected_outside_ag():
+    with pytest.raises(ValueError):
+        proto.emulate(op="rs", R=2, rank=0, M=0, N=256, K=64, rows_from=[128, 128])

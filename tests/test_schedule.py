@@ -261,3 +261,77 @@ def test_smem_rs_spread_noop_for_short_walks():
     _, tl0, _, _ = syn.schedule_build("rs", 4, 1, 1024, 512, 256, **kw)
     _, tl1, _, _ = syn.schedule_build("rs", 4, 1, 1024, 512, 256, reduce_spread=8, **kw)
     assert tl0.tolist() == tl1.tolist()  # 16 tiles over 8 walkers: 2 rounds only
+
+
+# --------------------------------------------------------------------------- A2A-GEMM
+# Row blocks of unequal size (rows_from[q] rows from source q, stacked in
+# ascending q); each block cut into `split` chunks, chunk j of block q holding
+# block rows [ceil(j*m/split), ceil((j+1)*m/split)).
+def a2a_chunk_rows(rows_from, split):
+    """Global [row0, row1) of every row chunk rc = q*split + j, by definition."""
+    off = np.concatenate([[0], np.cumsum(rows_from)]).tolist()
+    out = []
+    for q, m in enumerate(rows_from):
+        for j in range(split):
+            out.append((off[q] + -(-j * m // split), off[q] + -(-(j + 1) * m // split)))
+    return out
+
+
+def a2a_deps(rows_from, split, tm, tile_m=128):
+    R, M = len(rows_from), int(sum(rows_from))
+    rows = set(range(tm * tile_m, min((tm + 1) * tile_m, M)))
+    spans = a2a_chunk_rows(rows_from, split)
+    rcs = [rc for rc, (a, b) in enumerate(spans) if rows & set(range(a, b))]
+    return [rc * R + rc // split for rc in rcs]
+
+
+A2A_CASES = [
+    ([300, 0, 41, 1000], 1, 2, 256),
+    ([300, 0, 41, 1000], 3, 0, 512),
+    ([0, 0, 0, 128], 2, 1, 256),           # one source sends everything
+    ([5, 7, 0, 1, 900, 64, 0, 33], 4, 6, 256),
+    ([128, 128, 128, 128], 2, 3, 512),     # equal parts
+    ([2, 3], 8, 1, 256),                   # blocks smaller than split: empty chunks
+    ([4096, 1500, 2600, 0, 3000, 700, 2048, 512], 2, 4, 1024),
+]
+
+
+@pytest.mark.parametrize("rows_from,split,r,N", A2A_CASES)
+@pytest.mark.parametrize("order", ["row", "grouped"])
+def test_a2a_schedule_properties(rows_from, split, r, N, order):
+    R, M, K = len(rows_from), int(sum(rows_from)), 128
+    tile_n = 256
+    info, tl, tk, tr = syn.schedule_build_a2a(R, r, rows_from, N, K, split=split, order=order, tile_n=tile_n)
+    tiles_m, tiles_n = -(-M // 128), N // tile_n
+    assert info["a2a"] == 1 and info["M"] == M and info["M_r"] == 0
+    assert info["n_row_chunks"] == R * split and info["n_tiles"] == tiles_m * tiles_n
+    assert info["chunk_rows"] == max(-(-m // split) for m in rows_from)
+    assert sorted(tl.tolist()) == list(range(tiles_m * tiles_n))
+    # the same arrival order as AG-GEMM: local block first, then r+1, r+2, ...
+    assert tr.tolist() == expected_transfers("ag", R, r, split)
+    arrival = {code: a for a, code in enumerate(tr.tolist())}
+    for t, key in zip(tl.tolist(), tk.tolist()):
+        d = a2a_deps(rows_from, split, t // tiles_n)
+        assert d and key == max(arrival[c] for c in d), (t, key, d)
+    assert (np.diff(tk) >= 0).all()
+
+
+def test_a2a_equal_parts_is_the_ag_schedule():
+    for r, split in [(0, 1), (3, 2), (5, 3)]:
+        a = syn.schedule_build("ag", 8, r, 8192, 1792, 4096, split=split)
+        b = syn.schedule_build_a2a(8, r, [1024] * 8, 1792, 4096, split=split)
+        for x, y in zip(a[1:], b[1:]):
+            assert (x == y).all()
+        assert a[0]["chunk_rows"] == b[0]["chunk_rows"] and b[0]["a2a"] == 1
+
+
+@pytest.mark.parametrize("rows_from,split,status", [
+    ([4, -1, 3], 1, syn.ERR_INVALID),
+    ([0, 0, 0], 1, syn.ERR_INVALID),         # nothing to multiply
+    ([64, 64], 65, syn.ERR_INVALID),         # split > 64
+    ([1] * 9, 1, syn.ERR_UNSUPPORTED),       # R > 8
+])
+def test_a2a_invalid_rejected(rows_from, split, status):
+    with pytest.raises(syn.SynError) as e:
+        syn.schedule_build_a2a(len(rows_from), 0, rows_from, 256, 128, split=split)
+    assert e.value.status == status
