@@ -85,9 +85,13 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         err = "only dense row-major layouts are supported";
         return SYN_ERR_UNSUPPORTED;
     }
-    if (order < SYN_ORDER_ROW_MAJOR || order > SYN_ORDER_GROUPED) {
+    if (order < SYN_ORDER_ROW_MAJOR || order > SYN_ORDER_BANDED) {
         err = "unknown tile order";
         return SYN_ERR_INVALID;
+    }
+    if (order == SYN_ORDER_BANDED && op != SYN_OP_AG_GEMM) {
+        err = "the banded tile order is for AG-GEMM and A2A-GEMM";
+        return SYN_ERR_UNSUPPORTED;
     }
     const int64_t M_r = var_blocks ? 0 : L.M / R;
     if (chunk_rows < 0 || split < 0) {
@@ -204,8 +208,7 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         int64_t t0, t1, t2;
         int32_t tile;
     };
-    std::vector<Item> items;
-    items.reserve(s.n_tiles);
+    std::vector<int32_t> row_key((size_t)s.tiles_m, -1);
     for (int tm = 0; tm < s.tiles_m; ++tm) {
         int lo, hi;
         tile_row_chunks(s, tm, lo, hi);
@@ -225,9 +228,20 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
                     if (a > key) key = a;
                 }
         }
+        row_key[(size_t)tm] = key;
+    }
+    if (order == SYN_ORDER_BANDED)  // a band waits for the latest chunk of any of its rows
+        for (int b0 = 0; b0 < s.tiles_m; b0 += s.group_m) {
+            const int b1 = std::min(s.tiles_m, b0 + s.group_m);
+            const int32_t k = *std::max_element(row_key.begin() + b0, row_key.begin() + b1);
+            std::fill(row_key.begin() + b0, row_key.begin() + b1, k);
+        }
+    std::vector<Item> items;
+    items.reserve(s.n_tiles);
+    for (int tm = 0; tm < s.tiles_m; ++tm) {
         for (int tn = 0; tn < s.tiles_n; ++tn) {
             Item it;
-            it.key = key;
+            it.key = row_key[(size_t)tm];
             it.tile = tm * s.tiles_n + tn;
             switch (order) {
                 case SYN_ORDER_ROW_MAJOR:

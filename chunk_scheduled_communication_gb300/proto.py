@@ -35,7 +35,7 @@ def lib():
 
 
 OPS = {"ag": 0, "rs": 1, "ar": 2}
-ORDERS = {"row": 0, "col": 1, "grouped": 2}
+ORDERS = {"row": 0, "col": 1, "grouped": 2, "banded": 3}
 
 
 def emulate(op="ag", R=4, rank=0, M=1024, N=256, K=64, split=1, order="row", tile_m=128, tile_n=256,

@@ -72,7 +72,13 @@ typedef enum {
 typedef enum {
     SYN_ORDER_ROW_MAJOR = 0, /* tile rows in order, columns fastest             */
     SYN_ORDER_COL_MAJOR = 1, /* tile columns in order, rows fastest             */
-    SYN_ORDER_GROUPED = 2    /* group_m tile rows at a time, column by column   */
+    SYN_ORDER_GROUPED = 2,   /* group_m tile rows at a time, column by column   */
+    SYN_ORDER_BANDED = 3     /* AG-GEMM / A2A-GEMM only: bands of group_m tile
+                                rows, each keyed by the latest chunk any of its
+                                rows reads; bands in key order, each column by
+                                column.  Coarser than the chunk order, so each
+                                band reads the whole of B once from HBM and
+                                keeps its A rows in L2 (B larger than L2)   */
 } syn_order_t;
 
 /* Staging backends for one plan (method ¶3, paper §5.2, Fig. 7), plus the two

@@ -187,3 +187,27 @@ def test_mixtral_expert_up_full_size_sampled_rows(r):
     _, ce = run(w, r, backend="ce", split=1)
     ok, exc, frob = runner.bf16_close(ce["out"], got["out"])
     assert ok, (exc, frob)
+
+
+# ----------------------------------------------------------------------------- banded tile order
+@pytest.mark.parametrize("group_m,tile_m,backend", [(2, 128, "tma_colocated"), (4, 256, "tma_colocated"),
+                                                    (3, 128, "ce"), (2, 256, "decomposed")])
+def test_banded_order_bit_exact(group_m, tile_m, backend):
+    """The banded order (bands of group_m tile rows keyed by their latest
+    chunk) moves tiles, never values: integer inputs give the oracle's bits."""
+    w, rows, kind = a2a_case(8, INT8, 192, 512, kind="int")
+    inp, got = run(w, 3, rows, kind=kind, backend=backend, split=2, order="banded", tile_m=tile_m,
+                   group_m=group_m)
+    check(inp, got, kind)
+
+
+def test_banded_order_ag_gemm_bit_exact():
+    w = wl.scaled(wl.TINY_AG, M=3 * 200, K=192, N=512, R=3)
+    inp = wl.make_inputs(w, r=1, kind="int")
+    d = runner.upload(inp)
+    with runner.make_plan(d, split=2, order="banded", backend="tma_colocated", group_m=2) as plan:
+        runner.call(plan, d)
+        assert plan.sync() == syn.OK
+    g_ref, c_ref = oracle.ag_gemm(inp.shards, inp.B)
+    assert (runner.dev_to_u16(d.gathered) == g_ref).all()
+    assert (runner.dev_to_u16(d.out) == c_ref).all()

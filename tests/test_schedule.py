@@ -335,3 +335,50 @@ def test_a2a_invalid_rejected(rows_from, split, status):
     with pytest.raises(syn.SynError) as e:
         syn.schedule_build_a2a(len(rows_from), 0, rows_from, 256, 128, split=split)
     assert e.value.status == status
+
+
+# --------------------------------------------------------------------------- banded order
+@pytest.mark.parametrize("kind,args,group_m", [
+    ("a2a", ([300, 0, 41, 1000], 14336, 4096), 8),
+    ("a2a", ([869, 895, 930, 901, 841, 876, 904, 883], 14336, 4096), 4),
+    ("ag", (16384, 3584, 8192), 8),
+    ("ag", (4 * 100, 256, 128), 3),
+])
+@pytest.mark.parametrize("r,split", [(0, 1), (2, 3)])
+def test_banded_order(kind, args, group_m, r, split):
+    """Bands of group_m tile rows: a band's key is the latest arrival any of
+    its rows waits for; bands run in key order, each column by column."""
+    if kind == "a2a":
+        rows_from, N, K = args
+        R = len(rows_from)
+        if r >= R:
+            pytest.skip("no such rank")
+        info, tl, tk, tr = syn.schedule_build_a2a(R, r, rows_from, N, K, split=split, order="banded",
+                                                  group_m=group_m)
+        _, tl0, tk0, _ = syn.schedule_build_a2a(R, r, rows_from, N, K, split=split, order="row")
+    else:
+        M, N, K = args
+        R = 8 if M > 1000 else 4
+        info, tl, tk, tr = syn.schedule_build("ag", R, r, M, N, K, split=split, order="banded", group_m=group_m)
+        _, tl0, tk0, _ = syn.schedule_build("ag", R, r, M, N, K, split=split, order="row")
+    tiles_n = info["tiles_n"]
+    row_key = {}
+    for t, k in zip(tl0.tolist(), tk0.tolist()):
+        row_key[t // tiles_n] = k        # the chunk key of each tile row (row order)
+    band_key = {}
+    for tm, k in row_key.items():
+        b = tm // group_m
+        band_key[b] = max(band_key.get(b, -1), k)
+    assert sorted(tl.tolist()) == sorted(tl0.tolist())
+    for t, k in zip(tl.tolist(), tk.tolist()):
+        assert k == band_key[(t // tiles_n) // group_m]
+    want = sorted(tl.tolist(), key=lambda t: (band_key[(t // tiles_n) // group_m], (t // tiles_n) // group_m,
+                                               t % tiles_n, (t // tiles_n) % group_m))
+    assert tl.tolist() == want
+
+
+@pytest.mark.parametrize("op", ["rs", "ar"])
+def test_banded_order_rejected_for_rs_ar(op):
+    with pytest.raises(syn.SynError) as e:
+        syn.schedule_build(op, 8, 0, 8192, 4096, 1792, order="banded")
+    assert e.value.status == syn.ERR_UNSUPPORTED
