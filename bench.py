@@ -50,7 +50,8 @@ DEFAULT_KNOBS = {
     "ag": dict(backend="tma_colocated", split=4, order="grouped", tile_m=256, tile_n=256, comm_sms=8, stages=0),
     "rs": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=6),
     "ar": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=5),
-    "a2a": dict(backend="tma_colocated", split=2, order="grouped", tile_m=256, tile_n=256, comm_sms=8, stages=0),
+    "a2a": dict(backend="tma_colocated", split=1, order="banded", group_m=8, tile_m=256, tile_n=256, comm_sms=8,
+                stages=5),
 }
 # A2A-GEMM (the MoE all-to-all + expert GEMM) is measured beside the step, on
 # its own line of the JSON ("a2a"), not inside the headline value.

@@ -24,6 +24,7 @@ WORKLOADS = {
     "rs": wl.LLAMA3_8B_DOWN_RS,
     "ar": wl.QWEN2_7B_DOWN_AR,
     "ag70": wl.LLAMA3_70B_UP_AG,
+    "a2a": wl.MIXTRAL_8X7B_EXPERT_UP_A2A,
 }
 
 
@@ -32,7 +33,8 @@ def main(argv=None) -> int:
     ap.add_argument("--op", choices=sorted(WORKLOADS), default="ag")
     ap.add_argument("--backend", default="tma_colocated")
     ap.add_argument("--split", type=int, default=1)
-    ap.add_argument("--order", default="row", choices=["row", "col", "grouped"])
+    ap.add_argument("--order", default="row", choices=["row", "col", "grouped", "banded"])
+    ap.add_argument("--group-m", type=int, default=8)
     ap.add_argument("--tile-m", type=int, default=0)
     ap.add_argument("--tile-n", type=int, default=256)
     ap.add_argument("--tile-k", type=int, default=0)
@@ -46,7 +48,8 @@ def main(argv=None) -> int:
     d = runner.upload(wl.make_inputs(w, r=0), with_f32_out=(w.op == "rs"))  # RS: send rows; AR: no publish
     stream = torch.cuda.current_stream()
     with runner.make_plan(d, split=a.split, order=a.order, backend=a.backend, tile_m=a.tile_m,
-                          tile_n=a.tile_n, tile_k=a.tile_k, stages=a.stages, comm_sms=a.comm_sms) as p:
+                          tile_n=a.tile_n, tile_k=a.tile_k, stages=a.stages, comm_sms=a.comm_sms,
+                          group_m=a.group_m) as p:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(a.calls):

@@ -171,7 +171,7 @@ def test_mixtral_expert_up_full_size_sampled_rows(r):
     sampled rows (block boundaries and the ragged tail included) against the
     oracle, and the single-CTA CE path bit-identical."""
     w = wl.MIXTRAL_8X7B_EXPERT_UP_A2A
-    inp, got = run(w, r, backend="tma_colocated", split=2, order="grouped", tile_m=256)
+    inp, got = run(w, r, backend="tma_colocated", split=1, order="banded", group_m=8, tile_m=256, stages=5)
     g_ref = np.concatenate(inp.shards)
     assert (got["gathered"] == g_ref).all()
     M = g_ref.shape[0]
