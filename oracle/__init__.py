@@ -1,4 +1,4 @@
-"""Plain CPU oracle for AG-GEMM, GEMM-RS, GEMM-AR and A2A-GEMM (test infrastructure).
+"""Plain CPU oracle for AG-GEMM, GEMM-RS, GEMM-AR, A2A-GEMM and ring attention (test infrastructure).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` leg of ``bench.py`` may import this package; the product path
@@ -39,7 +39,7 @@ def build(force: bool = False) -> str:
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O3", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared", _SRC, "-o", tmp]
+           "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -68,8 +68,10 @@ def _load():
         lib.oracle_gemm_rs_send.argtypes = [i32, i32, i64, i64, i64, p, p, i64, i64, p]
         lib.oracle_gemm_ar.argtypes = [i32, i32, i64, i64, i64, p, p, p, i64, i64, p, p]
         lib.oracle_a2a_gemm.argtypes = [i32, p, i64, i64, p, p, i64, i64, p, p]
+        lib.oracle_ring_attention.argtypes = [i32, i32, i64, i32, i32, i32, i32, ctypes.c_double, p, p, p,
+                                              i64, i64, p, p]
         for f in ("oracle_gather", "oracle_gemm_f32", "oracle_ag_gemm", "oracle_gemm_rs_out",
-                  "oracle_gemm_rs_send", "oracle_gemm_ar", "oracle_a2a_gemm"):
+                  "oracle_gemm_rs_send", "oracle_gemm_ar", "oracle_a2a_gemm", "oracle_ring_attention"):
             getattr(lib, f).restype = None
         _lib = lib
         return lib
@@ -170,6 +172,29 @@ def a2a_gemm(parts, B, row0: int = 0, row1: int | None = None, want_gathered: bo
     lib.oracle_a2a_gemm(R, _ptr(rows), K, N, _ptr_array(parts), _ptr(B), row0, row1,
                         _ptr(g) if g is not None else None, _ptr(C))
     return g, C
+
+
+def ring_attention(Q, Ks, Vs, r: int, causal: bool = False, scale: float | None = None,
+                   row0: int = 0, row1: int | None = None):
+    """Ring attention forward of rank r over the keys of all ranks (fp64).
+
+    Q: uint16 [S_r, H_q, d]; Ks, Vs: R arrays uint16 [S_r, H_kv, d].
+    Returns (O float64 [row1-row0, H_q, d], lse float64 [row1-row0, H_q])."""
+    lib = _load()
+    Q = _u16(Q)
+    Ks = [_u16(k) for k in Ks]
+    Vs = [_u16(v) for v in Vs]
+    S_r, H_q, d = Q.shape
+    R = len(Ks)
+    H_kv = Ks[0].shape[1]
+    assert all(k.shape == (S_r, H_kv, d) for k in Ks + Vs) and H_q % H_kv == 0
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    row1 = S_r if row1 is None else row1
+    O = np.empty((row1 - row0, H_q, d), dtype=np.float64)
+    lse = np.empty((row1 - row0, H_q), dtype=np.float64)
+    lib.oracle_ring_attention(R, r, S_r, H_q, H_kv, d, 1 if causal else 0, scale, _ptr(Q), _ptr_array(Ks),
+                              _ptr_array(Vs), row0, row1, _ptr(O), _ptr(lse))
+    return O, lse
 
 
 def _peer_ptrs(peers, R, r, M, N):

@@ -20,6 +20,9 @@
  *              send[rows_q] = P[rows_q], q != r
  *              out_r = bf16_rne(P[rows_r] + sum_{q != r, ascending q} peer_q[rows_r])
  *   GEMM-AR  : out = bf16_rne(P + sum_{q != r, ascending q} peer_q);  publish = P
+ *   ring attention (sequence parallel, the pages' RingAttention workload):
+ *              O_r = softmax(scale . Q_r K^T [+ causal mask]) V over the keys of
+ *              all R ranks, in fp64 (see oracle_ring_attention)
  *   A2A-GEMM : G = concat_q(part_q), parts of rows_from[q] rows (bit copy),
  *              C = bf16_rne(G . B)   -- the MoE-style all-to-all + expert
  *              GEMM that the paper's sensitivity study (§6.3, Fig. 11)
@@ -40,6 +43,7 @@
  * and writes its outputs compactly: output row i goes to index (i - row0).
  * This lets callers sample rows of a large problem.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -262,5 +266,71 @@ void oracle_gemm_ar(int R, int r, int64_t M, int64_t K, int64_t N,
                 o[j] = oracle_bf16_rne(reduce_peers(acc[j], R, r, peers, g * N + j));
         }
         free(acc);
+    }
+}
+
+/* Ring attention forward of rank r (sequence parallelism: every rank holds
+ * S_r consecutive tokens; rank q's tokens have global positions
+ * [q*S_r, (q+1)*S_r)).  Layouts are token-major: Q [S_r, H_q, d],
+ * K[q] and V[q] [S_r, H_kv, d], bf16.  Query head h reads KV head
+ * h / (H_q / H_kv).  For query row i (global position r*S_r + i) and head h,
+ * over the R*S_r keys j in global order:
+ *   s_j   = scale * sum_k Q[i][h][k] * K[j][hk][k]        (fp64)
+ *   causal: keys with j > r*S_r + i take no part
+ *   O[i][h][:] = sum_j exp(s_j - m) V[j][hk][:] / sum_j exp(s_j - m),  m = max_j s_j
+ *   lse[i][h]  = m + log(sum_j exp(s_j - m))               (natural log)
+ * Rows [row0, row1) of the rank's queries are computed and written compactly
+ * (O [(row1-row0), H_q, d], lse [(row1-row0), H_q], both fp64; lse may be
+ * NULL).  Subtracting m changes nothing mathematically; it keeps exp finite. */
+void oracle_ring_attention(int R, int r, int64_t S_r, int H_q, int H_kv, int d, int causal,
+                           double scale, const uint16_t *Q, const uint16_t *const *K,
+                           const uint16_t *const *V, int64_t row0, int64_t row1,
+                           double *O, double *lse)
+{
+    const int G = H_q / H_kv;
+    const int64_t S = (int64_t)R * S_r;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)S * sizeof(double));
+        double *q = (double *)malloc((size_t)d * sizeof(double));
+#pragma omp for schedule(dynamic, 1) collapse(2)
+        for (int64_t i = row0; i < row1; ++i) {
+            for (int h = 0; h < H_q; ++h) {
+                const int hk = h / G;
+                const int64_t pos = (int64_t)r * S_r + i;
+                const int64_t nkeys = causal ? pos + 1 : S;
+                for (int k = 0; k < d; ++k)
+                    q[k] = (double)widen_bf16(Q[(i * H_q + h) * d + k]);
+                double m = -INFINITY;
+                for (int64_t j = 0; j < nkeys; ++j) {
+                    const uint16_t *kr = K[j / S_r] + ((j % S_r) * H_kv + hk) * d;
+                    double acc = 0.0;
+                    for (int k = 0; k < d; ++k)
+                        acc += q[k] * (double)widen_bf16(kr[k]);
+                    s[j] = scale * acc;
+                    if (s[j] > m)
+                        m = s[j];
+                }
+                double l = 0.0;
+                for (int64_t j = 0; j < nkeys; ++j) {
+                    s[j] = exp(s[j] - m);
+                    l += s[j];
+                }
+                double *o = O + ((i - row0) * H_q + h) * d;
+                for (int k = 0; k < d; ++k)
+                    o[k] = 0.0;
+                for (int64_t j = 0; j < nkeys; ++j) {
+                    const uint16_t *vr = V[j / S_r] + ((j % S_r) * H_kv + hk) * d;
+                    for (int k = 0; k < d; ++k)
+                        o[k] += s[j] * (double)widen_bf16(vr[k]);
+                }
+                for (int k = 0; k < d; ++k)
+                    o[k] /= l;
+                if (lse)
+                    lse[(i - row0) * H_q + h] = m + log(l);
+            }
+        }
+        free(s);
+        free(q);
     }
 }

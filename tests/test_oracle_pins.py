@@ -416,3 +416,98 @@ def test_a2a_part_independence_and_row_ranges(oracle_lib):
     M = int(off[-1])
     pieces = [oracle_lib.a2a_gemm(parts, B, a, b, want_gathered=False)[1] for a, b in [(0, 8), (8, 9), (9, M)]]
     assert (np.concatenate(pieces) == C).all()
+
+
+# --------------------------------------------------------------------------- ring attention
+# Sequence-parallel attention over the keys of all ranks (the pages'
+# RingAttention workload, summary Experiments, paper §6.1): the oracle is the
+# plain softmax(scale Q K^T [+ causal mask]) V in fp64.
+def _attn_inputs(rng, R, S_r, H_q, H_kv, d, scale=1.0):
+    b = lambda shape: wl.to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(scale))
+    return b((S_r, H_q, d)), [b((S_r, H_kv, d)) for _ in range(R)], [b((S_r, H_kv, d)) for _ in range(R)]
+
+
+def test_hand_worked_ring_attention(oracle_lib):
+    g = json.load(open(os.path.join(GOLD, "hand_worked_ops.json")))["ring_attention"]
+    Q, K, V = (_bits(np.array(g[k], dtype=np.float32)) for k in ("Q", "K", "V"))
+    for causal, ko, kl in ((False, "O", "lse"), (True, "O_causal", "lse_causal")):
+        O, lse = oracle_lib.ring_attention(Q, [K], [V], 0, causal=causal, scale=1.0)
+        assert np.abs(O - np.array(g[ko])).max() < 1e-15, (causal, O)
+        assert np.abs(lse - np.array(g[kl])).max() < 1e-15, (causal, lse)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("R,r,H_q,H_kv", [(3, 1, 4, 2), (2, 0, 2, 2), (4, 3, 4, 1)])
+def test_ring_attention_matches_library_sdpa(oracle_lib, causal, R, r, H_q, H_kv):
+    """torch's scaled_dot_product_attention in float64 over the concatenated
+    keys (GQA heads expanded by hand), with the global-position causal mask."""
+    rng = np.random.default_rng(40 + R + r)
+    S_r, d = 7, 16
+    Q, Ks, Vs = _attn_inputs(rng, R, S_r, H_q, H_kv, d)
+    O, lse = oracle_lib.ring_attention(Q, Ks, Vs, r, causal=causal)
+    q = torch.from_numpy(bits_to_f64(Q)).permute(1, 0, 2)                       # [H_q, S_r, d]
+    k = torch.from_numpy(np.concatenate([bits_to_f64(x) for x in Ks])).permute(1, 0, 2)
+    v = torch.from_numpy(np.concatenate([bits_to_f64(x) for x in Vs])).permute(1, 0, 2)
+    k = k.repeat_interleave(H_q // H_kv, dim=0)
+    v = v.repeat_interleave(H_q // H_kv, dim=0)
+    pos_q = r * S_r + torch.arange(S_r)[:, None]
+    pos_k = torch.arange(R * S_r)[None, :]
+    mask = (pos_k <= pos_q) if causal else torch.ones(S_r, R * S_r, dtype=torch.bool)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask).permute(1, 0, 2).numpy()
+    assert np.abs(O - ref).max() < 1e-12
+    scores = (q @ k.transpose(1, 2)) / np.sqrt(d)
+    ref_lse = torch.logsumexp(scores.masked_fill(~mask, float("-inf")), dim=-1).T.numpy()
+    assert np.abs(lse - ref_lse).max() < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_attention_zero_queries_average_the_visible_values(oracle_lib, causal):
+    rng = np.random.default_rng(50)
+    R, r, S_r, H, d = 3, 2, 5, 2, 8
+    _, Ks, Vs = _attn_inputs(rng, R, S_r, H, H, d)
+    Q = np.zeros((S_r, H, d), np.uint16)
+    O, lse = oracle_lib.ring_attention(Q, Ks, Vs, r, causal=causal)
+    V = np.concatenate([bits_to_f64(v) for v in Vs])
+    for i in range(S_r):
+        n = r * S_r + i + 1 if causal else R * S_r
+        assert np.allclose(O[i], V[:n].mean(axis=0), rtol=0, atol=1e-13)
+        assert np.allclose(lse[i], np.log(n), rtol=0, atol=1e-13)
+
+
+def test_ring_attention_one_dominant_key_selects_its_value(oracle_lib):
+    """Scores 0 everywhere but one key at 64: its weight is 1 - O(e^-64)."""
+    rng = np.random.default_rng(51)
+    R, r, S_r, H, d = 2, 1, 4, 1, 4
+    _, _, Vs = _attn_inputs(rng, R, S_r, H, H, d)
+    for jstar in (0, 5, 7):
+        Q = np.zeros((S_r, H, d), np.float32)
+        Q[:, :, 1] = 8.0
+        Ks = [np.zeros((S_r, H, d), np.float32) for _ in range(R)]
+        Ks[jstar // S_r][jstar % S_r, 0, 1] = 16.0
+        O, _ = oracle_lib.ring_attention(_bits(Q), [_bits(k) for k in Ks], Vs, r, scale=0.5)
+        want = bits_to_f64(Vs[jstar // S_r][jstar % S_r, 0])
+        bound = (R * S_r - 1) * np.exp(-64.0) * 2 * np.abs(np.stack([bits_to_f64(v) for v in Vs])).max()
+        assert np.abs(O[:, 0, :] - want).max() <= bound
+
+
+def test_ring_attention_lse_merges_per_rank_partials(oracle_lib):
+    """RingAttention's combination rule: attention over all keys equals the
+    per-rank partial attentions weighted by exp(lse_q - lse), lse = logsumexp_q lse_q."""
+    rng = np.random.default_rng(52)
+    R, r, S_r, H_q, H_kv, d = 4, 1, 6, 4, 2, 16
+    Q, Ks, Vs = _attn_inputs(rng, R, S_r, H_q, H_kv, d)
+    O, lse = oracle_lib.ring_attention(Q, Ks, Vs, r)
+    parts = [oracle_lib.ring_attention(Q, [Ks[q]], [Vs[q]], 0, scale=1.0 / np.sqrt(d)) for q in range(R)]
+    lse_all = np.logaddexp.reduce(np.stack([p[1] for p in parts]), axis=0)
+    merged = sum(np.exp(p[1] - lse_all)[..., None] * p[0] for p in parts)
+    assert np.abs(lse - lse_all).max() < 1e-12 and np.abs(O - merged).max() < 1e-12
+
+
+def test_ring_attention_gqa_equals_repeated_heads(oracle_lib):
+    rng = np.random.default_rng(53)
+    R, r, S_r, H_q, H_kv, d = 2, 0, 5, 6, 2, 8
+    Q, Ks, Vs = _attn_inputs(rng, R, S_r, H_q, H_kv, d)
+    O, lse = oracle_lib.ring_attention(Q, Ks, Vs, r, causal=True)
+    rep = lambda xs: [np.ascontiguousarray(np.repeat(x, H_q // H_kv, axis=1)) for x in xs]
+    O2, lse2 = oracle_lib.ring_attention(Q, rep(Ks), rep(Vs), r, causal=True)
+    assert (O == O2).all() and (lse == lse2).all()
