@@ -27,6 +27,7 @@
 #include <vector>
 
 #include "fused.h"
+#include "host_util.h"
 #include "schedule.h"
 #include "syn.h"
 
@@ -104,6 +105,20 @@ int encode_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esiz
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+namespace syn {
+int host_fail(int code, const std::string &msg) { return fail(code, msg); }
+int host_load_driver() { return load_driver(); }
+int host_encode_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, uint64_t cols,
+                   uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
+    return encode_2d(m, base, dt, esize, cols, rows, box_cols, box_rows, swz);
+}
+CUresult host_write32(cudaStream_t st, uint32_t *addr, uint32_t value) {
+    return p_write32(reinterpret_cast<CUstream>(st), reinterpret_cast<CUdeviceptr>(addr), value,
+                     CU_STREAM_WRITE_VALUE_DEFAULT);
+}
+uint64_t host_timeout_ns() { return env_timeout_ns(); }
+}  // namespace syn
 
 void syn::set_last_error(const std::string &msg) { g_err = msg; }
 

@@ -1,0 +1,883 @@
+// attn.cu -- fused ring attention forward (sequence parallelism) whose KV
+// loop walks the staged chunks in arrival order, and the C ABI of
+// include/syn_attn.h.
+//
+// Syncopate summary page, Experiments (paper §6.1: head-/sequence-parallel
+// attention and RingAttention) and method ¶2-¶4 (a tile waits only for the
+// chunks it reads; tiles follow the communication order).  One CTA computes
+// one 128-row query tile of one head on the tensor cores:
+//
+//   warp 0      TMA producer: the Q tile once, then for each KV block (128
+//               keys) in arrival order: wait for the block's chunk flags,
+//               load K and V into a two-slot ring
+//   warp 1      MMA issuer: S = Q.K^T into one of two TMEM score buffers,
+//               then O_j = P.V into one of two TMEM output buffers
+//   warps 4-7   softmax (one query row per thread, its TMEM lane): row max
+//               and exp2 of the scores, P (bf16) into shared memory for the
+//               P.V product, and the running output rescaled and summed in
+//               registers (acc = acc * exp2(m_old - m_new) + O_j)
+//
+// TMEM (512 columns): scores S0 S1 at 0 and 128, products O0 O1 at 256 and
+// 384, so Q.K^T of the next block and P.V of this one overlap the softmax.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "host_util.h"
+#include "protocol.h"
+#include "ptx.cuh"
+#include "syn.h"
+#include "syn_attn.h"
+
+namespace syn {
+namespace attn {
+
+constexpr int kD = 128;                      // head dimension
+constexpr int kBQ = 128;                     // query rows per CTA
+constexpr int kBK = 128;                     // keys per KV block
+constexpr int kTileBytes = 128 * 128 * 2;    // one 128 x 128 bf16 tile: two 64-wide boxes
+constexpr int kBoxBytes = kTileBytes / 2;    // 128 rows x 128 bytes, 128-byte swizzle
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + kTileBytes;    // 2 slots
+constexpr int OFF_V = OFF_K + 2 * kTileBytes;
+constexpr int OFF_P = OFF_V + 2 * kTileBytes;
+constexpr int OFF_BAR = OFF_P + kTileBytes;
+enum {
+    B_QF = 0,      // Q tile landed
+    B_QE = 1,      // Q tile read by the item's last Q.K^T
+    B_KF = 2,      // K slot s landed (2)
+    B_KE = 4,      // K slot s consumed by Q.K^T (2)
+    B_VF = 6,      // V slot s landed (2)
+    B_VE = 8,      // V slot s consumed by P.V (2)
+    B_SF = 10,     // score buffer s written (2)
+    B_SE = 12,     // score buffer s read by the softmax warps (2)
+    B_PF = 14,     // P written by the softmax warps
+    B_PE = 15,     // P consumed by P.V
+    B_OF = 16,     // product buffer s written (2)
+    B_OE = 18,     // product buffer s read (2)
+    B_DRAIN = 20,  // every MMA of the CTA completed
+    N_BAR = 21
+};
+constexpr int OFF_MISC = OFF_BAR + 8 * N_BAR;  // TMEM base, abort flag
+constexpr int SMEM_USED = OFF_MISC + 16;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;   // + the 1024-byte alignment of the tiles
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, 128, false);  // B = K tile, K-major
+constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, 128, true);   // B = V tile, MN-major
+constexpr int WHERE_FLAG = 1, WHERE_PIPE = 3;
+
+struct Params {
+    int32_t R, rank, S_r, H_q, G, causal, split, n_qtiles, n_items;
+    int32_t local_inplace, waits;
+    float scale_log2;  // scale * log2(e)
+    uint32_t epoch;
+    uint64_t timeout_ns;
+    const uint32_t *flags;  // [R * split]
+    uint16_t *out;          // [S_r, H_q, d]
+    float *lse;             // [S_r, H_q] or null
+    int32_t *err;           // {code, site, CTA, info}
+    // in-kernel staging (stage = 1): warps 2-3 of every CTA copy the other
+    // ranks' KV chunks into the gathered buffers in arrival order
+    int32_t stage, n_transfers, slices_per_transfer, drop_transfer;
+    int64_t row_bytes, slice_bytes;
+    const uint8_t *k_src[8], *v_src[8];
+    uint8_t *k_dst, *v_dst;
+    uint32_t *flags_w;      // the same flags, written by the stagers
+    uint32_t *cnt;          // [2][R * split] slice counters (epoch parity)
+};
+
+struct Maps {
+    CUtensorMap q, k, v;
+};
+
+__device__ __forceinline__ void raise(const Params &p, int code, int where, int info) {
+    if (atomicCAS(p.err, 0, code) == 0) {
+        p.err[1] = where;
+        p.err[2] = (int)blockIdx.x;
+        p.err[3] = info;
+    }
+}
+
+// Bounded wait on a shared-memory barrier phase; false on abort or timeout.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort, const Params &p) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    const uint64_t limit = p.timeout_ns * 4ull + 200000000ull;
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if ((n & 63u) == 0u) {
+            if (*reinterpret_cast<volatile int32_t *>(p.err) != 0) {
+                *abort = 1;
+                return false;
+            }
+            if (ptx::globaltimer() - t0 > limit) {
+                raise(p, SYN_ERR_TIMEOUT, WHERE_PIPE, (int)bar);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Wait used while draining on the way out: ignores the abort flag.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, const Params &p) {
+    const uint64_t t0 = ptx::globaltimer();
+    const uint64_t limit = p.timeout_ns * 4ull + 200000000ull;
+    for (uint32_t n = 0;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return;
+        if ((n & 63u) == 63u && ptx::globaltimer() - t0 > limit) {
+            raise(p, SYN_ERR_TIMEOUT, WHERE_PIPE, (int)bar);
+            return;
+        }
+    }
+}
+
+// Acquire-wait until chunk `code`'s flag carries this call's epoch.
+__device__ __forceinline__ bool wait_chunk(const Params &p, int code, volatile int *abort) {
+    const uint32_t *f = p.flags + code;
+    if (flag_ready(ptx::ld_acquire_gpu(f), p.epoch)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        __nanosleep(64);
+        if (flag_ready(ptx::ld_acquire_gpu(f), p.epoch)) return true;
+        if (*abort) return false;
+        if ((n & 15u) == 0u) {
+            if (*reinterpret_cast<volatile int32_t *>(p.err) != 0) {
+                *abort = 1;
+                return false;
+            }
+            if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                raise(p, SYN_ERR_TIMEOUT, WHERE_FLAG, code);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Source rank and chunk of staging transfer a (arrival order: the local shard
+// when it is not in place, then ranks r+1, r+2, ..., chunks ascending).
+__device__ __forceinline__ void transfer_of(const Params &p, int a, int &q, int &j) {
+    const int idx = a / p.split;
+    j = a - idx * p.split;
+    q = (p.rank + idx + (p.local_inplace ? 1 : 0)) % p.R;
+}
+
+// Stager warp `worker` of `n_workers`: slices worker, worker + n_workers, ...
+// of the transfer list, each a warp-wide copy of up to slice_bytes of a
+// chunk's K rows or V rows; the warp that completes a transfer's last slice
+// publishes its flag (release) once every slice's bytes are visible.
+__device__ void stage_kv(const Params &p, int worker, int n_workers, int lane) {
+    const int spt = p.slices_per_transfer, half = spt / 2;
+    const int nf = p.R * p.split;
+    uint32_t *cnt = p.cnt + (size_t)counter_half(p.epoch) * nf;
+    const int total = p.n_transfers * spt;
+    for (int g = worker; g < total; g += n_workers) {
+        const int a = g / spt, sl = g - a * spt;
+        int q, j;
+        transfer_of(p, a, q, j);
+        const int64_t lo = ((int64_t)j * p.S_r + p.split - 1) / p.split;
+        const int64_t hi = ((int64_t)(j + 1) * p.S_r + p.split - 1) / p.split;
+        const int64_t bytes = (hi - lo) * p.row_bytes;
+        const int64_t off = (int64_t)(sl % half) * p.slice_bytes;
+        const int64_t len = bytes - off < p.slice_bytes ? bytes - off : p.slice_bytes;
+        const uint8_t *src = (sl < half ? p.k_src[q] : p.v_src[q]) + lo * p.row_bytes + off;
+        uint8_t *dst = (sl < half ? p.k_dst : p.v_dst) + ((int64_t)q * p.S_r + lo) * p.row_bytes + off;
+        // 16-byte vectors, eight in flight per lane (4 KB per warp round)
+        for (int64_t b = (int64_t)lane * 16; b < len; b += 32 * 16 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (b + u * 512 < len) v[u] = __ldcs(reinterpret_cast<const uint4 *>(src + b + u * 512));
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (b + u * 512 < len) *reinterpret_cast<uint4 *>(dst + b + u * 512) = v[u];
+        }
+        __syncwarp();
+        if (lane == 0) {
+            ptx::fence_acq_rel_gpu();  // the warp's stores, observed through the barrier, before the count
+            const int code = q * p.split + j;
+            const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + code, 1u);
+            if (completes_transfer(old, (uint32_t)spt) && a != p.drop_transfer)
+                ptx::st_release_gpu(p.flags_w + code, p.epoch);
+        }
+        __syncwarp();
+    }
+}
+
+// The KV blocks a query tile visits, in chunk-arrival order: the shards of
+// ranks r, r+1, ..., r-1, each shard's blocks in ascending order.  Causal:
+// a block whose first key lies after the tile's last query is skipped (and
+// so are the shard's later blocks).
+struct KvIter {
+    int t, b, nb, last;
+    __device__ __forceinline__ void init(const Params &p, int q_row0) {
+        t = 0;
+        b = 0;
+        nb = p.S_r / kBK;
+        last = p.causal ? p.rank * p.S_r + q_row0 + kBQ - 1 : 0x7fffffff;
+    }
+    // first global key row of the next block, -1 past the end
+    __device__ __forceinline__ int next(const Params &p) {
+        while (t < p.R) {
+            const int q = (p.rank + t) % p.R;
+            if (b < nb) {
+                const int kv0 = q * p.S_r + b * kBK;
+                ++b;
+                if (kv0 <= last) return kv0;
+                b = nb;
+                continue;
+            }
+            ++t;
+            b = 0;
+        }
+        return -1;
+    }
+};
+
+// One step of a CTA's persistent walk: work item (query head, query tile)
+// item = blockIdx.x, + gridDim.x, ... (head-major, so concurrently running
+// CTAs share KV heads in L2), and the KV blocks of each item in order.
+struct Blk {
+    int h, q_row0, kv0;
+    bool first, last;
+};
+struct Walk {
+    int item, nxt;
+    bool fresh;  // the next block is its item's first
+    KvIter it;
+    __device__ __forceinline__ void start(const Params &p) {
+        fresh = true;
+        nxt = -1;
+        if (item < p.n_items) {
+            it.init(p, (item % p.n_qtiles) * kBQ);
+            nxt = it.next(p);
+        }
+    }
+    __device__ __forceinline__ void init(const Params &p) {
+        item = (int)blockIdx.x;
+        start(p);
+    }
+    __device__ __forceinline__ bool next(const Params &p, Blk &b) {
+        while (item < p.n_items && nxt < 0) {  // (every item has a block: its diagonal one)
+            item += (int)gridDim.x;
+            start(p);
+        }
+        if (item >= p.n_items) return false;
+        b.h = item / p.n_qtiles;
+        b.q_row0 = (item - b.h * p.n_qtiles) * kBQ;
+        b.kv0 = nxt;
+        b.first = fresh;
+        fresh = false;
+        nxt = it.next(p);
+        b.last = nxt < 0;
+        if (b.last) {
+            item += (int)gridDim.x;
+            start(p);
+        }
+        return true;
+    }
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Descriptors of a 128 x 128 bf16 tile held as two 64-wide, 128-byte-swizzled
+// boxes.  K-major (Q, K, P): 16-element slice kk lies in box kk/4, 32 bytes
+// per slice inside the swizzled row; 8-row atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+    return ptx::sdesc(tile + (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u, 16, 1024,
+                      ptx::kSwizzle128B);
+}
+// MN-major (V as the B operand: K = keys along rows, N = d across the two
+// boxes): slice kk is rows 16kk..16kk+15 (2048 bytes on), the boxes kBoxBytes apart.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
+    return ptx::sdesc(tile + (uint32_t)kk * 2048u, kBoxBytes, 1024, ptx::kSwizzle128B);
+}
+
+// acc = acc * a + O_g (the product of global block g), then free its buffer.
+__device__ __forceinline__ bool correct(float (&acc)[kD], float a, uint32_t g, uint32_t tl, uint32_t bar0,
+                                        volatile int *abort, const Params &p, int lane) {
+    const uint32_t s = g & 1u, ph = (g >> 1) & 1u;
+    const bool w = wait_bar(bar0 + 8 * (B_OF + s), ph, abort, p);
+    if (!__all_sync(0xffffffffu, w)) return false;
+    ptx::tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tl + 256u + s * 128u + (uint32_t)(c * 32), v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) acc[c * 32 + t] = fmaf(acc[c * 32 + t], a, __uint_as_float(v[t]));
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar0 + 8 * (B_OE + s));
+    return true;
+}
+
+// Normalised output row (bf16) and its log-sum-exp.
+__device__ __forceinline__ void store_row(const Params &p, const float (&acc)[kD], float m, float l, int h,
+                                          int q_row0, int row) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((int64_t)(q_row0 + row) * p.H_q + h) * kD);
+#pragma unroll
+    for (int k = 0; k < kD / 8; ++k) {
+        uint4 v;
+        v.x = pack_bf16(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
+        v.y = pack_bf16(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
+        v.z = pack_bf16(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
+        v.w = pack_bf16(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
+        dst[k] = v;
+    }
+    if (p.lse != nullptr)  // natural log: (m + log2 l) * ln 2, m in log2-scaled units
+        p.lse[(int64_t)(q_row0 + row) * p.H_q + h] = (m + log2f(l)) * 0.69314718055994531f;
+}
+
+__global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant__ Params p,
+                                                           const __grid_constant__ Maps m) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = ptx::smem_u32(sm);
+    const uint32_t bar0 = sbase + OFF_BAR;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
+    const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+
+    if (threadIdx.x == 0) {
+        *abort = 0;
+        ptx::mbar_init(bar(B_QF), 1);
+        ptx::mbar_init(bar(B_QE), 1);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(bar(B_KF + s), 1);
+            ptx::mbar_init(bar(B_KE + s), 1);
+            ptx::mbar_init(bar(B_VF + s), 1);
+            ptx::mbar_init(bar(B_VE + s), 1);
+            ptx::mbar_init(bar(B_SF + s), 1);
+            ptx::mbar_init(bar(B_SE + s), 4);  // one arrival per softmax warp
+            ptx::mbar_init(bar(B_OF + s), 1);
+            ptx::mbar_init(bar(B_OE + s), 4);
+        }
+        ptx::mbar_init(bar(B_PF), 4);
+        ptx::mbar_init(bar(B_PE), 1);
+        ptx::mbar_init(bar(B_DRAIN), 1);
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // CTA 0 clears the slice counters of the other epoch parity for the next call
+    if (p.stage && blockIdx.x == 0)
+        for (int i = (int)threadIdx.x; i < p.R * p.split; i += (int)blockDim.x)
+            p.cnt[(size_t)spare_half(p.epoch) * p.R * p.split + i] = 0u;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            const uint32_t sQ = sbase + OFF_Q, sK = sbase + OFF_K, sV = sbase + OFF_V;
+            Walk wk;
+            wk.init(p);
+            Blk b;
+            uint32_t g = 0, ic = 0, nk = 0, nv = 0;
+            for (; wk.next(p, b); ++g) {
+                const int hk = b.h / p.G;
+                // a new item: its Q tile replaces the previous one once that item's
+                // last Q.K^T has been issued and completed
+                if (b.first) {
+                    if (!wait_bar(bar(B_QE), (ic & 1u) ^ 1u, abort, p)) break;
+                    ptx::mbar_arrive_expect_tx(bar(B_QF), kTileBytes);
+                    ptx::tma_load_2d(sQ, &m.q, bar(B_QF), b.h * kD, b.q_row0);
+                    ptx::tma_load_2d(sQ + kBoxBytes, &m.q, bar(B_QF), b.h * kD + 64, b.q_row0);
+                    ++ic;
+                }
+                const int src = b.kv0 / p.S_r;
+                if (p.waits && !(p.local_inplace && src == p.rank)) {
+                    const int lr0 = b.kv0 - src * p.S_r;
+                    const int lo = (int)(((int64_t)lr0 * p.split) / p.S_r);
+                    const int hi = (int)(((int64_t)(lr0 + kBK - 1) * p.split) / p.S_r);
+                    bool ok = true;
+                    for (int c = lo; ok && c <= hi; ++c) ok = wait_chunk(p, src * p.split + c, abort);
+                    if (!ok) break;
+                    ptx::fence_proxy_async();  // generic acquire -> async-proxy (TMA) reads
+                }
+                const int s = (int)(g & 1u);
+                const uint32_t ph = (g >> 1) & 1u;
+                if (!wait_bar(bar(B_KE + s), ph ^ 1u, abort, p)) break;
+                ptx::mbar_arrive_expect_tx(bar(B_KF + s), kTileBytes);
+                ptx::tma_load_2d(sK + s * kTileBytes, &m.k, bar(B_KF + s), hk * kD, b.kv0);
+                ptx::tma_load_2d(sK + s * kTileBytes + kBoxBytes, &m.k, bar(B_KF + s), hk * kD + 64, b.kv0);
+                ++nk;
+                if (!wait_bar(bar(B_VE + s), ph ^ 1u, abort, p)) break;
+                ptx::mbar_arrive_expect_tx(bar(B_VF + s), kTileBytes);
+                ptx::tma_load_2d(sV + s * kTileBytes, &m.v, bar(B_VF + s), hk * kD, b.kv0);
+                ptx::tma_load_2d(sV + s * kTileBytes + kBoxBytes, &m.v, bar(B_VF + s), hk * kD + 64, b.kv0);
+                ++nv;
+            }
+            // every load issued must land before the CTA exits
+            if (ic > 0) drain_bar(bar(B_QF), (ic - 1u) & 1u, p);
+            for (uint32_t s = 0; s < 2; ++s) {
+                if (nk > s) drain_bar(bar(B_KF + (int)s), ((s + ((nk - 1u - s) / 2u) * 2u) >> 1) & 1u, p);
+                if (nv > s) drain_bar(bar(B_VF + (int)s), ((s + ((nv - 1u - s) / 2u) * 2u) >> 1) & 1u, p);
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            const uint32_t sQ = sbase + OFF_Q, sK = sbase + OFF_K, sV = sbase + OFF_V, sP = sbase + OFF_P;
+            auto pv = [&](uint32_t i) -> bool {
+                const int s = (int)(i & 1u);
+                const uint32_t ph = (i >> 1) & 1u;
+                if (!wait_bar(bar(B_PF), i & 1u, abort, p)) return false;
+                if (!wait_bar(bar(B_VF + s), ph, abort, p)) return false;
+                if (!wait_bar(bar(B_OE + s), ph ^ 1u, abort, p)) return false;
+                ptx::tc_fence_after();
+                const uint32_t d_o = tmem + 256u + (uint32_t)(s * 128);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    ptx::umma_bf16(d_o, kmajor_desc(sP, kk), mnmajor_desc(sV + s * kTileBytes, kk), IDESC_PV,
+                                   kk != 0 ? 1u : 0u);
+                ptx::umma_commit(bar(B_OF + s));
+                ptx::umma_commit(bar(B_VE + s));
+                ptx::umma_commit(bar(B_PE));
+                return true;
+            };
+            Walk wk;
+            wk.init(p);
+            Blk b;
+            uint32_t g = 0, ic = 0;
+            bool ok = true;
+            for (; wk.next(p, b); ++g) {
+                if (b.first) {
+                    if (!wait_bar(bar(B_QF), ic & 1u, abort, p)) {
+                        ok = false;
+                        break;
+                    }
+                    ++ic;
+                }
+                const int s = (int)(g & 1u);
+                const uint32_t ph = (g >> 1) & 1u;
+                if (!wait_bar(bar(B_KF + s), ph, abort, p) || !wait_bar(bar(B_SE + s), ph ^ 1u, abort, p)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_s = tmem + (uint32_t)(s * 128);
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    ptx::umma_bf16(d_s, kmajor_desc(sQ, kk), kmajor_desc(sK + s * kTileBytes, kk), IDESC_QK,
+                                   kk != 0 ? 1u : 0u);
+                ptx::umma_commit(bar(B_SF + s));
+                ptx::umma_commit(bar(B_KE + s));
+                if (b.last) ptx::umma_commit(bar(B_QE));  // the item's Q tile is no longer read
+                if (g > 0 && !pv(g - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (ok && g > 0) pv(g - 1);
+            // every MMA issued must complete before TMEM is released
+            ptx::umma_commit(bar(B_DRAIN));
+            drain_bar(bar(B_DRAIN), 0, p);
+        }
+    } else if (warp < 4) {
+        // ================= stagers =================
+        if (p.stage) stage_kv(p, (int)blockIdx.x * 2 + (warp - 2), (int)gridDim.x * 2, lane);
+    } else {
+        // ================= softmax, output rescaling, epilogue =================
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+        const uint32_t sP = sbase + OFF_P;
+        float acc[kD];
+#pragma unroll
+        for (int k = 0; k < kD; ++k) acc[k] = 0.f;
+        float mrow = -INFINITY, lrow = 0.f, a_pend = 0.f;
+        float m_fin = 0.f, l_fin = 0.f;  // the previous item's statistics, until its last correction
+        Blk prev = {0, 0, 0, false, false};
+        bool ok = true;
+        Walk wk;
+        wk.init(p);
+        Blk b;
+        uint32_t g = 0;
+        for (; wk.next(p, b); ++g) {
+            if (b.first) {
+                m_fin = mrow;
+                l_fin = lrow;
+                mrow = -INFINITY;
+                lrow = 0.f;
+            }
+            const int s = (int)(g & 1u);
+            const uint32_t ph = (g >> 1) & 1u;
+            bool w = wait_bar(bar(B_SF + s), ph, abort, p);
+            if (!__all_sync(0xffffffffu, w)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const int qpos0 = p.rank * p.S_r + b.q_row0;      // the tile's first query position
+            const int qpos = qpos0 + row;                     // this row's
+            const bool masked = p.causal && b.kv0 + kBK - 1 > qpos0;  // the block crosses the diagonal
+            const uint32_t ts = tl + (uint32_t)(s * 128);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(ts + (uint32_t)(c * 32), v);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    float x = __uint_as_float(v[t]) * p.scale_log2;
+                    if (masked && b.kv0 + c * 32 + t > qpos) x = -INFINITY;
+                    mx = fmaxf(mx, x);
+                }
+            }
+            const float m_new = fmaxf(mrow, mx);
+            const float base = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = ex2(mrow - base);
+            if (g > 0) {  // P.V of the previous block has read P
+                w = wait_bar(bar(B_PE), (g - 1u) & 1u, abort, p);
+                if (!__all_sync(0xffffffffu, w)) {
+                    ok = false;
+                    break;
+                }
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(ts + (uint32_t)(c * 32), v);
+                ptx::tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int t = 0; t < 32; t += 2) {
+                    float x0 = __uint_as_float(v[t]) * p.scale_log2;
+                    float x1 = __uint_as_float(v[t + 1]) * p.scale_log2;
+                    if (masked && b.kv0 + c * 32 + t > qpos) x0 = -INFINITY;
+                    if (masked && b.kv0 + c * 32 + t + 1 > qpos) x1 = -INFINITY;
+                    const float p0 = ex2(x0 - base), p1 = ex2(x1 - base);
+                    sum += p0 + p1;
+                    pk[t >> 1] = pack_bf16(p0, p1);
+                }
+                // keys c*32 .. c*32+31 of this row: box c/2, 16-byte chunks (c&1)*4 + u,
+                // XOR-swizzled by the row within its 8-row atom
+                const uint32_t rowbase = sP + (uint32_t)(c >> 1) * kBoxBytes + (uint32_t)row * 128u;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t chunk = (uint32_t)(((c & 1) * 4 + u) ^ (row & 7));
+                    ptx::st_shared_u4(rowbase + chunk * 16u, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::fence_proxy_async_smem();  // P's generic stores -> the MMA's async-proxy reads
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(bar(B_SE + s));
+                ptx::mbar_arrive(bar(B_PF));
+            }
+            lrow = lrow * alpha + sum;
+            mrow = m_new;
+            if (g > 0) {
+                if (!correct(acc, a_pend, g - 1u, tl, bar0, abort, p, lane)) {
+                    ok = false;
+                    break;
+                }
+                if (prev.last) {  // the previous item is complete
+                    store_row(p, acc, m_fin, l_fin, prev.h, prev.q_row0, row);
+#pragma unroll
+                    for (int k = 0; k < kD; ++k) acc[k] = 0.f;
+                }
+            }
+            a_pend = alpha;
+            prev = b;
+        }
+        if (ok && g > 0 && correct(acc, a_pend, g - 1u, tl, bar0, abort, p, lane))
+            store_row(p, acc, mrow, lrow, prev.h, prev.q_row0, row);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace attn
+}  // namespace syn
+
+using namespace syn;
+using namespace syn::attn;
+
+struct syn_attn_plan_s {
+    syn_attn_cfg_t cfg;
+    int device = 0, num_sms = 0;
+    int n_qtiles = 0, grid = 0;
+    uint32_t epoch = 0;
+    uint32_t *d_flags = nullptr;
+    uint32_t *d_cnt = nullptr;
+    int32_t *d_err = nullptr;
+    Maps maps;
+    std::vector<const void *> map_key;
+    int64_t row_bytes = 0;  // H_kv * d * 2
+};
+
+namespace {
+
+void free_attn(syn_attn_plan_s *pl) {
+    if (pl == nullptr) return;
+    cudaFree(pl->d_flags);
+    cudaFree(pl->d_cnt);
+    cudaFree(pl->d_err);
+    delete pl;
+}
+
+bool al16(const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; }
+
+
+}  // namespace
+
+#define ATT_CK(call)                                                                                  \
+    do {                                                                                              \
+        cudaError_t e__ = (call);                                                                     \
+        if (e__ != cudaSuccess) return host_fail(SYN_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e__)); \
+    } while (0)
+
+extern "C" {
+
+int syn_attn_cfg_default(syn_attn_cfg_t *c) {
+    if (c == nullptr) return host_fail(SYN_ERR_INVALID, "null cfg");
+    std::memset(c, 0, sizeof(*c));
+    c->R = 1;
+    c->S_r = 128;
+    c->H_q = c->H_kv = 1;
+    c->d = 128;
+    c->split = 1;
+    c->backend = SYN_BACKEND_TMA_COLOCATED;
+    c->debug_drop_chunk = -1;
+    return SYN_OK;
+}
+
+int syn_attn_plan_create(syn_attn_plan_t *out, const syn_attn_cfg_t *cfg) {
+    if (out == nullptr || cfg == nullptr) return host_fail(SYN_ERR_INVALID, "null argument");
+    *out = nullptr;
+    syn_attn_cfg_t c = *cfg;
+    if (c.split == 0) c.split = 1;
+    if (c.R < 1 || c.rank < 0 || c.rank >= c.R) return host_fail(SYN_ERR_INVALID, "need 0 <= rank < R");
+    if (c.R > 8) return host_fail(SYN_ERR_UNSUPPORTED, "R > 8");
+    if (c.d != kD) return host_fail(SYN_ERR_UNSUPPORTED, "head dimension must be 128");
+    if (c.S_r < kBQ || c.S_r % kBQ != 0) return host_fail(SYN_ERR_UNSUPPORTED, "S_r must be a positive multiple of 128");
+    if (c.S_r > (1 << 20)) return host_fail(SYN_ERR_UNSUPPORTED, "S_r > 2^20");
+    if (c.H_q < 1 || c.H_kv < 1 || c.H_q % c.H_kv != 0) return host_fail(SYN_ERR_INVALID, "need H_q % H_kv == 0");
+    if (c.H_q > 1024) return host_fail(SYN_ERR_UNSUPPORTED, "H_q > 1024");
+    if (c.causal != 0 && c.causal != 1) return host_fail(SYN_ERR_INVALID, "causal must be 0 or 1");
+    if (c.split < 1 || c.split > 64 || c.split > c.S_r / kBK)
+        return host_fail(SYN_ERR_INVALID, "split must be in [1, min(64, S_r/128)]");
+    if (c.backend != SYN_BACKEND_TMA_COLOCATED && c.backend != SYN_BACKEND_UNFUSED)
+        return host_fail(SYN_ERR_UNSUPPORTED,
+                         "ring attention stages with SYN_BACKEND_TMA_COLOCATED or SYN_BACKEND_UNFUSED");
+    if (!(c.scale >= 0.f) || !std::isfinite(c.scale)) return host_fail(SYN_ERR_INVALID, "bad scale");
+    int rc = host_load_driver();
+    if (rc != SYN_OK) return rc;
+    syn_attn_plan_s *pl = new syn_attn_plan_s();
+    pl->cfg = c;
+    if (pl->cfg.scale == 0.f) pl->cfg.scale = 1.f / std::sqrt((float)kD);
+    if (pl->cfg.timeout_ns == 0) pl->cfg.timeout_ns = host_timeout_ns();
+    pl->n_qtiles = (int)(c.S_r / kBQ);
+    pl->row_bytes = (int64_t)c.H_kv * kD * 2;
+    auto bail = [&](int code, const std::string &msg) {
+        free_attn(pl);
+        return host_fail(code, msg);
+    };
+#define PL_CK(call)                                                                                 \
+    do {                                                                                            \
+        cudaError_t e__ = (call);                                                                   \
+        if (e__ != cudaSuccess) return bail(SYN_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e__)); \
+    } while (0)
+    PL_CK(cudaGetDevice(&pl->device));
+    PL_CK(cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->device));
+    PL_CK(cudaFuncSetAttribute(ring_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+    int per_sm = 0;
+    PL_CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ring_attn_kernel, 256, SMEM_BYTES));
+    if (per_sm < 1) return bail(SYN_ERR_UNSUPPORTED, "the attention kernel cannot be resident");
+    // persistent: one CTA per SM (all co-resident: a cooperative launch), at
+    // most one per work item
+    pl->grid = std::min(pl->n_qtiles * c.H_q, pl->num_sms * per_sm);
+    const size_t nf = (size_t)c.R * c.split;
+    PL_CK(cudaMalloc(&pl->d_flags, nf * sizeof(uint32_t)));
+    PL_CK(cudaMemset(pl->d_flags, 0, nf * sizeof(uint32_t)));
+    PL_CK(cudaMalloc(&pl->d_cnt, 2 * nf * sizeof(uint32_t)));
+    PL_CK(cudaMemset(pl->d_cnt, 0, 2 * nf * sizeof(uint32_t)));
+    PL_CK(cudaMalloc(&pl->d_err, 4 * sizeof(int32_t)));
+    PL_CK(cudaMemset(pl->d_err, 0, 4 * sizeof(int32_t)));
+    PL_CK(cudaDeviceSynchronize());
+#undef PL_CK
+    *out = pl;
+    return SYN_OK;
+}
+
+int syn_attn_plan_destroy(syn_attn_plan_t plan) {
+    free_attn(plan);
+    return SYN_OK;
+}
+
+int syn_ring_attention(syn_attn_plan_t pl, const void *Q, const void *const *K_shards,
+                       const void *const *V_shards, void *K_gathered, void *V_gathered, void *O, float *lse,
+                       void *stream) {
+    if (pl == nullptr) return host_fail(SYN_ERR_INVALID, "null plan");
+    const syn_attn_cfg_t &c = pl->cfg;
+    if (Q == nullptr || K_shards == nullptr || V_shards == nullptr || K_gathered == nullptr ||
+        V_gathered == nullptr || O == nullptr)
+        return host_fail(SYN_ERR_INVALID, "null operand");
+    if (!al16(Q) || !al16(K_gathered) || !al16(V_gathered) || !al16(O) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+        return host_fail(SYN_ERR_INVALID, "operand not 16-byte aligned");
+    for (int q = 0; q < c.R; ++q)
+        if (K_shards[q] == nullptr || V_shards[q] == nullptr || !al16(K_shards[q]) || !al16(V_shards[q]))
+            return host_fail(SYN_ERR_INVALID, "shard pointer null or not 16-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t shard_bytes = c.S_r * pl->row_bytes;
+    uint8_t *kg = static_cast<uint8_t *>(K_gathered), *vg = static_cast<uint8_t *>(V_gathered);
+    const bool inplace = K_shards[c.rank] == kg + c.rank * shard_bytes && V_shards[c.rank] == vg + c.rank * shard_bytes;
+    std::vector<const void *> key = {Q, K_gathered, V_gathered};
+    if (key != pl->map_key) {
+        int rc;
+        if ((rc = host_encode_2d(&pl->maps.q, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)c.H_q * kD,
+                                 (uint64_t)c.S_r, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != SYN_OK ||
+            (rc = host_encode_2d(&pl->maps.k, K_gathered, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 (uint64_t)c.H_kv * kD, (uint64_t)c.R * c.S_r, 64, 128,
+                                 CU_TENSOR_MAP_SWIZZLE_128B)) != SYN_OK ||
+            (rc = host_encode_2d(&pl->maps.v, V_gathered, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 (uint64_t)c.H_kv * kD, (uint64_t)c.R * c.S_r, 64, 128,
+                                 CU_TENSOR_MAP_SWIZZLE_128B)) != SYN_OK)
+            return rc;
+        pl->map_key = key;
+    }
+    pl->epoch += 1;
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.R = c.R;
+    p.rank = c.rank;
+    p.S_r = (int32_t)c.S_r;
+    p.H_q = c.H_q;
+    p.G = c.H_q / c.H_kv;
+    p.causal = c.causal;
+    p.split = c.split;
+    p.n_qtiles = pl->n_qtiles;
+    p.n_items = pl->n_qtiles * c.H_q;
+    p.local_inplace = inplace ? 1 : 0;
+    p.scale_log2 = c.scale * 1.4426950408889634f;
+    p.epoch = pl->epoch;
+    p.timeout_ns = c.timeout_ns;
+    p.flags = pl->d_flags;
+    p.flags_w = pl->d_flags;
+    p.cnt = pl->d_cnt;
+    p.out = static_cast<uint16_t *>(O);
+    p.lse = lse;
+    p.err = pl->d_err;
+    p.row_bytes = pl->row_bytes;
+    p.n_transfers = (c.R - (inplace ? 1 : 0)) * c.split;
+    p.drop_transfer = c.debug_drop_chunk;
+    const int64_t max_chunk_bytes = ((c.S_r + c.split - 1) / c.split) * pl->row_bytes;
+    p.slice_bytes = std::min<int64_t>(64 * 1024, max_chunk_bytes);
+    p.slices_per_transfer = 2 * (int32_t)((max_chunk_bytes + p.slice_bytes - 1) / p.slice_bytes);
+    for (int q = 0; q < c.R; ++q) {
+        p.k_src[q] = static_cast<const uint8_t *>(K_shards[q]);
+        p.v_src[q] = static_cast<const uint8_t *>(V_shards[q]);
+    }
+    p.k_dst = kg;
+    p.v_dst = vg;
+    cudaLaunchConfig_t lc;
+    std::memset(&lc, 0, sizeof(lc));
+    lc.gridDim = dim3((unsigned)pl->grid, 1, 1);
+    lc.blockDim = dim3(256, 1, 1);
+    lc.dynamicSmemBytes = SMEM_BYTES;
+    lc.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: stagers and waiters coexist
+    attr[0].val.cooperative = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (c.backend == SYN_BACKEND_TMA_COLOCATED) {
+        p.stage = 1;
+        p.waits = 1;
+    } else {  // unfused: every copy first (in stream order), then the kernel without waits
+        for (int t = 0; t < c.R; ++t) {
+            const int q = (c.rank + t) % c.R;
+            if (q == c.rank && inplace) continue;
+            ATT_CK(cudaMemcpyAsync(kg + (int64_t)q * shard_bytes, K_shards[q], (size_t)shard_bytes,
+                                   cudaMemcpyDeviceToDevice, st));
+            ATT_CK(cudaMemcpyAsync(vg + (int64_t)q * shard_bytes, V_shards[q], (size_t)shard_bytes,
+                                   cudaMemcpyDeviceToDevice, st));
+        }
+        p.stage = 0;
+        p.waits = 0;
+    }
+    ATT_CK(cudaLaunchKernelEx(&lc, ring_attn_kernel, p, pl->maps));
+    return SYN_OK;
+}
+
+int syn_attn_sync_status(syn_attn_plan_t pl, void *stream) {
+    if (pl == nullptr) return host_fail(SYN_ERR_INVALID, "null plan");
+    ATT_CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+    int32_t e[4] = {0, 0, 0, 0};
+    ATT_CK(cudaMemcpy(e, pl->d_err, sizeof(e), cudaMemcpyDeviceToHost));
+    if (e[0] == 0) return SYN_OK;
+    ATT_CK(cudaMemset(pl->d_err, 0, 4 * sizeof(int32_t)));
+    ATT_CK(cudaMemset(pl->d_flags, 0, (size_t)pl->cfg.R * pl->cfg.split * sizeof(uint32_t)));
+    ATT_CK(cudaMemset(pl->d_cnt, 0, 2 * (size_t)pl->cfg.R * pl->cfg.split * sizeof(uint32_t)));
+    ATT_CK(cudaDeviceSynchronize());
+    return host_fail(e[0], std::string("device error ") + syn_status_string(e[0]) + " at site " +
+                               std::to_string(e[1]) + " in CTA " + std::to_string(e[2]) + " (info " +
+                               std::to_string(e[3]) + ")");
+}
+
+int syn_attn_plan_query(syn_attn_plan_t pl, syn_attn_info_t *info) {
+    if (pl == nullptr || info == nullptr) return host_fail(SYN_ERR_INVALID, "null argument");
+    std::memset(info, 0, sizeof(*info));
+    const syn_attn_cfg_t &c = pl->cfg;
+    info->R = c.R;
+    info->rank = c.rank;
+    info->H_q = c.H_q;
+    info->H_kv = c.H_kv;
+    info->d = c.d;
+    info->causal = c.causal;
+    info->split = c.split;
+    info->backend = c.backend;
+    info->S_r = c.S_r;
+    info->n_qtiles = pl->n_qtiles;
+    info->grid = pl->grid;
+    info->n_transfers = (c.R - 1) * c.split;  // with the local shard in place
+    info->smem_bytes = SMEM_BYTES;
+    info->epoch = pl->epoch;
+    return SYN_OK;
+}
+
+int syn_attn_plan_flags(syn_attn_plan_t pl, uint32_t *flags) {
+    if (pl == nullptr || flags == nullptr) return host_fail(SYN_ERR_INVALID, "null argument");
+    ATT_CK(cudaDeviceSynchronize());
+    ATT_CK(cudaMemcpy(flags, pl->d_flags, (size_t)pl->cfg.R * pl->cfg.split * sizeof(uint32_t),
+                      cudaMemcpyDeviceToHost));
+    return SYN_OK;
+}
+
+}  // extern "C"

@@ -161,3 +161,51 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns to float32 (via PyTorch)."""
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
     return t.to(torch.float32).numpy()
+
+
+# --------------------------------------------------------------------------- ring attention
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Sequence-parallel attention: R ranks of S_r tokens each, H_q query
+    heads over H_kv KV heads, head dimension d."""
+    name: str
+    R: int
+    S_r: int
+    H_q: int
+    H_kv: int
+    d: int = 128
+    causal: bool = False
+
+    @property
+    def flops(self) -> float:
+        """Tensor-core FLOPs of one rank's forward (Q.K^T and P.V)."""
+        keys = self.R * self.S_r
+        full = 4.0 * self.S_r * keys * self.d * self.H_q
+        if not self.causal:
+            return full
+        # keys up to each query's position: sum over the rank-r rows (taken at the last rank)
+        r = self.R - 1
+        visible = sum(r * self.S_r + i + 1 for i in range(self.S_r))
+        return 4.0 * visible * self.d * self.H_q
+
+
+# Llama-3-8B attention (32 query heads, 8 KV heads, d 128) over a 32K-token
+# context split across 8 ranks (4096 tokens each): the long-context ring
+# attention shape of the pages' attention workloads.
+LLAMA3_8B_RING_ATTN = AttnWorkload("llama3-8b-ring-attn-sp8-S32768-Hq32-Hkv8-d128", 8, 4096, 32, 8)
+LLAMA3_8B_RING_ATTN_CAUSAL = AttnWorkload("llama3-8b-ring-attn-causal-sp8-S32768-Hq32-Hkv8-d128", 8, 4096, 32, 8,
+                                          causal=True)
+TINY_RING_ATTN = AttnWorkload("tiny-ring-attn-R4-S256-Hq4-Hkv2", 4, 256, 4, 2)
+
+
+def make_attn_inputs(w: AttnWorkload, seed: int = 0):
+    """Q (rank-independent draw: every rank's queries come from the same
+    stream, the rank picks nothing), then K_q and V_q for q = 0..R-1, all
+    N(0,1) bf16 token-major.  Returns (Q [S_r, H_q, d], Ks, Vs) as uint16."""
+    rng = np.random.default_rng(seed)
+    Q = to_bf16_bits(_draw(rng, (w.S_r, w.H_q, w.d), 1.0, "normal"))
+    Ks, Vs = [], []
+    for _ in range(w.R):
+        Ks.append(to_bf16_bits(_draw(rng, (w.S_r, w.H_kv, w.d), 1.0, "normal")))
+        Vs.append(to_bf16_bits(_draw(rng, (w.S_r, w.H_kv, w.d), 1.0, "normal")))
+    return Q, Ks, Vs

@@ -63,3 +63,18 @@ def test_protocol_emulation_library_exports_its_header():
     assert names == ["syn_proto_emulate", "syn_proto_last_error"]
     lib = proto.lib()
     assert all(hasattr(lib, n) for n in names)
+
+
+def test_attention_library_exports_its_header():
+    from chunk_scheduled_communication_gb300 import attn
+    src = open(os.path.join(ROOT, "include", "syn_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = sorted(set(re.findall(r"\b(syn_[a-z0-9_]+)\s*\(", src)))
+    lib = ctypes.CDLL(syn.LIB_PATH)
+    assert names and not [n for n in names if not hasattr(lib, n)]
+    assert set(names) == set(attn.SIGS)
+    L = attn.lib()
+    assert L.syn_attn_plan_destroy(None) == 0
+    assert L.syn_attn_sync_status(None, None) == syn.ERR_INVALID
+    c = attn.make_cfg()
+    assert c.d == 128 and c.split == 1 and c.debug_drop_chunk == -1
