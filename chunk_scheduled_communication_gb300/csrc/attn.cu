@@ -11,14 +11,19 @@
 //               keys) in arrival order: wait for the block's chunk flags,
 //               load K and V into a two-slot ring
 //   warp 1      MMA issuer: S = Q.K^T into one of two TMEM score buffers,
-//               then O_j = P.V into one of two TMEM output buffers
+//               then O += P.V into the TMEM output accumulator
+//   warps 2-3   staging: copy the other ranks' KV chunks, publish flags
 //   warps 4-7   softmax (one query row per thread, its TMEM lane): row max
 //               and exp2 of the scores, P (bf16) into shared memory for the
-//               P.V product, and the running output rescaled and summed in
-//               registers (acc = acc * exp2(m_old - m_new) + O_j)
+//               P.V product; at the end of a work item the output row is
+//               read from TMEM, normalised and stored
 //
-// TMEM (512 columns): scores S0 S1 at 0 and 128, products O0 O1 at 256 and
-// 384, so Q.K^T of the next block and P.V of this one overlap the softmax.
+// TMEM (512 columns allocated): scores S0 S1 at 0 and 128, the output
+// accumulator at 256.  Q.K^T of the next block overlaps the softmax of this
+// one.  The exponentials use a running reference max m that may lag the
+// row's true max by up to 8 (log2 units, so every p <= 2^8): only when a
+// block raises the max by more than that is the TMEM accumulator (and the
+// running sum) rescaled by exp2(m_old - m_new), between two P.V products.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -59,10 +64,9 @@ enum {
     B_SE = 12,     // score buffer s read by the softmax warps (2)
     B_PF = 14,     // P written by the softmax warps
     B_PE = 15,     // P consumed by P.V
-    B_OF = 16,     // product buffer s written (2)
-    B_OE = 18,     // product buffer s read (2)
-    B_DRAIN = 20,  // every MMA of the CTA completed
-    N_BAR = 21
+    B_OE = 16,     // the output accumulator read out after an item's last P.V
+    B_DRAIN = 17,  // every MMA of the CTA completed
+    N_BAR = 18
 };
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BAR;  // TMEM base, abort flag
 constexpr int SMEM_USED = OFF_MISC + 16;
@@ -310,40 +314,28 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
     return ptx::sdesc(tile + (uint32_t)kk * 2048u, kBoxBytes, 1024, ptx::kSwizzle128B);
 }
 
-// acc = acc * a + O_g (the product of global block g), then free its buffer.
-__device__ __forceinline__ bool correct(float (&acc)[kD], float a, uint32_t g, uint32_t tl, uint32_t bar0,
-                                        volatile int *abort, const Params &p, int lane) {
-    const uint32_t s = g & 1u, ph = (g >> 1) & 1u;
-    const bool w = wait_bar(bar0 + 8 * (B_OF + s), ph, abort, p);
-    if (!__all_sync(0xffffffffu, w)) return false;
-    ptx::tc_fence_after();
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(tl + 256u + s * 128u + (uint32_t)(c * 32), v);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int t = 0; t < 32; ++t) acc[c * 32 + t] = fmaf(acc[c * 32 + t], a, __uint_as_float(v[t]));
-    }
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(bar0 + 8 * (B_OE + s));
-    return true;
-}
+constexpr float kRescale = 8.f;  // how far (log2 units) the reference max may lag
 
-// Normalised output row (bf16) and its log-sum-exp.
-__device__ __forceinline__ void store_row(const Params &p, const float (&acc)[kD], float m, float l, int h,
-                                          int q_row0, int row) {
+// The finished output row: read from TMEM, normalised, stored as bf16 (and
+// its log-sum-exp).
+__device__ __forceinline__ void store_row(const Params &p, uint32_t to, float m, float l, int h, int q_row0,
+                                          int row) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
     uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((int64_t)(q_row0 + row) * p.H_q + h) * kD);
 #pragma unroll
-    for (int k = 0; k < kD / 8; ++k) {
-        uint4 v;
-        v.x = pack_bf16(acc[8 * k + 0] * inv, acc[8 * k + 1] * inv);
-        v.y = pack_bf16(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
-        v.z = pack_bf16(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
-        v.w = pack_bf16(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
-        dst[k] = v;
+    for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(to + (uint32_t)(c * 32), v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint4 o;
+            o.x = pack_bf16(__uint_as_float(v[8 * k + 0]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
+            o.y = pack_bf16(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
+            o.z = pack_bf16(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
+            o.w = pack_bf16(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
+            dst[c * 4 + k] = o;
+        }
     }
     if (p.lse != nullptr)  // natural log: (m + log2 l) * ln 2, m in log2-scaled units
         p.lse[(int64_t)(q_row0 + row) * p.H_q + h] = (m + log2f(l)) * 0.69314718055994531f;
@@ -371,9 +363,8 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
             ptx::mbar_init(bar(B_VE + s), 1);
             ptx::mbar_init(bar(B_SF + s), 1);
             ptx::mbar_init(bar(B_SE + s), 4);  // one arrival per softmax warp
-            ptx::mbar_init(bar(B_OF + s), 1);
-            ptx::mbar_init(bar(B_OE + s), 4);
         }
+        ptx::mbar_init(bar(B_OE), 4);  // the output accumulator read out (one arrival per softmax warp)
         ptx::mbar_init(bar(B_PF), 4);
         ptx::mbar_init(bar(B_PE), 1);
         ptx::mbar_init(bar(B_DRAIN), 1);
@@ -446,28 +437,28 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
         // ================= MMA issuer =================
         if (lane == 0) {
             const uint32_t sQ = sbase + OFF_Q, sK = sbase + OFF_K, sV = sbase + OFF_V, sP = sbase + OFF_P;
-            auto pv = [&](uint32_t i) -> bool {
+            const uint32_t d_o = tmem + 256u;
+            // O (+)= P_i . V_i; an item's first product overwrites O once the
+            // softmax warps have read out the previous item (its `item`-th)
+            auto pv = [&](uint32_t i, bool first, uint32_t item) -> bool {
                 const int s = (int)(i & 1u);
-                const uint32_t ph = (i >> 1) & 1u;
                 if (!wait_bar(bar(B_PF), i & 1u, abort, p)) return false;
-                if (!wait_bar(bar(B_VF + s), ph, abort, p)) return false;
-                if (!wait_bar(bar(B_OE + s), ph ^ 1u, abort, p)) return false;
+                if (!wait_bar(bar(B_VF + s), (i >> 1) & 1u, abort, p)) return false;
+                if (first && item > 0 && !wait_bar(bar(B_OE), (item - 1u) & 1u, abort, p)) return false;
                 ptx::tc_fence_after();
-                const uint32_t d_o = tmem + 256u + (uint32_t)(s * 128);
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk)
                     ptx::umma_bf16(d_o, kmajor_desc(sP, kk), mnmajor_desc(sV + s * kTileBytes, kk), IDESC_PV,
-                                   kk != 0 ? 1u : 0u);
-                ptx::umma_commit(bar(B_OF + s));
+                                   (kk != 0 || !first) ? 1u : 0u);
                 ptx::umma_commit(bar(B_VE + s));
-                ptx::umma_commit(bar(B_PE));
+                ptx::umma_commit(bar(B_PE));  // P read and O updated
                 return true;
             };
             Walk wk;
             wk.init(p);
             Blk b;
             uint32_t g = 0, ic = 0;
-            bool ok = true;
+            bool ok = true, prev_first = false;
             for (; wk.next(p, b); ++g) {
                 if (b.first) {
                     if (!wait_bar(bar(B_QF), ic & 1u, abort, p)) {
@@ -491,12 +482,14 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
                 ptx::umma_commit(bar(B_SF + s));
                 ptx::umma_commit(bar(B_KE + s));
                 if (b.last) ptx::umma_commit(bar(B_QE));  // the item's Q tile is no longer read
-                if (g > 0 && !pv(g - 1)) {
+                // the previous block's product (its item started `ic - 1` or `ic - 2` items in)
+                if (g > 0 && !pv(g - 1u, prev_first, b.first ? ic - 2u : ic - 1u)) {
                     ok = false;
                     break;
                 }
+                prev_first = b.first;
             }
-            if (ok && g > 0) pv(g - 1);
+            if (ok && g > 0) pv(g - 1u, prev_first, ic - 1u);
             // every MMA issued must complete before TMEM is released
             ptx::umma_commit(bar(B_DRAIN));
             drain_bar(bar(B_DRAIN), 0, p);
@@ -509,74 +502,78 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+        const uint32_t to = tl + 256u;  // this warp's lanes of the output accumulator
         const uint32_t sP = sbase + OFF_P;
-        float acc[kD];
-#pragma unroll
-        for (int k = 0; k < kD; ++k) acc[k] = 0.f;
-        float mrow = -INFINITY, lrow = 0.f, a_pend = 0.f;
-        float m_fin = 0.f, l_fin = 0.f;  // the previous item's statistics, until its last correction
-        Blk prev = {0, 0, 0, false, false};
-        bool ok = true;
+        float mref = -INFINITY, lrow = 0.f;  // reference max (log2-scaled units), running sum
         Walk wk;
         wk.init(p);
         Blk b;
-        uint32_t g = 0;
-        for (; wk.next(p, b); ++g) {
+        for (uint32_t g = 0; wk.next(p, b); ++g) {
             if (b.first) {
-                m_fin = mrow;
-                l_fin = lrow;
-                mrow = -INFINITY;
+                mref = -INFINITY;
                 lrow = 0.f;
             }
             const int s = (int)(g & 1u);
-            const uint32_t ph = (g >> 1) & 1u;
-            bool w = wait_bar(bar(B_SF + s), ph, abort, p);
-            if (!__all_sync(0xffffffffu, w)) {
-                ok = false;
-                break;
-            }
+            bool w = wait_bar(bar(B_SF + s), (g >> 1) & 1u, abort, p);
+            if (!__all_sync(0xffffffffu, w)) break;
             ptx::tc_fence_after();
-            const int qpos0 = p.rank * p.S_r + b.q_row0;      // the tile's first query position
-            const int qpos = qpos0 + row;                     // this row's
+            const int qpos0 = p.rank * p.S_r + b.q_row0;              // the tile's first query position
+            const int qpos = qpos0 + row;                             // this row's
             const bool masked = p.causal && b.kv0 + kBK - 1 > qpos0;  // the block crosses the diagonal
             const uint32_t ts = tl + (uint32_t)(s * 128);
-            float mx = -INFINITY;
+            uint32_t v[kBK];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(ts + (uint32_t)(c * 32), v);
-                ptx::tmem_ld_wait();
+                uint32_t (&vc)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c);
+                ptx::tmem_ld_32x32b_x32(ts + (uint32_t)(c * 32), vc);
+            }
+            ptx::tmem_ld_wait();
+            if (masked) {
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    float x = __uint_as_float(v[t]) * p.scale_log2;
-                    if (masked && b.kv0 + c * 32 + t > qpos) x = -INFINITY;
-                    mx = fmaxf(mx, x);
-                }
+                for (int t = 0; t < kBK; ++t)
+                    if (b.kv0 + t > qpos) v[t] = __float_as_uint(-INFINITY);
             }
-            const float m_new = fmaxf(mrow, mx);
-            const float base = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = ex2(mrow - base);
-            if (g > 0) {  // P.V of the previous block has read P
+            float mx = -INFINITY;
+#pragma unroll
+            for (int t = 0; t < kBK; ++t) mx = fmaxf(mx, __uint_as_float(v[t]));
+            const float mcand = mx * p.scale_log2;  // (scale > 0: the max commutes with it)
+            // P.V of the previous block must be done: it read P, and O may be rescaled
+            if (g > 0) {
                 w = wait_bar(bar(B_PE), (g - 1u) & 1u, abort, p);
-                if (!__all_sync(0xffffffffu, w)) {
-                    ok = false;
-                    break;
+                if (!__all_sync(0xffffffffu, w)) break;
+                ptx::tc_fence_after();
+            }
+            if (b.first) {
+                mref = mcand;
+            } else {
+                const bool need = mcand > mref + kRescale;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? ex2(mref - mcand) : 1.f;
+                    if (need) {
+                        lrow *= alpha;
+                        mref = mcand;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        ptx::tmem_ld_32x32b_x32(to + (uint32_t)(c * 32), o);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                        ptx::tmem_st_32x32b_x32(to + (uint32_t)(c * 32), o);
+                    }
+                    ptx::tmem_st_wait();
                 }
             }
+            const float base = mref == -INFINITY ? 0.f : mref;
             float sum = 0.f;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(ts + (uint32_t)(c * 32), v);
-                ptx::tmem_ld_wait();
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 32; t += 2) {
-                    float x0 = __uint_as_float(v[t]) * p.scale_log2;
-                    float x1 = __uint_as_float(v[t + 1]) * p.scale_log2;
-                    if (masked && b.kv0 + c * 32 + t > qpos) x0 = -INFINITY;
-                    if (masked && b.kv0 + c * 32 + t + 1 > qpos) x1 = -INFINITY;
-                    const float p0 = ex2(x0 - base), p1 = ex2(x1 - base);
+                    const float p0 = ex2(fmaf(__uint_as_float(v[c * 32 + t]), p.scale_log2, -base));
+                    const float p1 = ex2(fmaf(__uint_as_float(v[c * 32 + t + 1]), p.scale_log2, -base));
                     sum += p0 + p1;
                     pk[t >> 1] = pack_bf16(p0, p1);
                 }
@@ -589,6 +586,7 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
                     ptx::st_shared_u4(rowbase + chunk * 16u, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                 }
             }
+            lrow += sum;
             ptx::tc_fence_before();
             ptx::fence_proxy_async_smem();  // P's generic stores -> the MMA's async-proxy reads
             __syncwarp();
@@ -596,24 +594,16 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
                 ptx::mbar_arrive(bar(B_SE + s));
                 ptx::mbar_arrive(bar(B_PF));
             }
-            lrow = lrow * alpha + sum;
-            mrow = m_new;
-            if (g > 0) {
-                if (!correct(acc, a_pend, g - 1u, tl, bar0, abort, p, lane)) {
-                    ok = false;
-                    break;
-                }
-                if (prev.last) {  // the previous item is complete
-                    store_row(p, acc, m_fin, l_fin, prev.h, prev.q_row0, row);
-#pragma unroll
-                    for (int k = 0; k < kD; ++k) acc[k] = 0.f;
-                }
+            if (b.last) {  // the item's output: after its last P.V, read O out of TMEM
+                w = wait_bar(bar(B_PE), g & 1u, abort, p);
+                if (!__all_sync(0xffffffffu, w)) break;
+                ptx::tc_fence_after();
+                store_row(p, to, mref, lrow, b.h, b.q_row0, row);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(B_OE));
             }
-            a_pend = alpha;
-            prev = b;
         }
-        if (ok && g > 0 && correct(acc, a_pend, g - 1u, tl, bar0, abort, p, lane))
-            store_row(p, acc, mrow, lrow, prev.h, prev.q_row0, row);
     }
     ptx::tc_fence_before();
     __syncthreads();
