@@ -11,19 +11,24 @@
 //               keys) in arrival order: wait for the block's chunk flags,
 //               load K and V into a two-slot ring
 //   warp 1      MMA issuer: S = Q.K^T into one of two TMEM score buffers,
-//               then O += P.V into the TMEM output accumulator
+//               then O_A += P_A.V_A and O_B += P_B.V_B
 //   warps 2-3   staging: copy the other ranks' KV chunks, publish flags
-//   warps 4-7   softmax (one query row per thread, its TMEM lane): row max
-//               and exp2 of the scores, P (bf16) into shared memory for the
-//               P.V product; at the end of a work item the output row is
-//               read from TMEM, normalised and stored
+//   warps 4-7   softmax half A (one query row per thread, its TMEM lane):
+//               keys 0-63 of every block
+//   warps 8-11  softmax half B: keys 64-127
 //
-// TMEM (512 columns allocated): scores S0 S1 at 0 and 128, the output
-// accumulator at 256.  Q.K^T of the next block overlaps the softmax of this
-// one.  The exponentials use a running reference max m that may lag the
-// row's true max by up to 8 (log2 units, so every p <= 2^8): only when a
-// block raises the max by more than that is the TMEM accumulator (and the
-// running sum) rescaled by exp2(m_old - m_new), between two P.V products.
+// Each half keeps its own running max, sum and TMEM output accumulator (the
+// two halves of the keys are two independent partial attentions), so the
+// halves never synchronise inside the KV loop; at the end of a work item
+// half A merges them: O = (O_A 2^(m_A-m) + O_B 2^(m_B-m)) / (l_A 2^(m_A-m) +
+// l_B 2^(m_B-m)), m = max(m_A, m_B).
+//
+// TMEM (512 columns): scores S0 S1 at 0 and 128, O_A at 256, O_B at 384.
+// Q.K^T of the next block overlaps the softmax of this one.  The
+// exponentials use a reference max that may lag the half-row's true max by
+// up to 8 (log2 units, so every p <= 2^8): only when a block raises it by
+// more is that half's TMEM accumulator (and sum) rescaled, between two
+// P.V products.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -62,14 +67,18 @@ enum {
     B_VE = 8,      // V slot s consumed by P.V (2)
     B_SF = 10,     // score buffer s written (2)
     B_SE = 12,     // score buffer s read by the softmax warps (2)
-    B_PF = 14,     // P written by the softmax warps
-    B_PE = 15,     // P consumed by P.V
-    B_OE = 16,     // the output accumulator read out after an item's last P.V
-    B_DRAIN = 17,  // every MMA of the CTA completed
-    N_BAR = 18
+    B_PF = 14,     // half h of P written (2)
+    B_PE = 16,     // half h of P consumed by its P.V, O_h updated (2)
+    B_OE = 18,     // both accumulators read out after an item's last P.V
+    B_BDONE = 19,  // half B's statistics of the item are in shared memory
+    B_DRAIN = 20,  // every MMA of the CTA completed
+    N_BAR = 21
 };
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BAR;  // TMEM base, abort flag
-constexpr int SMEM_USED = OFF_MISC + 16;
+constexpr int OFF_STATS = OFF_MISC + 16;       // half B's (max, sum) per row: 128 x 8 bytes
+constexpr int OFF_SEEN = OFF_STATS + 128 * 8;  // chunks the producer has acquired this call: 512 bits
+constexpr int SMEM_USED = OFF_SEEN + 64;
+constexpr int NTHREADS = 384;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;   // + the 1024-byte alignment of the tiles
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, 128, false);  // B = K tile, K-major
@@ -194,14 +203,14 @@ __device__ void stage_kv(const Params &p, int worker, int n_workers, int lane) {
         const int64_t len = bytes - off < p.slice_bytes ? bytes - off : p.slice_bytes;
         const uint8_t *src = (sl < half ? p.k_src[q] : p.v_src[q]) + lo * p.row_bytes + off;
         uint8_t *dst = (sl < half ? p.k_dst : p.v_dst) + ((int64_t)q * p.S_r + lo) * p.row_bytes + off;
-        // 16-byte vectors, eight in flight per lane (4 KB per warp round)
-        for (int64_t b = (int64_t)lane * 16; b < len; b += 32 * 16 * 8) {
-            uint4 v[8];
+        // 16-byte vectors, sixteen in flight per lane (8 KB per warp round)
+        for (int64_t b = (int64_t)lane * 16; b < len; b += 32 * 16 * 16) {
+            uint4 v[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < 16; ++u)
                 if (b + u * 512 < len) v[u] = __ldcs(reinterpret_cast<const uint4 *>(src + b + u * 512));
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < 16; ++u)
                 if (b + u * 512 < len) *reinterpret_cast<uint4 *>(dst + b + u * 512) = v[u];
         }
         __syncwarp();
@@ -316,32 +325,39 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
 
 constexpr float kRescale = 8.f;  // how far (log2 units) the reference max may lag
 
-// The finished output row: read from TMEM, normalised, stored as bf16 (and
-// its log-sum-exp).
-__device__ __forceinline__ void store_row(const Params &p, uint32_t to, float m, float l, int h, int q_row0,
-                                          int row) {
+// The finished output row: both halves' accumulators read from TMEM,
+// merged (scaled by fa and fb), normalised by l, stored as bf16; and its
+// log-sum-exp.
+__device__ __forceinline__ void store_merged(const Params &p, uint32_t oa, uint32_t ob, float fa, float fb, float m,
+                                             float l, int h, int q_row0, int row) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    fa *= inv;
+    fb *= inv;
     uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((int64_t)(q_row0 + row) * p.H_q + h) * kD);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(to + (uint32_t)(c * 32), v);
+        uint32_t va[32], vb[32];
+        ptx::tmem_ld_32x32b_x32(oa + (uint32_t)(c * 32), va);
+        ptx::tmem_ld_32x32b_x32(ob + (uint32_t)(c * 32), vb);
         ptx::tmem_ld_wait();
+        float o[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) o[t] = fmaf(__uint_as_float(va[t]), fa, __uint_as_float(vb[t]) * fb);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            uint4 o;
-            o.x = pack_bf16(__uint_as_float(v[8 * k + 0]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
-            o.y = pack_bf16(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
-            o.z = pack_bf16(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
-            o.w = pack_bf16(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
-            dst[c * 4 + k] = o;
+            uint4 q;
+            q.x = pack_bf16(o[8 * k + 0], o[8 * k + 1]);
+            q.y = pack_bf16(o[8 * k + 2], o[8 * k + 3]);
+            q.z = pack_bf16(o[8 * k + 4], o[8 * k + 5]);
+            q.w = pack_bf16(o[8 * k + 6], o[8 * k + 7]);
+            dst[c * 4 + k] = q;
         }
     }
     if (p.lse != nullptr)  // natural log: (m + log2 l) * ln 2, m in log2-scaled units
         p.lse[(int64_t)(q_row0 + row) * p.H_q + h] = (m + log2f(l)) * 0.69314718055994531f;
 }
 
-__global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant__ Params p,
+__global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_constant__ Params p,
                                                            const __grid_constant__ Maps m) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -362,11 +378,12 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
             ptx::mbar_init(bar(B_VF + s), 1);
             ptx::mbar_init(bar(B_VE + s), 1);
             ptx::mbar_init(bar(B_SF + s), 1);
-            ptx::mbar_init(bar(B_SE + s), 4);  // one arrival per softmax warp
+            ptx::mbar_init(bar(B_SE + s), 8);  // one arrival per softmax warp
+            ptx::mbar_init(bar(B_PF + s), 4);  // per half: its four warps
+            ptx::mbar_init(bar(B_PE + s), 1);
         }
-        ptx::mbar_init(bar(B_OE), 4);  // the output accumulator read out (one arrival per softmax warp)
-        ptx::mbar_init(bar(B_PF), 4);
-        ptx::mbar_init(bar(B_PE), 1);
+        ptx::mbar_init(bar(B_OE), 4);     // half A's warps, after the merge
+        ptx::mbar_init(bar(B_BDONE), 4);  // half B's warps
         ptx::mbar_init(bar(B_DRAIN), 1);
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -388,6 +405,8 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
         // ================= TMA producer =================
         if (lane == 0) {
             const uint32_t sQ = sbase + OFF_Q, sK = sbase + OFF_K, sV = sbase + OFF_V;
+            uint32_t *seen = reinterpret_cast<uint32_t *>(sm + OFF_SEEN);
+            for (int i = 0; i < 16; ++i) seen[i] = 0u;
             Walk wk;
             wk.init(p);
             Blk b;
@@ -405,13 +424,21 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
                 }
                 const int src = b.kv0 / p.S_r;
                 if (p.waits && !(p.local_inplace && src == p.rank)) {
+                    // each chunk is acquired (and fenced for the TMA reads) once per call;
+                    // every later item that reads it follows in this thread's program order
                     const int lr0 = b.kv0 - src * p.S_r;
                     const int lo = (int)(((int64_t)lr0 * p.split) / p.S_r);
                     const int hi = (int)(((int64_t)(lr0 + kBK - 1) * p.split) / p.S_r);
-                    bool ok = true;
-                    for (int c = lo; ok && c <= hi; ++c) ok = wait_chunk(p, src * p.split + c, abort);
+                    bool ok = true, fresh = false;
+                    for (int c = lo; ok && c <= hi; ++c) {
+                        const int code = src * p.split + c;
+                        if (seen[code >> 5] & (1u << (code & 31))) continue;
+                        ok = wait_chunk(p, code, abort);
+                        seen[code >> 5] |= 1u << (code & 31);
+                        fresh = true;
+                    }
                     if (!ok) break;
-                    ptx::fence_proxy_async();  // generic acquire -> async-proxy (TMA) reads
+                    if (fresh) ptx::fence_proxy_async();  // generic acquire -> async-proxy (TMA) reads
                 }
                 const int s = (int)(g & 1u);
                 const uint32_t ph = (g >> 1) & 1u;
@@ -437,21 +464,24 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
         // ================= MMA issuer =================
         if (lane == 0) {
             const uint32_t sQ = sbase + OFF_Q, sK = sbase + OFF_K, sV = sbase + OFF_V, sP = sbase + OFF_P;
-            const uint32_t d_o = tmem + 256u;
-            // O (+)= P_i . V_i; an item's first product overwrites O once the
-            // softmax warps have read out the previous item (its `item`-th)
+            // O_h (+)= P_h . V_h for the key halves h = 0, 1 (16-key slices 4h..4h+3
+            // of P and V); an item's first products overwrite O_A and O_B once the
+            // previous item (its `item`-th) has been read out
             auto pv = [&](uint32_t i, bool first, uint32_t item) -> bool {
                 const int s = (int)(i & 1u);
-                if (!wait_bar(bar(B_PF), i & 1u, abort, p)) return false;
                 if (!wait_bar(bar(B_VF + s), (i >> 1) & 1u, abort, p)) return false;
                 if (first && item > 0 && !wait_bar(bar(B_OE), (item - 1u) & 1u, abort, p)) return false;
-                ptx::tc_fence_after();
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!wait_bar(bar(B_PF + hh), i & 1u, abort, p)) return false;
+                    ptx::tc_fence_after();
+                    const uint32_t d_o = tmem + 256u + (uint32_t)(hh * 128);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    ptx::umma_bf16(d_o, kmajor_desc(sP, kk), mnmajor_desc(sV + s * kTileBytes, kk), IDESC_PV,
-                                   (kk != 0 || !first) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::umma_bf16(d_o, kmajor_desc(sP, 4 * hh + kk), mnmajor_desc(sV + s * kTileBytes, 4 * hh + kk),
+                                       IDESC_PV, (kk != 0 || !first) ? 1u : 0u);
+                    ptx::umma_commit(bar(B_PE + hh));  // half hh of P read, O_hh updated
+                }
                 ptx::umma_commit(bar(B_VE + s));
-                ptx::umma_commit(bar(B_PE));  // P read and O updated
                 return true;
             };
             Walk wk;
@@ -498,13 +528,16 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
         // ================= stagers =================
         if (p.stage) stage_kv(p, (int)blockIdx.x * 2 + (warp - 2), (int)gridDim.x * 2, lane);
     } else {
-        // ================= softmax, output rescaling, epilogue =================
+        // ================= softmax halves, output rescaling, epilogue =================
+        const int hx = (warp - 4) >> 2;  // key half: 0 = A (keys 0-63), 1 = B (keys 64-127)
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
-        const uint32_t to = tl + 256u;  // this warp's lanes of the output accumulator
-        const uint32_t sP = sbase + OFF_P;
+        const uint32_t to = tl + 256u + (uint32_t)(hx * 128);  // this half's output accumulator
+        const uint32_t sP = sbase + OFF_P + (uint32_t)hx * kBoxBytes;
+        float2 *stats = reinterpret_cast<float2 *>(sm + OFF_STATS);
         float mref = -INFINITY, lrow = 0.f;  // reference max (log2-scaled units), running sum
+        uint32_t items = 0;
         Walk wk;
         wk.init(p);
         Blk b;
@@ -519,27 +552,25 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
             ptx::tc_fence_after();
             const int qpos0 = p.rank * p.S_r + b.q_row0;              // the tile's first query position
             const int qpos = qpos0 + row;                             // this row's
-            const bool masked = p.causal && b.kv0 + kBK - 1 > qpos0;  // the block crosses the diagonal
-            const uint32_t ts = tl + (uint32_t)(s * 128);
-            uint32_t v[kBK];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t (&vc)[32] = *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c);
-                ptx::tmem_ld_32x32b_x32(ts + (uint32_t)(c * 32), vc);
-            }
+            const int k0 = b.kv0 + hx * 64;                           // this half's first key
+            const bool masked = p.causal && k0 + 63 > qpos0;          // the half-block crosses the diagonal
+            const uint32_t ts = tl + (uint32_t)(s * 128 + hx * 64);
+            uint32_t v[64];
+            ptx::tmem_ld_32x32b_x32(ts, *reinterpret_cast<uint32_t(*)[32]>(v));
+            ptx::tmem_ld_32x32b_x32(ts + 32u, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
             ptx::tmem_ld_wait();
             if (masked) {
 #pragma unroll
-                for (int t = 0; t < kBK; ++t)
-                    if (b.kv0 + t > qpos) v[t] = __float_as_uint(-INFINITY);
+                for (int t = 0; t < 64; ++t)
+                    if (k0 + t > qpos) v[t] = __float_as_uint(-INFINITY);
             }
             float mx = -INFINITY;
 #pragma unroll
-            for (int t = 0; t < kBK; ++t) mx = fmaxf(mx, __uint_as_float(v[t]));
+            for (int t = 0; t < 64; ++t) mx = fmaxf(mx, __uint_as_float(v[t]));
             const float mcand = mx * p.scale_log2;  // (scale > 0: the max commutes with it)
-            // P.V of the previous block must be done: it read P, and O may be rescaled
+            // this half's previous P.V must be done: it read P, and O may be rescaled
             if (g > 0) {
-                w = wait_bar(bar(B_PE), (g - 1u) & 1u, abort, p);
+                w = wait_bar(bar(B_PE + hx), (g - 1u) & 1u, abort, p);
                 if (!__all_sync(0xffffffffu, w)) break;
                 ptx::tc_fence_after();
             }
@@ -568,7 +599,7 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
             const float base = mref == -INFINITY ? 0.f : mref;
             float sum = 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int t = 0; t < 32; t += 2) {
@@ -577,12 +608,12 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
                     sum += p0 + p1;
                     pk[t >> 1] = pack_bf16(p0, p1);
                 }
-                // keys c*32 .. c*32+31 of this row: box c/2, 16-byte chunks (c&1)*4 + u,
-                // XOR-swizzled by the row within its 8-row atom
-                const uint32_t rowbase = sP + (uint32_t)(c >> 1) * kBoxBytes + (uint32_t)row * 128u;
+                // this half's keys c*32 .. c*32+31: 16-byte chunks c*4 + u of the
+                // half's box row, XOR-swizzled by the row within its 8-row atom
+                const uint32_t rowbase = sP + (uint32_t)row * 128u;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const uint32_t chunk = (uint32_t)(((c & 1) * 4 + u) ^ (row & 7));
+                    const uint32_t chunk = (uint32_t)((c * 4 + u) ^ (row & 7));
                     ptx::st_shared_u4(rowbase + chunk * 16u, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
                 }
             }
@@ -592,16 +623,30 @@ __global__ void __launch_bounds__(256, 1) ring_attn_kernel(const __grid_constant
             __syncwarp();
             if (lane == 0) {
                 ptx::mbar_arrive(bar(B_SE + s));
-                ptx::mbar_arrive(bar(B_PF));
+                ptx::mbar_arrive(bar(B_PF + hx));
             }
-            if (b.last) {  // the item's output: after its last P.V, read O out of TMEM
-                w = wait_bar(bar(B_PE), g & 1u, abort, p);
+            if (b.last) {  // the item's output, after this half's last P.V
+                w = wait_bar(bar(B_PE + hx), g & 1u, abort, p);
                 if (!__all_sync(0xffffffffu, w)) break;
                 ptx::tc_fence_after();
-                store_row(p, to, mref, lrow, b.h, b.q_row0, row);
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(B_OE));
+                if (hx == 1) {
+                    stats[row] = make_float2(mref, lrow);
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(B_BDONE));  // (release: the stats stores before it)
+                } else {
+                    w = wait_bar(bar(B_BDONE), items & 1u, abort, p);
+                    if (!__all_sync(0xffffffffu, w)) break;
+                    const float2 sb = stats[row];
+                    const float m = fmaxf(mref, sb.x);
+                    const float fa = mref == -INFINITY ? 0.f : ex2(mref - m);
+                    const float fb = sb.x == -INFINITY ? 0.f : ex2(sb.x - m);
+                    const float l = lrow * fa + sb.y * fb;
+                    store_merged(p, to, to + 128u, fa, fb, m, l, b.h, b.q_row0, row);
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(B_OE));
+                }
+                ++items;
             }
         }
     }
@@ -681,7 +726,7 @@ int syn_attn_plan_create(syn_attn_plan_t *out, const syn_attn_cfg_t *cfg) {
     if (c.H_q < 1 || c.H_kv < 1 || c.H_q % c.H_kv != 0) return host_fail(SYN_ERR_INVALID, "need H_q % H_kv == 0");
     if (c.H_q > 1024) return host_fail(SYN_ERR_UNSUPPORTED, "H_q > 1024");
     if (c.causal != 0 && c.causal != 1) return host_fail(SYN_ERR_INVALID, "causal must be 0 or 1");
-    if (c.split < 1 || c.split > 64 || c.split > c.S_r / kBK)
+    if (c.split < 1 || c.split > 64 || c.split > c.S_r / kBK)  // (R * split <= 512 chunk bits)
         return host_fail(SYN_ERR_INVALID, "split must be in [1, min(64, S_r/128)]");
     if (c.backend != SYN_BACKEND_TMA_COLOCATED && c.backend != SYN_BACKEND_UNFUSED)
         return host_fail(SYN_ERR_UNSUPPORTED,
@@ -708,7 +753,7 @@ int syn_attn_plan_create(syn_attn_plan_t *out, const syn_attn_cfg_t *cfg) {
     PL_CK(cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->device));
     PL_CK(cudaFuncSetAttribute(ring_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
     int per_sm = 0;
-    PL_CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ring_attn_kernel, 256, SMEM_BYTES));
+    PL_CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ring_attn_kernel, NTHREADS, SMEM_BYTES));
     if (per_sm < 1) return bail(SYN_ERR_UNSUPPORTED, "the attention kernel cannot be resident");
     // persistent: one CTA per SM (all co-resident: a cooperative launch), at
     // most one per work item
@@ -799,7 +844,7 @@ int syn_ring_attention(syn_attn_plan_t pl, const void *Q, const void *const *K_s
     cudaLaunchConfig_t lc;
     std::memset(&lc, 0, sizeof(lc));
     lc.gridDim = dim3((unsigned)pl->grid, 1, 1);
-    lc.blockDim = dim3(256, 1, 1);
+    lc.blockDim = dim3(NTHREADS, 1, 1);
     lc.dynamicSmemBytes = SMEM_BYTES;
     lc.stream = st;
     cudaLaunchAttribute attr[1];
