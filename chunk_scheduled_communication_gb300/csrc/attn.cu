@@ -24,7 +24,10 @@
 // l_B 2^(m_B-m)), m = max(m_A, m_B).
 //
 // TMEM (512 columns): scores S0 S1 at 0 and 128, O_A at 256, O_B at 384.
-// Q.K^T of the next block overlaps the softmax of this one.  The
+// Each half writes its bf16 probabilities over the first 32 columns of its
+// own part of the score buffer (P_A at column 0, P_B at 64), where P.V reads
+// them as a TMEM operand.  Q.K^T of the next block overlaps the softmax of
+// this one.  The
 // exponentials use a reference max that may lag the half-row's true max by
 // up to 8 (log2 units, so every p <= 2^8): only when a block raises it by
 // more is that half's TMEM accumulator (and sum) rescaled, between two
@@ -56,8 +59,7 @@ constexpr int kBoxBytes = kTileBytes / 2;    // 128 rows x 128 bytes, 128-byte s
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + kTileBytes;    // 2 slots
 constexpr int OFF_V = OFF_K + 2 * kTileBytes;
-constexpr int OFF_P = OFF_V + 2 * kTileBytes;
-constexpr int OFF_BAR = OFF_P + kTileBytes;
+constexpr int OFF_BAR = OFF_V + 2 * kTileBytes;
 enum {
     B_QF = 0,      // Q tile landed
     B_QE = 1,      // Q tile read by the item's last Q.K^T
@@ -66,13 +68,13 @@ enum {
     B_VF = 6,      // V slot s landed (2)
     B_VE = 8,      // V slot s consumed by P.V (2)
     B_SF = 10,     // score buffer s written (2)
-    B_SE = 12,     // score buffer s read by the softmax warps (2)
-    B_PF = 14,     // half h of P written (2)
-    B_PE = 16,     // half h of P consumed by its P.V, O_h updated (2)
-    B_OE = 18,     // both accumulators read out after an item's last P.V
-    B_BDONE = 19,  // half B's statistics of the item are in shared memory
-    B_DRAIN = 20,  // every MMA of the CTA completed
-    N_BAR = 21
+    B_SE = 12,     // score buffer s free: its P consumed by both halves' P.V (2)
+    B_PF = 14,     // half h of P written into score buffer s (4: index 2s + h)
+    B_PE = 18,     // half h's P.V of score buffer s done, O_h updated (4)
+    B_OE = 22,     // both accumulators read out after an item's last P.V
+    B_BDONE = 23,  // half B's statistics of the item are in shared memory
+    B_DRAIN = 24,  // every MMA of the CTA completed
+    N_BAR = 25
 };
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BAR;  // TMEM base, abort flag
 constexpr int OFF_STATS = OFF_MISC + 16;       // half B's (max, sum) per row: 128 x 8 bytes
@@ -82,7 +84,7 @@ constexpr int NTHREADS = 384;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;   // + the 1024-byte alignment of the tiles
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, 128, false);  // B = K tile, K-major
-constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, 128, true);   // B = V tile, MN-major
+constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, 128, true);   // A = P in TMEM, B = V tile, MN-major
 constexpr int WHERE_FLAG = 1, WHERE_PIPE = 3;
 
 struct Params {
@@ -378,9 +380,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             ptx::mbar_init(bar(B_VF + s), 1);
             ptx::mbar_init(bar(B_VE + s), 1);
             ptx::mbar_init(bar(B_SF + s), 1);
-            ptx::mbar_init(bar(B_SE + s), 8);  // one arrival per softmax warp
-            ptx::mbar_init(bar(B_PF + s), 4);  // per half: its four warps
-            ptx::mbar_init(bar(B_PE + s), 1);
+            ptx::mbar_init(bar(B_SE + s), 1);
+        }
+        for (int i = 0; i < 4; ++i) {
+            ptx::mbar_init(bar(B_PF + i), 4);  // per buffer and half: the half's four warps
+            ptx::mbar_init(bar(B_PE + i), 1);
         }
         ptx::mbar_init(bar(B_OE), 4);     // half A's warps, after the merge
         ptx::mbar_init(bar(B_BDONE), 4);  // half B's warps
@@ -463,25 +467,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            const uint32_t sQ = sbase + OFF_Q, sK = sbase + OFF_K, sV = sbase + OFF_V, sP = sbase + OFF_P;
-            // O_h (+)= P_h . V_h for the key halves h = 0, 1 (16-key slices 4h..4h+3
-            // of P and V); an item's first products overwrite O_A and O_B once the
-            // previous item (its `item`-th) has been read out
+            const uint32_t sQ = sbase + OFF_Q, sK = sbase + OFF_K, sV = sbase + OFF_V;
+            // O_h (+)= P_h . V_h for the key halves h = 0, 1: P_h from TMEM (8 columns
+            // per 16 keys), V rows 64h.. from shared memory; an item's first products
+            // overwrite O_A and O_B once the previous item (its `item`-th) has been
+            // read out
             auto pv = [&](uint32_t i, bool first, uint32_t item) -> bool {
-                const int s = (int)(i & 1u);
-                if (!wait_bar(bar(B_VF + s), (i >> 1) & 1u, abort, p)) return false;
+                const int s = (int)(i & 1u);  // V slot and score buffer of block i
+                const uint32_t u = (i >> 1) & 1u;
+                if (!wait_bar(bar(B_VF + s), u, abort, p)) return false;
                 if (first && item > 0 && !wait_bar(bar(B_OE), (item - 1u) & 1u, abort, p)) return false;
                 for (int hh = 0; hh < 2; ++hh) {
-                    if (!wait_bar(bar(B_PF + hh), i & 1u, abort, p)) return false;
+                    if (!wait_bar(bar(B_PF + 2 * s + hh), u, abort, p)) return false;
                     ptx::tc_fence_after();
                     const uint32_t d_o = tmem + 256u + (uint32_t)(hh * 128);
+                    const uint32_t a_p = tmem + (uint32_t)(s * 128 + hh * 64);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        ptx::umma_bf16(d_o, kmajor_desc(sP, 4 * hh + kk), mnmajor_desc(sV + s * kTileBytes, 4 * hh + kk),
-                                       IDESC_PV, (kk != 0 || !first) ? 1u : 0u);
-                    ptx::umma_commit(bar(B_PE + hh));  // half hh of P read, O_hh updated
+                        ptx::umma_bf16_ts(d_o, a_p + (uint32_t)(kk * 8), mnmajor_desc(sV + s * kTileBytes, 4 * hh + kk),
+                                          IDESC_PV, (kk != 0 || !first) ? 1u : 0u);
+                    ptx::umma_commit(bar(B_PE + 2 * s + hh));  // half hh's P read, O_hh updated
                 }
                 ptx::umma_commit(bar(B_VE + s));
+                ptx::umma_commit(bar(B_SE + s));  // the score buffer (and the P in it) is free
                 return true;
             };
             Walk wk;
@@ -534,10 +542,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
         const int row = qd * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
         const uint32_t to = tl + 256u + (uint32_t)(hx * 128);  // this half's output accumulator
-        const uint32_t sP = sbase + OFF_P + (uint32_t)hx * kBoxBytes;
         float2 *stats = reinterpret_cast<float2 *>(sm + OFF_STATS);
         float mref = -INFINITY, lrow = 0.f;  // reference max (log2-scaled units), running sum
         uint32_t items = 0;
+        // this half's P.V of block i done (P buffer i&1 read, O_h updated)
+        auto pv_done = [&](uint32_t i) {
+            const bool w = wait_bar(bar(B_PE + 2 * (int)(i & 1u) + hx), (i >> 1) & 1u, abort, p);
+            return __all_sync(0xffffffffu, w);
+        };
         Walk wk;
         wk.init(p);
         Blk b;
@@ -564,70 +576,59 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
                 for (int t = 0; t < 64; ++t)
                     if (k0 + t > qpos) v[t] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
+            // row max and (below) row sum as eight interleaved partials: short
+            // dependency chains instead of one of 64
+            float mp[8];
 #pragma unroll
-            for (int t = 0; t < 64; ++t) mx = fmaxf(mx, __uint_as_float(v[t]));
+            for (int k = 0; k < 8; ++k) mp[k] = __uint_as_float(v[k]);
+#pragma unroll
+            for (int t = 8; t < 64; ++t) mp[t & 7] = fmaxf(mp[t & 7], __uint_as_float(v[t]));
+            const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
             const float mcand = mx * p.scale_log2;  // (scale > 0: the max commutes with it)
-            // this half's previous P.V must be done: it read P, and O may be rescaled
-            if (g > 0) {
-                w = wait_bar(bar(B_PE + hx), (g - 1u) & 1u, abort, p);
-                if (!__all_sync(0xffffffffu, w)) break;
-                ptx::tc_fence_after();
-            }
-            if (b.first) {
-                mref = mcand;
-            } else {
-                const bool need = mcand > mref + kRescale;
-                if (__any_sync(0xffffffffu, need)) {
-                    const float alpha = need ? ex2(mref - mcand) : 1.f;
-                    if (need) {
-                        lrow *= alpha;
-                        mref = mcand;
-                    }
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t o[32];
-                        ptx::tmem_ld_32x32b_x32(to + (uint32_t)(c * 32), o);
-                        ptx::tmem_ld_wait();
-#pragma unroll
-                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-                        ptx::tmem_st_32x32b_x32(to + (uint32_t)(c * 32), o);
-                    }
-                    ptx::tmem_st_wait();
-                }
-            }
+            // a new reference max: the item's first block, or a rise of more than kRescale
+            const bool need = !b.first && mcand > mref + kRescale;
+            const float alpha = need ? ex2(mref - mcand) : 1.f;
+            if (b.first || need) mref = mcand;
             const float base = mref == -INFINITY ? 0.f : mref;
-            float sum = 0.f;
+            float sp[8];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t pk[16];
+            for (int k = 0; k < 8; ++k) sp[k] = 0.f;
+            uint32_t pk[32];
 #pragma unroll
-                for (int t = 0; t < 32; t += 2) {
-                    const float p0 = ex2(fmaf(__uint_as_float(v[c * 32 + t]), p.scale_log2, -base));
-                    const float p1 = ex2(fmaf(__uint_as_float(v[c * 32 + t + 1]), p.scale_log2, -base));
-                    sum += p0 + p1;
-                    pk[t >> 1] = pack_bf16(p0, p1);
-                }
-                // this half's keys c*32 .. c*32+31: 16-byte chunks c*4 + u of the
-                // half's box row, XOR-swizzled by the row within its 8-row atom
-                const uint32_t rowbase = sP + (uint32_t)row * 128u;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t chunk = (uint32_t)((c * 4 + u) ^ (row & 7));
-                    ptx::st_shared_u4(rowbase + chunk * 16u, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                }
+            for (int t = 0; t < 64; t += 2) {
+                const float p0 = ex2(fmaf(__uint_as_float(v[t]), p.scale_log2, -base));
+                const float p1 = ex2(fmaf(__uint_as_float(v[t + 1]), p.scale_log2, -base));
+                sp[(t >> 1) & 7] += p0 + p1;
+                pk[t >> 1] = pack_bf16(p0, p1);
             }
-            lrow += sum;
+            const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+            lrow = lrow * alpha + sum;
+            if (__any_sync(0xffffffffu, need)) {
+                // rescale this half's accumulator between P.V of the previous block
+                // and of this one
+                if (!pv_done(g - 1u)) break;
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    ptx::tmem_ld_32x32b_x32(to + (uint32_t)(c * 32), o);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                    ptx::tmem_st_32x32b_x32(to + (uint32_t)(c * 32), o);
+                }
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+            }
+            // P (bf16 pairs) over this half's first 32 score columns, which it has read
+            ptx::tmem_st_32x32b_x32(ts, pk);
+            ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::fence_proxy_async_smem();  // P's generic stores -> the MMA's async-proxy reads
             __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(bar(B_SE + s));
-                ptx::mbar_arrive(bar(B_PF + hx));
-            }
+            if (lane == 0) ptx::mbar_arrive(bar(B_PF + 2 * s + hx));
             if (b.last) {  // the item's output, after this half's last P.V
-                w = wait_bar(bar(B_PE + hx), g & 1u, abort, p);
-                if (!__all_sync(0xffffffffu, w)) break;
+                if (!pv_done(g)) break;
                 ptx::tc_fence_after();
                 if (hx == 1) {
                     stats[row] = make_float2(mref, lrow);
