@@ -477,6 +477,7 @@ def main():
             baselines[w.op] = res
 
     a2a = measure_a2a(knobs["a2a"], peaks, stream) if rank == 0 and not args.no_baselines else None
+    ring_attn = measure_attention(peaks, stream) if rank == 0 and not args.no_baselines else None
 
     # ---------------- CPU oracle baseline (rank 0, N = 1) ----------------
     cpu = None
@@ -498,7 +499,7 @@ def main():
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": sum(launches_per_call(p) for p in plans) * args.steps,
                 "per_call": per_call,
-                "clocks": clk, "per_op": per_op, "baselines": baselines, "a2a": a2a,
+                "clocks": clk, "per_op": per_op, "baselines": baselines, "a2a": a2a, "ring_attention": ring_attn,
                 "peaks": {**peaks, "source": peak_src}}
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -603,6 +604,64 @@ def measure_a2a(knobs, peaks, stream, reps=200):
             "cublas_plus_copy_us": cublas_plus_copy_us(w, d, stream),
             "flag_wait_share": wait_ns / busy_ns if busy_ns else None,
             "gpu_launches_per_call": launches, "knobs": knobs}
+
+
+def measure_attention(peaks, stream, reps=20):
+    """Ring attention (sequence parallel, chunk-scheduled KV exchange) on the
+    Llama-3-8B 32K-context shape, timed alone: CUDA events around `reps`
+    back-to-back calls after warm-up; the same kernel after copying every KV
+    shard first ("unfused"); torch's scaled_dot_product_attention on the
+    gathered keys as context."""
+    import torch
+
+    from chunk_scheduled_communication_gb300 import attn
+
+    def dev(b):
+        return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+
+    out = {}
+    for w, r in ((wl.LLAMA3_8B_RING_ATTN, 0), (wl.LLAMA3_8B_RING_ATTN_CAUSAL, wl.LLAMA3_8B_RING_ATTN_CAUSAL.R - 1)):
+        Q, Ks, Vs = wl.make_attn_inputs(w, 0)
+        kg = torch.zeros((w.R * w.S_r, w.H_kv, w.d), dtype=torch.bfloat16, device="cuda")
+        vg = torch.zeros_like(kg)
+        ks, vs = [dev(k) for k in Ks], [dev(v) for v in Vs]
+        sl = slice(r * w.S_r, (r + 1) * w.S_r)
+        kg[sl], vg[sl] = ks[r], vs[r]
+        ks[r], vs[r] = kg[sl], vg[sl]
+        q = dev(Q)
+        O = torch.empty((w.S_r, w.H_q, w.d), dtype=torch.bfloat16, device="cuda")
+        res = {"workload": w.name, "rank": r, "flops": w.flops}
+        for be in ("tma_colocated", "unfused"):
+            with attn.AttnPlan(R=w.R, rank=r, S_r=w.S_r, H_q=w.H_q, H_kv=w.H_kv, causal=w.causal,
+                               backend=be) as p:
+                for _ in range(3):
+                    p.run(q, ks, vs, kg, vg, O, stream=stream)
+                p.check(stream)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    p.run(q, ks, vs, kg, vg, O, stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                p.check(stream)
+            res[be + "_us"] = e0.elapsed_time(e1) / reps * 1e3
+        us = res["tma_colocated_us"]
+        res["tflops"] = w.flops / (us * 1e-6) / 1e12
+        res["roofline_frac_burst_peak"] = res["tflops"] / peaks["bf16_tflops"]
+        if not w.causal:  # (torch's masked path is not a flash kernel: no fair comparison)
+            qq, kk, vv = (x.permute(1, 0, 2).unsqueeze(0) for x in (q, kg, vg))
+            f = lambda: torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, enable_gqa=True)
+            for _ in range(3):
+                f()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                f()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            res["torch_sdpa_us"] = e0.elapsed_time(e1) / reps * 1e3
+        out["causal" if w.causal else "full"] = res
+    return out
 
 
 def launches_per_call(plan) -> int:
