@@ -661,6 +661,32 @@ def measure_attention(peaks, stream, reps=20):
             torch.cuda.synchronize()
             res["torch_sdpa_us"] = e0.elapsed_time(e1) / reps * 1e3
         out["causal" if w.causal else "full"] = res
+    # head-parallel layout (the all-to-all form): rank 0's 4 query heads over all 32K tokens
+    w = wl.LLAMA3_8B_RING_ATTN
+    Qs, Ks, Vs = wl.make_head_attn_inputs(w, 0)
+    hq, hkv = w.H_q // w.R, w.H_kv // w.R
+    qs, ks, vs = [dev(x) for x in Qs], [dev(x) for x in Ks], [dev(x) for x in Vs]
+    qg = torch.zeros((w.R * w.S_r, hq, w.d), dtype=torch.bfloat16, device="cuda")
+    kg = torch.zeros((w.R * w.S_r, hkv, w.d), dtype=torch.bfloat16, device="cuda")
+    vg = torch.zeros_like(kg)
+    O = torch.empty((w.R * w.S_r, hq, w.d), dtype=torch.bfloat16, device="cuda")
+    res = {"workload": w.name.replace("ring-attn-sp8", "head-parallel-attn-hp8"), "rank": 0, "flops": w.flops}
+    for be in ("tma_colocated", "unfused"):
+        with attn.AttnPlan(R=w.R, rank=0, S_r=w.S_r, H_q=w.H_q, H_kv=w.H_kv, backend=be, head_parallel=True) as p:
+            for _ in range(3):
+                p.run_head(qs, ks, vs, qg, kg, vg, O, stream=stream)
+            p.check(stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                p.run_head(qs, ks, vs, qg, kg, vg, O, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            p.check(stream)
+        res[be + "_us"] = e0.elapsed_time(e1) / reps * 1e3
+    res["tflops"] = w.flops / (res["tma_colocated_us"] * 1e-6) / 1e12
+    res["roofline_frac_burst_peak"] = res["tflops"] / peaks["bf16_tflops"]
+    out["head_parallel"] = res
     return out
 
 

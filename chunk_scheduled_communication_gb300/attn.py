@@ -16,7 +16,7 @@ class AttnCfg(ctypes.Structure):
     _fields_ = [("R", ctypes.c_int), ("rank", ctypes.c_int), ("S_r", ctypes.c_int64), ("H_q", ctypes.c_int),
                 ("H_kv", ctypes.c_int), ("d", ctypes.c_int), ("causal", ctypes.c_int), ("split", ctypes.c_int),
                 ("backend", ctypes.c_int), ("scale", ctypes.c_float), ("timeout_ns", ctypes.c_uint64),
-                ("debug_drop_chunk", ctypes.c_int)]
+                ("debug_drop_chunk", ctypes.c_int), ("head_parallel", ctypes.c_int)]
 
 
 class AttnInfo(ctypes.Structure):
@@ -34,6 +34,7 @@ SIGS = {
     "syn_attn_plan_create": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.POINTER(AttnCfg)]),
     "syn_attn_plan_destroy": (ctypes.c_int, [_P]),
     "syn_ring_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "syn_head_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "syn_attn_sync_status": (ctypes.c_int, [_P, _P]),
     "syn_attn_plan_query": (ctypes.c_int, [_P, ctypes.POINTER(AttnInfo)]),
     "syn_attn_plan_flags": (ctypes.c_int, [_P, _P]),
@@ -55,13 +56,14 @@ def lib():
 
 
 def make_cfg(R=1, rank=0, S_r=128, H_q=1, H_kv=1, d=128, causal=False, split=1, backend="tma_colocated", scale=0.0,
-             timeout_ns=0, drop_chunk=-1) -> AttnCfg:
+             timeout_ns=0, drop_chunk=-1, head_parallel=False) -> AttnCfg:
     c = AttnCfg()
     _check(lib().syn_attn_cfg_default(ctypes.byref(c)), "syn_attn_cfg_default")
     c.R, c.rank, c.S_r, c.H_q, c.H_kv, c.d = R, rank, S_r, H_q, H_kv, d
     c.causal, c.split = int(bool(causal)), split
     c.backend = syn.BACKENDS[backend] if isinstance(backend, str) else int(backend)
     c.scale, c.timeout_ns, c.debug_drop_chunk = scale, timeout_ns, drop_chunk
+    c.head_parallel = int(bool(head_parallel))
     return c
 
 
@@ -113,6 +115,13 @@ class AttnPlan:
         vs = (_P * R)(*[syn._ptr(t) for t in V_shards])
         _check(self._L.syn_ring_attention(self._h, syn._ptr(Q), ks, vs, syn._ptr(K_gathered), syn._ptr(V_gathered),
                                           syn._ptr(O), syn._ptr(lse), syn._stream(stream)), "syn_ring_attention")
+
+    def run_head(self, Q_shards, K_shards, V_shards, Q_gathered, K_gathered, V_gathered, O, lse=None, stream=None):
+        R = self.cfg.R
+        arr = lambda ts: (_P * R)(*[syn._ptr(t) for t in ts])
+        _check(self._L.syn_head_attention(self._h, arr(Q_shards), arr(K_shards), arr(V_shards), syn._ptr(Q_gathered),
+                                          syn._ptr(K_gathered), syn._ptr(V_gathered), syn._ptr(O), syn._ptr(lse),
+                                          syn._stream(stream)), "syn_head_attention")
 
     def sync(self, stream=None) -> int:
         return int(self._L.syn_attn_sync_status(self._h, syn._stream(stream)))

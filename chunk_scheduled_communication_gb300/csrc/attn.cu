@@ -88,7 +88,11 @@ constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, 128, true);   // A = P in
 constexpr int WHERE_FLAG = 1, WHERE_PIPE = 3;
 
 struct Params {
+    // ring mode: Q [S_r, H_q, d] local, queries at global positions rank*S_r + i;
+    // head mode: Q gathered [R*S_r, H_q, d] (H_q = the local query heads),
+    // queries at positions i, their rows waited for like the keys'
     int32_t R, rank, S_r, H_q, G, causal, split, n_qtiles, n_items;
+    int32_t head_mode, q_pos0;  // q_pos0: global position of Q row 0
     int32_t local_inplace, waits;
     float scale_log2;  // scale * log2(e)
     uint32_t epoch;
@@ -98,11 +102,15 @@ struct Params {
     float *lse;             // [S_r, H_q] or null
     int32_t *err;           // {code, site, CTA, info}
     // in-kernel staging (stage = 1): warps 2-3 of every CTA copy the other
-    // ranks' KV chunks into the gathered buffers in arrival order
-    int32_t stage, n_transfers, slices_per_transfer, drop_transfer;
-    int64_t row_bytes, slice_bytes;
-    const uint8_t *k_src[8], *v_src[8];
-    uint8_t *k_dst, *v_dst;
+    // ranks' chunks into the gathered buffers in arrival order.  Tensor x
+    // (K, V, and in head mode Q): row i of source q's chunk rows copies
+    // width[x] bytes from src[x][q] + i * src_pitch[x] + src_off[x] to
+    // dst[x] + (q * S_r + i) * width[x]; slices of slice_rows[x] rows
+    int32_t stage, n_transfers, n_tensors, drop_transfer;
+    int32_t slice_rows[3], slices_of[3];  // slices per chunk of tensor x (the largest chunk)
+    int64_t src_pitch[3], src_off[3], width[3];
+    const uint8_t *src[3][8];
+    uint8_t *dst[3];
     uint32_t *flags_w;      // the same flags, written by the stagers
     uint32_t *cnt;          // [2][R * split] slice counters (epoch parity)
 };
@@ -186,34 +194,70 @@ __device__ __forceinline__ void transfer_of(const Params &p, int a, int &q, int 
 }
 
 // Stager warp `worker` of `n_workers`: slices worker, worker + n_workers, ...
-// of the transfer list, each a warp-wide copy of up to slice_bytes of a
-// chunk's K rows or V rows; the warp that completes a transfer's last slice
+// of the transfer list (per transfer: slices_of[0] slices of tensor 0, then
+// tensor 1's, ...), each a warp-wide copy of up to slice_rows rows of one
+// tensor of a chunk; the warp that completes a transfer's last slice
 // publishes its flag (release) once every slice's bytes are visible.
-__device__ void stage_kv(const Params &p, int worker, int n_workers, int lane) {
-    const int spt = p.slices_per_transfer, half = spt / 2;
+__device__ void stage_chunks(const Params &p, int worker, int n_workers, int lane) {
+    int spt = 0;
+    for (int x = 0; x < p.n_tensors; ++x) spt += p.slices_of[x];
     const int nf = p.R * p.split;
     uint32_t *cnt = p.cnt + (size_t)counter_half(p.epoch) * nf;
     const int total = p.n_transfers * spt;
     for (int g = worker; g < total; g += n_workers) {
-        const int a = g / spt, sl = g - a * spt;
+        const int a = g / spt;
+        int sl = g - a * spt, x = 0;
+        while (sl >= p.slices_of[x]) sl -= p.slices_of[x++];
         int q, j;
         transfer_of(p, a, q, j);
         const int64_t lo = ((int64_t)j * p.S_r + p.split - 1) / p.split;
         const int64_t hi = ((int64_t)(j + 1) * p.S_r + p.split - 1) / p.split;
-        const int64_t bytes = (hi - lo) * p.row_bytes;
-        const int64_t off = (int64_t)(sl % half) * p.slice_bytes;
-        const int64_t len = bytes - off < p.slice_bytes ? bytes - off : p.slice_bytes;
-        const uint8_t *src = (sl < half ? p.k_src[q] : p.v_src[q]) + lo * p.row_bytes + off;
-        uint8_t *dst = (sl < half ? p.k_dst : p.v_dst) + ((int64_t)q * p.S_r + lo) * p.row_bytes + off;
-        // 16-byte vectors, sixteen in flight per lane (8 KB per warp round)
-        for (int64_t b = (int64_t)lane * 16; b < len; b += 32 * 16 * 16) {
+        const int64_t r0 = lo + (int64_t)sl * p.slice_rows[x];
+        const int64_t r1 = r0 + p.slice_rows[x] < hi ? r0 + p.slice_rows[x] : hi;
+        const int64_t w = p.width[x];
+        const int vpr = (int)(w / 16);  // 16-byte vectors per row
+        const uint8_t *src = p.src[x][q] + p.src_off[x] + r0 * p.src_pitch[x];
+        uint8_t *dst = p.dst[x] + ((int64_t)q * p.S_r + r0) * w;
+        const int nvec = r0 < r1 ? (int)(r1 - r0) * vpr : 0;
+        if (p.src_pitch[x] == w) {  // whole rows: one contiguous span
+            const int64_t len = (int64_t)nvec * 16;
+            for (int64_t b = (int64_t)lane * 16; b < len; b += 32 * 16 * 16) {
+                uint4 v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (b + u * 512 < len) v[u] = __ldcs(reinterpret_cast<const uint4 *>(src + b + u * 512));
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (b + u * 512 < len) *reinterpret_cast<uint4 *>(dst + b + u * 512) = v[u];
+            }
+        } else
+        // sixteen 16-byte vectors in flight per lane (8 KB per warp round); a
+        // lane's vectors are 32 apart, so its (row, column) advances by adds
+        for (int b = lane; b < nvec; b += 32 * 16) {
+            const int row0 = b / vpr, col0 = b - row0 * vpr;
             uint4 v[16];
+            int row = row0, col = col0;
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-                if (b + u * 512 < len) v[u] = __ldcs(reinterpret_cast<const uint4 *>(src + b + u * 512));
+            for (int u = 0; u < 16; ++u) {
+                if (b + u * 32 < nvec)
+                    v[u] = __ldcs(reinterpret_cast<const uint4 *>(src + (int64_t)row * p.src_pitch[x] + col * 16));
+                col += 32;
+                while (col >= vpr) {
+                    col -= vpr;
+                    ++row;
+                }
+            }
+            row = row0;
+            col = col0;
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-                if (b + u * 512 < len) *reinterpret_cast<uint4 *>(dst + b + u * 512) = v[u];
+            for (int u = 0; u < 16; ++u) {
+                if (b + u * 32 < nvec) *reinterpret_cast<uint4 *>(dst + (int64_t)row * w + col * 16) = v[u];
+                col += 32;
+                while (col >= vpr) {
+                    col -= vpr;
+                    ++row;
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) {
@@ -227,6 +271,26 @@ __device__ void stage_kv(const Params &p, int worker, int n_workers, int lane) {
     }
 }
 
+// Acquire (once per call and CTA: `seen` is the producer's bitmap) the flags
+// of the chunks holding gathered rows [row0, row0 + 128); false on timeout.
+__device__ __forceinline__ bool acquire_rows(const Params &p, int row0, uint32_t *seen, volatile int *abort) {
+    const int src = row0 / p.S_r;
+    if (!p.waits || (p.local_inplace && src == p.rank)) return true;
+    const int lr0 = row0 - src * p.S_r;
+    const int lo = (int)(((int64_t)lr0 * p.split) / p.S_r);
+    const int hi = (int)(((int64_t)(lr0 + kBK - 1) * p.split) / p.S_r);
+    bool fresh = false;
+    for (int c = lo; c <= hi; ++c) {
+        const int code = src * p.split + c;
+        if (seen[code >> 5] & (1u << (code & 31))) continue;
+        if (!wait_chunk(p, code, abort)) return false;
+        seen[code >> 5] |= 1u << (code & 31);
+        fresh = true;
+    }
+    if (fresh) ptx::fence_proxy_async();  // generic acquire -> async-proxy (TMA) reads
+    return true;
+}
+
 // The KV blocks a query tile visits, in chunk-arrival order: the shards of
 // ranks r, r+1, ..., r-1, each shard's blocks in ascending order.  Causal:
 // a block whose first key lies after the tile's last query is skipped (and
@@ -237,7 +301,7 @@ struct KvIter {
         t = 0;
         b = 0;
         nb = p.S_r / kBK;
-        last = p.causal ? p.rank * p.S_r + q_row0 + kBQ - 1 : 0x7fffffff;
+        last = p.causal ? p.q_pos0 + q_row0 + kBQ - 1 : 0x7fffffff;
     }
     // first global key row of the next block, -1 past the end
     __device__ __forceinline__ int next(const Params &p) {
@@ -420,30 +484,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
                 // a new item: its Q tile replaces the previous one once that item's
                 // last Q.K^T has been issued and completed
                 if (b.first) {
+                    if (p.head_mode && !acquire_rows(p, b.q_row0, seen, abort)) break;  // gathered queries
                     if (!wait_bar(bar(B_QE), (ic & 1u) ^ 1u, abort, p)) break;
                     ptx::mbar_arrive_expect_tx(bar(B_QF), kTileBytes);
                     ptx::tma_load_2d(sQ, &m.q, bar(B_QF), b.h * kD, b.q_row0);
                     ptx::tma_load_2d(sQ + kBoxBytes, &m.q, bar(B_QF), b.h * kD + 64, b.q_row0);
                     ++ic;
                 }
-                const int src = b.kv0 / p.S_r;
-                if (p.waits && !(p.local_inplace && src == p.rank)) {
-                    // each chunk is acquired (and fenced for the TMA reads) once per call;
-                    // every later item that reads it follows in this thread's program order
-                    const int lr0 = b.kv0 - src * p.S_r;
-                    const int lo = (int)(((int64_t)lr0 * p.split) / p.S_r);
-                    const int hi = (int)(((int64_t)(lr0 + kBK - 1) * p.split) / p.S_r);
-                    bool ok = true, fresh = false;
-                    for (int c = lo; ok && c <= hi; ++c) {
-                        const int code = src * p.split + c;
-                        if (seen[code >> 5] & (1u << (code & 31))) continue;
-                        ok = wait_chunk(p, code, abort);
-                        seen[code >> 5] |= 1u << (code & 31);
-                        fresh = true;
-                    }
-                    if (!ok) break;
-                    if (fresh) ptx::fence_proxy_async();  // generic acquire -> async-proxy (TMA) reads
-                }
+                if (!acquire_rows(p, b.kv0, seen, abort)) break;
                 const int s = (int)(g & 1u);
                 const uint32_t ph = (g >> 1) & 1u;
                 if (!wait_bar(bar(B_KE + s), ph ^ 1u, abort, p)) break;
@@ -534,7 +582,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
         }
     } else if (warp < 4) {
         // ================= stagers =================
-        if (p.stage) stage_kv(p, (int)blockIdx.x * 2 + (warp - 2), (int)gridDim.x * 2, lane);
+        if (p.stage) stage_chunks(p, (int)blockIdx.x * 2 + (warp - 2), (int)gridDim.x * 2, lane);
     } else {
         // ================= softmax halves, output rescaling, epilogue =================
         const int hx = (warp - 4) >> 2;  // key half: 0 = A (keys 0-63), 1 = B (keys 64-127)
@@ -562,7 +610,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             bool w = wait_bar(bar(B_SF + s), (g >> 1) & 1u, abort, p);
             if (!__all_sync(0xffffffffu, w)) break;
             ptx::tc_fence_after();
-            const int qpos0 = p.rank * p.S_r + b.q_row0;              // the tile's first query position
+            const int qpos0 = p.q_pos0 + b.q_row0;                    // the tile's first query position
             const int qpos = qpos0 + row;                             // this row's
             const int k0 = b.kv0 + hx * 64;                           // this half's first key
             const bool masked = p.causal && k0 + 63 > qpos0;          // the half-block crosses the diagonal
@@ -675,7 +723,6 @@ struct syn_attn_plan_s {
     int32_t *d_err = nullptr;
     Maps maps;
     std::vector<const void *> map_key;
-    int64_t row_bytes = 0;  // H_kv * d * 2
 };
 
 namespace {
@@ -711,6 +758,7 @@ int syn_attn_cfg_default(syn_attn_cfg_t *c) {
     c->split = 1;
     c->backend = SYN_BACKEND_TMA_COLOCATED;
     c->debug_drop_chunk = -1;
+    c->head_parallel = 0;
     return SYN_OK;
 }
 
@@ -739,8 +787,10 @@ int syn_attn_plan_create(syn_attn_plan_t *out, const syn_attn_cfg_t *cfg) {
     pl->cfg = c;
     if (pl->cfg.scale == 0.f) pl->cfg.scale = 1.f / std::sqrt((float)kD);
     if (pl->cfg.timeout_ns == 0) pl->cfg.timeout_ns = host_timeout_ns();
-    pl->n_qtiles = (int)(c.S_r / kBQ);
-    pl->row_bytes = (int64_t)c.H_kv * kD * 2;
+    if (c.head_parallel != 0 && c.head_parallel != 1) return host_fail(SYN_ERR_INVALID, "head_parallel must be 0 or 1");
+    if (c.head_parallel && (c.H_q % c.R != 0 || c.H_kv % c.R != 0))
+        return host_fail(SYN_ERR_INVALID, "head-parallel attention needs H_q and H_kv divisible by R");
+    pl->n_qtiles = (int)((c.head_parallel ? c.R * c.S_r : c.S_r) / kBQ);
     auto bail = [&](int code, const std::string &msg) {
         free_attn(pl);
         return host_fail(code, msg);
@@ -758,7 +808,7 @@ int syn_attn_plan_create(syn_attn_plan_t *out, const syn_attn_cfg_t *cfg) {
     if (per_sm < 1) return bail(SYN_ERR_UNSUPPORTED, "the attention kernel cannot be resident");
     // persistent: one CTA per SM (all co-resident: a cooperative launch), at
     // most one per work item
-    pl->grid = std::min(pl->n_qtiles * c.H_q, pl->num_sms * per_sm);
+    pl->grid = std::min(pl->n_qtiles * (c.head_parallel ? c.H_q / c.R : c.H_q), pl->num_sms * per_sm);
     const size_t nf = (size_t)c.R * c.split;
     PL_CK(cudaMalloc(&pl->d_flags, nf * sizeof(uint32_t)));
     PL_CK(cudaMemset(pl->d_flags, 0, nf * sizeof(uint32_t)));
@@ -777,34 +827,48 @@ int syn_attn_plan_destroy(syn_attn_plan_t plan) {
     return SYN_OK;
 }
 
-int syn_ring_attention(syn_attn_plan_t pl, const void *Q, const void *const *K_shards,
-                       const void *const *V_shards, void *K_gathered, void *V_gathered, void *O, float *lse,
-                       void *stream) {
+}  // extern "C"
+
+namespace {
+
+// One call of either mode.  Ring: Q local [S_r, H_q, d], K/V shards staged
+// whole; head: Q/K/V shards [S_r, H, d] of which the local heads' columns
+// are staged into gathered [R*S_r, H_loc, d] buffers.
+int attn_call(syn_attn_plan_s *pl, bool head, const void *Q, const void *const *Q_shards,
+              const void *const *K_shards, const void *const *V_shards, void *Q_gathered, void *K_gathered,
+              void *V_gathered, void *O, float *lse, void *stream) {
     if (pl == nullptr) return host_fail(SYN_ERR_INVALID, "null plan");
     const syn_attn_cfg_t &c = pl->cfg;
-    if (Q == nullptr || K_shards == nullptr || V_shards == nullptr || K_gathered == nullptr ||
-        V_gathered == nullptr || O == nullptr)
+    if ((c.head_parallel != 0) != head)
+        return host_fail(SYN_ERR_INVALID, "the plan was made for the other attention layout");
+    const void *Qk = head ? Q_gathered : Q;  // the queries the kernel reads
+    if (Qk == nullptr || K_shards == nullptr || V_shards == nullptr || K_gathered == nullptr ||
+        V_gathered == nullptr || O == nullptr || (head && Q_shards == nullptr))
         return host_fail(SYN_ERR_INVALID, "null operand");
-    if (!al16(Q) || !al16(K_gathered) || !al16(V_gathered) || !al16(O) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    if (!al16(Qk) || !al16(K_gathered) || !al16(V_gathered) || !al16(O) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
         return host_fail(SYN_ERR_INVALID, "operand not 16-byte aligned");
     for (int q = 0; q < c.R; ++q)
-        if (K_shards[q] == nullptr || V_shards[q] == nullptr || !al16(K_shards[q]) || !al16(V_shards[q]))
+        if (K_shards[q] == nullptr || V_shards[q] == nullptr || !al16(K_shards[q]) || !al16(V_shards[q]) ||
+            (head && (Q_shards[q] == nullptr || !al16(Q_shards[q]))))
             return host_fail(SYN_ERR_INVALID, "shard pointer null or not 16-byte aligned");
+    const int hq = head ? c.H_q / c.R : c.H_q;    // query heads the kernel computes
+    const int hkv = head ? c.H_kv / c.R : c.H_kv;  // KV heads in the gathered buffers
+    const int64_t n_qrows = head ? (int64_t)c.R * c.S_r : c.S_r;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int64_t shard_bytes = c.S_r * pl->row_bytes;
+    const int64_t kv_w = (int64_t)hkv * kD * 2;      // gathered K/V row bytes
+    const int64_t shard_bytes = c.S_r * kv_w;
     uint8_t *kg = static_cast<uint8_t *>(K_gathered), *vg = static_cast<uint8_t *>(V_gathered);
-    const bool inplace = K_shards[c.rank] == kg + c.rank * shard_bytes && V_shards[c.rank] == vg + c.rank * shard_bytes;
-    std::vector<const void *> key = {Q, K_gathered, V_gathered};
+    const bool inplace = !head && K_shards[c.rank] == kg + c.rank * shard_bytes &&
+                         V_shards[c.rank] == vg + c.rank * shard_bytes;
+    std::vector<const void *> key = {Qk, K_gathered, V_gathered};
     if (key != pl->map_key) {
         int rc;
-        if ((rc = host_encode_2d(&pl->maps.q, Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)c.H_q * kD,
-                                 (uint64_t)c.S_r, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != SYN_OK ||
-            (rc = host_encode_2d(&pl->maps.k, K_gathered, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                                 (uint64_t)c.H_kv * kD, (uint64_t)c.R * c.S_r, 64, 128,
-                                 CU_TENSOR_MAP_SWIZZLE_128B)) != SYN_OK ||
-            (rc = host_encode_2d(&pl->maps.v, V_gathered, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                                 (uint64_t)c.H_kv * kD, (uint64_t)c.R * c.S_r, 64, 128,
-                                 CU_TENSOR_MAP_SWIZZLE_128B)) != SYN_OK)
+        if ((rc = host_encode_2d(&pl->maps.q, Qk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)hq * kD,
+                                 (uint64_t)n_qrows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != SYN_OK ||
+            (rc = host_encode_2d(&pl->maps.k, K_gathered, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)hkv * kD,
+                                 (uint64_t)c.R * c.S_r, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != SYN_OK ||
+            (rc = host_encode_2d(&pl->maps.v, V_gathered, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)hkv * kD,
+                                 (uint64_t)c.R * c.S_r, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != SYN_OK)
             return rc;
         pl->map_key = key;
     }
@@ -814,12 +878,14 @@ int syn_ring_attention(syn_attn_plan_t pl, const void *Q, const void *const *K_s
     p.R = c.R;
     p.rank = c.rank;
     p.S_r = (int32_t)c.S_r;
-    p.H_q = c.H_q;
-    p.G = c.H_q / c.H_kv;
+    p.H_q = hq;
+    p.G = hq / hkv;
     p.causal = c.causal;
     p.split = c.split;
     p.n_qtiles = pl->n_qtiles;
-    p.n_items = pl->n_qtiles * c.H_q;
+    p.n_items = pl->n_qtiles * hq;
+    p.head_mode = head ? 1 : 0;
+    p.q_pos0 = head ? 0 : c.rank * (int32_t)c.S_r;
     p.local_inplace = inplace ? 1 : 0;
     p.scale_log2 = c.scale * 1.4426950408889634f;
     p.epoch = pl->epoch;
@@ -830,18 +896,24 @@ int syn_ring_attention(syn_attn_plan_t pl, const void *Q, const void *const *K_s
     p.out = static_cast<uint16_t *>(O);
     p.lse = lse;
     p.err = pl->d_err;
-    p.row_bytes = pl->row_bytes;
     p.n_transfers = (c.R - (inplace ? 1 : 0)) * c.split;
     p.drop_transfer = c.debug_drop_chunk;
-    const int64_t max_chunk_bytes = ((c.S_r + c.split - 1) / c.split) * pl->row_bytes;
-    p.slice_bytes = std::min<int64_t>(64 * 1024, max_chunk_bytes);
-    p.slices_per_transfer = 2 * (int32_t)((max_chunk_bytes + p.slice_bytes - 1) / p.slice_bytes);
-    for (int q = 0; q < c.R; ++q) {
-        p.k_src[q] = static_cast<const uint8_t *>(K_shards[q]);
-        p.v_src[q] = static_cast<const uint8_t *>(V_shards[q]);
+    // staged tensors: K, V (and Q in head mode); a source row holds every head,
+    // the gathered row only the local ones
+    const void *const *srcs[3] = {K_shards, V_shards, Q_shards};
+    void *dsts[3] = {K_gathered, V_gathered, Q_gathered};
+    const int heads_src[3] = {c.H_kv, c.H_kv, c.H_q}, heads_loc[3] = {hkv, hkv, hq};
+    p.n_tensors = head ? 3 : 2;
+    const int64_t max_rows = (c.S_r + c.split - 1) / c.split;
+    for (int x = 0; x < p.n_tensors; ++x) {
+        p.width[x] = (int64_t)heads_loc[x] * kD * 2;
+        p.src_pitch[x] = (int64_t)heads_src[x] * kD * 2;
+        p.src_off[x] = head ? (int64_t)c.rank * heads_loc[x] * kD * 2 : 0;
+        p.slice_rows[x] = (int32_t)std::max<int64_t>(1, (64 * 1024) / p.width[x]);
+        p.slices_of[x] = (int32_t)((max_rows + p.slice_rows[x] - 1) / p.slice_rows[x]);
+        for (int q = 0; q < c.R; ++q) p.src[x][q] = static_cast<const uint8_t *>(srcs[x][q]);
+        p.dst[x] = static_cast<uint8_t *>(dsts[x]);
     }
-    p.k_dst = kg;
-    p.v_dst = vg;
     cudaLaunchConfig_t lc;
     std::memset(&lc, 0, sizeof(lc));
     lc.gridDim = dim3((unsigned)pl->grid, 1, 1);
@@ -860,16 +932,33 @@ int syn_ring_attention(syn_attn_plan_t pl, const void *Q, const void *const *K_s
         for (int t = 0; t < c.R; ++t) {
             const int q = (c.rank + t) % c.R;
             if (q == c.rank && inplace) continue;
-            ATT_CK(cudaMemcpyAsync(kg + (int64_t)q * shard_bytes, K_shards[q], (size_t)shard_bytes,
-                                   cudaMemcpyDeviceToDevice, st));
-            ATT_CK(cudaMemcpyAsync(vg + (int64_t)q * shard_bytes, V_shards[q], (size_t)shard_bytes,
-                                   cudaMemcpyDeviceToDevice, st));
+            for (int x = 0; x < p.n_tensors; ++x)
+                ATT_CK(cudaMemcpy2DAsync(static_cast<uint8_t *>(dsts[x]) + (int64_t)q * c.S_r * p.width[x],
+                                         (size_t)p.width[x], p.src[x][q] + p.src_off[x], (size_t)p.src_pitch[x],
+                                         (size_t)p.width[x], (size_t)c.S_r, cudaMemcpyDeviceToDevice, st));
         }
         p.stage = 0;
         p.waits = 0;
     }
     ATT_CK(cudaLaunchKernelEx(&lc, ring_attn_kernel, p, pl->maps));
     return SYN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int syn_ring_attention(syn_attn_plan_t pl, const void *Q, const void *const *K_shards,
+                       const void *const *V_shards, void *K_gathered, void *V_gathered, void *O, float *lse,
+                       void *stream) {
+    return attn_call(pl, false, Q, nullptr, K_shards, V_shards, nullptr, K_gathered, V_gathered, O, lse, stream);
+}
+
+int syn_head_attention(syn_attn_plan_t pl, const void *const *Q_shards, const void *const *K_shards,
+                       const void *const *V_shards, void *Q_gathered, void *K_gathered, void *V_gathered,
+                       void *O, float *lse, void *stream) {
+    return attn_call(pl, true, nullptr, Q_shards, K_shards, V_shards, Q_gathered, K_gathered, V_gathered, O,
+                     lse, stream);
 }
 
 int syn_attn_sync_status(syn_attn_plan_t pl, void *stream) {
@@ -902,7 +991,7 @@ int syn_attn_plan_query(syn_attn_plan_t pl, syn_attn_info_t *info) {
     info->S_r = c.S_r;
     info->n_qtiles = pl->n_qtiles;
     info->grid = pl->grid;
-    info->n_transfers = (c.R - 1) * c.split;  // with the local shard in place
+    info->n_transfers = (c.head_parallel ? c.R : c.R - 1) * c.split;  // (ring: the local shard in place)
     info->smem_bytes = SMEM_BYTES;
     info->epoch = pl->epoch;
     return SYN_OK;

@@ -209,3 +209,15 @@ def make_attn_inputs(w: AttnWorkload, seed: int = 0):
         Ks.append(to_bf16_bits(_draw(rng, (w.S_r, w.H_kv, w.d), 1.0, "normal")))
         Vs.append(to_bf16_bits(_draw(rng, (w.S_r, w.H_kv, w.d), 1.0, "normal")))
     return Q, Ks, Vs
+
+
+def make_head_attn_inputs(w: AttnWorkload, seed: int = 0):
+    """Head-parallel layout: every rank's tokens of all heads.  For q = 0..R-1
+    in order: Q_q [S_r, H_q, d], K_q, V_q [S_r, H_kv, d], N(0,1) bf16."""
+    rng = np.random.default_rng(seed)
+    Qs, Ks, Vs = [], [], []
+    for _ in range(w.R):
+        Qs.append(to_bf16_bits(_draw(rng, (w.S_r, w.H_q, w.d), 1.0, "normal")))
+        Ks.append(to_bf16_bits(_draw(rng, (w.S_r, w.H_kv, w.d), 1.0, "normal")))
+        Vs.append(to_bf16_bits(_draw(rng, (w.S_r, w.H_kv, w.d), 1.0, "normal")))
+    return Qs, Ks, Vs

@@ -20,6 +20,13 @@
  *   in global order; causal: keys with global position j > r*S_r + i are
  *   excluded.  lse[i][h] = log sum_j exp(scale * Q[i][h] . K[j][hk]).
  *
+ * Head-parallel layout (head_parallel = 1; the all-to-all form): every rank
+ * holds S_r tokens of all heads; rank r computes the full-sequence attention
+ * of its heads h in [r*H_q/R, (r+1)*H_q/R) (KV heads [r*H_kv/R, ...)) for the
+ * queries of every rank.  The kernel stages Q, K and V columns of those heads
+ * from every rank into gathered buffers chunk by chunk (the local rank's too)
+ * and each query tile waits for its own chunk as well as the KV blocks'.
+ *
  * Precision: bf16 inputs; Q.K^T accumulated in fp32 by the tensor cores;
  * softmax in fp32 with exp2 (scores scaled by scale * log2(e)); the
  * probabilities are rounded to bf16 for the P.V product (fp32
@@ -63,13 +70,17 @@ typedef struct {
     int debug_drop_chunk; /* -1 = off; else the arrival index of a chunk whose
                              flag is never written (fault injection: the call
                              must end in SYN_ERR_TIMEOUT)                       */
+    int head_parallel;    /* 0: ring (sequence-parallel) layout, run with
+                             syn_ring_attention; 1: head-parallel layout, run
+                             with syn_head_attention (H_q and H_kv divisible
+                             by R)                                              */
 } syn_attn_cfg_t;
 
 /* Plan facts. */
 typedef struct {
     int R, rank, H_q, H_kv, d, causal, split, backend;
     int64_t S_r;
-    int n_qtiles;         /* S_r / 128                                          */
+    int n_qtiles;         /* query tiles: S_r / 128 (ring), R*S_r / 128 (head)  */
     int grid;             /* persistent CTAs: min(n_qtiles * H_q, resident CTAs);
                              work item (head h, query tile t) = h * n_qtiles + t
                              runs on CTA item mod grid                         */
@@ -106,6 +117,21 @@ int syn_attn_plan_destroy(syn_attn_plan_t plan);
 int syn_ring_attention(syn_attn_plan_t plan, const void *Q, const void *const *K_shards,
                        const void *const *V_shards, void *K_gathered, void *V_gathered, void *O,
                        float *lse, void *stream);
+
+/* One head-parallel attention forward of the plan's rank (asynchronous).
+ *   Q_shards, K_shards, V_shards : host arrays of R device pointers, rank q's
+ *                tokens of all heads: bf16 [S_r, H_q, d] and [S_r, H_kv, d]
+ *   Q_gathered : bf16 [R*S_r, H_q/R, d] output: row q*S_r + i holds rank q's
+ *                token i, heads r*H_q/R .. (r+1)*H_q/R - 1, bit for bit
+ *   K_gathered, V_gathered : bf16 [R*S_r, H_kv/R, d] outputs, likewise
+ *   O          : bf16 [R*S_r, H_q/R, d]: the local heads' attention for every
+ *                token (global positions: causal excludes later tokens)
+ *   lse        : nullable fp32 [R*S_r, H_q/R]
+ * 16-byte alignment as for syn_ring_attention; a ring plan returns
+ * SYN_ERR_INVALID here and a head-parallel plan in syn_ring_attention. */
+int syn_head_attention(syn_attn_plan_t plan, const void *const *Q_shards, const void *const *K_shards,
+                       const void *const *V_shards, void *Q_gathered, void *K_gathered,
+                       void *V_gathered, void *O, float *lse, void *stream);
 
 /* Synchronise `stream`, then read and clear
  * the device error word: SYN_OK, SYN_ERR_TIMEOUT, SYN_ERR_BOUNDS or

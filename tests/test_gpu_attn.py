@@ -163,3 +163,86 @@ def test_llama3_8b_full_size_sampled_rows(w, r):
     inp, got = run(w, r, split=2)
     rows = [(0, 2), (127, 129), (w.S_r // 2, w.S_r // 2 + 2), (w.S_r - 2, w.S_r)]
     check(w, r, inp, got, rows=rows)
+
+
+# ----------------------------------------------------------------------------- head-parallel layout
+def run_head(w, r, split=1, calls=1, seed=0, **cfg):
+    Qs, Ks, Vs = wl.make_head_attn_inputs(w, seed)
+    hq, hkv = w.H_q // w.R, w.H_kv // w.R
+    qs, ks, vs = [dev(x) for x in Qs], [dev(x) for x in Ks], [dev(x) for x in Vs]
+    qg = torch.zeros((w.R * w.S_r, hq, w.d), dtype=torch.bfloat16, device="cuda")
+    kg = torch.zeros((w.R * w.S_r, hkv, w.d), dtype=torch.bfloat16, device="cuda")
+    vg = torch.zeros_like(kg)
+    O = torch.empty((w.R * w.S_r, hq, w.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.R * w.S_r, hq), dtype=torch.float32, device="cuda")
+    with attn.AttnPlan(R=w.R, rank=r, S_r=w.S_r, H_q=w.H_q, H_kv=w.H_kv, causal=w.causal, split=split,
+                       head_parallel=True, **cfg) as plan:
+        for _ in range(calls):
+            plan.run_head(qs, ks, vs, qg, kg, vg, O, lse)
+        plan.check()
+    return (Qs, Ks, Vs), {"O": to_f64(O), "lse": lse.cpu().numpy().astype(np.float64), "qg": qg, "kg": kg, "vg": vg}
+
+
+def check_head(w, r, inp, got, rows=None):
+    """The head-parallel result is plain attention (one rank, global positions)
+    over the gathered local heads: the oracle with R = 1 on the gathered rows."""
+    Qs, Ks, Vs = inp
+    hq, hkv = w.H_q // w.R, w.H_kv // w.R
+    Qg = np.ascontiguousarray(np.concatenate([x[:, r * hq:(r + 1) * hq] for x in Qs]))
+    Kg = np.ascontiguousarray(np.concatenate([x[:, r * hkv:(r + 1) * hkv] for x in Ks]))
+    Vg = np.ascontiguousarray(np.concatenate([x[:, r * hkv:(r + 1) * hkv] for x in Vs]))
+    bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert (bits(got["qg"]) == Qg).all() and (bits(got["kg"]) == Kg).all() and (bits(got["vg"]) == Vg).all()
+    vmax = np.abs(wl.bf16_bits_to_f32(Vg)).max()
+    num = den = 0.0
+    for a, b in rows or [(0, w.R * w.S_r)]:
+        ref, ref_lse = oracle.ring_attention(Qg, [Kg], [Vg], 0, causal=w.causal, row0=a, row1=b)
+        g = got["O"][a:b]
+        bad = np.abs(g - ref) > 2.0 ** -8 * vmax + 2.0 ** -8 * np.abs(ref)
+        assert not bad.any(), (np.argwhere(bad)[:4], g[bad][:4], ref[bad][:4])
+        num += ((g - ref) ** 2).sum()
+        den += (ref ** 2).sum()
+        assert np.abs(got["lse"][a:b] - ref_lse).max() < 1e-3
+    assert np.sqrt(num / den) <= 4e-3, np.sqrt(num / den)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("r,split", [(0, 1), (1, 2), (3, 1)])
+def test_head_parallel_tiny(r, split, causal):
+    w = wl.AttnWorkload("tiny-head", 4, 256, 8, 4, causal=causal)
+    inp, got = run_head(w, r, split=split)
+    check_head(w, r, inp, got)
+
+
+def test_head_parallel_unfused_and_repeated_calls():
+    w = wl.AttnWorkload("tiny-head-gqa", 2, 384, 8, 2, causal=True)
+    inp, got = run_head(w, 1, split=3, backend="unfused")
+    check_head(w, 1, inp, got)
+    inp, got = run_head(w, 0, split=3, calls=3)
+    check_head(w, 0, inp, got)
+
+
+def test_layouts_are_not_interchangeable():
+    w = wl.AttnWorkload("two-ranks", 2, 256, 4, 2)
+    Q, Ks, Vs = wl.make_attn_inputs(w, 0)
+    q, ks, vs, kg, vg, O, lse = upload(w, 0, Q, Ks, Vs)
+    with attn.AttnPlan(R=w.R, rank=0, S_r=w.S_r, H_q=w.H_q, H_kv=w.H_kv, head_parallel=True) as plan:
+        with pytest.raises(syn.SynError) as e:
+            plan.run(q, ks, vs, kg, vg, O, lse)
+        assert e.value.status == syn.ERR_INVALID
+    with attn.AttnPlan(R=w.R, rank=0, S_r=w.S_r, H_q=w.H_q, H_kv=w.H_kv) as plan:
+        with pytest.raises(syn.SynError) as e:
+            plan.run_head([q, q], ks, vs, q, kg, vg, O, lse)
+        assert e.value.status == syn.ERR_INVALID
+    with pytest.raises(syn.SynError) as e:  # H_kv = 2 is not divisible by R = 4
+        attn.AttnPlan(R=4, rank=0, S_r=256, H_q=4, H_kv=2, head_parallel=True)
+    assert e.value.status == syn.ERR_INVALID
+
+
+def test_head_parallel_llama3_8b_full_size_sampled_rows():
+    """Llama-3-8B heads split over 8 ranks (4 query heads, 1 KV head each),
+    32K tokens, causal, rank 5: gathered Q/K/V bit-exact, sampled rows."""
+    w = wl.AttnWorkload("llama3-8b-head-parallel", 8, 4096, 32, 8, causal=True)
+    inp, got = run_head(w, 5, split=2)
+    rows = [(0, 2), (4095, 4097), (16384, 16386), (32766, 32768)]
+    check_head(w, 5, inp, got, rows=rows)
