@@ -55,7 +55,7 @@ def lib():
     return L
 
 
-def make_cfg(R=1, rank=0, S_r=128, H_q=1, H_kv=1, d=128, causal=False, split=1, backend="tma_colocated", scale=0.0,
+def make_cfg(R=1, rank=0, S_r=256, H_q=1, H_kv=1, d=128, causal=False, split=1, backend="tma_colocated", scale=0.0,
              timeout_ns=0, drop_chunk=-1, head_parallel=False) -> AttnCfg:
     c = AttnCfg()
     _check(lib().syn_attn_cfg_default(ctypes.byref(c)), "syn_attn_cfg_default")

@@ -52,33 +52,31 @@ namespace syn {
 namespace attn {
 
 constexpr int kD = 128;                      // head dimension
-constexpr int kBQ = 128;                     // query rows per CTA
+constexpr int kBQ = 128;                     // query rows per tile
+constexpr int kTiles = 2;                    // query tiles per work item
 constexpr int kBK = 128;                     // keys per KV block
 constexpr int kTileBytes = 128 * 128 * 2;    // one 128 x 128 bf16 tile: two 64-wide boxes
 constexpr int kBoxBytes = kTileBytes / 2;    // 128 rows x 128 bytes, 128-byte swizzle
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + kTileBytes;    // 2 slots
+constexpr int OFF_Q = 0;                     // kTiles tiles
+constexpr int OFF_K = OFF_Q + kTiles * kTileBytes;  // 2 slots
 constexpr int OFF_V = OFF_K + 2 * kTileBytes;
 constexpr int OFF_BAR = OFF_V + 2 * kTileBytes;
 enum {
-    B_QF = 0,      // Q tile landed
-    B_QE = 1,      // Q tile read by the item's last Q.K^T
+    B_QF = 0,      // the item's Q tiles landed
+    B_QE = 1,      // Q tiles read by the item's last Q.K^T
     B_KF = 2,      // K slot s landed (2)
-    B_KE = 4,      // K slot s consumed by Q.K^T (2)
+    B_KE = 4,      // K slot s consumed by both tiles' Q.K^T (2)
     B_VF = 6,      // V slot s landed (2)
-    B_VE = 8,      // V slot s consumed by P.V (2)
-    B_SF = 10,     // score buffer s written (2)
-    B_SE = 12,     // score buffer s free: its P consumed by both halves' P.V (2)
-    B_PF = 14,     // half h of P written into score buffer s (4: index 2s + h)
-    B_PE = 18,     // half h's P.V of score buffer s done, O_h updated (4)
-    B_OE = 22,     // both accumulators read out after an item's last P.V
-    B_BDONE = 23,  // half B's statistics of the item are in shared memory
-    B_DRAIN = 24,  // every MMA of the CTA completed
-    N_BAR = 25
+    B_VE = 8,      // V slot s consumed by both tiles' P.V (2)
+    B_SF = 10,     // tile t's scores written (2)
+    B_PF = 12,     // tile t's probabilities written over its scores (2)
+    B_PV = 14,     // tile t's P.V done: O_t updated, its score buffer free (2)
+    B_OE = 16,     // tile t's accumulator read out after an item's last P.V (2)
+    B_DRAIN = 18,  // every MMA of the CTA completed
+    N_BAR = 19
 };
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BAR;  // TMEM base, abort flag
-constexpr int OFF_STATS = OFF_MISC + 16;       // half B's (max, sum) per row: 128 x 8 bytes
-constexpr int OFF_SEEN = OFF_STATS + 128 * 8;  // chunks the producer has acquired this call: 512 bits
+constexpr int OFF_SEEN = OFF_MISC + 16;        // chunks the producer has acquired this call: 512 bits
 constexpr int SMEM_USED = OFF_SEEN + 64;
 constexpr int NTHREADS = 384;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;   // + the 1024-byte alignment of the tiles
@@ -221,24 +219,24 @@ __device__ void stage_chunks(const Params &p, int worker, int n_workers, int lan
         const int nvec = r0 < r1 ? (int)(r1 - r0) * vpr : 0;
         if (p.src_pitch[x] == w) {  // whole rows: one contiguous span
             const int64_t len = (int64_t)nvec * 16;
-            for (int64_t b = (int64_t)lane * 16; b < len; b += 32 * 16 * 16) {
-                uint4 v[16];
+            for (int64_t b = (int64_t)lane * 16; b < len; b += 32 * 16 * 8) {
+                uint4 v[8];
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
+                for (int u = 0; u < 8; ++u)
                     if (b + u * 512 < len) v[u] = __ldcs(reinterpret_cast<const uint4 *>(src + b + u * 512));
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
+                for (int u = 0; u < 8; ++u)
                     if (b + u * 512 < len) *reinterpret_cast<uint4 *>(dst + b + u * 512) = v[u];
             }
         } else
-        // sixteen 16-byte vectors in flight per lane (8 KB per warp round); a
+        // eight 16-byte vectors in flight per lane (4 KB per warp round); a
         // lane's vectors are 32 apart, so its (row, column) advances by adds
-        for (int b = lane; b < nvec; b += 32 * 16) {
+        for (int b = lane; b < nvec; b += 32 * 8) {
             const int row0 = b / vpr, col0 = b - row0 * vpr;
-            uint4 v[16];
+            uint4 v[8];
             int row = row0, col = col0;
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 if (b + u * 32 < nvec)
                     v[u] = __ldcs(reinterpret_cast<const uint4 *>(src + (int64_t)row * p.src_pitch[x] + col * 16));
                 col += 32;
@@ -250,7 +248,7 @@ __device__ void stage_chunks(const Params &p, int worker, int n_workers, int lan
             row = row0;
             col = col0;
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 if (b + u * 32 < nvec) *reinterpret_cast<uint4 *>(dst + (int64_t)row * w + col * 16) = v[u];
                 col += 32;
                 while (col >= vpr) {
@@ -301,7 +299,7 @@ struct KvIter {
         t = 0;
         b = 0;
         nb = p.S_r / kBK;
-        last = p.causal ? p.q_pos0 + q_row0 + kBQ - 1 : 0x7fffffff;
+        last = p.causal ? p.q_pos0 + q_row0 + kTiles * kBQ - 1 : 0x7fffffff;
     }
     // first global key row of the next block, -1 past the end
     __device__ __forceinline__ int next(const Params &p) {
@@ -336,7 +334,7 @@ struct Walk {
         fresh = true;
         nxt = -1;
         if (item < p.n_items) {
-            it.init(p, (item % p.n_qtiles) * kBQ);
+            it.init(p, (item % p.n_qtiles) * kTiles * kBQ);
             nxt = it.next(p);
         }
     }
@@ -351,7 +349,7 @@ struct Walk {
         }
         if (item >= p.n_items) return false;
         b.h = item / p.n_qtiles;
-        b.q_row0 = (item - b.h * p.n_qtiles) * kBQ;
+        b.q_row0 = (item - b.h * p.n_qtiles) * kTiles * kBQ;
         b.kv0 = nxt;
         b.first = fresh;
         fresh = false;
@@ -391,40 +389,39 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
 
 constexpr float kRescale = 8.f;  // how far (log2 units) the reference max may lag
 
-// The finished output row: both halves' accumulators read from TMEM,
-// merged (scaled by fa and fb), normalised by l, stored as bf16; and its
-// log-sum-exp.
-__device__ __forceinline__ void store_merged(const Params &p, uint32_t oa, uint32_t ob, float fa, float fb, float m,
-                                             float l, int h, int q_row0, int row) {
+// The finished output row: the accumulator read from TMEM, normalised by l,
+// stored as bf16; and its log-sum-exp.
+__device__ __forceinline__ void store_row(const Params &p, uint32_t to, float m, float l, int h, int row_g) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    fa *= inv;
-    fb *= inv;
-    uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((int64_t)(q_row0 + row) * p.H_q + h) * kD);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((int64_t)row_g * p.H_q + h) * kD);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        uint32_t va[32], vb[32];
-        ptx::tmem_ld_32x32b_x32(oa + (uint32_t)(c * 32), va);
-        ptx::tmem_ld_32x32b_x32(ob + (uint32_t)(c * 32), vb);
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(to + (uint32_t)(c * 32), v);
         ptx::tmem_ld_wait();
-        float o[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) o[t] = fmaf(__uint_as_float(va[t]), fa, __uint_as_float(vb[t]) * fb);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            uint4 q;
-            q.x = pack_bf16(o[8 * k + 0], o[8 * k + 1]);
-            q.y = pack_bf16(o[8 * k + 2], o[8 * k + 3]);
-            q.z = pack_bf16(o[8 * k + 4], o[8 * k + 5]);
-            q.w = pack_bf16(o[8 * k + 6], o[8 * k + 7]);
-            dst[c * 4 + k] = q;
+            uint4 o;
+            o.x = pack_bf16(__uint_as_float(v[8 * k + 0]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
+            o.y = pack_bf16(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
+            o.z = pack_bf16(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
+            o.w = pack_bf16(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
+            dst[c * 4 + k] = o;
         }
     }
     if (p.lse != nullptr)  // natural log: (m + log2 l) * ln 2, m in log2-scaled units
-        p.lse[(int64_t)(q_row0 + row) * p.H_q + h] = (m + log2f(l)) * 0.69314718055994531f;
+        p.lse[(int64_t)row_g * p.H_q + h] = (m + log2f(l)) * 0.69314718055994531f;
 }
 
+// Register split (setmaxnreg): the launch gives 168 registers per thread
+// (384 threads); the producer, MMA and staging warps give theirs down to 96
+// and the two softmax warpgroups take 200: 128 * 96 + 256 * 200 = 63,488 of
+// the 64,512 launched.
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 96;"); }
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 200;"); }
+
 __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_constant__ Params p,
-                                                           const __grid_constant__ Maps m) {
+                                                                const __grid_constant__ Maps m) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = ptx::smem_u32(sm);
@@ -444,14 +441,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             ptx::mbar_init(bar(B_VF + s), 1);
             ptx::mbar_init(bar(B_VE + s), 1);
             ptx::mbar_init(bar(B_SF + s), 1);
-            ptx::mbar_init(bar(B_SE + s), 1);
+            ptx::mbar_init(bar(B_PF + s), 4);  // the tile's four softmax warps
+            ptx::mbar_init(bar(B_PV + s), 1);
+            ptx::mbar_init(bar(B_OE + s), 4);
         }
-        for (int i = 0; i < 4; ++i) {
-            ptx::mbar_init(bar(B_PF + i), 4);  // per buffer and half: the half's four warps
-            ptx::mbar_init(bar(B_PE + i), 1);
-        }
-        ptx::mbar_init(bar(B_OE), 4);     // half A's warps, after the merge
-        ptx::mbar_init(bar(B_BDONE), 4);  // half B's warps
         ptx::mbar_init(bar(B_DRAIN), 1);
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -468,7 +461,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
     if (p.stage && blockIdx.x == 0)
         for (int i = (int)threadIdx.x; i < p.R * p.split; i += (int)blockDim.x)
             p.cnt[(size_t)spare_half(p.epoch) * p.R * p.split + i] = 0u;
-
+    if (warp < 4) {
+        regs_dec();
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
@@ -481,14 +475,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             uint32_t g = 0, ic = 0, nk = 0, nv = 0;
             for (; wk.next(p, b); ++g) {
                 const int hk = b.h / p.G;
-                // a new item: its Q tile replaces the previous one once that item's
-                // last Q.K^T has been issued and completed
                 if (b.first) {
-                    if (p.head_mode && !acquire_rows(p, b.q_row0, seen, abort)) break;  // gathered queries
-                    if (!wait_bar(bar(B_QE), (ic & 1u) ^ 1u, abort, p)) break;
-                    ptx::mbar_arrive_expect_tx(bar(B_QF), kTileBytes);
-                    ptx::tma_load_2d(sQ, &m.q, bar(B_QF), b.h * kD, b.q_row0);
-                    ptx::tma_load_2d(sQ + kBoxBytes, &m.q, bar(B_QF), b.h * kD + 64, b.q_row0);
+                    // the item's Q tiles (gathered queries: once their chunks are in)
+                    // replace the previous ones once that item's last Q.K^T completed
+                    bool ok = true;
+                    for (int t = 0; ok && p.head_mode && t < kTiles; ++t)
+                        ok = acquire_rows(p, b.q_row0 + t * kBQ, seen, abort);
+                    if (!ok || !wait_bar(bar(B_QE), (ic & 1u) ^ 1u, abort, p)) break;
+                    ptx::mbar_arrive_expect_tx(bar(B_QF), kTiles * kTileBytes);
+                    for (int t = 0; t < kTiles; ++t) {
+                        ptx::tma_load_2d(sQ + t * kTileBytes, &m.q, bar(B_QF), b.h * kD, b.q_row0 + t * kBQ);
+                        ptx::tma_load_2d(sQ + t * kTileBytes + kBoxBytes, &m.q, bar(B_QF), b.h * kD + 64,
+                                         b.q_row0 + t * kBQ);
+                    }
                     ++ic;
                 }
                 if (!acquire_rows(p, b.kv0, seen, abort)) break;
@@ -514,90 +513,96 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
+        // Per tile t the chain is Q.K^T(g) -> softmax -> P.V(g) -> Q.K^T(g+1) (the
+        // probabilities live in the tile's score buffer); the two tiles' chains
+        // interleave, so one tile's MMAs run while the other's softmax does.
         if (lane == 0) {
             const uint32_t sQ = sbase + OFF_Q, sK = sbase + OFF_K, sV = sbase + OFF_V;
-            // O_h (+)= P_h . V_h for the key halves h = 0, 1: P_h from TMEM (8 columns
-            // per 16 keys), V rows 64h.. from shared memory; an item's first products
-            // overwrite O_A and O_B once the previous item (its `item`-th) has been
-            // read out
-            auto pv = [&](uint32_t i, bool first, uint32_t item) -> bool {
-                const int s = (int)(i & 1u);  // V slot and score buffer of block i
-                const uint32_t u = (i >> 1) & 1u;
-                if (!wait_bar(bar(B_VF + s), u, abort, p)) return false;
-                if (first && item > 0 && !wait_bar(bar(B_OE), (item - 1u) & 1u, abort, p)) return false;
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (!wait_bar(bar(B_PF + 2 * s + hh), u, abort, p)) return false;
-                    ptx::tc_fence_after();
-                    const uint32_t d_o = tmem + 256u + (uint32_t)(hh * 128);
-                    const uint32_t a_p = tmem + (uint32_t)(s * 128 + hh * 64);
+            // S_t = Q_t . K_g^T (K slot g & 1)
+            auto qk = [&](uint32_t g, int t) -> bool {
+                const int s = (int)(g & 1u);
+                if (t == 0 && !wait_bar(bar(B_KF + s), (g >> 1) & 1u, abort, p)) return false;
+                // the tile's score buffer holds P(g-1) until P.V(g-1) has read it
+                if (g > 0 && !wait_bar(bar(B_PV + t), (g - 1u) & 1u, abort, p)) return false;
+                ptx::tc_fence_after();
+                const uint32_t d_s = tmem + (uint32_t)(t * 128);
+                const uint32_t q_t = sQ + (uint32_t)(t * kTileBytes);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        ptx::umma_bf16_ts(d_o, a_p + (uint32_t)(kk * 8), mnmajor_desc(sV + s * kTileBytes, 4 * hh + kk),
-                                          IDESC_PV, (kk != 0 || !first) ? 1u : 0u);
-                    ptx::umma_commit(bar(B_PE + 2 * s + hh));  // half hh's P read, O_hh updated
-                }
-                ptx::umma_commit(bar(B_VE + s));
-                ptx::umma_commit(bar(B_SE + s));  // the score buffer (and the P in it) is free
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    ptx::umma_bf16(d_s, kmajor_desc(q_t, kk), kmajor_desc(sK + s * kTileBytes, kk), IDESC_QK,
+                                   kk != 0 ? 1u : 0u);
+                ptx::umma_commit(bar(B_SF + t));
+                if (t == kTiles - 1) ptx::umma_commit(bar(B_KE + s));
+                return true;
+            };
+            // O_t (+)= P_t . V_g, P_t from TMEM (8 columns per 16 keys); an item's
+            // first product overwrites O_t once the previous item (`item` - 1)
+            // has been read out
+            auto pv = [&](uint32_t g, int t, bool first, uint32_t item) -> bool {
+                const int s = (int)(g & 1u);
+                if (!wait_bar(bar(B_PF + t), g & 1u, abort, p)) return false;
+                if (t == 0 && !wait_bar(bar(B_VF + s), (g >> 1) & 1u, abort, p)) return false;
+                if (first && item > 0 && !wait_bar(bar(B_OE + t), (item - 1u) & 1u, abort, p)) return false;
+                ptx::tc_fence_after();
+                const uint32_t d_o = tmem + 256u + (uint32_t)(t * 128);
+                const uint32_t a_p = tmem + (uint32_t)(t * 128);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    ptx::umma_bf16_ts(d_o, a_p + (uint32_t)(kk * 8), mnmajor_desc(sV + s * kTileBytes, kk), IDESC_PV,
+                                      (kk != 0 || !first) ? 1u : 0u);
+                ptx::umma_commit(bar(B_PV + t));
+                if (t == kTiles - 1) ptx::umma_commit(bar(B_VE + s));
                 return true;
             };
             Walk wk;
             wk.init(p);
-            Blk b;
-            uint32_t g = 0, ic = 0;
-            bool ok = true, prev_first = false;
-            for (; wk.next(p, b); ++g) {
-                if (b.first) {
+            Blk cur, nxt;
+            bool ok = true, has = wk.next(p, cur);
+            uint32_t g = 0, ic = 0, item_cur = 0;
+            if (has) {  // prologue: the first block's Q.K^T for both tiles
+                ok = wait_bar(bar(B_QF), 0u, abort, p);
+                ic = 1;
+                for (int t = 0; ok && t < kTiles; ++t) ok = qk(0, t);
+                if (ok && cur.last) ptx::umma_commit(bar(B_QE));
+            }
+            while (ok && has) {
+                const bool has_next = wk.next(p, nxt);
+                if (has_next && nxt.first) {  // a new item: its Q tiles
                     if (!wait_bar(bar(B_QF), ic & 1u, abort, p)) {
                         ok = false;
                         break;
                     }
                     ++ic;
                 }
-                const int s = (int)(g & 1u);
-                const uint32_t ph = (g >> 1) & 1u;
-                if (!wait_bar(bar(B_KF + s), ph, abort, p) || !wait_bar(bar(B_SE + s), ph ^ 1u, abort, p)) {
-                    ok = false;
-                    break;
+                for (int t = 0; ok && t < kTiles; ++t) {
+                    ok = pv(g, t, cur.first, item_cur);
+                    if (ok && has_next) ok = qk(g + 1u, t);
                 }
-                ptx::tc_fence_after();
-                const uint32_t d_s = tmem + (uint32_t)(s * 128);
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
-                    ptx::umma_bf16(d_s, kmajor_desc(sQ, kk), kmajor_desc(sK + s * kTileBytes, kk), IDESC_QK,
-                                   kk != 0 ? 1u : 0u);
-                ptx::umma_commit(bar(B_SF + s));
-                ptx::umma_commit(bar(B_KE + s));
-                if (b.last) ptx::umma_commit(bar(B_QE));  // the item's Q tile is no longer read
-                // the previous block's product (its item started `ic - 1` or `ic - 2` items in)
-                if (g > 0 && !pv(g - 1u, prev_first, b.first ? ic - 2u : ic - 1u)) {
-                    ok = false;
-                    break;
-                }
-                prev_first = b.first;
+                if (!ok) break;
+                if (has_next && nxt.last) ptx::umma_commit(bar(B_QE));  // the item's Q tiles are no longer read
+                if (has_next && nxt.first) ++item_cur;
+                cur = nxt;
+                has = has_next;
+                ++g;
             }
-            if (ok && g > 0) pv(g - 1u, prev_first, ic - 1u);
             // every MMA issued must complete before TMEM is released
             ptx::umma_commit(bar(B_DRAIN));
             drain_bar(bar(B_DRAIN), 0, p);
         }
-    } else if (warp < 4) {
+    } else {
         // ================= stagers =================
         if (p.stage) stage_chunks(p, (int)blockIdx.x * 2 + (warp - 2), (int)gridDim.x * 2, lane);
+    }
     } else {
-        // ================= softmax halves, output rescaling, epilogue =================
-        const int hx = (warp - 4) >> 2;  // key half: 0 = A (keys 0-63), 1 = B (keys 64-127)
+        regs_inc();
+        // ================= softmax of tile t, output rescaling, epilogue =================
+        const int t = (warp - 4) >> 2;
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
-        const uint32_t to = tl + 256u + (uint32_t)(hx * 128);  // this half's output accumulator
-        float2 *stats = reinterpret_cast<float2 *>(sm + OFF_STATS);
+        const uint32_t ts = tl + (uint32_t)(t * 128);         // the tile's scores (then probabilities)
+        const uint32_t to = tl + 256u + (uint32_t)(t * 128);  // the tile's output accumulator
         float mref = -INFINITY, lrow = 0.f;  // reference max (log2-scaled units), running sum
-        uint32_t items = 0;
-        // this half's P.V of block i done (P buffer i&1 read, O_h updated)
-        auto pv_done = [&](uint32_t i) {
-            const bool w = wait_bar(bar(B_PE + 2 * (int)(i & 1u) + hx), (i >> 1) & 1u, abort, p);
-            return __all_sync(0xffffffffu, w);
-        };
         Walk wk;
         wk.init(p);
         Blk b;
@@ -606,31 +611,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
                 mref = -INFINITY;
                 lrow = 0.f;
             }
-            const int s = (int)(g & 1u);
-            bool w = wait_bar(bar(B_SF + s), (g >> 1) & 1u, abort, p);
+            bool w = wait_bar(bar(B_SF + t), g & 1u, abort, p);
             if (!__all_sync(0xffffffffu, w)) break;
             ptx::tc_fence_after();
-            const int qpos0 = p.q_pos0 + b.q_row0;                    // the tile's first query position
+            const int qrow = b.q_row0 + t * kBQ;                      // the tile's first query row
+            const int qpos0 = p.q_pos0 + qrow;                        // its global position
             const int qpos = qpos0 + row;                             // this row's
-            const int k0 = b.kv0 + hx * 64;                           // this half's first key
-            const bool masked = p.causal && k0 + 63 > qpos0;          // the half-block crosses the diagonal
-            const uint32_t ts = tl + (uint32_t)(s * 128 + hx * 64);
-            uint32_t v[64];
-            ptx::tmem_ld_32x32b_x32(ts, *reinterpret_cast<uint32_t(*)[32]>(v));
-            ptx::tmem_ld_32x32b_x32(ts + 32u, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            const bool masked = p.causal && b.kv0 + kBK - 1 > qpos0;  // the block crosses the diagonal
+            uint32_t v[kBK];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                ptx::tmem_ld_32x32b_x32(ts + (uint32_t)(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
             ptx::tmem_ld_wait();
             if (masked) {
 #pragma unroll
-                for (int t = 0; t < 64; ++t)
-                    if (k0 + t > qpos) v[t] = __float_as_uint(-INFINITY);
+                for (int k = 0; k < kBK; ++k)
+                    if (b.kv0 + k > qpos) v[k] = __float_as_uint(-INFINITY);
             }
-            // row max and (below) row sum as eight interleaved partials: short
-            // dependency chains instead of one of 64
             float mp[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) mp[k] = __uint_as_float(v[k]);
 #pragma unroll
-            for (int t = 8; t < 64; ++t) mp[t & 7] = fmaxf(mp[t & 7], __uint_as_float(v[t]));
+            for (int k = 8; k < kBK; ++k) mp[k & 7] = fmaxf(mp[k & 7], __uint_as_float(v[k]));
             const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
             const float mcand = mx * p.scale_log2;  // (scale > 0: the max commutes with it)
@@ -638,64 +640,49 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             const bool need = !b.first && mcand > mref + kRescale;
             const float alpha = need ? ex2(mref - mcand) : 1.f;
             if (b.first || need) mref = mcand;
-            const float base = mref == -INFINITY ? 0.f : mref;
-            float sp[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) sp[k] = 0.f;
-            uint32_t pk[32];
-#pragma unroll
-            for (int t = 0; t < 64; t += 2) {
-                const float p0 = ex2(fmaf(__uint_as_float(v[t]), p.scale_log2, -base));
-                const float p1 = ex2(fmaf(__uint_as_float(v[t + 1]), p.scale_log2, -base));
-                sp[(t >> 1) & 7] += p0 + p1;
-                pk[t >> 1] = pack_bf16(p0, p1);
-            }
-            const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-            lrow = lrow * alpha + sum;
             if (__any_sync(0xffffffffu, need)) {
-                // rescale this half's accumulator between P.V of the previous block
-                // and of this one
-                if (!pv_done(g - 1u)) break;
-                ptx::tc_fence_after();
+                // P.V(g-1) completed before this block's Q.K^T could overwrite the
+                // scores, so the accumulator is stable: rescale it
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
                     ptx::tmem_ld_32x32b_x32(to + (uint32_t)(c * 32), o);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
                     ptx::tmem_st_32x32b_x32(to + (uint32_t)(c * 32), o);
                 }
-                ptx::tmem_st_wait();
-                ptx::tc_fence_before();
             }
-            // P (bf16 pairs) over this half's first 32 score columns, which it has read
-            ptx::tmem_st_32x32b_x32(ts, pk);
+            const float base = mref == -INFINITY ? 0.f : mref;
+            float sp[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sp[k] = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {  // probabilities of 64 keys, as bf16 pairs in 32 columns
+                uint32_t pk[32];
+#pragma unroll
+                for (int k = 0; k < 64; k += 2) {
+                    const float p0 = ex2(fmaf(__uint_as_float(v[hh * 64 + k]), p.scale_log2, -base));
+                    const float p1 = ex2(fmaf(__uint_as_float(v[hh * 64 + k + 1]), p.scale_log2, -base));
+                    sp[(k >> 1) & 7] += p0 + p1;
+                    pk[k >> 1] = pack_bf16(p0, p1);
+                }
+                ptx::tmem_st_32x32b_x32(ts + (uint32_t)(hh * 32), pk);
+            }
+            const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+            lrow = lrow * alpha + sum;
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(B_PF + 2 * s + hx));
-            if (b.last) {  // the item's output, after this half's last P.V
-                if (!pv_done(g)) break;
+            if (lane == 0) ptx::mbar_arrive(bar(B_PF + t));
+            if (b.last) {  // the item's output, after the tile's last P.V
+                w = wait_bar(bar(B_PV + t), g & 1u, abort, p);
+                if (!__all_sync(0xffffffffu, w)) break;
                 ptx::tc_fence_after();
-                if (hx == 1) {
-                    stats[row] = make_float2(mref, lrow);
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bar(B_BDONE));  // (release: the stats stores before it)
-                } else {
-                    w = wait_bar(bar(B_BDONE), items & 1u, abort, p);
-                    if (!__all_sync(0xffffffffu, w)) break;
-                    const float2 sb = stats[row];
-                    const float m = fmaxf(mref, sb.x);
-                    const float fa = mref == -INFINITY ? 0.f : ex2(mref - m);
-                    const float fb = sb.x == -INFINITY ? 0.f : ex2(sb.x - m);
-                    const float l = lrow * fa + sb.y * fb;
-                    store_merged(p, to, to + 128u, fa, fb, m, l, b.h, b.q_row0, row);
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bar(B_OE));
-                }
-                ++items;
+                store_row(p, to, mref, lrow, b.h, qrow + row);
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(B_OE + t));
             }
         }
     }
@@ -752,7 +739,7 @@ int syn_attn_cfg_default(syn_attn_cfg_t *c) {
     if (c == nullptr) return host_fail(SYN_ERR_INVALID, "null cfg");
     std::memset(c, 0, sizeof(*c));
     c->R = 1;
-    c->S_r = 128;
+    c->S_r = 256;
     c->H_q = c->H_kv = 1;
     c->d = 128;
     c->split = 1;
@@ -770,7 +757,8 @@ int syn_attn_plan_create(syn_attn_plan_t *out, const syn_attn_cfg_t *cfg) {
     if (c.R < 1 || c.rank < 0 || c.rank >= c.R) return host_fail(SYN_ERR_INVALID, "need 0 <= rank < R");
     if (c.R > 8) return host_fail(SYN_ERR_UNSUPPORTED, "R > 8");
     if (c.d != kD) return host_fail(SYN_ERR_UNSUPPORTED, "head dimension must be 128");
-    if (c.S_r < kBQ || c.S_r % kBQ != 0) return host_fail(SYN_ERR_UNSUPPORTED, "S_r must be a positive multiple of 128");
+    if (c.S_r < kTiles * kBQ || c.S_r % (kTiles * kBQ) != 0)
+        return host_fail(SYN_ERR_UNSUPPORTED, "S_r must be a positive multiple of 256");
     if (c.S_r > (1 << 20)) return host_fail(SYN_ERR_UNSUPPORTED, "S_r > 2^20");
     if (c.H_q < 1 || c.H_kv < 1 || c.H_q % c.H_kv != 0) return host_fail(SYN_ERR_INVALID, "need H_q % H_kv == 0");
     if (c.H_q > 1024) return host_fail(SYN_ERR_UNSUPPORTED, "H_q > 1024");
@@ -808,7 +796,7 @@ int syn_attn_plan_create(syn_attn_plan_t *out, const syn_attn_cfg_t *cfg) {
     if (per_sm < 1) return bail(SYN_ERR_UNSUPPORTED, "the attention kernel cannot be resident");
     // persistent: one CTA per SM (all co-resident: a cooperative launch), at
     // most one per work item
-    pl->grid = std::min(pl->n_qtiles * (c.head_parallel ? c.H_q / c.R : c.H_q), pl->num_sms * per_sm);
+    pl->grid = std::min(pl->n_qtiles / kTiles * (c.head_parallel ? c.H_q / c.R : c.H_q), pl->num_sms * per_sm);
     const size_t nf = (size_t)c.R * c.split;
     PL_CK(cudaMalloc(&pl->d_flags, nf * sizeof(uint32_t)));
     PL_CK(cudaMemset(pl->d_flags, 0, nf * sizeof(uint32_t)));
@@ -882,8 +870,8 @@ int attn_call(syn_attn_plan_s *pl, bool head, const void *Q, const void *const *
     p.G = hq / hkv;
     p.causal = c.causal;
     p.split = c.split;
-    p.n_qtiles = pl->n_qtiles;
-    p.n_items = pl->n_qtiles * hq;
+    p.n_qtiles = pl->n_qtiles / kTiles;  // (the kernel's items per head: tile pairs)
+    p.n_items = p.n_qtiles * hq;
     p.head_mode = head ? 1 : 0;
     p.q_pos0 = head ? 0 : c.rank * (int32_t)c.S_r;
     p.local_inplace = inplace ? 1 : 0;

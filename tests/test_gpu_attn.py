@@ -105,7 +105,7 @@ def test_tiny_causal(r, split):
 
 @pytest.mark.parametrize("H_q,H_kv", [(2, 2), (8, 1), (6, 3)])
 def test_head_groupings(H_q, H_kv):
-    w = wl.AttnWorkload("heads", 2, 384, H_q, H_kv)
+    w = wl.AttnWorkload("heads", 2, 512, H_q, H_kv)
     inp, got = run(w, 1, split=3)
     check(w, 1, inp, got)
 
@@ -146,7 +146,7 @@ def test_dropped_chunk_times_out_then_recovers():
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(S_r=200), syn.ERR_UNSUPPORTED), (dict(d=64), syn.ERR_UNSUPPORTED), (dict(H_q=3, H_kv=2), syn.ERR_INVALID),
+    (dict(S_r=200), syn.ERR_UNSUPPORTED), (dict(S_r=384), syn.ERR_UNSUPPORTED), (dict(d=64), syn.ERR_UNSUPPORTED), (dict(H_q=3, H_kv=2), syn.ERR_INVALID),
     (dict(split=3, S_r=256), syn.ERR_INVALID), (dict(backend="ce"), syn.ERR_UNSUPPORTED),
     (dict(R=2, rank=2), syn.ERR_INVALID)])
 def test_invalid_configurations_rejected(kw, status):
@@ -215,7 +215,7 @@ def test_head_parallel_tiny(r, split, causal):
 
 
 def test_head_parallel_unfused_and_repeated_calls():
-    w = wl.AttnWorkload("tiny-head-gqa", 2, 384, 8, 2, causal=True)
+    w = wl.AttnWorkload("tiny-head-gqa", 2, 512, 8, 2, causal=True)
     inp, got = run_head(w, 1, split=3, backend="unfused")
     check_head(w, 1, inp, got)
     inp, got = run_head(w, 0, split=3, calls=3)
