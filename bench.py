@@ -528,8 +528,10 @@ def run_sweep(args):
         for order in ("row", "grouped", "col"):
             points.append(dict(backend="ce", split=split, order=order, tile_m=256))
             points.append(dict(backend="tma_colocated", split=split, order=order, tile_m=256))
+            points.append(dict(backend="ldst_colocated", split=split, order=order, tile_m=256))
         for cs in (4, 8, 16):
             points.append(dict(backend="tma_dedicated", split=split, order="row", comm_sms=cs, tile_m=256))
+            points.append(dict(backend="ldst_dedicated", split=split, order="row", comm_sms=cs, tile_m=256))
     for pt in points:
         kn = dict(pt)
         split, order = kn.pop("split"), kn.pop("order")

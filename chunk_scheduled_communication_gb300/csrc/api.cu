@@ -11,6 +11,8 @@
 //                 stream
 //   TMA_DEDICATED comm_sms extra CTAs of the same cooperative grid copy chunks
 //   TMA_COLOCATED a staging warp in every GEMM CTA copies chunk slices
+//   LDST_DEDICATED / LDST_COLOCATED  the same placements, copying with warp-wide
+//                 16-byte vector loads and stores instead of TMA bulk copies
 //   TMA_COLOCATED_SMEM  GEMM-RS/AR: peers fetched per tile into shared memory
 //   UNFUSED       whole staging copy, then the same kernel without waits
 //   DECOMPOSED    one kernel launch per chunk group after its copies (the
@@ -296,7 +298,8 @@ cudaError_t launch(syn_plan_s *pl, const KernelParams &p, int grid, cudaStream_t
     // kernel waits for that grid before it touches global memory)
     const int be = pl->kn.backend;
     lc.overlap_prev = lc.pair && (be == SYN_BACKEND_TMA_DEDICATED || be == SYN_BACKEND_TMA_COLOCATED ||
-                                  be == SYN_BACKEND_TMA_COLOCATED_SMEM);
+                                  be == SYN_BACKEND_TMA_COLOCATED_SMEM || be == SYN_BACKEND_LDST_DEDICATED ||
+                                  be == SYN_BACKEND_LDST_COLOCATED);
     switch (pl->s.op) {
         case SYN_OP_AG_GEMM: return launch_fused_ag(p, pl->maps, lc, st);
         case SYN_OP_GEMM_RS: return launch_fused_rs(p, pl->maps, lc, st);
@@ -352,11 +355,15 @@ int run(syn_plan_s *pl, KernelParams &p, cudaStream_t st) {
             }
             return SYN_OK;
         }
+        case SYN_BACKEND_LDST_DEDICATED:
         case SYN_BACKEND_TMA_DEDICATED:
+            p.ldst = be == SYN_BACKEND_LDST_DEDICATED ? 1 : 0;
             p.n_comm = pl->grid_comm;
             SYN_CK(launch(pl, p, pl->grid_compute + pl->grid_comm, st));
             return SYN_OK;
+        case SYN_BACKEND_LDST_COLOCATED:
         case SYN_BACKEND_TMA_COLOCATED:
+            p.ldst = be == SYN_BACKEND_LDST_COLOCATED ? 1 : 0;
             p.colocated = 1;
             SYN_CK(launch(pl, p, pl->grid_compute, st));
             return SYN_OK;
@@ -463,11 +470,12 @@ int plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_layout_
     int rc = load_driver();
     if (rc != SYN_OK) return rc;
     const syn_knobs_t kn = resolve_knobs(knobs);
-    if (kn.backend < SYN_BACKEND_CE || kn.backend > SYN_BACKEND_DECOMPOSED)
+    if (kn.backend < SYN_BACKEND_CE || kn.backend > SYN_BACKEND_LDST_COLOCATED)
         return fail(SYN_ERR_INVALID, "unknown backend");
     if (kn.backend == SYN_BACKEND_TMA_COLOCATED_SMEM && op == SYN_OP_AG_GEMM)
         return fail(SYN_ERR_UNSUPPORTED, "TMA_COLOCATED_SMEM applies to GEMM-RS/AR only");
-    if (kn.backend == SYN_BACKEND_TMA_DEDICATED && (kn.comm_sms < 1 || kn.comm_sms > 32))
+    const bool dedicated = kn.backend == SYN_BACKEND_TMA_DEDICATED || kn.backend == SYN_BACKEND_LDST_DEDICATED;
+    if (dedicated && (kn.comm_sms < 1 || kn.comm_sms > 32))
         return fail(SYN_ERR_INVALID, "comm_sms must be in [1, 32]");
 
     syn_plan_s *pl = new syn_plan_s();
@@ -522,7 +530,7 @@ int plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_layout_
         pl->resident = std::min(pl->num_sms, 2 * nc);
     }
     const int cta_per_tile = pl->lc.pair ? 2 : 1;
-    if (kn.backend == SYN_BACKEND_TMA_DEDICATED) {
+    if (dedicated) {
         pl->grid_comm = pl->lc.pair ? (kn.comm_sms + 1) / 2 * 2 : kn.comm_sms;
         if (pl->grid_comm >= pl->resident) return bail(SYN_ERR_INVALID, "comm_sms >= resident CTAs");
         pl->grid_compute = std::min(s.n_tiles, (pl->resident - pl->grid_comm) / cta_per_tile) * cta_per_tile;

@@ -441,6 +441,60 @@ __device__ __forceinline__ void stage_slices(const KernelParams &p, int worker, 
     land_pending();
 }
 
+// Load/store staging (the pages' load/store lowerings): warp `worker` of `W`
+// copies slices worker, worker + W, ... with every lane moving 16-byte
+// vectors (eight in flight per lane); after a slice lane 0 fences, counts it,
+// and the warp that completes a transfer publishes its flag (release).
+__device__ __forceinline__ void stage_slices_ldst(const KernelParams &p, int worker, int W, int lane,
+                                                  volatile int *abort) {
+    const int spt = p.slices_per_transfer;
+    const int total = p.n_transfers * spt;
+    const int n_flags = p.n_rc * p.R;
+    uint32_t *cnt = p.in_cnt + (size_t)counter_half(p.epoch) * n_flags;
+    for (int g = worker; g < total; g += W) {
+        if (*abort) return;
+        const int a = g / spt, sl = g % spt;
+        const int code = p.transfers[a];
+        if (code < 0 || code >= n_flags) {  // the transfer table holds a code outside the flags
+            if (lane == 0) {
+                raise_error(p, SYN_ERR_BOUNDS, WHERE_BOUNDS, a);
+                *abort = 1;
+            }
+            return;
+        }
+        if (p.op == OP_AG && p.local_inplace && code % p.R == p.rank) continue;
+        const uint8_t *src;
+        uint8_t *dst;
+        int64_t bytes;
+        transfer_span(p, code, src, dst, bytes);
+        const int64_t off = (int64_t)sl * p.slice_bytes;
+        const int64_t len = bytes - off < p.slice_bytes ? bytes - off : p.slice_bytes;
+        // (slices past the end of a shorter chunk copy nothing but still count)
+        for (int64_t b = (int64_t)lane * 16; b < len; b += 32 * 16 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (b + u * 512 < len) v[u] = __ldcs(reinterpret_cast<const uint4 *>(src + off + b + u * 512));
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (b + u * 512 < len) *reinterpret_cast<uint4 *>(dst + off + b + u * 512) = v[u];
+        }
+        __syncwarp();
+        if (lane == 0) {
+            ptx::fence_acq_rel_gpu();  // the warp's stores, observed through the barrier, before the count
+            const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + code, 1u);
+            if (completes_transfer(old, (uint32_t)spt) && a != p.drop_transfer) {
+                if (a == p.delay_transfer) {  // fault injection: publish late (bounded by the delay)
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (ptx::globaltimer() - t0 < p.delay_ns && !*abort) __nanosleep(1000);
+                }
+                ptx::st_release_gpu(p.in_flags + code, p.epoch);
+            }
+        }
+        __syncwarp();
+    }
+}
+
 // ------------------------------------------------------------------ epilogue helpers
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -618,7 +672,10 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
             ptx::fence_proxy_async_smem();
         }
         __syncthreads();
-        if ((int)threadIdx.x < C::COMM_NBUF) {
+        if (p.ldst) {  // every warp copies with vector loads and stores
+            constexpr int NW = C::NTHREADS / 32;
+            stage_slices_ldst(p, ((int)blockIdx.x - p.G) * NW + warp, p.n_comm * NW, lane, abort);
+        } else if ((int)threadIdx.x < C::COMM_NBUF) {
             const int c = (int)threadIdx.x;
             stage_slices(p, ((int)blockIdx.x - p.G) * C::COMM_NBUF + c, p.n_comm * C::COMM_NBUF,
                          sbase + c * C::COMM_BUF_BYTES, 1, C::COMM_BUF_BYTES, bar0 + 8 * c, abort);
@@ -1101,6 +1158,7 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
         }
     } else if (warp == 7) {
         // ================= co-located stager =================
+        if (p.colocated && p.ldst) stage_slices_ldst(p, (int)blockIdx.x, p.G, lane, abort);
         if constexpr (C::NSTG > 0)
             // one copier per CTA, double-buffered: with one worker per GEMM CTA the
             // first round of slices covers only the earliest chunks in arrival order

@@ -43,6 +43,7 @@ struct TensorMaps {  // CUtensorMap carries its own alignment
 struct KernelParams {
     int32_t op, R, rank;
     int32_t M, N, K, M_r, cr, split, n_rc;  // cr: rows of the largest chunk
+    int32_t ldst;                  // staging copies by warps with vector loads/stores
     RowBlocks rb;                  // row blocks and chunk geometry
     int32_t tiles_m, tiles_n;
     int32_t t_begin, t_end;        // range of tile_list this launch runs

@@ -122,7 +122,8 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
 
     // ---- candidate space ---------------------------------------------------------
     std::vector<syn_backend_t> backends = {SYN_BACKEND_CE, SYN_BACKEND_TMA_DEDICATED,
-                                           SYN_BACKEND_TMA_COLOCATED};
+                                           SYN_BACKEND_TMA_COLOCATED, SYN_BACKEND_LDST_DEDICATED,
+                                           SYN_BACKEND_LDST_COLOCATED};
     if (op != SYN_OP_AG_GEMM) backends.push_back(SYN_BACKEND_TMA_COLOCATED_SMEM);
     const int comm_opts[] = {4, 8, 16};
     const int split_opts[] = {1, 2, 3, 4, 6, 8};
@@ -136,7 +137,8 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
         if (L.N % tn) continue;
         if (op == SYN_OP_GEMM_RS && M_r % tm) continue;
         for (syn_backend_t be : backends)
-            for (int ci = 0; ci < (be == SYN_BACKEND_TMA_DEDICATED ? 3 : 1); ++ci)
+            for (int ci = 0;
+                 ci < ((be == SYN_BACKEND_TMA_DEDICATED || be == SYN_BACKEND_LDST_DEDICATED) ? 3 : 1); ++ci)
                 for (int sp : split_opts) {
                     if (sp > M_r) continue;
                     for (syn_order_t od : order_opts) {

@@ -22,10 +22,11 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS = 0, -1, -2,
 OP_AG_GEMM, OP_GEMM_RS, OP_GEMM_AR = 0, 1, 2
 ORDER_ROW_MAJOR, ORDER_COL_MAJOR, ORDER_GROUPED, ORDER_BANDED = 0, 1, 2, 3
 (BACKEND_CE, BACKEND_TMA_DEDICATED, BACKEND_TMA_COLOCATED, BACKEND_TMA_COLOCATED_SMEM,
- BACKEND_UNFUSED, BACKEND_DECOMPOSED) = range(6)
+ BACKEND_UNFUSED, BACKEND_DECOMPOSED, BACKEND_LDST_DEDICATED, BACKEND_LDST_COLOCATED) = range(8)
 BACKEND_NAMES = {BACKEND_CE: "ce", BACKEND_TMA_DEDICATED: "tma_dedicated",
                  BACKEND_TMA_COLOCATED: "tma_colocated", BACKEND_TMA_COLOCATED_SMEM: "tma_colocated_smem",
-                 BACKEND_UNFUSED: "unfused", BACKEND_DECOMPOSED: "decomposed"}
+                 BACKEND_UNFUSED: "unfused", BACKEND_DECOMPOSED: "decomposed",
+                 BACKEND_LDST_DEDICATED: "ldst_dedicated", BACKEND_LDST_COLOCATED: "ldst_colocated"}
 BACKENDS = {v: k for k, v in BACKEND_NAMES.items()}
 ORDERS = {"row": ORDER_ROW_MAJOR, "col": ORDER_COL_MAJOR, "grouped": ORDER_GROUPED, "banded": ORDER_BANDED}
 OPS = {"ag": OP_AG_GEMM, "rs": OP_GEMM_RS, "ar": OP_GEMM_AR}

@@ -100,8 +100,15 @@ typedef enum {
                                        of peer tiles in the epilogue            */
     SYN_BACKEND_UNFUSED = 4,        /* baseline: whole staging copy first, then
                                        the same GEMM kernel without waits         */
-    SYN_BACKEND_DECOMPOSED = 5      /* baseline: one GEMM launch per chunk group,
+    SYN_BACKEND_DECOMPOSED = 5,     /* baseline: one GEMM launch per chunk group,
                                        each after its chunks' copies (Fig. 2(b)) */
+    SYN_BACKEND_LDST_DEDICATED = 6, /* as TMA_DEDICATED, but every warp of the
+                                       staging CTAs copies slices with 16-byte
+                                       vector loads and stores                   */
+    SYN_BACKEND_LDST_COLOCATED = 7  /* one warp of every GEMM CTA copies slices
+                                       with 16-byte vector loads and stores (no
+                                       shared-memory staging buffers, so the
+                                       GEMM keeps its deepest pipeline)          */
 } syn_backend_t;
 
 /* Shapes.  M = rows of the gathered / full output space (all ranks),

@@ -18,7 +18,8 @@ from chunk_scheduled_communication_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-BACKENDS = ["ce", "tma_dedicated", "tma_colocated", "unfused", "decomposed"]
+BACKENDS = ["ce", "tma_dedicated", "tma_colocated", "unfused", "decomposed", "ldst_dedicated",
+            "ldst_colocated"]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -20,7 +20,8 @@ from chunk_scheduled_communication_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-DEV_BACKENDS = ["ce", "tma_dedicated", "tma_colocated", "unfused", "decomposed"]
+DEV_BACKENDS = ["ce", "tma_dedicated", "tma_colocated", "unfused", "decomposed", "ldst_dedicated",
+                "ldst_colocated"]
 RSAR_BACKENDS = DEV_BACKENDS + ["tma_colocated_smem"]
 
 
@@ -116,7 +117,7 @@ INT_AR = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=2 * 333, K=128, N=384, R=2)  # M tail
 
 
 @pytest.mark.parametrize("w", [INT_AG, INT_RS, INT_AR], ids=["ag", "rs", "ar"])
-@pytest.mark.parametrize("backend", ["ce", "tma_dedicated", "tma_colocated"])
+@pytest.mark.parametrize("backend", ["ce", "tma_dedicated", "tma_colocated", "ldst_dedicated", "ldst_colocated"])
 def test_integer_inputs_bit_exact(w, backend):
     for r in (0, w.R - 1):
         got = run(w, r, backend=backend, kind="int", comm_sms=3)
@@ -391,16 +392,19 @@ INT_AR_PAIR = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=2 * 333, K=128, N=512, R=2)
     (INT_AG_PAIR, "tma_colocated", 6), (INT_AG_PAIR, "tma_colocated", 5), (INT_AG_PAIR, "tma_colocated", 4),
     (INT_AG_PAIR, "ce", 7),
     (INT_AG_PAIR, "ce", 5), (INT_AG_PAIR, "tma_dedicated", 7), (INT_AG_PAIR, "unfused", 7),
-    (INT_AG_PAIR, "decomposed", 7),
+    (INT_AG_PAIR, "decomposed", 7), (INT_AG_PAIR, "ldst_colocated", 7), (INT_AG_PAIR, "ldst_colocated", 5),
+    (INT_AG_PAIR, "ldst_dedicated", 7),
     (INT_RS_PAIR, "smem_ring", 3), (INT_RS_PAIR, "smem_ring", 4),
     (INT_RS_PAIR, "smem_ring", 5), (INT_RS_PAIR, "smem_ring", 6),
     (INT_RS_PAIR, "tma_colocated_smem", 4), (INT_RS_PAIR, "tma_colocated_smem", 5),
     (INT_RS_PAIR, "tma_colocated_smem", 6), (INT_RS_PAIR, "tma_colocated_smem", 7),
-    (INT_RS_PAIR, "tma_colocated", 4), (INT_RS_PAIR, "ce", 4),
+    (INT_RS_PAIR, "tma_colocated", 4), (INT_RS_PAIR, "ce", 4), (INT_RS_PAIR, "ldst_colocated", 4),
+    (INT_RS_PAIR, "ldst_dedicated", 4),
     (INT_AR_PAIR, "smem_ring", 4), (INT_AR_PAIR, "smem_ring", 6),
     (INT_AR_PAIR, "tma_colocated_smem", 4), (INT_AR_PAIR, "tma_colocated_smem", 5),
     (INT_AR_PAIR, "tma_colocated_smem", 6), (INT_AR_PAIR, "tma_colocated_smem", 7),
-    (INT_AR_PAIR, "tma_colocated", 4), (INT_AR_PAIR, "ce", 3),
+    (INT_AR_PAIR, "tma_colocated", 4), (INT_AR_PAIR, "ce", 3), (INT_AR_PAIR, "ldst_colocated", 3),
+    (INT_AR_PAIR, "ldst_dedicated", 3),
 ], ids=lambda v: str(getattr(v, "op", v)))
 def test_cta_pair_instances_bit_exact(w, backend, stages):
     """256-row tiles shared by a CTA pair (2-CTA UMMA) give the oracle's bits
