@@ -369,6 +369,32 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Packed fp32 pairs (f32x2 arithmetic: one instruction for two lanes of work)
+// and a three-input max.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unf2(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -628,11 +654,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
                 for (int k = 0; k < kBK; ++k)
                     if (b.kv0 + k > qpos) v[k] = __float_as_uint(-INFINITY);
             }
+            // row max: eight interleaved partials, two new scores per three-input max
             float mp[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) mp[k] = __uint_as_float(v[k]);
 #pragma unroll
-            for (int k = 8; k < kBK; ++k) mp[k & 7] = fmaxf(mp[k & 7], __uint_as_float(v[k]));
+            for (int k = 8; k < kBK; k += 2)
+                mp[(k >> 1) & 7] = max3(mp[(k >> 1) & 7], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
             const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
             const float mcand = mx * p.scale_log2;  // (scale > 0: the max commutes with it)
@@ -654,22 +682,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
                 }
             }
             const float base = mref == -INFINITY ? 0.f : mref;
-            float sp[8];
+            // probabilities: the exponent arguments and the running sums two keys at
+            // a time (f32x2), four interleaved pair-sums
+            const uint64_t scale2 = f2(p.scale_log2, p.scale_log2), nbase2 = f2(-base, -base);
+            uint64_t sp[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) sp[k] = 0.f;
+            for (int k = 0; k < 4; ++k) sp[k] = f2(0.f, 0.f);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {  // probabilities of 64 keys, as bf16 pairs in 32 columns
                 uint32_t pk[32];
 #pragma unroll
                 for (int k = 0; k < 64; k += 2) {
-                    const float p0 = ex2(fmaf(__uint_as_float(v[hh * 64 + k]), p.scale_log2, -base));
-                    const float p1 = ex2(fmaf(__uint_as_float(v[hh * 64 + k + 1]), p.scale_log2, -base));
-                    sp[(k >> 1) & 7] += p0 + p1;
+                    float x0, x1;
+                    unf2(fma2(f2(__uint_as_float(v[hh * 64 + k]), __uint_as_float(v[hh * 64 + k + 1])), scale2, nbase2),
+                         x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    sp[(k >> 1) & 3] = add2(sp[(k >> 1) & 3], f2(p0, p1));
                     pk[k >> 1] = pack_bf16(p0, p1);
                 }
                 ptx::tmem_st_32x32b_x32(ts + (uint32_t)(hh * 32), pk);
             }
-            const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+            float s0, s1, s2, s3, s4, s5, s6, s7;
+            unf2(sp[0], s0, s1);
+            unf2(sp[1], s2, s3);
+            unf2(sp[2], s4, s5);
+            unf2(sp[3], s6, s7);
+            const float sum = ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
             lrow = lrow * alpha + sum;
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
