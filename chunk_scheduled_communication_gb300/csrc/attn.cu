@@ -4,34 +4,29 @@
 //
 // Syncopate summary page, Experiments (paper §6.1: head-/sequence-parallel
 // attention and RingAttention) and method ¶2-¶4 (a tile waits only for the
-// chunks it reads; tiles follow the communication order).  One CTA computes
-// one 128-row query tile of one head on the tensor cores:
+// chunks it reads; tiles follow the communication order).  A persistent CTA
+// (one per SM, a cooperative launch) takes work items of one head and two
+// 128-row query tiles (t = 0, 1) in turn and computes them on the tensor
+// cores, KV block by KV block (128 keys) in chunk-arrival order:
 //
-//   warp 0      TMA producer: the Q tile once, then for each KV block (128
-//               keys) in arrival order: wait for the block's chunk flags,
-//               load K and V into a two-slot ring
-//   warp 1      MMA issuer: S = Q.K^T into one of two TMEM score buffers,
-//               then O_A += P_A.V_A and O_B += P_B.V_B
-//   warps 2-3   staging: copy the other ranks' KV chunks, publish flags
-//   warps 4-7   softmax half A (one query row per thread, its TMEM lane):
-//               keys 0-63 of every block
-//   warps 8-11  softmax half B: keys 64-127
+//   warp 0      TMA producer: an item's Q tiles, then for each KV block:
+//               wait for the chunk flags of its rows, load K and V into a
+//               two-slot ring
+//   warps 1, 3  MMA issuers, one per tile: S_t = Q_t.K^T into the tile's
+//               TMEM score buffer, then O_t += P_t.V
+//   warp 2      staging: copy the other ranks' KV chunks, publish flags
+//   warps 4-7   softmax of tile 0 (one query row per thread, its TMEM lane)
+//   warps 8-11  softmax of tile 1
 //
-// Each half keeps its own running max, sum and TMEM output accumulator (the
-// two halves of the keys are two independent partial attentions), so the
-// halves never synchronise inside the KV loop; at the end of a work item
-// half A merges them: O = (O_A 2^(m_A-m) + O_B 2^(m_B-m)) / (l_A 2^(m_A-m) +
-// l_B 2^(m_B-m)), m = max(m_A, m_B).
-//
-// TMEM (512 columns): scores S0 S1 at 0 and 128, O_A at 256, O_B at 384.
-// Each half writes its bf16 probabilities over the first 32 columns of its
-// own part of the score buffer (P_A at column 0, P_B at 64), where P.V reads
-// them as a TMEM operand.  Q.K^T of the next block overlaps the softmax of
-// this one.  The
-// exponentials use a reference max that may lag the half-row's true max by
-// up to 8 (log2 units, so every p <= 2^8): only when a block raises it by
-// more is that half's TMEM accumulator (and sum) rescaled, between two
-// P.V products.
+// TMEM (512 columns): S_t at 128t, O_t at 256 + 128t.  The softmax writes
+// the bf16 probabilities over the first 64 columns of the tile's score
+// buffer, where P.V reads them as a TMEM operand; so a tile's Q.K^T of block
+// g+1 waits for its P.V of block g, and the two tiles' chains interleave on
+// the tensor pipe (one tile's MMAs run while the other's softmax does).  The
+// exponentials use a reference max that may lag the row's true max by up to
+// 8 (log2 units, so every p <= 2^8): only when a block raises it by more is
+// the tile's TMEM accumulator (and sum) rescaled, between two P.V products.
+// The softmax warps hold 200 registers each, the other warps 96 (setmaxnreg).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -65,15 +60,15 @@ enum {
     B_QF = 0,      // the item's Q tiles landed
     B_QE = 1,      // Q tiles read by the item's last Q.K^T
     B_KF = 2,      // K slot s landed (2)
-    B_KE = 4,      // K slot s consumed by both tiles' Q.K^T (2)
+    B_KE = 4,      // K slot s consumed by both tiles' Q.K^T (2; one commit per tile's issuer)
     B_VF = 6,      // V slot s landed (2)
-    B_VE = 8,      // V slot s consumed by both tiles' P.V (2)
+    B_VE = 8,      // V slot s consumed by both tiles' P.V (2; one commit per tile's issuer)
     B_SF = 10,     // tile t's scores written (2)
     B_PF = 12,     // tile t's probabilities written over its scores (2)
     B_PV = 14,     // tile t's P.V done: O_t updated, its score buffer free (2)
     B_OE = 16,     // tile t's accumulator read out after an item's last P.V (2)
-    B_DRAIN = 18,  // every MMA of the CTA completed
-    N_BAR = 19
+    B_DRAIN = 18,  // every MMA of tile t's issuer completed (2)
+    N_BAR = 20
 };
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BAR;  // TMEM base, abort flag
 constexpr int OFF_SEEN = OFF_MISC + 16;        // chunks the producer has acquired this call: 512 bits
@@ -99,7 +94,7 @@ struct Params {
     uint16_t *out;          // [S_r, H_q, d]
     float *lse;             // [S_r, H_q] or null
     int32_t *err;           // {code, site, CTA, info}
-    // in-kernel staging (stage = 1): warps 2-3 of every CTA copy the other
+    // in-kernel staging (stage = 1): warp 2 of every CTA copies the other
     // ranks' chunks into the gathered buffers in arrival order.  Tensor x
     // (K, V, and in head mode Q): row i of source q's chunk rows copies
     // width[x] bytes from src[x][q] + i * src_pitch[x] + src_off[x] to
@@ -460,18 +455,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
     if (threadIdx.x == 0) {
         *abort = 0;
         ptx::mbar_init(bar(B_QF), 1);
-        ptx::mbar_init(bar(B_QE), 1);
+        ptx::mbar_init(bar(B_QE), kTiles);  // each tile's issuer commits once
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(bar(B_KF + s), 1);
-            ptx::mbar_init(bar(B_KE + s), 1);
+            ptx::mbar_init(bar(B_KE + s), kTiles);
             ptx::mbar_init(bar(B_VF + s), 1);
-            ptx::mbar_init(bar(B_VE + s), 1);
+            ptx::mbar_init(bar(B_VE + s), kTiles);
             ptx::mbar_init(bar(B_SF + s), 1);
             ptx::mbar_init(bar(B_PF + s), 4);  // the tile's four softmax warps
             ptx::mbar_init(bar(B_PV + s), 1);
             ptx::mbar_init(bar(B_OE + s), 4);
+            ptx::mbar_init(bar(B_DRAIN + s), 1);
         }
-        ptx::mbar_init(bar(B_DRAIN), 1);
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
     }
@@ -537,47 +532,48 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
                 if (nv > s) drain_bar(bar(B_VF + (int)s), ((s + ((nv - 1u - s) / 2u) * 2u) >> 1) & 1u, p);
             }
         }
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
-        // Per tile t the chain is Q.K^T(g) -> softmax -> P.V(g) -> Q.K^T(g+1) (the
-        // probabilities live in the tile's score buffer); the two tiles' chains
-        // interleave, so one tile's MMAs run while the other's softmax does.
+    } else if (warp == 1 || warp == 3) {
+        // ================= MMA issuers: warp 1 for tile 0, warp 3 for tile 1 =================
+        // Tile t's chain is Q.K^T(g) -> softmax -> P.V(g) -> Q.K^T(g+1) (the
+        // probabilities live in the tile's score buffer).  Each tile has its own
+        // issuing thread, so neither tile's next MMA queues behind the other
+        // tile's waits; a K or V slot is free once both issuers have committed it.
         if (lane == 0) {
+            const int t = warp == 1 ? 0 : 1;
             const uint32_t sQ = sbase + OFF_Q, sK = sbase + OFF_K, sV = sbase + OFF_V;
+            const uint32_t d_s = tmem + (uint32_t)(t * 128);         // S_t, then P_t
+            const uint32_t d_o = tmem + 256u + (uint32_t)(t * 128);  // O_t
+            const uint32_t q_t = sQ + (uint32_t)(t * kTileBytes);
             // S_t = Q_t . K_g^T (K slot g & 1)
-            auto qk = [&](uint32_t g, int t) -> bool {
+            auto qk = [&](uint32_t g) -> bool {
                 const int s = (int)(g & 1u);
-                if (t == 0 && !wait_bar(bar(B_KF + s), (g >> 1) & 1u, abort, p)) return false;
-                // the tile's score buffer holds P(g-1) until P.V(g-1) has read it
+                if (!wait_bar(bar(B_KF + s), (g >> 1) & 1u, abort, p)) return false;
+                // the score buffer holds P(g-1) until P.V(g-1) has read it
                 if (g > 0 && !wait_bar(bar(B_PV + t), (g - 1u) & 1u, abort, p)) return false;
                 ptx::tc_fence_after();
-                const uint32_t d_s = tmem + (uint32_t)(t * 128);
-                const uint32_t q_t = sQ + (uint32_t)(t * kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
                     ptx::umma_bf16(d_s, kmajor_desc(q_t, kk), kmajor_desc(sK + s * kTileBytes, kk), IDESC_QK,
                                    kk != 0 ? 1u : 0u);
                 ptx::umma_commit(bar(B_SF + t));
-                if (t == kTiles - 1) ptx::umma_commit(bar(B_KE + s));
+                ptx::umma_commit(bar(B_KE + s));
                 return true;
             };
             // O_t (+)= P_t . V_g, P_t from TMEM (8 columns per 16 keys); an item's
             // first product overwrites O_t once the previous item (`item` - 1)
             // has been read out
-            auto pv = [&](uint32_t g, int t, bool first, uint32_t item) -> bool {
+            auto pv = [&](uint32_t g, bool first, uint32_t item) -> bool {
                 const int s = (int)(g & 1u);
                 if (!wait_bar(bar(B_PF + t), g & 1u, abort, p)) return false;
-                if (t == 0 && !wait_bar(bar(B_VF + s), (g >> 1) & 1u, abort, p)) return false;
+                if (!wait_bar(bar(B_VF + s), (g >> 1) & 1u, abort, p)) return false;
                 if (first && item > 0 && !wait_bar(bar(B_OE + t), (item - 1u) & 1u, abort, p)) return false;
                 ptx::tc_fence_after();
-                const uint32_t d_o = tmem + 256u + (uint32_t)(t * 128);
-                const uint32_t a_p = tmem + (uint32_t)(t * 128);
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk)
-                    ptx::umma_bf16_ts(d_o, a_p + (uint32_t)(kk * 8), mnmajor_desc(sV + s * kTileBytes, kk), IDESC_PV,
+                    ptx::umma_bf16_ts(d_o, d_s + (uint32_t)(kk * 8), mnmajor_desc(sV + s * kTileBytes, kk), IDESC_PV,
                                       (kk != 0 || !first) ? 1u : 0u);
                 ptx::umma_commit(bar(B_PV + t));
-                if (t == kTiles - 1) ptx::umma_commit(bar(B_VE + s));
+                ptx::umma_commit(bar(B_VE + s));
                 return true;
             };
             Walk wk;
@@ -585,39 +581,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             Blk cur, nxt;
             bool ok = true, has = wk.next(p, cur);
             uint32_t g = 0, ic = 0, item_cur = 0;
-            if (has) {  // prologue: the first block's Q.K^T for both tiles
+            if (has) {  // prologue: the first block's Q.K^T
                 ok = wait_bar(bar(B_QF), 0u, abort, p);
                 ic = 1;
-                for (int t = 0; ok && t < kTiles; ++t) ok = qk(0, t);
+                if (ok) ok = qk(0);
                 if (ok && cur.last) ptx::umma_commit(bar(B_QE));
             }
             while (ok && has) {
                 const bool has_next = wk.next(p, nxt);
                 if (has_next && nxt.first) {  // a new item: its Q tiles
-                    if (!wait_bar(bar(B_QF), ic & 1u, abort, p)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!wait_bar(bar(B_QF), ic & 1u, abort, p)) break;
                     ++ic;
                 }
-                for (int t = 0; ok && t < kTiles; ++t) {
-                    ok = pv(g, t, cur.first, item_cur);
-                    if (ok && has_next) ok = qk(g + 1u, t);
-                }
+                ok = pv(g, cur.first, item_cur);
+                if (ok && has_next) ok = qk(g + 1u);
                 if (!ok) break;
-                if (has_next && nxt.last) ptx::umma_commit(bar(B_QE));  // the item's Q tiles are no longer read
+                if (has_next && nxt.last) ptx::umma_commit(bar(B_QE));  // the item's Q tile is no longer read
                 if (has_next && nxt.first) ++item_cur;
                 cur = nxt;
                 has = has_next;
                 ++g;
             }
             // every MMA issued must complete before TMEM is released
-            ptx::umma_commit(bar(B_DRAIN));
-            drain_bar(bar(B_DRAIN), 0, p);
+            ptx::umma_commit(bar(B_DRAIN + t));
+            drain_bar(bar(B_DRAIN + t), 0, p);
         }
     } else {
-        // ================= stagers =================
-        if (p.stage) stage_chunks(p, (int)blockIdx.x * 2 + (warp - 2), (int)gridDim.x * 2, lane);
+        // ================= stager (warp 2) =================
+        if (p.stage) stage_chunks(p, (int)blockIdx.x, (int)gridDim.x, lane);
     }
     } else {
         regs_inc();

@@ -8,7 +8,7 @@
  * R ranks each hold S_r consecutive tokens of Q, K and V; rank r computes
  * attention of its own queries over the keys of every rank.  One persistent
  * kernel (a cooperative launch, one CTA per SM) both stages the other ranks'
- * KV shards into gathered buffers chunk by chunk -- staging warps in every
+ * KV shards into gathered buffers chunk by chunk -- a staging warp in every
  * CTA, ranks r+1, r+2, ... in turn as in the GEMM plans, each chunk
  * publishing a ready flag once its bytes have landed -- and computes: each
  * (query tile, head) work item visits the KV blocks in that arrival order
