@@ -21,8 +21,10 @@
 // TMEM (512 columns): S_t at 128t, O_t at 256 + 128t.  The softmax writes
 // the bf16 probabilities over the first 64 columns of the tile's score
 // buffer, where P.V reads them as a TMEM operand; so a tile's Q.K^T of block
-// g+1 waits for its P.V of block g, and the two tiles' chains interleave on
-// the tensor pipe (one tile's MMAs run while the other's softmax does).  The
+// g+1 waits for its P.V of block g.  The two tiles take turns at the
+// exponentials (tile 1's of block g after tile 0's, tile 0's of block g+1
+// after tile 1's of block g), so one tile's MMAs run while the other's
+// softmax does and neither shares the exp2 unit.  The
 // exponentials use a reference max that may lag the row's true max by up to
 // 8 (log2 units, so every p <= 2^8): only when a block raises it by more is
 // the tile's TMEM accumulator (and sum) rescaled, between two P.V products.
@@ -68,7 +70,8 @@ enum {
     B_PV = 14,     // tile t's P.V done: O_t updated, its score buffer free (2)
     B_OE = 16,     // tile t's accumulator read out after an item's last P.V (2)
     B_DRAIN = 18,  // every MMA of tile t's issuer completed (2)
-    N_BAR = 20
+    B_XD = 20,     // tile t's exponentials of a block done (2): the tiles take turns
+    N_BAR = 22
 };
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BAR;  // TMEM base, abort flag
 constexpr int OFF_SEEN = OFF_MISC + 16;        // chunks the producer has acquired this call: 512 bits
@@ -466,6 +469,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             ptx::mbar_init(bar(B_PV + s), 1);
             ptx::mbar_init(bar(B_OE + s), 4);
             ptx::mbar_init(bar(B_DRAIN + s), 1);
+            ptx::mbar_init(bar(B_XD + s), 4);  // the tile's four softmax warps
         }
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -672,6 +676,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
                     ptx::tmem_st_32x32b_x32(to + (uint32_t)(c * 32), o);
                 }
             }
+            // the tiles take turns at the exponentials (tile 1's of block g after tile
+            // 0's, tile 0's of block g+1 after tile 1's of block g), so each runs them
+            // alone while the other tile's products run on the tensor pipe
+            if (t == 1 || g > 0) {
+                w = wait_bar(bar(B_XD + (1 - t)), (t == 1 ? g : g - 1u) & 1u, abort, p);
+                if (!__all_sync(0xffffffffu, w)) break;
+            }
             const float base = mref == -INFINITY ? 0.f : mref;
             // probabilities: the exponent arguments and the running sums two keys at
             // a time (f32x2), four interleaved pair-sums
@@ -703,7 +714,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(B_PF + t));
+            if (lane == 0) {
+                ptx::mbar_arrive(bar(B_PF + t));
+                ptx::mbar_arrive(bar(B_XD + t));
+            }
             if (b.last) {  // the item's output, after the tile's last P.V
                 w = wait_bar(bar(B_PV + t), g & 1u, abort, p);
                 if (!__all_sync(0xffffffffu, w)) break;
