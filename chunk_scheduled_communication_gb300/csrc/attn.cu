@@ -13,15 +13,17 @@
 //               wait for the chunk flags of its rows, load K and V into a
 //               two-slot ring
 //   warps 1, 3  MMA issuers, one per tile: S_t = Q_t.K^T into the tile's
-//               TMEM score buffer, then O_t += P_t.V
+//               TMEM score buffer (two 64-key halves), then O_t += P_t.V
 //   warp 2      staging: copy the other ranks' KV chunks, publish flags
 //   warps 4-7   softmax of tile 0 (one query row per thread, its TMEM lane)
 //   warps 8-11  softmax of tile 1
 //
 // TMEM (512 columns): S_t at 128t, O_t at 256 + 128t.  The softmax writes
-// the bf16 probabilities over the first 64 columns of the tile's score
-// buffer, where P.V reads them as a TMEM operand; so a tile's Q.K^T of block
-// g+1 waits for its P.V of block g.  The two tiles take turns at the
+// the bf16 probabilities over the upper 64 columns of the tile's score
+// buffer, where P.V reads them as a TMEM operand.  A tile's Q.K^T of block
+// g+1 runs in two 64-key halves: the lower half as soon as the softmax has
+// loaded the scores of block g into registers, the upper half once P.V of
+// block g has read the probabilities.  The two tiles take turns at the
 // exponentials (tile 1's of block g after tile 0's, tile 0's of block g+1
 // after tile 1's of block g), so one tile's MMAs run while the other's
 // softmax does and neither shares the exp2 unit.  The
@@ -71,7 +73,8 @@ enum {
     B_OE = 16,     // tile t's accumulator read out after an item's last P.V (2)
     B_DRAIN = 18,  // every MMA of tile t's issuer completed (2)
     B_XD = 20,     // tile t's exponentials of a block done (2): the tiles take turns
-    N_BAR = 22
+    B_SL = 22,     // tile t's scores loaded into the softmax registers (2)
+    N_BAR = 24
 };
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BAR;  // TMEM base, abort flag
 constexpr int OFF_SEEN = OFF_MISC + 16;        // chunks the producer has acquired this call: 512 bits
@@ -79,7 +82,7 @@ constexpr int SMEM_USED = OFF_SEEN + 64;
 constexpr int NTHREADS = 384;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;   // + the 1024-byte alignment of the tiles
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, 128, false);  // B = K tile, K-major
+constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(128, 64, false);   // B = 64 keys of the K tile, K-major
 constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(128, 128, true);   // A = P in TMEM, B = V tile, MN-major
 constexpr int WHERE_FLAG = 1, WHERE_PIPE = 3;
 
@@ -470,6 +473,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             ptx::mbar_init(bar(B_OE + s), 4);
             ptx::mbar_init(bar(B_DRAIN + s), 1);
             ptx::mbar_init(bar(B_XD + s), 4);  // the tile's four softmax warps
+            ptx::mbar_init(bar(B_SL + s), 4);
         }
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -548,19 +552,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             const uint32_t d_s = tmem + (uint32_t)(t * 128);         // S_t, then P_t
             const uint32_t d_o = tmem + 256u + (uint32_t)(t * 128);  // O_t
             const uint32_t q_t = sQ + (uint32_t)(t * kTileBytes);
-            // S_t = Q_t . K_g^T (K slot g & 1)
-            auto qk = [&](uint32_t g) -> bool {
+            // S_t = Q_t . K_g^T (K slot g & 1) in two halves of 64 keys: the lower
+            // half (score columns 0-63) once the softmax has loaded S(g-1), the
+            // upper half (columns 64-127, where P(g-1) lives) once P.V(g-1) read it
+            auto qk_half = [&](uint32_t g, int half) -> bool {
                 const int s = (int)(g & 1u);
-                if (!wait_bar(bar(B_KF + s), (g >> 1) & 1u, abort, p)) return false;
-                // the score buffer holds P(g-1) until P.V(g-1) has read it
-                if (g > 0 && !wait_bar(bar(B_PV + t), (g - 1u) & 1u, abort, p)) return false;
+                if (half == 0) {
+                    if (!wait_bar(bar(B_KF + s), (g >> 1) & 1u, abort, p)) return false;
+                    if (g > 0 && !wait_bar(bar(B_SL + t), (g - 1u) & 1u, abort, p)) return false;
+                } else if (g > 0 && !wait_bar(bar(B_PV + t), (g - 1u) & 1u, abort, p)) {
+                    return false;
+                }
                 ptx::tc_fence_after();
+                const uint32_t k_h = sK + s * kTileBytes + (uint32_t)half * 8192u;  // key rows 64*half..
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
-                    ptx::umma_bf16(d_s, kmajor_desc(q_t, kk), kmajor_desc(sK + s * kTileBytes, kk), IDESC_QK,
+                    ptx::umma_bf16(d_s + (uint32_t)(half * 64), kmajor_desc(q_t, kk), kmajor_desc(k_h, kk), IDESC_QK,
                                    kk != 0 ? 1u : 0u);
-                ptx::umma_commit(bar(B_SF + t));
-                ptx::umma_commit(bar(B_KE + s));
+                if (half == 1) {
+                    ptx::umma_commit(bar(B_SF + t));
+                    ptx::umma_commit(bar(B_KE + s));
+                }
                 return true;
             };
             // O_t (+)= P_t . V_g, P_t from TMEM (8 columns per 16 keys); an item's
@@ -574,7 +586,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk)
-                    ptx::umma_bf16_ts(d_o, d_s + (uint32_t)(kk * 8), mnmajor_desc(sV + s * kTileBytes, kk), IDESC_PV,
+                    ptx::umma_bf16_ts(d_o, d_s + 64u + (uint32_t)(kk * 8), mnmajor_desc(sV + s * kTileBytes, kk), IDESC_PV,
                                       (kk != 0 || !first) ? 1u : 0u);
                 ptx::umma_commit(bar(B_PV + t));
                 ptx::umma_commit(bar(B_VE + s));
@@ -588,7 +600,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             if (has) {  // prologue: the first block's Q.K^T
                 ok = wait_bar(bar(B_QF), 0u, abort, p);
                 ic = 1;
-                if (ok) ok = qk(0);
+                if (ok) ok = qk_half(0, 0);
+                if (ok) ok = qk_half(0, 1);
                 if (ok && cur.last) ptx::umma_commit(bar(B_QE));
             }
             while (ok && has) {
@@ -597,8 +610,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
                     if (!wait_bar(bar(B_QF), ic & 1u, abort, p)) break;
                     ++ic;
                 }
-                ok = pv(g, cur.first, item_cur);
-                if (ok && has_next) ok = qk(g + 1u);
+                if (has_next) ok = qk_half(g + 1u, 0);
+                if (ok) ok = pv(g, cur.first, item_cur);
+                if (ok && has_next) ok = qk_half(g + 1u, 1);
                 if (!ok) break;
                 if (has_next && nxt.last) ptx::umma_commit(bar(B_QE));  // the item's Q tile is no longer read
                 if (has_next && nxt.first) ++item_cur;
@@ -644,6 +658,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
             for (int c = 0; c < 4; ++c)
                 ptx::tmem_ld_32x32b_x32(ts + (uint32_t)(c * 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
             ptx::tmem_ld_wait();
+            // the scores are in registers: the next block's lower half may overwrite them
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(B_SL + t));
             if (masked) {
 #pragma unroll
                 for (int k = 0; k < kBK; ++k)
@@ -702,7 +720,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ring_attn_kernel(const __grid_con
                     sp[(k >> 1) & 3] = add2(sp[(k >> 1) & 3], f2(p0, p1));
                     pk[k >> 1] = pack_bf16(p0, p1);
                 }
-                ptx::tmem_st_32x32b_x32(ts + (uint32_t)(hh * 32), pk);
+                ptx::tmem_st_32x32b_x32(ts + 64u + (uint32_t)(hh * 32), pk);
             }
             float s0, s1, s2, s3, s4, s5, s6, s7;
             unf2(sp[0], s0, s1);
