@@ -114,7 +114,7 @@ __device__ __forceinline__ float4 ld_f4(const float *p) {
 // 16-byte streaming load of data that is read-only for the whole kernel
 __device__ __forceinline__ float4 ld_nc_f4(const float *p) {
     float4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "l"(p));
     return v;
