@@ -48,14 +48,15 @@ typedef struct syn_attn_plan_s *syn_attn_plan_t; /* opaque, owned by the library
 
 typedef struct {
     int R, rank;          /* simulated ranks (1..8) and the local rank          */
-    int64_t S_r;          /* tokens per rank, a multiple of 128                 */
+    int64_t S_r;          /* tokens per rank, a multiple of 256 (work items
+                             take two 128-row query tiles)                     */
     int H_q, H_kv;        /* query and KV heads, H_q % H_kv == 0                */
     int d;                /* head dimension: 128                                */
     int causal;           /* 0 or 1 (global positions)                          */
     int split;            /* chunks per rank's KV shard, 1..S_r/128 (0 = 1);
                              chunk j of a shard holds its rows
                              [ceil(j*S_r/split), ceil((j+1)*S_r/split))        */
-    int backend;          /* SYN_BACKEND_TMA_COLOCATED (staging warps inside the
+    int backend;          /* SYN_BACKEND_TMA_COLOCATED (a staging warp inside the
                              attention kernel, the default) or
                              SYN_BACKEND_UNFUSED (every copy first with
                              cudaMemcpyAsync, then the kernel without waits).
@@ -81,16 +82,18 @@ typedef struct {
     int R, rank, H_q, H_kv, d, causal, split, backend;
     int64_t S_r;
     int n_qtiles;         /* query tiles: S_r / 128 (ring), R*S_r / 128 (head)  */
-    int grid;             /* persistent CTAs: min(n_qtiles * H_q, resident CTAs);
-                             work item (head h, query tile t) = h * n_qtiles + t
-                             runs on CTA item mod grid                         */
+    int grid;             /* persistent CTAs: min(n_qtiles / 2 * heads, resident
+                             CTAs), heads = H_q (ring) or H_q / R (head);
+                             work item (head h, tile pair t) = h * n_qtiles / 2
+                             + t (query tiles 2t and 2t+1) runs on CTA item mod
+                             grid                                              */
     int n_transfers;      /* staged chunks (R-1, or R when the local shard is
                              not in place, times split)                        */
     int smem_bytes;
     uint32_t epoch;       /* calls issued so far                               */
 } syn_attn_info_t;
 
-/* Defaults: R 1, rank 0, S_r 128, 1 head, d 128, not causal, split 1,
+/* Defaults: R 1, rank 0, S_r 256, 1 head, d 128, not causal, split 1,
  * SYN_BACKEND_TMA_COLOCATED. */
 int syn_attn_cfg_default(syn_attn_cfg_t *cfg);
 
