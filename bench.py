@@ -662,6 +662,8 @@ def measure_attention(peaks, stream, reps=20):
             e1.record(stream)
             torch.cuda.synchronize()
             res["torch_sdpa_us"] = e0.elapsed_time(e1) / reps * 1e3
+        if not w.causal:  # the ncu capture in profiles/ is of this launch (rank 0, non-causal)
+            res["dram_traffic_per_launch"] = recorded_traffic("attn")
         out["causal" if w.causal else "full"] = res
     # head-parallel layout (the all-to-all form): rank 0's 4 query heads over all 32K tokens
     w = wl.LLAMA3_8B_RING_ATTN
