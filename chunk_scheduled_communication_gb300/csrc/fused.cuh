@@ -24,11 +24,12 @@
 //   warp 7      co-located stager: copies this CTA's share of chunk slices with
 //               TMA bulk copies (double-buffered) and publishes the chunk flags
 // CTAs with blockIdx.x >= G are dedicated staging CTAs (7 single-buffer copier threads).
-// RED instances (GEMM-RS/AR with resident peers) run 384 threads: the epilogue
-// stores a reducing tile's fp32 partial and frees the accumulator at once, and
-// warps 8-11 (GEMM-AR: also 6-7), joined by every other warp once its own role
-// is done, add the peer partials to it with plain coalesced loads (same
-// additions, same order, as the epilogue's own peer path).
+// RED instances (GEMM-RS/AR with resident peers) run 384 threads (GEMM-RS)
+// or 640 (GEMM-AR): the epilogue stores a reducing tile's fp32 partial and
+// frees the accumulator at once, and warps 8-11 (GEMM-AR: 6-19), joined by
+// every other warp once its own role is done, add the peer partials to it
+// with plain coalesced loads (same additions, same order, as the epilogue's
+// own peer path).
 //
 // Two MMA shapes.  Single CTA: 128 x BN x 16 UMMAs (tcgen05 cta_group::1), each
 // CTA stages its A rows and all BN columns of B.  CTA pair (PAIR, 2-CTA
@@ -73,6 +74,14 @@ constexpr int kSmemRings = 224 * 1024;
 // whether the CTA carries the co-located staging buffers (STG), and whether
 // CTA pairs share 256-row tiles (PAIR).  For RS/AR the peer-tile ring takes
 // whatever shared memory is left.
+// Threads of a CTA: 256; RED instances add reducer warps, four for GEMM-RS
+// (384: its few reducing tiles run beside MMAs that need the memory system)
+// and twelve for GEMM-AR (640, 96 registers a thread: its reduction outlasts
+// the MMAs, and the rate at which it streams the peers grows with the warps
+// doing it -- 16 / 20 / 24 warps measured 98.0 / 97.2 / 104 us on the
+// Qwen2-7B FFN down shape against 100.4 with 12; at 24 the registers spill).
+constexpr int red_threads(int op, bool red) { return red ? (op == OP_AR ? 640 : 384) : 256; }
+
 template <int OP, int BN, int S_, int BK_, bool STG, bool PAIR, bool RED>
 struct KCfg {
     static constexpr int CTAS = PAIR ? 2 : 1;
@@ -88,11 +97,11 @@ struct KCfg {
     static constexpr bool STG_ = STG;
     static constexpr bool PAIR_ = PAIR;
     // RED (GEMM-RS/AR with resident peers): the epilogue only stores the fp32
-    // partial of a reducing tile and frees the accumulator; four more warps
-    // (warps 8-11) then stream the peer sum with plain loads, so no peer ring
+    // partial of a reducing tile and frees the accumulator; more warps (8-11,
+    // GEMM-AR 8-19) then stream the peer sum with plain loads, so no peer ring
     // is needed and every byte of the rings goes to pipeline stages
     static constexpr bool RED_ = RED;
-    static constexpr int NTHREADS = RED ? 384 : 256;
+    static constexpr int NTHREADS = red_threads(OP, RED);
     // A (K-major): 8-row swizzle atoms of 8 * BK * 2 bytes
     static constexpr uint32_t A_SBO = 8 * BK * 2;
     static constexpr uint32_t A_SWZ = BK == 64 ? ptx::kSwizzle128B : ptx::kSwizzle64B;
@@ -553,7 +562,7 @@ __device__ __forceinline__ void count_produced(const KernelParams &p, int r0, in
 template <int OP, int BN, int ROWS>
 __device__ __forceinline__ void reduce_rows(const KernelParams &p, int row0, int col0, int lane) {
     constexpr int H = BN / 128;
-    constexpr int U = 2;
+    constexpr int U = OP == OP_AR ? 1 : 2;  // (GEMM-AR's wider CTA has 128 registers a thread)
     static_assert(ROWS % U == 0, "rows per pass");
     const int64_t N = p.N;
 #pragma unroll 1
@@ -602,9 +611,10 @@ __device__ __forceinline__ void reduce_rows(const KernelParams &p, int row0, int
 // to do: item k is row group k % 4 (8 rows) of TMEM lane quadrant (k / 4) % 4
 // of the walker's (k / 16)-th reducing tile, in this CTA's rows.  Warps claim
 // items in order from a shared-memory counter; an item starts once the
-// epilogue warp of its quadrant has stored that tile's partial.  Warps 6-11
-// work from the start, the epilogue, producer and MMA warps join when their
-// own work is done, so the reduction that outlasts the MMAs runs on all twelve.
+// epilogue warp of its quadrant has stored that tile's partial.  Warps 8 on
+// (GEMM-AR: 6 on) work from the start, the epilogue, producer and MMA warps
+// join when their own work is done, so GEMM-AR's reduction, which outlasts
+// its MMAs, ends up on all twenty warps.
 template <class C, int OP, int BN>
 __device__ __forceinline__ void reduce_worker(const KernelParams &p, uint8_t *sm, uint32_t sbase, int unit,
                                               int n_units, uint32_t crank, int lane, volatile int *abort) {
@@ -646,7 +656,7 @@ __device__ __forceinline__ void reduce_worker(const KernelParams &p, uint8_t *sm
 
 // ------------------------------------------------------------------ the kernel
 template <int OP, int BN, int S, int BK, bool STG, bool PAIR, bool RED>
-__global__ void __launch_bounds__(RED ? 384 : 256, 1)
+__global__ void __launch_bounds__(red_threads(OP, RED), 1)
     syn_fused_kernel(const __grid_constant__ KernelParams p, const __grid_constant__ TensorMaps tm) {
     using C = KCfg<OP, BN, S, BK, STG, PAIR, RED>;
     extern __shared__ uint8_t smem_raw[];
@@ -1167,7 +1177,7 @@ __global__ void __launch_bounds__(RED ? 384 : 256, 1)
                              bar0 + 8 * C::BAR_STG, abort);
     }
     // ================= reducers (RED) =================
-    // warps 8-11 from the start, the others once their own role is done.
+    // warps 8 on from the start, the others once their own role is done.
     // Warps 6-7 have no role here: GEMM-AR, whose reduction outlasts the MMAs,
     // puts them to work at once; GEMM-RS, whose few reducing tiles run early
     // beside MMAs that need the memory system, keeps them out.
