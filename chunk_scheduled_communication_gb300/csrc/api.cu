@@ -417,7 +417,7 @@ extern "C" {
 int syn_knobs_default(syn_knobs_t *k) {
     if (k == nullptr) return fail(SYN_ERR_INVALID, "null knobs");
     std::memset(k, 0, sizeof(*k));
-    k->backend = SYN_BACKEND_CE;
+    k->backend = SYN_BACKEND_TMA_COLOCATED;
     k->comm_sms = 8;
     k->tile_m = 128;
     k->tile_n = 256;

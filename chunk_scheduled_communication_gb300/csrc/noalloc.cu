@@ -11,13 +11,19 @@
 // This variant keeps that scratch in one file-scope __device__ array of fixed,
 // modest size (SYN_NOALLOC_SCRATCH_BYTES, held by every GPU that loads the
 // library until the process exits) and runs the same fused AG-GEMM kernel with
-// the co-located TMA staging backend, so the whole call is one kernel launch
-// plus small copies into that array.  The caller passes inputs and outputs.
+// the co-located TMA staging backend, so the whole call is two kernel
+// launches: a small one that fills that array, then the GEMM.  The caller
+// passes inputs and outputs.
 //
 // Host code never dereferences or passes the array's name to a kernel: in host
 // code that name is only a stand-in for the symbol.  The device address is
 // looked up once per device with cudaGetSymbolAddress (with that device
 // current) during the first call on that device.
+//
+// Each call writes its tile and transfer lists into the array, and clears the
+// flags, counters and error word, with one small kernel that receives the
+// lists by value as its parameter block (at most 16.6 KB): no host buffer
+// has to outlive the call, and nothing waits for the host.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -27,6 +33,7 @@
 #include <string>
 
 #include "fused.h"
+#include "host_util.h"
 #include "schedule.h"
 #include "syn.h"
 
@@ -88,6 +95,35 @@ bool encode(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint
 // counters and the error word of the call in flight.
 static __device__ __align__(256) unsigned char g_syn_noalloc_scratch[SYN_NOALLOC_SCRATCH_BYTES];
 
+namespace {
+
+// One call's schedule tables, passed by value to the fill kernel.
+struct NoallocTables {
+    int32_t n_tiles, n_transfers;
+    int32_t tiles[SYN_NOALLOC_MAX_TILES];
+    int32_t transfers[SYN_NOALLOC_MAX_ROW_CHUNKS];
+};
+static_assert(sizeof(NoallocTables) <= 32000, "kernel parameter block limit");
+
+// Writes the tables into the scratch array and zeroes everything after them
+// (flags, counters, error word).  Device code names the array directly.
+__global__ void noalloc_fill(const __grid_constant__ NoallocTables t) {
+    int32_t *tiles = reinterpret_cast<int32_t *>(g_syn_noalloc_scratch + kOffTiles);
+    int32_t *transfers = reinterpret_cast<int32_t *>(g_syn_noalloc_scratch + kOffTransfers);
+    uint32_t *clear = reinterpret_cast<uint32_t *>(g_syn_noalloc_scratch + kOffInFlags);
+    constexpr int n_clear = (kUsed - kOffInFlags) / 4;
+    const int stride = (int)(gridDim.x * blockDim.x);
+    for (int i = (int)(blockIdx.x * blockDim.x + threadIdx.x); i < SYN_NOALLOC_MAX_TILES; i += stride) {
+        if (i < t.n_tiles) tiles[i] = t.tiles[i];
+        if (i < t.n_transfers && i < SYN_NOALLOC_MAX_ROW_CHUNKS) transfers[i] = t.transfers[i];
+        if (i < n_clear) clear[i] = 0u;
+    }
+}
+static_assert((kUsed - kOffInFlags) / 4 <= SYN_NOALLOC_MAX_TILES, "one pass of the fill loop clears the rest");
+static_assert(kOffInFlags % 4 == 0 && kUsed % 4 == 0, "word-aligned layout");
+
+}  // namespace
+
 extern "C" int syn_ag_gemm_noalloc(int R, int rank, const syn_layout_t *layout, int split,
                                    syn_order_t order, const void *const *shards, void *gathered,
                                    const void *B, void *C, int32_t *status_dev, void *stream) {
@@ -97,7 +133,7 @@ extern "C" int syn_ag_gemm_noalloc(int R, int rank, const syn_layout_t *layout, 
     syn_knobs_default(&kn);
     kn.backend = SYN_BACKEND_TMA_COLOCATED;
     kn.tile_n = (layout->N % 256 == 0) ? 256 : 128;
-    kn.timeout_ns = 2000000000ull;
+    kn.timeout_ns = syn::host_timeout_ns();  // as plans: SYN_TIMEOUT_NS, else 2 s
     Schedule s;
     std::string err;
     int rc = build_schedule(SYN_OP_AG_GEMM, R, rank, *layout, 0, split, order, kn, s, err);
@@ -140,12 +176,21 @@ extern "C" int syn_ag_gemm_noalloc(int R, int rank, const syn_layout_t *layout, 
 
     // ---- this call's tables in, flags / counters / error word cleared ----
     // (the array keeps the previous call's contents)
-    if (cudaMemcpyAsync(scratch + kOffTiles, s.tile_list.data(), s.tile_list.size() * 4,
-                        cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(scratch + kOffTransfers, s.transfers.data(), s.transfers.size() * 4,
-                        cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemsetAsync(scratch + kOffInFlags, 0, (size_t)(kUsed - kOffInFlags), st) != cudaSuccess)
-        return fail(SYN_ERR_CUDA, "staging the schedule into the scratch array failed");
+    if (s.transfers.size() > (size_t)SYN_NOALLOC_MAX_ROW_CHUNKS)
+        return fail(SYN_ERR_UNSUPPORTED, "syn_ag_gemm_noalloc: too many staging transfers");
+    {
+        NoallocTables t;
+        std::memset(&t, 0, sizeof(t));
+        t.n_tiles = s.n_tiles;
+        t.n_transfers = (int32_t)s.transfers.size();
+        std::memcpy(t.tiles, s.tile_list.data(), s.tile_list.size() * 4);
+        std::memcpy(t.transfers, s.transfers.data(), s.transfers.size() * 4);
+        noalloc_fill<<<8, 256, 0, st>>>(t);
+        const cudaError_t fe = cudaGetLastError();
+        if (fe != cudaSuccess)
+            return fail(SYN_ERR_CUDA, std::string("writing the schedule into the scratch array: ") +
+                                          cudaGetErrorString(fe));
+    }
 
     TensorMaps maps;
     std::memset(&maps, 0, sizeof(maps));
@@ -174,6 +219,7 @@ extern "C" int syn_ag_gemm_noalloc(int R, int rank, const syn_layout_t *layout, 
     p.colocated = 1;
     p.waits = 1;
     p.drop_transfer = -1;
+    p.delay_transfer = -1;
     p.epoch = 1;  // flags were cleared, so every call can use the same epoch
     p.timeout_ns = kn.timeout_ns;
     p.tile_list = reinterpret_cast<const int32_t *>(scratch + kOffTiles);

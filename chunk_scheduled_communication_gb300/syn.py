@@ -131,7 +131,7 @@ def _check(status: int, where: str):
         raise SynError(status, where)
 
 
-def make_knobs(backend="ce", comm_sms=8, tile_n=256, group_m=8, slice_kb=128, timeout_ns=0,
+def make_knobs(backend="tma_colocated", comm_sms=8, tile_n=256, group_m=8, slice_kb=128, timeout_ns=0,
                drop_chunk=-1, trace=0, stages=0, tile_k=0, tile_m=0, reduce_spread=0,
                reduce_warps=0, ce_streams=0, delay_chunk=-1, delay_us=0, corrupt_entry=0,
                rs_push=0) -> Knobs:

@@ -238,7 +238,9 @@ int syn_schedule_build(syn_op_t op, int R, int rank, const syn_layout_t *layout,
                        const syn_knobs_t *knobs, syn_plan_info_t *info,
                        int32_t *tile_list, int32_t *tile_key, int32_t *transfers);
 
-/* Fill *knobs with the defaults (CE backend, 128x256 tiles, 2 s timeout). */
+/* Fill *knobs with the defaults: TMA_COLOCATED staging (the chunks are copied
+ * by a warp inside every GEMM CTA, so progress never depends on another
+ * engine running beside the kernel), 128x256 tiles, 2 s timeout. */
 int syn_knobs_default(syn_knobs_t *knobs);
 
 /* Build a plan on the current CUDA device: validates, builds the schedule,
@@ -394,7 +396,10 @@ int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *layout,
  * device array of SYN_NOALLOC_SCRATCH_BYTES that every GPU loading libsyn
  * keeps until the process exits.  The first call on a device looks up that
  * array's address (cudaGetSymbolAddress) with the device current; make that
- * first call before any stream capture.  Shapes beyond SYN_NOALLOC_MAX_TILES
+ * first call before any stream capture.  Every call writes its schedule into
+ * the array with a small kernel that takes the tables as its parameters (no
+ * host buffer outlives the call), then launches the GEMM; device waits are
+ * bounded as for plans (SYN_TIMEOUT_NS, else 2 s).  Shapes beyond SYN_NOALLOC_MAX_TILES
  * output tiles (128 x tile_n, tile_n = 256 if N % 256 == 0 else 128) or
  * SYN_NOALLOC_MAX_ROW_CHUNKS chunks return SYN_ERR_UNSUPPORTED with a
  * message in syn_last_error().  No cudaMalloc, cudaFree or allocating library

@@ -37,7 +37,7 @@ def test_status_strings_and_defaults():
     assert L.syn_status_string(0) == b"SYN_OK"
     assert L.syn_status_string(-4) == b"SYN_ERR_TIMEOUT"
     k = syn.make_knobs()
-    assert k.backend == syn.BACKEND_CE and k.tile_n == 256 and k.debug_drop_chunk == -1
+    assert k.backend == syn.BACKEND_TMA_COLOCATED and k.tile_n == 256 and k.debug_drop_chunk == -1
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from chunk_scheduled_communication_gb300 import runner, syn
+from chunk_scheduled_communication_gb300 import runner, syn, tuned
 from chunk_scheduled_communication_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -536,9 +536,10 @@ def test_copy_engine_streams_bit_exact(ce_streams):
 def test_rs_push_mode_adds_send_rows(w, stages, kind):
     """GEMM-RS push mode: every send row is added (fp32, TMA reduce-add) into
     `send`, the destination ranks' receive accumulators; rows of the local
-    block are untouched and out_r is unchanged.  The added value is the same
-    P the pull mode stores, so the result is bit-exact against init + P, and
-    a second call adds P again."""
+    block are untouched and out_r is unchanged.  Checked against the oracle's
+    P (its send rows): init + P after one call and (init + P) + P after two,
+    bit-exact for integer inputs and within the fp32 tolerance otherwise.  The
+    added value is also the same P the pull mode stores (bit-exact)."""
     r = 1
     inp = inputs(w, r, 0, kind)
     rng = np.random.default_rng(7)
@@ -560,6 +561,15 @@ def test_rs_push_mode_adds_send_rows(w, stages, kind):
         twice = d.f32_out.cpu().numpy()
     keep = np.ones(w.M, bool)
     keep[r * w.M_r:(r + 1) * w.M_r] = False
+    _, P_ora = oracle.gemm_rs(inp.A, inp.B, inp.peers, w.R, r, send_rows=(0, w.M))
+    want_once = init[keep] + P_ora[keep]
+    want_twice = want_once + P_ora[keep]
+    if kind == "int":
+        assert (once[keep] == want_once).all() and (twice[keep] == want_twice).all()
+    else:
+        for got_, want_ in ((once[keep], want_once), (twice[keep], want_twice)):
+            ok, exc, frob = runner.f_close(got_, want_)
+            assert ok, (exc, frob)
     assert (once[keep] == (init[keep] + P[keep])).all()
     assert (twice[keep] == ((init[keep] + P[keep]) + P[keep])).all()
     assert (once[~keep] == init[~keep]).all() and (twice[~keep] == init[~keep]).all()
@@ -585,3 +595,26 @@ def test_uncompiled_stage_count_is_rejected():
     with pytest.raises(syn.SynError) as e:
         runner.make_plan(d, backend="tma_colocated_smem", tile_n=256, stages=5)
     assert e.value.status == syn.ERR_UNSUPPORTED
+
+
+# ----------------------------------------------------------------------------- the benchmark's configuration
+@pytest.mark.parametrize("w", [wl.LLAMA3_8B_UP_AG, wl.LLAMA3_8B_DOWN_RS, wl.QWEN2_7B_DOWN_AR],
+                         ids=["ag", "rs", "ar"])
+def test_benchmark_configuration_full_size_against_oracle(w):
+    """Full size, normal inputs, in exactly the launch configuration the
+    benchmark times (its knobs, GEMM-RS with `send`, GEMM-AR with publish
+    NULL so the plan keeps the partial sums in its own buffer), two calls in a
+    row on one plan: every output element against the oracle."""
+    split, order, kn = tuned.knobs_for(w.op)
+    inp = inputs(w, 0)
+    d = runner.upload(inp, with_f32_out=(w.op == "rs"))
+    with runner.make_plan(d, split=split, order=order, **kn) as plan:
+        for _ in range(2):
+            runner.call(plan, d)
+        assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+    got = {"out": runner.dev_to_u16(d.out)}
+    if w.op == "ag":
+        got["gathered"] = runner.dev_to_u16(d.gathered)
+    elif w.op == "rs":
+        got["f32"] = d.f32_out.cpu().numpy()
+    check_against_oracle(w, 0, got)

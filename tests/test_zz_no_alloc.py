@@ -4,15 +4,17 @@ Plug-in hosts that hand an operator only its tensors, and serving loops that
 forbid cudaMalloc/cudaFree after start-up, cannot use syn_plan_create (it
 allocates the plan's flags and tables).  This entry point keeps that scratch in
 one static device array instead.  The test calls it through the C ABI twice in
-a row, on two different shapes, and checks each result against the plan-based
-syn_ag_gemm within the parity tolerance (the array keeps the previous call's
-contents, so the second call also checks that the entry point clears what must
-start at zero).  It lives in its own file so that it is collected last.
+a row, on two different shapes, and checks each result against the CPU oracle
+(gathered buffer bit-exact, C within the parity tolerance) and against the
+plan-based syn_ag_gemm on the same inputs (within the same tolerance).  The
+array keeps the previous call's contents, so the second call also checks that
+the entry point clears what must start at zero.  It lives in its own file so
+that it is collected last.
 """
-import numpy as np
 import pytest
 import torch
 
+import oracle
 from chunk_scheduled_communication_gb300 import runner, syn
 from chunk_scheduled_communication_gb300 import workloads as wl
 
@@ -36,20 +38,25 @@ def _noalloc_result(w, inp, split):
     return runner.dev_to_u16(d.gathered), runner.dev_to_u16(d.out), status.cpu().numpy()
 
 
-def test_noalloc_matches_plan_entry_point_on_two_calls_in_a_row():
+def test_noalloc_matches_oracle_and_plan_entry_point_on_two_calls_in_a_row():
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     torch.cuda.set_device(0)
+    oracle.build()
     cases = [(wl.scaled(wl.LLAMA3_8B_UP_AG, M=8 * 256, K=1024, N=768), 3, 2),
              (wl.TINY_AG, 1, 1)]
     for w, r, split in cases:
-        inp = wl.make_inputs(w, r=r, seed=5)
+        inp = wl.make_inputs(w, r=r, seed=0)
+        g_ora, c_ora = oracle.ag_gemm(inp.shards, inp.B)
         g_ref, c_ref = _plan_result(w, inp)
         g, c, status = _noalloc_result(w, inp, split)
         assert status[0] == 0, status
-        assert (g == g_ref).all(), "gathered buffer differs"
+        assert (g == g_ora).all(), "gathered buffer differs from the oracle's"
+        ok, exc, frob = runner.bf16_close(c, c_ora)
+        assert ok, (w.name, "oracle", exc, frob)
+        assert (g == g_ref).all(), "gathered buffer differs from the plan entry point's"
         ok, exc, frob = runner.bf16_close(c, c_ref)
-        assert ok, (w.name, exc, frob)
+        assert ok, (w.name, "plan entry point", exc, frob)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
