@@ -574,10 +574,11 @@ int plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_layout_
         PL_CK(cudaMalloc(&pl->d_trace, 5 * (size_t)s.n_tiles * sizeof(unsigned long long)));
         PL_CK(cudaMemset(pl->d_trace, 0, 5 * (size_t)s.n_tiles * sizeof(unsigned long long)));
     }
-    if (pl->lc.red && s.op == SYN_OP_GEMM_RS) {
-        // the local block's partial rows (GEMM-AR keeps them in the publish
-        // buffer, or in a buffer made on the first call without one)
-        pl->red_bytes = (size_t)s.M_r * s.N * sizeof(float);
+    if (pl->lc.red) {
+        // GEMM-RS: the local block's partial rows, stored by the epilogue for
+        // the reducer warps; GEMM-AR: the peer sums S, stored by the reducer
+        // warps for the epilogue
+        pl->red_bytes = (size_t)(s.op == SYN_OP_GEMM_RS ? s.M_r : s.M) * s.N * sizeof(float);
         PL_CK(cudaMalloc(&pl->d_red, pl->red_bytes));
     }
     if (staged_peers(pl)) {
@@ -756,23 +757,15 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
     int64_t red_rows = 0;
     int32_t red_row_off = 0;
     if (plan->lc.red) {
+        red_buf = plan->d_red;
         if (op == SYN_OP_GEMM_RS) {
-            red_buf = plan->d_red;
             red_rows = s.M_r;
             red_row_off = (int32_t)(s.rank * s.M_r);
-        } else if (f32_out != nullptr) {
-            red_buf = f32_out;
-            red_rows = s.M;
         } else {
-            if (plan->d_red == nullptr) {
-                plan->red_bytes = (size_t)s.M * s.N * sizeof(float);
-                SYN_CK(cudaMalloc(&plan->d_red, plan->red_bytes));
-            }
-            red_buf = plan->d_red;
             red_rows = s.M;
         }
     }
-    std::vector<const void *> key = {A, B, f32_out, red_buf};
+    std::vector<const void *> key = {A, B, f32_out, red_buf, out};
     if (!staged)
         for (int q = 0; q < s.R; ++q) key.push_back(q == s.rank ? nullptr : peers[q]);
     if (key != plan->map_key) {
@@ -801,6 +794,12 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
         if (red_buf != nullptr &&
             (rc = encode_2d(&plan->maps.red, red_buf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.N,
                             (uint64_t)red_rows, 32, 32)) != SYN_OK)
+            return rc;
+        // GEMM-AR with reducer warps: bf16 tile stores of out by the epilogue,
+        // 32 columns x 32 rows, 64-byte swizzle
+        if (op == SYN_OP_GEMM_AR && plan->lc.red &&
+            (rc = encode_2d(&plan->maps.c, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.N, s.M, 32, 32,
+                            CU_TENSOR_MAP_SWIZZLE_64B)) != SYN_OK)
             return rc;
         plan->map_key = key;
     }

@@ -68,6 +68,31 @@ namespace syn {
 // buffers (barriers and bookkeeping come on top).
 constexpr int kSmemRings = 224 * 1024;
 
+// Pre-summed GEMM-AR: most S chunk loads an epilogue warp keeps in flight.
+// Two: every further slot takes shared memory from L1, and the reducer warps'
+// peer stream slows as L1 shrinks (measured on the Qwen2-7B FFN down shape,
+// 4 stages: 84.3 us with two slots, 91.8 us with four).
+#ifndef SYN_PS_NSL_MAX
+#define SYN_PS_NSL_MAX 2
+#endif
+#ifndef SYN_PS_PEER_CG
+#define SYN_PS_PEER_CG 0
+#endif
+#ifndef SYN_OUT_EVICT_FIRST
+#define SYN_OUT_EVICT_FIRST 0
+#endif
+
+// TMA tile store of an operator output that this kernel never reads back:
+// with SYN_OUT_EVICT_FIRST its lines are the first to leave L2, so they are
+// written back while this kernel runs rather than during the next one.
+__device__ __forceinline__ void store_out_tile(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y) {
+#if SYN_OUT_EVICT_FIRST
+    ptx::tma_store_2d_hint(map, src, x, y, ptx::policy_evict_first());
+#else
+    ptx::tma_store_2d(map, src, x, y);
+#endif
+}
+
 // Compile-time shape of one kernel instance: operator, tile width BN, GEMM
 // pipeline stages S, k-block depth BK (64: 128-byte A rows, 128-byte swizzle;
 // 32: 64-byte A rows, 64-byte swizzle, half-size stages so twice as many fit),
@@ -102,6 +127,23 @@ struct KCfg {
     // is needed and every byte of the rings goes to pipeline stages
     static constexpr bool RED_ = RED;
     static constexpr int NTHREADS = red_threads(OP, RED);
+    // PRESUM (GEMM-AR with reducer warps): the reducer warps sum the peer
+    // partials of the walker's tiles, S = ((peer_q1 + peer_q2) + ...) over
+    // q != rank ascending, from the start of the kernel into a plan buffer --
+    // they depend on no tile's MMAs -- and the epilogue adds that one fp32
+    // tile to the accumulator: out = rne(P + S).  Per epilogue warp: PS_NSL
+    // shared-memory slots of 32 x 32 fp32 that TMA fills with S, and two
+    // 32 x 32 bf16 slots for the TMA stores of out.  Reducer items of tile j
+    // count into completion slot j % PS_NS; the epilogue's acknowledgement of
+    // tile j lets items of tile j + PS_NS start.
+    static constexpr bool PRESUM = RED && OP == OP_AR;
+    static constexpr int PS_SLOT = 32 * 32 * 4;
+    static constexpr int PS_OUT = 32 * 32 * 2;
+    static constexpr int PS_ROOM = (kSmemRings - S * STAGE_BYTES) / 4 - 2 * PS_OUT;
+    static constexpr int PS_NSL = PS_ROOM / PS_SLOT >= SYN_PS_NSL_MAX ? SYN_PS_NSL_MAX
+                                                                      : PS_ROOM / PS_SLOT;  // S loads in flight
+    static constexpr int PS_WARP = PS_NSL * PS_SLOT + 2 * PS_OUT;
+    static constexpr int PS_NS = 8;
     // A (K-major): 8-row swizzle atoms of 8 * BK * 2 bytes
     static constexpr uint32_t A_SBO = 8 * BK * 2;
     static constexpr uint32_t A_SWZ = BK == 64 ? ptx::kSwizzle128B : ptx::kSwizzle64B;
@@ -131,7 +173,8 @@ struct KCfg {
     static_assert(S * STAGE_BYTES + P * PEER_BYTES + NSTG * STG_BYTES <= kSmemRings, "rings");
     static constexpr int EPI_LEFT = kSmemRings - S * STAGE_BYTES - P * PEER_BYTES - NSTG * STG_BYTES;
     static constexpr bool EPI_TMA = OP == OP_AG ? EPI_AG : EPI_LEFT >= EPI_WANT;
-    static constexpr int EPI_BYTES = EPI_TMA ? EPI_WANT : 0;
+    static constexpr int EPI_BYTES = PRESUM ? 4 * PS_WARP : EPI_TMA ? EPI_WANT : 0;
+    static_assert(!PRESUM || (PS_NSL >= 2 && EPI_LEFT >= 4 * PS_WARP), "pre-summed reduction: epilogue slots");
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + S * A_BYTES;
@@ -149,7 +192,8 @@ struct KCfg {
     static constexpr int BAR_STG = BAR_PEMPTY + P;
     static constexpr int BAR_DRAIN = BAR_STG + NSTG;
     static constexpr int BAR_PEERDONE = BAR_DRAIN + 1;  // PAIR: odd producer finished issuing
-    static constexpr int NBAR = BAR_PEERDONE + 1;
+    static constexpr int BAR_SLD = BAR_PEERDONE + 1;     // PRESUM: S slot loads, PS_NSL per epilogue warp
+    static constexpr int NBAR = BAR_SLD + (PRESUM ? 4 * PS_NSL : 0);
     static constexpr int COMM_BUF_BYTES = 32768;
     static constexpr int COMM_NBUF = OFF_BAR / COMM_BUF_BYTES;
     static constexpr int NBAR_ALL = NBAR > COMM_NBUF ? NBAR : COMM_NBUF;
@@ -161,7 +205,11 @@ struct KCfg {
     static constexpr int OFF_RED_READY = OFF_MISC + 16;
     static constexpr int OFF_RED_NEXT = OFF_MISC + 32;
     static constexpr int OFF_RED_TOTAL = OFF_MISC + 36;
-    static constexpr int SMEM_USED = OFF_MISC + 48;
+    // PRESUM: completed reducer items per (slot j % PS_NS, TMEM lane quadrant),
+    // then per quadrant the tiles whose completion the epilogue has seen
+    static constexpr int OFF_PS_DONE = OFF_MISC + 48;
+    static constexpr int OFF_PS_ACK = OFF_PS_DONE + PS_NS * 4 * 4;
+    static constexpr int SMEM_USED = OFF_MISC + 48 + (PRESUM ? PS_NS * 16 + 16 : 0);
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(OFF_B % 1024 == 0 && OFF_PEER % 1024 == 0 && OFF_STG % 1024 == 0 && OFF_EPI % 1024 == 0,
@@ -553,12 +601,40 @@ __device__ __forceinline__ void count_produced(const KernelParams &p, int r0, in
     }
 }
 
+// The order every GEMM-RS / GEMM-AR path adds in: the peer partials first,
+// S = ((peer_q1 + peer_q2) + ...) over q != rank ascending, then the local
+// partial, out = bf16(P + S) -- one order for every backend, so their outputs
+// are bit-identical; and it lets the peer sum start before P exists.
+
 // Deferred reduction of ROWS rows x BN columns starting at (row0, col0): out =
-// bf16(((P + peer_q0) + peer_q1) + ...) over q != rank ascending, P the fp32
-// partial the epilogue stored in red_buf -- the same additions in the same
-// order as the epilogue's own peer path.  One warp; lane l takes columns
-// 4l..4l+3 of every 128-column half, so every load and store of the warp is
-// one contiguous row segment, and U rows x all sources are in flight at once.
+// bf16(P + S), P the fp32 partial the epilogue stored in red_buf -- the same
+// additions in the same order as the epilogue's own peer path.  One warp;
+// lane l takes columns 4l..4l+3 of every 128-column half, so every load and
+// store of the warp is one contiguous row segment, and U rows x all sources
+// are in flight at once.
+// S of one float4 column group: the left fold over q != rank ascending of
+// pv[q][u][h]; -0 (the identity of an fp32 sum) when there is no peer.
+template <int U, int H>
+__device__ __forceinline__ float4 peer_sum(const KernelParams &p, const float4 (&pv)[kMaxRanks][U][H], int u,
+                                           int h) {
+    float4 s = make_float4(-0.f, -0.f, -0.f, -0.f);
+    bool first = true;
+#pragma unroll
+    for (int q = 0; q < kMaxRanks; ++q)
+        if (q < p.R && q != p.rank) {
+            if (first) {
+                s = pv[q][u][h];
+                first = false;
+            } else {
+                s.x = s.x + pv[q][u][h].x;
+                s.y = s.y + pv[q][u][h].y;
+                s.z = s.z + pv[q][u][h].z;
+                s.w = s.w + pv[q][u][h].w;
+            }
+        }
+    return s;
+}
+
 template <int OP, int BN, int ROWS>
 __device__ __forceinline__ void reduce_rows(const KernelParams &p, int row0, int col0, int lane) {
     constexpr int H = BN / 128;
@@ -592,14 +668,11 @@ __device__ __forceinline__ void reduce_rows(const KernelParams &p, int row0, int
 #pragma unroll
             for (int h = 0; h < H; ++h) {
                 float4 a = acc[u][h];
-#pragma unroll
-                for (int q = 0; q < kMaxRanks; ++q)
-                    if (q < p.R && q != p.rank) {
-                        a.x = a.x + pv[q][u][h].x;
-                        a.y = a.y + pv[q][u][h].y;
-                        a.z = a.z + pv[q][u][h].z;
-                        a.w = a.w + pv[q][u][h].w;
-                    }
+                const float4 sum = peer_sum(p, pv, u, h);
+                a.x = a.x + sum.x;
+                a.y = a.y + sum.y;
+                a.z = a.z + sum.z;
+                a.w = a.w + sum.w;
                 ptx::st_u32x2(p.out + (int64_t)orow * N + col0 + 4 * lane + 128 * h,
                               pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
             }
@@ -652,6 +725,264 @@ __device__ __forceinline__ void reduce_worker(const KernelParams &p, uint8_t *sm
         const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
         reduce_rows<OP, BN, RG>(p, tmi * C::TILE_M + (int)crank * C::BM + q * 32 + g * RG, tni * BN, lane);
     }
+}
+
+// ------------------------------------------------------------------ pre-summed GEMM-AR reduction
+// Acquire-wait until the shared-memory counter at `addr` reaches `want`
+// (written by other warps of this CTA with release operations).  False on
+// abort or timeout.
+__device__ __forceinline__ bool wait_smem_at_least(uint32_t addr, uint32_t want, const KernelParams &p,
+                                                   volatile int *abort) {
+    if ((int32_t)(ptx::ld_acquire_cta_shared(addr) - want) >= 0) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    const uint64_t limit = p.timeout_ns * 4ull + 200000000ull;
+    uint32_t sleep_ns = 32;
+    for (uint32_t n = 1;; ++n) {
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 512u) sleep_ns *= 2u;
+        if ((int32_t)(ptx::ld_acquire_cta_shared(addr) - want) >= 0) return true;
+        if (*abort) return false;
+        if ((n & 31u) == 0u) {
+            if (grid_failed(p)) {
+                *abort = 1;
+                return false;
+            }
+            if (ptx::globaltimer() - t0 > limit) {
+                raise_error(p, SYN_ERR_TIMEOUT, WHERE_PIPE, (int)want);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// S for ROWS rows x BN columns at (row0, col0): the peer partials summed in
+// ascending q (q != rank), stored fp32 into red_buf.  One warp, one row per
+// pass; lane l takes columns 4l..4l+3 of every 128-column half, so every load
+// and store of the warp is one contiguous row segment.
+template <int BN, int ROWS>
+__device__ __forceinline__ void presum_rows(const KernelParams &p, int row0, int col0, int lane) {
+    constexpr int H = BN / 128;
+    const int64_t N = p.N;
+#pragma unroll 1
+    for (int rr = 0; rr < ROWS; ++rr) {
+        const int row = row0 + rr;
+        if (row >= p.M) break;
+        float4 pv[kMaxRanks][1][H];
+#pragma unroll
+        for (int h = 0; h < H; ++h)
+#pragma unroll
+            for (int q = 0; q < kMaxRanks; ++q)
+                if (q < p.R && q != p.rank) {
+                    const float *src = reinterpret_cast<const float *>(p.stage_src[q]) + (int64_t)row * N +
+                                       col0 + 4 * lane + 128 * h;
+                    pv[q][0][h] = SYN_PS_PEER_CG ? ptx::ld_cg_f4(src) : ptx::ld_nc_f4(src);
+                }
+#pragma unroll
+        for (int h = 0; h < H; ++h)
+            ptx::st_f4(p.red_buf + (int64_t)(row - p.red_row_off) * N + col0 + 4 * lane + 128 * h,
+                       peer_sum(p, pv, 0, h));
+    }
+}
+
+// Reducer side of the pre-summed GEMM-AR: item k is row pair k % 16 of TMEM
+// lane quadrant (k / 16) % 4 of the walker's (k / 64)-th tile, in this CTA's
+// rows.  An item of tile j >= PS_NS first waits until the epilogue warp of
+// its quadrant has seen tile j - PS_NS complete (so completion slot j % PS_NS
+// is free), then sums the peers and counts itself complete (release).
+// Returns 1 when done, 0 when the walk has no tile for item k, -1 on abort.
+template <class C, int BN>
+__device__ __forceinline__ int presum_item(const KernelParams &p, uint32_t sbase, int unit, int n_units,
+                                           uint32_t crank, int lane, volatile int *abort, uint32_t k) {
+    constexpr int RG = 2;
+    constexpr int PER_Q = 32 / RG;
+    constexpr int PER_TILE = 4 * PER_Q;
+    const int j = (int)(k / PER_TILE), q = (int)(k / PER_Q) % 4, g = (int)(k % PER_Q);
+    const int t = walk_entry(p, unit, n_units, j);
+    if (t < 0) return 0;
+    const int tile = tile_at(p, t, abort);
+    if (tile < 0) return -1;
+    if (j >= C::PS_NS) {
+        int ok = 1;
+        if (lane == 0)
+            ok = wait_smem_at_least(sbase + C::OFF_PS_ACK + 4 * q, (uint32_t)(j - C::PS_NS + 1), p, abort);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return -1;
+    }
+    const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
+    presum_rows<BN, RG>(p, tmi * C::TILE_M + (int)crank * C::BM + q * 32 + g * RG, tni * BN, lane);
+    // the stores before the count, for the epilogue's TMA loads
+    ptx::fence_proxy_async_global();
+    __threadfence_block();
+    __syncwarp();
+    if (lane == 0)
+        ptx::red_add_release_cta_shared(sbase + C::OFF_PS_DONE + 4 * ((j % C::PS_NS) * 4 + q), 1u);
+    return 1;
+}
+
+// Reducer warps claim items in order from a shared-memory counter until the
+// walk has none left.
+template <class C, int BN>
+__device__ __forceinline__ void presum_worker(const KernelParams &p, uint8_t *sm, uint32_t sbase, int unit,
+                                              int n_units, uint32_t crank, int lane, volatile int *abort) {
+    uint32_t *next = reinterpret_cast<uint32_t *>(sm + C::OFF_RED_NEXT);
+    for (;;) {
+        uint32_t k = 0;
+        if (lane == 0) k = atomicAdd(next, 1u);
+        k = __shfl_sync(0xffffffffu, k, 0);
+        if (presum_item<C, BN>(p, sbase, unit, n_units, crank, lane, abort, k) != 1) return;
+    }
+}
+
+// Epilogue side of the pre-summed GEMM-AR, one warp (TMEM lane quadrant qd),
+// the whole walk: per tile, wait until the tile's S rows of this quadrant are
+// complete, then per 32-column chunk TMA-load S into a slot, read the
+// accumulator, out = bf16(P + S) through a TMA tile store (and publish = P,
+// when given, from the S slot the warp has just read), and drop the S lines
+// from L2 (dead once read).  Returns false when the CTA aborts.
+template <class C, int BN>
+__device__ __forceinline__ void presum_epilogue(const KernelParams &p, const TensorMaps &tm, uint32_t sbase,
+                                                uint32_t bar0, uint32_t tmem_base, int unit, int n_units,
+                                                uint32_t crank, bool leader, int warp, int lane,
+                                                volatile int *abort) {
+    constexpr int PER_Q = 16;
+    constexpr int NCC = BN / 32;
+    const int qd = warp & 3;
+    const uint32_t wbase = sbase + C::OFF_EPI + (uint32_t)((warp - 2) * C::PS_WARP);
+    const uint32_t sbar = bar0 + 8 * (C::BAR_SLD + (warp - 2) * C::PS_NSL);
+    const bool pub = p.f32_out != nullptr;
+    uint32_t ph = 0;       // parity of each S slot's next phase
+    uint32_t pending = 0;  // S slots with a load in flight (lane 0's view)
+    uint32_t tc = 0;
+    auto drain = [&]() {
+        if (lane == 0) {
+            for (int b = 0; b < C::PS_NSL; ++b)
+                if ((pending >> b) & 1u) bwait_drain(sbar + 8 * b, (ph >> b) & 1u, p);
+            ptx::bulk_wait_all();
+        }
+        __syncwarp();
+    };
+    for (int i = 0;; ++i) {
+        const int t = walk_entry(p, unit, n_units, i);
+        if (t < 0) break;
+        const int tile = tile_at(p, t, abort);
+        if (tile < 0) break;
+        const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
+        const int acc = (int)(tc & 1u);
+        const uint32_t aph = (tc >> 1) & 1u;
+        bool ok = bwait<C::PAIR_>(bar0 + 8 * (C::BAR_TFULL + acc), aph, abort, p);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        ptx::tc_fence_after();
+        if (p.trace != nullptr && leader && warp == 2 && lane == 0) p.trace[5 * t + 2] = ptx::globaltimer();
+        const int wrow0 = tmi * C::TILE_M + (int)crank * C::BM + qd * 32;  // this warp's first row
+        const bool valid = wrow0 < p.M;
+        const int row = wrow0 + lane;
+        const int sy = wrow0 - p.red_row_off;
+        const uint32_t tbase = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * BN);
+        auto load_s = [&](int cc) {  // lane 0
+            const int b = cc % C::PS_NSL;
+            ptx::mbar_arrive_expect_tx(sbar + 8 * b, C::PS_SLOT);
+            ptx::tma_load_2d(wbase + (uint32_t)(b * C::PS_SLOT), &tm.red, sbar + 8 * b, tni * BN + cc * 32, sy);
+            pending |= 1u << b;
+        };
+        const uint32_t done_addr = sbase + C::OFF_PS_DONE + 4 * ((i % C::PS_NS) * 4 + qd);
+        const uint32_t want = (uint32_t)(PER_Q * (i / C::PS_NS + 1));
+        // this quadrant's S rows of the tile are complete; acknowledge, so
+        // items of tile i + PS_NS may reuse the completion slot
+        int st = 1;
+        if (lane == 0) {
+            st = wait_smem_at_least(done_addr, want, p, abort) ? 1 : 0;
+            if (st) {
+                ptx::st_release_cta_shared(sbase + C::OFF_PS_ACK + 4 * qd, (uint32_t)(i + 1));
+                ptx::fence_proxy_async_global();  // the reducers' generic stores before the TMA loads
+                if (valid)
+                    for (int cc = 0; cc < C::PS_NSL && cc < NCC; ++cc) load_s(cc);
+            }
+        }
+        st = __shfl_sync(0xffffffffu, st, 0);
+        if (!st) break;
+        bool dead = false;
+#pragma unroll 1
+        for (int cc = 0; cc < NCC; ++cc) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
+            ptx::tmem_ld_wait();
+            if (!valid) continue;
+            const int b = cc % C::PS_NSL;
+            ok = bwait(sbar + 8 * b, (ph >> b) & 1u, abort, p);
+            if (!__all_sync(0xffffffffu, ok)) {
+                dead = true;
+                break;
+            }
+            ph ^= 1u << b;
+            if (lane == 0) pending &= ~(1u << b);
+            const int col = tni * BN + cc * 32;
+            const uint32_t srow = wbase + (uint32_t)(b * C::PS_SLOT) + (uint32_t)(lane * 128);
+            float f[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t a = srow + ((uint32_t)(c ^ (lane & 7)) << 4);
+                const float4 x = ptx::ld_shared_f4(a);
+                f[4 * c + 0] = __uint_as_float(v[4 * c + 0]) + x.x;
+                f[4 * c + 1] = __uint_as_float(v[4 * c + 1]) + x.y;
+                f[4 * c + 2] = __uint_as_float(v[4 * c + 2]) + x.z;
+                f[4 * c + 3] = __uint_as_float(v[4 * c + 3]) + x.w;
+                if (pub)  // publish = P, into this lane's own row of the slot it has just read
+                    ptx::st_shared_f4(a, __uint_as_float(v[4 * c + 0]), __uint_as_float(v[4 * c + 1]),
+                                      __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+            }
+            const uint32_t ob = wbase + (uint32_t)(C::PS_NSL * C::PS_SLOT + (cc & 1) * C::PS_OUT);
+            if (lane == 0) ptx::bulk_wait_read<1>();  // the stores of chunk cc - 2 have read their slots
+            __syncwarp();
+            // row `lane` (64 bytes), 16-byte chunk c at position c ^ ((lane >> 1) & 3) (64-byte swizzle)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                ptx::st_shared_u4(ob + (uint32_t)(lane * 64) + ((uint32_t)(c ^ ((lane >> 1) & 3)) << 4),
+                                  pack_bf16x2(f[8 * c], f[8 * c + 1]), pack_bf16x2(f[8 * c + 2], f[8 * c + 3]),
+                                  pack_bf16x2(f[8 * c + 4], f[8 * c + 5]),
+                                  pack_bf16x2(f[8 * c + 6], f[8 * c + 7]));
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (pub) store_out_tile(&tm.f32out, wbase + (uint32_t)(b * C::PS_SLOT), col, wrow0);
+                store_out_tile(&tm.c, ob, col, wrow0);
+                ptx::bulk_commit();
+                if (cc + C::PS_NSL < NCC) {
+                    if (pub) ptx::bulk_wait_read<0>();  // the publish store has read slot b
+                    load_s(cc + C::PS_NSL);
+                }
+            }
+            // this lane's S line of the chunk is dead: drop it from L2 unwritten
+            if (row < p.M) ptx::discard_l2_128(p.red_buf + (int64_t)(row - p.red_row_off) * p.N + col);
+        }
+        if (dead) {
+            drain();
+            break;
+        }
+        // release the accumulator (the even CTA's MMA waits for both CTAs)
+        ptx::tc_fence_before();
+        __syncwarp();
+        const uint32_t tempty = bar0 + 8 * (C::BAR_TEMPTY + acc);
+        if (lane == 0) {
+            if (leader)
+                ptx::mbar_arrive(tempty);
+            else
+                ptx::mbar_arrive_remote(ptx::mapa(tempty, 0));
+        }
+        if (p.trace != nullptr && leader && warp == 2 && lane == 0) p.trace[5 * t + 3] = ptx::globaltimer();
+        if (pub) {
+            // publish rows land before their chunk's produced flag
+            if (lane == 0) {
+                ptx::bulk_wait_all();
+                ptx::fence_proxy_async();
+            }
+            __syncwarp();
+            count_produced(p, tmi * C::TILE_M, C::TILE_M, C::CTAS, lane);
+        }
+        ++tc;
+    }
+    if (lane == 0) ptx::bulk_wait_all();  // every out store has landed before the CTA exits
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -709,6 +1040,11 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                 reinterpret_cast<volatile uint32_t *>(sm + C::OFF_RED_READY)[q] = 0u;
             *reinterpret_cast<volatile uint32_t *>(sm + C::OFF_RED_NEXT) = 0u;
             *reinterpret_cast<volatile uint32_t *>(sm + C::OFF_RED_TOTAL) = 0u;
+        }
+        if constexpr (C::PRESUM) {
+            for (int q = 0; q < C::PS_NS * 4 + 4; ++q)
+                reinterpret_cast<volatile uint32_t *>(sm + C::OFF_PS_DONE)[q] = 0u;
+            for (int b = 0; b < 4 * C::PS_NSL; ++b) ptx::mbar_init(bar0 + 8 * (C::BAR_SLD + b), 1);
         }
         for (int s = 0; s < C::S; ++s) {
             ptx::mbar_init(bar0 + 8 * (C::BAR_FULL + s), 1);
@@ -920,6 +1256,11 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                 ptx::umma_commit(bar0 + 8 * C::BAR_DRAIN);
             bwait_drain(bar0 + 8 * C::BAR_DRAIN, 0, p);
         }
+    } else if (warp >= 2 && warp < 6 && C::PRESUM) {
+        // ================= epilogue: pre-summed GEMM-AR =================
+        if constexpr (C::PRESUM)
+            presum_epilogue<C, BN>(p, tm, sbase, bar0, tmem_base, unit, n_units, crank, leader, warp, lane,
+                                   abort);
     } else if (warp >= 2 && warp < 6) {
         // ================= epilogue =================
         const int qd = warp & 3;  // TMEM lane quadrant this warp may access
@@ -994,7 +1335,7 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                             ptx::fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                ptx::tma_store_2d(&tm.c, buf, col, wrow0);
+                                store_out_tile(&tm.c, buf, col, wrow0);
                                 ptx::bulk_commit();
                             }
                         }
@@ -1020,6 +1361,8 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                             // destination's receive accumulator
                             if (OP == OP_RS && !red && p.send_push)
                                 ptx::tma_reduce_add_2d(fmap, buf, col, fy);
+                            else if (fmap == &tm.f32out)  // send / publish rows
+                                store_out_tile(fmap, buf, col, fy);
                             else
                                 ptx::tma_store_2d(fmap, buf, col, fy);
                             ptx::bulk_commit();
@@ -1035,6 +1378,9 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                     continue;  // the reducer warps add the peers to the stored partial
                 } else {
                 if (!red) continue;
+                // S = peer sum in ascending q, then out = P + S
+                float sacc[32];
+                bool first = true;
                 for (int q = 0; q < p.R; ++q) {
                     if (q == p.rank) continue;
                     const int slot = (int)(pit % C::P);
@@ -1049,20 +1395,29 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                     const uint32_t rowaddr = sPeer + slot * C::PEER_BYTES + lrow * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        float4 x;
-                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                     : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
-                                     : "r"(rowaddr + ((uint32_t)(c ^ (lrow & 7)) << 4)));
-                        f[4 * c + 0] = f[4 * c + 0] + x.x;
-                        f[4 * c + 1] = f[4 * c + 1] + x.y;
-                        f[4 * c + 2] = f[4 * c + 2] + x.z;
-                        f[4 * c + 3] = f[4 * c + 3] + x.w;
+                        const float4 x = ptx::ld_shared_f4(rowaddr + ((uint32_t)(c ^ (lrow & 7)) << 4));
+                        if (first) {
+                            sacc[4 * c + 0] = x.x;
+                            sacc[4 * c + 1] = x.y;
+                            sacc[4 * c + 2] = x.z;
+                            sacc[4 * c + 3] = x.w;
+                        } else {
+                            sacc[4 * c + 0] = sacc[4 * c + 0] + x.x;
+                            sacc[4 * c + 1] = sacc[4 * c + 1] + x.y;
+                            sacc[4 * c + 2] = sacc[4 * c + 2] + x.z;
+                            sacc[4 * c + 3] = sacc[4 * c + 3] + x.w;
+                        }
                     }
+                    first = false;
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(bar0 + 8 * (C::BAR_PEMPTY + slot));
                     ++pit;
                 }
                 if (dead) break;
+                if (!first) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) f[j] = f[j] + sacc[j];
+                }
                 if (in_range) {
                     const int orow = OP == OP_RS ? row - p.rank * p.M_r : row;
                     store_bf16_row32(p.out + (int64_t)orow * p.N + col, f);
@@ -1181,7 +1536,10 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
     // Warps 6-7 have no role here: GEMM-AR, whose reduction outlasts the MMAs,
     // puts them to work at once; GEMM-RS, whose few reducing tiles run early
     // beside MMAs that need the memory system, keeps them out.
-    if constexpr (RED) {
+    if constexpr (C::PRESUM) {
+        __syncwarp();
+        presum_worker<C, BN>(p, sm, sbase, unit, n_units, crank, lane, abort);
+    } else if constexpr (RED) {
         if (OP == OP_AR || (warp != 6 && warp != 7)) {
             __syncwarp();
             reduce_worker<C, OP, BN>(p, sm, sbase, unit, n_units, crank, lane, abort);
@@ -1301,10 +1659,17 @@ bool dispatch_cfg(const LaunchCfg &lc, Fn &&fn) {
         SYN_CFG(true, 256, 4, 64, true)
         SYN_CFG(true, 256, 3, 64, false) SYN_CFG(true, 256, 4, 64, false) SYN_CFG(true, 256, 5, 64, false)
         SYN_CFG(true, 256, 6, 64, false)
-        SYN_CFG_R(false, 256, 4, 64, false, true)
-        SYN_CFG_R(true, 256, 4, 64, false, true)
-        SYN_CFG_R(true, 256, 5, 64, false, true) SYN_CFG_R(true, 256, 6, 64, false, true)
-        SYN_CFG_R(true, 256, 7, 64, false, true)
+        if constexpr (OP == OP_RS) {
+            SYN_CFG_R(false, 256, 4, 64, false, true)
+            SYN_CFG_R(true, 256, 4, 64, false, true)
+            SYN_CFG_R(true, 256, 5, 64, false, true) SYN_CFG_R(true, 256, 6, 64, false, true)
+            SYN_CFG_R(true, 256, 7, 64, false, true)
+        } else {
+            // pre-summed GEMM-AR: the epilogue's S and out slots need 48 KB
+            SYN_CFG_R(false, 256, 3, 64, false, true)
+            SYN_CFG_R(true, 256, 3, 64, false, true) SYN_CFG_R(true, 256, 4, 64, false, true)
+            SYN_CFG_R(true, 256, 5, 64, false, true)
+        }
         return false;
     }
 #undef SYN_CFG

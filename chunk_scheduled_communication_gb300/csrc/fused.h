@@ -121,7 +121,7 @@ cudaError_t launch_fused_ar(const KernelParams &p, const TensorMaps &tm, const L
 int fused_smem_bytes(int op, const LaunchCfg &lc);
 // Default pipeline depth of a (tile_n, tile_k, stg, pair, red) choice.
 inline int default_stages(int op, int tile_n, int tile_k, bool stg, bool pair, bool red = false) {
-    if (red) return pair ? (op == OP_AR ? 5 : 6) : 4;
+    if (red) return pair ? (op == OP_AR ? 4 : 6) : (op == OP_AR ? 3 : 4);
     if (pair) return op == OP_AG ? (stg ? 5 : 7) : 4;
     if (tile_k == 32) return op == OP_AG ? (stg ? 8 : 9) : 6;
     if (op == OP_AG) return tile_n == 256 ? 4 : 6;

@@ -72,6 +72,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void fence_acq_rel_gpu() {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
+// order this thread's generic-proxy global-memory accesses with later
+// async-proxy (TMA) accesses of global memory
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- scoped memory ops
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
@@ -100,6 +105,17 @@ __device__ __forceinline__ uint32_t ld_acquire_cta_shared(uint32_t addr) {
 __device__ __forceinline__ void st_release_cta_shared(uint32_t addr, uint32_t v) {
     asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void red_add_release_cta_shared(uint32_t addr, uint32_t v) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 x;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                 : "r"(addr)
+                 : "memory");
+    return x;
+}
 
 // ---------------------------------------------------------------- vector global loads / stores
 // 16-byte load from L2 (data this kernel wrote earlier, possibly through TMA)
@@ -109,6 +125,14 @@ __device__ __forceinline__ float4 ld_f4(const float *p) {
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "l"(p)
                  : "memory");
+    return v;
+}
+// 16-byte load cached in L2 only, with a 256-byte L2 fetch
+__device__ __forceinline__ float4 ld_cg_f4(const float *p) {
+    float4 v;
+    asm volatile("ld.global.cg.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
     return v;
 }
 // 16-byte streaming load of data that is read-only for the whole kernel
@@ -121,6 +145,15 @@ __device__ __forceinline__ float4 ld_nc_f4(const float *p) {
 }
 __device__ __forceinline__ void st_u32x2(void *p, uint32_t a, uint32_t b) {
     asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void st_f4(float *p, float4 v) {
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+// drop the 128-byte L2 line at p (128-byte aligned) without writing it back:
+// for scratch data that is dead once read, so it never costs a DRAM write
+__device__ __forceinline__ void discard_l2_128(const void *p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA (tensor, tiled, 2-D)
@@ -140,6 +173,21 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y), "r"(src)
                  : "memory");
+}
+// the same with an L2 cache policy (createpolicy) for the written lines
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y,
+                                                  uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(src), "l"(policy)
+        : "memory");
+}
+// L2 policy: the lines are the first to leave L2 when room is needed
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 // shared -> global tile reduce-add (fp32 add into the destination, performed
 // at the memory side; bulk group of the issuing thread)

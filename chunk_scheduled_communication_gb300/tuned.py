@@ -11,7 +11,7 @@ from __future__ import annotations
 STEP_KNOBS = {
     "ag": dict(backend="tma_colocated", split=4, order="grouped", tile_m=256, tile_n=256, comm_sms=8, stages=0),
     "rs": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=6),
-    "ar": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=5),
+    "ar": dict(backend="tma_colocated_smem", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=4),
     "a2a": dict(backend="tma_colocated", split=1, order="banded", group_m=8, tile_m=256, tile_n=256, comm_sms=8,
                 stages=5),
 }

@@ -143,15 +143,16 @@ typedef struct {
     int stages;            /* GEMM shared-memory pipeline depth; 0 = the
                               default of the chosen instance:
                                 tile_m 256: AG 5 (co-located stagers) / 7;
-                                  RS / AR with reducer warps 6 / 5, with the
+                                  RS / AR with reducer warps 6 / 4, with the
                                   epilogue peer ring 4;
-                                tile_m 128: reducer warps 4; AG 4 / 6
+                                tile_m 128: reducer warps RS 4, AR 3; AG 4 / 6
                                   (tile_n 256 / 128); RS, AR 3 / 4;
                                 tile_k 32: AG 8 (co-located) / 9, RS, AR 6.
-                              Other compiled depths: tile_m 256 AG 4-7, RS /
-                              AR 3-7; tile_m 128 RS / AR 2-6 (the peer ring
-                              takes the memory the stages leave).  A depth
-                              that is not compiled is SYN_ERR_UNSUPPORTED.   */
+                              Other compiled depths: tile_m 256 AG 4-7, RS
+                              3-7, AR 3-7 (with reducer warps 3-5); tile_m
+                              128 RS / AR 2-6 (the peer ring takes the memory
+                              the stages leave).  A depth that is not
+                              compiled is SYN_ERR_UNSUPPORTED.               */
     int tile_k;            /* k-block depth per pipeline stage: 64 or 32
                               (0 = 64).  32 halves each stage, so twice as
                               many fit and more loads are in flight.         */
@@ -165,15 +166,17 @@ typedef struct {
                               its own grid, syn_schedule_build (which knows no
                               grid) keeps them first.                         */
     int reduce_warps;      /* GEMM-RS/AR with TMA_COLOCATED_SMEM, tile_n 256,
-                              tile_k 64: 0 = default: the epilogue stores each
-                              reducing tile's fp32 partial and frees the
-                              accumulator at once, and four extra warps per CTA
-                              add the peer partials with plain loads (GEMM-RS:
-                              the plan holds a (M/R) x N fp32 buffer for the
-                              local block; GEMM-AR: the partial goes to
-                              `publish`, or to a M x N fp32 buffer the plan
-                              makes on the first call without one).  Same
-                              additions in the same order as -1, bit for bit.
+                              tile_k 64: 0 = default: extra warps per CTA add
+                              the peer partials with plain loads.  GEMM-RS:
+                              the epilogue stores each reducing tile's fp32
+                              partial into a (M/R) x N plan buffer and frees
+                              the accumulator at once; four reducer warps
+                              then add the peers to it.  GEMM-AR: from the
+                              start of the kernel, fourteen reducer warps sum
+                              the peers of the CTA's tiles in walk order into
+                              a M x N plan buffer, and the epilogue adds that
+                              sum to the accumulator.  Same additions in the
+                              same order as -1, bit for bit.
                               -1 = the epilogue adds the peers itself through a
                               shared-memory ring of peer tiles.              */
     int ce_streams;        /* CE: side streams the chunk copies are spread over
@@ -278,8 +281,8 @@ int syn_ag_gemm(syn_plan_t plan, const void *const *shards, void *gathered,
  *   send          : nullable fp32 [M, N]; rows of every rank q != r receive
  *                   the local partial P = A.B (the chunks peers would pull);
  *                   rows of rank r are not written
- *   out_r         : bf16 [M/R, N] = rne(P[rows_r] + sum_{q != r, ascending}
- *                   peer_q[rows_r])
+ *   out_r         : bf16 [M/R, N] = rne(P[rows_r] + S), S = the peers' rows
+ *                   summed first, sum_{q != r, ascending} peer_q[rows_r]
  * Send tiles run first (in ring order of their destination), reduce tiles last
  * when peers are staged; with resident peers (TMA_COLOCATED_SMEM) the reduce
  * tiles are spread over the walk (knobs.reduce_spread). */
@@ -288,7 +291,9 @@ int syn_gemm_rs(syn_plan_t plan, const void *A, const void *B,
                 void *stream);
 
 /* GEMM-AllReduce for the plan's rank r (summary page, Experiments, paper §6.1).
- *   out     : bf16 [M, N] = rne(A.B + sum_{q != r, ascending} peer_q)
+ *   out     : bf16 [M, N] = rne(A.B + S), S = sum_{q != r, ascending} peer_q
+ *             (every GEMM-RS / GEMM-AR path adds the peers first, then the
+ *             local partial: the same bits whatever the backend)
  *   publish : nullable fp32 [M, N] = A.B (the local partial peers would pull)
  * Other arguments as for syn_gemm_rs. */
 int syn_gemm_ar(syn_plan_t plan, const void *A, const void *B,

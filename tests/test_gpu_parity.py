@@ -402,7 +402,6 @@ INT_AR_PAIR = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=2 * 333, K=128, N=512, R=2)
     (INT_RS_PAIR, "ldst_dedicated", 4),
     (INT_AR_PAIR, "smem_ring", 4), (INT_AR_PAIR, "smem_ring", 6),
     (INT_AR_PAIR, "tma_colocated_smem", 4), (INT_AR_PAIR, "tma_colocated_smem", 5),
-    (INT_AR_PAIR, "tma_colocated_smem", 6), (INT_AR_PAIR, "tma_colocated_smem", 7),
     (INT_AR_PAIR, "tma_colocated", 4), (INT_AR_PAIR, "ce", 3), (INT_AR_PAIR, "ldst_colocated", 3),
     (INT_AR_PAIR, "ldst_dedicated", 3),
 ], ids=lambda v: str(getattr(v, "op", v)))
@@ -501,8 +500,8 @@ def test_reducer_warps_bit_identical_to_epilogue_ring(w, tile_m):
 
 
 def test_reducer_warps_ar_without_publish():
-    """GEMM-AR with no publish buffer: the plan keeps the partials in a buffer
-    of its own, made on the first such call, and the output is unchanged."""
+    """GEMM-AR with no publish buffer (the reducer warps' peer sums live in the
+    plan's own buffer either way): three calls, oracle bits on integer inputs."""
     w, r = INT_AR_PAIR, 1
     inp = inputs(w, r, 0, "int")
     d = runner.upload(inp, with_f32_out=False)
@@ -618,3 +617,49 @@ def test_benchmark_configuration_full_size_against_oracle(w):
     elif w.op == "rs":
         got["f32"] = d.f32_out.cpu().numpy()
     check_against_oracle(w, 0, got)
+
+
+
+# ----------------------------------------------------------------------------- pre-summed GEMM-AR
+# 704 pair tiles over 76 walkers (or 1408 single tiles over 152): walkers run
+# 9 or 10 tiles, more than the reducer warps' 8 completion slots, so reducer
+# items of a walker's ninth tile wait for the epilogue's acknowledgement of
+# its first
+INT_AR_LONG_WALK = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=2 * 2816, K=64, N=8192, R=2)
+
+
+@pytest.mark.parametrize("tile_m,stages,publish", [(256, 5, False), (256, 4, True), (128, 3, False),
+                                                   (128, 3, True)])
+def test_presum_ar_long_walks_bit_exact(tile_m, stages, publish):
+    """GEMM-AR with reducer warps that sum the peer partials ahead of the
+    MMAs: walks longer than the completion ring, with and without publish,
+    two calls in a row, give the oracle's bits on integer inputs."""
+    w, r = INT_AR_LONG_WALK, 1
+    inp = inputs(w, r, 0, "int")
+    d = runner.upload(inp, with_f32_out=publish)
+    with runner.make_plan(d, split=1, order="row", backend="tma_colocated_smem", tile_m=tile_m, tile_n=256,
+                          stages=stages) as plan:
+        for _ in range(2):
+            runner.call(plan, d)
+        assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+    got = {"out": runner.dev_to_u16(d.out)}
+    if publish:
+        got["f32"] = d.f32_out.cpu().numpy()
+    check_against_oracle(w, r, got, kind="int")
+
+
+@pytest.mark.parametrize("R", [1, 3, 8])
+def test_presum_ar_rank_counts_bit_exact(R):
+    """Pre-summed GEMM-AR for one rank (no peer: out = rne(P)), an odd rank
+    count and eight ranks, with an M tail: oracle bits on integer inputs for
+    the first and the last rank."""
+    w = wl.scaled(wl.QWEN2_7B_DOWN_AR, M=R * 200, K=192, N=512, R=R)
+    for r in sorted({0, R - 1}):
+        inp = inputs(w, r, 0, "int")
+        d = runner.upload(inp)
+        with runner.make_plan(d, split=1, order="row", backend="tma_colocated_smem", tile_m=256,
+                              tile_n=256) as plan:
+            runner.call(plan, d)
+            assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+        check_against_oracle(w, r, {"out": runner.dev_to_u16(d.out), "f32": d.f32_out.cpu().numpy()},
+                             kind="int")
