@@ -514,6 +514,11 @@ def main():
             baselines[w.op] = res
 
     a2a = measure_a2a(knobs["a2a"], peaks, stream) if rank == 0 and not args.no_baselines else None
+    extra = {}
+    if rank == 0 and not args.no_baselines:
+        extra["cfg5"] = measure_cfg5(peaks, stream)
+        extra["ar_split"] = measure_ar_split(peaks, stream)
+        extra["rs_staged"] = measure_rs_variants(peaks, stream)
     ring_attn = measure_attention(peaks, stream) if rank == 0 and not args.no_baselines else None
 
     # ---------------- CPU oracle baseline (rank 0, N = 1) ----------------
@@ -537,6 +542,7 @@ def main():
                 "gpu_launches": sum(launches_per_call(p) for p in plans) * args.steps,
                 "per_call": per_call,
                 "clocks": clk, "per_op": per_op, "baselines": baselines, "a2a": a2a, "ring_attention": ring_attn,
+                **extra,
                 "peaks": {**peaks, "source": peak_src}}
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -729,6 +735,104 @@ def measure_attention(peaks, stream, reps=20):
     res["roofline_frac_burst_peak"] = res["tflops"] / peaks["bf16_tflops"]
     out["head_parallel"] = res
     return out
+
+
+def time_calls(plan, d, stream, reps=20, warm=3) -> float:
+    """Mean microseconds per call over `reps` back-to-back calls after `warm`
+    untimed ones (CUDA events on the launching stream); checks the plan's
+    error word afterwards."""
+    import torch
+
+    from chunk_scheduled_communication_gb300 import runner
+    for _ in range(warm):
+        runner.call(plan, d, stream)
+    plan.check(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        runner.call(plan, d, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    plan.check(stream)
+    return e0.elapsed_time(e1) / reps * 1e3
+
+
+def measure_cfg5(peaks, stream):
+    """The Llama-3-70B FFN up-projection AG-GEMM (the pages' tuning-space
+    workload, Syncopate summary §6.3 / Fig. 11) at the best point of its sweep,
+    timed alone (burst tensor peak), beside the unfused baseline and the
+    flag-wait share of a traced plan."""
+    from chunk_scheduled_communication_gb300 import runner
+    w = wl.LLAMA3_70B_UP_AG
+    d = runner.upload(wl.make_inputs(w, r=0, seed=0))
+    split, order, kn = tuned.knobs_for("ag70")
+    with runner.make_plan(d, split=split, order=order, **kn) as p:
+        us = time_calls(p, d, stream)
+    with runner.make_plan(d, split=split, order=order, **{**kn, "backend": "unfused", "stages": 0}) as p:
+        unfused_us = time_calls(p, d, stream, reps=10)
+    with runner.make_plan(d, split=split, order=order, trace=1, **kn) as p:
+        time_calls(p, d, stream, reps=5, warm=1)
+        wait_ns, busy_ns = p.stats()
+    byts = algorithmic_bytes(w)
+    t_roof = max(w.flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+    return {"workload": w.name, "knobs": tuned.STEP_KNOBS["ag70"], "us": us, "tflops": w.flops / us / 1e6,
+            "roofline_frac_burst_peak": t_roof / (us * 1e-6), "unfused_us": unfused_us,
+            "fused_speedup_vs_unfused": unfused_us / us, "flag_wait_share": wait_ns / busy_ns if busy_ns else None}
+
+
+def measure_ar_split(peaks, stream):
+    """GEMM-AR against chunk split and message size (the pages' GEMM-AR
+    sensitivity, Syncopate summary §6.3 / Fig. 11: best near ~128 MB messages
+    and 2-3 splits): the staged backends -- the copy engine and co-located TMA
+    staging copy every peer partial into a receive buffer, chunk by chunk,
+    and the epilogue waits on each chunk's flag -- at splits 1-4, for the
+    Qwen2-7B shape (58.7 MB fp32 partial per rank) and the same layer over
+    8192 tokens (117.4 MB), beside the resident-peer kernel the step uses."""
+    from chunk_scheduled_communication_gb300 import runner
+    out = []
+    for w in (wl.QWEN2_7B_DOWN_AR, wl.scaled(wl.QWEN2_7B_DOWN_AR, M=8192)):
+        d = runner.upload(wl.make_inputs(w, r=0, seed=0), with_f32_out=False)
+        msg_mb = w.M * w.N * 4 / 1e6
+        byts = algorithmic_bytes(w)
+        pts = []
+        for be in ("ce", "tma_colocated"):
+            for split in (1, 2, 3, 4):
+                with runner.make_plan(d, split=split, order="row", backend=be, tile_m=256, tile_n=256) as p:
+                    us = time_calls(p, d, stream, reps=10)
+                pts.append({"backend": be, "split": split, "us": us, "gbs": byts / us / 1e3})
+        split, order, kn = tuned.knobs_for("ar")
+        with runner.make_plan(d, split=split, order=order, **kn) as p:
+            res_us = time_calls(p, d, stream, reps=20)
+        best = min(pts, key=lambda x: x["us"])
+        out.append({"workload": w.name, "message_mb_per_rank": msg_mb, "algorithmic_bytes": byts,
+                    "staged": pts, "best_staged": best, "worst_over_best_staged": max(x["us"] for x in pts) / best["us"],
+                    "resident_us": res_us, "resident_frac_hbm": byts / (res_us * 1e-6) / (peaks["hbm_gbs"] * 1e9)})
+        del d
+    return out
+
+
+def measure_rs_variants(peaks, stream):
+    """GEMM-RS beside the step's resident-peer pull kernel: staged backends
+    whose epilogue waits on every peer chunk's flag (co-located TMA staging
+    into the receive buffer, splits 1, 2, 4, with the flag-wait share), and
+    the push mode (send rows added at the destination by TMA reduce-add)."""
+    from chunk_scheduled_communication_gb300 import runner
+    w = wl.LLAMA3_8B_DOWN_RS
+    d = runner.upload(wl.make_inputs(w, r=0, seed=0))
+    split, order, kn = tuned.knobs_for("rs")
+    with runner.make_plan(d, split=split, order=order, **kn) as p:
+        pull_us = time_calls(p, d, stream)
+    with runner.make_plan(d, split=split, order=order, rs_push=1, **kn) as p:
+        push_us = time_calls(p, d, stream)
+    staged = []
+    for s in (1, 2, 4):
+        with runner.make_plan(d, split=s, order="row", backend="tma_colocated", tile_m=256, tile_n=256,
+                              trace=1) as p:
+            us = time_calls(p, d, stream, reps=10)
+            wait_ns, busy_ns = p.stats()
+        staged.append({"backend": "tma_colocated", "split": s, "us": us,
+                       "flag_wait_share": wait_ns / busy_ns if busy_ns else None})
+    return {"workload": w.name, "pull_us": pull_us, "push_us": push_us, "staged": staged}
 
 
 def launches_per_call(plan) -> int:
