@@ -517,6 +517,8 @@ int plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_layout_
                     "no compiled kernel for tile_m " + std::to_string(s.tile_m) + ", tile_n " +
                         std::to_string(pl->lc.tile_n) + ", tile_k " + std::to_string(pl->lc.tile_k) +
                         ", stages " + std::to_string(pl->lc.stages) + " with this operator and backend");
+    if (kn.direct_fetch && s.op != SYN_OP_AG_GEMM)
+        return bail(SYN_ERR_UNSUPPORTED, "direct_fetch applies to AG-GEMM and A2A-GEMM only");
     if (kn.rs_push && (s.op != SYN_OP_GEMM_RS || epi_tma_rs(pl->lc) != 1))
         return bail(SYN_ERR_UNSUPPORTED,
                     "rs_push needs GEMM-RS with TMA_COLOCATED_SMEM reducer warps and a pipeline depth "
@@ -700,13 +702,28 @@ int gather_gemm(syn_plan_t plan, bool a2a, const void *const *shards, void *gath
         return fail(SYN_ERR_INVALID, "operand not 16-byte aligned");
     const int64_t row_bytes = s.K * 2;
     // tensor maps (cached on the operand pointers)
+    const bool direct = plan->kn.direct_fetch != 0;
     std::vector<const void *> key = {gathered, B, C};
+    if (direct)
+        for (int q = 0; q < s.R; ++q) key.push_back(shards[q]);
     if (key != plan->map_key) {
         if ((rc = encode_operands(plan, gathered, B)) != SYN_OK) return rc;
         // bf16 tile stores of the epilogue: 32 columns x 32 rows, 64-byte swizzle
         if ((rc = encode_2d(&plan->maps.c, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.N, s.M, 32, 32,
                             CU_TENSOR_MAP_SWIZZLE_64B)) != SYN_OK)
             return rc;
+        // direct fetch: each source shard as an A operand in place (same boxes as `gathered`)
+        if (direct) {
+            const int tk = plan->lc.tile_k;
+            const CUtensorMapSwizzle a_swz = tk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+            for (int q = 0; q < s.R; ++q) {
+                const int64_t rows = block_rows(s.rb, q);
+                if (rows == 0) continue;
+                if ((rc = encode_2d(&plan->maps.peer[q], shards[q], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.K,
+                                    (uint64_t)rows, tk, 128, a_swz)) != SYN_OK)
+                    return rc;
+            }
+        }
         plan->map_key = key;
     }
     plan->epoch += 1;
@@ -722,6 +739,7 @@ int gather_gemm(syn_plan_t plan, bool a2a, const void *const *shards, void *gath
     p.out = static_cast<uint16_t *>(C);
     p.f32_out = nullptr;
     p.epi_tma = 1;
+    p.direct_fetch = direct ? 1 : 0;  // (only where the backend's tiles wait on flags)
     return run(plan, p, static_cast<cudaStream_t>(stream));
 }
 

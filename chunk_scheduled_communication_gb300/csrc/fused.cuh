@@ -1110,18 +1110,32 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                 if (tile < 0) break;
                 const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
                 const int r0 = tmi * C::TILE_M + (int)crank * C::BM;  // this CTA's rows
+                // direct fetch: the source rank whose shard this tile's A rows
+                // are read from in place (-1: the staged copy in `gathered`)
+                int dq = -1;
                 if (OP == OP_AG && p.waits) {
                     int lo, hi;
                     chunk_range(p, r0, C::BM, lo, hi);
-                    for (int rc = lo; ok && rc <= hi; ++rc) {
-                        const int q = rc / p.split;
-                        if ((p.local_inplace && q == p.rank) || chunk_empty(p.rb, rc)) continue;
-                        ok = wait_flag(p.in_flags + rc * p.R + q, p, abort, WHERE_AG_FLAG,
-                                       rc * p.R + q, wait_ns);
+                    if (p.direct_fetch && lo <= hi && lo / p.split == hi / p.split) {
+                        const int q = lo / p.split;
+                        bool ready = true;
+                        for (int rc = lo; ready && rc <= hi; ++rc)
+                            if (!(p.local_inplace && q == p.rank) && !chunk_empty(p.rb, rc))
+                                ready = flag_ready(ptx::ld_acquire_gpu(p.in_flags + rc * p.R + q), p.epoch);
+                        if (!ready) dq = q;  // every row lies in source q's block
                     }
+                    if (dq < 0)
+                        for (int rc = lo; ok && rc <= hi; ++rc) {
+                            const int q = rc / p.split;
+                            if ((p.local_inplace && q == p.rank) || chunk_empty(p.rb, rc)) continue;
+                            ok = wait_flag(p.in_flags + rc * p.R + q, p, abort, WHERE_AG_FLAG,
+                                           rc * p.R + q, wait_ns);
+                        }
                     if (!ok) break;
                     ptx::fence_proxy_async();  // generic acquire -> async-proxy (TMA) reads
                 }
+                const CUtensorMap *amap = dq < 0 ? &tm.a : &tm.peer[dq];
+                const int ay = dq < 0 ? r0 : r0 - (int)p.rb.off[dq];
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = (int)(it % C::S);
                     const uint32_t ph = (it / C::S) & 1u;
@@ -1138,7 +1152,7 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                     if (leader) {
                         // arm the phase that both CTAs' bytes complete
                         ptx::mbar_arrive_expect_tx(full, C::TX_BYTES);
-                        ptx::tma_load_2d(a_dst, &tm.a, full, kb * C::BK, r0);
+                        ptx::tma_load_2d(a_dst, amap, full, kb * C::BK, ay);
 #pragma unroll
                         for (int i = 0; i < C::BN_CTA / 64; ++i)
                             ptx::tma_load_2d(b_dst + i * C::B_BOX_BYTES, &tm.b, full, bcol + i * 64,
@@ -1146,7 +1160,7 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                     } else {
                         // the odd CTA's bytes complete on the even CTA's ring barrier
                         const uint32_t rfull = ptx::mapa(full, 0);
-                        ptx::tma_load_2d_pair(a_dst, &tm.a, rfull, kb * C::BK, r0);
+                        ptx::tma_load_2d_pair(a_dst, amap, rfull, kb * C::BK, ay);
 #pragma unroll
                         for (int i = 0; i < C::BN_CTA / 64; ++i)
                             ptx::tma_load_2d_pair(b_dst + i * C::B_BOX_BYTES, &tm.b, rfull,

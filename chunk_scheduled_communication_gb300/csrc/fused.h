@@ -35,6 +35,7 @@ struct TensorMaps {  // CUtensorMap carries its own alignment
     CUtensorMap a;                 // AG: gathered [M,K]; RS/AR: A [M,K]   (bf16, box 64x128)
     CUtensorMap b;                 // B [K,N]                               (bf16, box 64x64)
     CUtensorMap peer[kMaxRanks];   // RS/AR: peer q partial rows            (fp32, box 32x128)
+                                   // AG with direct_fetch: shard q [rows_q, K] (bf16, as `a`)
     CUtensorMap f32out;            // RS/AR: send / publish [M,N]           (fp32, box 32x32)
     CUtensorMap c;                 // AG: C [M,N]                           (bf16, box 32x32)
     CUtensorMap red;               // RED: partials of reducing tiles       (fp32, box 32x32)
@@ -52,6 +53,8 @@ struct KernelParams {
     int32_t colocated;             // GEMM CTAs run the staging warp
     int32_t waits;                 // consumers wait on in_flags
     int32_t local_inplace;         // AG: local shard aliases its gathered slot
+    int32_t direct_fetch;          // AG: tiles whose chunks have not arrived read the source shard
+                                   // through tm.peer[q] instead of waiting
     int32_t drop_transfer;         // fault injection: arrival index never published
     int32_t delay_transfer;        // fault injection: arrival index published late (device stagers)
     uint32_t delay_ns;             //   by this long

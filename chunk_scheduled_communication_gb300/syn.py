@@ -44,7 +44,8 @@ class Knobs(ctypes.Structure):
                 ("trace", ctypes.c_int), ("stages", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("reduce_spread", ctypes.c_int), ("reduce_warps", ctypes.c_int),
                 ("ce_streams", ctypes.c_int), ("rs_push", ctypes.c_int), ("debug_delay_chunk", ctypes.c_int),
-                ("debug_delay_us", ctypes.c_int), ("debug_corrupt_entry", ctypes.c_int)]
+                ("debug_delay_us", ctypes.c_int), ("debug_corrupt_entry", ctypes.c_int),
+                ("direct_fetch", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -134,7 +135,7 @@ def _check(status: int, where: str):
 def make_knobs(backend="tma_colocated", comm_sms=8, tile_n=256, group_m=8, slice_kb=128, timeout_ns=0,
                drop_chunk=-1, trace=0, stages=0, tile_k=0, tile_m=0, reduce_spread=0,
                reduce_warps=0, ce_streams=0, delay_chunk=-1, delay_us=0, corrupt_entry=0,
-               rs_push=0) -> Knobs:
+               rs_push=0, direct_fetch=0) -> Knobs:
     k = Knobs()
     _check(lib().syn_knobs_default(ctypes.byref(k)), "syn_knobs_default")
     k.backend = BACKENDS[backend] if isinstance(backend, str) else int(backend)
@@ -146,6 +147,7 @@ def make_knobs(backend="tma_colocated", comm_sms=8, tile_n=256, group_m=8, slice
     k.ce_streams = ce_streams
     k.rs_push = rs_push
     k.debug_delay_chunk, k.debug_delay_us, k.debug_corrupt_entry = delay_chunk, delay_us, corrupt_entry
+    k.direct_fetch = direct_fetch
     return k
 
 

@@ -201,6 +201,16 @@ typedef struct {
                               entry (n - 1) mod n_transfers) an out-of-range
                               value at plan creation; every call then ends in
                               SYN_ERR_BOUNDS, with no out-of-range access     */
+    int direct_fetch;      /* AG-GEMM / A2A-GEMM with device stagers: 1 = a
+                              tile whose chunks have not arrived when the
+                              producer reaches it, and whose rows all come
+                              from one source rank, reads them in place
+                              from that rank's shard (TMA, the pages'
+                              in-place lowering) instead of waiting; tiles
+                              whose chunks have arrived read the staged
+                              copy.  The stagers still fill `gathered`
+                              completely.  0 = off: every tile waits for its
+                              chunks (default)                                */
 } syn_knobs_t;
 
 /* Everything a caller or a test may want to know about a plan. */

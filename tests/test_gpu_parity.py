@@ -663,3 +663,54 @@ def test_presum_ar_rank_counts_bit_exact(R):
             assert plan.sync() == syn.OK, syn.lib().syn_last_error()
         check_against_oracle(w, r, {"out": runner.dev_to_u16(d.out), "f32": d.f32_out.cpu().numpy()},
                              kind="int")
+
+
+
+# ----------------------------------------------------------------------------- direct fetch (AG-GEMM)
+INT_AG_ALIGNED = wl.scaled(wl.TINY_AG, M=4 * 256, K=192, N=512, R=4)   # every tile's rows in one shard
+
+
+@pytest.mark.parametrize("backend,tile_m", [("tma_colocated", 256), ("tma_colocated", 128), ("tma_dedicated", 256),
+                                            ("ce", 256), ("ldst_colocated", 256), ("tma_colocated_ragged", 256)])
+def test_direct_fetch_bit_exact(backend, tile_m):
+    """Tiles whose chunks have not arrived read the source shard in place:
+    C and the gathered buffer are the oracle's bits (integer inputs), two
+    calls in a row, for both ends of the rank range; on the ragged shape
+    (shards of 200 rows) tiles that straddle two shards wait as usual."""
+    w = INT_AG_ALIGNED
+    if backend == "tma_colocated_ragged":
+        backend, w = "tma_colocated", INT_AG_PAIR
+    for r in (0, w.R - 1):
+        inp = inputs(w, r, 0, "int")
+        d = runner.upload(inp)
+        with runner.make_plan(d, split=2, order="row", backend=backend, tile_m=tile_m, tile_n=256, comm_sms=2,
+                              direct_fetch=1) as plan:
+            for _ in range(2):
+                runner.call(plan, d)
+            assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+        check_against_oracle(w, r, {"out": runner.dev_to_u16(d.out), "gathered": runner.dev_to_u16(d.gathered)},
+                             kind="int")
+
+
+@pytest.mark.parametrize("backend", ["tma_colocated", "ce"])
+def test_direct_fetch_reads_an_unpublished_chunk_in_place(backend):
+    """A transfer whose ready flag is never published (its bytes are still
+    copied) stalls no tile when direct fetch is on: the tiles that need it
+    read the source shard, the call succeeds and matches the oracle.  (With
+    direct fetch off the same plan ends in SYN_ERR_TIMEOUT, as tested above.)"""
+    w, r = INT_AG_ALIGNED, 1
+    inp = inputs(w, r, 0, "int")
+    d = runner.upload(inp)
+    with runner.make_plan(d, split=2, order="row", backend=backend, tile_m=256, drop_chunk=2,
+                          timeout_ns=50_000_000, direct_fetch=1) as plan:
+        runner.call(plan, d)
+        assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+    check_against_oracle(w, r, {"out": runner.dev_to_u16(d.out), "gathered": runner.dev_to_u16(d.gathered)},
+                         kind="int")
+
+
+def test_direct_fetch_rejected_for_rs_ar():
+    d = runner.upload(inputs(INT_AR_PAIR, 0, 0, "int"))
+    with pytest.raises(syn.SynError) as e:
+        runner.make_plan(d, backend="tma_colocated", tile_m=256, direct_fetch=1)
+    assert e.value.status == syn.ERR_UNSUPPORTED
