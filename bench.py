@@ -48,8 +48,9 @@ WORKLOAD_NAME = ("llama3-8b-ffn-tp8 step: AG-GEMM up (8192x4096x1792) + qwen2-7b
                  "(4096x2368x3584) + GEMM-RS down (8192x1792x4096, send)")
 STEP = [wl.LLAMA3_8B_UP_AG, wl.QWEN2_7B_DOWN_AR, wl.LLAMA3_8B_DOWN_RS]
 
-# Knobs per operator: the measured best points, shared with the parity tests.
-DEFAULT_KNOBS = tuned.STEP_KNOBS
+# Knobs per operator: the autotuner's cache entries where present, else the
+# measured best points (shared with the parity tests).
+DEFAULT_KNOBS, KNOBS_SOURCE = tuned.bench_knobs()
 # A2A-GEMM (the MoE all-to-all + expert GEMM) is measured beside the step, on
 # its own line of the JSON ("a2a"), not inside the headline value.
 A2A = wl.MIXTRAL_8X7B_EXPERT_UP_A2A
@@ -393,7 +394,7 @@ def main():
                             w.flops / (peaks["bf16_tflops_sustained"] * 1e12),
                             byts / (peaks["hbm_gbs"] * 1e9)) / (ms * 1e-3),
                         "bound": "tensor" if w.flops / (tensor_peak * 1e12) >= byts / (peaks["hbm_gbs"] * 1e9) else "hbm",
-                        "knobs": knobs[w.op]}
+                        "knobs": knobs[w.op], "knobs_source": KNOBS_SOURCE.get(w.op)}
     dom = max(per_op, key=lambda k: per_op[k]["us"])
     dw = STEP[[w.op for w in STEP].index(dom)]
     if per_op[dom]["bound"] == "tensor":
@@ -519,11 +520,14 @@ def main():
     if rank == 0 and not args.no_baselines:
         for w, inp, d in zip(STEP, host_inputs, devs):
             res = {}
-            for be in ("unfused", "decomposed"):
+            for be in ("unfused", "decomposed", "decomposed_per_shard"):
                 kn = dict(knobs[w.op])
                 split, order = kn.pop("split"), kn.pop("order")
-                kn["backend"] = be
+                kn["backend"] = "decomposed" if be.startswith("decomposed") else be
                 kn["stages"] = 0  # the default depth of the baseline kernel instance
+                kn.pop("direct_fetch", None)
+                if be == "decomposed_per_shard":
+                    split = 1  # one GEMM launch per source shard / rank block
                 with runner.make_plan(d, split=split, order=order, **kn) as bp:
                     for _ in range(5):
                         runner.call(bp, d, stream)

@@ -6,17 +6,33 @@
 // that a wrong backend, SM allocation or tile order can cost more than 2x.
 // Entwine's abstract adds that the SMs given to communication must be balanced
 // against the slowdown of compute.  Here every candidate is a runtime
-// configuration of the same precompiled kernels, so the search is: create a
-// plan, warm up, time a few calls with CUDA events (L2 flushed in between),
-// keep the median, pick the fastest.
+// configuration of the same precompiled kernels, so the search creates a plan,
+// times back-to-back calls of it with CUDA events and keeps the fastest.
+//
+// The space is the product of seven dimensions -- staging placement (backend,
+// and communication SMs for the dedicated backends), tile shape, split, tile
+// order (with its group height), pipeline depth, the reduction path of
+// resident-peer GEMM-RS / GEMM-AR, and direct fetch for AG-GEMM -- too large
+// to time exhaustively (thousands of points).  It is searched by coordinate
+// descent from a good starting point: each dimension in turn is swept with
+// the others held at the best point so far; every candidate of a sweep gets
+// a cheap timing of two calls, the fastest tenth (at least two) are re-timed
+// over ten calls, and the best re-timed mean wins.  Passes repeat until one
+// finds nothing faster or the budget runs out.  A candidate whose plan cannot
+// be made (a depth that is not compiled, a shape outside its limits) costs no
+// GPU time; one that fails its call (a device wait running past the tuner's
+// short bound) is dropped at once.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <chrono>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <fstream>
+#include <functional>
+#include <set>
 #include <sstream>
 #include <string>
 #include <vector>
@@ -38,10 +54,20 @@ std::string cache_key(int op, int R, int rank, const syn_layout_t &L) {
     return o.str();
 }
 
-long field(const std::string &line, const char *name) {
+// Every field a candidate sets, as JSON members (also the dedupe key).
+std::string cand_json(const Cand &c) {
+    std::ostringstream o;
+    o << "\"backend\":" << (int)c.kn.backend << ",\"comm_sms\":" << c.kn.comm_sms << ",\"tile_m\":" << c.kn.tile_m
+      << ",\"tile_n\":" << c.kn.tile_n << ",\"group_m\":" << c.kn.group_m << ",\"stages\":" << c.kn.stages
+      << ",\"reduce_warps\":" << c.kn.reduce_warps << ",\"direct_fetch\":" << c.kn.direct_fetch
+      << ",\"split\":" << c.split << ",\"order\":" << (int)c.order;
+    return o.str();
+}
+
+long field(const std::string &line, const char *name, long dflt = -1) {
     const std::string k = std::string("\"") + name + "\":";
     const size_t pos = line.find(k);
-    if (pos == std::string::npos) return -1;
+    if (pos == std::string::npos) return dflt;
     return std::strtol(line.c_str() + pos + k.size(), nullptr, 10);
 }
 
@@ -57,6 +83,8 @@ struct DevBuf {
     ~DevBuf() { cudaFree(p); }
 };
 
+bool dedicated(syn_backend_t b) { return b == SYN_BACKEND_TMA_DEDICATED || b == SYN_BACKEND_LDST_DEDICATED; }
+
 }  // namespace
 
 extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *layout, double budget_s,
@@ -69,6 +97,7 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
     if (budget_s <= 0) budget_s = 60.0;
     const std::string key = cache_key(op, R, rank, L);
     const char *cache_path = std::getenv("SYN_TUNE_CACHE");
+    const char *log_path = std::getenv("SYN_TUNE_LOG");
 
     // ---- cache hit ----------------------------------------------------------
     if (cache_path != nullptr && *cache_path) {
@@ -79,13 +108,15 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
         if (!hit.empty()) {
             syn_knobs_default(best);
             best->backend = (syn_backend_t)field(hit, "backend");
-            best->comm_sms = (int)field(hit, "comm_sms");
-            best->tile_n = (int)field(hit, "tile_n");
-            const long tm = field(hit, "tile_m");
-            best->tile_m = tm > 0 ? (int)tm : 128;
-            best->group_m = (int)field(hit, "group_m");
-            *best_split = (int)field(hit, "split");
-            *best_order = (syn_order_t)field(hit, "order");
+            best->comm_sms = (int)field(hit, "comm_sms", 8);
+            best->tile_n = (int)field(hit, "tile_n", 256);
+            best->tile_m = (int)field(hit, "tile_m", 128);
+            best->group_m = (int)field(hit, "group_m", 8);
+            best->stages = (int)field(hit, "stages", 0);
+            best->reduce_warps = (int)field(hit, "reduce_warps", 0);
+            best->direct_fetch = (int)field(hit, "direct_fetch", 0);
+            *best_split = (int)field(hit, "split", 1);
+            *best_order = (syn_order_t)field(hit, "order", 0);
             if (best_us) *best_us = field_d(hit, "us");
             return SYN_OK;
         }
@@ -93,11 +124,9 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
 
     // ---- scratch operands ------------------------------------------------------
     const int64_t M_r = L.M / R;
-    DevBuf a, b, c, peerbuf, f32, flush;
-    const size_t flush_bytes = 512ull << 20;
+    DevBuf a, b, c, peerbuf, f32;
     if (cudaMalloc(&b.p, (size_t)L.K * L.N * 2) != cudaSuccess) return SYN_ERR_CUDA;
     if (cudaMalloc(&a.p, (size_t)L.M * L.K * 2) != cudaSuccess) return SYN_ERR_CUDA;
-    if (cudaMalloc(&flush.p, flush_bytes) != cudaSuccess) return SYN_ERR_CUDA;
     cudaMemset(a.p, 0x3C, (size_t)L.M * L.K * 2);
     cudaMemset(b.p, 0x3C, (size_t)L.K * L.N * 2);
     std::vector<const void *> shards(R);
@@ -120,100 +149,199 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
     }
     if (cudaDeviceSynchronize() != cudaSuccess) return SYN_ERR_CUDA;
 
-    // ---- candidate space ---------------------------------------------------------
-    std::vector<syn_backend_t> backends = {SYN_BACKEND_CE, SYN_BACKEND_TMA_DEDICATED,
-                                           SYN_BACKEND_TMA_COLOCATED, SYN_BACKEND_LDST_DEDICATED,
-                                           SYN_BACKEND_LDST_COLOCATED};
-    if (op != SYN_OP_AG_GEMM) backends.push_back(SYN_BACKEND_TMA_COLOCATED_SMEM);
-    const int comm_opts[] = {4, 8, 16};
-    const int split_opts[] = {1, 2, 3, 4, 6, 8};
-    const syn_order_t order_opts[] = {SYN_ORDER_ROW_MAJOR, SYN_ORDER_GROUPED, SYN_ORDER_COL_MAJOR};
-    // tile shapes: 256 x 256 on a CTA pair first (the fastest instances), then
-    // 128 x 256 and 128 x 128 on one CTA
-    const int shape_opts[][2] = {{256, 256}, {128, 256}, {128, 128}};
-    std::vector<Cand> cands;
-    for (const auto &shape : shape_opts) {
-        const int tm = shape[0], tn = shape[1];
-        if (L.N % tn) continue;
-        if (op == SYN_OP_GEMM_RS && M_r % tm) continue;
-        for (syn_backend_t be : backends)
-            for (int ci = 0;
-                 ci < ((be == SYN_BACKEND_TMA_DEDICATED || be == SYN_BACKEND_LDST_DEDICATED) ? 3 : 1); ++ci)
-                for (int sp : split_opts) {
-                    if (sp > M_r) continue;
-                    for (syn_order_t od : order_opts) {
-                        Cand cd;
-                        syn_knobs_default(&cd.kn);
-                        cd.kn.backend = be;
-                        cd.kn.comm_sms = comm_opts[ci];
-                        cd.kn.tile_m = tm;
-                        cd.kn.tile_n = tn;
-                        cd.split = sp;
-                        cd.order = od;
-                        cands.push_back(cd);
-                    }
-                }
-    }
-
     cudaStream_t st;
     if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return SYN_ERR_CUDA;
     cudaEvent_t e0, e1;
     cudaEventCreate(&e0);
     cudaEventCreate(&e1);
     const auto t_start = std::chrono::steady_clock::now();
-    double best_t = 1e30;
-    int best_i = -1;
-    for (size_t i = 0; i < cands.size(); ++i) {
-        const double el =
-            std::chrono::duration<double>(std::chrono::steady_clock::now() - t_start).count();
-        if (el > budget_s) break;
-        const Cand &cd = cands[i];
+    auto elapsed = [&]() {
+        return std::chrono::duration<double>(std::chrono::steady_clock::now() - t_start).count();
+    };
+    std::ofstream log;
+    if (log_path != nullptr && *log_path) log.open(log_path, std::ios::app);
+
+    // Mean time of one call over `reps` back-to-back calls between two events
+    // (after one untimed call), as the benchmark times its kernels: inputs at
+    // full size are larger than L2, and a flush between calls would leave
+    // dirty lines whose write-back lands on the next call.  -1 when the plan
+    // cannot be made or a call fails (the candidate is dropped).
+    auto measure = [&](const Cand &cd, int reps, const char *phase) -> double {
+        syn_knobs_t kn = cd.kn;
+        kn.timeout_ns = 50000000ull;  // a correct call finishes in milliseconds
         syn_plan_t plan = nullptr;
-        if (syn_plan_create(&plan, op, R, rank, &L, 0, cd.split, cd.order, &cd.kn) != SYN_OK) continue;
+        if (syn_plan_create(&plan, op, R, rank, &L, 0, cd.split, cd.order, &kn) != SYN_OK) return -1.0;
         auto call = [&]() -> int {
             if (op == SYN_OP_AG_GEMM) return syn_ag_gemm(plan, shards.data(), a.p, b.p, c.p, st);
-            if (op == SYN_OP_GEMM_RS)
-                return syn_gemm_rs(plan, a.p, b.p, peers.data(), (float *)f32.p, c.p, st);
+            if (op == SYN_OP_GEMM_RS) return syn_gemm_rs(plan, a.p, b.p, peers.data(), (float *)f32.p, c.p, st);
             return syn_gemm_ar(plan, a.p, b.p, peers.data(), nullptr, c.p, st);
         };
-        bool ok = true;
-        for (int w = 0; w < 2 && ok; ++w) ok = call() == SYN_OK;
-        ok = ok && syn_sync_status(plan, st) == SYN_OK;
-        std::vector<float> ts;
-        for (int rep = 0; rep < 5 && ok; ++rep) {
-            cudaMemsetAsync(flush.p, rep, flush_bytes, st);
+        bool ok = call() == SYN_OK && syn_sync_status(plan, st) == SYN_OK;
+        float ms = 0;
+        if (ok) {
             cudaEventRecord(e0, st);
-            ok = call() == SYN_OK;
+            for (int rep = 0; rep < reps && ok; ++rep) ok = call() == SYN_OK;
             cudaEventRecord(e1, st);
-            if (ok) ok = syn_sync_status(plan, st) == SYN_OK;
-            float ms = 0;
+            ok = ok && syn_sync_status(plan, st) == SYN_OK;
             if (ok) cudaEventElapsedTime(&ms, e0, e1);
-            ts.push_back(ms);
         }
         syn_plan_destroy(plan);
-        if (!ok) continue;
-        std::sort(ts.begin(), ts.end());
-        const double med = ts[ts.size() / 2] * 1000.0;
-        if (med < best_t) {
-            best_t = med;
-            best_i = (int)i;
+        if (!ok) return -1.0;
+        const double us = ms * 1000.0 / reps;
+        if (log.is_open())
+            log << "{" << key << ",\"phase\":\"" << phase << "\"," << cand_json(cd) << ",\"us\":" << us << "}\n";
+        return us;
+    };
+
+    // ---- the space ----------------------------------------------------------------
+    const bool ag = op == SYN_OP_AG_GEMM;
+    Cand start;
+    syn_knobs_default(&start.kn);
+    start.kn.tile_m = 256;
+    start.kn.tile_n = L.N % 256 == 0 ? 256 : 128;
+    if (op == SYN_OP_GEMM_RS && M_r % 256 != 0) start.kn.tile_m = 128;
+    if (L.M / R < 256 && ag) start.kn.tile_m = 128;
+    start.kn.backend = ag ? SYN_BACKEND_TMA_COLOCATED : SYN_BACKEND_TMA_COLOCATED_SMEM;
+    start.split = 1;
+    start.order = ag ? SYN_ORDER_GROUPED : SYN_ORDER_ROW_MAJOR;
+
+    using Sweep = std::function<std::vector<Cand>(const Cand &)>;
+    std::vector<Sweep> dims;
+    dims.push_back([&](const Cand &x) {  // staging placement
+        std::vector<Cand> v;
+        std::vector<syn_backend_t> bes = {SYN_BACKEND_CE, SYN_BACKEND_TMA_DEDICATED, SYN_BACKEND_TMA_COLOCATED,
+                                          SYN_BACKEND_LDST_DEDICATED, SYN_BACKEND_LDST_COLOCATED};
+        if (!ag) bes.push_back(SYN_BACKEND_TMA_COLOCATED_SMEM);
+        for (syn_backend_t be : bes)
+            for (int cs : {4, 8, 16}) {
+                if (!dedicated(be) && cs != 8) continue;
+                Cand y = x;
+                y.kn.backend = be;
+                y.kn.comm_sms = cs;
+                v.push_back(y);
+            }
+        return v;
+    });
+    dims.push_back([&](const Cand &x) {  // tile shape
+        std::vector<Cand> v;
+        for (auto sh : {std::pair<int, int>{256, 256}, {128, 256}, {128, 128}}) {
+            if (L.N % sh.second) continue;
+            if (op == SYN_OP_GEMM_RS && M_r % sh.first) continue;
+            Cand y = x;
+            y.kn.tile_m = sh.first;
+            y.kn.tile_n = sh.second;
+            y.kn.stages = 0;  // the default depth of the new instance
+            v.push_back(y);
         }
+        return v;
+    });
+    dims.push_back([&](const Cand &x) {  // split (chunks per shard / rank block)
+        std::vector<Cand> v;
+        for (int sp : {1, 2, 3, 4, 6, 8}) {
+            if (sp > M_r) continue;
+            Cand y = x;
+            y.split = sp;
+            v.push_back(y);
+        }
+        return v;
+    });
+    dims.push_back([&](const Cand &x) {  // tile order and group height
+        std::vector<Cand> v;
+        for (syn_order_t od : {SYN_ORDER_ROW_MAJOR, SYN_ORDER_COL_MAJOR}) {
+            Cand y = x;
+            y.order = od;
+            v.push_back(y);
+        }
+        for (int g : {4, 8, 16})
+            for (syn_order_t od : {SYN_ORDER_GROUPED, SYN_ORDER_BANDED}) {
+                if (od == SYN_ORDER_BANDED && !ag) continue;
+                Cand y = x;
+                y.order = od;
+                y.kn.group_m = g;
+                v.push_back(y);
+            }
+        return v;
+    });
+    dims.push_back([&](const Cand &x) {  // pipeline depth (uncompiled depths fail at plan creation)
+        std::vector<Cand> v;
+        for (int s = 0; s <= 9; ++s) {
+            if (s == 1 || s == 2) continue;
+            Cand y = x;
+            y.kn.stages = s;
+            v.push_back(y);
+        }
+        return v;
+    });
+    if (!ag)
+        dims.push_back([&](const Cand &x) {  // reduction path with resident peers
+            std::vector<Cand> v;
+            if (x.kn.backend != SYN_BACKEND_TMA_COLOCATED_SMEM) return v;
+            for (int rw : {0, -1}) {
+                Cand y = x;
+                y.kn.reduce_warps = rw;
+                y.kn.stages = 0;
+                v.push_back(y);
+            }
+            return v;
+        });
+    else
+        dims.push_back([&](const Cand &x) {  // direct fetch of chunks not yet arrived
+            std::vector<Cand> v;
+            for (int df : {0, 1}) {
+                Cand y = x;
+                y.kn.direct_fetch = df;
+                v.push_back(y);
+            }
+            return v;
+        });
+
+    // ---- coordinate descent ----------------------------------------------------------
+    Cand cur = start;
+    double t_cur = measure(cur, 10, "final");
+    std::set<std::string> seen = {cand_json(cur)};
+    if (t_cur < 0) {  // the starting point failed: fall back to the library defaults
+        syn_knobs_default(&cur.kn);
+        cur.split = 1;
+        cur.order = SYN_ORDER_ROW_MAJOR;
+        t_cur = measure(cur, 10, "final");
+        seen.insert(cand_json(cur));
+    }
+    for (int pass = 0; pass < 3 && elapsed() < budget_s; ++pass) {
+        bool improved = false;
+        for (size_t d = 0; d < dims.size() && elapsed() < budget_s; ++d) {
+            std::vector<std::pair<double, Cand>> quick;
+            for (const Cand &y : dims[d](cur)) {
+                if (elapsed() > budget_s) break;
+                if (!seen.insert(cand_json(y)).second) continue;
+                const double t = measure(y, 2, "quick");
+                if (t > 0) quick.emplace_back(t, y);
+            }
+            std::sort(quick.begin(), quick.end(),
+                      [](const std::pair<double, Cand> &l, const std::pair<double, Cand> &r) { return l.first < r.first; });
+            const size_t top = std::min(quick.size(), std::max<size_t>(2, (quick.size() + 9) / 10));
+            for (size_t i = 0; i < top && elapsed() < budget_s; ++i) {
+                const double t = measure(quick[i].second, 10, "final");
+                if (t > 0 && (t_cur < 0 || t < t_cur)) {
+                    t_cur = t;
+                    cur = quick[i].second;
+                    improved = true;
+                }
+            }
+        }
+        if (!improved) break;
     }
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
     cudaStreamDestroy(st);
-    if (best_i < 0) return SYN_ERR_CUDA;
-    *best = cands[best_i].kn;
-    *best_split = cands[best_i].split;
-    *best_order = cands[best_i].order;
-    if (best_us) *best_us = best_t;
+    if (t_cur < 0) return SYN_ERR_CUDA;
+    *best = cur.kn;
+    best->timeout_ns = 0;
+    *best_split = cur.split;
+    *best_order = cur.order;
+    if (best_us) *best_us = t_cur;
     if (cache_path != nullptr && *cache_path) {
         std::ofstream out(cache_path, std::ios::app);
-        out << "{" << key << ",\"backend\":" << (int)best->backend << ",\"comm_sms\":" << best->comm_sms
-            << ",\"tile_m\":" << best->tile_m << ",\"tile_n\":" << best->tile_n
-            << ",\"group_m\":" << best->group_m
-            << ",\"split\":" << *best_split << ",\"order\":" << (int)*best_order << ",\"us\":" << best_t
-            << "}\n";
+        out << "{" << key << "," << cand_json(cur) << ",\"us\":" << t_cur << "}\n";
     }
     return SYN_OK;
 }

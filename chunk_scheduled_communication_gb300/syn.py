@@ -331,8 +331,9 @@ def autotune(op, R, rank, M, N, K, budget_s=60.0):
     _check(L.syn_autotune(_op(op), R, rank, ctypes.byref(lay), budget_s, ctypes.byref(kn), ctypes.byref(split),
                           ctypes.byref(order), ctypes.byref(us)), "syn_autotune")
     return {"backend": BACKEND_NAMES.get(kn.backend, kn.backend), "comm_sms": kn.comm_sms,
-            "tile_m": kn.tile_m, "tile_n": kn.tile_n,
-            "group_m": kn.group_m, "split": split.value, "order": order.value, "us": us.value}
+            "tile_m": kn.tile_m, "tile_n": kn.tile_n, "group_m": kn.group_m, "stages": kn.stages,
+            "reduce_warps": kn.reduce_warps, "direct_fetch": kn.direct_fetch,
+            "split": split.value, "order": order.value, "us": us.value}
 
 
 def ag_gemm_noalloc(R, rank, M, N, K, shards, gathered, B, C, split=1, order="row", status=None,

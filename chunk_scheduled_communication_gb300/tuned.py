@@ -4,10 +4,18 @@ The knobs each operator of the benchmark step (and the A2A-GEMM beside it) is
 timed with: the measured best points on GB300 (256 x 256 output tiles on CTA
 pairs; AG-GEMM and A2A-GEMM staged by the co-located TMA warps, the AG-GEMM
 tiles whose chunks have not arrived yet reading the source shard in place;
-GEMM-RS and GEMM-AR reading the resident peer partials in place).  The parity tests run the
-same configurations, so what the benchmark times is what the tests check.
+GEMM-RS and GEMM-AR reading the resident peer partials in place).  Where the
+autotuner's cache (``tune_cache.jsonl`` beside this file, written by
+``tune_step.py``, or the file SYN_TUNE_CACHE names) holds an entry for a
+step operator's shape, that entry wins.  The parity tests run the same
+configurations, so what the benchmark times is what the tests check.
 """
 from __future__ import annotations
+
+import json
+import os
+
+from . import workloads as wl
 
 STEP_KNOBS = {
     "ag": dict(backend="tma_colocated", split=4, order="grouped", tile_m=256, tile_n=256, comm_sms=8, stages=0,
@@ -20,8 +28,53 @@ STEP_KNOBS = {
     "ag70": dict(backend="tma_colocated", split=1, order="row", tile_m=256, tile_n=256, comm_sms=8, stages=0),
 }
 
+STEP_WORKLOADS = {"ag": wl.LLAMA3_8B_UP_AG, "ar": wl.QWEN2_7B_DOWN_AR, "rs": wl.LLAMA3_8B_DOWN_RS}
+CACHE_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tune_cache.jsonl")
+_BACKEND_NAMES = {0: "ce", 1: "tma_dedicated", 2: "tma_colocated", 3: "tma_colocated_smem", 4: "unfused",
+                  5: "decomposed", 6: "ldst_dedicated", 7: "ldst_colocated"}
+_ORDER_NAMES = {0: "row", 1: "col", 2: "grouped", 3: "banded"}
+_OP_CODES = {"ag": 0, "rs": 1, "ar": 2}
+
+
+def cache_path() -> str:
+    return os.environ.get("SYN_TUNE_CACHE") or CACHE_PATH
+
+
+def from_cache(op: str, w: wl.Workload, rank: int = 0, path: str | None = None) -> dict | None:
+    """The autotuner's entry for (op, shape, rank) in STEP_KNOBS form, or None."""
+    path = path or cache_path()
+    if op not in _OP_CODES or not os.path.exists(path):
+        return None
+    hit = None
+    for line in open(path):
+        line = line.strip()
+        if not line:
+            continue
+        e = json.loads(line)
+        if (e.get("op"), e.get("R"), e.get("rank"), e.get("M"), e.get("N"), e.get("K")) == \
+                (_OP_CODES[op], w.R, rank, w.M, w.N, w.K) and "phase" not in e:
+            hit = e  # the latest entry wins, as in the tuner
+    if hit is None:
+        return None
+    return dict(backend=_BACKEND_NAMES[hit["backend"]], split=hit["split"], order=_ORDER_NAMES[hit["order"]],
+                tile_m=hit["tile_m"], tile_n=hit["tile_n"], comm_sms=hit["comm_sms"], group_m=hit["group_m"],
+                stages=hit["stages"], reduce_warps=hit["reduce_warps"], direct_fetch=hit["direct_fetch"])
+
+
+def bench_knobs() -> tuple[dict, dict]:
+    """(knobs per operator, where each came from): the tuner's cache entry for
+    each step operator's shape where there is one, else STEP_KNOBS."""
+    knobs = {k: dict(v) for k, v in STEP_KNOBS.items()}
+    source = {k: "measured defaults" for k in knobs}
+    for op, w in STEP_WORKLOADS.items():
+        hit = from_cache(op, w)
+        if hit is not None:
+            knobs[op] = hit
+            source[op] = "autotuner cache"
+    return knobs, source
+
 
 def knobs_for(op: str) -> tuple[int, str, dict]:
     """(split, order, remaining knobs) of operator `op`'s benchmark configuration."""
-    kn = dict(STEP_KNOBS[op])
+    kn = dict(bench_knobs()[0][op])
     return kn.pop("split"), kn.pop("order"), kn

@@ -387,12 +387,20 @@ int syn_plan_trace(syn_plan_t plan, uint64_t *out);
 
 /* Enumerate-and-measure autotuner (summary page, method ¶4 and paper §6.3,
  * Fig. 11; Entwine's communication-SM balance).  Allocates its own scratch
- * operands of the given shape, times every candidate (backend, comm_sms,
- * split, tile order, tile_n) with CUDA events, and returns the fastest.
- * budget_s bounds the wall time (0 = 60 s).  If the SYN_TUNE_CACHE
- * environment variable names a file, results are cached there as JSON lines
- * keyed by (op, R, rank, M, N, K) and a cache hit returns without measuring.
- * best_us may be NULL. */
+ * operands of the given shape and searches staging placement (backend and
+ * comm_sms), tile shape, split, tile order with group_m, pipeline depth,
+ * reduce_warps (GEMM-RS/AR) and direct_fetch (AG-GEMM) by coordinate descent:
+ * each dimension swept with the others held at the best point so far, every
+ * candidate timed over two back-to-back calls (CUDA events), the fastest
+ * tenth (at least two) re-timed over ten, the best re-timed mean kept;
+ * passes repeat until one finds nothing faster.  Candidates run
+ * with a 50 ms wait bound and are dropped on their first error.  budget_s
+ * bounds the wall time (0 = 60 s).  If the SYN_TUNE_CACHE environment
+ * variable names a file, results are cached there as JSON lines keyed by
+ * (op, R, rank, M, N, K) and a cache hit returns without measuring; if
+ * SYN_TUNE_LOG names a file, every timing is appended to it (phase "quick" or
+ * "final").  *best_us is the winner's re-timed mean, the smallest "final"
+ * timing of the search.  best_us may be NULL. */
 int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *layout,
                  double budget_s, syn_knobs_t *best, int *best_split,
                  syn_order_t *best_order, double *best_us);

@@ -327,12 +327,35 @@ def test_per_tile_trace_is_consistent(tile_m):
         assert (np.diff(tr[mine, 0]) >= 0).all()
 
 
-def test_autotune_small_budget(tmp_path, monkeypatch):
+@pytest.mark.parametrize("op", ["ag", "rs", "ar"])
+def test_autotune_winner_is_fastest_and_passes_parity(op, tmp_path, monkeypatch):
+    """The tuner returns the smallest re-timed median it recorded, the winning
+    knobs give the oracle's bits on integer inputs of the tuned shape, and a
+    second call is a cache hit with the same knobs."""
+    import json
+    w = {"ag": INT_AG_ALIGNED, "rs": INT_RS_PAIR, "ar": INT_AR_PAIR}[op]
     monkeypatch.setenv("SYN_TUNE_CACHE", str(tmp_path / "tune.jsonl"))
-    best = syn.autotune("ag", 4, 0, 4 * 256, 512, 512, budget_s=5.0)
+    monkeypatch.setenv("SYN_TUNE_LOG", str(tmp_path / "log.jsonl"))
+    best = syn.autotune(op, w.R, 0, w.M, w.N, w.K, budget_s=30.0)
     assert best["backend"] in syn.BACKENDS and best["us"] > 0
-    again = syn.autotune("ag", 4, 0, 4 * 256, 512, 512, budget_s=5.0)  # cache hit
-    assert again["backend"] == best["backend"] and again["split"] == best["split"]
+    finals = [json.loads(x)["us"] for x in open(tmp_path / "log.jsonl") if '"phase":"final"' in x]
+    assert finals and abs(best["us"] - min(finals)) <= 1e-4 * best["us"]
+    kn = {k: best[k] for k in ("backend", "comm_sms", "tile_m", "tile_n", "group_m", "stages", "reduce_warps",
+                               "direct_fetch")}
+    inp = inputs(w, 0, 0, "int")
+    d = runner.upload(inp)
+    with runner.make_plan(d, split=best["split"], order=best["order"], **kn) as plan:
+        for _ in range(2):
+            runner.call(plan, d)
+        assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+    got = {"out": runner.dev_to_u16(d.out)}
+    if op == "ag":
+        got["gathered"] = runner.dev_to_u16(d.gathered)
+    else:
+        got["f32"] = d.f32_out.cpu().numpy()
+    check_against_oracle(w, 0, got, kind="int")
+    again = syn.autotune(op, w.R, 0, w.M, w.N, w.K, budget_s=30.0)  # cache hit
+    assert {k: again[k] for k in kn} == kn and again["split"] == best["split"] and again["order"] == best["order"]
 
 
 # ----------------------------------------------------------------------------- pipeline depths
