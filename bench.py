@@ -526,8 +526,10 @@ def main():
                 kn["backend"] = "decomposed" if be.startswith("decomposed") else be
                 kn["stages"] = 0  # the default depth of the baseline kernel instance
                 kn.pop("direct_fetch", None)
-                if be == "decomposed_per_shard":
-                    split = 1  # one GEMM launch per source shard / rank block
+                if be in ("unfused", "decomposed_per_shard"):
+                    # unfused: the whole copy in one piece per source; decomposed
+                    # per shard: one GEMM launch per source shard / rank block
+                    split = 1
                 with runner.make_plan(d, split=split, order=order, **kn) as bp:
                     for _ in range(5):
                         runner.call(bp, d, stream)
