@@ -554,6 +554,7 @@ def main():
         extra["cfg5"] = measure_cfg5(peaks, stream)
         extra["ar_split"] = measure_ar_split(peaks, stream)
         extra["rs_staged"] = measure_rs_variants(peaks, stream)
+        extra["wave_quantization"] = measure_wave_quantization(peaks, stream)
     ring_attn = measure_attention(peaks, stream) if rank == 0 and not args.no_baselines else None
 
     # ---------------- CPU oracle baseline (rank 0, N = 1) ----------------
@@ -868,6 +869,43 @@ def measure_rs_variants(peaks, stream):
         staged.append({"backend": "tma_colocated", "split": s, "us": us,
                        "flag_wait_share": wait_ns / busy_ns if busy_ns else None})
     return {"workload": w.name, "pull_us": pull_us, "push_us": push_us, "staged": staged}
+
+
+def measure_wave_quantization(peaks, stream):
+    """The pages' first observation (Syncopate summary, Observation 1, paper
+    Fig. 2(a)): a GEMM over one chunk of rows leaves SMs idle when its tiles
+    do not fill whole waves, which is why splitting a GEMM into per-chunk
+    kernels (the decomposed baseline) loses.  The Llama-3-8B FFN up GEMM
+    (K 4096, N 1792) over M rows for M from one 256-row tile row to the full
+    8192: this library's kernel with nothing to stage (one rank, CTA pairs,
+    256 x 256 tiles over 76 pair walkers) and cuBLAS (torch.matmul), each
+    timed alone, as TFLOP/s and fraction of the burst peak."""
+    import torch
+
+    from chunk_scheduled_communication_gb300 import runner
+    K, N = 4096, 1792
+    out = []
+    for M in (256, 512, 1024, 2048, 2560, 2816, 3072, 4096, 5120, 5632, 6144, 8192):
+        w = wl.Workload(f"wave-M{M}", wl.OP_AG, 1, M, K, N, 1.0, 0.02)
+        d = runner.upload(wl.make_inputs(w, r=0, seed=0))
+        with runner.make_plan(d, split=1, order="grouped", backend="tma_colocated", tile_m=256, tile_n=256) as p:
+            us = time_calls(p, d, stream, reps=20)
+        for _ in range(3):
+            torch.matmul(d.gathered, d.B, out=d.out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(20):
+            torch.matmul(d.gathered, d.B, out=d.out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        cub = e0.elapsed_time(e1) / 20 * 1e3
+        tiles = (M // 256) * (N // 256)
+        flops = 2.0 * M * N * K
+        out.append({"M": M, "pair_tiles": tiles, "waves": tiles / 76, "us": us,
+                    "frac_of_burst": flops / (us * 1e-6) / (peaks["bf16_tflops"] * 1e12),
+                    "cublas_us": cub, "cublas_frac_of_burst": flops / (cub * 1e-6) / (peaks["bf16_tflops"] * 1e12)})
+        del d
+    return out
 
 
 def launches_per_call(plan) -> int:

@@ -75,23 +75,6 @@ constexpr int kSmemRings = 224 * 1024;
 #ifndef SYN_PS_NSL_MAX
 #define SYN_PS_NSL_MAX 2
 #endif
-#ifndef SYN_PS_PEER_CG
-#define SYN_PS_PEER_CG 0
-#endif
-#ifndef SYN_OUT_EVICT_FIRST
-#define SYN_OUT_EVICT_FIRST 0
-#endif
-
-// TMA tile store of an operator output that this kernel never reads back:
-// with SYN_OUT_EVICT_FIRST its lines are the first to leave L2, so they are
-// written back while this kernel runs rather than during the next one.
-__device__ __forceinline__ void store_out_tile(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y) {
-#if SYN_OUT_EVICT_FIRST
-    ptx::tma_store_2d_hint(map, src, x, y, ptx::policy_evict_first());
-#else
-    ptx::tma_store_2d(map, src, x, y);
-#endif
-}
 
 // Compile-time shape of one kernel instance: operator, tile width BN, GEMM
 // pipeline stages S, k-block depth BK (64: 128-byte A rows, 128-byte swizzle;
@@ -776,7 +759,7 @@ __device__ __forceinline__ void presum_rows(const KernelParams &p, int row0, int
                 if (q < p.R && q != p.rank) {
                     const float *src = reinterpret_cast<const float *>(p.stage_src[q]) + (int64_t)row * N +
                                        col0 + 4 * lane + 128 * h;
-                    pv[q][0][h] = SYN_PS_PEER_CG ? ptx::ld_cg_f4(src) : ptx::ld_nc_f4(src);
+                    pv[q][0][h] = ptx::ld_nc_f4(src);
                 }
 #pragma unroll
         for (int h = 0; h < H; ++h)
@@ -944,8 +927,8 @@ __device__ __forceinline__ void presum_epilogue(const KernelParams &p, const Ten
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                if (pub) store_out_tile(&tm.f32out, wbase + (uint32_t)(b * C::PS_SLOT), col, wrow0);
-                store_out_tile(&tm.c, ob, col, wrow0);
+                if (pub) ptx::tma_store_2d(&tm.f32out, wbase + (uint32_t)(b * C::PS_SLOT), col, wrow0);
+                ptx::tma_store_2d(&tm.c, ob, col, wrow0);
                 ptx::bulk_commit();
                 if (cc + C::PS_NSL < NCC) {
                     if (pub) ptx::bulk_wait_read<0>();  // the publish store has read slot b
@@ -1349,7 +1332,7 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                             ptx::fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                store_out_tile(&tm.c, buf, col, wrow0);
+                                ptx::tma_store_2d(&tm.c, buf, col, wrow0);
                                 ptx::bulk_commit();
                             }
                         }
@@ -1375,8 +1358,6 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                             // destination's receive accumulator
                             if (OP == OP_RS && !red && p.send_push)
                                 ptx::tma_reduce_add_2d(fmap, buf, col, fy);
-                            else if (fmap == &tm.f32out)  // send / publish rows
-                                store_out_tile(fmap, buf, col, fy);
                             else
                                 ptx::tma_store_2d(fmap, buf, col, fy);
                             ptx::bulk_commit();

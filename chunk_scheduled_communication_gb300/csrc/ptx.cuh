@@ -127,14 +127,6 @@ __device__ __forceinline__ float4 ld_f4(const float *p) {
                  : "memory");
     return v;
 }
-// 16-byte load cached in L2 only, with a 256-byte L2 fetch
-__device__ __forceinline__ float4 ld_cg_f4(const float *p) {
-    float4 v;
-    asm volatile("ld.global.cg.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
-}
 // 16-byte streaming load of data that is read-only for the whole kernel
 __device__ __forceinline__ float4 ld_nc_f4(const float *p) {
     float4 v;
@@ -173,21 +165,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y), "r"(src)
                  : "memory");
-}
-// the same with an L2 cache policy (createpolicy) for the written lines
-__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y,
-                                                  uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(x), "r"(y), "r"(src), "l"(policy)
-        : "memory");
-}
-// L2 policy: the lines are the first to leave L2 when room is needed
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
 }
 // shared -> global tile reduce-add (fp32 add into the destination, performed
 // at the memory side; bulk group of the issuing thread)

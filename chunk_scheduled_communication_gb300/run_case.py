@@ -81,6 +81,9 @@ def main(argv=None) -> int:
     ap.add_argument("--tile-k", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--comm-sms", type=int, default=8)
+    ap.add_argument("--direct-fetch", type=int, default=0)
+    ap.add_argument("--tuned", action="store_true",
+                    help="the benchmark's launch configuration of the operator (other knob flags ignored)")
     ap.add_argument("--calls", type=int, default=4)
     a = ap.parse_args(argv)
     if a.op in ATTN_WORKLOADS:
@@ -90,9 +93,14 @@ def main(argv=None) -> int:
     torch.cuda.set_device(0)
     d = runner.upload(wl.make_inputs(w, r=0), with_f32_out=(w.op == "rs"))  # RS: send rows; AR: no publish
     stream = torch.cuda.current_stream()
-    with runner.make_plan(d, split=a.split, order=a.order, backend=a.backend, tile_m=a.tile_m,
-                          tile_n=a.tile_n, tile_k=a.tile_k, stages=a.stages, comm_sms=a.comm_sms,
-                          group_m=a.group_m) as p:
+    if a.tuned:
+        from . import tuned
+        split, order, kn = tuned.knobs_for(a.op if a.op != "ag70" else "ag70")
+    else:
+        split, order = a.split, a.order
+        kn = dict(backend=a.backend, tile_m=a.tile_m, tile_n=a.tile_n, tile_k=a.tile_k, stages=a.stages,
+                  comm_sms=a.comm_sms, group_m=a.group_m, direct_fetch=a.direct_fetch)
+    with runner.make_plan(d, split=split, order=order, **kn) as p:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(a.calls):
@@ -101,7 +109,7 @@ def main(argv=None) -> int:
         torch.cuda.synchronize()
         p.check(stream)
         info = p.info()
-    print(json.dumps({"workload": w.name, "backend": a.backend, "split": a.split, "order": a.order,
+    print(json.dumps({"workload": w.name, "knobs": kn, "split": split, "order": order,
                       "tile_m": info.get("tile_m", a.tile_m), "calls": a.calls,
                       "us_per_call": e0.elapsed_time(e1) / a.calls * 1e3}), flush=True)
     return 0
