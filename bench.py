@@ -851,7 +851,8 @@ def measure_rs_variants(peaks, stream):
     """GEMM-RS beside the step's resident-peer pull kernel: staged backends
     whose epilogue waits on every peer chunk's flag (co-located TMA staging
     into the receive buffer, splits 1, 2, 4, with the flag-wait share), and
-    the push mode (send rows added at the destination by TMA reduce-add)."""
+    the push mode (send rows added at the destination by TMA reduce-add),
+    issued by the epilogue or by 8 / 32 dedicated push SMs."""
     from chunk_scheduled_communication_gb300 import runner
     w = wl.LLAMA3_8B_DOWN_RS
     d = runner.upload(wl.make_inputs(w, r=0, seed=0))
@@ -860,6 +861,10 @@ def measure_rs_variants(peaks, stream):
         pull_us = time_calls(p, d, stream)
     with runner.make_plan(d, split=split, order=order, rs_push=1, **kn) as p:
         push_us = time_calls(p, d, stream)
+    push_ded = {}
+    for n in (8, 32):  # the pushes issued by n dedicated push SMs instead of the epilogue
+        with runner.make_plan(d, split=split, order=order, rs_push=1, push_sms=n, **kn) as p:
+            push_ded[n] = time_calls(p, d, stream, reps=5)
     staged = []
     for s in (1, 2, 4):
         with runner.make_plan(d, split=s, order="row", backend="tma_colocated", tile_m=256, tile_n=256,
@@ -868,7 +873,8 @@ def measure_rs_variants(peaks, stream):
             wait_ns, busy_ns = p.stats()
         staged.append({"backend": "tma_colocated", "split": s, "us": us,
                        "flag_wait_share": wait_ns / busy_ns if busy_ns else None})
-    return {"workload": w.name, "pull_us": pull_us, "push_us": push_us, "staged": staged}
+    return {"workload": w.name, "pull_us": pull_us, "push_us": push_us, "push_dedicated_sms_us": push_ded,
+            "staged": staged}
 
 
 def measure_wave_quantization(peaks, stream):

@@ -141,6 +141,9 @@ struct syn_plan_s {
     uint64_t recv_bytes = 0;
     float *d_red = nullptr;                 // RED: fp32 partials of the reducing tiles
     size_t red_bytes = 0;
+    float *d_push = nullptr;                // dedicated push: send rows as produced [M, N]
+    int32_t *d_push_list = nullptr;         // dedicated push: send row chunks, production order
+    int n_push = 0;
     int64_t recv_slot_rows = 0;
     cudaStream_t side = nullptr;            // side stream 0 (DECOMPOSED copies; CE stream 0)
     std::vector<cudaStream_t> ce_side;      // CE: transfers go round-robin over these
@@ -176,6 +179,8 @@ void free_plan(syn_plan_s *pl) {
     cudaFree(pl->d_trace);
     cudaFree(pl->d_recv);
     cudaFree(pl->d_red);
+    cudaFree(pl->d_push);
+    cudaFree(pl->d_push_list);
     for (cudaEvent_t e : pl->ev_transfer) cudaEventDestroy(e);
     if (pl->ev_fork) cudaEventDestroy(pl->ev_fork);
     if (pl->ev_join) cudaEventDestroy(pl->ev_join);
@@ -369,7 +374,8 @@ int run(syn_plan_s *pl, KernelParams &p, cudaStream_t st) {
             return SYN_OK;
         case SYN_BACKEND_TMA_COLOCATED_SMEM:
             p.waits = 0;  // the peers' partials are resident: fetched per tile, no staging
-            SYN_CK(launch(pl, p, pl->grid_compute, st));
+            if (p.push_dedicated) p.n_comm = pl->grid_comm;
+            SYN_CK(launch(pl, p, pl->grid_compute + (p.push_dedicated ? pl->grid_comm : 0), st));
             return SYN_OK;
         case SYN_BACKEND_UNFUSED:
             if ((rc = ce_copies(pl, p, &st, 1, false, false)) != SYN_OK) return rc;
@@ -519,6 +525,9 @@ int plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_layout_
                         ", stages " + std::to_string(pl->lc.stages) + " with this operator and backend");
     if (kn.direct_fetch && s.op != SYN_OP_AG_GEMM)
         return bail(SYN_ERR_UNSUPPORTED, "direct_fetch applies to AG-GEMM and A2A-GEMM only");
+    const bool push_ded = kn.rs_push && kn.push_sms > 0;
+    if (kn.push_sms < 0 || kn.push_sms > 32) return bail(SYN_ERR_INVALID, "push_sms must be in [0, 32]");
+    if (kn.push_sms > 0 && !kn.rs_push) return bail(SYN_ERR_INVALID, "push_sms needs rs_push = 1");
     if (kn.rs_push && (s.op != SYN_OP_GEMM_RS || epi_tma_rs(pl->lc) != 1))
         return bail(SYN_ERR_UNSUPPORTED,
                     "rs_push needs GEMM-RS with TMA_COLOCATED_SMEM reducer warps and a pipeline depth "
@@ -532,8 +541,9 @@ int plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_layout_
         pl->resident = std::min(pl->num_sms, 2 * nc);
     }
     const int cta_per_tile = pl->lc.pair ? 2 : 1;
-    if (dedicated) {
-        pl->grid_comm = pl->lc.pair ? (kn.comm_sms + 1) / 2 * 2 : kn.comm_sms;
+    if (dedicated || push_ded) {
+        const int n = push_ded ? kn.push_sms : kn.comm_sms;
+        pl->grid_comm = pl->lc.pair ? (n + 1) / 2 * 2 : n;
         if (pl->grid_comm >= pl->resident) return bail(SYN_ERR_INVALID, "comm_sms >= resident CTAs");
         pl->grid_compute = std::min(s.n_tiles, (pl->resident - pl->grid_comm) / cta_per_tile) * cta_per_tile;
     } else {
@@ -582,6 +592,24 @@ int plan_create(syn_plan_t *out, syn_op_t op, int R, int rank, const syn_layout_
         // warps for the epilogue
         pl->red_bytes = (size_t)(s.op == SYN_OP_GEMM_RS ? s.M_r : s.M) * s.N * sizeof(float);
         PL_CK(cudaMalloc(&pl->d_red, pl->red_bytes));
+    }
+    if (push_ded) {
+        for (int rc = 0; rc < s.n_rc; ++rc)
+            if ((chunk_row0(s.rb, rc + 1) - chunk_row0(s.rb, rc)) % 32 != 0)
+                return bail(SYN_ERR_UNSUPPORTED, "push_sms needs chunks of a multiple of 32 rows");
+        // the send row chunks (every chunk of another rank's block), in the
+        // order the tile walk produces them: destinations in ring order
+        // r + 1, r + 2, ..., then chunk index
+        std::vector<int32_t> lst;
+        for (int d = 1; d < s.R; ++d) {
+            const int q = (s.rank + d) % s.R;
+            for (int j = 0; j < s.split; ++j) lst.push_back(q * s.split + j);
+        }
+        pl->n_push = (int)lst.size();
+        PL_CK(cudaMalloc(&pl->d_push, (size_t)s.M * s.N * sizeof(float)));
+        PL_CK(cudaMalloc(&pl->d_push_list, std::max<size_t>(1, lst.size()) * sizeof(int32_t)));
+        if (!lst.empty())
+            PL_CK(cudaMemcpy(pl->d_push_list, lst.data(), lst.size() * sizeof(int32_t), cudaMemcpyHostToDevice));
     }
     if (staged_peers(pl)) {
         pl->recv_slot_rows = (s.op == SYN_OP_GEMM_RS) ? s.M_r : s.M;
@@ -804,10 +832,19 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
                 return rc;
         }
         // fp32 tile stores of the epilogue (used by instances with staging room):
-        // 32 columns x 32 rows, 128-byte swizzle
+        // 32 columns x 32 rows, 128-byte swizzle; with dedicated push CTAs the
+        // send rows go to the plan's push buffer first
+        const bool push_ded = op == SYN_OP_GEMM_RS && plan->d_push != nullptr && f32_out != nullptr;
         if (f32_out != nullptr &&
-            (rc = encode_2d(&plan->maps.f32out, f32_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.N, s.M, 32,
-                            32)) != SYN_OK)
+            (rc = encode_2d(&plan->maps.f32out, push_ded ? plan->d_push : f32_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                            4, s.N, s.M, 32, 32)) != SYN_OK)
+            return rc;
+        // the push CTAs' boxes: 256 columns x 32 rows, no swizzle
+        if (push_ded &&
+            ((rc = encode_2d(&plan->maps.push_src, plan->d_push, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.N, s.M,
+                             kPushBoxCols, 32, CU_TENSOR_MAP_SWIZZLE_NONE)) != SYN_OK ||
+             (rc = encode_2d(&plan->maps.push_dst, f32_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.N, s.M,
+                             kPushBoxCols, 32, CU_TENSOR_MAP_SWIZZLE_NONE)) != SYN_OK))
             return rc;
         if (red_buf != nullptr &&
             (rc = encode_2d(&plan->maps.red, red_buf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.N,
@@ -831,6 +868,14 @@ static int rs_ar_call(syn_plan_t plan, int op, const void *A, const void *B,
     p.red_row_off = red_row_off;
     p.epi_tma = 1;
     p.send_push = (op == SYN_OP_GEMM_RS && plan->kn.rs_push) ? 1 : 0;
+    if (p.send_push && plan->d_push != nullptr && f32_out != nullptr) {
+        // dedicated push CTAs add the produced rows; the epilogue only stores them
+        p.send_push = 0;
+        p.push_dedicated = 1;
+        p.push_buf = plan->d_push;
+        p.push_list = plan->d_push_list;
+        p.n_push = plan->n_push;
+    }
     p.recv_slot_rows = plan->recv_slot_rows;
     p.peer_row_off = (staged && op == SYN_OP_GEMM_RS) ? (int32_t)(s.rank * s.M_r) : 0;
     p.out = static_cast<uint16_t *>(out);

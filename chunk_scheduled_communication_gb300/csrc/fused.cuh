@@ -177,7 +177,7 @@ struct KCfg {
     static constexpr int BAR_PEERDONE = BAR_DRAIN + 1;  // PAIR: odd producer finished issuing
     static constexpr int BAR_SLD = BAR_PEERDONE + 1;     // PRESUM: S slot loads, PS_NSL per epilogue warp
     static constexpr int NBAR = BAR_SLD + (PRESUM ? 4 * PS_NSL : 0);
-    static constexpr int COMM_BUF_BYTES = 32768;
+    static constexpr int COMM_BUF_BYTES = 32768;  // (one 256 x 32 fp32 push box)
     static constexpr int COMM_NBUF = OFF_BAR / COMM_BUF_BYTES;
     static constexpr int NBAR_ALL = NBAR > COMM_NBUF ? NBAR : COMM_NBUF;
     static constexpr int OFF_MISC = OFF_BAR + NBAR_ALL * 8;
@@ -479,6 +479,68 @@ __device__ __forceinline__ void stage_slices(const KernelParams &p, int worker, 
         }
     }
     land_pending();
+}
+
+// Dedicated push (GEMM-RS push mode with push CTAs): worker `worker` of `W`
+// takes boxes worker, worker + W, ... (32 rows x 256 columns, 32 KB) of the
+// send chunks in production order.  Per chunk it waits until the chunk's rows
+// are produced (out flag, acquire), then per box TMA-loads it from push_buf
+// into its shared-memory buffer and adds it into the destination's receive
+// accumulator (`send`) with a TMA tile reduce-add, reloading the buffer as
+// soon as the add has read it.  Once its boxes of a chunk have landed it
+// counts them; the worker that completes the chunk's count publishes the
+// delivered flag (in_flags[rc * R + rank]: this rank's contribution to chunk
+// rc has arrived).  Chunk rows are a multiple of 32 (the host checks).
+__device__ __forceinline__ void push_slices(const KernelParams &p, const TensorMaps &tm, int worker, int W,
+                                            uint32_t buf, uint32_t bar, volatile int *abort) {
+    constexpr int BOX_COLS = kPushBoxCols, BOX_ROWS = 32;
+    constexpr uint32_t BOX_BYTES = BOX_COLS * BOX_ROWS * 4;
+    const int n_flags = p.n_rc * p.R;
+    const int col_boxes = (p.N + BOX_COLS - 1) / BOX_COLS;
+    uint32_t *cnt = p.in_cnt + (size_t)counter_half(p.epoch) * n_flags;
+    uint32_t phase = 0;
+    unsigned long long wait_ns = 0;
+    for (int a = 0, g = 0; a < p.n_push; ++a) {
+        const int rc = p.push_list[a];
+        if (rc < 0 || rc >= p.n_rc) {  // the push table holds a chunk outside the plan
+            ptx::bulk_wait_all();
+            raise_error(p, SYN_ERR_BOUNDS, WHERE_BOUNDS, a);
+            *abort = 1;
+            return;
+        }
+        const int row0 = (int)chunk_row0(p.rb, rc);
+        const int n_boxes = (int)(chunk_row0(p.rb, rc + 1) - row0) / BOX_ROWS * col_boxes;
+        uint32_t mine = 0;
+        for (int bx = 0; bx < n_boxes; ++bx, ++g) {
+            if (g % W != worker) continue;
+            if (mine == 0) {
+                if (!wait_flag(p.out_flags + rc, p, abort, WHERE_STAGER, rc, wait_ns)) {
+                    ptx::bulk_wait_all();
+                    return;
+                }
+                ptx::fence_proxy_async();  // generic acquire -> async-proxy (TMA) reads
+            }
+            const int x = (bx % col_boxes) * BOX_COLS, y = row0 + (bx / col_boxes) * BOX_ROWS;
+            ptx::bulk_wait_read_all();  // the previous box's add has read the buffer
+            ptx::mbar_arrive_expect_tx(bar, BOX_BYTES);
+            ptx::tma_load_2d(buf, &tm.push_src, bar, x, y);
+            if (!bwait(bar, phase, abort, p)) {
+                bwait_drain(bar, phase, p);  // the load in flight lands before the CTA leaves
+                ptx::bulk_wait_all();
+                return;
+            }
+            phase ^= 1u;
+            ptx::tma_reduce_add_2d(&tm.push_dst, buf, x, y);
+            ptx::bulk_commit();
+            ++mine;
+        }
+        if (mine > 0) {
+            ptx::bulk_wait_all();  // this worker's adds to the chunk have landed
+            ptx::fence_proxy_async();
+            const uint32_t old = ptx::atom_add_acq_rel_gpu(cnt + rc * p.R + p.rank, mine);
+            if (old + mine == (uint32_t)n_boxes) ptx::st_release_gpu(p.in_flags + rc * p.R + p.rank, p.epoch);
+        }
+    }
 }
 
 // Load/store staging (the pages' load/store lowerings): warp `worker` of `W`
@@ -996,7 +1058,13 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
             ptx::fence_proxy_async_smem();
         }
         __syncthreads();
-        if (p.ldst) {  // every warp copies with vector loads and stores
+        if (p.push_dedicated) {  // GEMM-RS push mode: add produced send chunks at their destinations
+            if ((int)threadIdx.x < C::COMM_NBUF) {
+                const int c = (int)threadIdx.x;
+                push_slices(p, tm, ((int)blockIdx.x - p.G) * C::COMM_NBUF + c, p.n_comm * C::COMM_NBUF,
+                            sbase + c * C::COMM_BUF_BYTES, bar0 + 8 * c, abort);
+            }
+        } else if (p.ldst) {  // every warp copies with vector loads and stores
             constexpr int NW = C::NTHREADS / 32;
             stage_slices_ldst(p, ((int)blockIdx.x - p.G) * NW + warp, p.n_comm * NW, lane, abort);
         } else if ((int)threadIdx.x < C::COMM_NBUF) {

@@ -39,7 +39,13 @@ struct TensorMaps {  // CUtensorMap carries its own alignment
     CUtensorMap f32out;            // RS/AR: send / publish [M,N]           (fp32, box 32x32)
     CUtensorMap c;                 // AG: C [M,N]                           (bf16, box 32x32)
     CUtensorMap red;               // RED: partials of reducing tiles       (fp32, box 32x32)
+    CUtensorMap push_src;          // dedicated push: push_buf [M,N]        (fp32, box 256x32, no swizzle)
+    CUtensorMap push_dst;          // dedicated push: send [M,N]            (fp32, box 256x32, no swizzle)
 };
+
+// Dedicated push CTAs move boxes of kPushBoxCols x 32 fp32 (the host encodes
+// the push tensor maps with the same box, no swizzle).
+constexpr int kPushBoxCols = 256;
 
 struct KernelParams {
     int32_t op, R, rank;
@@ -85,6 +91,13 @@ struct KernelParams {
                                    // with staging room store the epilogue through TMA
     float *red_buf;                // RED instances: fp32 partials of the reducing tiles,
     int32_t red_row_off;           // row r stored at row r - red_row_off
+    // GEMM-RS push mode with dedicated push CTAs (blockIdx.x >= G): the
+    // epilogue stores send rows into push_buf [M, N] and counts them as
+    // produced; the push CTAs add each produced chunk into f32_out (`send`)
+    const int32_t *push_list;      // send row chunks in production order
+    int32_t n_push;
+    int32_t push_dedicated;
+    float *push_buf;
 };
 
 // Receive-buffer slot of source rank q (the local rank has none).

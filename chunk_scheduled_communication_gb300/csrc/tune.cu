@@ -60,6 +60,7 @@ std::string cand_json(const Cand &c) {
     o << "\"backend\":" << (int)c.kn.backend << ",\"comm_sms\":" << c.kn.comm_sms << ",\"tile_m\":" << c.kn.tile_m
       << ",\"tile_n\":" << c.kn.tile_n << ",\"group_m\":" << c.kn.group_m << ",\"stages\":" << c.kn.stages
       << ",\"reduce_warps\":" << c.kn.reduce_warps << ",\"direct_fetch\":" << c.kn.direct_fetch
+      << ",\"push_sms\":" << c.kn.push_sms
       << ",\"split\":" << c.split << ",\"order\":" << (int)c.order;
     return o.str();
 }
@@ -95,7 +96,10 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
     const syn_layout_t L = *layout;
     if (L.M <= 0 || L.N <= 0 || L.K <= 0 || R < 1 || L.M % R != 0) return SYN_ERR_INVALID;
     if (budget_s <= 0) budget_s = 60.0;
-    const std::string key = cache_key(op, R, rank, L);
+    // push-mode GEMM-RS (requested through best->rs_push on input) is a
+    // different computation from pull mode: tuned and cached separately
+    const bool push = op == SYN_OP_GEMM_RS && best->rs_push != 0;
+    const std::string key = cache_key(op, R, rank, L) + (push ? ",\"push\":1" : "");
     const char *cache_path = std::getenv("SYN_TUNE_CACHE");
     const char *log_path = std::getenv("SYN_TUNE_LOG");
 
@@ -115,6 +119,8 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
             best->stages = (int)field(hit, "stages", 0);
             best->reduce_warps = (int)field(hit, "reduce_warps", 0);
             best->direct_fetch = (int)field(hit, "direct_fetch", 0);
+            best->rs_push = push ? 1 : 0;
+            best->push_sms = (int)field(hit, "push_sms", 0);
             *best_split = (int)field(hit, "split", 1);
             *best_order = (syn_order_t)field(hit, "order", 0);
             if (best_us) *best_us = field_d(hit, "us");
@@ -202,6 +208,7 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
     if (op == SYN_OP_GEMM_RS && M_r % 256 != 0) start.kn.tile_m = 128;
     if (L.M / R < 256 && ag) start.kn.tile_m = 128;
     start.kn.backend = ag ? SYN_BACKEND_TMA_COLOCATED : SYN_BACKEND_TMA_COLOCATED_SMEM;
+    start.kn.rs_push = push ? 1 : 0;
     start.split = 1;
     start.order = ag ? SYN_ORDER_GROUPED : SYN_ORDER_ROW_MAJOR;
 
@@ -272,6 +279,16 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
         }
         return v;
     });
+    if (push)
+        dims.push_back([&](const Cand &x) {  // who issues the pushes: the epilogue, or n push SMs
+            std::vector<Cand> v;
+            for (int n : {0, 4, 8, 16, 32}) {
+                Cand y = x;
+                y.kn.push_sms = n;
+                v.push_back(y);
+            }
+            return v;
+        });
     if (!ag)
         dims.push_back([&](const Cand &x) {  // reduction path with resident peers
             std::vector<Cand> v;
@@ -301,6 +318,7 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
     std::set<std::string> seen = {cand_json(cur)};
     if (t_cur < 0) {  // the starting point failed: fall back to the library defaults
         syn_knobs_default(&cur.kn);
+        cur.kn.rs_push = push ? 1 : 0;
         cur.split = 1;
         cur.order = SYN_ORDER_ROW_MAJOR;
         t_cur = measure(cur, 10, "final");

@@ -45,7 +45,7 @@ class Knobs(ctypes.Structure):
                 ("reduce_spread", ctypes.c_int), ("reduce_warps", ctypes.c_int),
                 ("ce_streams", ctypes.c_int), ("rs_push", ctypes.c_int), ("debug_delay_chunk", ctypes.c_int),
                 ("debug_delay_us", ctypes.c_int), ("debug_corrupt_entry", ctypes.c_int),
-                ("direct_fetch", ctypes.c_int)]
+                ("direct_fetch", ctypes.c_int), ("push_sms", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -135,7 +135,7 @@ def _check(status: int, where: str):
 def make_knobs(backend="tma_colocated", comm_sms=8, tile_n=256, group_m=8, slice_kb=128, timeout_ns=0,
                drop_chunk=-1, trace=0, stages=0, tile_k=0, tile_m=0, reduce_spread=0,
                reduce_warps=0, ce_streams=0, delay_chunk=-1, delay_us=0, corrupt_entry=0,
-               rs_push=0, direct_fetch=0) -> Knobs:
+               rs_push=0, direct_fetch=0, push_sms=0) -> Knobs:
     k = Knobs()
     _check(lib().syn_knobs_default(ctypes.byref(k)), "syn_knobs_default")
     k.backend = BACKENDS[backend] if isinstance(backend, str) else int(backend)
@@ -148,6 +148,7 @@ def make_knobs(backend="tma_colocated", comm_sms=8, tile_n=256, group_m=8, slice
     k.rs_push = rs_push
     k.debug_delay_chunk, k.debug_delay_us, k.debug_corrupt_entry = delay_chunk, delay_us, corrupt_entry
     k.direct_fetch = direct_fetch
+    k.push_sms = push_sms
     return k
 
 
@@ -321,10 +322,11 @@ class Plan:
         _check(self.sync(stream), "syn_sync_status")
 
 
-def autotune(op, R, rank, M, N, K, budget_s=60.0):
+def autotune(op, R, rank, M, N, K, budget_s=60.0, rs_push=0):
     L = lib()
     lay = Layout(M, N, K, 0, 0, 0)
     kn = Knobs()
+    kn.rs_push = rs_push
     split = ctypes.c_int()
     order = ctypes.c_int()
     us = ctypes.c_double()
@@ -332,7 +334,8 @@ def autotune(op, R, rank, M, N, K, budget_s=60.0):
                           ctypes.byref(order), ctypes.byref(us)), "syn_autotune")
     return {"backend": BACKEND_NAMES.get(kn.backend, kn.backend), "comm_sms": kn.comm_sms,
             "tile_m": kn.tile_m, "tile_n": kn.tile_n, "group_m": kn.group_m, "stages": kn.stages,
-            "reduce_warps": kn.reduce_warps, "direct_fetch": kn.direct_fetch,
+            "reduce_warps": kn.reduce_warps, "direct_fetch": kn.direct_fetch, "rs_push": kn.rs_push,
+            "push_sms": kn.push_sms,
             "split": split.value, "order": order.value, "us": us.value}
 
 

@@ -211,6 +211,19 @@ typedef struct {
                               copy.  The stagers still fill `gathered`
                               completely.  0 = off: every tile waits for its
                               chunks (default)                                */
+    int push_sms;          /* GEMM-RS push mode (rs_push = 1): 0 = the epilogue
+                              warps add each send tile into `send` with TMA
+                              tile reduce-adds; n > 0 = n dedicated push CTAs
+                              (SMs) of the same grid do it instead: the
+                              epilogue stores send rows into a plan buffer and
+                              counts each row chunk produced, and the push
+                              CTAs, as each chunk's produced flag arrives (in
+                              production order: destinations in ring order),
+                              add it into `send` with bulk reduce-adds and
+                              publish its delivered flag (syn_plan_flags:
+                              in_flags[rc * R + rank]).  The compute grid
+                              shrinks by n SMs: the communication-SM balance
+                              of the Entwine abstract.  1..32             */
 } syn_knobs_t;
 
 /* Everything a caller or a test may want to know about a plan. */
@@ -400,7 +413,10 @@ int syn_plan_trace(syn_plan_t plan, uint64_t *out);
  * (op, R, rank, M, N, K) and a cache hit returns without measuring; if
  * SYN_TUNE_LOG names a file, every timing is appended to it (phase "quick" or
  * "final").  *best_us is the winner's re-timed mean, the smallest "final"
- * timing of the search.  best_us may be NULL. */
+ * timing of the search.  best_us may be NULL.
+ * *best is also read on input for one field: best->rs_push != 0 with
+ * SYN_OP_GEMM_RS tunes push mode (a different computation, cached under its
+ * own key) and adds push_sms (0, 4, 8, 16, 32) to the search. */
 int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *layout,
                  double budget_s, syn_knobs_t *best, int *best_split,
                  syn_order_t *best_order, double *best_us);

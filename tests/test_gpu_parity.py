@@ -358,6 +358,24 @@ def test_autotune_winner_is_fastest_and_passes_parity(op, tmp_path, monkeypatch)
     assert {k: again[k] for k in kn} == kn and again["split"] == best["split"] and again["order"] == best["order"]
 
 
+def test_autotune_push_mode_searches_push_sms(tmp_path, monkeypatch):
+    """Push-mode GEMM-RS is tuned as its own problem: the search includes the
+    number of dedicated push SMs, returns push mode, and the winner is the
+    smallest re-timed mean recorded."""
+    import json
+    w = INT_RS_PAIR
+    monkeypatch.setenv("SYN_TUNE_CACHE", str(tmp_path / "tune.jsonl"))
+    monkeypatch.setenv("SYN_TUNE_LOG", str(tmp_path / "log.jsonl"))
+    best = syn.autotune("rs", w.R, 0, w.M, w.N, w.K, budget_s=30.0, rs_push=1)
+    assert best["rs_push"] == 1 and best["us"] > 0
+    rows = [json.loads(x) for x in open(tmp_path / "log.jsonl")]
+    assert {0, 4, 8}.issubset({r["push_sms"] for r in rows})
+    finals = [r["us"] for r in rows if r["phase"] == "final"]
+    assert abs(best["us"] - min(finals)) <= 1e-4 * best["us"]
+    pull = syn.autotune("rs", w.R, 0, w.M, w.N, w.K, budget_s=30.0)  # a separate cache entry
+    assert pull["rs_push"] == 0 and pull["push_sms"] == 0
+
+
 # ----------------------------------------------------------------------------- pipeline depths
 INT_RS_SMALL = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=4 * 128, K=192, N=512, R=4)
 
@@ -737,3 +755,55 @@ def test_direct_fetch_rejected_for_rs_ar():
     with pytest.raises(syn.SynError) as e:
         runner.make_plan(d, backend="tma_colocated", tile_m=256, direct_fetch=1)
     assert e.value.status == syn.ERR_UNSUPPORTED
+
+
+
+@pytest.mark.parametrize("w,push_sms,kind", [(INT_RS_PAIR, 2, "int"), (INT_RS_SPREAD, 6, "int"),
+                                             (wl.LLAMA3_8B_DOWN_RS, 16, "normal")], ids=["pair", "spread", "full"])
+def test_rs_push_dedicated_sms_adds_send_rows(w, push_sms, kind):
+    """GEMM-RS push mode with dedicated push CTAs: the epilogue stores the send
+    rows, and the push CTAs add each produced chunk into `send` (bulk
+    reduce-add) and publish its delivered flag.  Against the oracle's P: init
+    + P after one call and (init + P) + P after two (bit-exact for integer
+    inputs), local rows untouched, out_r unchanged, every chunk delivered."""
+    r = 1
+    inp = inputs(w, r, 0, kind)
+    rng = np.random.default_rng(11)
+    init = rng.integers(-4, 5, size=(w.M, w.N)).astype(np.float32) if kind == "int" else \
+        rng.standard_normal((w.M, w.N)).astype(np.float32)
+    d = runner.upload(inp)
+    d.f32_out.copy_(torch.from_numpy(init))
+    with runner.make_plan(d, split=2, order="row", backend="tma_colocated_smem", tile_m=256, tile_n=256,
+                          rs_push=1, push_sms=push_sms) as plan:
+        assert plan.info()["grid_comm"] == push_sms
+        runner.call(plan, d)
+        assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+        once = d.f32_out.cpu().numpy()
+        runner.call(plan, d)
+        assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+        twice = d.f32_out.cpu().numpy()
+        fin, _ = plan.flags()
+        info = plan.info()
+    keep = np.ones(w.M, bool)
+    keep[r * w.M_r:(r + 1) * w.M_r] = False
+    _, P = oracle.gemm_rs(inp.A, inp.B, inp.peers, w.R, r, send_rows=(0, w.M))
+    want_once = init[keep] + P[keep]
+    want_twice = want_once + P[keep]
+    if kind == "int":
+        assert (once[keep] == want_once).all() and (twice[keep] == want_twice).all()
+    else:
+        for got_, want_ in ((once[keep], want_once), (twice[keep], want_twice)):
+            ok, exc, frob = runner.f_close(got_, want_)
+            assert ok, (exc, frob)
+    assert (once[~keep] == init[~keep]).all() and (twice[~keep] == init[~keep]).all()
+    for rc in range(info["n_row_chunks"]):
+        if rc // info["split"] != r:
+            assert fin[rc * w.R + r] == info["epoch"]
+    check_against_oracle(w, r, {"out": runner.dev_to_u16(d.out)}, kind=kind)
+
+
+def test_push_sms_needs_push_mode():
+    d = runner.upload(inputs(INT_RS_PAIR, 0, 0, "int"))
+    with pytest.raises(syn.SynError) as e:
+        runner.make_plan(d, backend="tma_colocated_smem", tile_m=256, push_sms=4)
+    assert e.value.status == syn.ERR_INVALID
