@@ -176,7 +176,11 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
         syn_knobs_t kn = cd.kn;
         kn.timeout_ns = 50000000ull;  // a correct call finishes in milliseconds
         syn_plan_t plan = nullptr;
-        if (syn_plan_create(&plan, op, R, rank, &L, 0, cd.split, cd.order, &kn) != SYN_OK) return -1.0;
+        if (syn_plan_create(&plan, op, R, rank, &L, 0, cd.split, cd.order, &kn) != SYN_OK) {
+            if (log.is_open())  // a point outside the instance's limits or not compiled
+                log << "{" << key << ",\"phase\":\"dropped\"," << cand_json(cd) << ",\"us\":-1}\n";
+            return -1.0;
+        }
         auto call = [&]() -> int {
             if (op == SYN_OP_AG_GEMM) return syn_ag_gemm(plan, shards.data(), a.p, b.p, c.p, st);
             if (op == SYN_OP_GEMM_RS) return syn_gemm_rs(plan, a.p, b.p, peers.data(), (float *)f32.p, c.p, st);
@@ -192,7 +196,11 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
             if (ok) cudaEventElapsedTime(&ms, e0, e1);
         }
         syn_plan_destroy(plan);
-        if (!ok) return -1.0;
+        if (!ok) {
+            if (log.is_open())
+                log << "{" << key << ",\"phase\":\"failed\"," << cand_json(cd) << ",\"us\":-1}\n";
+            return -1.0;
+        }
         const double us = ms * 1000.0 / reps;
         if (log.is_open())
             log << "{" << key << ",\"phase\":\"" << phase << "\"," << cand_json(cd) << ",\"us\":" << us << "}\n";

@@ -411,8 +411,9 @@ int syn_plan_trace(syn_plan_t plan, uint64_t *out);
  * bounds the wall time (0 = 60 s).  If the SYN_TUNE_CACHE environment
  * variable names a file, results are cached there as JSON lines keyed by
  * (op, R, rank, M, N, K) and a cache hit returns without measuring; if
- * SYN_TUNE_LOG names a file, every timing is appended to it (phase "quick" or
- * "final").  *best_us is the winner's re-timed mean, the smallest "final"
+ * SYN_TUNE_LOG names a file, every candidate is appended to it (phase
+ * "quick" or "final" with its time; "dropped" when its plan cannot be made,
+ * "failed" when a call failed, both with us = -1).  *best_us is the winner's re-timed mean, the smallest "final"
  * timing of the search.  best_us may be NULL.
  * *best is also read on input for one field: best->rs_push != 0 with
  * SYN_OP_GEMM_RS tunes push mode (a different computation, cached under its

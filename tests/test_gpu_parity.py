@@ -339,6 +339,7 @@ def test_autotune_winner_is_fastest_and_passes_parity(op, tmp_path, monkeypatch)
     best = syn.autotune(op, w.R, 0, w.M, w.N, w.K, budget_s=30.0)
     assert best["backend"] in syn.BACKENDS and best["us"] > 0
     finals = [json.loads(x)["us"] for x in open(tmp_path / "log.jsonl") if '"phase":"final"' in x]
+    assert finals
     assert finals and abs(best["us"] - min(finals)) <= 1e-4 * best["us"]
     kn = {k: best[k] for k in ("backend", "comm_sms", "tile_m", "tile_n", "group_m", "stages", "reduce_warps",
                                "direct_fetch")}
@@ -369,7 +370,7 @@ def test_autotune_push_mode_searches_push_sms(tmp_path, monkeypatch):
     best = syn.autotune("rs", w.R, 0, w.M, w.N, w.K, budget_s=30.0, rs_push=1)
     assert best["rs_push"] == 1 and best["us"] > 0
     rows = [json.loads(x) for x in open(tmp_path / "log.jsonl")]
-    assert {0, 4, 8}.issubset({r["push_sms"] for r in rows})
+    assert {0, 4, 8, 16, 32}.issubset({r["push_sms"] for r in rows})  # tried (timed or dropped)
     finals = [r["us"] for r in rows if r["phase"] == "final"]
     assert abs(best["us"] - min(finals)) <= 1e-4 * best["us"]
     pull = syn.autotune("rs", w.R, 0, w.M, w.N, w.K, budget_s=30.0)  # a separate cache entry
