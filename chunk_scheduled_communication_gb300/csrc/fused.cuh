@@ -598,15 +598,27 @@ __device__ __forceinline__ void stage_slices_ldst(const KernelParams &p, int wor
 }
 
 // ------------------------------------------------------------------ epilogue helpers
+// 32-column chunks of tile column tni that hold columns < N (all BN / 32 but
+// in the last tile column when N is not a multiple of the tile width); the
+// chunks past N are neither read from TMEM nor stored nor fed with peers.
+template <int BN>
+__device__ __forceinline__ int live_chunks(const KernelParams &p, int tni) {
+    const int left = p.N - tni * BN;
+    return left >= BN ? BN / 32 : (left + 31) / 32;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ void store_bf16_row32(uint16_t *dst, const float (&f)[32]) {
+// (lim: the columns left in the row from dst on; N is a multiple of 8, so a
+// 16-byte vector is either wholly inside the row or wholly past its end)
+__device__ __forceinline__ void store_bf16_row32(uint16_t *dst, const float (&f)[32], int lim) {
     uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+        if (8 * j >= lim) break;
         uint4 v;
         v.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
         v.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
@@ -616,10 +628,11 @@ __device__ __forceinline__ void store_bf16_row32(uint16_t *dst, const float (&f)
     }
 }
 
-__device__ __forceinline__ void store_f32_row32(float *dst, const float (&f)[32]) {
+__device__ __forceinline__ void store_f32_row32(float *dst, const float (&f)[32], int lim) {
     float4 *d = reinterpret_cast<float4 *>(dst);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) d[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+    for (int j = 0; j < 8; ++j)
+        if (4 * j < lim) d[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
 }
 
 // Producer side of a tile that writes send/publish rows: once this warp's rows
@@ -693,10 +706,10 @@ __device__ __forceinline__ void reduce_rows(const KernelParams &p, int row0, int
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int row = row0 + rr + u;
-            const bool live = row < p.M;
             const float *src = p.red_buf + (int64_t)(row - p.red_row_off) * N + col0 + 4 * lane;
 #pragma unroll
             for (int h = 0; h < H; ++h) {
+                const bool live = row < p.M && col0 + 4 * lane + 128 * h < N;
                 acc[u][h] = live ? ptx::ld_f4(src + 128 * h) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int q = 0; q < kMaxRanks; ++q)
@@ -712,6 +725,7 @@ __device__ __forceinline__ void reduce_rows(const KernelParams &p, int row0, int
             const int orow = OP == OP_RS ? row - p.rank * p.M_r : row;
 #pragma unroll
             for (int h = 0; h < H; ++h) {
+                if (col0 + 4 * lane + 128 * h >= N) continue;
                 float4 a = acc[u][h];
                 const float4 sum = peer_sum(p, pv, u, h);
                 a.x = a.x + sum.x;
@@ -818,15 +832,16 @@ __device__ __forceinline__ void presum_rows(const KernelParams &p, int row0, int
         for (int h = 0; h < H; ++h)
 #pragma unroll
             for (int q = 0; q < kMaxRanks; ++q)
-                if (q < p.R && q != p.rank) {
+                if (q < p.R && q != p.rank && col0 + 4 * lane + 128 * h < N) {
                     const float *src = reinterpret_cast<const float *>(p.stage_src[q]) + (int64_t)row * N +
                                        col0 + 4 * lane + 128 * h;
                     pv[q][0][h] = ptx::ld_nc_f4(src);
                 }
 #pragma unroll
         for (int h = 0; h < H; ++h)
-            ptx::st_f4(p.red_buf + (int64_t)(row - p.red_row_off) * N + col0 + 4 * lane + 128 * h,
-                       peer_sum(p, pv, 0, h));
+            if (col0 + 4 * lane + 128 * h < N)
+                ptx::st_f4(p.red_buf + (int64_t)(row - p.red_row_off) * N + col0 + 4 * lane + 128 * h,
+                           peer_sum(p, pv, 0, h));
     }
 }
 
@@ -891,7 +906,6 @@ __device__ __forceinline__ void presum_epilogue(const KernelParams &p, const Ten
                                                 uint32_t crank, bool leader, int warp, int lane,
                                                 volatile int *abort) {
     constexpr int PER_Q = 16;
-    constexpr int NCC = BN / 32;
     const int qd = warp & 3;
     const uint32_t wbase = sbase + C::OFF_EPI + (uint32_t)((warp - 2) * C::PS_WARP);
     const uint32_t sbar = bar0 + 8 * (C::BAR_SLD + (warp - 2) * C::PS_NSL);
@@ -924,6 +938,7 @@ __device__ __forceinline__ void presum_epilogue(const KernelParams &p, const Ten
         const int row = wrow0 + lane;
         const int sy = wrow0 - p.red_row_off;
         const uint32_t tbase = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * BN);
+        const int ncc = live_chunks<BN>(p, tni);
         auto load_s = [&](int cc) {  // lane 0
             const int b = cc % C::PS_NSL;
             ptx::mbar_arrive_expect_tx(sbar + 8 * b, C::PS_SLOT);
@@ -941,14 +956,14 @@ __device__ __forceinline__ void presum_epilogue(const KernelParams &p, const Ten
                 ptx::st_release_cta_shared(sbase + C::OFF_PS_ACK + 4 * qd, (uint32_t)(i + 1));
                 ptx::fence_proxy_async_global();  // the reducers' generic stores before the TMA loads
                 if (valid)
-                    for (int cc = 0; cc < C::PS_NSL && cc < NCC; ++cc) load_s(cc);
+                    for (int cc = 0; cc < C::PS_NSL && cc < ncc; ++cc) load_s(cc);
             }
         }
         st = __shfl_sync(0xffffffffu, st, 0);
         if (!st) break;
         bool dead = false;
 #pragma unroll 1
-        for (int cc = 0; cc < NCC; ++cc) {
+        for (int cc = 0; cc < ncc; ++cc) {
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
             ptx::tmem_ld_wait();
@@ -992,13 +1007,15 @@ __device__ __forceinline__ void presum_epilogue(const KernelParams &p, const Ten
                 if (pub) ptx::tma_store_2d(&tm.f32out, wbase + (uint32_t)(b * C::PS_SLOT), col, wrow0);
                 ptx::tma_store_2d(&tm.c, ob, col, wrow0);
                 ptx::bulk_commit();
-                if (cc + C::PS_NSL < NCC) {
+                if (cc + C::PS_NSL < ncc) {
                     if (pub) ptx::bulk_wait_read<0>();  // the publish store has read slot b
                     load_s(cc + C::PS_NSL);
                 }
             }
             // this lane's S line of the chunk is dead: drop it from L2 unwritten
-            if (row < p.M) ptx::discard_l2_128(p.red_buf + (int64_t)(row - p.red_row_off) * p.N + col);
+            // (only whole 128-byte lines: with N % 32 != 0 rows do not start on one)
+            if (row < p.M && (p.N & 31) == 0 && col + 32 <= p.N)
+                ptx::discard_l2_128(p.red_buf + (int64_t)(row - p.red_row_off) * p.N + col);
         }
         if (dead) {
             drain();
@@ -1146,7 +1163,7 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
     }
 
     unsigned long long wait_ns = 0;
-    const int KB = p.K / C::BK;
+    const int KB = (p.K + C::BK - 1) / C::BK;  // a partial last k-block reads zeros past K
 
     if (warp == 0) {
         // ================= TMA producer =================
@@ -1372,8 +1389,9 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                 }
             }
             const uint32_t ebuf = sbase + C::OFF_EPI + (uint32_t)((warp - 2) * 2 * C::EPI_SLOT);
+            const int ncc = live_chunks<BN>(p, tni);
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
+            for (int cc = 0; cc < ncc; ++cc) {
                 uint32_t v[32];
                 ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
                 ptx::tmem_ld_wait();
@@ -1405,7 +1423,7 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                             }
                         }
                     } else if (in_range) {
-                        store_bf16_row32(p.out + (int64_t)row * p.N + col, f);
+                        store_bf16_row32(p.out + (int64_t)row * p.N + col, f, p.N - col);
                     }
                     continue;
                 } else {
@@ -1433,9 +1451,9 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                     }
                 } else {
                     if (p.f32_out != nullptr && in_range && (OP == OP_AR || !red))
-                        store_f32_row32(p.f32_out + (int64_t)row * p.N + col, f);
+                        store_f32_row32(p.f32_out + (int64_t)row * p.N + col, f, p.N - col);
                     if (RED && red && in_range && p.red_buf != p.f32_out)
-                        store_f32_row32(p.red_buf + (int64_t)(row - p.red_row_off) * p.N + col, f);
+                        store_f32_row32(p.red_buf + (int64_t)(row - p.red_row_off) * p.N + col, f, p.N - col);
                 }
                 if constexpr (RED) {
                     continue;  // the reducer warps add the peers to the stored partial
@@ -1483,7 +1501,7 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                 }
                 if (in_range) {
                     const int orow = OP == OP_RS ? row - p.rank * p.M_r : row;
-                    store_bf16_row32(p.out + (int64_t)orow * p.N + col, f);
+                    store_bf16_row32(p.out + (int64_t)orow * p.N + col, f, p.N - col);
                 }
                 }  // !RED
                 }  // OP != OP_AG
@@ -1560,7 +1578,8 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                     ptx::fence_proxy_async();
                 }
                 const int prow = r0 - p.peer_row_off;
-                for (int cc = 0; ok && cc < BN / 32; ++cc) {
+                const int ncc = live_chunks<BN>(p, tni);
+                for (int cc = 0; ok && cc < ncc; ++cc) {
                     for (int q = 0; q < p.R; ++q) {
                         if (q == p.rank) continue;
                         const int slot = (int)(pit % C::P);

@@ -132,12 +132,15 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         err = "tile_n must be 128 or 256";
         return SYN_ERR_UNSUPPORTED;
     }
-    if (L.K % kTileK != 0) {
-        err = "K must be a multiple of 64";
+    // Tails: the last k-block and the last column of tiles may be partial (the
+    // TMA loads fill past K and N with zeros, the stores stop at N); rows of
+    // bf16 operands and fp32 partials must start on 16-byte boundaries.
+    if (L.K % 8 != 0) {
+        err = "K must be a multiple of 8 (16-byte bf16 rows)";
         return SYN_ERR_UNSUPPORTED;
     }
-    if (L.N % tile_n != 0) {
-        err = "N must be a multiple of tile_n";
+    if (L.N % 8 != 0) {
+        err = "N must be a multiple of 8 (16-byte bf16 rows)";
         return SYN_ERR_UNSUPPORTED;
     }
     if (op == SYN_OP_GEMM_RS && M_r % tile_m != 0) {
@@ -177,7 +180,7 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
     s.tile_m = tile_m;
     s.tile_n = tile_n;
     s.tiles_m = (int)((L.M + tile_m - 1) / tile_m);
-    s.tiles_n = (int)(L.N / tile_n);
+    s.tiles_n = (int)((L.N + tile_n - 1) / tile_n);
     s.n_tiles = s.tiles_m * s.tiles_n;
     s.n_rc = R * split;
 

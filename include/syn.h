@@ -34,10 +34,14 @@
  *  - Matrices are row-major.  bf16 operands are IEEE bfloat16; partials fp32.
  *  - The plan owns its flags, counters, error word, tables, staging receive
  *    buffers and helper streams; syn_plan_destroy() frees them.
- *  - Limits of this version: 1 <= R <= 8; K % 64 == 0; N % tile_n == 0; dense
+ *  - Limits of this version: 1 <= R <= 8; K % 8 == 0 and N % 8 == 0 (every
+ *    bf16 row and fp32 partial row starts on a 16-byte boundary); dense
  *    layouts (ld* == 0 or equal to the row length); GEMM-RS needs
- *    (M/R) % 128 == 0.  M may have a tail (M % 128 != 0) for AG-GEMM and
- *    GEMM-AR.
+ *    (M/R) % tile_m == 0.  M may have a tail (M % 128 != 0) for AG-GEMM and
+ *    GEMM-AR.  K need not be a multiple of the 64-element k-block nor N of
+ *    tile_n: the TMA operand loads read zeros past K and N, so the last
+ *    k-block and the last column of tiles are partial, and no store reaches
+ *    past column N.
  */
 #ifndef SYN_H
 #define SYN_H

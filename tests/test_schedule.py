@@ -141,8 +141,9 @@ def test_rs_send_tiles_first_reduce_tiles_last():
 @pytest.mark.parametrize("kw,status", [
     (dict(op="ag", R=4, rank=4, M=256, N=256, K=256), syn.ERR_INVALID),
     (dict(op="ag", R=3, rank=0, M=256, N=256, K=256), syn.ERR_INVALID),      # M % R
-    (dict(op="ag", R=4, rank=0, M=256, N=256, K=100), syn.ERR_UNSUPPORTED),  # K % 64
-    (dict(op="ag", R=4, rank=0, M=256, N=200, K=256), syn.ERR_UNSUPPORTED),  # N % tile_n
+    (dict(op="ag", R=4, rank=0, M=256, N=256, K=100), syn.ERR_UNSUPPORTED),  # K % 8
+    (dict(op="ag", R=4, rank=0, M=256, N=204, K=256), syn.ERR_UNSUPPORTED),  # N % 8
+    (dict(op="rs", R=4, rank=0, M=1024, N=256, K=60), syn.ERR_UNSUPPORTED),  # K % 8
     (dict(op="ag", R=16, rank=0, M=256, N=256, K=256), syn.ERR_UNSUPPORTED),  # R > 8
     (dict(op="rs", R=4, rank=0, M=4 * 96, N=256, K=256), syn.ERR_UNSUPPORTED),  # M_r % 128
     (dict(op="ag", R=4, rank=0, M=256, N=256, K=256, split=65), syn.ERR_INVALID),  # split > M_r
@@ -154,6 +155,17 @@ def test_invalid_shapes_rejected(kw, status):
     with pytest.raises(syn.SynError) as e:
         syn.schedule_build(*args, **kw)
     assert e.value.status == status
+
+
+def test_k_and_n_tails_give_a_partial_last_tile_column():
+    """K and N need only be multiples of 8: the last column of tiles covers the
+    N tail (ceil(N / tile_n) tile columns), and the tile list still holds every
+    tile once."""
+    for N, tile_n in [(520, 256), (520, 128), (392, 256), (8, 128)]:
+        info, tl, _, _ = syn.schedule_build("ag", 4, 1, 4 * 150, N, 200, split=2, order="row", tile_n=tile_n)
+        tiles_n = -(-N // tile_n)
+        assert info["tiles_n"] == tiles_n
+        assert sorted(tl.tolist()) == list(range(info["tiles_m"] * tiles_n))
 
 
 def test_chunk_rows_and_split_agree():
