@@ -336,13 +336,32 @@ __device__ __forceinline__ void chunk_range(const KernelParams &p, int r0, int n
     chunk_range_of(p.M, p.rb, r0, nrows, lo, hi);
 }
 
-// Does the tile starting at row r0 reduce peers?  AR: always; RS: tiles of the
-// local row block (tiles never straddle rank blocks for RS).
+// Do rows [r0, r0 + nrows) (a tile's, or one CTA's share of it) reduce peers?
+// AR: always; RS: when some of them lie in the local row block (a tile may
+// straddle the block's edges; each 32-row warp group lies wholly inside or
+// outside it, since M_r % 32 == 0).
 template <int OP>
-__device__ __forceinline__ bool reduces(const KernelParams &p, int r0) {
+__device__ __forceinline__ bool reduces(const KernelParams &p, int r0, int nrows) {
     if (OP == OP_AR) return true;
-    if (OP == OP_RS) return r0 / p.M_r == p.rank;
+    if (OP == OP_RS) {
+        const int lo = p.rank * p.M_r;  // (< M <= 2^30)
+        return r0 < lo + p.M_r && r0 + nrows > lo;
+    }
     return false;
+}
+// GEMM-RS: do rows [r0, r0 + nrows) clipped to M include rows outside the
+// local block (rows to send)?
+template <int OP>
+__device__ __forceinline__ bool sends(const KernelParams &p, int r0, int nrows) {
+    if (OP != OP_RS) return false;
+    const int lo = p.rank * p.M_r, r1 = r0 + nrows < p.M ? r0 + nrows : p.M;
+    return r0 < lo || r1 > lo + p.M_r;
+}
+// GEMM-RS: is row `row` one of the local block's (reduced, not sent)?  AR: all rows.
+template <int OP>
+__device__ __forceinline__ bool local_row(const KernelParams &p, int row) {
+    const int lo = p.rank * p.M_r;  // (< M <= 2^30)
+    return OP != OP_RS || (row >= lo && row < lo + p.M_r);
 }
 
 // ------------------------------------------------------------------ tile walk
@@ -775,14 +794,17 @@ __device__ __forceinline__ void reduce_worker(const KernelParams &p, uint8_t *sm
             if (t < 0) return;  // (cannot happen: the epilogue stored tile j)
             const int tl = tile_at(p, t, abort);
             if (tl < 0) return;
-            if (reduces<OP>(p, (tl / p.tiles_n) * C::TILE_M)) {
+            if (reduces<OP>(p, (tl / p.tiles_n) * C::TILE_M + (int)crank * C::BM, C::BM)) {
                 ++scan_j;
                 cur_t = t;
             }
         }
         const int tile = p.tile_list[cur_t];
         const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
-        reduce_rows<OP, BN, RG>(p, tmi * C::TILE_M + (int)crank * C::BM + q * 32 + g * RG, tni * BN, lane);
+        const int row0 = tmi * C::TILE_M + (int)crank * C::BM + q * 32 + g * RG;
+        // (GEMM-RS: a quadrant of a tile straddling the local block's edge may
+        // hold sent rows; its 32 rows lie wholly in or out of the block)
+        if (local_row<OP>(p, row0)) reduce_rows<OP, BN, RG>(p, row0, tni * BN, lane);
     }
 }
 
@@ -1366,23 +1388,28 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
             const int tr0 = tmi * C::TILE_M;                       // tile's first row
             const int row = tr0 + (int)crank * C::BM + lrow;       // this thread's row
             const bool in_range = row < p.M;
-            const bool red = reduces<OP>(p, tr0);
+            // red: this CTA's rows of the tile reduce (it takes the peer ring, or
+            // hands its quadrants to the reducer warps); wl: this warp's 32 rows
+            // are reduced rather than sent (GEMM-RS: local-block rows; a tile may
+            // straddle the block's edge)
+            const bool red = reduces<OP>(p, tr0 + (int)crank * C::BM, C::BM);
             const uint32_t tbase = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(acc * BN);
             bool dead = false;
             // fp32 store of this tile (at most one): send / publish, or (RED) the
             // reducing tile's partial; with EPI_TMA through this warp's staging
             // buffers and TMA tile stores of its 32 rows
             const int wrow0 = tr0 + (int)crank * C::BM + qd * 32;  // this warp's first row
+            const bool wl = local_row<OP>(p, wrow0);
             const CUtensorMap *fmap = nullptr;
             int fy = 0;
             if constexpr (C::EPI_TMA && OP == OP_AG) {
                 if (p.epi_tma && wrow0 < p.M) fmap = &tm.c;
             } else if constexpr (C::EPI_TMA) {
                 if (p.epi_tma && wrow0 < p.M) {
-                    if (p.f32_out != nullptr && (OP == OP_AR || !red)) {
+                    if (p.f32_out != nullptr && (OP == OP_AR || !wl)) {
                         fmap = &tm.f32out;
                         fy = wrow0;
-                    } else if (RED && red && p.red_buf != p.f32_out) {
+                    } else if (RED && wl && p.red_buf != p.f32_out) {
                         fmap = &tm.red;
                         fy = wrow0 - p.red_row_off;
                     }
@@ -1442,7 +1469,7 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                         if (lane == 0) {
                             // GEMM-RS push mode: send rows are added into the
                             // destination's receive accumulator
-                            if (OP == OP_RS && !red && p.send_push)
+                            if (OP == OP_RS && !wl && p.send_push)
                                 ptx::tma_reduce_add_2d(fmap, buf, col, fy);
                             else
                                 ptx::tma_store_2d(fmap, buf, col, fy);
@@ -1450,9 +1477,9 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                         }
                     }
                 } else {
-                    if (p.f32_out != nullptr && in_range && (OP == OP_AR || !red))
+                    if (p.f32_out != nullptr && in_range && (OP == OP_AR || !wl))
                         store_f32_row32(p.f32_out + (int64_t)row * p.N + col, f, p.N - col);
-                    if (RED && red && in_range && p.red_buf != p.f32_out)
+                    if (RED && wl && in_range && p.red_buf != p.f32_out)
                         store_f32_row32(p.red_buf + (int64_t)(row - p.red_row_off) * p.N + col, f, p.N - col);
                 }
                 if constexpr (RED) {
@@ -1499,7 +1526,7 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) f[j] = f[j] + sacc[j];
                 }
-                if (in_range) {
+                if (in_range && wl) {
                     const int orow = OP == OP_RS ? row - p.rank * p.M_r : row;
                     store_bf16_row32(p.out + (int64_t)orow * p.N + col, f, p.N - col);
                 }
@@ -1541,7 +1568,7 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                     }
                 }
             }
-            if (OP != OP_AG && p.f32_out != nullptr && (OP == OP_AR || !red))
+            if (OP != OP_AG && p.f32_out != nullptr && (OP == OP_AR || sends<OP>(p, tr0, C::TILE_M)))
                 count_produced(p, tr0, C::TILE_M, C::CTAS, lane);
             ++tc;
         }
@@ -1563,11 +1590,17 @@ __global__ void __launch_bounds__(red_threads(OP, RED), 1)
                 if (tile < 0) break;
                 const int tmi = tile / p.tiles_n, tni = tile - tmi * p.tiles_n;
                 const int tr0 = tmi * C::TILE_M;
-                if (!reduces<OP>(p, tr0)) continue;
                 const int r0 = tr0 + (int)crank * C::BM;  // this CTA's rows
+                if (!reduces<OP>(p, r0, C::BM)) continue;
                 if (p.waits) {
+                    // the chunks of the rows this CTA reduces (GEMM-RS: its local-block rows)
+                    int a = r0, b = r0 + C::BM;
+                    if (OP == OP_RS) {
+                        a = max(a, p.rank * p.M_r);
+                        b = min(b, (p.rank + 1) * p.M_r);
+                    }
                     int lo, hi;
-                    chunk_range(p, r0, C::BM, lo, hi);
+                    chunk_range(p, a, b - a, lo, hi);
                     for (int rc = lo; ok && rc <= hi; ++rc)
                         for (int q = 0; ok && q < p.R; ++q) {
                             if (q == p.rank) continue;

@@ -106,10 +106,16 @@ void tile_waits(const State &st, int tile, std::vector<int> &codes) {
     const Schedule &s = st.s;
     const int op = st.cfg->op;
     codes.clear();
-    const int64_t r0 = (int64_t)(tile / s.tiles_n) * s.tile_m;
-    if (op == 1 && r0 / s.M_r != s.rank) return;  // GEMM-RS send tile: consumes nothing
+    int64_t r0 = (int64_t)(tile / s.tiles_n) * s.tile_m, nrows = s.tile_m;
+    if (op == 1) {  // GEMM-RS: only the rows of the local block consume chunks
+        int64_t a, b;
+        local_rows_of(s.M_r, s.rank, r0, nrows, a, b);
+        if (a >= b) return;  // a send tile: consumes nothing
+        r0 = a;
+        nrows = b - a;
+    }
     int lo, hi;
-    chunk_range_of(s.M, s.rb, r0, s.tile_m, lo, hi);
+    chunk_range_of(s.M, s.rb, r0, nrows, lo, hi);
     for (int rc = lo; rc <= hi; ++rc) {
         if (op == 0) {
             const int q = rc / s.split;

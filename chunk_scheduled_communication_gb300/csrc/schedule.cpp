@@ -39,6 +39,13 @@ namespace syn {
 
 static int ring_pos(int q, int r, int R) { return ((q - r) % R + R) % R; }
 
+// GEMM-RS: does tile row tm hold rows of the local block (so it reduces)?
+static bool reduces_rows(const Schedule &s, int tm) {
+    int64_t a, b;
+    local_rows_of(s.M_r, s.rank, (int64_t)tm * s.tile_m, s.tile_m, a, b);
+    return a < b;
+}
+
 int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
                    int64_t chunk_rows, int split, syn_order_t order,
                    const syn_knobs_t &kn, Schedule &s, std::string &err, const int64_t *block_rows) {
@@ -143,8 +150,9 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         err = "N must be a multiple of 8 (16-byte bf16 rows)";
         return SYN_ERR_UNSUPPORTED;
     }
-    if (op == SYN_OP_GEMM_RS && M_r % tile_m != 0) {
-        err = "GEMM-RS needs (M/R) % tile_m == 0";
+    if (op == SYN_OP_GEMM_RS && M_r % 32 != 0) {
+        // (a warp's 32 epilogue rows are either all sent or all reduced)
+        err = "GEMM-RS needs (M/R) % 32 == 0";
         return SYN_ERR_UNSUPPORTED;
     }
     if (L.M > (int64_t)1 << 30 || L.N > (int64_t)1 << 30 || L.K > (int64_t)1 << 30) {
@@ -217,7 +225,7 @@ int build_schedule(syn_op_t op, int R, int rank, const syn_layout_t &L,
         tile_row_chunks(s, tm, lo, hi);
         int32_t key = -1;
         const int block = block_of_row(s.rb, (int64_t)tm * tile_m);
-        if (op == SYN_OP_GEMM_RS && block != rank) {
+        if (op == SYN_OP_GEMM_RS && !reduces_rows(s, tm)) {
             // send tile: produces chunk(s) for rank `block`; ring order
             const int j = chunk_of_row(s.rb, (int64_t)tm * tile_m) - block * split;
             key = (ring_pos(block, rank, R) - 1) * split + j - (R - 1) * split;
@@ -281,8 +289,7 @@ void spread_reduce_tiles(Schedule &s, int units, bool early) {
     if (rounds < 3) return;
     std::vector<int32_t> red, red_key, snd, snd_key;
     for (int i = 0; i < T; ++i) {
-        const int tm = s.tile_list[i] / s.tiles_n;
-        const bool is_red = ((int64_t)tm * s.tile_m) / s.M_r == s.rank;
+        const bool is_red = reduces_rows(s, s.tile_list[i] / s.tiles_n);
         (is_red ? red : snd).push_back(s.tile_list[i]);
         (is_red ? red_key : snd_key).push_back(s.tile_key[i]);
     }

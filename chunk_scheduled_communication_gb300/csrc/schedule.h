@@ -48,6 +48,16 @@ SYN_SCHED_HD RowBlocks uniform_blocks(int R, int64_t M_r, int split) {
 }
 SYN_SCHED_HD int64_t block_rows(const RowBlocks &b, int q) { return b.off[q + 1] - b.off[q]; }
 
+// GEMM-RS: the rows [a, b) of rows [r0, r0 + nrows) that lie in block `rank`
+// (rows [rank * M_r, (rank + 1) * M_r)), the ones a tile reduces with the
+// peers' partials; empty (a >= b) for a tile that only sends.  A tile may
+// straddle the block's edges when M_r is not a multiple of the tile height.
+SYN_SCHED_HD void local_rows_of(int64_t M_r, int rank, int64_t r0, int64_t nrows, int64_t &a, int64_t &b) {
+    const int64_t lo = (int64_t)rank * M_r, hi = lo + M_r;
+    a = r0 > lo ? r0 : lo;
+    b = r0 + nrows < hi ? r0 + nrows : hi;
+}
+
 // First row of row chunk rc (rc == R*split gives the end of the row space).
 SYN_SCHED_HD int64_t chunk_row0(const RowBlocks &b, int rc) {
     const int q = rc / b.split, j = rc - q * b.split;

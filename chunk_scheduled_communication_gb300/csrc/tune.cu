@@ -240,7 +240,6 @@ extern "C" int syn_autotune(syn_op_t op, int R, int rank, const syn_layout_t *la
     dims.push_back([&](const Cand &x) {  // tile shape
         std::vector<Cand> v;
         for (auto sh : {std::pair<int, int>{256, 256}, {128, 256}, {128, 128}}) {
-            if (op == SYN_OP_GEMM_RS && M_r % sh.first) continue;
             Cand y = x;
             y.kn.tile_m = sh.first;
             y.kn.tile_n = sh.second;

@@ -37,11 +37,12 @@
  *  - Limits of this version: 1 <= R <= 8; K % 8 == 0 and N % 8 == 0 (every
  *    bf16 row and fp32 partial row starts on a 16-byte boundary); dense
  *    layouts (ld* == 0 or equal to the row length); GEMM-RS needs
- *    (M/R) % tile_m == 0.  M may have a tail (M % 128 != 0) for AG-GEMM and
- *    GEMM-AR.  K need not be a multiple of the 64-element k-block nor N of
- *    tile_n: the TMA operand loads read zeros past K and N, so the last
- *    k-block and the last column of tiles are partial, and no store reaches
- *    past column N.
+ *    (M/R) % 32 == 0 (a tile may hold rows of several rank blocks, sent and
+ *    reduced ones; each 32-row warp group lies in one block).  M may have a
+ *    tail (M % tile_m != 0).  K need not be a multiple of the 64-element
+ *    k-block nor N of tile_n: the TMA operand loads read zeros past K and N,
+ *    so the last k-block and the last column of tiles are partial, and no
+ *    store reaches past column N.
  */
 #ifndef SYN_H
 #define SYN_H
@@ -130,8 +131,7 @@ typedef struct {
     int comm_sms;          /* TMA_DEDICATED: CTAs (SMs) given to staging, 1..32  */
     int tile_m;            /* rows per output tile: 128 (one CTA per tile) or
                               256 (a 2-CTA cluster shares the tile with
-                              cta_group::2 UMMAs; GEMM-RS then needs M/R to be
-                              a multiple of 256); 0 = 128                     */
+                              cta_group::2 UMMAs); 0 = 128                    */
     int tile_n;            /* 128 or 256 (0 = 256)                               */
     int group_m;           /* SYN_ORDER_GROUPED group height in tiles (0 = 8)   */
     int slice_kb;          /* device stagers: KiB per slice of a chunk (0 = 128) */

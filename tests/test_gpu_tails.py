@@ -187,3 +187,65 @@ def test_a2a_tails(backend):
         g, C = oracle.a2a_gemm(inp.shards, inp.B)
         assert (runner.dev_to_u16(d.gathered) == g).all()
         assert (runner.dev_to_u16(d.out) == C).all()
+
+
+# ----------------------------------------------------------------------------- GEMM-RS row-block tails
+# Rank blocks of M/R rows that are not whole tiles: a tile may hold rows of two
+# or more blocks, some sent and some reduced (each 32-row warp group lies in
+# one block).  96-row blocks under 128-row tiles, 160-row blocks under 256-row
+# CTA-pair tiles (ragged last tile), with K and N tails as well.
+RS_STRADDLE = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=4 * 96, K=200, N=392, R=4)
+RS_STRADDLE_PAIR = wl.scaled(wl.LLAMA3_8B_DOWN_RS, M=5 * 160, K=136, N=520, R=5)
+
+
+def _every_rank(w, ranks=None, **knobs):
+    for r in (ranks if ranks is not None else range(w.R)):
+        inp, got = _run(w, r, **dict(knobs))
+        _check(w, r, inp, got)
+
+
+@pytest.mark.parametrize("backend", PLAIN)
+def test_rs_straddling_tiles_every_backend(backend):
+    _every_rank(RS_STRADDLE, backend=backend, tile_n=256)
+
+
+@pytest.mark.parametrize("knobs", [
+    dict(tile_m=128, tile_n=256),                   # reducer warps
+    dict(tile_m=128, tile_n=256, reduce_warps=-1),  # epilogue peer ring
+    dict(tile_m=128, tile_n=128),
+], ids=["reducers", "ring", "ring-n128"])
+def test_rs_straddling_tiles_resident_peers(knobs):
+    _every_rank(RS_STRADDLE, backend="tma_colocated_smem", **knobs)
+
+
+@pytest.mark.parametrize("knobs", [
+    dict(backend="tma_colocated_smem", stages=6),                    # pair + reducer warps
+    dict(backend="tma_colocated_smem", stages=5, reduce_warps=-1),   # pair + epilogue peer ring
+    dict(backend="tma_colocated", stages=4),
+    dict(backend="ce", stages=4),
+], ids=["reducers", "ring", "tma_colocated", "ce"])
+def test_rs_straddling_pair_tiles(knobs):
+    _every_rank(RS_STRADDLE_PAIR, ranks=(0, 2, 4), tile_m=256, tile_n=256, **knobs)
+
+
+@pytest.mark.parametrize("push_sms", [0, 4])
+def test_rs_straddling_push_mode(push_sms):
+    """Push mode where tiles straddle block edges: only the sent rows are added
+    into `send`; the local block's rows of `send` stay untouched."""
+    w = RS_STRADDLE_PAIR
+    for r in (1, 4):
+        inp = wl.make_inputs(w, r=r, seed=0, kind="int")
+        init = np.random.default_rng(6).integers(-4, 5, size=(w.M, w.N)).astype(np.float32)
+        d = runner.upload(inp)
+        d.f32_out.copy_(torch.from_numpy(init))
+        with runner.make_plan(d, split=5, order="row", backend="tma_colocated_smem", tile_m=256, tile_n=256,
+                              rs_push=1, push_sms=push_sms) as plan:
+            runner.call(plan, d)
+            assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+            once = d.f32_out.cpu().numpy()
+        out, P = oracle.gemm_rs(inp.A, inp.B, inp.peers, w.R, r, send_rows=(0, w.M))
+        keep = np.ones(w.M, bool)
+        keep[r * w.M_r:(r + 1) * w.M_r] = False
+        assert (once[keep] == init[keep] + P[keep]).all()
+        assert (once[~keep] == init[~keep]).all()
+        assert (runner.dev_to_u16(d.out) == out).all()

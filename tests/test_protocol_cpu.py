@@ -28,6 +28,8 @@ def n_tiles(M, N, tile_m, tile_n):
     ("ag", 8, 5, 4096, 512, 64, 3, "row", 256),       # uneven 3-way split, 256-row tiles
     ("rs", 4, 2, 1024, 512, 64, 2, "row", 128),
     ("rs", 8, 7, 2048, 256, 64, 4, "grouped", 256),
+    ("rs", 4, 1, 4 * 96, 256, 64, 2, "row", 128),      # blocks of 96 rows: tiles straddle block edges
+    ("rs", 5, 3, 5 * 160, 256, 64, 3, "row", 256),     # odd R, pair tiles straddling, ragged last tile
     ("ar", 4, 0, 1000, 256, 64, 3, "row", 128),       # M tail, uneven chunks
     ("ar", 2, 1, 512, 512, 64, 1, "col", 256),
 ])
@@ -82,7 +84,7 @@ def test_a_broken_protocol_is_caught():
 
 def test_rejected_plan_reports_invalid():
     with pytest.raises(ValueError):
-        proto.emulate(op="rs", R=4, rank=0, M=4 * 100, N=256, K=64)  # M/R not a multiple of 128
+        proto.emulate(op="rs", R=4, rank=0, M=4 * 100, N=256, K=64)  # M/R not a multiple of 32
 
 
 # --------------------------------------------------------------------------- A2A-GEMM row blocks

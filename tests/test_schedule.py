@@ -145,7 +145,7 @@ def test_rs_send_tiles_first_reduce_tiles_last():
     (dict(op="ag", R=4, rank=0, M=256, N=204, K=256), syn.ERR_UNSUPPORTED),  # N % 8
     (dict(op="rs", R=4, rank=0, M=1024, N=256, K=60), syn.ERR_UNSUPPORTED),  # K % 8
     (dict(op="ag", R=16, rank=0, M=256, N=256, K=256), syn.ERR_UNSUPPORTED),  # R > 8
-    (dict(op="rs", R=4, rank=0, M=4 * 96, N=256, K=256), syn.ERR_UNSUPPORTED),  # M_r % 128
+    (dict(op="rs", R=4, rank=0, M=4 * 100, N=256, K=256), syn.ERR_UNSUPPORTED),  # M_r % 32
     (dict(op="ag", R=4, rank=0, M=256, N=256, K=256, split=65), syn.ERR_INVALID),  # split > M_r
     (dict(op="ag", R=4, rank=0, M=256, N=256, K=256, chunk_rows=32, split=4), syn.ERR_INVALID),
 ])
@@ -213,10 +213,53 @@ def test_pair_tiles_of_256_rows(op, R, r, M, N, K, split):
     assert (np.diff(tk) >= 0).all()
 
 
-def test_pair_tiles_rs_needs_256_row_blocks():
-    with pytest.raises(syn.SynError) as e:
-        syn.schedule_build("rs", 4, 0, 4 * 384, 256, 256, tile_m=256)
-    assert e.value.status == syn.ERR_UNSUPPORTED
+def test_rs_row_blocks_need_32_row_multiples():
+    """GEMM-RS row blocks need not be whole tiles (a tile may straddle a block
+    edge) but must be whole 32-row warp groups."""
+    syn.schedule_build("rs", 4, 0, 4 * 384, 256, 256, tile_m=256)
+    syn.schedule_build("rs", 4, 0, 4 * 96, 256, 256, tile_m=128)
+    for tile_m in (128, 256):
+        with pytest.raises(syn.SynError) as e:
+            syn.schedule_build("rs", 4, 0, 4 * 368, 256, 256, tile_m=tile_m)
+        assert e.value.status == syn.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("R,r,M_r,tile_m,split,backend", [
+    (4, 1, 96, 128, 1, "tma_colocated"),     # block 1 = rows 96..191: straddles tiles 0 and 1
+    (4, 2, 96, 128, 3, "ce"),
+    (4, 3, 160, 256, 2, "tma_colocated"),    # pair tiles, block 3 = rows 480..639, ragged last tile
+    (3, 0, 32, 128, 1, "tma_colocated"),     # the whole row space is one tile
+    (8, 5, 96, 256, 1, "tma_colocated_smem"),
+])
+def test_rs_straddling_tiles_reduce_and_wait_on_local_chunks(R, r, M_r, tile_m, split, backend):
+    """A GEMM-RS tile reduces when any of its rows lie in the local block; it
+    then waits only for (is keyed after) the local chunks its rows touch.
+    Tiles with no local rows are send tiles, ordered before the reduce tiles
+    when peers are staged.  Every tile appears once."""
+    M, N, K = R * M_r, 256, 128
+    info, tl, tk, tr = syn.schedule_build("rs", R, r, M, N, K, split=split, order="row", tile_m=tile_m,
+                                          backend=backend)
+    T = info["n_tiles"]
+    assert sorted(tl.tolist()) == list(range(T))
+    tiles_n = N // 256
+    lo, hi = r * M_r, (r + 1) * M_r
+    red = np.array([max(lo, (t // tiles_n) * tile_m) < min(hi, (t // tiles_n + 1) * tile_m) for t in tl])
+    assert red.any()
+    if backend == "tma_colocated_smem":
+        assert len(tr) == 0
+        assert red[:int(red.sum())].all()  # resident peers: reduce tiles first
+        return
+    # staged peers: send tiles first, then reduce tiles by their latest local chunk's arrival
+    assert not red[:int((~red).sum())].any()
+    arrival = {code: a for a, code in enumerate(tr.tolist())}
+    bounds = [lo + (j * M_r + split - 1) // split for j in range(split + 1)]
+    for t, k, is_red in zip(tl.tolist(), tk.tolist(), red.tolist()):
+        if not is_red:
+            continue
+        a, b = max(lo, (t // tiles_n) * tile_m), min(hi, (t // tiles_n + 1) * tile_m)
+        chunks = [r * split + j for j in range(split) if bounds[j] < b and bounds[j + 1] > a]
+        want = max(arrival[rc * R + q] for rc in chunks for q in range(R) if q != r)
+        assert k == want
 
 
 @pytest.mark.parametrize("R,r,M,N,K,tile_m,tile_n,units", [
