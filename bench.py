@@ -422,9 +422,14 @@ def main():
                 pairs.append((h, d.shards[q]))
         else:
             pairs.append((_t.from_numpy(inp.A.view(np.int16)).view(_t.bfloat16).pin_memory(), d.A))
+            # the peers' partials the operator reads: GEMM-AR all rows; GEMM-RS
+            # only the rows of the local block (the rows a reduce-scatter delivers
+            # to this rank; the kernel reads no other row of a peer's partial)
+            rows = slice(0, w.M) if w.op == "ar" else slice(inp.r * w.M_r, (inp.r + 1) * w.M_r)
             for q in range(w.R):
                 if d.peers[q] is not None:
-                    pairs.append((_t.from_numpy(inp.peers[q]).pin_memory(), d.peers[q]))
+                    h = _t.from_numpy(np.ascontiguousarray(inp.peers[q][rows])).pin_memory()
+                    pairs.append((h, d.peers[q][rows]))
         pairs.append((_t.from_numpy(inp.B.view(np.int16)).view(_t.bfloat16).pin_memory(), d.B))
         out_h = _t.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
         pinned.append((pairs, out_h, d.out))

@@ -304,7 +304,10 @@ int syn_ag_gemm(syn_plan_t plan, const void *const *shards, void *gathered,
  * §6.1).
  *   A             : bf16 [M, K], B : bf16 [K, N]
  *   peer_partials : host array of R device pointers, fp32 [M, N] each: peer q's
- *                   partial product; entry r is ignored (may be NULL)
+ *                   partial product; entry r is ignored (may be NULL); only
+ *                   rows_r (rows [r*M/R, (r+1)*M/R)) of each affect the
+ *                   result (a tile straddling that block's edge may load,
+ *                   but does not use, the rows next to it)
  *   send          : nullable fp32 [M, N]; rows of every rank q != r receive
  *                   the local partial P = A.B (the chunks peers would pull);
  *                   rows of rank r are not written
