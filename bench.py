@@ -641,11 +641,13 @@ def run_sweep(args):
     return 0
 
 
-def measure_a2a(knobs, peaks, stream, reps=200):
+def measure_a2a(knobs, peaks, stream, reps=50):
     """A2A-GEMM on the expert-parallel MoE workload (rank 0's expert), timed
     alone: CUDA events around `reps` back-to-back calls after warm-up, the
     unfused baseline (all copies, then the GEMM) the same way, cuBLAS + copy
-    for context, and the flag-wait share from a traced plan."""
+    for context (the same number of back-to-back calls, so all three run
+    equally long under the power cap), and the flag-wait share from a traced
+    plan."""
     import torch
 
     from chunk_scheduled_communication_gb300 import runner
