@@ -249,3 +249,24 @@ def test_rs_straddling_push_mode(push_sms):
         assert (once[keep] == init[keep] + P[keep]).all()
         assert (once[~keep] == init[~keep]).all()
         assert (runner.dev_to_u16(d.out) == out).all()
+
+
+@pytest.mark.parametrize("tile_m,backend", [(128, "tma_colocated"), (256, "tma_colocated"), (128, "ce")])
+def test_rs_straddling_dropped_chunk_times_out_then_recovers(tile_m, backend):
+    """A straddling GEMM-RS tile waits for the local chunks its rows touch: a
+    staging transfer of the local block whose flag is never published ends
+    the call in SYN_ERR_TIMEOUT (bounded waits, no hang), and the next plan
+    gives the oracle's bits."""
+    w = RS_STRADDLE if tile_m == 128 else RS_STRADDLE_PAIR
+    r = 1
+    inp = wl.make_inputs(w, r=r, seed=0, kind="int")
+    d = runner.upload(inp)
+    with runner.make_plan(d, split=2, order="row", backend=backend, tile_m=tile_m, tile_n=256, comm_sms=2,
+                          drop_chunk=0, timeout_ns=20_000_000) as bad:
+        runner.call(bad, d)
+        assert bad.sync() == syn.ERR_TIMEOUT
+    with runner.make_plan(d, split=2, order="row", backend=backend, tile_m=tile_m, tile_n=256,
+                          comm_sms=2) as good:
+        runner.call(good, d)
+        assert good.sync() == syn.OK, syn.lib().syn_last_error()
+    _check(w, r, inp, {"out": runner.dev_to_u16(d.out), "f32": d.f32_out.cpu().numpy()})
