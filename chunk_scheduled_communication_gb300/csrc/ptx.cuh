@@ -202,13 +202,6 @@ __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes
                  "r"(bytes)
                  : "memory");
 }
-// shared -> global bulk fp32 reduce-add (the add happens at the memory side;
-// bulk group of the issuing thread); 16-byte aligned, size a multiple of 16
-__device__ __forceinline__ void bulk_reduce_add_f32(void *dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
-                 "r"(src), "r"(bytes)
-                 : "memory");
-}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

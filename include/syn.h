@@ -223,7 +223,7 @@ typedef struct {
                               counts each row chunk produced, and the push
                               CTAs, as each chunk's produced flag arrives (in
                               production order: destinations in ring order),
-                              add it into `send` with bulk reduce-adds and
+                              add it into `send` with TMA tile reduce-adds and
                               publish its delivered flag (syn_plan_flags:
                               in_flags[rc * R + rank]).  The compute grid
                               shrinks by n SMs: the communication-SM balance

@@ -763,8 +763,8 @@ def test_direct_fetch_rejected_for_rs_ar():
                                              (wl.LLAMA3_8B_DOWN_RS, 16, "normal")], ids=["pair", "spread", "full"])
 def test_rs_push_dedicated_sms_adds_send_rows(w, push_sms, kind):
     """GEMM-RS push mode with dedicated push CTAs: the epilogue stores the send
-    rows, and the push CTAs add each produced chunk into `send` (bulk
-    reduce-add) and publish its delivered flag.  Against the oracle's P: init
+    rows, and the push CTAs add each produced chunk into `send` (TMA
+    tile reduce-add) and publish its delivered flag.  Against the oracle's P: init
     + P after one call and (init + P) + P after two (bit-exact for integer
     inputs), local rows untouched, out_r unchanged, every chunk delivered."""
     r = 1
