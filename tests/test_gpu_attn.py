@@ -246,3 +246,14 @@ def test_head_parallel_llama3_8b_full_size_sampled_rows():
     inp, got = run_head(w, 5, split=2)
     rows = [(0, 2), (4095, 4097), (16384, 16386), (32766, 32768)]
     check_head(w, 5, inp, got, rows=rows)
+
+
+@pytest.mark.parametrize("causal,r", [(False, 2), (True, 7)])
+def test_ring_attention_64_chunks_per_shard(causal, r):
+    """The finest KV chunking the plan takes: eight ranks, 64 chunks of one
+    128-key block each per shard (512 chunk flags, one wait per block),
+    two calls in a row; sampled query rows against the oracle."""
+    w = wl.AttnWorkload("ring-attn-max-split", 8, 64 * 128, 2, 1, causal=causal)
+    inp, got = run(w, r, split=64, calls=2)
+    assert got["info"]["n_transfers"] == (w.R - 1) * 64
+    check(w, r, inp, got, rows=[(0, 16), (4096, 4112), (w.S_r - 16, w.S_r)])
