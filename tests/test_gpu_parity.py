@@ -661,6 +661,37 @@ def test_benchmark_configuration_full_size_against_oracle(w):
     check_against_oracle(w, 0, got)
 
 
+@pytest.mark.parametrize("w,r", [(w, r) for w in (wl.LLAMA3_8B_UP_AG, wl.LLAMA3_8B_DOWN_RS, wl.QWEN2_7B_DOWN_AR)
+                                 for r in range(1, 8)],
+                         ids=[f"{o}-r{r}" for o in ("ag", "rs", "ar") for r in range(1, 8)])
+def test_benchmark_configuration_other_ranks(w, r):
+    """The benchmark's launch configuration at full size for every rank other
+    than 0: every output element against the oracle."""
+    split, order, kn = tuned.knobs_for(w.op)
+    inp = wl.make_inputs(w, r=r, seed=0)
+    d = runner.upload(inp, with_f32_out=(w.op == "rs"))
+    with runner.make_plan(d, split=split, order=order, **kn) as plan:
+        runner.call(plan, d)
+        assert plan.sync() == syn.OK, syn.lib().syn_last_error()
+    got = {"out": runner.dev_to_u16(d.out)}
+    if w.op == "ag":
+        got["gathered"] = runner.dev_to_u16(d.gathered)
+        g, C = oracle.ag_gemm(inp.shards, inp.B)
+        assert (got["gathered"] == g).all()
+        ok, exc, frob = runner.bf16_close(got["out"], C)
+        assert ok, (exc, frob)
+        return
+    if w.op == "rs":
+        ref, f32 = oracle.gemm_rs(inp.A, inp.B, inp.peers, w.R, r, send_rows=(0, w.M))
+        keep = np.ones(w.M, bool)
+        keep[r * w.M_r:(r + 1) * w.M_r] = False
+        ok, exc, frob = runner.f_close(d.f32_out.cpu().numpy()[keep], f32[keep])
+        assert ok, ("send", exc, frob)
+    else:
+        ref, _ = oracle.gemm_ar(inp.A, inp.B, inp.peers, w.R, r)
+    ok, exc, frob = runner.bf16_close(got["out"], ref)
+    assert ok, (exc, frob)
+
 
 # ----------------------------------------------------------------------------- pre-summed GEMM-AR
 # 704 pair tiles over 76 walkers (or 1408 single tiles over 152): walkers run
