@@ -78,3 +78,31 @@ def test_attention_library_exports_its_header():
     assert L.syn_attn_sync_status(None, None) == syn.ERR_INVALID
     c = attn.make_cfg()
     assert c.d == 128 and c.split == 1 and c.debug_drop_chunk == -1
+
+
+def test_headers_compile_as_plain_c(tmp_path):
+    """The boundary is a C ABI: both public headers compile as C11 on their
+    own (no C++ or CUDA types), and the operator calls type-check from C."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_abi.c"
+    src.write_text(
+        '#include "syn.h"\n#include "syn_attn.h"\n#include "syn_proto.h"\n'
+        "int use(const void *const *shards, void *gathered, const void *B, void *C, void *stream) {\n"
+        "    syn_layout_t L = {1024, 512, 256, 0, 0, 0};\n"
+        "    syn_knobs_t kn;\n"
+        "    syn_plan_t plan;\n"
+        "    if (syn_knobs_default(&kn) != SYN_OK) return -1;\n"
+        "    if (syn_plan_create(&plan, SYN_OP_AG_GEMM, 4, 1, &L, 0, 2, SYN_ORDER_ROW_MAJOR, &kn) != SYN_OK)\n"
+        "        return (int)syn_last_error()[0];\n"
+        "    syn_ag_gemm(plan, shards, gathered, B, C, stream);\n"
+        "    int st = syn_sync_status(plan, stream);\n"
+        "    syn_plan_destroy(plan);\n"
+        "    return st;\n"
+        "}\n")
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.join(ROOT, "include"),
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
